@@ -1,0 +1,264 @@
+"""fp64 CPU oracle for the MoE layer forward -- TEST INFRASTRUCTURE ONLY.
+
+Only the test-suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` import this package.  The CUDA library never imports, links or
+calls it, and the two share no code.
+
+The arithmetic lives in ``moe_oracle.c`` (plain C, fp64, per-token loops); this
+module compiles it with gcc (``build()``) and marshals numpy arrays through
+ctypes.  Each wrapper names the C function it calls; the C file cites the
+passage of the source pages each step follows.
+
+Parity status of each function (see tests/test_oracle_pins.py for the pins):
+  route, slot_map, local_mask, permute, expert_mlp, moe_tokens, bf16 rounding:
+  pinned (closed forms, brute force, invariants, independent numpy/torch
+  routines).  No function here is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libmoe_oracle.so")
+
+NONLOCAL_SKIP = 0
+NONLOCAL_MOD = 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile moe_oracle.c into a shared library (gcc, OpenMP, no FP contraction)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
+           "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        i32, i64 = ctypes.c_int32, ctypes.c_int64
+        lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
+        lib.oracle_bf16_to_f64.restype = ctypes.c_double
+        lib.oracle_f64_to_bf16.argtypes = [ctypes.c_double]
+        lib.oracle_f64_to_bf16.restype = ctypes.c_uint16
+        lib.oracle_route.argtypes = [P, P, P, i64, i32, i32, i32, i32, P, P, P]
+        lib.oracle_route.restype = None
+        lib.oracle_slot_map.argtypes = [P, i64, i32, P, P, P]
+        lib.oracle_slot_map.restype = None
+        lib.oracle_local_mask.argtypes = [P, P, i64, i32, i32, i32, P, P, P]
+        lib.oracle_local_mask.restype = None
+        lib.oracle_permute.argtypes = [P, i64, i32, P, P, P, P]
+        lib.oracle_permute.restype = None
+        lib.oracle_expert_mlp.argtypes = [P, P, P, i32, i32, P, P]
+        lib.oracle_expert_mlp.restype = None
+        lib.oracle_moe_tokens.argtypes = [P, i64, i32, P, P, i32, i32, i32, P, P, i32, i32, i32,
+                                          P, P, i32, i32, P, P, i32, P, P, i64, P, P, P, P]
+        lib.oracle_moe_tokens.restype = None
+        lib.oracle_set_threads.argtypes = [i32]
+        lib.oracle_set_threads.restype = None
+        lib.oracle_get_threads.argtypes = []
+        lib.oracle_get_threads.restype = i32
+        _lib = lib
+        return lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _u16(a) -> np.ndarray:
+    """bf16 data as a C-contiguous uint16 numpy array (accepts a torch bf16 tensor)."""
+    if a is None:
+        return None
+    if hasattr(a, "dtype") and str(a.dtype) == "torch.bfloat16":
+        import torch
+        return np.ascontiguousarray(a.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16))
+    a = np.asarray(a)
+    assert a.dtype == np.uint16, a.dtype
+    return np.ascontiguousarray(a)
+
+
+def _np(a, dtype):
+    if a is None:
+        return None
+    if hasattr(a, "detach"):
+        a = a.detach().cpu().numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=dtype))
+
+
+def set_threads(n: int) -> None:
+    _load().oracle_set_threads(int(n))
+
+
+def get_threads() -> int:
+    return int(_load().oracle_get_threads())
+
+
+def bf16_to_f64(b: int) -> float:
+    return float(_load().oracle_bf16_to_f64(int(b)))
+
+
+def f64_to_bf16(v: float) -> int:
+    """Round to nearest bf16, ties to even; returns the bf16 bit pattern."""
+    return int(_load().oracle_f64_to_bf16(float(v)))
+
+
+def route(x, Wg, bias, k: int, renorm: bool):
+    """C oracle_route: returns (ids [T,k] int32, w [T,k] float64, logits [T,E] float64)."""
+    lib = _load()
+    x = _u16(x)
+    Wg = _np(Wg, np.float32)
+    bias = _np(bias, np.float32)
+    T, H = x.shape
+    E = Wg.shape[0]
+    ids = np.empty((T, k), np.int32)
+    w = np.empty((T, k), np.float64)
+    logits = np.empty((T, E), np.float64)
+    lib.oracle_route(_ptr(x), _ptr(Wg), _ptr(bias), T, H, E, k, int(bool(renorm)),
+                     _ptr(ids), _ptr(w), _ptr(logits))
+    return ids, w, logits
+
+
+def slot_map(ids, rep_offset=None, rep_slots=None):
+    """C oracle_slot_map: expert id -> expert slot (identity when rep_offset is None)."""
+    lib = _load()
+    ids = _np(ids, np.int32)
+    T, k = ids.shape
+    ro = _np(rep_offset, np.int32)
+    rs = _np(rep_slots, np.int32)
+    out = np.empty((T, k), np.int32)
+    lib.oracle_slot_map(_ptr(ids), T, k, _ptr(ro), _ptr(rs), _ptr(out))
+    return out
+
+
+def local_mask(slots, w, start: int, count: int, mode: int = NONLOCAL_SKIP):
+    """C oracle_local_mask: returns (slots_out, w_out, mask) with the input's shape."""
+    lib = _load()
+    slots = _np(slots, np.int32)
+    w = _np(w, np.float64)
+    shape = slots.shape
+    P = slots.size
+    so = np.empty(shape, np.int32)
+    wo = np.empty(shape, np.float64)
+    m = np.empty(shape, np.uint8)
+    lib.oracle_local_mask(_ptr(slots), _ptr(w), P, start, count, mode, _ptr(so), _ptr(wo), _ptr(m))
+    return so, wo, m.astype(bool)
+
+
+def permute(slots, S: int):
+    """C oracle_permute: returns (counts [S], offsets [S+1], perm_src [total], pair_row [P])."""
+    lib = _load()
+    slots = _np(slots, np.int32).reshape(-1)
+    P = slots.size
+    counts = np.empty(S, np.int32)
+    offsets = np.empty(S + 1, np.int32)
+    perm_src = np.full(max(P, 1), -1, np.int32)
+    pair_row = np.empty(max(P, 1), np.int32)
+    lib.oracle_permute(_ptr(slots), P, S, _ptr(counts), _ptr(offsets), _ptr(perm_src), _ptr(pair_row))
+    total = int(offsets[S])
+    return counts, offsets, perm_src[:total].copy(), pair_row[:P].copy()
+
+
+def expert_mlp(x_row, W1, W2):
+    """C oracle_expert_mlp: one token through one SwiGLU expert. Returns (y [H] f64, h [I] bf16 bits)."""
+    lib = _load()
+    x_row = _u16(x_row).reshape(-1)
+    W1 = _u16(W1)
+    W2 = _u16(W2)
+    H = x_row.size
+    I = W1.shape[0] // 2
+    assert W1.shape == (2 * I, H) and W2.shape == (H, I)
+    y = np.empty(H, np.float64)
+    h = np.empty(I, np.uint16)
+    lib.oracle_expert_mlp(_ptr(x_row), _ptr(W1), _ptr(W2), H, I, _ptr(y), _ptr(h))
+    return y, h
+
+
+def moe_tokens(x, Wg, bias, k, renorm, W1, W2, tokens=None, rep_offset=None, rep_slots=None,
+               local_start=0, local_count=-1, mode=NONLOCAL_SKIP,
+               W1s=None, W2s=None, shared_gate_w=None):
+    """C oracle_moe_tokens: full layer output (float64) for the listed tokens.
+
+    W1 [S_local, 2I, H], W2 [S_local, H, I] are indexed by local slot.
+    W1s [n_shared, 2*I_sh, H] / W2s [n_shared, H, I_sh] (or None).
+    Returns dict(out [n,H] f64, ids [n,k], w [n,k] f64 (after the mask), slots [n,k]).
+    """
+    lib = _load()
+    x = _u16(x)
+    T, H = x.shape
+    Wg = _np(Wg, np.float32)
+    bias = _np(bias, np.float32)
+    E = Wg.shape[0]
+    W1 = _u16(W1)
+    W2 = _u16(W2)
+    I = W1.shape[1] // 2
+    if tokens is None:
+        tokens = np.arange(T, dtype=np.int64)
+    tokens = _np(tokens, np.int64).reshape(-1)
+    n = tokens.size
+    ro = _np(rep_offset, np.int32)
+    rs = _np(rep_slots, np.int32)
+    n_shared, I_sh = 0, 0
+    if W1s is not None:
+        W1s = _u16(W1s)
+        W2s = _u16(W2s)
+        n_shared = W1s.shape[0]
+        I_sh = W1s.shape[1] // 2
+    gw = _u16(shared_gate_w)
+    out = np.empty((n, H), np.float64)
+    ids = np.empty((n, k), np.int32)
+    w = np.empty((n, k), np.float64)
+    sl = np.empty((n, k), np.int32)
+    lib.oracle_moe_tokens(_ptr(x), T, H, _ptr(Wg), _ptr(bias), E, k, int(bool(renorm)),
+                          _ptr(ro), _ptr(rs), local_start, local_count, mode,
+                          _ptr(W1), _ptr(W2), I, n_shared, _ptr(W1s), _ptr(W2s), I_sh, _ptr(gw),
+                          _ptr(tokens), n, _ptr(out), _ptr(ids), _ptr(w), _ptr(sl))
+    return dict(out=out, ids=ids, w=w, slots=sl)
+
+
+def moe_layer(x, Wg, bias, k, renorm, W1, W2, rep_offset=None, rep_slots=None,
+              local_start=0, local_count=-1, mode=NONLOCAL_SKIP,
+              W1s=None, W2s=None, shared_gate_w=None, S=None):
+    """The whole layer on a batch: routing, slot map, mask, permutation and outputs.
+
+    Composes the C steps in the order the layer runs them; returns a dict with
+    ids, w (router weights), slots/w_masked (after slot map and mask), counts,
+    offsets, perm_src, pair_row and out [T, H] (float64).
+    """
+    ids, w, logits = route(x, Wg, bias, k, renorm)
+    slots = slot_map(ids, rep_offset, rep_slots)
+    if S is None:
+        S = Wg.shape[0] if rep_offset is None else int(np.asarray(rep_offset)[-1])
+    if local_count is not None and local_count >= 0:
+        slots_l, w_l, mask = local_mask(slots, w, local_start, local_count, mode)
+        S_local = local_count
+    else:
+        slots_l, w_l, mask = slots, w, np.ones_like(slots, dtype=bool)
+        S_local = S
+    counts, offsets, perm_src, pair_row = permute(slots_l, S_local)
+    res = moe_tokens(x, Wg, bias, k, renorm, W1, W2, None, rep_offset, rep_slots,
+                     local_start, local_count if local_count is not None else -1, mode,
+                     W1s, W2s, shared_gate_w)
+    return dict(ids=ids, w=w, logits=logits, slots_global=slots, slots=slots_l, w_masked=w_l,
+                mask=mask, counts=counts, offsets=offsets, perm_src=perm_src,
+                pair_row=pair_row.reshape(ids.shape), out=res["out"])

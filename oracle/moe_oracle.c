@@ -1,0 +1,404 @@
+/*
+ * moe_oracle.c -- plain, slow fp64 CPU oracle for the forward pass of one
+ * Mixture-of-Experts (MoE) layer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test-suite, the smoke check and the
+ * CPU-baseline leg of the benchmark load this file (through oracle/__init__.py).
+ * The CUDA library never includes, links or calls it, and it shares no source
+ * with the CUDA library: no headers, helpers, tables or constants.
+ *
+ * What it computes, step by step (each function cites the passage it follows):
+ *   1. router: logits = x . Wg^T (+ optional per-expert logit bias), a softmax
+ *      over all experts, top-k by logit with ties to the lower expert id, and
+ *      optional renormalisation of the k probabilities;
+ *   2. expert -> expert-slot map (identity, or a replica table);
+ *   3. optional expert-parallel local-range mask and remap;
+ *   4. per-slot counts, exclusive-scan offsets, and the stable permutation of
+ *      (token, k) pairs grouped by slot;
+ *   5. per selected expert a gated MLP (SwiGLU) with the intermediate rounded
+ *      to bf16, and one routing-weighted sum over the k experts per token, plus
+ *      optional shared experts (optionally scaled by a sigmoid gate).
+ *
+ * Arithmetic: every input is bf16 or fp32; products of a bf16 with a bf16 or
+ * fp32 value are exact in fp64, sums run in fp64 in ascending index order, and
+ * exp() is the C library's double-precision exp.  The one deliberate rounding
+ * is the SwiGLU intermediate h, rounded to bf16 (round to nearest, ties to
+ * even) as the GPU path also does.  Build with -ffp-contract=off so x86 and Arm
+ * hosts give bit-identical results.
+ *
+ * Parity pins: tests/test_oracle_pins.py checks every function here against
+ * closed forms, brute force, invariants and independent library routines.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_NONLOCAL_SKIP 0
+#define ORACLE_NONLOCAL_MOD 1
+
+/* ------------------------------------------------------------------------- */
+/* bf16 <-> double                                                            */
+/* ------------------------------------------------------------------------- */
+
+/* A bf16 value is the upper 16 bits of an IEEE binary32 value. */
+double oracle_bf16_to_f64(uint16_t b)
+{
+    uint32_t u = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Round a double to the nearest bf16 value, ties to even (8 significant bits,
+ * binary32 exponent range, gradual underflow with spacing 2^-133, overflow to
+ * infinity).  Done on the value itself: scale by a power of two so the last
+ * kept bit has weight 1, round to an integer with nearbyint() under the
+ * default round-to-nearest-even mode, scale back. */
+uint16_t oracle_f64_to_bf16(double v)
+{
+    if (isnan(v)) return (uint16_t)0x7FC0u;
+    uint16_t sign = signbit(v) ? (uint16_t)0x8000u : (uint16_t)0;
+    double a = fabs(v);
+    if (a == 0.0) return sign;
+    if (isinf(a)) return (uint16_t)(sign | 0x7F80u);
+    int e;
+    (void)frexp(a, &e);            /* a = m * 2^e with m in [0.5, 1) */
+    int lsb = (e - 1) - 7;         /* weight of the 8th significant bit */
+    if (lsb < -133) lsb = -133;    /* bf16 subnormal spacing */
+    double q = ldexp(a, -lsb);     /* exact */
+    double r = nearbyint(q);       /* ties to even */
+    double res = ldexp(r, lsb);    /* exact */
+    const double bf16_max = 3.3895313892515355e38; /* (2 - 2^-7) * 2^127 */
+    if (res > bf16_max) return (uint16_t)(sign | 0x7F80u);
+    float f = (float)res; /* exact: res has <= 8 significant bits in range */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(sign | (uint16_t)((u >> 16) & 0x7FFFu));
+}
+
+/* ------------------------------------------------------------------------- */
+/* 1. Router                                                                  */
+/* ------------------------------------------------------------------------- */
+
+/* Router for tokens t in [0, T): gate logits, softmax over all E experts, top-k
+ * by logit (ties to the lower expert id), optional renormalisation.
+ *
+ * Follows the vLLM EP FusedMoE patch (ep_fused_moe_patch.py), module docstring
+ * "EP expert dispatch": top-k routing produces global expert ids, identical on
+ * every rank; and its patched FusedMoE __init__ (renormalize=True default,
+ * routing over the global expert count).  Softmax over all experts comes
+ * first, then top-k ("softmax-then-top-k with renorm").  Selection is on the
+ * logits: softmax is strictly increasing in the logit, so the order is the
+ * same, and ties between distinct logits cannot be created by rounding of
+ * probabilities.
+ *
+ *   x       [T, H] bf16 bits      Wg [E, H] fp32      bias [E] fp32 or NULL
+ *   ids     [T, k] int32 out      (descending logit, ties to lower id)
+ *   w       [T, k] double out     (p_e, or p_e / sum of the k selected p)
+ *   logits  [T, E] double out, or NULL
+ */
+void oracle_route(const uint16_t *x, const float *Wg, const float *bias,
+                  int64_t T, int H, int E, int k, int renorm,
+                  int32_t *ids, double *w, double *logits)
+{
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t t = 0; t < T; ++t) {
+        double *l = (double *)malloc(sizeof(double) * (size_t)E);
+        char *taken = (char *)calloc((size_t)E, 1);
+        const uint16_t *xt = x + (size_t)t * (size_t)H;
+        for (int e = 0; e < E; ++e) {
+            const float *we = Wg + (size_t)e * (size_t)H;
+            double s = 0.0;
+            for (int h = 0; h < H; ++h) s += oracle_bf16_to_f64(xt[h]) * (double)we[h];
+            if (bias) s += (double)bias[e];
+            l[e] = s;
+            if (logits) logits[(size_t)t * (size_t)E + (size_t)e] = s;
+        }
+        /* softmax over all experts */
+        double m = l[0];
+        for (int e = 1; e < E; ++e) if (l[e] > m) m = l[e];
+        double z = 0.0;
+        for (int e = 0; e < E; ++e) z += exp(l[e] - m);
+        /* top-k: k passes of "largest remaining logit, lowest id on ties" */
+        double psum = 0.0;
+        for (int j = 0; j < k; ++j) {
+            int best = -1;
+            for (int e = 0; e < E; ++e) {
+                if (taken[e]) continue;
+                if (best < 0 || l[e] > l[best]) best = e;
+            }
+            taken[best] = 1;
+            ids[(size_t)t * (size_t)k + (size_t)j] = best;
+            double p = exp(l[best] - m) / z;
+            w[(size_t)t * (size_t)k + (size_t)j] = p;
+            psum += p;
+        }
+        if (renorm)
+            for (int j = 0; j < k; ++j) w[(size_t)t * (size_t)k + (size_t)j] /= psum;
+        free(l);
+        free(taken);
+    }
+}
+
+/* ------------------------------------------------------------------------- */
+/* 2. Expert -> expert slot                                                   */
+/* ------------------------------------------------------------------------- */
+
+/* Map each (token, k) pair's expert id to an expert slot.
+ *
+ * TensorRT-LLM PR #4495 ("large-scale EP (part 3): refactor FusedMoe for
+ * redundant expert"), Description: the router computes expert ids (model side),
+ * while the fused MoE op computes on expert slots (engine side), into which the
+ * module loads the weights; with no mapping an expert's slot id is its id.
+ * With redundant experts an expert owns rep_count[e] = rep_offset[e+1] -
+ * rep_offset[e] slots, listed at rep_slots[rep_offset[e] ...], and token t uses
+ * replica (t mod rep_count[e]).
+ *
+ *   ids [T, k]; rep_offset [E+1] or NULL (identity); rep_slots [S]
+ *   slots [T, k] out
+ */
+void oracle_slot_map(const int32_t *ids, int64_t T, int k,
+                     const int32_t *rep_offset, const int32_t *rep_slots,
+                     int32_t *slots)
+{
+    for (int64_t t = 0; t < T; ++t) {
+        for (int j = 0; j < k; ++j) {
+            size_t p = (size_t)t * (size_t)k + (size_t)j;
+            int32_t e = ids[p];
+            if (!rep_offset) {
+                slots[p] = e;
+            } else {
+                int64_t c = (int64_t)rep_offset[e + 1] - (int64_t)rep_offset[e];
+                slots[p] = rep_slots[rep_offset[e] + (int32_t)(t % c)];
+            }
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------- */
+/* 3. Expert-parallel local-range mask and remap                              */
+/* ------------------------------------------------------------------------- */
+
+/* vLLM EP FusedMoE patch, function ep_mask_and_remap: a pair is local when its
+ * id lies in [start, start + count); every routing weight is multiplied by the
+ * local mask (non-local pairs contribute nothing); local ids become id - start;
+ * non-local ids become id mod count (MOD mode, the function as printed: the
+ * pair is still computed, with weight 0) or -1 (SKIP mode: the pair is dropped,
+ * the token-level skip that the function's comments attribute to the upstream
+ * ragged gather).  Here the ids are expert-slot ids.
+ *
+ *   slots [P] in; w_in [P] in; slots_out [P] out; w_out [P] out; mask [P] out
+ */
+void oracle_local_mask(const int32_t *slots, const double *w_in, int64_t P,
+                       int start, int count, int mode,
+                       int32_t *slots_out, double *w_out, uint8_t *mask)
+{
+    for (int64_t p = 0; p < P; ++p) {
+        int32_t s = slots[p];
+        int m = (s >= start) && (s < start + count);
+        w_out[p] = w_in[p] * (double)m;
+        if (mask) mask[p] = (uint8_t)m;
+        if (m)
+            slots_out[p] = s - start;
+        else
+            slots_out[p] = (mode == ORACLE_NONLOCAL_MOD) ? (s % count) : -1;
+    }
+}
+
+/* ------------------------------------------------------------------------- */
+/* 4. Counts, offsets, permutation                                            */
+/* ------------------------------------------------------------------------- */
+
+/* Group the kept pairs by slot: counts[s] = number of pairs with slot s,
+ * offsets = exclusive scan of counts (offsets[S] = total), and within a slot
+ * the pairs keep ascending pair index p = t*k + j (a stable sort by slot).
+ * perm_src[r] = pair placed in row r (r < offsets[S]); pair_row[p] = its row,
+ * or -1 for a dropped pair (slot -1).
+ *
+ * The per-expert loop of the vLLM EP FusedMoE patch (module docstring: the
+ * per-expert loop skips experts whose count is 0) visits exactly these groups.
+ */
+void oracle_permute(const int32_t *slots, int64_t P, int S,
+                    int32_t *counts, int32_t *offsets,
+                    int32_t *perm_src, int32_t *pair_row)
+{
+    for (int s = 0; s < S; ++s) counts[s] = 0;
+    for (int64_t p = 0; p < P; ++p)
+        if (slots[p] >= 0) counts[slots[p]] += 1;
+    offsets[0] = 0;
+    for (int s = 0; s < S; ++s) offsets[s + 1] = offsets[s] + counts[s];
+    int32_t *next = (int32_t *)malloc(sizeof(int32_t) * (size_t)(S > 0 ? S : 1));
+    for (int s = 0; s < S; ++s) next[s] = offsets[s];
+    for (int64_t p = 0; p < P; ++p) {
+        int32_t s = slots[p];
+        if (s < 0) {
+            pair_row[p] = -1;
+        } else {
+            int32_t r = next[s]++;
+            perm_src[r] = (int32_t)p;
+            pair_row[p] = r;
+        }
+    }
+    free(next);
+}
+
+/* ------------------------------------------------------------------------- */
+/* 5. Gated MLP (SwiGLU) of one expert on one token                          */
+/* ------------------------------------------------------------------------- */
+
+/* y = W2 . bf16( silu(W1_gate . x) * (W1_up . x) ),  silu(z) = z / (1 + e^-z).
+ *
+ * Per-expert gated MLP as in the TensorRT-LLM AutoDeploy MoE ops (PR #10985,
+ * "MoE all-to-all paradigm": is_gated_mlp / act_fn per expert) and the
+ * per-expert compute of the vLLM EP FusedMoE patch.  W1 packs the gate rows
+ * first and the up rows second.
+ *
+ *   x [H] bf16;  W1 [2I, H] bf16 (rows 0..I-1 gate, I..2I-1 up);  W2 [H, I] bf16
+ *   y [H] double out;  h [I] bf16 bits out (or NULL)
+ */
+void oracle_expert_mlp(const uint16_t *x, const uint16_t *W1, const uint16_t *W2,
+                       int H, int I, double *y, uint16_t *h_out)
+{
+    double *h = (double *)malloc(sizeof(double) * (size_t)I);
+    for (int i = 0; i < I; ++i) {
+        const uint16_t *wg = W1 + (size_t)i * (size_t)H;
+        const uint16_t *wu = W1 + ((size_t)I + (size_t)i) * (size_t)H;
+        double g = 0.0, u = 0.0;
+        for (int hh = 0; hh < H; ++hh) g += oracle_bf16_to_f64(wg[hh]) * oracle_bf16_to_f64(x[hh]);
+        for (int hh = 0; hh < H; ++hh) u += oracle_bf16_to_f64(wu[hh]) * oracle_bf16_to_f64(x[hh]);
+        double a = g / (1.0 + exp(-g)) * u;
+        uint16_t b = oracle_f64_to_bf16(a);
+        if (h_out) h_out[i] = b;
+        h[i] = oracle_bf16_to_f64(b);
+    }
+    for (int o = 0; o < H; ++o) {
+        const uint16_t *w2 = W2 + (size_t)o * (size_t)I;
+        double s = 0.0;
+        for (int i = 0; i < I; ++i) s += oracle_bf16_to_f64(w2[i]) * h[i];
+        y[o] = s;
+    }
+    free(h);
+}
+
+/* ------------------------------------------------------------------------- */
+/* The layer, for a list of tokens                                            */
+/* ------------------------------------------------------------------------- */
+
+/* Output rows of the MoE layer for the tokens listed in tok[0..n) (indices
+ * into x; a token's result does not depend on the other tokens).
+ *
+ * out[t] = sum over j in 0..k-1, in order, of w_j * y_j    (kept pairs only)
+ *        + g_t * sum over shared experts of y_shared
+ * where w_j is the routing weight after the local mask, y_j the gated MLP of
+ * the pair's slot (W1/W2 are indexed by local slot), and g_t = sigmoid(x_t .
+ * w_s) when shared_gate_w is given, else 1.
+ *
+ * The weighted sum of the selected experts' outputs per token is the one the
+ * DeepSpeed AutoTP MoE PR (#6964) reduces once per layer; the shared expert is
+ * added to the routed output as in ep_reduce_output of the vLLM EP FusedMoE
+ * patch (out = routed_out + shared_out).
+ *
+ * Shared experts: n_shared experts of intermediate size I_sh each; W1s holds
+ * them one after another, each [2*I_sh, H] (gate rows, then up rows); W2s holds
+ * them one after another, each [H, I_sh].
+ *
+ * Also writes per listed token its ids / weights / slots (arrays [n, k]).
+ */
+void oracle_moe_tokens(const uint16_t *x, int64_t T, int H,
+                       const float *Wg, const float *bias, int E, int k, int renorm,
+                       const int32_t *rep_offset, const int32_t *rep_slots,
+                       int local_start, int local_count, int mode,
+                       const uint16_t *W1, const uint16_t *W2, int I,
+                       int n_shared, const uint16_t *W1s, const uint16_t *W2s, int I_sh,
+                       const uint16_t *shared_gate_w,
+                       const int64_t *tok, int64_t n,
+                       double *out, int32_t *ids_out, double *w_out, int32_t *slot_out)
+{
+    (void)T;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t q = 0; q < n; ++q) {
+        int64_t t = tok[q];
+        const uint16_t *xt = x + (size_t)t * (size_t)H;
+        int32_t *ids = (int32_t *)malloc(sizeof(int32_t) * (size_t)k);
+        double *w = (double *)malloc(sizeof(double) * (size_t)k);
+        int32_t *sl = (int32_t *)malloc(sizeof(int32_t) * (size_t)k);
+        int32_t *sl2 = (int32_t *)malloc(sizeof(int32_t) * (size_t)k);
+        double *w2 = (double *)malloc(sizeof(double) * (size_t)k);
+        double *y = (double *)malloc(sizeof(double) * (size_t)H);
+        double *o = out + (size_t)q * (size_t)H;
+
+        /* steps 1-3 for this one token (the slot map needs its index t) */
+        oracle_route(xt, Wg, bias, 1, H, E, k, renorm, ids, w, NULL);
+        for (int j = 0; j < k; ++j) {
+            int32_t e = ids[j];
+            if (!rep_offset) {
+                sl[j] = e;
+            } else {
+                int64_t c = (int64_t)rep_offset[e + 1] - (int64_t)rep_offset[e];
+                sl[j] = rep_slots[rep_offset[e] + (int32_t)(t % c)];
+            }
+        }
+        if (local_count >= 0) {
+            oracle_local_mask(sl, w, k, local_start, local_count, mode, sl2, w2, NULL);
+        } else {
+            for (int j = 0; j < k; ++j) { sl2[j] = sl[j]; w2[j] = w[j]; }
+        }
+        for (int j = 0; j < k; ++j) {
+            ids_out[(size_t)q * (size_t)k + (size_t)j] = ids[j];
+            w_out[(size_t)q * (size_t)k + (size_t)j] = w2[j];
+            slot_out[(size_t)q * (size_t)k + (size_t)j] = sl2[j];
+        }
+
+        /* step 5: weighted sum over the k experts, in order */
+        for (int hh = 0; hh < H; ++hh) o[hh] = 0.0;
+        for (int j = 0; j < k; ++j) {
+            int32_t s = sl2[j];
+            if (s < 0) continue;
+            oracle_expert_mlp(xt, W1 + (size_t)s * 2u * (size_t)I * (size_t)H,
+                              W2 + (size_t)s * (size_t)H * (size_t)I, H, I, y, NULL);
+            for (int hh = 0; hh < H; ++hh) o[hh] += w2[j] * y[hh];
+        }
+        if (n_shared > 0) {
+            double g = 1.0;
+            if (shared_gate_w) {
+                double z = 0.0;
+                for (int hh = 0; hh < H; ++hh)
+                    z += oracle_bf16_to_f64(xt[hh]) * oracle_bf16_to_f64(shared_gate_w[hh]);
+                g = 1.0 / (1.0 + exp(-z));
+            }
+            double *ysum = (double *)calloc((size_t)H, sizeof(double));
+            for (int sidx = 0; sidx < n_shared; ++sidx) {
+                oracle_expert_mlp(xt, W1s + (size_t)sidx * 2u * (size_t)I_sh * (size_t)H,
+                                  W2s + (size_t)sidx * (size_t)H * (size_t)I_sh, H, I_sh, y, NULL);
+                for (int hh = 0; hh < H; ++hh) ysum[hh] += y[hh];
+            }
+            for (int hh = 0; hh < H; ++hh) o[hh] += g * ysum[hh];
+            free(ysum);
+        }
+        free(ids); free(w); free(sl); free(sl2); free(w2); free(y);
+    }
+}
+
+/* Thread count used by the OpenMP loops above (token-parallel only; the
+ * arithmetic of each token is sequential, so results do not depend on it). */
+void oracle_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+int oracle_get_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

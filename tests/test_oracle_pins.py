@@ -1,0 +1,340 @@
+"""Pins of the fp64 CPU oracle against what the method and mathematics fix.
+
+Every check here is independent of the oracle's own code path: brute force over
+subsets, numpy matrix products, torch casts, hand-worked examples in
+tests/golden/, closed forms (top_k = 1, top_k = E, shared expert alone) and
+invariants (counts, bijections, token permutation, disjoint local ranges, slot
+maps).  A dropped term, a wrong sign or index, or a transposed operand in the
+oracle fails at least one of them.
+"""
+import itertools
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as mi
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _bf16_np(t: torch.Tensor) -> np.ndarray:
+    return t.to(torch.float64).numpy()
+
+
+def _small_cfg(**kw):
+    base = dict(name="pin", T=24, H=64, I=64, E=6, k=2, renorm=True)
+    base.update(kw)
+    return mi.MoEConfig(**base)
+
+
+def _numpy_mlp(x64, W1, W2):
+    """Dense SwiGLU MLP with numpy products; h rounded through torch's bf16 cast."""
+    I = W1.shape[0] // 2
+    W1n, W2n = _bf16_np(W1), _bf16_np(W2)
+    g = x64 @ W1n[:I].T
+    u = x64 @ W1n[I:].T
+    a = g / (1.0 + np.exp(-g)) * u
+    h = torch.from_numpy(a).to(torch.bfloat16).to(torch.float64).numpy()
+    return h @ W2n.T
+
+
+# --------------------------------------------------------------------------- bf16
+
+def test_bf16_round_matches_torch_on_fp32_values():
+    g = torch.Generator().manual_seed(1)
+    vals = torch.cat([
+        torch.randn(20000, generator=g) * 10.0 ** torch.randint(-40, 38, (20000,), generator=g).float(),
+        torch.tensor([0.0, -0.0, 1.0, -1.0, 3.0e38, -3.0e38, 1e-40, -1e-40, 2.0 ** -133, 2.0 ** -134,
+                      1.00390625, 1.01171875, 65504.0]),
+    ]).float()
+    want = vals.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = np.array([oracle.f64_to_bf16(float(v)) for v in vals.tolist()], dtype=np.uint16)
+    assert np.array_equal(got, want)
+
+
+def test_bf16_round_ties_to_even_and_overflow():
+    # 1 + 2^-8 lies halfway between 1 and 1 + 2^-7: ties to the even significand (1.0)
+    assert oracle.f64_to_bf16(1.0 + 2.0 ** -8) == 0x3F80
+    # 1 + 3*2^-8 lies halfway between 1+2^-7 and 1+2^-6: even is 1+2^-6
+    assert oracle.f64_to_bf16(1.0 + 3 * 2.0 ** -8) == 0x3F82
+    # just above the halfway point rounds up (a value no fp32 can hold exactly)
+    assert oracle.f64_to_bf16(1.0 + 2.0 ** -8 + 2.0 ** -40) == 0x3F81
+    assert oracle.f64_to_bf16(1e39) == 0x7F80
+    assert oracle.f64_to_bf16(-1e39) == 0xFF80
+    for b in (0x0001, 0x3F80, 0x4049, 0xC2F7, 0x7F7F):
+        assert oracle.f64_to_bf16(oracle.bf16_to_f64(b)) == b
+
+
+# --------------------------------------------------------------------------- router
+
+def test_gate_logits_match_numpy_product():
+    cfg = _small_cfg(T=40, H=96, E=7, zipf_s=1.1)
+    inp = mi.make_inputs(cfg)
+    ids, w, logits = oracle.route(inp["x"], inp["Wg"], inp["bias"], cfg.k, cfg.renorm)
+    ref = _bf16_np(inp["x"]) @ inp["Wg"].double().numpy().T + inp["bias"].double().numpy()
+    np.testing.assert_allclose(logits, ref, rtol=0, atol=1e-12)
+
+
+def test_topk_matches_brute_force_over_subsets():
+    for E, k in ((8, 2), (7, 3), (6, 6), (5, 1)):
+        cfg = _small_cfg(T=30, H=48, E=E, k=k)
+        inp = mi.make_inputs(cfg)
+        ids, w, logits = oracle.route(inp["x"], inp["Wg"], None, k, False)
+        for t in range(cfg.T):
+            l = logits[t]
+            best = max(itertools.combinations(range(E), k), key=lambda s: (sum(l[list(s)]),
+                                                                              [-i for i in s]))
+            assert sorted(ids[t].tolist()) == sorted(best)
+            # descending logit within the selection
+            assert all(l[ids[t][j]] >= l[ids[t][j + 1]] for j in range(k - 1))
+
+
+def test_topk_exact_ties_go_to_lower_index():
+    H, E, k = 32, 8, 3
+    g = torch.Generator().manual_seed(5)
+    Wg = torch.randn(E, H, generator=g) * 0.02
+    Wg[6] = Wg[2]          # experts 2 and 6 always tie
+    Wg[5] = Wg[1]          # experts 1 and 5 always tie
+    x = torch.randn(16, H, generator=g).to(torch.bfloat16)
+    x[3] = 0               # an all-zero token: every logit is exactly 0
+    ids, w, logits = oracle.route(x, Wg, None, k, False)
+    assert ids[3].tolist() == [0, 1, 2]
+    for t in range(16):
+        sel = ids[t].tolist()
+        for lo, hi in ((2, 6), (1, 5)):
+            if hi in sel:
+                assert lo in sel and sel.index(lo) < sel.index(hi)
+
+
+def test_softmax_and_renorm_weights():
+    cfg = _small_cfg(T=20, H=64, E=6, k=6)
+    inp = mi.make_inputs(cfg)
+    _, w_all, logits = oracle.route(inp["x"], inp["Wg"], None, 6, False)
+    np.testing.assert_allclose(w_all.sum(1), 1.0, atol=1e-14)
+    # k < E, renorm off: the weights are the softmax probabilities of the selected experts
+    ids, w, logits = oracle.route(inp["x"], inp["Wg"], None, 2, False)
+    p = np.exp(logits - logits.max(1, keepdims=True))
+    p /= p.sum(1, keepdims=True)
+    np.testing.assert_allclose(w, np.take_along_axis(p, ids, 1), rtol=1e-13)
+    # renorm on: the selected probabilities divided by their sum
+    ids_r, w_r, _ = oracle.route(inp["x"], inp["Wg"], None, 2, True)
+    assert np.array_equal(ids, ids_r)
+    sel = np.take_along_axis(p, ids, 1)
+    np.testing.assert_allclose(w_r, sel / sel.sum(1, keepdims=True), rtol=1e-13)
+    # k = 1 with renorm: weight exactly 1
+    _, w1, _ = oracle.route(inp["x"], inp["Wg"], None, 1, True)
+    assert np.all(w1 == 1.0)
+
+
+# --------------------------------------------------------------------------- slots, mask, permute
+
+def _read_golden(name):
+    lines = [ln.split("#")[0].strip() for ln in open(os.path.join(GOLDEN, name))]
+    return [ln for ln in lines if ln]
+
+
+def test_slot_map_golden_example():
+    lines = _read_golden("slot_map_example.txt")
+    ro = np.array(lines[0].split()[1:], np.int32)
+    rs = np.array(lines[1].split()[1:], np.int32)
+    ids, want = [], []
+    for ln in lines[2:]:
+        lhs, rhs = ln.split("->")
+        ids.append([int(v) for v in lhs.split()[1:]])
+        want.append([int(v) for v in rhs.split()])
+    got = oracle.slot_map(np.array(ids, np.int32), ro, rs)
+    assert got.tolist() == want
+
+
+def test_identity_slot_table_equals_no_map():
+    g = torch.Generator().manual_seed(2)
+    ids = torch.randint(0, 9, (50, 3), generator=g).numpy().astype(np.int32)
+    ro = np.arange(10, dtype=np.int32)
+    rs = np.arange(9, dtype=np.int32)
+    assert np.array_equal(oracle.slot_map(ids, ro, rs), oracle.slot_map(ids))
+    assert np.array_equal(oracle.slot_map(ids), ids)
+
+
+def test_ep_mask_and_remap_golden_example():
+    lines = _read_golden("ep_mask_and_remap_example.txt")
+    start = int(lines[0].split()[1])
+    count = int(lines[1].split()[1])
+    ids, w, want = [], [], []
+    for ln in lines[2:]:
+        lhs, rhs = ln.split("->")
+        a = lhs.split()
+        ids.append(int(a[0]))
+        w.append(float(a[1]))
+        want.append(rhs.split())
+    ids = np.array(ids, np.int32)
+    w = np.array(w)
+    s_mod, w_mod, m = oracle.local_mask(ids, w, start, count, oracle.NONLOCAL_MOD)
+    s_skip, w_skip, m2 = oracle.local_mask(ids, w, start, count, oracle.NONLOCAL_SKIP)
+    for i, r in enumerate(want):
+        assert int(m[i]) == int(r[0]) and int(m2[i]) == int(r[0])
+        assert w_mod[i] == float(r[1]) and w_skip[i] == float(r[1])
+        assert s_mod[i] == int(r[2])
+        assert s_skip[i] == int(r[3])
+
+
+def test_permutation_invariants():
+    g = torch.Generator().manual_seed(3)
+    for S, P in ((1, 1), (5, 0), (7, 300), (40, 1000)):
+        slots = torch.randint(-1, S, (P,), generator=g).numpy().astype(np.int32)
+        counts, offsets, perm_src, pair_row = oracle.permute(slots, S)
+        kept = int((slots >= 0).sum())
+        assert counts.sum() == kept and offsets[0] == 0 and offsets[S] == kept
+        assert np.array_equal(np.diff(offsets), counts)
+        assert np.array_equal(np.bincount(slots[slots >= 0], minlength=S), counts)
+        # pair_row and perm_src are mutually inverse on the kept pairs
+        assert sorted(perm_src.tolist()) == sorted(np.nonzero(slots >= 0)[0].tolist())
+        for r, p in enumerate(perm_src):
+            assert pair_row[p] == r
+        assert np.all(pair_row[slots < 0] == -1)
+        # each slot's rows hold its pairs in ascending pair index
+        for s in range(S):
+            rows = perm_src[offsets[s]:offsets[s + 1]]
+            assert np.all(slots[rows] == s) and np.all(np.diff(rows) > 0)
+
+
+# --------------------------------------------------------------------------- expert MLP and the layer
+
+def test_expert_mlp_matches_numpy_dense_mlp():
+    cfg = _small_cfg(H=96, I=80, E=1)
+    inp = mi.make_inputs(cfg)
+    x = inp["x"][:5]
+    W1, W2 = inp["W1"][0], inp["W2"][0]
+    ref = _numpy_mlp(_bf16_np(x), W1, W2)
+    for t in range(5):
+        y, h = oracle.expert_mlp(x[t], W1, W2)
+        np.testing.assert_allclose(y, ref[t], rtol=0, atol=1e-3 * np.abs(ref[t]).max())
+
+
+def test_top1_with_renorm_equals_single_dense_expert():
+    cfg = _small_cfg(T=16, H=64, I=64, E=5, k=1, renorm=True)
+    inp = mi.make_inputs(cfg)
+    res = oracle.moe_layer(inp["x"], inp["Wg"], None, 1, True, inp["W1"], inp["W2"])
+    x64 = _bf16_np(inp["x"])
+    for t in range(cfg.T):
+        e = int(res["ids"][t, 0])
+        ref = _numpy_mlp(x64[t:t + 1], inp["W1"][e], inp["W2"][e])[0]
+        np.testing.assert_allclose(res["out"][t], ref, rtol=0, atol=1e-3 * np.abs(ref).max())
+
+
+def test_topk_all_experts_equals_dense_softmax_mixture():
+    cfg = _small_cfg(T=12, H=64, I=64, E=4, k=4, renorm=True)
+    inp = mi.make_inputs(cfg)
+    res = oracle.moe_layer(inp["x"], inp["Wg"], None, 4, True, inp["W1"], inp["W2"])
+    x64 = _bf16_np(inp["x"])
+    l = x64 @ inp["Wg"].double().numpy().T
+    p = np.exp(l - l.max(1, keepdims=True))
+    p /= p.sum(1, keepdims=True)
+    ref = sum(p[:, e:e + 1] * _numpy_mlp(x64, inp["W1"][e], inp["W2"][e]) for e in range(4))
+    np.testing.assert_allclose(res["out"], ref, rtol=0, atol=1e-3 * np.abs(ref).max())
+
+
+def test_shared_expert_alone_and_sigmoid_gate():
+    cfg = _small_cfg(T=10, H=64, I=64, E=4, k=2, n_shared=2, I_shared=48, shared_gate=True)
+    inp = mi.make_inputs(cfg)
+    W2zero = torch.zeros_like(inp["W2"])
+    res = oracle.moe_layer(inp["x"], inp["Wg"], None, 2, True, inp["W1"], W2zero,
+                           W1s=inp["W1s"], W2s=inp["W2s"], shared_gate_w=inp["w_s"])
+    x64 = _bf16_np(inp["x"])
+    gate = 1.0 / (1.0 + np.exp(-(x64 @ _bf16_np(inp["w_s"]))))
+    ref = sum(_numpy_mlp(x64, inp["W1s"][i], inp["W2s"][i]) for i in range(2)) * gate[:, None]
+    np.testing.assert_allclose(res["out"], ref, rtol=0, atol=1e-3 * np.abs(ref).max())
+    # without the gate vector the shared experts are added unscaled
+    res2 = oracle.moe_layer(inp["x"], inp["Wg"], None, 2, True, inp["W1"], W2zero,
+                            W1s=inp["W1s"], W2s=inp["W2s"])
+    ref2 = sum(_numpy_mlp(x64, inp["W1s"][i], inp["W2s"][i]) for i in range(2))
+    np.testing.assert_allclose(res2["out"], ref2, rtol=0, atol=1e-3 * np.abs(ref2).max())
+
+
+def test_token_permutation_invariance_bitwise():
+    cfg = _small_cfg(T=20, H=64, I=64, E=6, k=3, n_shared=1, I_shared=64, shared_gate=True)
+    inp = mi.make_inputs(cfg)
+    perm = torch.randperm(cfg.T, generator=torch.Generator().manual_seed(9))
+    args = dict(W1s=inp["W1s"], W2s=inp["W2s"], shared_gate_w=inp["w_s"])
+    a = oracle.moe_layer(inp["x"], inp["Wg"], None, 3, True, inp["W1"], inp["W2"], **args)
+    b = oracle.moe_layer(inp["x"][perm], inp["Wg"], None, 3, True, inp["W1"], inp["W2"], **args)
+    assert np.array_equal(a["out"][perm.numpy()], b["out"])
+    assert np.array_equal(a["ids"][perm.numpy()], b["ids"])
+    assert np.array_equal(a["counts"], b["counts"])
+
+
+def test_disjoint_local_ranges_sum_to_full_layer():
+    cfg = _small_cfg(T=30, H=64, I=64, E=8, k=3)
+    inp = mi.make_inputs(cfg)
+    full = oracle.moe_layer(inp["x"], inp["Wg"], None, 3, True, inp["W1"], inp["W2"])
+    acc = np.zeros_like(full["out"])
+    for start in (0, 2, 4, 6):
+        part = oracle.moe_layer(inp["x"], inp["Wg"], None, 3, True, inp["W1"][start:start + 2],
+                                inp["W2"][start:start + 2], local_start=start, local_count=2)
+        mod = oracle.moe_layer(inp["x"], inp["Wg"], None, 3, True, inp["W1"][start:start + 2],
+                               inp["W2"][start:start + 2], local_start=start, local_count=2,
+                               mode=oracle.NONLOCAL_MOD)
+        # MOD computes the non-local pairs with weight 0: they contribute exactly nothing
+        assert np.array_equal(part["out"], mod["out"])
+        assert mod["counts"].sum() == cfg.T * 3
+        assert part["counts"].sum() == int(((full["ids"] >= start) & (full["ids"] < start + 2)).sum())
+        acc += part["out"]
+    np.testing.assert_allclose(acc, full["out"], rtol=0, atol=1e-12 * np.abs(full["out"]).max())
+    # a range that owns no pair contributes exactly zero
+    ids = full["ids"]
+    unused = [e for e in range(8) if not (ids == e).any()]
+    if unused:
+        e = unused[0]
+        z = oracle.moe_layer(inp["x"], inp["Wg"], None, 3, True, inp["W1"][e:e + 1],
+                             inp["W2"][e:e + 1], local_start=e, local_count=1)
+        assert np.all(z["out"] == 0.0)
+
+
+def test_replica_slots_equal_identity_map():
+    cfg = _small_cfg(T=40, H=64, I=64, E=8, k=3, S=11, n_hot=3, zipf_s=1.1)
+    inp = mi.make_inputs(cfg)
+    tab = mi.slot_table(cfg)
+    W1e = inp["W1"].new_empty((8,) + tuple(inp["W1"].shape[1:]))
+    W2e = inp["W2"].new_empty((8,) + tuple(inp["W2"].shape[1:]))
+    for s, e in enumerate(tab["expert_of_slot"].tolist()):
+        W1e[e] = inp["W1"][s]
+        W2e[e] = inp["W2"][s]
+    rep = oracle.moe_layer(inp["x"], inp["Wg"], inp["bias"], 3, True, inp["W1"], inp["W2"],
+                           rep_offset=inp["rep_offset"], rep_slots=inp["rep_slots"])
+    ident = oracle.moe_layer(inp["x"], inp["Wg"], inp["bias"], 3, True, W1e, W2e)
+    assert np.array_equal(rep["out"], ident["out"])
+    assert rep["counts"].sum() == cfg.T * 3
+    # replica choice follows the token index
+    ro, rs = tab["rep_offset"].numpy(), tab["rep_slots"].numpy()
+    for t in range(cfg.T):
+        for j in range(3):
+            e = rep["ids"][t, j]
+            c = ro[e + 1] - ro[e]
+            assert rep["slots_global"][t, j] == rs[ro[e] + t % c]
+
+
+def test_moe_tokens_matches_batch_layer_on_a_sample():
+    cfg = _small_cfg(T=25, H=64, I=64, E=6, k=2, n_shared=1, I_shared=32, shared_gate=True)
+    inp = mi.make_inputs(cfg)
+    args = dict(W1s=inp["W1s"], W2s=inp["W2s"], shared_gate_w=inp["w_s"])
+    full = oracle.moe_layer(inp["x"], inp["Wg"], None, 2, True, inp["W1"], inp["W2"], **args)
+    tok = np.array([24, 0, 7, 7, 13])
+    part = oracle.moe_tokens(inp["x"], inp["Wg"], None, 2, True, inp["W1"], inp["W2"], tokens=tok, **args)
+    assert np.array_equal(part["out"], full["out"][tok])
+    assert np.array_equal(part["ids"], full["ids"][tok])
+
+
+@pytest.mark.parametrize("threads", [1, 3])
+def test_results_do_not_depend_on_thread_count(threads):
+    cfg = _small_cfg(T=33, H=64, I=64, E=6, k=2)
+    inp = mi.make_inputs(cfg)
+    old = oracle.get_threads()
+    try:
+        oracle.set_threads(threads)
+        a = oracle.moe_layer(inp["x"], inp["Wg"], None, 2, True, inp["W1"], inp["W2"])
+    finally:
+        oracle.set_threads(old)
+    b = oracle.moe_layer(inp["x"], inp["Wg"], None, 2, True, inp["W1"], inp["W2"])
+    assert np.array_equal(a["out"], b["out"])
