@@ -1,0 +1,384 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 MoE layer forward (route -> permute -> FC1+SwiGLU ->
+FC2 -> combine) on seeded synthetic inputs.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  A step is one full layer forward over one
+batch of T tokens.  `value` = tokens of all ranks / max-over-ranks time, with
+inputs resident in HBM; `e2e` = the same through the public API with the
+token activations copied from pinned host memory and the output copied back
+inside the timed region (weights are resident model parameters).  The
+per-kernel breakdown and the roofline of the dominant kernel come from a
+second timed pass that launches the same kernels stage by stage with CUDA
+events on the launching stream.  With N > 1 (torchrun), every rank runs its
+own independent batch (weak scaling, no collective on the data path).
+`--impl reference` times the fp64 CPU oracle on a bounded sample instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import moe_inputs as mi  # noqa: E402
+
+METRIC = "MoE-layer tokens/s at 1 GB300; % of BF16 tensor peak (prefill) / HBM BW (decode)"
+DEFAULT_WORKLOAD = "qwen2_moe_like_prefill"
+
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant kernel,
+# from one ncu capture (profiles/), valid only while the kernel source hashes to
+# the recorded value.
+NCU_TRAFFIC = {}
+
+
+def _src_hash(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, src="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(self.dev)], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(local)
+    return ws, rank, local
+
+
+def _barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, ws: int) -> float:
+    """Largest value over all ranks (timing is taken as the slowest rank)."""
+    if ws <= 1:
+        return value
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _work(cfg, rows: int, active_slots: int):
+    """Algorithmic flops and bytes of the layer's kernels for one batch."""
+    T, H, I, k = cfg.T, cfg.H, cfg.I, cfg.k
+    Ish = cfg.n_shared * cfg.I_shared
+    fc1_flops = 4.0 * H * (rows * I + T * Ish)
+    fc2_flops = 2.0 * H * (rows * I + T * Ish)
+    w1 = active_slots * 2 * I * H * 2 + 2 * Ish * H * 2
+    w2 = active_slots * H * I * 2 + H * Ish * 2
+    fc1_bytes = w1 + (rows + T * (Ish > 0)) * H * 2 + rows * I * 2 + T * Ish * 2
+    fc2_bytes = w2 + rows * I * 2 + T * Ish * 2 + rows * H * 2 + (T * H * 2 if Ish else 0)
+    return dict(fc1_flops=fc1_flops, fc2_flops=fc2_flops, fc1_bytes=fc1_bytes, fc2_bytes=fc2_bytes,
+                gate_flops=2.0 * T * H * cfg.E)
+
+
+def run_cpu_baseline(inp_dev, cfg, target_s=10.0, T_cap=None):
+    """The fp64 oracle on the host cores, on the first n tokens of the batch."""
+    import numpy as np  # noqa: F401
+    import oracle
+    from moe_inputs import shared_concat  # noqa: F401
+    oracle.build()
+    oracle.set_threads(os.cpu_count() or 1)
+    cpu = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in inp_dev.items()}
+
+    def run(n):
+        t0 = time.perf_counter()
+        oracle.moe_layer(cpu["x"][:n], cpu["Wg"], cpu["bias"], cfg.k, cfg.renorm, cpu["W1"], cpu["W2"],
+                         rep_offset=cpu["rep_offset"], rep_slots=cpu["rep_slots"], W1s=cpu["W1s"],
+                         W2s=cpu["W2s"], shared_gate_w=cpu["w_s"], S=cfg.slots)
+        return time.perf_counter() - t0
+
+    threads = oracle.get_threads()
+    n0 = min(cfg.T, max(threads, 8))
+    t0 = run(n0)
+    n = int(max(n0, min(T_cap or cfg.T, n0 * target_s / max(t0, 1e-3))))
+    n = max(1, min(n, cfg.T))
+    t = run(n)
+    return dict(value=n / t, unit="tokens/s", cores=threads, kind="oracle",
+                sample=f"first {n} of the {cfg.T} tokens of {cfg.name}, whole layer in fp64 "
+                       f"({t:.1f} s, {threads} OpenMP threads)"), t
+
+
+def bench_ours(args):
+    import serving_router_gate_gb300 as moe
+    from serving_router_gate_gb300.layer import layer_from_inputs
+
+    ws_, rank, local = _dist()
+    cfg = mi.CONFIGS[args.workload]
+    dev = torch.device("cuda", local)
+    inp = mi.make_inputs(cfg, device=dev)
+    layer = layer_from_inputs(inp, dev)
+    x = inp["x"]
+    T, H = cfg.T, cfg.H
+    stream = torch.cuda.current_stream()
+    K, W = args.steps, args.warmup
+
+    for _ in range(W):
+        layer.forward(x)
+    torch.cuda.synchronize()
+    rows = int(layer.offsets[-1])
+    active = int((layer.counts > 0).sum())
+    status = moe.moe_get_device_status(layer.ws)
+    if status:
+        raise RuntimeError(f"device status {status} after warm-up")
+
+    # ---- timed pass: the whole layer, K steps ----
+    clocks = ClockSampler(torch.cuda.current_device())
+    _barrier(ws_)
+    torch.cuda.synchronize()
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        layer.forward(x)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    _barrier(ws_)
+    ms = e0.elapsed_time(e1) / K
+    ms = max_over_ranks(ms, ws_)
+    kernels_per_step = 2 + 4 + 3  # router 2, permute 4, FC1, FC2, finalize
+
+    # ---- staged pass: same kernels, events around each stage ----
+    Ish = cfg.n_shared * cfg.I_shared
+    P = T * cfg.k
+    h = torch.empty((P, cfg.I), dtype=torch.bfloat16, device=dev)
+    y = torch.empty((P, H), dtype=torch.bfloat16, device=dev)
+    h_sh = torch.empty((T, Ish), dtype=torch.bfloat16, device=dev) if Ish else None
+    y_sh = torch.empty((T, H), dtype=torch.bfloat16, device=dev) if Ish else None
+    names = ["route", "permute", "fc1", "fc2", "finalize"]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    xs = x if Ish else None
+    for i in range(K + W):
+        e = evs[i - W] if i >= W else None
+        if e: e[0].record(stream)
+        layer.route(x)
+        if e: e[1].record(stream)
+        layer.permute(x)
+        if e: e[2].record(stream)
+        moe.moe_grouped_fc1(layer.x_perm, layer.offsets, layer.W1, xs, layer.W1s, h, h_sh, layer.ws)
+        if e: e[3].record(stream)
+        moe.moe_grouped_fc2(h, layer.offsets, layer.W2, h_sh, layer.W2s, y, y_sh, layer.ws)
+        if e: e[4].record(stream)
+        moe.moe_finalize(y, layer.pair_row, layer.topk_w, y_sh, xs, layer.gate, layer.out, layer.ws)
+        if e: e[5].record(stream)
+    torch.cuda.synchronize()
+    stage_ms = {n: statistics.mean(ev[j].elapsed_time(ev[j + 1]) for ev in evs) for j, n in enumerate(names)}
+
+    # ---- e2e pass: host activations in, host output out ----
+    x_pin = x.cpu().pin_memory()
+    out_pin = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(x)
+    for _ in range(W):
+        x_dev.copy_(x_pin, non_blocking=True)
+        o = layer.forward(x_dev)
+        out_pin.copy_(o, non_blocking=True)
+    torch.cuda.synchronize()
+    _barrier(ws_)
+    e0.record(stream)
+    for _ in range(K):
+        x_dev.copy_(x_pin, non_blocking=True)
+        o = layer.forward(x_dev)
+        out_pin.copy_(o, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1) / K, ws_)
+    status = moe.moe_get_device_status(layer.ws)
+    if status:
+        raise RuntimeError(f"device status {status} after the timed runs")
+
+    peaks = _peaks()
+    wk = _work(cfg, rows, active)
+    decode = T <= 256
+    fc1_s = stage_ms["fc1"] * 1e-3
+    if decode:
+        achieved = wk["fc1_bytes"] / fc1_s / 1e9
+        roof = dict(bound="hbm", kernel="grouped_gemm_kernel<FC1+SwiGLU>", achieved=achieved, peak=peaks["hbm"],
+                    unit="GB/s", frac=achieved / peaks["hbm"], peak_kind=f"{peaks['src']} hbm_gbs")
+        per_unit = f"{wk['fc1_bytes']:.0f} algorithmic bytes per launch (active slots' W1 + shared W1 + A rows + h)"
+    else:
+        achieved = wk["fc1_flops"] / fc1_s / 1e12
+        roof = dict(bound="tensor", kernel="grouped_gemm_kernel<FC1+SwiGLU>", achieved=achieved,
+                    peak=peaks["bf16_sustained"], unit="TFLOP/s", frac=achieved / peaks["bf16_sustained"],
+                    peak_kind=f"{peaks['src']} bf16_tflops_sustained (kernel timed inside a seconds-long loop)")
+        per_unit = f"{wk['fc1_flops']:.4g} flops per launch = 4*H*(rows*I + T*I_shared)"
+    key = (args.workload, _src_hash(os.path.join(ROOT, "serving_router_gate_gb300", "csrc", "moe_grouped_gemm.cu")))
+    roof["traffic"] = NCU_TRAFFIC.get(key)
+    roof["work"] = per_unit
+
+    total_tokens = T * ws_
+    res = {
+        "metric": METRIC, "value": total_tokens / (ms * 1e-3), "unit": "tokens/s", "n_gpus": ws_, "steps": K,
+        "warmup": W, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic: seeded N(0,1) activations, N(0,sigma) random-init weights of the "
+                                 "workload's shapes (no checkpoint)",
+        "config": {"workload": cfg.name, "shape": mi.describe(cfg), "tokens_per_gpu": T,
+                   "parallelism": f"replicas x{ws_} (independent token batches, no collective)",
+                   "l2": "inputs larger than L2 (expert weights %.2f GB per step)" % (
+                       (cfg.slots * 3 * cfg.I * H * 2 + 3 * Ish * H * 2) / 1e9)},
+        "roofline": roof,
+        "e2e": {"value": total_tokens / (ms_e2e * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2,
+                "d2h_bytes_per_step": T * H * 2, "ms_per_step": ms_e2e},
+        "gpu_launches": kernels_per_step * K,
+        "clocks": clk,
+        "kernels_ms": stage_ms,
+        "tflops_layer": (wk["fc1_flops"] + wk["fc2_flops"] + wk["gate_flops"]) / (ms * 1e-3) / 1e12,
+        "grouped_gemm_tflops": (wk["fc1_flops"] + wk["fc2_flops"]) / ((stage_ms["fc1"] + stage_ms["fc2"]) * 1e-3) / 1e12,
+        "rows": rows, "active_slots": active,
+    }
+    if rank == 0 and ws_ == 1 and not args.no_cpu_baseline:
+        base, _ = run_cpu_baseline(inp, cfg, target_s=args.cpu_seconds)
+        res["cpu_baseline"] = base
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if ws_ > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def bench_reference(args):
+    """The fp64 oracle, as it stands, on the host cores: each step a bounded
+    sample of the workload (its first n tokens through the whole layer)."""
+    ws_ = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    oracle.set_threads(os.cpu_count() or 1)
+    cfg = mi.CONFIGS[args.workload]
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = mi.make_inputs(cfg, device=dev)
+    cpu = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+
+    def step(n):
+        oracle.moe_layer(cpu["x"][:n], cpu["Wg"], cpu["bias"], cfg.k, cfg.renorm, cpu["W1"], cpu["W2"],
+                         rep_offset=cpu["rep_offset"], rep_slots=cpu["rep_slots"], W1s=cpu["W1s"],
+                         W2s=cpu["W2s"], shared_gate_w=cpu["w_s"], S=cfg.slots)
+
+    threads = oracle.get_threads()
+    n0 = min(cfg.T, max(8, threads))
+    t0 = time.perf_counter()
+    step(n0)
+    per = (time.perf_counter() - t0) / n0
+    budget = 150.0 / max(1, args.steps + args.warmup)  # whole run within a few minutes
+    n = max(1, min(cfg.T, int(budget / max(per, 1e-6))))
+    for _ in range(args.warmup):
+        step(n)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step(n)
+    dt = (time.perf_counter() - t0) / args.steps
+    v = n / dt
+    res = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": ws_,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic: seeded inputs of the workload's shapes",
+           "config": {"workload": cfg.name, "shape": mi.describe(cfg), "tokens_per_step": n},
+           "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                            "sample": f"first {n} of the {cfg.T} tokens per step, whole layer in fp64"},
+           "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(res), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(mi.CONFIGS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        bench_reference(args)
+    else:
+        bench_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,252 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) Mixture-of-Experts layer forward.
+ *
+ * One MoE layer on one GPU, in three stream-ordered calls:
+ *
+ *   moe_route    gate GEMM (fp32), softmax over all experts, top-k by logit
+ *                with ties to the lower expert id, optional renormalisation;
+ *   moe_permute  expert -> expert-slot map (identity or replica table),
+ *                optional expert-parallel local-range mask/remap, per-slot
+ *                histogram, exclusive scan, stable token scatter;
+ *   moe_forward  grouped GEMM FC1 with a fused SwiGLU epilogue, grouped GEMM
+ *                FC2, then the routing-weighted combine of each token's k
+ *                expert outputs plus an optional shared expert.
+ *
+ * moe_forward is also exposed as its three stages (moe_grouped_fc1,
+ * moe_grouped_fc2, moe_finalize) so each can be checked on its own.
+ *
+ * Conventions (all calls):
+ *  - Every data pointer is a DEVICE pointer owned by the caller.  Shapes are
+ *    row-major with the last index contiguous.  bf16 data is passed as its
+ *    16-bit patterns (moe_bf16_t).  Pointers must be 16-byte aligned and row
+ *    strides multiples of 16 bytes (true when H and I are multiples of 64).
+ *  - The library allocates no memory and never synchronises the host: every
+ *    call enqueues kernels on `stream` and returns.  Scratch space is the
+ *    caller's workspace `ws` (size from moe_workspace_size, zeroed once with
+ *    moe_workspace_init).  Calls that share a workspace must be ordered on one
+ *    stream; calls that overlap on the GPU with one workspace race.
+ *  - The return value reports host-side argument checks and launch errors.
+ *    Errors found by kernels (an expert id or slot id out of range, a wait
+ *    that timed out) are OR-ed into a status word inside `ws`; read and clear
+ *    it with moe_get_device_status.  Kernels never trap: a bad pair is dropped
+ *    and flagged, a timed-out wait abandons its tile and flags.
+ *  - T = 0 is valid and enqueues nothing.
+ *  - Supported sizes: H and I multiples of 64, 1 <= k <= 32, k <= E <= 512,
+ *    S (slots) <= 1024, T * k < 2^31; anything else -> MOE_ERR_UNSUPPORTED.
+ *
+ * Source pages of the method (cited by title and section):
+ *  [TRT-4495]  TensorRT-LLM PR #4495, "large-scale EP (part 3): refactor
+ *              FusedMoe for redundant expert", Description (experts vs expert
+ *              slots; weights live in slots; the fused op computes on slots).
+ *  [TRT-10985] TensorRT-LLM PR #10985, "MoE all-to-all paradigm" (fused MoE op
+ *              trtllm_moe_fused(tokens, experts, weights[, mapping_config]),
+ *              gated-MLP experts, workspace sized by max_num_tokens).
+ *  [VLLM-EP]   vLLM EP-aware FusedMoE override (ep_fused_moe_patch.py): module
+ *              docstring "EP expert dispatch" (global top-k ids on every rank,
+ *              mask non-local experts, per-expert loop that skips count 0),
+ *              ep_mask_and_remap, ep_reduce_output, the patched __init__.
+ *  [DS-6964]   DeepSpeed PR #6964, AutoTP for MoE models (one reduction after
+ *              the weighted sum of the selected experts' outputs per layer).
+ */
+#ifndef SERVING_ROUTER_GATE_GB300_MOE_H
+#define SERVING_ROUTER_GATE_GB300_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t moe_bf16_t;            /* bf16 bit pattern */
+typedef struct CUstream_st *moe_stream_t; /* same handle as cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,    /* a NULL pointer, a negative size, k > E, a range outside [0, S) ... */
+    MOE_ERR_UNSUPPORTED = 2,    /* sizes outside the supported envelope above */
+    MOE_ERR_WORKSPACE = 3,      /* ws is NULL or smaller than the call needs */
+    MOE_ERR_CUDA = 4,           /* a CUDA runtime/driver call failed (launch, tensor map, attribute) */
+    MOE_ERR_DEVICE_BOUNDS = 8,  /* device status bit: an expert or slot id was out of range (pair dropped) */
+    MOE_ERR_TIMEOUT = 16        /* device status bit: a bounded wait inside a kernel gave up */
+} moe_status_t;
+
+typedef enum {
+    MOE_NONLOCAL_SKIP = 0,      /* non-local pairs get slot -1 and are not computed */
+    MOE_NONLOCAL_MOD = 1        /* non-local pairs get slot (slot mod local_count) with weight 0 */
+} moe_nonlocal_mode_t;
+
+/* Human-readable name of a status value (static string). */
+MOE_API const char *moe_status_string(int status);
+
+/* Bytes of workspace that moe_route, moe_permute and moe_forward need for up
+ * to max_T tokens (the same buffer serves all three calls).  S = number of
+ * expert slots the forward computes (the local count when a local range is
+ * used), I_shared_total = summed intermediate size of the shared experts (0:
+ * none).  Returns 0 for invalid sizes.  Sized by the largest token count the
+ * caller will pass, as [TRT-10985] sizes its workspace by max_num_tokens. */
+MOE_API size_t moe_workspace_size(int64_t max_T, int H, int I, int E, int S, int k, int I_shared_total);
+
+/* Zero the workspace's header (status word and counters).  Call once after
+ * allocating ws, before the first call that uses it. */
+MOE_API moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Read the device status word (an OR of MOE_ERR_DEVICE_BOUNDS /
+ * MOE_ERR_TIMEOUT bits, 0 when clean) into *device_status and clear it.  This
+ * call synchronises `stream` (it copies 4 bytes to the host). */
+MOE_API moe_status_t moe_get_device_status(void *ws, moe_stream_t stream, int32_t *device_status);
+
+/* Number of tokens whose top-k decision needed the fp64 recheck in the last
+ * moe_route calls since moe_workspace_init (diagnostic; synchronises). */
+MOE_API moe_status_t moe_get_route_stats(void *ws, moe_stream_t stream, int64_t *refined_tokens);
+
+/* ------------------------------------------------------------------------ */
+/* moe_route -- router: gate GEMM, softmax, top-k, renormalisation.          */
+/* ------------------------------------------------------------------------ */
+/* [VLLM-EP] docstring "EP expert dispatch": top-k routing produces global
+ * expert ids, identical on every rank; patched __init__: renormalize defaults
+ * to true and routing runs over the global expert count.
+ *
+ *   x          [T, H] bf16         token activations
+ *   gate_w     [E, H] fp32         router weight
+ *   logit_bias [E] fp32 or NULL    added to the logits before the softmax
+ *   renorm     0/1                 divide the k probabilities by their sum
+ *   topk_ids   [T, k] int32 out    experts by descending logit, ties -> lower id
+ *   topk_w     [T, k] fp32 out     softmax probability over all E experts of
+ *                                  each selected expert (renormalised if asked)
+ *
+ * Logits are computed in fp32 on CUDA cores with a certified error bound per
+ * token; whenever two logits that decide the selection or its order lie within
+ * that bound, those logits are recomputed in fp64, so the ids equal those of an
+ * exact (fp64) evaluation up to fp64 rounding. */
+MOE_API moe_status_t moe_route(const moe_bf16_t *x, const float *gate_w, const float *logit_bias,
+                       int64_t T, int H, int E, int k, int renorm,
+                       int32_t *topk_ids, float *topk_w,
+                       void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* moe_permute -- slot map, local mask/remap, histogram, scan, scatter.     */
+/* ------------------------------------------------------------------------ */
+/* Slot map [TRT-4495]: slot = expert id when rep_offset is NULL (then S must
+ * equal E); otherwise expert e owns rep_offset[e+1] - rep_offset[e] >= 1 slots
+ * listed at rep_slots[rep_offset[e] ...] and token t uses replica (t mod that
+ * count).  Local range [VLLM-EP] ep_mask_and_remap, applied to slot ids when
+ * local_count >= 0: a pair is local iff local_start <= slot < local_start +
+ * local_count; topk_w is multiplied by that 0/1 mask IN PLACE; local slots
+ * become slot - local_start, non-local ones -1 (MOE_NONLOCAL_SKIP) or slot mod
+ * local_count (MOE_NONLOCAL_MOD, computed with weight 0).  local_count = -1:
+ * no mask, S_local = S.  Otherwise S_local = local_count.
+ *
+ *   topk_ids  [T, k] int32 in      expert ids (out-of-range ids are dropped and flagged)
+ *   topk_w    [T, k] fp32 in/out   routing weights, zeroed for non-local pairs
+ *   rep_offset [E+1] int32 or NULL, rep_slots [S] int32
+ *   x         [T, H] bf16 in
+ *   slot_ids  [T, k] int32 out     local slot of each pair, or -1 (dropped)
+ *   counts    [S_local] int32 out  pairs per local slot
+ *   offsets   [S_local+1] int32 out exclusive scan of counts (offsets[S_local] = rows)
+ *   perm_src  [T*k] int32 out      row r (< offsets[S_local]) holds pair perm_src[r]
+ *                                  (pair index t*k + j); entries past the row count
+ *                                  are left unspecified
+ *   pair_row  [T*k] int32 out      row of pair p, or -1
+ *   x_perm    [T*k, H] bf16 out    x_perm[r] = x[perm_src[r] / k]; rows past the
+ *                                  row count are left unspecified
+ * Rows of one slot hold its pairs in ascending pair index (a stable grouping). */
+MOE_API moe_status_t moe_permute(const int32_t *topk_ids, float *topk_w, int64_t T, int k, int E,
+                         const int32_t *rep_offset, const int32_t *rep_slots, int S,
+                         int local_start, int local_count, int nonlocal_mode,
+                         const moe_bf16_t *x, int H,
+                         int32_t *slot_ids, int32_t *counts, int32_t *offsets,
+                         int32_t *perm_src, int32_t *pair_row, moe_bf16_t *x_perm,
+                         void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* moe_forward -- FC1 + SwiGLU, FC2, weighted combine (+ shared expert).    */
+/* ------------------------------------------------------------------------ */
+/* Per slot s (rows offsets[s] .. offsets[s+1]-1 of x_perm), the gated MLP of
+ * [TRT-10985] (is_gated_mlp, act_fn per expert):
+ *     h = bf16( silu(x_perm W1[s]_gate^T) * (x_perm W1[s]_up^T) ),  y = bf16(h W2[s]^T)
+ * slots with no rows are skipped ([VLLM-EP] docstring: the per-expert loop
+ * skips experts with count 0).  Then per token, the weighted sum of its
+ * selected experts' outputs in fixed j order ([DS-6964]; [VLLM-EP]
+ * ep_reduce_output adds the shared expert: out = routed + shared):
+ *     out[t] = bf16( sum_j topk_w[t,j] * y[pair_row[t,j]]  (pairs with row -1 skipped)
+ *                    + g_t * shared(x[t]) )
+ * where shared() is the gated MLP with W1s/W2s and g_t = sigmoid(x[t] . shared_gate_w)
+ * (fp32 dot) when shared_gate_w is given, else 1.
+ *
+ *   x_perm    [P_cap, H] bf16       permuted activations (moe_permute)
+ *   offsets   [S_local+1] int32     row offsets per slot (device; read by the kernels)
+ *   P_cap     rows of x_perm's allocation (>= offsets[S_local]; normally T*k)
+ *   W1        [S_local, 2I, H] bf16  per slot: I gate rows, then I up rows
+ *   W2        [S_local, H, I] bf16
+ *   pair_row  [T, k] int32, topk_w [T, k] fp32 (after the mask)
+ *   x         [T, H] bf16           input of the shared expert (may be NULL if none)
+ *   W1s       [2*I_shared_total, H] bf16 (gate rows then up rows) or NULL
+ *   W2s       [H, I_shared_total] bf16 or NULL
+ *   shared_gate_w [H] bf16 or NULL
+ *   out       [T, H] bf16 out
+ * Several shared experts are passed as one gated MLP whose gate rows, up rows
+ * and W2 columns are the experts' concatenated (the sum of their outputs). */
+MOE_API moe_status_t moe_forward(const moe_bf16_t *x_perm, const int32_t *offsets, int S_local, int64_t P_cap,
+                         const moe_bf16_t *W1, const moe_bf16_t *W2, int H, int I,
+                         const int32_t *pair_row, const float *topk_w, int64_t T, int k,
+                         const moe_bf16_t *x, const moe_bf16_t *W1s, const moe_bf16_t *W2s,
+                         int I_shared_total, const moe_bf16_t *shared_gate_w,
+                         moe_bf16_t *out, void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/* ---- the three stages of moe_forward ------------------------------------ */
+
+/* FC1 + SwiGLU on the tcgen05 tensor cores.  Routed problem: for each of the G
+ * groups, rows offsets[g] .. offsets[g+1]-1 of a ([rows_cap, K=H] bf16) times
+ * W1[g] ([2I, H]) -> h ([rows_cap, I] bf16).  Shared problem (skipped when
+ * I_shared_total = 0): a_shared ([T, H]) times W1s ([2*I_shared_total, H]) ->
+ * h_shared ([T, I_shared_total] bf16).  ws: only its status word is used. */
+MOE_API moe_status_t moe_grouped_fc1(const moe_bf16_t *a, int64_t rows_cap, const int32_t *offsets, int G,
+                             const moe_bf16_t *W1, int H, int I,
+                             const moe_bf16_t *a_shared, int64_t T, const moe_bf16_t *W1s,
+                             int I_shared_total, moe_bf16_t *h, moe_bf16_t *h_shared,
+                             void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/* FC2 on the tcgen05 tensor cores: h ([rows_cap, I]) times W2[g] ([H, I]) ->
+ * y ([rows_cap, H] bf16) per group; h_shared ([T, I_shared_total]) times W2s
+ * ([H, I_shared_total]) -> y_shared ([T, H] bf16). */
+MOE_API moe_status_t moe_grouped_fc2(const moe_bf16_t *h, int64_t rows_cap, const int32_t *offsets, int G,
+                             const moe_bf16_t *W2, int H, int I,
+                             const moe_bf16_t *h_shared, int64_t T, const moe_bf16_t *W2s,
+                             int I_shared_total, moe_bf16_t *y, moe_bf16_t *y_shared,
+                             void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Unpermute + weighted combine: out[t] = bf16(sum_j topk_w[t,j] * y[pair_row[t,j]]
+ * + g_t * y_shared[t]), fp32 accumulation in fixed j order.  y_shared may be
+ * NULL (no shared expert); g_t as in moe_forward (x and shared_gate_w NULL ->
+ * g_t = 1).  pair_row entries outside [0, rows_cap) other than -1 are
+ * dropped and flagged. */
+MOE_API moe_status_t moe_finalize(const moe_bf16_t *y, int64_t rows_cap, const int32_t *pair_row,
+                          const float *topk_w, int64_t T, int k, int H,
+                          const moe_bf16_t *y_shared, const moe_bf16_t *x,
+                          const moe_bf16_t *shared_gate_w, moe_bf16_t *out,
+                          void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/* ---- diagnostics ---------------------------------------------------------- */
+
+/* Launch one block whose single thread waits on an mbarrier that nothing ever
+ * completes, with the same bounded wait the GEMM kernels use, limited to
+ * timeout_ns.  The kernel returns normally and sets MOE_ERR_TIMEOUT in the
+ * device status word.  Lets a test check the timeout path without a hang. */
+MOE_API moe_status_t moe_debug_wait_timeout(void *ws, size_t ws_bytes, uint64_t timeout_ns, moe_stream_t stream);
+
+/* Set the limit (ns) after which a wait inside a kernel gives up (default 4 s).
+ * Process-wide; applies to launches made after the call. */
+MOE_API void moe_set_wait_timeout_ns(uint64_t timeout_ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SERVING_ROUTER_GATE_GB300_MOE_H */

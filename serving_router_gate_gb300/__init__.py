@@ -1,0 +1,239 @@
+"""Python binding of the GB300 MoE layer library (include/moe.h).
+
+Thin ctypes marshalling over libmoe_gb300.so: each function takes torch CUDA
+tensors, checks dtype / device / contiguity / shape, and passes raw pointers,
+sizes and the current torch stream to the C function of the same name.  Every
+step of the layer runs in the library's CUDA kernels; nothing here computes.
+
+The library must be built (``serving_router_gate_gb300._build.build()``, or
+``__graft_entry__.build()``); importing this module without it raises
+ImportError -- there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "MOE_OK", "MOE_ERR_INVALID_ARG", "MOE_ERR_UNSUPPORTED", "MOE_ERR_WORKSPACE", "MOE_ERR_CUDA",
+    "MOE_ERR_DEVICE_BOUNDS", "MOE_ERR_TIMEOUT", "MOE_NONLOCAL_SKIP", "MOE_NONLOCAL_MOD", "MoEError",
+    "lib_path", "moe_workspace_size", "moe_workspace_init", "moe_get_device_status", "moe_get_route_stats",
+    "moe_route", "moe_permute", "moe_forward", "moe_grouped_fc1", "moe_grouped_fc2", "moe_finalize",
+    "moe_debug_wait_timeout", "moe_set_wait_timeout_ns", "EXPORTED_SYMBOLS",
+]
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = 1
+MOE_ERR_UNSUPPORTED = 2
+MOE_ERR_WORKSPACE = 3
+MOE_ERR_CUDA = 4
+MOE_ERR_DEVICE_BOUNDS = 8
+MOE_ERR_TIMEOUT = 16
+MOE_NONLOCAL_SKIP = 0
+MOE_NONLOCAL_MOD = 1
+
+EXPORTED_SYMBOLS = (
+    "moe_status_string", "moe_workspace_size", "moe_workspace_init", "moe_get_device_status",
+    "moe_get_route_stats", "moe_route", "moe_permute", "moe_forward", "moe_grouped_fc1", "moe_grouped_fc2",
+    "moe_finalize", "moe_debug_wait_timeout", "moe_set_wait_timeout_ns",
+)
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {_lib.moe_status_string(status).decode()} (status {status})")
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def _load():
+    path = _build.LIB_PATH
+    if not os.path.exists(path):
+        raise ImportError(f"CUDA library not built: {path} is missing (run serving_router_gate_gb300._build.build())")
+    lib = ctypes.CDLL(path)
+    P, i32, i64, sz, u64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_uint64
+    sig = {
+        "moe_status_string": ([ctypes.c_int], ctypes.c_char_p),
+        "moe_workspace_size": ([i64, i32, i32, i32, i32, i32, i32], sz),
+        "moe_workspace_init": ([P, sz, P], i32),
+        "moe_get_device_status": ([P, P, P], i32),
+        "moe_get_route_stats": ([P, P, P], i32),
+        "moe_route": ([P, P, P, i64, i32, i32, i32, i32, P, P, P, sz, P], i32),
+        "moe_permute": ([P, P, i64, i32, i32, P, P, i32, i32, i32, i32, P, i32, P, P, P, P, P, P, P, sz, P], i32),
+        "moe_forward": ([P, P, i32, i64, P, P, i32, i32, P, P, i64, i32, P, P, P, i32, P, P, P, sz, P], i32),
+        "moe_grouped_fc1": ([P, i64, P, i32, P, i32, i32, P, i64, P, i32, P, P, P, sz, P], i32),
+        "moe_grouped_fc2": ([P, i64, P, i32, P, i32, i32, P, i64, P, i32, P, P, P, sz, P], i32),
+        "moe_finalize": ([P, i64, P, P, i64, i32, i32, P, P, P, P, P, sz, P], i32),
+        "moe_debug_wait_timeout": ([P, sz, u64, P], i32),
+        "moe_set_wait_timeout_ns": ([u64], None),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    return lib
+
+
+_lib = _load()
+
+
+# ----------------------------------------------------------------------------- marshalling helpers
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t, name, dtype=None, shape=None, allow_none=False):
+    if t is None:
+        if allow_none:
+            return None
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _check(fn, status):
+    if status != MOE_OK:
+        raise MoEError(fn, status)
+
+
+_bf16, _f32, _i32 = torch.bfloat16, torch.float32, torch.int32
+
+
+# ----------------------------------------------------------------------------- API (names of include/moe.h)
+
+def moe_workspace_size(max_T, H, I, E, S, k, I_shared_total=0) -> int:
+    n = _lib.moe_workspace_size(max_T, H, I, E, S, k, I_shared_total)
+    if n == 0:
+        raise MoEError("moe_workspace_size", MOE_ERR_UNSUPPORTED)
+    return int(n)
+
+
+def moe_workspace_init(ws, stream=None):
+    _check("moe_workspace_init", _lib.moe_workspace_init(_ptr(ws, "ws", torch.uint8), ws.numel(), _stream(stream)))
+
+
+def moe_get_device_status(ws, stream=None) -> int:
+    v = ctypes.c_int32(0)
+    _check("moe_get_device_status",
+           _lib.moe_get_device_status(_ptr(ws, "ws", torch.uint8), _stream(stream), ctypes.byref(v)))
+    return int(v.value)
+
+
+def moe_get_route_stats(ws, stream=None) -> int:
+    v = ctypes.c_int64(0)
+    _check("moe_get_route_stats",
+           _lib.moe_get_route_stats(_ptr(ws, "ws", torch.uint8), _stream(stream), ctypes.byref(v)))
+    return int(v.value)
+
+
+def moe_route(x, gate_w, logit_bias, k, renorm, topk_ids, topk_w, ws, stream=None):
+    T, H = x.shape
+    E = gate_w.shape[0]
+    st = _lib.moe_route(_ptr(x, "x", _bf16, (T, H)), _ptr(gate_w, "gate_w", _f32, (E, H)),
+                        _ptr(logit_bias, "logit_bias", _f32, (E,), allow_none=True), T, H, E, k, int(bool(renorm)),
+                        _ptr(topk_ids, "topk_ids", _i32, (T, k)), _ptr(topk_w, "topk_w", _f32, (T, k)),
+                        _ptr(ws, "ws", torch.uint8), ws.numel(), _stream(stream))
+    _check("moe_route", st)
+
+
+def moe_permute(topk_ids, topk_w, E, rep_offset, rep_slots, S, local_start, local_count, nonlocal_mode, x,
+                slot_ids, counts, offsets, perm_src, pair_row, x_perm, ws, stream=None):
+    T, k = topk_ids.shape
+    H = x.shape[1]
+    S_local = local_count if local_count >= 0 else S
+    st = _lib.moe_permute(_ptr(topk_ids, "topk_ids", _i32, (T, k)), _ptr(topk_w, "topk_w", _f32, (T, k)), T, k, E,
+                          _ptr(rep_offset, "rep_offset", _i32, (E + 1,), allow_none=True),
+                          _ptr(rep_slots, "rep_slots", _i32, (S,), allow_none=True), S, local_start, local_count,
+                          nonlocal_mode, _ptr(x, "x", _bf16, (T, H)), H,
+                          _ptr(slot_ids, "slot_ids", _i32, (T, k)), _ptr(counts, "counts", _i32, (S_local,)),
+                          _ptr(offsets, "offsets", _i32, (S_local + 1,)), _ptr(perm_src, "perm_src", _i32, (T * k,)),
+                          _ptr(pair_row, "pair_row", _i32, (T, k)), _ptr(x_perm, "x_perm", _bf16, (T * k, H)),
+                          _ptr(ws, "ws", torch.uint8), ws.numel(), _stream(stream))
+    _check("moe_permute", st)
+
+
+def moe_forward(x_perm, offsets, W1, W2, pair_row, topk_w, x, W1s, W2s, shared_gate_w, out, ws, stream=None):
+    P_cap, H = x_perm.shape
+    S_local = offsets.shape[0] - 1
+    I = W2.shape[2]
+    T, k = pair_row.shape
+    I_sh = 0 if W2s is None else W2s.shape[1]
+    st = _lib.moe_forward(_ptr(x_perm, "x_perm", _bf16), _ptr(offsets, "offsets", _i32), S_local, P_cap,
+                          _ptr(W1, "W1", _bf16, (S_local, 2 * I, H)), _ptr(W2, "W2", _bf16, (S_local, H, I)), H, I,
+                          _ptr(pair_row, "pair_row", _i32), _ptr(topk_w, "topk_w", _f32, (T, k)), T, k,
+                          _ptr(x, "x", _bf16, (T, H), allow_none=True),
+                          _ptr(W1s, "W1s", _bf16, (2 * I_sh, H), allow_none=True),
+                          _ptr(W2s, "W2s", _bf16, (H, I_sh), allow_none=True), I_sh,
+                          _ptr(shared_gate_w, "shared_gate_w", _bf16, (H,), allow_none=True),
+                          _ptr(out, "out", _bf16, (T, H)), _ptr(ws, "ws", torch.uint8), ws.numel(), _stream(stream))
+    _check("moe_forward", st)
+
+
+def moe_grouped_fc1(a, offsets, W1, a_shared, W1s, h, h_shared, ws, stream=None):
+    rows_cap, H = a.shape
+    G = offsets.shape[0] - 1
+    I = W1.shape[1] // 2
+    T = 0 if a_shared is None else a_shared.shape[0]
+    I_sh = 0 if W1s is None else W1s.shape[0] // 2
+    st = _lib.moe_grouped_fc1(_ptr(a, "a", _bf16), rows_cap, _ptr(offsets, "offsets", _i32), G,
+                              _ptr(W1, "W1", _bf16, (G, 2 * I, H)), H, I,
+                              _ptr(a_shared, "a_shared", _bf16, (T, H), allow_none=True), T,
+                              _ptr(W1s, "W1s", _bf16, (2 * I_sh, H), allow_none=True), I_sh,
+                              _ptr(h, "h", _bf16, (rows_cap, I)),
+                              _ptr(h_shared, "h_shared", _bf16, (T, I_sh), allow_none=True),
+                              _ptr(ws, "ws", torch.uint8), ws.numel(), _stream(stream))
+    _check("moe_grouped_fc1", st)
+
+
+def moe_grouped_fc2(h, offsets, W2, h_shared, W2s, y, y_shared, ws, stream=None):
+    rows_cap, I = h.shape
+    G = offsets.shape[0] - 1
+    H = W2.shape[1]
+    T = 0 if h_shared is None else h_shared.shape[0]
+    I_sh = 0 if W2s is None else W2s.shape[1]
+    st = _lib.moe_grouped_fc2(_ptr(h, "h", _bf16), rows_cap, _ptr(offsets, "offsets", _i32), G,
+                              _ptr(W2, "W2", _bf16, (G, H, I)), H, I,
+                              _ptr(h_shared, "h_shared", _bf16, (T, I_sh), allow_none=True), T,
+                              _ptr(W2s, "W2s", _bf16, (H, I_sh), allow_none=True), I_sh,
+                              _ptr(y, "y", _bf16, (rows_cap, H)),
+                              _ptr(y_shared, "y_shared", _bf16, (T, H), allow_none=True),
+                              _ptr(ws, "ws", torch.uint8), ws.numel(), _stream(stream))
+    _check("moe_grouped_fc2", st)
+
+
+def moe_finalize(y, pair_row, topk_w, y_shared, x, shared_gate_w, out, ws, stream=None):
+    rows_cap, H = y.shape
+    T, k = pair_row.shape
+    st = _lib.moe_finalize(_ptr(y, "y", _bf16), rows_cap, _ptr(pair_row, "pair_row", _i32, (T, k)),
+                           _ptr(topk_w, "topk_w", _f32, (T, k)), T, k, H,
+                           _ptr(y_shared, "y_shared", _bf16, (T, H), allow_none=True),
+                           _ptr(x, "x", _bf16, (T, H), allow_none=True),
+                           _ptr(shared_gate_w, "shared_gate_w", _bf16, (H,), allow_none=True),
+                           _ptr(out, "out", _bf16, (T, H)), _ptr(ws, "ws", torch.uint8), ws.numel(), _stream(stream))
+    _check("moe_finalize", st)
+
+
+def moe_debug_wait_timeout(ws, timeout_ns, stream=None):
+    _check("moe_debug_wait_timeout",
+           _lib.moe_debug_wait_timeout(_ptr(ws, "ws", torch.uint8), ws.numel(), int(timeout_ns), _stream(stream)))
+
+
+def moe_set_wait_timeout_ns(timeout_ns: int) -> None:
+    _lib.moe_set_wait_timeout_ns(int(timeout_ns))

@@ -1,0 +1,320 @@
+// moe_api.cu -- the C ABI of include/moe.h: argument checks, workspace
+// carve-up and kernel launches.  No allocation, no host synchronisation
+// (except the two explicit status readers).
+#include <algorithm>
+#include <atomic>
+#include <mutex>
+
+#include "moe_internal.cuh"
+
+using namespace moe;
+
+namespace {
+
+std::atomic<uint64_t> g_timeout_ns{4000000000ull};
+
+int device_sms() {
+    static std::mutex mu;
+    static int cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+    if (dev >= 0 && dev < 64) cache[dev] = n;
+    return n;
+}
+
+size_t a256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+struct ForwardLayout {
+    size_t h, h_sh, y, y_sh, total;
+};
+
+ForwardLayout forward_layout(int64_t P_cap, int64_t T, int H, int I, int I_sh) {
+    ForwardLayout L;
+    size_t off = kWsHeaderBytes;
+    L.h = off;
+    off += a256((size_t)P_cap * (size_t)I * 2);
+    L.h_sh = off;
+    off += a256((size_t)(I_sh > 0 ? T : 0) * (size_t)I_sh * 2);
+    L.y = off;
+    off += a256((size_t)P_cap * (size_t)H * 2);
+    L.y_sh = off;
+    off += a256((size_t)(I_sh > 0 ? T : 0) * (size_t)H * 2);
+    L.total = off;
+    return L;
+}
+
+size_t route_need(int64_t T, int H, int E) { return kWsHeaderBytes + router_scratch_bytes(T, H, E, 0); }
+size_t permute_need(int64_t P, int S_local) { return kWsHeaderBytes + permute_scratch_bytes(P, S_local); }
+
+bool dim_ok(int v) { return v > 0 && v % 64 == 0 && v <= (1 << 20); }
+
+moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(int status) {
+    switch (status) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "unsupported size";
+        case MOE_ERR_WORKSPACE: return "workspace missing or too small";
+        case MOE_ERR_CUDA: return "CUDA error";
+        case MOE_ERR_DEVICE_BOUNDS: return "device: id out of range";
+        case MOE_ERR_TIMEOUT: return "device: bounded wait timed out";
+        case MOE_ERR_DEVICE_BOUNDS | MOE_ERR_TIMEOUT: return "device: id out of range and wait timed out";
+        default: return "unknown status";
+    }
+}
+
+void moe_set_wait_timeout_ns(uint64_t timeout_ns) { g_timeout_ns.store(timeout_ns > 0 ? timeout_ns : 1); }
+
+size_t moe_workspace_size(int64_t max_T, int H, int I, int E, int S, int k, int I_shared_total) {
+    if (max_T < 0 || !dim_ok(H) || !dim_ok(I) || E < 1 || E > 512 || S < 1 || S > 1024 || k < 1 || k > 32 ||
+        k > E || I_shared_total < 0 || (I_shared_total > 0 && !dim_ok(I_shared_total)))
+        return 0;
+    const int64_t P = max_T * k;
+    size_t need = route_need(max_T, H, E);
+    need = std::max(need, permute_need(P, S));
+    need = std::max(need, forward_layout(P, max_T, H, I, I_shared_total).total);
+    return need;
+}
+
+moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream) {
+    if (!ws || ws_bytes < kWsHeaderBytes) return MOE_ERR_WORKSPACE;
+    return cuda_status(cudaMemsetAsync(ws, 0, kWsHeaderBytes, (cudaStream_t)stream));
+}
+
+moe_status_t moe_get_device_status(void* ws, moe_stream_t stream, int32_t* device_status) {
+    if (!ws || !device_status) return MOE_ERR_INVALID_ARG;
+    WsHeader* hdr = static_cast<WsHeader*>(ws);
+    int32_t v = 0;
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaMemcpyAsync(&v, &hdr->status, sizeof(v), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(&hdr->status, 0, sizeof(int32_t), s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    *device_status = v;
+    return MOE_OK;
+}
+
+moe_status_t moe_get_route_stats(void* ws, moe_stream_t stream, int64_t* refined_tokens) {
+    if (!ws || !refined_tokens) return MOE_ERR_INVALID_ARG;
+    WsHeader* hdr = static_cast<WsHeader*>(ws);
+    unsigned long long v = 0;
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaMemcpyAsync(&v, &hdr->refined, sizeof(v), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    *refined_tokens = (int64_t)v;
+    return MOE_OK;
+}
+
+moe_status_t moe_route(const moe_bf16_t* x, const float* gate_w, const float* logit_bias, int64_t T, int H, int E,
+                       int k, int renorm, int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes,
+                       moe_stream_t stream) {
+    if (T < 0 || H <= 0 || E <= 0 || k <= 0 || k > E) return MOE_ERR_INVALID_ARG;
+    if (!dim_ok(H) || E > 512 || k > 32 || T * (int64_t)k >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+    if (T == 0) return MOE_OK;
+    if (!x || !gate_w || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+    if (!ws || ws_bytes < route_need(T, H, E)) return MOE_ERR_WORKSPACE;
+    const int sms = device_sms();
+    RouterLaunch L;
+    L.x = x;
+    L.Wg = gate_w;
+    L.bias = logit_bias;
+    L.T = T;
+    L.H = H;
+    L.E = E;
+    L.k = k;
+    L.renorm = renorm ? 1 : 0;
+    L.ids = topk_ids;
+    L.w = topk_w;
+    L.hdr = static_cast<WsHeader*>(ws);
+    router_carve(static_cast<char*>(ws) + kWsHeaderBytes, T, E, &L.part, &L.xsq, &L.wsq);
+    router_plan(T, H, E, sms, &L.nsplit, &L.KC);
+    return cuda_status(launch_router(L, sms, (cudaStream_t)stream));
+}
+
+moe_status_t moe_permute(const int32_t* topk_ids, float* topk_w, int64_t T, int k, int E, const int32_t* rep_offset,
+                         const int32_t* rep_slots, int S, int local_start, int local_count, int nonlocal_mode,
+                         const moe_bf16_t* x, int H, int32_t* slot_ids, int32_t* counts, int32_t* offsets,
+                         int32_t* perm_src, int32_t* pair_row, moe_bf16_t* x_perm, void* ws, size_t ws_bytes,
+                         moe_stream_t stream) {
+    if (T < 0 || k <= 0 || E <= 0 || S <= 0 || H <= 0) return MOE_ERR_INVALID_ARG;
+    if (!rep_offset && S != E) return MOE_ERR_INVALID_ARG;
+    if (rep_offset && !rep_slots) return MOE_ERR_INVALID_ARG;
+    if (nonlocal_mode != MOE_NONLOCAL_SKIP && nonlocal_mode != MOE_NONLOCAL_MOD) return MOE_ERR_INVALID_ARG;
+    if (local_count != -1 && (local_count < 1 || local_start < 0 || (int64_t)local_start + local_count > S))
+        return MOE_ERR_INVALID_ARG;
+    const int S_local = local_count >= 0 ? local_count : S;
+    if (!dim_ok(H) || k > 32 || S_local > 1024 || T * (int64_t)k >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+    if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (T == 0) {
+        // an empty batch still has well-defined counts and offsets (all zero)
+        cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * (size_t)S_local, s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (size_t)(S_local + 1), s);
+        return cuda_status(e);
+    }
+    if (!topk_ids || !topk_w || !x || !slot_ids || !perm_src || !pair_row || !x_perm) return MOE_ERR_INVALID_ARG;
+    const int64_t P = T * k;
+    if (!ws || ws_bytes < permute_need(P, S_local)) return MOE_ERR_WORKSPACE;
+    PermuteLaunch L;
+    L.ids = topk_ids;
+    L.w = topk_w;
+    L.T = T;
+    L.k = k;
+    L.E = E;
+    L.rep_offset = rep_offset;
+    L.rep_slots = rep_slots;
+    L.S = S;
+    L.local_start = local_start;
+    L.local_count = local_count;
+    L.mode = nonlocal_mode;
+    L.S_local = S_local;
+    L.x = x;
+    L.H = H;
+    L.slot_ids = slot_ids;
+    L.counts = counts;
+    L.offsets = offsets;
+    L.perm_src = perm_src;
+    L.pair_row = pair_row;
+    L.x_perm = x_perm;
+    L.hdr = static_cast<WsHeader*>(ws);
+    permute_carve(static_cast<char*>(ws) + kWsHeaderBytes, P, S_local, &L.chunk_cnt, &L.chunk_base);
+    return cuda_status(launch_permute(L, device_sms(), s));
+}
+
+static moe_status_t gemm_call(bool fc1, const moe_bf16_t* a, int64_t rows_cap, const int32_t* offsets, int G,
+                              const moe_bf16_t* W, int H, int I, const moe_bf16_t* a_sh, int64_t T,
+                              const moe_bf16_t* Ws, int I_sh, moe_bf16_t* out, moe_bf16_t* out_sh, void* ws,
+                              cudaStream_t s) {
+    GemmLaunch L;
+    L.swiglu = fc1;
+    L.a = a;
+    L.rows_cap = rows_cap;
+    L.offsets = offsets;
+    L.G = G;
+    L.b = W;
+    L.K = fc1 ? H : I;
+    L.Nb = fc1 ? 2 * I : H;
+    L.N_out = fc1 ? I : H;
+    L.out = out;
+    L.a_sh = a_sh;
+    L.T_sh = I_sh > 0 ? T : 0;
+    L.b_sh = Ws;
+    L.K_sh = fc1 ? H : I_sh;
+    L.Nb_sh = fc1 ? 2 * I_sh : H;
+    L.N_out_sh = fc1 ? I_sh : H;
+    L.out_sh = out_sh;
+    L.hdr = static_cast<WsHeader*>(ws);
+    L.timeout_ns = g_timeout_ns.load();
+    const char* why = nullptr;
+    return cuda_status(launch_grouped_gemm(L, device_sms(), s, &why));
+}
+
+static moe_status_t check_gemm_args(const moe_bf16_t* a, int64_t rows_cap, const int32_t* offsets, int G,
+                                    const moe_bf16_t* W, int H, int I, const moe_bf16_t* a_sh, int64_t T,
+                                    const moe_bf16_t* Ws, int I_sh, const moe_bf16_t* out,
+                                    const moe_bf16_t* out_sh, void* ws, size_t ws_bytes) {
+    if (rows_cap < 0 || G < 0 || H <= 0 || I <= 0 || T < 0 || I_sh < 0) return MOE_ERR_INVALID_ARG;
+    if (!dim_ok(H) || !dim_ok(I) || (I_sh > 0 && !dim_ok(I_sh)) || G > 1024 || rows_cap >= (int64_t(1) << 31) ||
+        T >= (int64_t(1) << 31))
+        return MOE_ERR_UNSUPPORTED;
+    if (G > 0 && rows_cap > 0 && (!a || !offsets || !W || !out)) return MOE_ERR_INVALID_ARG;
+    if (I_sh > 0 && T > 0 && (!a_sh || !Ws || !out_sh)) return MOE_ERR_INVALID_ARG;
+    if (!ws || ws_bytes < kWsHeaderBytes) return MOE_ERR_WORKSPACE;
+    return MOE_OK;
+}
+
+moe_status_t moe_grouped_fc1(const moe_bf16_t* a, int64_t rows_cap, const int32_t* offsets, int G,
+                             const moe_bf16_t* W1, int H, int I, const moe_bf16_t* a_shared, int64_t T,
+                             const moe_bf16_t* W1s, int I_shared_total, moe_bf16_t* h, moe_bf16_t* h_shared,
+                             void* ws, size_t ws_bytes, moe_stream_t stream) {
+    moe_status_t st = check_gemm_args(a, rows_cap, offsets, G, W1, H, I, a_shared, T, W1s, I_shared_total, h,
+                                      h_shared, ws, ws_bytes);
+    if (st != MOE_OK) return st;
+    return gemm_call(true, a, rows_cap, offsets, G, W1, H, I, a_shared, T, W1s, I_shared_total, h, h_shared, ws,
+                     (cudaStream_t)stream);
+}
+
+moe_status_t moe_grouped_fc2(const moe_bf16_t* h, int64_t rows_cap, const int32_t* offsets, int G,
+                             const moe_bf16_t* W2, int H, int I, const moe_bf16_t* h_shared, int64_t T,
+                             const moe_bf16_t* W2s, int I_shared_total, moe_bf16_t* y, moe_bf16_t* y_shared,
+                             void* ws, size_t ws_bytes, moe_stream_t stream) {
+    moe_status_t st = check_gemm_args(h, rows_cap, offsets, G, W2, H, I, h_shared, T, W2s, I_shared_total, y,
+                                      y_shared, ws, ws_bytes);
+    if (st != MOE_OK) return st;
+    return gemm_call(false, h, rows_cap, offsets, G, W2, H, I, h_shared, T, W2s, I_shared_total, y, y_shared, ws,
+                     (cudaStream_t)stream);
+}
+
+moe_status_t moe_finalize(const moe_bf16_t* y, int64_t rows_cap, const int32_t* pair_row, const float* topk_w,
+                          int64_t T, int k, int H, const moe_bf16_t* y_shared, const moe_bf16_t* x,
+                          const moe_bf16_t* shared_gate_w, moe_bf16_t* out, void* ws, size_t ws_bytes,
+                          moe_stream_t stream) {
+    if (T < 0 || k <= 0 || H <= 0 || rows_cap < 0) return MOE_ERR_INVALID_ARG;
+    if (!dim_ok(H) || k > 32) return MOE_ERR_UNSUPPORTED;
+    if (T == 0) return MOE_OK;
+    if (!pair_row || !topk_w || !out || (rows_cap > 0 && !y)) return MOE_ERR_INVALID_ARG;
+    if (shared_gate_w && (!x || !y_shared)) return MOE_ERR_INVALID_ARG;
+    if (!ws || ws_bytes < kWsHeaderBytes) return MOE_ERR_WORKSPACE;
+    FinalizeLaunch L;
+    L.y = y;
+    L.rows_cap = rows_cap;
+    L.pair_row = pair_row;
+    L.w = topk_w;
+    L.T = T;
+    L.k = k;
+    L.H = H;
+    L.y_sh = y_shared;
+    L.x = x;
+    L.gate_w = shared_gate_w;
+    L.out = out;
+    L.hdr = static_cast<WsHeader*>(ws);
+    return cuda_status(launch_finalize(L, device_sms(), (cudaStream_t)stream));
+}
+
+moe_status_t moe_forward(const moe_bf16_t* x_perm, const int32_t* offsets, int S_local, int64_t P_cap,
+                         const moe_bf16_t* W1, const moe_bf16_t* W2, int H, int I, const int32_t* pair_row,
+                         const float* topk_w, int64_t T, int k, const moe_bf16_t* x, const moe_bf16_t* W1s,
+                         const moe_bf16_t* W2s, int I_shared_total, const moe_bf16_t* shared_gate_w, moe_bf16_t* out,
+                         void* ws, size_t ws_bytes, moe_stream_t stream) {
+    if (T < 0 || k <= 0 || S_local <= 0 || P_cap < 0 || H <= 0 || I <= 0 || I_shared_total < 0)
+        return MOE_ERR_INVALID_ARG;
+    if (!dim_ok(H) || !dim_ok(I) || (I_shared_total > 0 && !dim_ok(I_shared_total)) || k > 32 || S_local > 1024 ||
+        P_cap >= (int64_t(1) << 31))
+        return MOE_ERR_UNSUPPORTED;
+    if (T == 0) return MOE_OK;
+    if (!x_perm || !offsets || !W1 || !W2 || !pair_row || !topk_w || !out) return MOE_ERR_INVALID_ARG;
+    if (I_shared_total > 0 && (!x || !W1s || !W2s)) return MOE_ERR_INVALID_ARG;
+    if (shared_gate_w && (I_shared_total == 0 || !x)) return MOE_ERR_INVALID_ARG;
+    const ForwardLayout FL = forward_layout(P_cap, T, H, I, I_shared_total);
+    if (!ws || ws_bytes < FL.total) return MOE_ERR_WORKSPACE;
+    char* base = static_cast<char*>(ws);
+    moe_bf16_t* h = reinterpret_cast<moe_bf16_t*>(base + FL.h);
+    moe_bf16_t* h_sh = I_shared_total > 0 ? reinterpret_cast<moe_bf16_t*>(base + FL.h_sh) : nullptr;
+    moe_bf16_t* y = reinterpret_cast<moe_bf16_t*>(base + FL.y);
+    moe_bf16_t* y_sh = I_shared_total > 0 ? reinterpret_cast<moe_bf16_t*>(base + FL.y_sh) : nullptr;
+    cudaStream_t s = (cudaStream_t)stream;
+    moe_status_t st = gemm_call(true, x_perm, P_cap, offsets, S_local, W1, H, I, x, T, W1s, I_shared_total, h, h_sh,
+                                ws, s);
+    if (st != MOE_OK) return st;
+    st = gemm_call(false, h, P_cap, offsets, S_local, W2, H, I, h_sh, T, W2s, I_shared_total, y, y_sh, ws, s);
+    if (st != MOE_OK) return st;
+    return moe_finalize(y, P_cap, pair_row, topk_w, T, k, H, y_sh, x, shared_gate_w, out, ws, ws_bytes, stream);
+}
+
+moe_status_t moe_debug_wait_timeout(void* ws, size_t ws_bytes, uint64_t timeout_ns, moe_stream_t stream) {
+    if (!ws || ws_bytes < kWsHeaderBytes) return MOE_ERR_WORKSPACE;
+    if (timeout_ns == 0 || timeout_ns > 10000000000ull) return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_wait_timeout_probe(static_cast<WsHeader*>(ws), timeout_ns, (cudaStream_t)stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,295 @@
+// moe_internal.cuh -- device helpers shared by the kernels of the GB300 MoE
+// layer: status word, bounded waits, mbarrier / TMA / tcgen05 inline PTX.
+// Internal to the library (not installed); the public ABI is include/moe.h.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// Workspace header (first kWsHeaderBytes bytes of every workspace)
+// ---------------------------------------------------------------------------
+constexpr size_t kWsHeaderBytes = 256;
+struct WsHeader {
+    int32_t status;              // OR of MOE_ERR_DEVICE_BOUNDS / MOE_ERR_TIMEOUT
+    int32_t pad0;
+    unsigned long long refined;  // tokens whose top-k needed the fp64 recheck
+};
+
+__device__ __forceinline__ void report(int32_t* status, int32_t code) {
+    if (status) atomicOr(status, code);
+}
+
+// ---------------------------------------------------------------------------
+// bf16 helpers (bit patterns in uint16_t)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
+
+__device__ __forceinline__ void unpack8(const uint4& v, float f[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // round to nearest even
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// ---------------------------------------------------------------------------
+// Time and bounded waits
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar_addr), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait until the phase with the given parity of `bar` has completed.  Gives up
+// (returns false) once `timeout_ns` has passed since the wait began, or as soon
+// as *abort becomes nonzero; never spins without a bound.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns,
+                                          const volatile int* abort) {
+    const uint32_t a = smem_u32(bar);
+    if (mbar_try_wait(a, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    uint32_t polls = 0;
+    while (true) {
+        if (mbar_try_wait(a, parity)) return true;
+        if ((++polls & 255u) == 0u) {
+            if (abort && *abort) return false;
+            if (globaltimer_ns() - t0 > timeout_ns) return false;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// TMA (cp.async.bulk.tensor), no multicast
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
+                                            int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05 (5th-generation tensor cores, accumulators in tensor memory)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulation.
+__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on `bar` when all tcgen05 operations issued so far by this thread complete.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
+// 32 lanes x 32 consecutive 32-bit columns: thread i of the warp gets lane
+// (base lane + i), columns col .. col+31.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor of a K-major bf16 tile written by TMA with
+// 128-byte swizzle: rows of 64 elements (128 B), 8-row groups 1024 B apart.
+// The tile base must be 1024-byte aligned; stepping K by 16 elements inside the
+// 128-byte row advances the start address by 32 bytes.
+__device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);  // start address (16-byte units)
+    d |= (uint64_t)1 << 16;                        // leading byte offset (unused for swizzled K-major)
+    d |= (uint64_t)(1024 >> 4) << 32;              // stride byte offset: next 8-row group
+    d |= (uint64_t)1 << 46;                        // descriptor version
+    d |= (uint64_t)2 << 61;                        // swizzle: 128 B
+    return d;
+}
+
+// Instruction descriptor of tcgen05.mma.kind::f16: bf16 A and B (both
+// K-major), fp32 D, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+    return (1u << 4)                              // D format: f32
+           | (1u << 7)                            // A format: bf16
+           | (1u << 10)                           // B format: bf16
+           | ((uint32_t)(N >> 3) << 17)           // N / 8
+           | ((uint32_t)(M >> 4) << 24);          // M / 16
+}
+
+// ---------------------------------------------------------------------------
+// Internal launchers (defined in the kernel files, called by moe_api.cu)
+// ---------------------------------------------------------------------------
+struct RouterLaunch {
+    const uint16_t* x;
+    const float* Wg;
+    const float* bias;
+    int64_t T;
+    int H, E, k, renorm;
+    int32_t* ids;
+    float* w;
+    float* part;   // [nsplit][T][E]
+    float* xsq;    // [nsplit][T]
+    float* wsq;    // [nsplit][E]
+    int nsplit, KC;
+    WsHeader* hdr;
+};
+size_t router_scratch_bytes(int64_t T, int H, int E, int num_sms);
+void router_carve(void* base, int64_t T, int E, float** part, float** xsq, float** wsq);
+void router_plan(int64_t T, int H, int E, int num_sms, int* nsplit, int* KC);
+cudaError_t launch_router(const RouterLaunch& L, int num_sms, cudaStream_t s);
+
+struct PermuteLaunch {
+    const int32_t* ids;
+    float* w;
+    int64_t T;
+    int k, E;
+    const int32_t* rep_offset;
+    const int32_t* rep_slots;
+    int S, local_start, local_count, mode, S_local;
+    const uint16_t* x;
+    int H;
+    int32_t* slot_ids;
+    int32_t* counts;
+    int32_t* offsets;
+    int32_t* perm_src;
+    int32_t* pair_row;
+    uint16_t* x_perm;
+    int32_t* chunk_cnt;   // [nchunks][S_local]
+    int32_t* chunk_base;  // [nchunks][S_local]
+    WsHeader* hdr;
+};
+size_t permute_scratch_bytes(int64_t P, int S_local);
+void permute_carve(void* base, int64_t P, int S_local, int32_t** chunk_cnt, int32_t** chunk_base);
+cudaError_t launch_permute(const PermuteLaunch& L, int num_sms, cudaStream_t s);
+
+struct GemmLaunch {
+    bool swiglu;               // FC1 (gate/up pairs, SwiGLU epilogue) or FC2
+    const uint16_t* a;         // routed A [rows_cap, K]
+    int64_t rows_cap;
+    const int32_t* offsets;    // [G+1]
+    int G;
+    const uint16_t* b;         // routed B [G, Nb, K]
+    int K, Nb, N_out;          // Nb rows of B per group; N_out output columns
+    uint16_t* out;             // [rows_cap, N_out]
+    const uint16_t* a_sh;      // shared A [T_sh, K_sh] (or null)
+    int64_t T_sh;
+    const uint16_t* b_sh;      // shared B [Nb_sh, K_sh]
+    int K_sh, Nb_sh, N_out_sh;
+    uint16_t* out_sh;          // [T_sh, N_out_sh]
+    WsHeader* hdr;
+    uint64_t timeout_ns;
+};
+cudaError_t launch_grouped_gemm(const GemmLaunch& L, int num_sms, cudaStream_t s, const char** why);
+
+struct FinalizeLaunch {
+    const uint16_t* y;
+    int64_t rows_cap;
+    const int32_t* pair_row;
+    const float* w;
+    int64_t T;
+    int k, H;
+    const uint16_t* y_sh;
+    const uint16_t* x;
+    const uint16_t* gate_w;
+    uint16_t* out;
+    WsHeader* hdr;
+};
+cudaError_t launch_finalize(const FinalizeLaunch& L, int num_sms, cudaStream_t s);
+
+cudaError_t launch_wait_timeout_probe(WsHeader* hdr, uint64_t timeout_ns, cudaStream_t s);
+
+}  // namespace moe

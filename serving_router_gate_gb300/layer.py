@@ -1,0 +1,110 @@
+"""One MoE layer on one GPU: buffers for up to max_T tokens and the three
+stream-ordered library calls (moe_route -> moe_permute -> moe_forward).
+
+Weights are handed over per expert slot, as the fused op of the TensorRT-LLM
+redundant-expert refactor (PR #4495) computes on slots: W1 [S_local, 2I, H]
+(gate rows then up rows), W2 [S_local, H, I].  With a local expert range only
+the local slots' weights are passed (the vLLM EP weight loader keeps only the
+local experts).  All tensors live on the current CUDA device; nothing is
+allocated per call and no call synchronises the host.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import (MOE_NONLOCAL_SKIP, moe_forward, moe_permute, moe_route, moe_workspace_init,
+               moe_workspace_size)
+
+
+class MoELayer:
+    def __init__(self, Wg: torch.Tensor, W1: torch.Tensor, W2: torch.Tensor, k: int, renorm: bool,
+                 max_T: int, logit_bias: Optional[torch.Tensor] = None,
+                 rep_offset: Optional[torch.Tensor] = None, rep_slots: Optional[torch.Tensor] = None,
+                 S: Optional[int] = None, local_start: int = 0, local_count: int = -1,
+                 nonlocal_mode: int = MOE_NONLOCAL_SKIP, W1s: Optional[torch.Tensor] = None,
+                 W2s: Optional[torch.Tensor] = None, shared_gate_w: Optional[torch.Tensor] = None):
+        self.Wg, self.W1, self.W2 = Wg, W1, W2
+        self.E, self.H = Wg.shape
+        self.I = W2.shape[2]
+        self.k, self.renorm = int(k), bool(renorm)
+        self.bias = logit_bias
+        self.rep_offset, self.rep_slots = rep_offset, rep_slots
+        self.S = int(S if S is not None else (self.E if rep_offset is None else rep_slots.shape[0]))
+        self.local_start, self.local_count, self.mode = int(local_start), int(local_count), int(nonlocal_mode)
+        self.S_local = self.local_count if self.local_count >= 0 else self.S
+        assert W1.shape == (self.S_local, 2 * self.I, self.H), W1.shape
+        self.W1s, self.W2s, self.gate = W1s, W2s, shared_gate_w
+        self.I_sh = 0 if W2s is None else W2s.shape[1]
+        self.max_T = int(max_T)
+        dev = Wg.device
+        T, k, H = self.max_T, self.k, self.H
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.topk_ids = torch.empty((T, k), **i32)
+        self.topk_w = torch.empty((T, k), dtype=torch.float32, device=dev)
+        self.slot_ids = torch.empty((T, k), **i32)
+        self.counts = torch.empty((self.S_local,), **i32)
+        self.offsets = torch.empty((self.S_local + 1,), **i32)
+        self.perm_src = torch.empty((T * k,), **i32)
+        self.pair_row = torch.empty((T, k), **i32)
+        self.x_perm = torch.empty((T * k, H), dtype=torch.bfloat16, device=dev)
+        self.out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        nbytes = moe_workspace_size(T, H, self.I, self.E, max(self.S, self.S_local), k, self.I_sh)
+        self.ws = torch.empty((nbytes,), dtype=torch.uint8, device=dev)
+        moe_workspace_init(self.ws)
+
+    def views(self, T: int) -> dict:
+        k = self.k
+        return dict(topk_ids=self.topk_ids[:T], topk_w=self.topk_w[:T], slot_ids=self.slot_ids[:T],
+                    counts=self.counts, offsets=self.offsets, perm_src=self.perm_src[:T * k],
+                    pair_row=self.pair_row[:T], x_perm=self.x_perm[:T * k], out=self.out[:T])
+
+    def route(self, x: torch.Tensor, stream=None) -> dict:
+        v = self.views(x.shape[0])
+        moe_route(x, self.Wg, self.bias, self.k, self.renorm, v["topk_ids"], v["topk_w"], self.ws, stream)
+        return v
+
+    def permute(self, x: torch.Tensor, stream=None) -> dict:
+        v = self.views(x.shape[0])
+        moe_permute(v["topk_ids"], v["topk_w"], self.E, self.rep_offset, self.rep_slots, self.S,
+                    self.local_start, self.local_count, self.mode, x, v["slot_ids"], v["counts"], v["offsets"],
+                    v["perm_src"], v["pair_row"], v["x_perm"], self.ws, stream)
+        return v
+
+    def expert_forward(self, x: torch.Tensor, stream=None) -> dict:
+        v = self.views(x.shape[0])
+        moe_forward(v["x_perm"], v["offsets"], self.W1, self.W2, v["pair_row"], v["topk_w"],
+                    x if (self.I_sh > 0) else None, self.W1s, self.W2s, self.gate, v["out"], self.ws, stream)
+        return v
+
+    def forward(self, x: torch.Tensor, stream=None) -> torch.Tensor:
+        """out [T, H] bf16 (a view of the layer's output buffer) for x [T, H] bf16, T <= max_T."""
+        assert x.shape[0] <= self.max_T and x.shape[1] == self.H
+        if x.shape[0] == 0:
+            return self.out[:0]
+        self.route(x, stream)
+        self.permute(x, stream)
+        return self.expert_forward(x, stream)["out"]
+
+
+def layer_from_inputs(inp: dict, device="cuda", max_T: Optional[int] = None, local_start: int = 0,
+                      local_count: int = -1, nonlocal_mode: int = MOE_NONLOCAL_SKIP) -> MoELayer:
+    """A MoELayer over the tensors of moe_inputs.make_inputs() (moved to `device`)."""
+    from moe_inputs import shared_concat
+    cfg = inp["cfg"]
+
+    def d(t):
+        return None if t is None else t.to(device).contiguous()
+
+    W1, W2 = inp["W1"], inp["W2"]
+    if local_count >= 0:
+        W1 = W1[local_start:local_start + local_count]
+        W2 = W2[local_start:local_start + local_count]
+    W1s = W2s = None
+    if inp["W1s"] is not None:
+        W1s, W2s = shared_concat(inp["W1s"], inp["W2s"])
+    return MoELayer(d(inp["Wg"]), d(W1), d(W2), cfg.k, cfg.renorm, max_T or cfg.T, logit_bias=d(inp["bias"]),
+                    rep_offset=d(inp["rep_offset"]), rep_slots=d(inp["rep_slots"]), S=cfg.slots,
+                    local_start=local_start, local_count=local_count, nonlocal_mode=nonlocal_mode,
+                    W1s=d(W1s), W2s=d(W2s), shared_gate_w=d(inp["w_s"]))

@@ -1,0 +1,130 @@
+"""Host-only checks of the C ABI: the library loads, exports every function
+include/moe.h declares, sizes workspaces, and rejects bad arguments on the host
+before any kernel launch (every case here fails validation, so no pointer is
+ever dereferenced and no CUDA call is reached)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import serving_router_gate_gb300 as moe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"^MOE_API[^(]*?\b(moe_[a-z0-9_]+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_three_calls():
+    names = _declared()
+    for n in ("moe_route", "moe_permute", "moe_forward", "moe_workspace_size", "moe_get_device_status"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(moe.lib_path())
+    for name in _declared():
+        assert hasattr(lib, name), name
+    assert sorted(moe.EXPORTED_SYMBOLS) == _declared()
+
+
+def test_status_strings():
+    for code in (0, 1, 2, 3, 4, 8, 16):
+        assert moe._lib.moe_status_string(code)
+
+
+def test_workspace_size():
+    n2 = moe.moe_workspace_size(4096, 2048, 1408, 60, 60, 4, 5632)
+    # at least h and y of every pair plus the shared expert's h and y
+    assert n2 >= 2 * (4096 * 4 * (1408 + 2048) + 4096 * (5632 + 2048))
+    n5 = moe.moe_workspace_size(16384, 7168, 2048, 256, 288, 8, 0)
+    assert n5 >= 2 * 16384 * 8 * (2048 + 7168)
+    assert moe.moe_workspace_size(1, 2048, 1408, 64, 64, 6, 5632) > 0
+    assert moe.moe_workspace_size(0, 256, 512, 8, 8, 2, 0) > 0
+    for bad in ((64, 100, 512, 8, 8, 2, 0),      # H not a multiple of 64
+                (64, 256, 500, 8, 8, 2, 0),      # I not a multiple of 64
+                (64, 256, 512, 8, 8, 9, 0),      # k > E
+                (64, 256, 512, 600, 600, 2, 0),  # E > 512
+                (64, 256, 512, 8, 2000, 2, 0),   # S > 1024
+                (-1, 256, 512, 8, 8, 2, 0)):
+        assert moe._lib.moe_workspace_size(*bad) == 0
+
+
+FAKE = ctypes.c_void_p(0x1000)  # never dereferenced: every call below fails host validation first
+
+
+def test_route_rejects_bad_arguments_on_host():
+    r = moe._lib.moe_route
+    assert r(FAKE, FAKE, None, 16, 256, 8, 9, 1, FAKE, FAKE, FAKE, 1 << 30, None) == moe.MOE_ERR_INVALID_ARG
+    assert r(FAKE, FAKE, None, -1, 256, 8, 2, 1, FAKE, FAKE, FAKE, 1 << 30, None) == moe.MOE_ERR_INVALID_ARG
+    assert r(FAKE, FAKE, None, 16, 100, 8, 2, 1, FAKE, FAKE, FAKE, 1 << 30, None) == moe.MOE_ERR_UNSUPPORTED
+    assert r(FAKE, FAKE, None, 16, 256, 600, 2, 1, FAKE, FAKE, FAKE, 1 << 30, None) == moe.MOE_ERR_UNSUPPORTED
+    assert r(None, FAKE, None, 16, 256, 8, 2, 1, FAKE, FAKE, FAKE, 1 << 30, None) == moe.MOE_ERR_INVALID_ARG
+    assert r(FAKE, FAKE, None, 16, 256, 8, 2, 1, FAKE, FAKE, None, 1 << 30, None) == moe.MOE_ERR_WORKSPACE
+    assert r(FAKE, FAKE, None, 16, 256, 8, 2, 1, FAKE, FAKE, FAKE, 64, None) == moe.MOE_ERR_WORKSPACE
+    assert r(None, None, None, 0, 256, 8, 2, 1, None, None, None, 0, None) == moe.MOE_OK  # T = 0: no-op
+
+
+def test_permute_rejects_bad_arguments_on_host():
+    p = moe._lib.moe_permute
+
+    def call(T=16, k=2, E=8, ro=None, rs=None, S=8, ls=0, lc=-1, mode=0, H=256, ws=FAKE, wsb=1 << 30, ids=FAKE):
+        return p(ids, FAKE, T, k, E, ro, rs, S, ls, lc, mode, FAKE, H, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                 ws, wsb, None)
+
+    assert call(S=9) == moe.MOE_ERR_INVALID_ARG                    # no table but S != E
+    assert call(ro=FAKE, rs=None, S=9) == moe.MOE_ERR_INVALID_ARG  # table without slots
+    assert call(mode=2) == moe.MOE_ERR_INVALID_ARG
+    assert call(ls=6, lc=4) == moe.MOE_ERR_INVALID_ARG             # range past S
+    assert call(ls=-1, lc=4) == moe.MOE_ERR_INVALID_ARG
+    assert call(lc=0) == moe.MOE_ERR_INVALID_ARG
+    assert call(H=96) == moe.MOE_ERR_UNSUPPORTED
+    assert call(k=33, E=64, S=64) == moe.MOE_ERR_UNSUPPORTED
+    assert call(ids=None) == moe.MOE_ERR_INVALID_ARG
+    assert call(ws=None) == moe.MOE_ERR_WORKSPACE
+    assert call(wsb=300) == moe.MOE_ERR_WORKSPACE
+
+
+def test_forward_and_stages_reject_bad_arguments_on_host():
+    f = moe._lib.moe_forward
+
+    def call(S_local=8, P_cap=32, H=256, I=512, T=16, k=2, x=FAKE, W1s=None, W2s=None, I_sh=0, gate=None,
+             ws=FAKE, wsb=1 << 30, out=FAKE):
+        return f(FAKE, FAKE, S_local, P_cap, FAKE, FAKE, H, I, FAKE, FAKE, T, k, x, W1s, W2s, I_sh, gate, out,
+                 ws, wsb, None)
+
+    assert call(S_local=0) == moe.MOE_ERR_INVALID_ARG
+    assert call(I=100) == moe.MOE_ERR_UNSUPPORTED
+    assert call(I_sh=256) == moe.MOE_ERR_INVALID_ARG         # shared size without shared weights
+    assert call(gate=FAKE) == moe.MOE_ERR_INVALID_ARG        # gate without a shared expert
+    assert call(out=None) == moe.MOE_ERR_INVALID_ARG
+    assert call(ws=None) == moe.MOE_ERR_WORKSPACE
+    assert call(wsb=1000) == moe.MOE_ERR_WORKSPACE
+    assert call(T=0) == moe.MOE_OK
+    fc1 = moe._lib.moe_grouped_fc1
+    assert fc1(FAKE, 32, FAKE, 2000, FAKE, 256, 512, None, 0, None, 0, FAKE, None, FAKE, 1 << 20,
+               None) == moe.MOE_ERR_UNSUPPORTED
+    assert fc1(FAKE, 32, None, 4, FAKE, 256, 512, None, 0, None, 0, FAKE, None, FAKE, 1 << 20,
+               None) == moe.MOE_ERR_INVALID_ARG
+    assert fc1(FAKE, 32, FAKE, 4, FAKE, 256, 512, None, 0, None, 0, FAKE, None, None, 0,
+               None) == moe.MOE_ERR_WORKSPACE
+    fin = moe._lib.moe_finalize
+    assert fin(FAKE, 32, FAKE, FAKE, 16, 2, 256, None, None, FAKE, FAKE, FAKE, 1 << 20,
+               None) == moe.MOE_ERR_INVALID_ARG  # gate without x / y_shared
+    assert fin(FAKE, 32, FAKE, FAKE, 16, 40, 256, None, None, None, FAKE, FAKE, 1 << 20,
+               None) == moe.MOE_ERR_UNSUPPORTED
+    dbg = moe._lib.moe_debug_wait_timeout
+    assert dbg(FAKE, 1 << 20, 0, None) == moe.MOE_ERR_INVALID_ARG
+    assert dbg(None, 0, 1000, None) == moe.MOE_ERR_WORKSPACE
+
+
+def test_binding_rejects_cpu_tensors():
+    import torch
+    x = torch.zeros(4, 256, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        moe.moe_route(x, torch.zeros(8, 256), None, 2, True, torch.zeros(4, 2, dtype=torch.int32),
+                      torch.zeros(4, 2), torch.zeros(1 << 20, dtype=torch.uint8))

@@ -1,0 +1,248 @@
+"""GPU parity of the CUDA layer against the fp64 oracle, through the C ABI.
+
+Small and mid-size workloads are compared in full (several M/N/K tiles, ragged
+per-slot tails, partial N tiles); the full-size workloads compare routing and
+permutation bit-exactly on every token and the layer output on sampled tokens.
+Tolerances: see tests/parity_util.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as mi
+import oracle
+import serving_router_gate_gb300 as moe
+from serving_router_gate_gb300.layer import layer_from_inputs
+
+from parity_util import (check_out, check_routing, check_x_perm, make, oracle_layer, oracle_routing,
+                         oracle_threads, run_gpu, sample_tokens, to_cpu)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True, scope="module")
+def _threads():
+    oracle_threads()
+
+
+def _full_check(inp, local_start=0, local_count=-1, mode=0):
+    g = run_gpu(inp, local_start, local_count, mode)
+    ref = oracle_layer(to_cpu(inp), local_start, local_count, mode)
+    check_routing(g, dict(ids=ref["ids"], w=ref["w"], w_masked=ref["w_masked"], slots=ref["slots"],
+                          counts=ref["counts"], offsets=ref["offsets"], perm_src=ref["perm_src"],
+                          pair_row=ref["pair_row"]), to_cpu(inp), masked=local_count >= 0)
+    check_x_perm(g, inp["x"].cuda(), inp["cfg"].k)
+    check_out(g["out"], ref["out"])
+    st = moe.moe_get_device_status(g["layer"].ws)
+    assert st == 0, f"device status {st}"
+    return g, ref
+
+
+# --------------------------------------------------------------------------- small / mid sizes, full compare
+
+@pytest.mark.parametrize("renorm", [True, False])
+def test_tiny_layer(renorm):
+    _full_check(make("tiny", renorm=renorm))
+
+
+MID = mi.MoEConfig("mid", T=1000, H=512, I=384, E=12, k=3, renorm=True, n_shared=1, I_shared=256,
+                   shared_gate=True)
+
+
+def test_mid_layer_with_gated_shared_expert():
+    _full_check(mi.make_inputs(MID))
+
+
+def test_partial_n_tiles_and_two_shared_experts():
+    cfg = mi.MoEConfig("odd", T=200, H=320, I=320, E=5, k=2, renorm=False, n_shared=2, I_shared=192)
+    _full_check(mi.make_inputs(cfg))
+
+
+def test_replica_slots_with_zipf_bias():
+    cfg = mi.MoEConfig("rep", T=700, H=256, I=256, E=10, S=13, n_hot=3, zipf_s=1.1, k=4, renorm=True)
+    _full_check(mi.make_inputs(cfg))
+
+
+def test_local_ranges_sum_to_full_and_mod_equals_skip():
+    cfg = mi.MoEConfig("ranges", T=600, H=256, I=256, E=16, k=4, renorm=True)
+    inp = mi.make_inputs(cfg)
+    full, _ = _full_check(inp)
+    acc = torch.zeros(cfg.T, cfg.H, dtype=torch.float64)
+    for start in (0, 4, 8, 12):
+        g_skip, ref = _full_check(inp, start, 4, moe.MOE_NONLOCAL_SKIP)
+        g_mod, _ = _full_check(inp, start, 4, moe.MOE_NONLOCAL_MOD)
+        # MOD computes the non-local pairs with weight 0: bitwise the same output
+        assert torch.equal(g_skip["out"].view(torch.int16), g_mod["out"].view(torch.int16))
+        assert int(g_mod["counts"].sum()) == cfg.T * cfg.k
+        acc += g_skip["out"].double()
+    check_out(acc.to(torch.bfloat16), full["out"].double().numpy(), "sum of local ranges")
+
+
+def test_all_experts_selected_and_single_expert():
+    _full_check(mi.make_inputs(mi.MoEConfig("kE", T=130, H=256, I=256, E=8, k=8, renorm=True)))
+    _full_check(mi.make_inputs(mi.MoEConfig("k1", T=130, H=256, I=256, E=8, k=1, renorm=True)))
+
+
+def test_one_hot_expert_gets_every_token():
+    cfg = mi.MoEConfig("hot", T=900, H=256, I=256, E=8, k=2, renorm=False)
+    inp = mi.make_inputs(cfg)
+    inp["bias"] = torch.zeros(cfg.E)
+    inp["bias"][5] = 50.0  # every token picks expert 5 first: one group of 900 rows (8 m-tiles)
+    g, ref = _full_check(inp)
+    assert int(g["counts"][5]) == cfg.T
+
+
+def test_local_range_without_pairs_gives_zero():
+    cfg = mi.MoEConfig("empty", T=64, H=256, I=256, E=8, k=2, renorm=True)
+    inp = mi.make_inputs(cfg)
+    inp["bias"] = torch.zeros(cfg.E)
+    inp["bias"][:4] = 60.0  # experts 4..7 are never chosen
+    g, _ = _full_check(inp, 4, 4, moe.MOE_NONLOCAL_SKIP)
+    assert g["rows"] == 0
+    assert torch.count_nonzero(g["out"].float()) == 0
+
+
+def test_zero_tokens_is_a_noop():
+    inp = make("tiny")
+    layer = layer_from_inputs(inp, "cuda")
+    out = layer.forward(inp["x"][:0].cuda())
+    assert out.shape == (0, 256)
+    torch.cuda.synchronize()
+
+
+def test_two_runs_are_bitwise_identical():
+    inp = mi.make_inputs(MID)
+    layer = layer_from_inputs(inp, "cuda")
+    x = inp["x"].cuda()
+    a = layer.forward(x).clone()
+    b = layer.forward(x).clone()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_replica_table_equals_identity_map():
+    cfg = mi.MoEConfig("rep2", T=500, H=256, I=256, E=10, S=13, n_hot=3, k=3, renorm=True)
+    inp = mi.make_inputs(cfg)
+    g_rep = run_gpu(inp)
+    ident = dict(inp)
+    W1e = torch.empty((cfg.E,) + tuple(inp["W1"].shape[1:]), dtype=torch.bfloat16)
+    W2e = torch.empty((cfg.E,) + tuple(inp["W2"].shape[1:]), dtype=torch.bfloat16)
+    for s, e in enumerate(inp["expert_of_slot"].tolist()):
+        W1e[e], W2e[e] = inp["W1"][s], inp["W2"][s]
+    ident.update(W1=W1e, W2=W2e, rep_offset=None, rep_slots=None, cfg=cfg.with_(S=None, n_hot=0))
+    g_id = run_gpu(ident)
+    assert torch.equal(g_rep["topk_ids"], g_id["topk_ids"])
+    np.testing.assert_allclose(g_rep["out"].float().numpy(), g_id["out"].float().numpy(), rtol=0, atol=2e-3)
+
+
+# --------------------------------------------------------------------------- stages on their own
+
+def test_stages_fc1_fc2_finalize_against_oracle_rows():
+    cfg = MID
+    inp = mi.make_inputs(cfg)
+    g = run_gpu(inp)
+    layer = g["layer"]
+    rows = g["rows"]
+    ref = oracle_layer(to_cpu(inp))
+    dev = torch.device("cuda")
+    h = torch.empty((cfg.T * cfg.k, cfg.I), dtype=torch.bfloat16, device=dev)
+    y = torch.empty((cfg.T * cfg.k, cfg.H), dtype=torch.bfloat16, device=dev)
+    moe.moe_grouped_fc1(layer.x_perm, layer.offsets, layer.W1, None, None, h, None, layer.ws)
+    moe.moe_grouped_fc2(h, layer.offsets, layer.W2, None, None, y, None, layer.ws)
+    torch.cuda.synchronize()
+    # a sample of rows: h and y of row r equal the oracle's expert MLP of its (token, slot)
+    perm = g["perm_src"].numpy()
+    slots = ref["slots"].reshape(-1)
+    xs = inp["x"]
+    for r in sample_tokens(rows, 24, seed=1):
+        p = int(perm[r])
+        t, s = p // cfg.k, int(slots[p])
+        y_ref, h_ref = oracle.expert_mlp(xs[t], inp["W1"][s], inp["W2"][s])
+        h_ref_f = torch.from_numpy(h_ref.view(np.int16)).view(torch.bfloat16).double().numpy()
+        hg = h[r].double().cpu().numpy()
+        assert np.abs(hg - h_ref_f).max() <= 2.0 ** -7 * np.abs(h_ref_f).max() + 1e-6
+        check_out(y[r:r + 1], y_ref[None, :], f"y row {r}")
+    # finalize alone on the oracle-free GPU y reproduces moe_forward's output bitwise
+    out = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=dev)
+    W1s, W2s = mi.shared_concat(inp["W1s"], inp["W2s"])
+    h_sh = torch.empty((cfg.T, cfg.I_shared), dtype=torch.bfloat16, device=dev)
+    y_sh = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=dev)
+    x = xs.cuda()
+    moe.moe_grouped_fc1(layer.x_perm, layer.offsets, layer.W1, x, W1s.cuda(), h, h_sh, layer.ws)
+    moe.moe_grouped_fc2(h, layer.offsets, layer.W2, h_sh, W2s.cuda(), y, y_sh, layer.ws)
+    moe.moe_finalize(y, layer.pair_row, layer.topk_w, y_sh, x, inp["w_s"].cuda(), out, layer.ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), layer.out.view(torch.int16))
+    check_out(out, ref["out"])
+
+
+# --------------------------------------------------------------------------- device-side error paths
+
+def test_out_of_range_expert_ids_are_dropped_and_flagged():
+    inp = make("tiny")
+    layer = layer_from_inputs(inp, "cuda")
+    x = inp["x"].cuda()
+    layer.route(x)
+    layer.topk_ids[3, 1] = 1000   # caught by the permute kernel's bounds check
+    layer.topk_ids[7, 0] = -5
+    layer.permute(x)
+    layer.expert_forward(x)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status(layer.ws) & moe.MOE_ERR_DEVICE_BOUNDS
+    assert int(layer.pair_row[3, 1]) == -1 and int(layer.pair_row[7, 0]) == -1
+    assert int(layer.counts.sum()) == 64 * 2 - 2
+    assert moe.moe_get_device_status(layer.ws) == 0  # reading clears the word
+
+
+def test_bounded_wait_times_out_with_status():
+    ws = torch.zeros(1 << 12, dtype=torch.uint8, device="cuda")
+    moe.moe_workspace_init(ws)
+    moe.moe_debug_wait_timeout(ws, 2_000_000)  # 2 ms; nothing ever arrives
+    assert moe.moe_get_device_status(ws) == moe.MOE_ERR_TIMEOUT
+    # the context is still usable
+    a = torch.ones(4, device="cuda")
+    assert float((a + a).sum()) == 8.0
+
+
+# --------------------------------------------------------------------------- full-size workloads
+
+@pytest.mark.parametrize("T", [1, 8, 32, 128])
+def test_decode_workload_full(T):
+    _full_check(make(f"dsv2_lite_like_decode_t{T}"))
+
+
+def _full_size(name, n_samples, local_ranges=None):
+    cfg = mi.CONFIGS[name]
+    inp = mi.make_inputs(cfg, device="cpu", weights_device="cuda")
+    inp_cpu = to_cpu(inp)
+    g = run_gpu(inp)
+    ref = oracle_routing(inp_cpu)
+    check_routing(g, ref, inp_cpu, masked=False)
+    check_x_perm(g, inp["x"].cuda(), cfg.k)
+    tok = sample_tokens(cfg.T, n_samples)
+    part = oracle_layer(inp_cpu, tokens=tok)
+    check_out(g["out"][tok], part["out"])
+    assert moe.moe_get_device_status(g["layer"].ws) == 0
+    if local_ranges:
+        acc = torch.zeros(cfg.T, cfg.H, dtype=torch.float64)
+        for start, count in local_ranges:
+            gl = run_gpu(inp, start, count, moe.MOE_NONLOCAL_SKIP)
+            refl = oracle_routing(inp_cpu, start, count, moe.MOE_NONLOCAL_SKIP)
+            check_routing(gl, refl, inp_cpu, masked=True)
+            pl = oracle_layer(inp_cpu, start, count, moe.MOE_NONLOCAL_SKIP, tokens=tok[:8])
+            check_out(gl["out"][tok[:8]], pl["out"], f"local range {start}")
+            acc += gl["out"].double()
+            del gl
+        check_out(acc.to(torch.bfloat16), g["out"].double().numpy(), "sum of local ranges")
+    return g
+
+
+def test_qwen2_moe_like_prefill_full_size():
+    _full_size("qwen2_moe_like_prefill", 48)
+
+
+def test_large_expert_prefill_full_size_and_local_ranges():
+    _full_size("large_expert_prefill", 16, local_ranges=[(0, 64), (64, 64), (128, 64), (192, 64)])
+
+
+def test_redundant_slots_prefill_full_size():
+    _full_size("redundant_slots_prefill", 16)
