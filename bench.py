@@ -40,7 +40,10 @@ DEFAULT_WORKLOAD = "qwen2_moe_like_prefill"
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant kernel,
 # from one ncu capture (profiles/), valid only while the kernel source hashes to
 # the recorded value.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # profiles/grouped_gemm_qwen2_moe_like_prefill.md: 822.35 MB read + 87.58 MB written
+    ("qwen2_moe_like_prefill", "8066cc6a28812a00"): 909.93e6,
+}
 
 
 def _src_hash(path):
@@ -74,7 +77,7 @@ class ClockSampler:
             os.close(fd)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                          "-lms", "200", "-i", str(self.dev)], stdout=self.f,
+                                          "-lms", "50", "-i", str(self.dev)], stdout=self.f,
                                          stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -365,8 +368,8 @@ def bench_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(mi.CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
