@@ -130,6 +130,30 @@ MOE_API moe_status_t moe_route(const moe_bf16_t *x, const float *gate_w, const f
                        int32_t *topk_ids, float *topk_w,
                        void *ws, size_t ws_bytes, moe_stream_t stream);
 
+/* moe_route_noalloc -- moe_route without a workspace.  The source pages have
+ * no counterpart of this call; it exists for callers that cannot allocate
+ * device memory at all: a plugin that its host framework hands only input and
+ * output buffers, a runtime whose device memory belongs to a pool this library
+ * cannot reach, or a service that forbids device allocation once it is
+ * running.  Same arguments, kernels and results as moe_route (the same ids;
+ * weights within the same certified fp32 bound), minus the workspace.
+ *
+ * Its scratch is a 16 MiB array in this library's own device memory
+ * (file-scope __device__ storage, held by every GPU that loads the library
+ * until the process exits).  Limit: nsplit*T*E + nsplit*T + nsplit*E fp32
+ * values (each part rounded up to 256 bytes) must fit in 16 MiB for the
+ * smallest split nsplit = 1, i.e. roughly T*(E+1) <= 4.19 million; larger
+ * calls return MOE_ERR_UNSUPPORTED before any launch.  The call allocates
+ * nothing (no cudaMalloc, no allocating library routine).  The first call on
+ * each device looks up the array's device address (cudaGetSymbolAddress), so
+ * make that first call before any stream capture.  Every call reuses the same
+ * array: calls that overlap on the GPU (on two streams) race; calls ordered on
+ * one stream do not.  The refined-token counter of moe_get_route_stats is not
+ * kept by this call. */
+MOE_API moe_status_t moe_route_noalloc(const moe_bf16_t *x, const float *gate_w, const float *logit_bias,
+                               int64_t T, int H, int E, int k, int renorm,
+                               int32_t *topk_ids, float *topk_w, moe_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* moe_permute -- slot map, local mask/remap, histogram, scan, scatter.     */
 /* ------------------------------------------------------------------------ */

@@ -23,7 +23,7 @@ __all__ = [
     "MOE_ERR_DEVICE_BOUNDS", "MOE_ERR_TIMEOUT", "MOE_NONLOCAL_SKIP", "MOE_NONLOCAL_MOD", "MoEError",
     "lib_path", "moe_workspace_size", "moe_workspace_init", "moe_get_device_status", "moe_get_route_stats",
     "moe_route", "moe_permute", "moe_forward", "moe_grouped_fc1", "moe_grouped_fc2", "moe_finalize",
-    "moe_debug_wait_timeout", "moe_set_wait_timeout_ns", "EXPORTED_SYMBOLS",
+    "moe_debug_wait_timeout", "moe_set_wait_timeout_ns", "moe_route_noalloc", "EXPORTED_SYMBOLS",
 ]
 
 MOE_OK = 0
@@ -39,7 +39,7 @@ MOE_NONLOCAL_MOD = 1
 EXPORTED_SYMBOLS = (
     "moe_status_string", "moe_workspace_size", "moe_workspace_init", "moe_get_device_status",
     "moe_get_route_stats", "moe_route", "moe_permute", "moe_forward", "moe_grouped_fc1", "moe_grouped_fc2",
-    "moe_finalize", "moe_debug_wait_timeout", "moe_set_wait_timeout_ns",
+    "moe_finalize", "moe_debug_wait_timeout", "moe_set_wait_timeout_ns", "moe_route_noalloc",
 )
 
 
@@ -73,6 +73,7 @@ def _load():
         "moe_finalize": ([P, i64, P, P, i64, i32, i32, P, P, P, P, P, sz, P], i32),
         "moe_debug_wait_timeout": ([P, sz, u64, P], i32),
         "moe_set_wait_timeout_ns": ([u64], None),
+        "moe_route_noalloc": ([P, P, P, i64, i32, i32, i32, i32, P, P, P], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -151,6 +152,17 @@ def moe_route(x, gate_w, logit_bias, k, renorm, topk_ids, topk_w, ws, stream=Non
                         _ptr(topk_ids, "topk_ids", _i32, (T, k)), _ptr(topk_w, "topk_w", _f32, (T, k)),
                         _ptr(ws, "ws", torch.uint8), ws.numel(), _stream(stream))
     _check("moe_route", st)
+
+
+def moe_route_noalloc(x, gate_w, logit_bias, k, renorm, topk_ids, topk_w, stream=None):
+    """moe_route without a workspace: scratch in the library's own fixed 16 MiB device array."""
+    T, H = x.shape
+    E = gate_w.shape[0]
+    st = _lib.moe_route_noalloc(_ptr(x, "x", _bf16, (T, H)), _ptr(gate_w, "gate_w", _f32, (E, H)),
+                                _ptr(logit_bias, "logit_bias", _f32, (E,), allow_none=True), T, H, E, k,
+                                int(bool(renorm)), _ptr(topk_ids, "topk_ids", _i32, (T, k)),
+                                _ptr(topk_w, "topk_w", _f32, (T, k)), _stream(stream))
+    _check("moe_route_noalloc", st)
 
 
 def moe_permute(topk_ids, topk_w, E, rep_offset, rep_slots, S, local_start, local_count, nonlocal_mode, x,
