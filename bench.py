@@ -206,7 +206,11 @@ def bench_ours(args):
     if status:
         raise RuntimeError(f"device status {status} after warm-up")
 
-    # ---- timed pass: the whole layer, K steps ----
+    # ---- timed pass: the whole layer, K steps (replayed from a CUDA graph of one step) ----
+    graph = layer.capture(x) if args.graph else None
+    step = graph.replay if graph is not None else (lambda: layer.forward(x))
+    for _ in range(W):
+        step()
     clocks = ClockSampler(torch.cuda.current_device())
     _barrier(ws_)
     torch.cuda.synchronize()
@@ -214,7 +218,7 @@ def bench_ours(args):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(K):
-        layer.forward(x)
+        step()
     e1.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
@@ -253,17 +257,23 @@ def bench_ours(args):
     x_pin = x.cpu().pin_memory()
     out_pin = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
     x_dev = torch.empty_like(x)
+    h2d = lambda: x_dev.copy_(x_pin, non_blocking=True)  # noqa: E731
+    d2h = lambda: out_pin.copy_(layer.out[:T], non_blocking=True)  # noqa: E731
+    if args.graph:
+        g_e2e = layer.capture(x_dev, pre=h2d, post=d2h)
+        e2e_step = g_e2e.replay
+    else:
+        def e2e_step():
+            h2d()
+            layer.forward(x_dev)
+            d2h()
     for _ in range(W):
-        x_dev.copy_(x_pin, non_blocking=True)
-        o = layer.forward(x_dev)
-        out_pin.copy_(o, non_blocking=True)
+        e2e_step()
     torch.cuda.synchronize()
     _barrier(ws_)
     e0.record(stream)
     for _ in range(K):
-        x_dev.copy_(x_pin, non_blocking=True)
-        o = layer.forward(x_dev)
-        out_pin.copy_(o, non_blocking=True)
+        e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
     ms_e2e = max_over_ranks(e0.elapsed_time(e1) / K, ws_)
@@ -298,6 +308,7 @@ def bench_ours(args):
                                  "workload's shapes (no checkpoint)",
         "config": {"workload": cfg.name, "shape": mi.describe(cfg), "tokens_per_gpu": T,
                    "parallelism": f"replicas x{ws_} (independent token batches, no collective)",
+                   "cuda_graph": bool(args.graph),
                    "l2": "inputs larger than L2 (expert weights %.2f GB per step)" % (
                        (cfg.slots * 3 * cfg.I * H * 2 + 3 * Ish * H * 2) / 1e9)},
         "roofline": roof,
@@ -373,6 +384,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(mi.CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", dest="graph", action="store_false",
+                    help="launch every step from Python instead of replaying a CUDA graph of one step")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args()
     if args.warmup < 3:

@@ -187,7 +187,7 @@ moe_status_t moe_permute(const int32_t* topk_ids, float* topk_w, int64_t T, int 
     L.pair_row = pair_row;
     L.x_perm = x_perm;
     L.hdr = static_cast<WsHeader*>(ws);
-    permute_carve(static_cast<char*>(ws) + kWsHeaderBytes, P, S_local, &L.chunk_cnt, &L.chunk_base);
+    permute_carve(static_cast<char*>(ws) + kWsHeaderBytes, P, S_local, &L.rank, &L.chunk_cnt, &L.chunk_base);
     return cuda_status(launch_permute(L, device_sms(), s));
 }
 

@@ -7,13 +7,15 @@
 // to the routed output (out = routed_out + shared_out).  The shared gate
 // sigmoid(x . w_s) is the Qwen2-MoE-style scaled shared expert.
 //
-// One CTA per token (grid-stride).  Each thread owns 8 consecutive columns
-// (one 16-byte vector) at a time and accumulates in fp32 in fixed j order:
+// One warp per token (8 tokens per 256-thread CTA, grid-stride).  Lane j < k
+// holds pair j's row and weight and broadcasts them with shuffles.  Each lane
+// owns the 16-byte vectors lane, lane+32, ... of the row; it issues the loads
+// of up to 4 pairs' rows (and then of the shared-expert row) before using them,
+// and accumulates in fp32 in fixed j order:
 //   acc = fma(w_j, y[row_j], acc) for j = 0..k-1 (rows of -1 skipped),
 //   acc = fma(g, y_shared, acc), out = bf16_rn(acc).
-// The gate dot product x . w_s is reduced in a fixed order (per-thread strided
-// partials, warp xor-butterfly, warps in index order), so results are
-// bit-reproducible.
+// The gate dot product x . w_s is a per-lane strided partial sum followed by a
+// warp xor-butterfly, so every lane holds the same bit-reproducible value.
 #include <algorithm>
 
 #include "moe_internal.cuh"
@@ -21,37 +23,36 @@
 namespace moe {
 namespace {
 
-constexpr int FZ_THREADS = 256;
-constexpr int FZ_MAXK = 32;
+constexpr int FZ_WARPS = 8;
+constexpr int FZ_UNROLL = 2;  // vectors per lane per pass
+constexpr int FZ_BATCH = 4;   // pairs whose loads are issued together
 
-__global__ void __launch_bounds__(FZ_THREADS) finalize_kernel(
+__global__ void __launch_bounds__(FZ_WARPS * 32) finalize_kernel(
     const uint16_t* __restrict__ y, int64_t rows_cap, const int32_t* __restrict__ pair_row,
     const float* __restrict__ w, int64_t T, int k, int H, const uint16_t* __restrict__ y_sh,
     const uint16_t* __restrict__ x, const uint16_t* __restrict__ gate_w, uint16_t* __restrict__ out,
     int32_t* status) {
-    __shared__ int64_t s_row[FZ_MAXK];
-    __shared__ float s_w[FZ_MAXK];
-    __shared__ float s_red[FZ_THREADS / 32];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
     const int vec = H / 8;
-
-    for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
-        if (tid < k) {
-            const int32_t r = pair_row[t * k + tid];
-            int64_t rr = r;
-            if (r < -1 || r >= rows_cap) {
+    for (int64_t t = (int64_t)blockIdx.x * FZ_WARPS + warp; t < T; t += (int64_t)gridDim.x * FZ_WARPS) {
+        int64_t my_row = -1;
+        float my_w = 0.f;
+        if (lane < k) {
+            const int32_t r = pair_row[t * k + lane];
+            my_row = r;
+            if (r < -1 || (int64_t)r >= rows_cap) {
                 report(status, MOE_ERR_DEVICE_BOUNDS);
-                rr = -1;
+                my_row = -1;
             }
-            s_row[tid] = rr;
-            s_w[tid] = w[t * k + tid];
+            my_w = w[t * k + lane];
         }
         float g = 1.0f;
         if (y_sh && gate_w) {
             const uint4* xv = reinterpret_cast<const uint4*>(x + t * H);
             const uint4* gv = reinterpret_cast<const uint4*>(gate_w);
             float d = 0.f;
-            for (int v = tid; v < vec; v += FZ_THREADS) {
+            for (int v = lane; v < vec; v += 32) {
                 float a[8], b[8];
                 unpack8(__ldg(xv + v), a);
                 unpack8(__ldg(gv + v), b);
@@ -60,50 +61,85 @@ __global__ void __launch_bounds__(FZ_THREADS) finalize_kernel(
             }
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
-            if (lane == 0) s_red[warp] = d;
-            __syncthreads();
-            float dot = 0.f;
-            for (int i = 0; i < FZ_THREADS / 32; ++i) dot += s_red[i];
-            g = 1.0f / (1.0f + expf(-dot));
+            g = 1.0f / (1.0f + expf(-d));
         }
-        __syncthreads();
-
-        for (int v = tid; v < vec; v += FZ_THREADS) {
-            float acc[8];
+        uint4* orow = reinterpret_cast<uint4*>(out + t * H);
+        const uint4* srow = y_sh ? reinterpret_cast<const uint4*>(y_sh + t * H) : nullptr;
+        for (int v0 = lane; v0 < vec; v0 += 32 * FZ_UNROLL) {
+            float acc[FZ_UNROLL][8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-            for (int j = 0; j < k; ++j) {
-                const int64_t r = s_row[j];
-                if (r < 0) continue;
-                float f[8];
-                unpack8(__ldg(reinterpret_cast<const uint4*>(y + r * H) + v), f);
-                const float wj = s_w[j];
+            for (int u = 0; u < FZ_UNROLL; ++u)
 #pragma unroll
-                for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, f[i], acc[i]);
+                for (int i = 0; i < 8; ++i) acc[u][i] = 0.f;
+            // pairs in batches of FZ_BATCH: every load of a batch is issued before any use
+            for (int j0 = 0; j0 < k; j0 += FZ_BATCH) {
+                uint4 ld[FZ_BATCH][FZ_UNROLL];
+                float wj[FZ_BATCH];
+#pragma unroll
+                for (int b = 0; b < FZ_BATCH; ++b) {
+                    const int j = j0 + b;
+                    const int64_t r = __shfl_sync(0xffffffffu, my_row, j & 31);
+                    wj[b] = __shfl_sync(0xffffffffu, my_w, j & 31);
+                    const bool use = (j < k) && (r >= 0);
+                    if (!use) wj[b] = 0.f;
+                    const uint4* yrow = reinterpret_cast<const uint4*>(y + (use ? r : 0) * H);
+#pragma unroll
+                    for (int u = 0; u < FZ_UNROLL; ++u) {
+                        const int v = v0 + 32 * u;
+                        ld[b][u] = (use && v < vec) ? __ldg(yrow + v) : make_uint4(0, 0, 0, 0);
+                    }
+                }
+#pragma unroll
+                for (int b = 0; b < FZ_BATCH; ++b) {
+                    if (j0 + b >= k) break;
+                    if (__shfl_sync(0xffffffffu, my_row, (j0 + b) & 31) < 0) continue;
+#pragma unroll
+                    for (int u = 0; u < FZ_UNROLL; ++u) {
+                        float f[8];
+                        unpack8(ld[b][u], f);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) acc[u][i] = fmaf(wj[b], f[i], acc[u][i]);
+                    }
+                }
             }
-            if (y_sh) {
-                float f[8];
-                unpack8(__ldg(reinterpret_cast<const uint4*>(y_sh + t * H) + v), f);
+            if (srow) {
+                uint4 ld[FZ_UNROLL];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) acc[i] = fmaf(g, f[i], acc[i]);
+                for (int u = 0; u < FZ_UNROLL; ++u) {
+                    const int v = v0 + 32 * u;
+                    ld[u] = v < vec ? __ldg(srow + v) : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int u = 0; u < FZ_UNROLL; ++u) {
+                    float f[8];
+                    unpack8(ld[u], f);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) acc[u][i] = fmaf(g, f[i], acc[u][i]);
+                }
             }
-            uint4 o;
-            o.x = pack_bf16x2(acc[0], acc[1]);
-            o.y = pack_bf16x2(acc[2], acc[3]);
-            o.z = pack_bf16x2(acc[4], acc[5]);
-            o.w = pack_bf16x2(acc[6], acc[7]);
-            reinterpret_cast<uint4*>(out + t * H)[v] = o;
+#pragma unroll
+            for (int u = 0; u < FZ_UNROLL; ++u) {
+                const int v = v0 + 32 * u;
+                if (v < vec) {
+                    uint4 o;
+                    o.x = pack_bf16x2(acc[u][0], acc[u][1]);
+                    o.y = pack_bf16x2(acc[u][2], acc[u][3]);
+                    o.z = pack_bf16x2(acc[u][4], acc[u][5]);
+                    o.w = pack_bf16x2(acc[u][6], acc[u][7]);
+                    orow[v] = o;
+                }
+            }
         }
-        __syncthreads();
     }
 }
 
 }  // namespace
 
 cudaError_t launch_finalize(const FinalizeLaunch& L, int num_sms, cudaStream_t s) {
-    const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(L.T, (int64_t)num_sms * 16));
-    finalize_kernel<<<grid, FZ_THREADS, 0, s>>>(L.y, L.rows_cap, L.pair_row, L.w, L.T, L.k, L.H, L.y_sh, L.x,
-                                                L.gate_w, L.out, L.hdr ? &L.hdr->status : nullptr);
+    const int64_t want = (L.T + FZ_WARPS - 1) / FZ_WARPS;
+    const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms * 8));
+    finalize_kernel<<<grid, FZ_WARPS * 32, 0, s>>>(L.y, L.rows_cap, L.pair_row, L.w, L.T, L.k, L.H, L.y_sh, L.x,
+                                                   L.gate_w, L.out, L.hdr ? &L.hdr->status : nullptr);
     return cudaGetLastError();
 }
 

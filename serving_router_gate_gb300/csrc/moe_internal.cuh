@@ -248,12 +248,13 @@ struct PermuteLaunch {
     int32_t* perm_src;
     int32_t* pair_row;
     uint16_t* x_perm;
+    int32_t* rank;        // [T*k] rank of each pair among its chunk's pairs of its slot
     int32_t* chunk_cnt;   // [nchunks][S_local]
     int32_t* chunk_base;  // [nchunks][S_local]
     WsHeader* hdr;
 };
 size_t permute_scratch_bytes(int64_t P, int S_local);
-void permute_carve(void* base, int64_t P, int S_local, int32_t** chunk_cnt, int32_t** chunk_base);
+void permute_carve(void* base, int64_t P, int S_local, int32_t** rank, int32_t** chunk_cnt, int32_t** chunk_base);
 cudaError_t launch_permute(const PermuteLaunch& L, int num_sms, cudaStream_t s);
 
 struct GemmLaunch {

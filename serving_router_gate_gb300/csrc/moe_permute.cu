@@ -16,18 +16,21 @@
 //    counts, and within a slot pairs keep ascending pair index t*k + j.
 //
 // Pipeline (no atomics decide any output position; results are deterministic):
-//  K1 permute_count_kernel  one warp per chunk of 512 pairs: slot map + mask,
-//                           writes slot_ids (and zeroes masked weights), and
-//                           the chunk's per-slot counts.
-//  K2 permute_scan_kernel   one CTA: counts = column sums, offsets = exclusive
-//                           scan, base[c][s] = offsets[s] + sum of earlier
-//                           chunks' counts of s.
-//  K3 permute_place_kernel  one warp per chunk: walks its pairs in order, 32 at
-//                           a time; lanes with equal slots are ranked with
-//                           __match_any_sync, so row = base + running count +
-//                           rank among lower lanes.  Writes pair_row, perm_src.
-//  K4 permute_gather_kernel one warp per row: x_perm[r] = x[perm_src[r] / k]
-//                           with 16-byte loads/stores.
+//  K1 permute_rank_kernel    one warp per chunk of 256 pairs: slot map + mask
+//                            (writes slot_ids, zeroes masked weights), then the
+//                            stable rank of each pair among the chunk's pairs of
+//                            its slot (__match_any_sync over 32 lanes plus a
+//                            per-warp running count), and the chunk's per-slot
+//                            counts.
+//  K2 permute_scan_kernel    one CTA: counts = column sums, offsets = exclusive
+//                            scan, base[c][s] = offsets[s] + earlier chunks'
+//                            counts of s.
+//  K3 permute_scatter_kernel fully parallel, 8 pairs per warp step:
+//                            row = base[chunk][slot] + rank; writes pair_row
+//                            and perm_src, and the warp copies x[t] into
+//                            x_perm[row] with 16-byte loads/stores.
+#include <stdint.h>
+
 #include <algorithm>
 
 #include "moe_internal.cuh"
@@ -35,7 +38,8 @@
 namespace moe {
 namespace {
 
-constexpr int PM_CHUNK = 512;     // pairs per warp-chunk
+constexpr int PM_CHUNK = 256;     // pairs per warp-chunk
+constexpr int PM_ROUNDS = PM_CHUNK / 32;
 constexpr int PM_WARPS = 8;       // warps per CTA in K1 / K3
 constexpr int PM_SCAN_THREADS = 1024;
 
@@ -60,36 +64,56 @@ __device__ __forceinline__ int32_t map_slot(int32_t e, int64_t t, int E, const i
     return s;
 }
 
-__global__ void __launch_bounds__(PM_WARPS * 32) permute_count_kernel(
+__global__ void __launch_bounds__(PM_WARPS * 32) permute_rank_kernel(
     const int32_t* __restrict__ ids, float* __restrict__ w, int64_t P, int k, int E,
     const int32_t* __restrict__ rep_offset, const int32_t* __restrict__ rep_slots, int S, int local_start,
-    int local_count, int mode, int S_local, int32_t* __restrict__ slot_ids, int32_t* __restrict__ chunk_cnt,
-    int64_t nchunks, int32_t* status) {
-    extern __shared__ int32_t pm_cnt[];  // [PM_WARPS][S_local]
+    int local_count, int mode, int S_local, int32_t* __restrict__ slot_ids, int32_t* __restrict__ rank,
+    int32_t* __restrict__ chunk_cnt, int64_t nchunks, int32_t* status) {
+    extern __shared__ int32_t pm_cur[];  // [PM_WARPS][S_local]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int32_t* cnt = pm_cnt + (size_t)warp * S_local;
-    for (int s = lane; s < S_local; s += 32) cnt[s] = 0;
+    int32_t* cur = pm_cur + (size_t)warp * S_local;
+    for (int s = lane; s < S_local; s += 32) cur[s] = 0;
     __syncwarp();
     const int64_t c = (int64_t)blockIdx.x * PM_WARPS + warp;
     if (c >= nchunks) return;
     const int64_t p0 = c * PM_CHUNK;
-    const int64_t p1 = min(P, p0 + PM_CHUNK);
-    for (int64_t p = p0 + lane; p < p1; p += 32) {
-        const int64_t t = p / k;
-        int32_t s = map_slot(ids[p], t, E, rep_offset, rep_slots, S, status);
-        if (s >= 0 && local_count >= 0) {
+
+    // slot of each of this lane's pairs (all loads issued before any use)
+    int32_t sl[PM_ROUNDS];
+#pragma unroll
+    for (int r = 0; r < PM_ROUNDS; ++r) {
+        const int64_t p = p0 + r * 32 + lane;
+        sl[r] = (p < P) ? ids[p] : INT32_MIN;
+    }
+#pragma unroll
+    for (int r = 0; r < PM_ROUNDS; ++r) {
+        const int64_t p = p0 + r * 32 + lane;
+        if (p >= P) {
+            sl[r] = -2;  // padding lane: neither counted nor written
+            continue;
+        }
+        int32_t s = map_slot(sl[r], p / k, E, rep_offset, rep_slots, S, status);
+        if (local_count >= 0) {
             const bool local = (s >= local_start) && (s < local_start + local_count);
             w[p] = w[p] * (local ? 1.0f : 0.0f);
-            s = local ? s - local_start : (mode == MOE_NONLOCAL_MOD ? s % local_count : -1);
-        } else if (s < 0 && local_count >= 0) {
-            w[p] = w[p] * 0.0f;
+            if (s >= 0) s = local ? s - local_start : (mode == MOE_NONLOCAL_MOD ? s % local_count : -1);
         }
         slot_ids[p] = s;
-        if (s >= 0) atomicAdd(&cnt[s], 1);
+        sl[r] = s;
     }
-    __syncwarp();
+    // stable rank of each pair among the chunk's pairs of its slot
+    const uint32_t lt_mask = (1u << lane) - 1u;
+#pragma unroll
+    for (int r = 0; r < PM_ROUNDS; ++r) {
+        const int32_t s = sl[r];
+        const uint32_t peers = __match_any_sync(0xffffffffu, s);
+        if (s >= 0) rank[p0 + r * 32 + lane] = cur[s] + __popc(peers & lt_mask);
+        __syncwarp();
+        if (s >= 0 && lane == 31 - __clz(peers)) cur[s] += __popc(peers);
+        __syncwarp();
+    }
     int32_t* dst = chunk_cnt + c * S_local;
-    for (int s = lane; s < S_local; s += 32) dst[s] = cnt[s];
+    for (int s = lane; s < S_local; s += 32) dst[s] = cur[s];
 }
 
 __global__ void __launch_bounds__(PM_SCAN_THREADS) permute_scan_kernel(const int32_t* __restrict__ chunk_cnt,
@@ -101,7 +125,13 @@ __global__ void __launch_bounds__(PM_SCAN_THREADS) permute_scan_kernel(const int
     const int s = threadIdx.x;
     int32_t tot = 0;
     if (s < S_local) {
-        for (int64_t c = 0; c < nchunks; ++c) tot += chunk_cnt[c * S_local + s];
+        int64_t c = 0;
+        for (; c + 4 <= nchunks; c += 4) {
+            const int32_t a0 = chunk_cnt[(c + 0) * S_local + s], a1 = chunk_cnt[(c + 1) * S_local + s];
+            const int32_t a2 = chunk_cnt[(c + 2) * S_local + s], a3 = chunk_cnt[(c + 3) * S_local + s];
+            tot += a0 + a1 + a2 + a3;
+        }
+        for (; c < nchunks; ++c) tot += chunk_cnt[c * S_local + s];
         counts[s] = tot;
     }
     // block exclusive scan of tot over s
@@ -129,63 +159,49 @@ __global__ void __launch_bounds__(PM_SCAN_THREADS) permute_scan_kernel(const int
         offsets[s] = excl;
         int32_t run = excl;
         for (int64_t c = 0; c < nchunks; ++c) {
+            const int32_t v = chunk_cnt[c * S_local + s];
             chunk_base[c * S_local + s] = run;
-            run += chunk_cnt[c * S_local + s];
+            run += v;
         }
         if (s == S_local - 1) offsets[S_local] = excl + tot;
     }
 }
 
-__global__ void __launch_bounds__(PM_WARPS * 32) permute_place_kernel(const int32_t* __restrict__ slot_ids,
-                                                                      int64_t P, int S_local,
-                                                                      const int32_t* __restrict__ chunk_base,
-                                                                      int64_t nchunks,
-                                                                      int32_t* __restrict__ pair_row,
-                                                                      int32_t* __restrict__ perm_src) {
-    extern __shared__ int32_t pm_cur[];  // [PM_WARPS][S_local]
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t c = (int64_t)blockIdx.x * PM_WARPS + warp;
-    if (c >= nchunks) return;
-    int32_t* cur = pm_cur + (size_t)warp * S_local;
-    for (int s = lane; s < S_local; s += 32) cur[s] = chunk_base[c * S_local + s];
-    __syncwarp();
-    const int64_t p0 = c * PM_CHUNK;
-    const uint32_t lt_mask = (1u << lane) - 1u;
-    for (int it = 0; it < PM_CHUNK / 32; ++it) {
-        const int64_t p = p0 + it * 32 + lane;
-        if (p0 + it * 32 >= P) break;
-        const int32_t s = (p < P) ? slot_ids[p] : -2;
-        const uint32_t peers = __match_any_sync(0xffffffffu, s);
-        if (s >= 0) {
-            const int32_t row = cur[s] + __popc(peers & lt_mask);
-            pair_row[p] = row;
-            perm_src[row] = (int32_t)p;
-        } else if (s == -1) {
-            pair_row[p] = -1;
-        }
-        __syncwarp();
-        if (s >= 0 && lane == 31 - __clz(peers)) cur[s] += __popc(peers);
-        __syncwarp();
-    }
-}
+// row of each pair = its chunk's base for the slot + its rank inside the chunk.
+// A warp takes 8 pairs per step: lanes 0..7 compute the rows (and write
+// pair_row / perm_src), then the whole warp copies the 8 rows of x.
+constexpr int PS_PAIRS = 8;
 
-__global__ void __launch_bounds__(256) permute_gather_kernel(const uint16_t* __restrict__ x,
-                                                             const int32_t* __restrict__ perm_src,
-                                                             const int32_t* __restrict__ offsets, int S_local,
-                                                             int k, int H, int64_t P, uint16_t* __restrict__ x_perm,
-                                                             int32_t* status) {
+__global__ void __launch_bounds__(256) permute_scatter_kernel(const uint16_t* __restrict__ x,
+                                                              const int32_t* __restrict__ slot_ids,
+                                                              const int32_t* __restrict__ rank,
+                                                              const int32_t* __restrict__ chunk_base, int S_local,
+                                                              int64_t P, int k, int H,
+                                                              int32_t* __restrict__ pair_row,
+                                                              int32_t* __restrict__ perm_src,
+                                                              uint16_t* __restrict__ x_perm) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int32_t rows = offsets[S_local];
     const int vec = H / 8;
-    for (int64_t r = (int64_t)blockIdx.x * 8 + warp; r < rows; r += (int64_t)gridDim.x * 8) {
-        const int32_t p = perm_src[r];
-        if (p < 0 || p >= P) {
-            if (lane == 0) report(status, MOE_ERR_DEVICE_BOUNDS);
-            continue;
+    for (int64_t pb = ((int64_t)blockIdx.x * 8 + warp) * PS_PAIRS; pb < P;
+         pb += (int64_t)gridDim.x * 8 * PS_PAIRS) {
+        int32_t row = -1;
+        if (lane < PS_PAIRS && pb + lane < P) {
+            const int64_t p = pb + lane;
+            const int32_t s = slot_ids[p];
+            if (s >= 0) {
+                row = chunk_base[(p / PM_CHUNK) * S_local + s] + rank[p];
+                perm_src[row] = (int32_t)p;
+            }
+            pair_row[p] = row;
         }
-        const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)(p / k) * H);
-        uint4* dst = reinterpret_cast<uint4*>(x_perm + r * H);
-        for (int v = lane; v < vec; v += 32) dst[v] = __ldg(src + v);
+        const int nj = (int)min((int64_t)PS_PAIRS, P - pb);
+        for (int j = 0; j < nj; ++j) {
+            const int32_t r = __shfl_sync(0xffffffffu, row, j);
+            if (r < 0) continue;
+            const uint4* src = reinterpret_cast<const uint4*>(x + ((pb + j) / k) * H);
+            uint4* dst = reinterpret_cast<uint4*>(x_perm + (int64_t)r * H);
+            for (int v = lane; v < vec; v += 32) dst[v] = __ldg(src + v);
+        }
     }
 }
 
@@ -195,38 +211,39 @@ static size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 size_t permute_scratch_bytes(int64_t P, int S_local) {
     const int64_t nchunks = (P + PM_CHUNK - 1) / PM_CHUNK;
-    return 2 * align256((size_t)std::max<int64_t>(nchunks, 1) * (size_t)S_local * sizeof(int32_t));
+    return align256((size_t)std::max<int64_t>(P, 1) * sizeof(int32_t)) +
+           2 * align256((size_t)std::max<int64_t>(nchunks, 1) * (size_t)S_local * sizeof(int32_t));
 }
 
-void permute_carve(void* base, int64_t P, int S_local, int32_t** chunk_cnt, int32_t** chunk_base) {
+void permute_carve(void* base, int64_t P, int S_local, int32_t** rank, int32_t** chunk_cnt, int32_t** chunk_base) {
     const int64_t nchunks = (P + PM_CHUNK - 1) / PM_CHUNK;
+    const size_t r = align256((size_t)std::max<int64_t>(P, 1) * sizeof(int32_t));
     const size_t one = align256((size_t)std::max<int64_t>(nchunks, 1) * (size_t)S_local * sizeof(int32_t));
-    *chunk_cnt = static_cast<int32_t*>(base);
-    *chunk_base = reinterpret_cast<int32_t*>(static_cast<char*>(base) + one);
+    char* b = static_cast<char*>(base);
+    *rank = reinterpret_cast<int32_t*>(b);
+    *chunk_cnt = reinterpret_cast<int32_t*>(b + r);
+    *chunk_base = reinterpret_cast<int32_t*>(b + r + one);
 }
 
 cudaError_t launch_permute(const PermuteLaunch& L, int num_sms, cudaStream_t s) {
     const int64_t P = L.T * L.k;
     const int64_t nchunks = (P + PM_CHUNK - 1) / PM_CHUNK;
-    const unsigned g13 = (unsigned)((nchunks + PM_WARPS - 1) / PM_WARPS);
+    const unsigned g1 = (unsigned)((nchunks + PM_WARPS - 1) / PM_WARPS);
     const size_t smem = (size_t)PM_WARPS * L.S_local * sizeof(int32_t);
     int32_t* status = &L.hdr->status;
-    permute_count_kernel<<<g13, PM_WARPS * 32, smem, s>>>(L.ids, L.w, P, L.k, L.E, L.rep_offset, L.rep_slots, L.S,
-                                                          L.local_start, L.local_count, L.mode, L.S_local,
-                                                          L.slot_ids, L.chunk_cnt, nchunks, status);
+    permute_rank_kernel<<<g1, PM_WARPS * 32, smem, s>>>(L.ids, L.w, P, L.k, L.E, L.rep_offset, L.rep_slots, L.S,
+                                                        L.local_start, L.local_count, L.mode, L.S_local,
+                                                        L.slot_ids, L.rank, L.chunk_cnt, nchunks, status);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     permute_scan_kernel<<<1, PM_SCAN_THREADS, 0, s>>>(L.chunk_cnt, nchunks, L.S_local, L.counts, L.offsets,
                                                       L.chunk_base);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    permute_place_kernel<<<g13, PM_WARPS * 32, smem, s>>>(L.slot_ids, P, L.S_local, L.chunk_base, nchunks,
-                                                          L.pair_row, L.perm_src);
-    err = cudaGetLastError();
-    if (err != cudaSuccess) return err;
-    const int64_t want = (P + 7) / 8;
-    const unsigned g4 = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms * 8));
-    permute_gather_kernel<<<g4, 256, 0, s>>>(L.x, L.perm_src, L.offsets, L.S_local, L.k, L.H, P, L.x_perm, status);
+    const int64_t want = (P + 8 * PS_PAIRS - 1) / (8 * PS_PAIRS);
+    const unsigned g3 = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms * 8));
+    permute_scatter_kernel<<<g3, 256, 0, s>>>(L.x, L.slot_ids, L.rank, L.chunk_base, L.S_local, P, L.k, L.H,
+                                              L.pair_row, L.perm_src, L.x_perm);
     return cudaGetLastError();
 }
 

@@ -10,11 +10,12 @@
 //
 // Two kernels:
 //  1. router_logits_kernel: partial logits l[t,e] over a K range per CTA.
-//     Tile 64 tokens x 64 experts x K-range; each thread owns 4x4 outputs.
-//     Accumulation is nested (32-term chunks -> groups of 8 chunks -> the
-//     CTA's range), which keeps the worst-case rounding error of every logit
-//     below gamma_n * (||x_t|| ||w_e|| + |b_e|) with a small n (about 70 for
-//     H = 7168) instead of n = H.  The CTAs of the first token/expert tile
+//     Tile 64 tokens x 64 experts x K-range; each thread owns 4x4 outputs,
+//     read as float4 along k from padded k-contiguous shared-memory rows.
+//     Accumulation is nested (even/odd-k chains of 16 terms per 32-k chunk ->
+//     groups of 8 chunks -> the CTA's range), which keeps the worst-case
+//     rounding error of every logit below gamma_n * (||x_t|| ||w_e|| + |b_e|)
+//     with a small n (about 60 for H = 7168) instead of n = H.  The CTAs of the first token/expert tile
 //     also emit the partial squared norms of x rows and Wg rows.
 //  2. router_select_kernel: one warp per token.  Sums the split partials in
 //     fixed order, adds the bias, and takes the k+1 largest logits (ties ->
@@ -26,6 +27,7 @@
 //     optional renormalisation (divide by their sum, in j order).
 #include <float.h>
 #include <limits.h>
+#include <stdint.h>
 
 #include <algorithm>
 
@@ -44,16 +46,41 @@ constexpr int RT_MAX_SPLIT = 32;
 
 constexpr int RS_WARPS = 8;      // select: tokens (warps) per CTA
 constexpr int RS_MAXE = 512;
-constexpr int RS_PER_LANE = RS_MAXE / 32;
 
-__global__ void __launch_bounds__(RT_THREADS) router_logits_kernel(const uint16_t* __restrict__ x,
-                                                                   const float* __restrict__ Wg, int64_t T,
-                                                                   int H, int E, int KC,
-                                                                   float* __restrict__ part,
-                                                                   float* __restrict__ xsq,
-                                                                   float* __restrict__ wsq) {
-    __shared__ __align__(16) float xs[2][RT_BK][RT_BT + 4];
-    __shared__ __align__(16) float wsm[2][RT_BK][RT_BE + 4];
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc, bool valid) {
+    // 16-byte global->shared copy; zero-fills when !valid (source size 0)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)), "l"(gsrc),
+                 "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Tile: 64 tokens x 64 experts x a K range per CTA, 256 threads, 4x4 outputs
+// per thread.  Shared memory holds k-contiguous rows padded to 36 floats, so
+// the float4 reads along k are bank-conflict-free.  Wg chunks arrive through a
+// 4-stage cp.async ring; x chunks are loaded two chunks ahead into registers,
+// converted to fp32 and stored into a double-buffered tile.  Thread (tg, eg)
+// owns tokens tg + 16 i and experts eg + 16 j (i, j < 4).  Each logit's sum:
+// per 32-k chunk (one stage), two interleaved chains -- even k and odd k, each
+// in ascending k, advanced together by packed fp32 FMAs -- then their sum;
+// chunks summed in groups of 8, groups summed over the CTA's range.
+constexpr int RT_LD = RT_BK + 4;  // padded row length (floats)
+constexpr int RT_WSTAGES = 4;
+constexpr size_t RT_SMEM = sizeof(float) * RT_LD * (RT_WSTAGES * RT_BE + 2 * RT_BT);
+
+__global__ void __launch_bounds__(RT_THREADS, 2) router_logits_kernel(const uint16_t* __restrict__ x,
+                                                                      const float* __restrict__ Wg, int64_t T,
+                                                                      int H, int E, int KC,
+                                                                      float* __restrict__ part,
+                                                                      float* __restrict__ xsq,
+                                                                      float* __restrict__ wsq) {
+    extern __shared__ __align__(16) float rt_smem[];
+    float (*wsm)[RT_BE][RT_LD] = reinterpret_cast<float (*)[RT_BE][RT_LD]>(rt_smem);
+    float (*xs)[RT_BT][RT_LD] = reinterpret_cast<float (*)[RT_BT][RT_LD]>(rt_smem + RT_WSTAGES * RT_BE * RT_LD);
 
     const int tid = threadIdx.x;
     const int64_t t0 = (int64_t)blockIdx.x * RT_BT;
@@ -63,80 +90,95 @@ __global__ void __launch_bounds__(RT_THREADS) router_logits_kernel(const uint16_
     const int kend = min(H, kbeg + KC);
     const int nchunk = (kend - kbeg) / RT_BK;
 
-    // loader: thread -> (row of the tile, 8 consecutive k)
-    const int lrow = tid >> 2;
-    const int lk = (tid & 3) * 8;
-    const int64_t xt = t0 + lrow;
-    const bool xvalid = xt < T;
-    const int we = e0 + lrow;
-    const bool wvalid = we < E;
-    const uint16_t* xsrc = x + (xvalid ? xt : 0) * (int64_t)H + kbeg + lk;
-    const float* wsrc = Wg + (int64_t)(wvalid ? we : 0) * H + kbeg + lk;
+    // x loader: row tid/4 of the tile, 8 consecutive k at (tid%4)*8
+    const int xr = tid >> 2, xk = (tid & 3) * 8;
+    const bool xvalid = t0 + xr < T;
+    const uint16_t* xsrc = x + (xvalid ? t0 + xr : 0) * (int64_t)H + kbeg + xk;
+    // Wg loader: 64 rows x 32 floats = 512 16-byte pieces, two per thread
+    const int wr0 = tid >> 3, wk0 = (tid & 7) * 4;
+    const int wr1 = wr0 + 32;
+    const bool wv0 = e0 + wr0 < E, wv1 = e0 + wr1 < E;
+    const float* wsrc0 = Wg + (int64_t)(wv0 ? e0 + wr0 : 0) * H + kbeg + wk0;
+    const float* wsrc1 = Wg + (int64_t)(wv1 ? e0 + wr1 : 0) * H + kbeg + wk0;
 
-    uint4 xr = make_uint4(0, 0, 0, 0);
-    float4 wr0 = make_float4(0.f, 0.f, 0.f, 0.f), wr1 = wr0;
-    auto gload = [&](int c) {
-        if (xvalid) xr = __ldg(reinterpret_cast<const uint4*>(xsrc + c * RT_BK));
-        if (wvalid) {
-            wr0 = __ldg(reinterpret_cast<const float4*>(wsrc + c * RT_BK));
-            wr1 = __ldg(reinterpret_cast<const float4*>(wsrc + c * RT_BK + 4));
+    auto issue_w = [&](int c) {  // always commits a group (empty past the end) so counts stay uniform
+        if (c < nchunk) {
+            const int st = c % RT_WSTAGES;
+            cp_async16(&wsm[st][wr0][wk0], wsrc0 + c * RT_BK, wv0);
+            cp_async16(&wsm[st][wr1][wk0], wsrc1 + c * RT_BK, wv1);
         }
+        cp_async_commit();
     };
-    auto sstore = [&](int buf) {
+    auto load_x = [&](int c) -> uint4 {
+        return (xvalid && c < nchunk) ? __ldg(reinterpret_cast<const uint4*>(xsrc + c * RT_BK))
+                                      : make_uint4(0, 0, 0, 0);
+    };
+    auto store_x = [&](int buf, const uint4& v) {
         float f[8];
-        unpack8(xr, f);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) xs[buf][lk + i][lrow] = f[i];
-        wsm[buf][lk + 0][lrow] = wr0.x;
-        wsm[buf][lk + 1][lrow] = wr0.y;
-        wsm[buf][lk + 2][lrow] = wr0.z;
-        wsm[buf][lk + 3][lrow] = wr0.w;
-        wsm[buf][lk + 4][lrow] = wr1.x;
-        wsm[buf][lk + 5][lrow] = wr1.y;
-        wsm[buf][lk + 6][lrow] = wr1.z;
-        wsm[buf][lk + 7][lrow] = wr1.w;
+        unpack8(v, f);
+        *reinterpret_cast<float4*>(&xs[buf][xr][xk]) = make_float4(f[0], f[1], f[2], f[3]);
+        *reinterpret_cast<float4*>(&xs[buf][xr][xk + 4]) = make_float4(f[4], f[5], f[6], f[7]);
     };
 
-    const int ty = tid >> 4;  // tokens ty*4 .. +3
-    const int tx = tid & 15;  // experts tx*4 .. +3
+    // warp w covers token groups 4*(w/2) .. +3 and expert groups 8*(w%2) .. +7:
+    // per load instruction 4 distinct x rows and 8 distinct Wg rows (one
+    // shared-memory wavefront each)
+    const int wid = tid >> 5, ln = tid & 31;
+    const int tg = (wid >> 1) * 4 + (ln >> 3);
+    const int eg = (wid & 1) * 8 + (ln & 7);
     const bool do_xn = (blockIdx.y == 0) && (tid < RT_BT);
     const bool do_wn = (blockIdx.x == 0) && (tid >= 64) && (tid < 64 + RT_BE);
-    float a1[4][4], a2[4][4], a3[4][4];
+    // level 1: one packed pair per output -- (sum over even k, sum over odd k)
+    // of the chunk, advanced by __ffma2_rn (two independent round-to-nearest
+    // fmas); levels 2 and 3: fp32
+    float2 a1[4][4];
+    float a2[4][4], a3[4][4];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) a1[i][j] = a2[i][j] = a3[i][j] = 0.f;
+        for (int j = 0; j < 4; ++j) {
+            a1[i][j] = make_float2(0.f, 0.f);
+            a2[i][j] = a3[i][j] = 0.f;
+        }
     float nsq = 0.f;
 
-    if (nchunk > 0) {
-        gload(0);
-        sstore(0);
-    }
+    // prologue: Wg chunks 0..2 in flight, x chunk 0 in shared memory, x chunks 1, 2 in registers
+    for (int c = 0; c < RT_WSTAGES - 1; ++c) issue_w(c);
+    store_x(0, load_x(0));
+    uint4 xn1 = load_x(1), xn2 = load_x(2);
+    cp_async_wait_group<RT_WSTAGES - 2>();
     __syncthreads();
+
     for (int c = 0; c < nchunk; ++c) {
         const int buf = c & 1;
-        if (c + 1 < nchunk) gload(c + 1);
-#pragma unroll 8
-        for (int kk = 0; kk < RT_BK; ++kk) {
-            const float4 av = *reinterpret_cast<const float4*>(&xs[buf][kk][ty * 4]);
-            const float4 bv = *reinterpret_cast<const float4*>(&wsm[buf][kk][tx * 4]);
-            const float a[4] = {av.x, av.y, av.z, av.w};
-            const float b[4] = {bv.x, bv.y, bv.z, bv.w};
+        const int st = c % RT_WSTAGES;
+        issue_w(c + RT_WSTAGES - 1);
+        const uint4 xn3 = load_x(c + 3);
+#pragma unroll 2
+        for (int kk = 0; kk < RT_BK; kk += 4) {
+            float4 xa[4], wb[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) xa[i] = *reinterpret_cast<const float4*>(&xs[buf][tg + 16 * i][kk]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) wb[j] = *reinterpret_cast<const float4*>(&wsm[st][eg + 16 * j][kk]);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) a1[i][j] = fmaf(a[i], b[j], a1[i][j]);
+                for (int j = 0; j < 4; ++j) {
+                    a1[i][j] = __ffma2_rn(make_float2(xa[i].x, xa[i].y), make_float2(wb[j].x, wb[j].y), a1[i][j]);
+                    a1[i][j] = __ffma2_rn(make_float2(xa[i].z, xa[i].w), make_float2(wb[j].z, wb[j].w), a1[i][j]);
+                }
         }
         if (do_xn) {
 #pragma unroll 8
             for (int kk = 0; kk < RT_BK; ++kk) {
-                const float v = xs[buf][kk][tid];
+                const float v = xs[buf][tid][kk];
                 nsq = fmaf(v, v, nsq);
             }
         } else if (do_wn) {
 #pragma unroll 8
             for (int kk = 0; kk < RT_BK; ++kk) {
-                const float v = wsm[buf][kk][tid - 64];
+                const float v = wsm[st][tid - 64][kk];
                 nsq = fmaf(v, v, nsq);
             }
         }
@@ -144,8 +186,8 @@ __global__ void __launch_bounds__(RT_THREADS) router_logits_kernel(const uint16_
         for (int i = 0; i < 4; ++i)
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                a2[i][j] += a1[i][j];
-                a1[i][j] = 0.f;
+                a2[i][j] += a1[i][j].x + a1[i][j].y;
+                a1[i][j] = make_float2(0.f, 0.f);
             }
         if ((c % RT_GROUP) == RT_GROUP - 1) {
 #pragma unroll
@@ -156,7 +198,10 @@ __global__ void __launch_bounds__(RT_THREADS) router_logits_kernel(const uint16_
                     a2[i][j] = 0.f;
                 }
         }
-        if (c + 1 < nchunk) sstore(buf ^ 1);
+        store_x(buf ^ 1, xn1);
+        xn1 = xn2;
+        xn2 = xn3;
+        cp_async_wait_group<RT_WSTAGES - 2>();  // Wg chunk c+1 has landed
         __syncthreads();
     }
 #pragma unroll
@@ -166,12 +211,12 @@ __global__ void __launch_bounds__(RT_THREADS) router_logits_kernel(const uint16_
 
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const int64_t t = t0 + ty * 4 + i;
+        const int64_t t = t0 + tg + 16 * i;
         if (t >= T) continue;
         float* dst = part + ((int64_t)sp * T + t) * E;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const int e = e0 + tx * 4 + j;
+            const int e = e0 + eg + 16 * j;
             if (e < E) dst[e] = a3[i][j];
         }
     }
@@ -203,19 +248,20 @@ __device__ double refine_dot(const uint16_t* __restrict__ xrow, const float* __r
     return s;
 }
 
-__device__ __forceinline__ double gamma_n(double n, double u) { return n * u / (1.0 - n * u); }
-
-__device__ __forceinline__ float pick(const float (&l)[RS_PER_LANE], int idx) {
+template <int PL>
+__device__ __forceinline__ float pick(const float (&l)[PL], int idx) {
     float v = 0.f;
 #pragma unroll
-    for (int i = 0; i < RS_PER_LANE; ++i)
+    for (int i = 0; i < PL; ++i)
         if (i == idx) v = l[i];
     return v;
 }
 
+// PL = experts per lane (E <= 32 * PL); lane holds experts lane + 32*i.
+template <int PL>
 __global__ void __launch_bounds__(RS_WARPS * 32) router_select_kernel(
     const float* __restrict__ part, const float* __restrict__ xsq, const float* __restrict__ wsq, int nsplit,
-    int chain_n, const float* __restrict__ bias, const uint16_t* __restrict__ x, const float* __restrict__ Wg,
+    float thr_coef, const float* __restrict__ bias, const uint16_t* __restrict__ x, const float* __restrict__ Wg,
     int64_t T, int H, int E, int k, int renorm, int32_t* __restrict__ ids, float* __restrict__ wout,
     WsHeader* hdr) {
     extern __shared__ __align__(16) unsigned char rs_smem[];
@@ -232,10 +278,14 @@ __global__ void __launch_bounds__(RS_WARPS * 32) router_select_kernel(
     // CTA prologue: max_e ||w_e||^2 and max_e |b_e|
     float wm = 0.f, bm = 0.f;
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        float v[RT_MAX_SPLIT];  // all loads in flight before the (ordered) sum
+#pragma unroll
+        for (int q = 0; q < RT_MAX_SPLIT; ++q) v[q] = q < nsplit ? __ldg(wsq + (int64_t)q * E + e) : 0.f;
         float s = 0.f;
-        for (int q = 0; q < nsplit; ++q) s += wsq[(int64_t)q * E + e];
+#pragma unroll
+        for (int q = 0; q < RT_MAX_SPLIT; ++q) s += v[q];
         wm = fmaxf(wm, s);
-        if (bias) bm = fmaxf(bm, fabsf(bias[e]));
+        if (bias) bm = fmaxf(bm, fabsf(__ldg(bias + e)));
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
@@ -253,30 +303,50 @@ __global__ void __launch_bounds__(RS_WARPS * 32) router_select_kernel(
         wm = fmaxf(wm, s_red[0][i]);
         bm = fmaxf(bm, s_red[1][i]);
     }
-    const double wnorm_max = sqrt((double)wm);
-    const double bias_max = (double)bm;
-    const double g32 = gamma_n((double)chain_n, 1.0 / 16777216.0);             // u = 2^-24
-    const double g64 = gamma_n((double)H + 2.0, 1.0 / 9007199254740992.0);      // u = 2^-53
+    // fp32 bound arithmetic: thr_coef already carries a 1 % margin, far above the
+    // relative rounding (< 2^-20) of the few fp32 operations below
+    const float wnorm_max = sqrtf(wm);
+    const float bias_max = bm;
 
     for (int64_t t = (int64_t)blockIdx.x * RS_WARPS + warp; t < T; t += (int64_t)gridDim.x * RS_WARPS) {
-        // fp32 logits of this token: lane holds experts lane + 32*i
-        float l[RS_PER_LANE];
+        // fp32 logits of this token: sum of the split partials in split order, then the bias
+        float l[PL];
 #pragma unroll
-        for (int i = 0; i < RS_PER_LANE; ++i) {
+        for (int i = 0; i < PL; ++i) l[i] = 0.f;
+        const float* pt = part + t * E + lane;
+        constexpr int QB = PL >= 16 ? 1 : 16 / PL;  // splits whose loads are issued together
+        for (int q0 = 0; q0 < nsplit; q0 += QB) {
+            float v[QB][PL];
+#pragma unroll
+            for (int b = 0; b < QB; ++b)
+#pragma unroll
+                for (int i = 0; i < PL; ++i)
+                    v[b][i] = (q0 + b < nsplit && lane + 32 * i < E) ? __ldg(pt + (int64_t)(q0 + b) * T * E + 32 * i)
+                                                                     : 0.f;
+#pragma unroll
+            for (int b = 0; b < QB; ++b)
+#pragma unroll
+                for (int i = 0; i < PL; ++i) l[i] += v[b][i];
+        }
+#pragma unroll
+        for (int i = 0; i < PL; ++i) {
             const int e = lane + 32 * i;
-            float v = -INFINITY;
+            float v = l[i];
             if (e < E) {
-                v = 0.f;
-                for (int q = 0; q < nsplit; ++q) v += part[((int64_t)q * T + t) * E + e];
                 if (bias) v += bias[e];
                 if (v != v) v = -INFINITY;  // NaN logits never win
+            } else {
+                v = -INFINITY;
             }
             l[i] = v;
         }
+        // squared norm of x_t: only bounds the error (inflated by 1.01), order is immaterial
         float xs2 = 0.f;
-        for (int q = 0; q < nsplit; ++q) xs2 += xsq[(int64_t)q * T + t];
-        const double mag = (sqrt((double)xs2) * wnorm_max + bias_max) * 1.01;
-        const double thr = 2.0 * (g32 + g64) * mag;  // two logits closer than this: order not certain
+        for (int q = lane; q < nsplit; q += 32) xs2 += xsq[(int64_t)q * T + t];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) xs2 += __shfl_xor_sync(0xffffffffu, xs2, off);
+        // two fp32 logits closer than thr may be in either true order
+        const float thr = thr_coef * fmaf(sqrtf(xs2), wnorm_max, bias_max);
 
         // extract candidates in (logit desc, id asc) order until the cluster
         // that contains rank k-1 is closed
@@ -287,7 +357,7 @@ __global__ void __launch_bounds__(RS_WARPS * 32) router_select_kernel(
             float bv = -INFINITY;
             int be = INT_MAX;
 #pragma unroll
-            for (int i = 0; i < RS_PER_LANE; ++i) {
+            for (int i = 0; i < PL; ++i) {
                 const int e = lane + 32 * i;
                 if (e < E && !((taken >> i) & 1u)) {
                     if (l[i] > bv || (l[i] == bv && e < be)) {
@@ -313,7 +383,7 @@ __global__ void __launch_bounds__(RS_WARPS * 32) router_select_kernel(
             }
             ++R;
             if (R >= k + 1) {
-                const double gap = (double)prev_v - (double)bv;
+                const float gap = prev_v - bv;
                 if (!(gap <= thr)) break;
             }
             prev_v = bv;
@@ -325,7 +395,7 @@ __global__ void __launch_bounds__(RS_WARPS * 32) router_select_kernel(
         int a = 0;
         while (a < R && a < k) {
             int b = a;
-            while (b + 1 < R && ((double)s_v[b] - (double)s_v[b + 1]) <= thr) ++b;
+            while (b + 1 < R && (s_v[b] - s_v[b + 1]) <= thr) ++b;
             if (b > a) {
                 refined = true;
                 for (int m = a; m <= b; ++m) {
@@ -355,7 +425,7 @@ __global__ void __launch_bounds__(RS_WARPS * 32) router_select_kernel(
                     const float v = (float)s_ref[m];
                     if ((e & 31) == lane) {
 #pragma unroll
-                        for (int i = 0; i < RS_PER_LANE; ++i)
+                        for (int i = 0; i < PL; ++i)
                             if (i == (e >> 5)) l[i] = v;
                     }
                 }
@@ -367,13 +437,13 @@ __global__ void __launch_bounds__(RS_WARPS * 32) router_select_kernel(
         // softmax over all E, probabilities of the selected k
         float mx = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < RS_PER_LANE; ++i)
+        for (int i = 0; i < PL; ++i)
             if (lane + 32 * i < E) mx = fmaxf(mx, l[i]);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
         float z = 0.f;
 #pragma unroll
-        for (int i = 0; i < RS_PER_LANE; ++i)
+        for (int i = 0; i < PL; ++i)
             if (lane + 32 * i < E) z += expf(l[i] - mx);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
@@ -400,18 +470,31 @@ __global__ void __launch_bounds__(RS_WARPS * 32) router_select_kernel(
 
 }  // namespace
 
+// Split of H into K ranges: the CTAs run in waves of (resident CTAs per SM x
+// SMs), so pick the range length that minimises waves x (range + a fixed
+// per-CTA overhead of about three chunks).
 void router_plan(int64_t T, int H, int E, int num_sms, int* nsplit, int* KC) {
     const int64_t tT = (T + RT_BT - 1) / RT_BT;
     const int64_t tE = (E + RT_BE - 1) / RT_BE;
     const int64_t base = tT * tE;
-    const int64_t target = std::min<int64_t>(2 * (int64_t)num_sms, RT_TARGET_MAX);
-    int64_t ns = (target + base - 1) / base;
-    const int64_t ns_max = std::max(1, std::min(RT_MAX_SPLIT, H / 256));
-    ns = std::max<int64_t>(1, std::min(ns, ns_max));
-    int kc = (int)((H + ns - 1) / ns);
-    kc = (kc + RT_BK - 1) / RT_BK * RT_BK;
-    *KC = kc;
-    *nsplit = (H + kc - 1) / kc;
+    const int64_t slots = std::max<int64_t>(1, std::min<int64_t>(2 * (int64_t)num_sms, RT_TARGET_MAX));
+    int best_kc = H, best_ns = 1;
+    int64_t best_cost = INT64_MAX;
+    for (int kc = RT_BK; kc <= H; kc += RT_BK) {
+        const int ns = (H + kc - 1) / kc;
+        if (ns > RT_MAX_SPLIT) continue;
+        if ((int64_t)(ns - 1) * kc >= H) continue;  // same split as a shorter range
+        if (base * ns > RT_TARGET_MAX + base) continue;  // the workspace is sized for this bound
+        const int64_t waves = (base * ns + slots - 1) / slots;
+        const int64_t cost = waves * (kc + 3 * RT_BK);
+        if (cost < best_cost) {
+            best_cost = cost;
+            best_kc = kc;
+            best_ns = ns;
+        }
+    }
+    *KC = best_kc;
+    *nsplit = best_ns;
 }
 
 static size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
@@ -447,23 +530,50 @@ cudaError_t launch_router(const RouterLaunch& L, int num_sms, cudaStream_t s) {
     const int64_t tT = (L.T + RT_BT - 1) / RT_BT;
     const int tE = (L.E + RT_BE - 1) / RT_BE;
     dim3 grid1((unsigned)tT, (unsigned)tE, (unsigned)L.nsplit);
-    router_logits_kernel<<<grid1, RT_THREADS, 0, s>>>(L.x, L.Wg, L.T, L.H, L.E, L.KC, L.part, L.xsq, L.wsq);
-    cudaError_t err = cudaGetLastError();
+    cudaError_t err = cudaFuncSetAttribute(router_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)RT_SMEM);
+    if (err != cudaSuccess) return err;
+    router_logits_kernel<<<grid1, RT_THREADS, RT_SMEM, s>>>(L.x, L.Wg, L.T, L.H, L.E, L.KC, L.part, L.xsq, L.wsq);
+    err = cudaGetLastError();
     if (err != cudaSuccess) return err;
 
     // worst-case rounding depth of one logit: 32-term chunk, 8-chunk group,
     // groups in the CTA range, split partials, bias
     const int groups = (L.KC + RT_BK * RT_GROUP - 1) / (RT_BK * RT_GROUP);
-    const int chain_n = RT_BK + RT_GROUP + groups + L.nsplit + 1;
+    // rounding depth: the even/odd 16-term chains of a chunk, their sum, 8 chunks
+    // of a group, the groups of the range, the split partials, the bias
+    const int chain_n = RT_BK / 2 + 1 + RT_GROUP + groups + L.nsplit + 1;
+    // per-logit bound B_t = (gamma_n(fp32) + gamma_{H+2}(fp64)) * (||x_t|| max||w_e|| + max|b_e|);
+    // threshold on a gap = 2 B_t, with a 1 % margin that covers the fp32 evaluation
+    const double u32 = 1.0 / 16777216.0, u64 = 1.0 / 9007199254740992.0;
+    const double g32 = chain_n * u32 / (1.0 - chain_n * u32);
+    const double g64 = (L.H + 2.0) * u64 / (1.0 - (L.H + 2.0) * u64);
+    const float thr_coef = (float)(2.0 * (g32 + g64) * 1.01);
     const size_t smem = (size_t)RS_WARPS * L.E * (sizeof(double) + sizeof(int) + sizeof(float));
-    if (smem > 48 * 1024) {
-        err = cudaFuncSetAttribute(router_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (err != cudaSuccess) return err;
-    }
     const int64_t want = (L.T + RS_WARPS - 1) / RS_WARPS;
     const unsigned grid2 = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms * 8));
-    router_select_kernel<<<grid2, RS_WARPS * 32, smem, s>>>(L.part, L.xsq, L.wsq, L.nsplit, chain_n, L.bias, L.x,
-                                                             L.Wg, L.T, L.H, L.E, L.k, L.renorm, L.ids, L.w, L.hdr);
+#define MOE_SELECT(PLV)                                                                                          \
+    do {                                                                                                         \
+        if (smem > 48 * 1024) {                                                                                  \
+            err = cudaFuncSetAttribute(router_select_kernel<PLV>, cudaFuncAttributeMaxDynamicSharedMemorySize,  \
+                                       (int)smem);                                                               \
+            if (err != cudaSuccess) return err;                                                                  \
+        }                                                                                                        \
+        router_select_kernel<PLV><<<grid2, RS_WARPS * 32, smem, s>>>(L.part, L.xsq, L.wsq, L.nsplit, thr_coef,   \
+                                                                     L.bias, L.x, L.Wg, L.T, L.H, L.E, L.k,      \
+                                                                     L.renorm, L.ids, L.w, L.hdr);               \
+    } while (0)
+    if (L.E <= 32)
+        MOE_SELECT(1);
+    else if (L.E <= 64)
+        MOE_SELECT(2);
+    else if (L.E <= 128)
+        MOE_SELECT(4);
+    else if (L.E <= 256)
+        MOE_SELECT(8);
+    else
+        MOE_SELECT(16);
+#undef MOE_SELECT
     return cudaGetLastError();
 }
 

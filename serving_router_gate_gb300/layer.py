@@ -78,6 +78,32 @@ class MoELayer:
                     x if (self.I_sh > 0) else None, self.W1s, self.W2s, self.gate, v["out"], self.ws, stream)
         return v
 
+    def capture(self, x: torch.Tensor, pre=None, post=None) -> "torch.cuda.CUDAGraph":
+        """Record one forward (optionally wrapped by pre()/post() stream work, e.g.
+        host<->device copies) into a CUDA graph; replaying it re-runs the same
+        kernels with the same pointers.  Every library call is capturable: none
+        synchronises or allocates, and tensor maps are built on the host when the
+        call is recorded.  Run one forward outside capture first, so per-device
+        one-time set-up happens before recording."""
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            if pre:
+                pre()
+            self.forward(x)
+            if post:
+                post()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            if pre:
+                pre()
+            self.forward(x)
+            if post:
+                post()
+        return g
+
     def forward(self, x: torch.Tensor, stream=None) -> torch.Tensor:
         """out [T, H] bf16 (a view of the layer's output buffer) for x [T, H] bf16, T <= max_T."""
         assert x.shape[0] <= self.max_T and x.shape[1] == self.H

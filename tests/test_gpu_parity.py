@@ -119,6 +119,19 @@ def test_two_runs_are_bitwise_identical():
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
+def test_cuda_graph_replay_matches_eager_launches():
+    inp = mi.make_inputs(MID)
+    layer = layer_from_inputs(inp, "cuda")
+    x = inp["x"].cuda()
+    eager = layer.forward(x).clone()
+    g = layer.capture(x)
+    layer.out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(layer.out.view(torch.int16), eager.view(torch.int16))
+    assert moe.moe_get_device_status(layer.ws) == 0
+
+
 def test_replica_table_equals_identity_map():
     cfg = mi.MoEConfig("rep2", T=500, H=256, I=256, E=10, S=13, n_hot=3, k=3, renorm=True)
     inp = mi.make_inputs(cfg)
