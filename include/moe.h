@@ -269,6 +269,17 @@ MOE_API moe_status_t moe_debug_wait_timeout(void *ws, size_t ws_bytes, uint64_t 
  * Process-wide; applies to launches made after the call. */
 MOE_API void moe_set_wait_timeout_ns(uint64_t timeout_ns);
 
+/* How the grouped GEMMs map tiles to CTAs (process-wide, for launches made
+ * after the call): 0 = (default) one CTA per 128-row tile (tcgen05.mma
+ * cta_group::1); 1 = CTA pairs (thread-block clusters of 2) running 2-SM MMAs
+ * (cta_group::2, M = 256: each SM stages its A rows and half of the weight
+ * tile) when the launch has at least 4 tiles per SM; 2 = CTA pairs whenever a
+ * launch has two or more tiles.  All modes give bitwise the same results.
+ * Pairs lose on ragged groups with an odd number of 128-row tiles (half a pair
+ * idles) and, on a power-capped GB300, on total energy, so 0 is the default.
+ * MOE_ERR_INVALID_ARG for other values. */
+MOE_API moe_status_t moe_set_gemm_pair_mode(int mode);
+
 #ifdef __cplusplus
 }
 #endif

@@ -23,7 +23,8 @@ __all__ = [
     "MOE_ERR_DEVICE_BOUNDS", "MOE_ERR_TIMEOUT", "MOE_NONLOCAL_SKIP", "MOE_NONLOCAL_MOD", "MoEError",
     "lib_path", "moe_workspace_size", "moe_workspace_init", "moe_get_device_status", "moe_get_route_stats",
     "moe_route", "moe_permute", "moe_forward", "moe_grouped_fc1", "moe_grouped_fc2", "moe_finalize",
-    "moe_debug_wait_timeout", "moe_set_wait_timeout_ns", "moe_route_noalloc", "EXPORTED_SYMBOLS",
+    "moe_debug_wait_timeout", "moe_set_wait_timeout_ns", "moe_route_noalloc", "moe_set_gemm_pair_mode",
+    "EXPORTED_SYMBOLS",
 ]
 
 MOE_OK = 0
@@ -40,6 +41,7 @@ EXPORTED_SYMBOLS = (
     "moe_status_string", "moe_workspace_size", "moe_workspace_init", "moe_get_device_status",
     "moe_get_route_stats", "moe_route", "moe_permute", "moe_forward", "moe_grouped_fc1", "moe_grouped_fc2",
     "moe_finalize", "moe_debug_wait_timeout", "moe_set_wait_timeout_ns", "moe_route_noalloc",
+    "moe_set_gemm_pair_mode",
 )
 
 
@@ -74,6 +76,7 @@ def _load():
         "moe_debug_wait_timeout": ([P, sz, u64, P], i32),
         "moe_set_wait_timeout_ns": ([u64], None),
         "moe_route_noalloc": ([P, P, P, i64, i32, i32, i32, i32, P, P, P], i32),
+        "moe_set_gemm_pair_mode": ([i32], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -249,3 +252,8 @@ def moe_debug_wait_timeout(ws, timeout_ns, stream=None):
 
 def moe_set_wait_timeout_ns(timeout_ns: int) -> None:
     _lib.moe_set_wait_timeout_ns(int(timeout_ns))
+
+
+def moe_set_gemm_pair_mode(mode: int) -> None:
+    """0: one CTA per tile (default); 1: 2-SM CTA pairs for large launches; 2: pairs whenever possible."""
+    _check("moe_set_gemm_pair_mode", _lib.moe_set_gemm_pair_mode(int(mode)))

@@ -12,6 +12,7 @@ using namespace moe;
 namespace {
 
 std::atomic<uint64_t> g_timeout_ns{4000000000ull};
+std::atomic<int> g_pair_mode{0};
 
 int device_sms() {
     static std::mutex mu;
@@ -73,6 +74,12 @@ const char* moe_status_string(int status) {
 }
 
 void moe_set_wait_timeout_ns(uint64_t timeout_ns) { g_timeout_ns.store(timeout_ns > 0 ? timeout_ns : 1); }
+
+moe_status_t moe_set_gemm_pair_mode(int mode) {
+    if (mode < 0 || mode > 2) return MOE_ERR_INVALID_ARG;
+    g_pair_mode.store(mode);
+    return MOE_OK;
+}
 
 size_t moe_workspace_size(int64_t max_T, int H, int I, int E, int S, int k, int I_shared_total) {
     if (max_T < 0 || !dim_ok(H) || !dim_ok(I) || E < 1 || E > 512 || S < 1 || S > 1024 || k < 1 || k > 32 ||
@@ -215,6 +222,7 @@ static moe_status_t gemm_call(bool fc1, const moe_bf16_t* a, int64_t rows_cap, c
     L.out_sh = out_sh;
     L.hdr = static_cast<WsHeader*>(ws);
     L.timeout_ns = g_timeout_ns.load();
+    L.pair_mode = g_pair_mode.load();
     const char* why = nullptr;
     return cuda_status(launch_grouped_gemm(L, device_sms(), s, &why));
 }

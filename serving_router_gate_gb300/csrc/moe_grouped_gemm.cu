@@ -6,12 +6,12 @@
 // act_fn per expert); slots with no rows get no tiles (vLLM EP FusedMoE patch,
 // module docstring: the per-expert loop skips experts with count 0).
 //
-// Design (one CTA per SM, persistent, 192 threads):
+// Design (persistent, one CTA per SM, 192 threads, warp-specialised):
 //   warp 0      TMA producer: A tile [128 x 64] and B tile [256 x 64] (bf16,
 //               128-byte swizzle) per K step into a 4-stage shared-memory ring.
-//               FC1 loads the B tile as two 128-row halves -- gate rows n0.. and
-//               up rows I+n0.. -- so one MMA of N = 256 yields matching gate
-//               and up columns, with no weight re-layout.
+//               FC1's B tile is two 128-row halves -- gate rows n0.. and up
+//               rows I+n0.. -- so one MMA of N = 256 yields matching gate and
+//               up columns, with no weight re-layout.
 //   warp 1      tensor memory allocator (512 columns = 2 accumulators of
 //               256 fp32 columns) and, on one thread, the MMA issuer:
 //               tcgen05.mma.cta_group::1.kind::f16 M=128 N=256 K=16, four per
@@ -21,6 +21,16 @@
 //               FC2: y = bf16(acc); 16-byte stores; rows past the slot's count
 //               are not stored.  Two accumulators let the epilogue of one tile
 //               overlap the main loop of the next.
+// Pair mode (kPair, clusters of 2 CTAs): one tcgen05.mma.cta_group::2 of
+// M = 256 spans the pair.  Each CTA stages its own 128 rows of A and one
+// 128-row half of the B tile (32 KB per stage instead of 48, 6 stages), so every
+// weight byte is read once per pair and each SM's shared memory carries half of
+// B.  The leader (rank 0) issues the MMAs; both CTAs' copies are counted on the
+// leader's stage barriers, its commits are multicast to both CTAs, and both
+// CTAs' epilogues release the leader's accumulator barriers.  The two CTAs take
+// consecutive m-tiles of one (slot, n-tile); an odd leftover m-tile leaves the
+// second CTA without rows (its half is computed and discarded).  Single mode
+// (one CTA per tile, 4 stages of 48 KB) serves small launches.
 // Tiles: an optional dense "shared expert" problem (M = T) first, then the
 // routed problem, whose ragged per-slot row counts are read on the device from
 // the offsets array (no host synchronisation): slot g has ceil(M_g / 128)
@@ -38,18 +48,26 @@
 namespace moe {
 namespace {
 
-constexpr int BM = 128;
+constexpr int BM = 128;            // rows of A per CTA
 constexpr int BN = 256;            // MMA N
 constexpr int BK = 64;             // bf16 elements per 128-byte swizzle row
 constexpr int UMMA_K = 16;
-constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = BN * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int NUM_THREADS = 192;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int MAX_GROUPS = 1024;
-constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+constexpr int MAX_STAGES = 6;
+constexpr uint16_t PAIR_MASK = 0x3;
+
+// per mode: a CTA holds all of B (single) or its 128-row half (pair)
+template <bool kPair>
+struct Cfg {
+    static constexpr int B_BYTES = (kPair ? BN / 2 : BN) * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = kPair ? 6 : 4;
+    // 2-CTA MMA: M = 256 across the pair
+    static constexpr uint32_t IDESC = idesc_bf16_f32(kPair ? 2 * BM : BM, BN);
+};
 
 struct GemmParams {
     const int32_t* offsets;  // [G+1] routed row offsets (device)
@@ -66,8 +84,8 @@ struct GemmParams {
 };
 
 struct SmemMeta {
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
+    uint64_t full[MAX_STAGES];
+    uint64_t empty[MAX_STAGES];
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t drain;
@@ -78,26 +96,36 @@ struct SmemMeta {
     int ts[MAX_GROUPS + 1];
 };
 
-constexpr size_t SMEM_BYTES = 1024 /*alignment slack*/ + (size_t)STAGES * STAGE_BYTES + sizeof(SmemMeta);
+template <bool kPair>
+constexpr size_t smem_bytes() {
+    return 1024 /*alignment slack*/ + (size_t)Cfg<kPair>::STAGES * Cfg<kPair>::STAGE_BYTES + sizeof(SmemMeta);
+}
 
 struct Tile {
     int prob;        // 0 routed, 1 shared
     int g;           // routed group
     int nt;          // n-tile
-    int row0;        // first row in A / out
-    int rows_valid;  // rows of this tile that belong to the group
+    int row0;        // first row in A / out of this CTA's m-tile
+    int rows_valid;  // rows of this CTA's m-tile that belong to the group (may be 0)
 };
 
-template <bool kFC1>
-__device__ __forceinline__ Tile tile_of(int u, const GemmParams& p, const SmemMeta& m, int n_sh_tiles, int mt_sh) {
+// work units along M: pairs of m-tiles in pair mode, single m-tiles otherwise
+template <bool kPair>
+__device__ __forceinline__ int units_of(int mtiles) {
+    return kPair ? (mtiles + 1) >> 1 : mtiles;
+}
+
+template <bool kFC1, bool kPair>
+__device__ __forceinline__ Tile tile_of(int u, const GemmParams& p, const SmemMeta& m, int n_sh_tiles, int mu_sh,
+                                        int crank) {
     Tile tl;
     if (u < n_sh_tiles) {
         tl.prob = 1;
         tl.g = 0;
-        tl.nt = u / mt_sh;
-        const int mt = u % mt_sh;
+        tl.nt = u / mu_sh;
+        const int mt = kPair ? 2 * (u % mu_sh) + crank : u % mu_sh;
         tl.row0 = mt * BM;
-        tl.rows_valid = (int)min((int64_t)BM, p.T_sh - (int64_t)mt * BM);
+        tl.rows_valid = (int)max((int64_t)0, min((int64_t)BM, p.T_sh - (int64_t)mt * BM));
         return tl;
     }
     u -= n_sh_tiles;
@@ -112,21 +140,25 @@ __device__ __forceinline__ Tile tile_of(int u, const GemmParams& p, const SmemMe
     const int g = lo;
     const int local = u - m.ts[g];
     const int M = m.off[g + 1] - m.off[g];
-    const int MT = (M + BM - 1) / BM;
+    const int MU = units_of<kPair>((M + BM - 1) / BM);
     tl.prob = 0;
     tl.g = g;
-    tl.nt = local / MT;
-    const int mt = local % MT;
+    tl.nt = local / MU;
+    const int mt = kPair ? 2 * (local % MU) + crank : local % MU;
     tl.row0 = m.off[g] + mt * BM;
-    tl.rows_valid = min(BM, M - mt * BM);
+    tl.rows_valid = max(0, min(BM, M - mt * BM));
     return tl;
 }
 
-template <bool kFC1>
+template <bool kFC1, bool kPair>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmAs,
                         const __grid_constant__ CUtensorMap tmBs) {
+    constexpr int STAGES = Cfg<kPair>::STAGES;
+    constexpr int B_BYTES = Cfg<kPair>::B_BYTES;
+    constexpr int STAGE_BYTES = Cfg<kPair>::STAGE_BYTES;
+    constexpr uint32_t IDESC = Cfg<kPair>::IDESC;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t* smA = smem;
@@ -136,16 +168,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     constexpr int OW = kFC1 ? BN / 2 : BN;
+    const int crank = kPair ? (int)cluster_ctarank() : 0;
+    const int unit0 = kPair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int nunits = kPair ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
     // ---------------- prologue ----------------
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&m.full[s], 1);
-            mbar_init(&m.empty[s], 1);
+            mbar_init(&m.full[s], 1);   // pair mode: only the leader's, fed by both CTAs' copies
+            mbar_init(&m.empty[s], 1);  // released by the (leader's) MMA commit
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&m.tfull[b], 1);
-            mbar_init(&m.tempty[b], 4);
+            mbar_init(&m.tempty[b], kPair ? 8 : 4);  // pair mode: the epilogue warps of both CTAs
         }
         mbar_init(&m.drain, 1);
         m.abort = 0;
@@ -156,11 +191,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tma_prefetch_desc(&tmBs);
     }
     if (warp == 1) {
-        tmem_alloc(&m.tmem_base, TMEM_COLS);
-        tmem_relinquish();
+        if (kPair) {
+            tmem_alloc_pair(&m.tmem_base, TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(&m.tmem_base, TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     if (warp == 2) {
-        // routed tile prefix: ts[g] = NT * sum_{g' < g} ceil(M_g' / BM)
+        // routed unit prefix: ts[g] = NT * sum_{g' < g} units(ceil(M_g' / BM))
         const int G = p.G;
         const int NT = (p.N_out + OW - 1) / OW;
         for (int i = lane; i <= G; i += 32) m.off[i] = (G > 0) ? p.offsets[i] : 0;
@@ -173,7 +213,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int beg = min(G, lane * C), end = min(G, beg + C);
         int local = 0;
         if (ok)
-            for (int g = beg; g < end; ++g) local += ((m.off[g + 1] - m.off[g] + BM - 1) / BM) * NT;
+            for (int g = beg; g < end; ++g) local += units_of<kPair>((m.off[g + 1] - m.off[g] + BM - 1) / BM) * NT;
         int incl = local;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -183,7 +223,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         int run = incl - local;
         for (int g = beg; g < end; ++g) {
             m.ts[g] = run;
-            if (ok) run += ((m.off[g + 1] - m.off[g] + BM - 1) / BM) * NT;
+            if (ok) run += units_of<kPair>((m.off[g + 1] - m.off[g] + BM - 1) / BM) * NT;
         }
         const int total = __shfl_sync(0xffffffffu, incl, 31);
         if (lane == 0) {
@@ -193,12 +233,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     }
     tc_fence_before();
-    __syncthreads();
+    if (kPair) {
+        __syncwarp();        // barrier.cluster.*.aligned: each warp arrives converged
+        cluster_sync_all();  // the peer's multicasts may target this CTA's barriers from here on
+    } else {
+        __syncthreads();
+    }
     tc_fence_after();
 
     const uint32_t tmem_base = m.tmem_base;
-    const int mt_sh = p.T_sh > 0 ? (int)((p.T_sh + BM - 1) / BM) : 0;
-    const int n_sh_tiles = p.T_sh > 0 ? mt_sh * ((p.N_out_sh + OW - 1) / OW) : 0;
+    const int mu_sh = p.T_sh > 0 ? units_of<kPair>((int)((p.T_sh + BM - 1) / BM)) : 0;
+    const int n_sh_tiles = p.T_sh > 0 ? mu_sh * ((p.N_out_sh + OW - 1) / OW) : 0;
     const int total_tiles = n_sh_tiles + m.routed_tiles;
     const volatile int* abortp = &m.abort;
 
@@ -208,8 +253,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t stage = 0, phase = 0;
             int64_t issued = 0;
             bool failed = false;
-            for (int u = blockIdx.x; u < total_tiles && !failed; u += gridDim.x) {
-                const Tile tl = tile_of<kFC1>(u, p, m, n_sh_tiles, mt_sh);
+            for (int u = unit0; u < total_tiles && !failed; u += nunits) {
+                const Tile tl = tile_of<kFC1, kPair>(u, p, m, n_sh_tiles, mu_sh, crank);
                 const CUtensorMap* mA = tl.prob ? &tmAs : &tmA;
                 const CUtensorMap* mB = tl.prob ? &tmBs : &tmB;
                 const int nkb = (tl.prob ? p.K_sh : p.K) / BK;
@@ -219,14 +264,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         failed = true;
                         break;
                     }
-                    mbar_arrive_expect_tx(&m.full[stage], STAGE_BYTES);
                     uint8_t* a_dst = smA + (size_t)stage * A_BYTES;
                     uint8_t* b_dst = smB + (size_t)stage * B_BYTES;
-                    tma_load_2d(a_dst, mA, &m.full[stage], kb * BK, tl.row0);
-                    if (kFC1) {
+                    if (kPair) {
+                        // this CTA's A rows and its 128-row half of B; the bytes of both
+                        // CTAs are counted on the leader's stage barrier
+                        const uint32_t lead_full = mapa_shared(&m.full[stage], 0);
+                        if (crank == 0) mbar_arrive_expect_tx(&m.full[stage], 2 * STAGE_BYTES);
+                        const int brow = kFC1 ? (crank ? up : 0) + tl.nt * (BN / 2) : tl.nt * BN + crank * (BN / 2);
+                        tma_load_2d_pair(a_dst, mA, lead_full, kb * BK, tl.row0);
+                        tma_load_3d_pair(b_dst, mB, lead_full, kb * BK, brow, tl.g);
+                    } else if (kFC1) {
+                        mbar_arrive_expect_tx(&m.full[stage], STAGE_BYTES);
+                        tma_load_2d(a_dst, mA, &m.full[stage], kb * BK, tl.row0);
                         tma_load_3d(b_dst, mB, &m.full[stage], kb * BK, tl.nt * (BN / 2), tl.g);
                         tma_load_3d(b_dst + B_BYTES / 2, mB, &m.full[stage], kb * BK, up + tl.nt * (BN / 2), tl.g);
                     } else {
+                        mbar_arrive_expect_tx(&m.full[stage], STAGE_BYTES);
+                        tma_load_2d(a_dst, mA, &m.full[stage], kb * BK, tl.row0);
                         tma_load_3d(b_dst, mB, &m.full[stage], kb * BK, tl.nt * BN, tl.g);
                     }
                     ++issued;
@@ -239,19 +294,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (failed) {
                 m.abort = 1;
                 report(p.status, MOE_ERR_TIMEOUT);
-                // let the copies still in flight land before the CTA may exit
-                for (int64_t j = (issued > STAGES ? issued - STAGES : 0); j < issued; ++j)
-                    (void)mbar_wait(&m.full[j % STAGES], (uint32_t)((j / STAGES) & 1), p.timeout_ns, nullptr);
+                // let the copies still in flight land before the CTA may exit (in pair
+                // mode both CTAs' copies complete on the leader's barriers)
+                if (!kPair || crank == 0)
+                    for (int64_t j = (issued > STAGES ? issued - STAGES : 0); j < issued; ++j)
+                        (void)mbar_wait(&m.full[j % STAGES], (uint32_t)((j / STAGES) & 1), p.timeout_ns, nullptr);
+            }
+            // tail: wait until the MMAs have released the last stages, so no commit
+            // arrival can target this CTA after it exits
+            for (int j = 0; j < STAGES; ++j) {
+                (void)mbar_wait(&m.empty[stage], phase ^ 1u, p.timeout_ns, nullptr);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ---------------- MMA issuer ----------------
+        if (lane == 0 && crank == 0) {
+            // ---------------- MMA issuer (the pair's leader in pair mode) ----------------
             uint32_t stage = 0, phase = 0;
             bool failed = false;
             int i = 0;
-            for (int u = blockIdx.x; u < total_tiles && !failed; u += gridDim.x, ++i) {
-                const Tile tl = tile_of<kFC1>(u, p, m, n_sh_tiles, mt_sh);
+            for (int u = unit0; u < total_tiles && !failed; u += nunits, ++i) {
+                const Tile tl = tile_of<kFC1, kPair>(u, p, m, n_sh_tiles, mu_sh, crank);
                 const int nkb = (tl.prob ? p.K_sh : p.K) / BK;
                 const int buf = i & 1;
                 if (!mbar_wait(&m.tempty[buf], (uint32_t)(((i >> 1) & 1) ^ 1), p.timeout_ns, abortp)) {
@@ -270,24 +336,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint32_t b0 = smem_u32(smB + (size_t)stage * B_BYTES);
 #pragma unroll
                     for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                        tc_mma_bf16(d, sw128_kmajor_desc(a0 + kk * UMMA_K * 2), sw128_kmajor_desc(b0 + kk * UMMA_K * 2),
-                                    IDESC, (kb | kk) != 0 ? 1u : 0u);
+                        const uint64_t ad = sw128_kmajor_desc(a0 + kk * UMMA_K * 2);
+                        const uint64_t bd = sw128_kmajor_desc(b0 + kk * UMMA_K * 2);
+                        if (kPair)
+                            tc_mma_bf16_pair(d, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+                        else
+                            tc_mma_bf16(d, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
                     }
-                    tc_commit(&m.empty[stage]);
+                    if (kPair)
+                        tc_commit_pair_multicast(&m.empty[stage], PAIR_MASK);
+                    else
+                        tc_commit(&m.empty[stage]);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (failed) break;
-                tc_commit(&m.tfull[buf]);
+                if (kPair)
+                    tc_commit_pair_multicast(&m.tfull[buf], PAIR_MASK);
+                else
+                    tc_commit(&m.tfull[buf]);
             }
             if (failed) {
                 m.abort = 1;
                 report(p.status, MOE_ERR_TIMEOUT);
             }
             // all MMAs issued by this thread complete before TMEM is freed
-            tc_commit(&m.drain);
+            if (kPair)
+                tc_commit_pair_multicast(&m.drain, 0x1);
+            else
+                tc_commit(&m.drain);
             (void)mbar_wait(&m.drain, 0, p.timeout_ns, nullptr);
         }
     } else {
@@ -295,8 +374,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int q = warp & 3;              // TMEM lane quarter of this warp
         const int row_in = q * 32 + lane;    // tile row of this thread
         int i = 0;
-        for (int u = blockIdx.x; u < total_tiles; u += gridDim.x, ++i) {
-            const Tile tl = tile_of<kFC1>(u, p, m, n_sh_tiles, mt_sh);
+        for (int u = unit0; u < total_tiles; u += nunits, ++i) {
+            const Tile tl = tile_of<kFC1, kPair>(u, p, m, n_sh_tiles, mu_sh, crank);
             const int buf = i & 1;
             // every lane polls; the warp proceeds (reconverged, as tcgen05.ld
             // .sync.aligned requires) only if all lanes saw the phase complete
@@ -364,17 +443,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&m.tempty[buf]);
+            if (lane == 0) {
+                if (kPair)
+                    mbar_arrive_cluster(mapa_shared(&m.tempty[buf], 0));  // the leader's barrier
+                else
+                    mbar_arrive(&m.tempty[buf]);
+            }
         }
     }
 
     // ---------------- teardown ----------------
     tc_fence_before();
-    __syncthreads();
+    if (kPair) {
+        __syncwarp();        // lane 0 of warps 0 and 1 arrives late from its role loop
+        cluster_sync_all();  // neither CTA leaves while its peer may still address it
+    } else {
+        __syncthreads();
+    }
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem_base, TMEM_COLS);
+        if (kPair)
+            tmem_dealloc_pair(tmem_base, TMEM_COLS);
+        else
+            tmem_dealloc(tmem_base, TMEM_COLS);
     }
 }
 
@@ -431,20 +523,67 @@ bool encode_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Raise the dynamic shared-memory limit of a kernel instantiation once per device.
-template <bool kFC1>
-cudaError_t configure_once() {
+// Per-device launch facts of one kernel instantiation: shared-memory limit set,
+// and (pair mode) how many 2-CTA clusters can be resident at once.
+struct KernelInfo {
+    bool ready = false;
+    int max_clusters = 0;
+};
+
+template <bool kFC1, bool kPair>
+cudaError_t kernel_info(int num_sms, KernelInfo* out) {
     static std::mutex mu;
-    static bool done[64] = {};
+    static KernelInfo info[64];
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(mu);
-    if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
-    err = cudaFuncSetAttribute(grouped_gemm_kernel<kFC1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)SMEM_BYTES);
-    if (err == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
-    return err;
+    if (!info[dev].ready) {
+        err = cudaFuncSetAttribute(grouped_gemm_kernel<kFC1, kPair>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)smem_bytes<kPair>());
+        if (err != cudaSuccess) return err;
+        int clusters = 0;
+        if (kPair) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(2 * num_sms);
+            cfg.blockDim = dim3(NUM_THREADS);
+            cfg.dynamicSmemBytes = smem_bytes<kPair>();
+            cudaLaunchAttribute attr;
+            attr.id = cudaLaunchAttributeClusterDimension;
+            attr.val.clusterDim.x = 2;
+            attr.val.clusterDim.y = 1;
+            attr.val.clusterDim.z = 1;
+            cfg.attrs = &attr;
+            cfg.numAttrs = 1;
+            err = cudaOccupancyMaxActiveClusters(&clusters, grouped_gemm_kernel<kFC1, kPair>, &cfg);
+            if (err != cudaSuccess) return err;
+        }
+        info[dev].max_clusters = clusters;
+        info[dev].ready = true;
+    }
+    *out = info[dev];
+    return cudaSuccess;
+}
+
+template <bool kFC1, bool kPair>
+cudaError_t launch_kernel(const GemmParams& p, const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mAs,
+                          const CUtensorMap& mBs, unsigned grid, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = smem_bytes<kPair>();
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    if (kPair) {
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = 2;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<kFC1, kPair>, p, mA, mB, mAs, mBs);
 }
 
 }  // namespace
@@ -457,7 +596,15 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& L, int num_sms, cudaStream_t s
         *why = "too many groups";
         return cudaErrorInvalidValue;
     }
-    const uint32_t brows = L.swiglu ? BN / 2 : BN;
+    const int ow = L.swiglu ? BN / 2 : BN;
+    // upper bound of single-mode tiles; pairs pay off when there are enough of them
+    int64_t bound = 0;
+    if (has_routed) bound += (int64_t)((L.N_out + ow - 1) / ow) * ((L.rows_cap + BM - 1) / BM + L.G);
+    if (has_shared) bound += (int64_t)((L.N_out_sh + ow - 1) / ow) * ((L.T_sh + BM - 1) / BM);
+    const bool pair = L.pair_mode == 2 ? bound >= 2 : (L.pair_mode == 1 && bound >= 4 * (int64_t)num_sms);
+
+    // B boxes: 128 rows (FC1 gate/up halves, or any half in pair mode), else 256
+    const uint32_t brows = (L.swiglu || pair) ? BN / 2 : BN;
     CUtensorMap mA, mB, mAs, mBs;
     bool ok = true;
     if (has_routed) {
@@ -496,22 +643,32 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& L, int num_sms, cudaStream_t s
     p.status = &L.hdr->status;
     p.timeout_ns = L.timeout_ns;
 
-    const int ow = L.swiglu ? BN / 2 : BN;
-    int64_t bound = 0;
-    if (has_routed) bound += (int64_t)((L.N_out + ow - 1) / ow) * ((L.rows_cap + BM - 1) / BM + L.G);
-    if (has_shared) bound += (int64_t)((L.N_out_sh + ow - 1) / ow) * ((L.T_sh + BM - 1) / BM);
-    const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(bound, num_sms));
-
-    cudaError_t err = L.swiglu ? configure_once<true>() : configure_once<false>();
+    KernelInfo info;
+    cudaError_t err;
+    if (L.swiglu)
+        err = pair ? kernel_info<true, true>(num_sms, &info) : kernel_info<true, false>(num_sms, &info);
+    else
+        err = pair ? kernel_info<false, true>(num_sms, &info) : kernel_info<false, false>(num_sms, &info);
     if (err != cudaSuccess) {
-        *why = "cudaFuncSetAttribute(max dynamic shared memory) failed";
+        *why = "kernel attribute / occupancy query failed";
         return err;
     }
+    unsigned grid;
+    if (pair) {
+        const int64_t units = (bound + 1) / 2;
+        const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(units, std::max(1, info.max_clusters)));
+        grid = (unsigned)(2 * clusters);
+    } else {
+        grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(bound, num_sms));
+    }
     if (L.swiglu)
-        grouped_gemm_kernel<true><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(p, mA, mB, mAs, mBs);
+        err = pair ? launch_kernel<true, true>(p, mA, mB, mAs, mBs, grid, s)
+                   : launch_kernel<true, false>(p, mA, mB, mAs, mBs, grid, s);
     else
-        grouped_gemm_kernel<false><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(p, mA, mB, mAs, mBs);
-    return cudaGetLastError();
+        err = pair ? launch_kernel<false, true>(p, mA, mB, mAs, mBs, grid, s)
+                   : launch_kernel<false, false>(p, mA, mB, mAs, mBs, grid, s);
+    if (err != cudaSuccess) *why = "launch failed";
+    return err;
 }
 
 cudaError_t launch_wait_timeout_probe(WsHeader* hdr, uint64_t timeout_ns, cudaStream_t s) {

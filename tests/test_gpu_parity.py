@@ -119,6 +119,25 @@ def test_two_runs_are_bitwise_identical():
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
+@pytest.mark.parametrize("mode", [0, 2])
+def test_gemm_tile_modes_single_and_pairs(mode):
+    # pairs of CTAs sharing weight tiles by multicast (mode 2 forces them on a
+    # mid-size layer: groups with odd and even m-tile counts, shared problem
+    # with an odd count) and single CTAs must give the same results
+    cfg = mi.MoEConfig("pairs", T=1400, H=512, I=384, E=6, k=3, renorm=True, n_shared=1, I_shared=384,
+                       shared_gate=True)
+    inp = mi.make_inputs(cfg)
+    try:
+        moe.moe_set_gemm_pair_mode(mode)
+        g, _ = _full_check(inp)
+        ref0 = g["out"]
+        moe.moe_set_gemm_pair_mode(0 if mode else 2)
+        g2 = run_gpu(inp)
+        assert torch.equal(g2["out"].view(torch.int16), ref0.view(torch.int16))
+    finally:
+        moe.moe_set_gemm_pair_mode(1)
+
+
 def test_cuda_graph_replay_matches_eager_launches():
     inp = mi.make_inputs(MID)
     layer = layer_from_inputs(inp, "cuda")
