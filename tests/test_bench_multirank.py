@@ -1,0 +1,49 @@
+"""The bench's multi-rank host logic on CPU with world size 2 (gloo): the step
+time is the maximum over ranks and the throughput counts every rank's tokens."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        import bench
+        ms_local = [3.0, 5.0][rank]           # rank 1 is the slower one
+        value, ms = bench.aggregate_throughput(4096, ms_local, world)
+        q.put((rank, value, ms, bench.max_over_ranks(float(rank), world)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_and_whole_job_throughput_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, value, ms, mx in res:
+        assert ms == 5.0 and mx == 1.0
+        assert value == pytest.approx(2 * 4096 / 5e-3)
+
+
+def test_single_rank_is_local_time():
+    import bench
+    value, ms = bench.aggregate_throughput(100, 2.0, 1)
+    assert ms == 2.0 and value == pytest.approx(100 / 2e-3)
