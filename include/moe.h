@@ -280,6 +280,12 @@ MOE_API void moe_set_wait_timeout_ns(uint64_t timeout_ns);
  * MOE_ERR_INVALID_ARG for other values. */
 MOE_API moe_status_t moe_set_gemm_pair_mode(int mode);
 
+/* 1 (default): launch the layer's kernels with programmatic dependent launch,
+ * so each kernel's launch and set-up overlap the end of the previous one (each
+ * still waits for its predecessor before touching memory); 0: plain stream
+ * order.  Process-wide; results are identical.  MOE_ERR_INVALID_ARG otherwise. */
+MOE_API moe_status_t moe_set_pdl(int enable);
+
 #ifdef __cplusplus
 }
 #endif

@@ -24,7 +24,7 @@ __all__ = [
     "lib_path", "moe_workspace_size", "moe_workspace_init", "moe_get_device_status", "moe_get_route_stats",
     "moe_route", "moe_permute", "moe_forward", "moe_grouped_fc1", "moe_grouped_fc2", "moe_finalize",
     "moe_debug_wait_timeout", "moe_set_wait_timeout_ns", "moe_route_noalloc", "moe_set_gemm_pair_mode",
-    "EXPORTED_SYMBOLS",
+    "moe_set_pdl", "EXPORTED_SYMBOLS",
 ]
 
 MOE_OK = 0
@@ -41,7 +41,7 @@ EXPORTED_SYMBOLS = (
     "moe_status_string", "moe_workspace_size", "moe_workspace_init", "moe_get_device_status",
     "moe_get_route_stats", "moe_route", "moe_permute", "moe_forward", "moe_grouped_fc1", "moe_grouped_fc2",
     "moe_finalize", "moe_debug_wait_timeout", "moe_set_wait_timeout_ns", "moe_route_noalloc",
-    "moe_set_gemm_pair_mode",
+    "moe_set_gemm_pair_mode", "moe_set_pdl",
 )
 
 
@@ -77,6 +77,7 @@ def _load():
         "moe_set_wait_timeout_ns": ([u64], None),
         "moe_route_noalloc": ([P, P, P, i64, i32, i32, i32, i32, P, P, P], i32),
         "moe_set_gemm_pair_mode": ([i32], i32),
+        "moe_set_pdl": ([i32], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -252,6 +253,11 @@ def moe_debug_wait_timeout(ws, timeout_ns, stream=None):
 
 def moe_set_wait_timeout_ns(timeout_ns: int) -> None:
     _lib.moe_set_wait_timeout_ns(int(timeout_ns))
+
+
+def moe_set_pdl(enable: bool) -> None:
+    """Launch kernels with programmatic dependent launch (default) or in plain stream order."""
+    _check("moe_set_pdl", _lib.moe_set_pdl(int(bool(enable))))
 
 
 def moe_set_gemm_pair_mode(mode: int) -> None:

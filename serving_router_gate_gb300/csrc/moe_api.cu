@@ -13,6 +13,7 @@ namespace {
 
 std::atomic<uint64_t> g_timeout_ns{4000000000ull};
 std::atomic<int> g_pair_mode{0};
+std::atomic<int> g_pdl{1};
 
 int device_sms() {
     static std::mutex mu;
@@ -57,6 +58,8 @@ moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE
 
 }  // namespace
 
+bool moe::pdl_enabled() { return g_pdl.load() != 0; }
+
 extern "C" {
 
 const char* moe_status_string(int status) {
@@ -74,6 +77,12 @@ const char* moe_status_string(int status) {
 }
 
 void moe_set_wait_timeout_ns(uint64_t timeout_ns) { g_timeout_ns.store(timeout_ns > 0 ? timeout_ns : 1); }
+
+moe_status_t moe_set_pdl(int enable) {
+    if (enable != 0 && enable != 1) return MOE_ERR_INVALID_ARG;
+    g_pdl.store(enable);
+    return MOE_OK;
+}
 
 moe_status_t moe_set_gemm_pair_mode(int mode) {
     if (mode < 0 || mode > 2) return MOE_ERR_INVALID_ARG;

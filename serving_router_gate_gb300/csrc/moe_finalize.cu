@@ -7,11 +7,12 @@
 // to the routed output (out = routed_out + shared_out).  The shared gate
 // sigmoid(x . w_s) is the Qwen2-MoE-style scaled shared expert.
 //
-// One warp per token (8 tokens per 256-thread CTA, grid-stride).  Lane j < k
-// holds pair j's row and weight and broadcasts them with shuffles.  Each lane
-// owns the 16-byte vectors lane, lane+32, ... of the row; it issues the loads
-// of up to 4 pairs' rows (and then of the shared-expert row) before using them,
-// and accumulates in fp32 in fixed j order:
+// One warp per work unit -- a token's whole row, or (few tokens) a 256-column
+// slice of it -- 8 warps per CTA, grid-stride.  Lane j < k holds pair j's row
+// and weight and broadcasts them with shuffles.  Each lane owns the 16-byte
+// vectors lane, lane+32, ... of the unit; it issues the loads of up to 8 pairs'
+// rows (and then of the shared-expert row) before using them, and accumulates
+// in fp32 in fixed j order:
 //   acc = fma(w_j, y[row_j], acc) for j = 0..k-1 (rows of -1 skipped),
 //   acc = fma(g, y_shared, acc), out = bf16_rn(acc).
 // The gate dot product x . w_s is a per-lane strided partial sum followed by a
@@ -24,18 +25,26 @@ namespace moe {
 namespace {
 
 constexpr int FZ_WARPS = 8;
-constexpr int FZ_UNROLL = 2;  // vectors per lane per pass
-constexpr int FZ_BATCH = 4;   // pairs whose loads are issued together
 
-__global__ void __launch_bounds__(FZ_WARPS * 32) finalize_kernel(
+// FZ_UNROLL vectors per lane per pass; FZ_BATCH pairs whose loads are issued
+// together (rows: 2 x 4; slices, one vector per lane: 1 x 8)
+template <int FZ_UNROLL, int FZ_BATCH>
+__global__ void __launch_bounds__(FZ_WARPS * 32, 3) finalize_kernel(
     const uint16_t* __restrict__ y, int64_t rows_cap, const int32_t* __restrict__ pair_row,
-    const float* __restrict__ w, int64_t T, int k, int H, const uint16_t* __restrict__ y_sh,
+    const float* __restrict__ w, int64_t T, int k, int H, int unit_cols, const uint16_t* __restrict__ y_sh,
     const uint16_t* __restrict__ x, const uint16_t* __restrict__ gate_w, uint16_t* __restrict__ out,
     int32_t* status) {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int vec = H / 8;
-    for (int64_t t = (int64_t)blockIdx.x * FZ_WARPS + warp; t < T; t += (int64_t)gridDim.x * FZ_WARPS) {
+    const int units_per_token = H / unit_cols;
+    const int64_t units = T * units_per_token;
+    for (int64_t un = (int64_t)blockIdx.x * FZ_WARPS + warp; un < units; un += (int64_t)gridDim.x * FZ_WARPS) {
+        const int64_t t = un / units_per_token;
+        const int v_beg = (int)(un % units_per_token) * (unit_cols / 8);
+        const int v_end = v_beg + unit_cols / 8;
         int64_t my_row = -1;
         float my_w = 0.f;
         if (lane < k) {
@@ -65,7 +74,7 @@ __global__ void __launch_bounds__(FZ_WARPS * 32) finalize_kernel(
         }
         uint4* orow = reinterpret_cast<uint4*>(out + t * H);
         const uint4* srow = y_sh ? reinterpret_cast<const uint4*>(y_sh + t * H) : nullptr;
-        for (int v0 = lane; v0 < vec; v0 += 32 * FZ_UNROLL) {
+        for (int v0 = v_beg + lane; v0 < v_end; v0 += 32 * FZ_UNROLL) {
             float acc[FZ_UNROLL][8];
 #pragma unroll
             for (int u = 0; u < FZ_UNROLL; ++u)
@@ -86,7 +95,7 @@ __global__ void __launch_bounds__(FZ_WARPS * 32) finalize_kernel(
 #pragma unroll
                     for (int u = 0; u < FZ_UNROLL; ++u) {
                         const int v = v0 + 32 * u;
-                        ld[b][u] = (use && v < vec) ? __ldg(yrow + v) : make_uint4(0, 0, 0, 0);
+                        ld[b][u] = (use && v < v_end) ? __ldg(yrow + v) : make_uint4(0, 0, 0, 0);
                     }
                 }
 #pragma unroll
@@ -107,7 +116,7 @@ __global__ void __launch_bounds__(FZ_WARPS * 32) finalize_kernel(
 #pragma unroll
                 for (int u = 0; u < FZ_UNROLL; ++u) {
                     const int v = v0 + 32 * u;
-                    ld[u] = v < vec ? __ldg(srow + v) : make_uint4(0, 0, 0, 0);
+                    ld[u] = v < v_end ? __ldg(srow + v) : make_uint4(0, 0, 0, 0);
                 }
 #pragma unroll
                 for (int u = 0; u < FZ_UNROLL; ++u) {
@@ -120,7 +129,7 @@ __global__ void __launch_bounds__(FZ_WARPS * 32) finalize_kernel(
 #pragma unroll
             for (int u = 0; u < FZ_UNROLL; ++u) {
                 const int v = v0 + 32 * u;
-                if (v < vec) {
+                if (v < v_end) {
                     uint4 o;
                     o.x = pack_bf16x2(acc[u][0], acc[u][1]);
                     o.y = pack_bf16x2(acc[u][2], acc[u][3]);
@@ -136,11 +145,19 @@ __global__ void __launch_bounds__(FZ_WARPS * 32) finalize_kernel(
 }  // namespace
 
 cudaError_t launch_finalize(const FinalizeLaunch& L, int num_sms, cudaStream_t s) {
-    const int64_t want = (L.T + FZ_WARPS - 1) / FZ_WARPS;
+    // work unit of one warp: a whole row when there are enough tokens to fill
+    // the GPU, else 256-column slices (each slice recomputes the gate dot)
+    int unit_cols = L.H;
+    if (L.T < 64LL * num_sms && L.H % 256 == 0) unit_cols = 256;
+    const int64_t units = L.T * (L.H / unit_cols);
+    const int64_t want = (units + FZ_WARPS - 1) / FZ_WARPS;
     const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms * 8));
-    finalize_kernel<<<grid, FZ_WARPS * 32, 0, s>>>(L.y, L.rows_cap, L.pair_row, L.w, L.T, L.k, L.H, L.y_sh, L.x,
-                                                   L.gate_w, L.out, L.hdr ? &L.hdr->status : nullptr);
-    return cudaGetLastError();
+    if (unit_cols == L.H)
+        return launch_k(finalize_kernel<2, 4>, dim3(grid), dim3(FZ_WARPS * 32), 0, s, L.y, L.rows_cap, L.pair_row,
+                        L.w, L.T, L.k, L.H, unit_cols, L.y_sh, L.x, L.gate_w, L.out,
+                        L.hdr ? &L.hdr->status : nullptr);
+    return launch_k(finalize_kernel<1, 8>, dim3(grid), dim3(FZ_WARPS * 32), 0, s, L.y, L.rows_cap, L.pair_row, L.w,
+                    L.T, L.k, L.H, unit_cols, L.y_sh, L.x, L.gate_w, L.out, L.hdr ? &L.hdr->status : nullptr);
 }
 
 }  // namespace moe

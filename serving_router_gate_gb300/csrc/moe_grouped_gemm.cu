@@ -8,7 +8,9 @@
 //
 // Design (persistent, one CTA per SM, 192 threads, warp-specialised):
 //   warp 0      TMA producer: A tile [128 x 64] and B tile [256 x 64] (bf16,
-//               128-byte swizzle) per K step into a 4-stage shared-memory ring.
+//               128-byte swizzle) per K step into a 4-stage shared-memory ring;
+//               a tile with at most 32 rows of its group loads only 32 A rows
+//               (the MMA reads all 128; the rest are never stored).
 //               FC1's B tile is two 128-row halves -- gate rows n0.. and up
 //               rows I+n0.. -- so one MMA of N = 256 yields matching gate and
 //               up columns, with no weight re-layout.
@@ -49,22 +51,25 @@ namespace moe {
 namespace {
 
 constexpr int BM = 128;            // rows of A per CTA
-constexpr int BN = 256;            // MMA N
 constexpr int BK = 64;             // bf16 elements per 128-byte swizzle row
 constexpr int UMMA_K = 16;
 constexpr int A_BYTES = BM * BK * 2;
+constexpr int BM_SHORT = 32;                      // A rows loaded for tiles with at most 32 rows
+constexpr int A_SHORT_BYTES = BM_SHORT * BK * 2;
 constexpr int NUM_THREADS = 192;
-constexpr int TMEM_COLS = 2 * BN;
 constexpr int MAX_GROUPS = 1024;
-constexpr int MAX_STAGES = 6;
+constexpr int MAX_STAGES = 8;
+constexpr int RING_BYTES = 192 * 1024;  // shared memory for the operand ring
 constexpr uint16_t PAIR_MASK = 0x3;
 
-// per mode: a CTA holds all of B (single) or its 128-row half (pair)
-template <bool kPair>
+// per instantiation: MMA N = BN (256 for large launches, 128 / 64 to spread
+// small ones over more CTAs); a CTA holds all of B (single) or its half (pair)
+template <bool kPair, int BN>
 struct Cfg {
     static constexpr int B_BYTES = (kPair ? BN / 2 : BN) * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = kPair ? 6 : 4;
+    static constexpr int STAGES = RING_BYTES / STAGE_BYTES < MAX_STAGES ? RING_BYTES / STAGE_BYTES : MAX_STAGES;
+    static constexpr int TMEM_COLS = 2 * BN;  // two accumulators of BN fp32 columns
     // 2-CTA MMA: M = 256 across the pair
     static constexpr uint32_t IDESC = idesc_bf16_f32(kPair ? 2 * BM : BM, BN);
 };
@@ -96,9 +101,9 @@ struct SmemMeta {
     int ts[MAX_GROUPS + 1];
 };
 
-template <bool kPair>
+template <bool kPair, int BN>
 constexpr size_t smem_bytes() {
-    return 1024 /*alignment slack*/ + (size_t)Cfg<kPair>::STAGES * Cfg<kPair>::STAGE_BYTES + sizeof(SmemMeta);
+    return 1024 /*alignment slack*/ + (size_t)Cfg<kPair, BN>::STAGES * Cfg<kPair, BN>::STAGE_BYTES + sizeof(SmemMeta);
 }
 
 struct Tile {
@@ -150,15 +155,18 @@ __device__ __forceinline__ Tile tile_of(int u, const GemmParams& p, const SmemMe
     return tl;
 }
 
-template <bool kFC1, bool kPair>
+template <bool kFC1, bool kPair, int BN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmAs,
-                        const __grid_constant__ CUtensorMap tmBs) {
-    constexpr int STAGES = Cfg<kPair>::STAGES;
-    constexpr int B_BYTES = Cfg<kPair>::B_BYTES;
-    constexpr int STAGE_BYTES = Cfg<kPair>::STAGE_BYTES;
-    constexpr uint32_t IDESC = Cfg<kPair>::IDESC;
+                        const __grid_constant__ CUtensorMap tmBs, const __grid_constant__ CUtensorMap tmA32,
+                        const __grid_constant__ CUtensorMap tmAs32) {
+    constexpr int STAGES = Cfg<kPair, BN>::STAGES;
+    constexpr int B_BYTES = Cfg<kPair, BN>::B_BYTES;
+    constexpr int STAGE_BYTES = Cfg<kPair, BN>::STAGE_BYTES;
+    constexpr uint32_t IDESC = Cfg<kPair, BN>::IDESC;
+    constexpr int TMEM_COLS = Cfg<kPair, BN>::TMEM_COLS;
+    static_assert(!kPair || BN == 256, "pair mode uses N = 256");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t* smA = smem;
@@ -189,6 +197,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tma_prefetch_desc(&tmB);
         tma_prefetch_desc(&tmAs);
         tma_prefetch_desc(&tmBs);
+        tma_prefetch_desc(&tmA32);
+        tma_prefetch_desc(&tmAs32);
     }
     if (warp == 1) {
         if (kPair) {
@@ -199,6 +209,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tmem_relinquish();
         }
     }
+    // everything above touches no memory of earlier kernels; from here on it may
+    pdl_wait();
+    pdl_trigger();
     if (warp == 2) {
         // routed unit prefix: ts[g] = NT * sum_{g' < g} units(ceil(M_g' / BM))
         const int G = p.G;
@@ -255,10 +268,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bool failed = false;
             for (int u = unit0; u < total_tiles && !failed; u += nunits) {
                 const Tile tl = tile_of<kFC1, kPair>(u, p, m, n_sh_tiles, mu_sh, crank);
-                const CUtensorMap* mA = tl.prob ? &tmAs : &tmA;
+                // a tile with at most 32 rows of its group loads only 32 A rows: the MMA
+                // still reads 128, but rows past the group's count are never stored
+                const bool short_a = tl.rows_valid <= BM_SHORT;
+                const CUtensorMap* mA = tl.prob ? (short_a ? &tmAs32 : &tmAs) : (short_a ? &tmA32 : &tmA);
                 const CUtensorMap* mB = tl.prob ? &tmBs : &tmB;
                 const int nkb = (tl.prob ? p.K_sh : p.K) / BK;
                 const int up = tl.prob ? p.up_off_sh : p.up_off;
+                const uint32_t a_bytes = short_a ? A_SHORT_BYTES : A_BYTES;
+                uint32_t pair_bytes = 0;  // pair mode: bytes of both CTAs, counted by the leader
+                if (kPair) {
+                    const Tile other = tile_of<kFC1, kPair>(u, p, m, n_sh_tiles, mu_sh, crank ^ 1);
+                    pair_bytes = a_bytes + (other.rows_valid <= BM_SHORT ? A_SHORT_BYTES : A_BYTES) + 2 * B_BYTES;
+                }
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (!mbar_wait(&m.empty[stage], phase ^ 1u, p.timeout_ns, abortp)) {
                         failed = true;
@@ -270,17 +292,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         // this CTA's A rows and its 128-row half of B; the bytes of both
                         // CTAs are counted on the leader's stage barrier
                         const uint32_t lead_full = mapa_shared(&m.full[stage], 0);
-                        if (crank == 0) mbar_arrive_expect_tx(&m.full[stage], 2 * STAGE_BYTES);
+                        if (crank == 0) mbar_arrive_expect_tx(&m.full[stage], pair_bytes);
                         const int brow = kFC1 ? (crank ? up : 0) + tl.nt * (BN / 2) : tl.nt * BN + crank * (BN / 2);
                         tma_load_2d_pair(a_dst, mA, lead_full, kb * BK, tl.row0);
                         tma_load_3d_pair(b_dst, mB, lead_full, kb * BK, brow, tl.g);
                     } else if (kFC1) {
-                        mbar_arrive_expect_tx(&m.full[stage], STAGE_BYTES);
+                        mbar_arrive_expect_tx(&m.full[stage], a_bytes + B_BYTES);
                         tma_load_2d(a_dst, mA, &m.full[stage], kb * BK, tl.row0);
                         tma_load_3d(b_dst, mB, &m.full[stage], kb * BK, tl.nt * (BN / 2), tl.g);
                         tma_load_3d(b_dst + B_BYTES / 2, mB, &m.full[stage], kb * BK, up + tl.nt * (BN / 2), tl.g);
                     } else {
-                        mbar_arrive_expect_tx(&m.full[stage], STAGE_BYTES);
+                        mbar_arrive_expect_tx(&m.full[stage], a_bytes + B_BYTES);
                         tma_load_2d(a_dst, mA, &m.full[stage], kb * BK, tl.row0);
                         tma_load_3d(b_dst, mB, &m.full[stage], kb * BK, tl.nt * BN, tl.g);
                     }
@@ -530,7 +552,7 @@ struct KernelInfo {
     int max_clusters = 0;
 };
 
-template <bool kFC1, bool kPair>
+template <bool kFC1, bool kPair, int BN>
 cudaError_t kernel_info(int num_sms, KernelInfo* out) {
     static std::mutex mu;
     static KernelInfo info[64];
@@ -540,15 +562,15 @@ cudaError_t kernel_info(int num_sms, KernelInfo* out) {
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(mu);
     if (!info[dev].ready) {
-        err = cudaFuncSetAttribute(grouped_gemm_kernel<kFC1, kPair>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)smem_bytes<kPair>());
+        err = cudaFuncSetAttribute(grouped_gemm_kernel<kFC1, kPair, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)smem_bytes<kPair, BN>());
         if (err != cudaSuccess) return err;
         int clusters = 0;
         if (kPair) {
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(2 * num_sms);
             cfg.blockDim = dim3(NUM_THREADS);
-            cfg.dynamicSmemBytes = smem_bytes<kPair>();
+            cfg.dynamicSmemBytes = smem_bytes<kPair, BN>();
             cudaLaunchAttribute attr;
             attr.id = cudaLaunchAttributeClusterDimension;
             attr.val.clusterDim.x = 2;
@@ -556,7 +578,7 @@ cudaError_t kernel_info(int num_sms, KernelInfo* out) {
             attr.val.clusterDim.z = 1;
             cfg.attrs = &attr;
             cfg.numAttrs = 1;
-            err = cudaOccupancyMaxActiveClusters(&clusters, grouped_gemm_kernel<kFC1, kPair>, &cfg);
+            err = cudaOccupancyMaxActiveClusters(&clusters, grouped_gemm_kernel<kFC1, kPair, BN>, &cfg);
             if (err != cudaSuccess) return err;
         }
         info[dev].max_clusters = clusters;
@@ -566,24 +588,126 @@ cudaError_t kernel_info(int num_sms, KernelInfo* out) {
     return cudaSuccess;
 }
 
-template <bool kFC1, bool kPair>
+template <bool kFC1, bool kPair, int BN>
 cudaError_t launch_kernel(const GemmParams& p, const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mAs,
-                          const CUtensorMap& mBs, unsigned grid, cudaStream_t s) {
+                          const CUtensorMap& mBs, const CUtensorMap& mA32, const CUtensorMap& mAs32, unsigned grid,
+                          cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(NUM_THREADS);
-    cfg.dynamicSmemBytes = smem_bytes<kPair>();
+    cfg.dynamicSmemBytes = smem_bytes<kPair, BN>();
     cfg.stream = s;
-    cudaLaunchAttribute attr;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
     if (kPair) {
-        attr.id = cudaLaunchAttributeClusterDimension;
-        attr.val.clusterDim.x = 2;
-        attr.val.clusterDim.y = 1;
-        attr.val.clusterDim.z = 1;
-        cfg.attrs = &attr;
-        cfg.numAttrs = 1;
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = 2;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
     }
-    return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<kFC1, kPair>, p, mA, mB, mAs, mBs);
+    if (pdl_enabled()) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<kFC1, kPair, BN>, p, mA, mB, mAs, mBs, mA32, mAs32);
+}
+
+// Tensor maps, parameters and grid of one launch with MMA N = BN.
+template <bool kFC1, bool kPair, int BN>
+cudaError_t launch_bn(const GemmLaunch& L, int num_sms, int64_t bound, cudaStream_t s, const char** why) {
+    const bool has_routed = L.G > 0 && L.rows_cap > 0;
+    const bool has_shared = L.T_sh > 0 && L.b_sh != nullptr && L.N_out_sh > 0;
+    // B boxes: FC1 loads gate and up halves of BN/2 rows; FC2 BN rows (pair: 128)
+    const uint32_t brows = kFC1 ? BN / 2 : (kPair ? BN / 2 : BN);
+    CUtensorMap mA, mB, mAs, mBs, mA32, mAs32;
+    bool ok = true;
+    if (has_routed) {
+        ok = ok && encode_2d(&mA, L.a, (uint64_t)L.K, (uint64_t)L.rows_cap, BM);
+        ok = ok && encode_2d(&mA32, L.a, (uint64_t)L.K, (uint64_t)L.rows_cap, BM_SHORT);
+        ok = ok && encode_3d(&mB, L.b, (uint64_t)L.K, (uint64_t)L.Nb, (uint64_t)L.G, brows);
+    }
+    if (has_shared) {
+        ok = ok && encode_2d(&mAs, L.a_sh, (uint64_t)L.K_sh, (uint64_t)L.T_sh, BM);
+        ok = ok && encode_2d(&mAs32, L.a_sh, (uint64_t)L.K_sh, (uint64_t)L.T_sh, BM_SHORT);
+        ok = ok && encode_3d(&mBs, L.b_sh, (uint64_t)L.K_sh, (uint64_t)L.Nb_sh, 1, brows);
+    }
+    if (!ok) {
+        *why = "cuTensorMapEncodeTiled failed";
+        return cudaErrorInvalidValue;
+    }
+    if (!has_routed) {
+        mA = mAs;
+        mA32 = mAs32;
+        mB = mBs;
+    }
+    if (!has_shared) {
+        mAs = mA;
+        mAs32 = mA32;
+        mBs = mB;
+    }
+    GemmParams p;
+    p.offsets = L.offsets;
+    p.G = has_routed ? L.G : 0;
+    p.K = L.K;
+    p.K_sh = L.K_sh;
+    p.N_out = L.N_out;
+    p.N_out_sh = L.N_out_sh;
+    p.up_off = kFC1 ? L.Nb / 2 : 0;
+    p.up_off_sh = kFC1 ? L.Nb_sh / 2 : 0;
+    p.rows_cap = L.rows_cap;
+    p.T_sh = has_shared ? L.T_sh : 0;
+    p.out = L.out;
+    p.out_sh = L.out_sh;
+    p.status = &L.hdr->status;
+    p.timeout_ns = L.timeout_ns;
+
+    KernelInfo info;
+    cudaError_t err = kernel_info<kFC1, kPair, BN>(num_sms, &info);
+    if (err != cudaSuccess) {
+        *why = "kernel attribute / occupancy query failed";
+        return err;
+    }
+    unsigned grid;
+    if (kPair) {
+        const int64_t units = (bound + 1) / 2;
+        const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(units, std::max(1, info.max_clusters)));
+        grid = (unsigned)(2 * clusters);
+    } else {
+        grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(bound, num_sms));
+    }
+    err = launch_kernel<kFC1, kPair, BN>(p, mA, mB, mAs, mBs, mA32, mAs32, grid, s);
+    if (err != cudaSuccess) *why = "launch failed";
+    return err;
+}
+
+// Upper bound of the tiles of a launch with MMA N = bn (single CTAs): at most
+// min(G, rows) groups are non-empty, each adding at most one partial m-tile.
+int64_t tile_bound(const GemmLaunch& L, int bn) {
+    const int ow = L.swiglu ? bn / 2 : bn;
+    int64_t bound = 0;
+    if (L.G > 0 && L.rows_cap > 0)
+        bound += (int64_t)((L.N_out + ow - 1) / ow) *
+                 ((L.rows_cap + BM - 1) / BM + std::min<int64_t>(L.G, L.rows_cap));
+    if (L.T_sh > 0 && L.b_sh != nullptr && L.N_out_sh > 0)
+        bound += (int64_t)((L.N_out_sh + ow - 1) / ow) * ((L.T_sh + BM - 1) / BM);
+    return bound;
+}
+
+template <bool kFC1>
+cudaError_t dispatch(const GemmLaunch& L, int num_sms, cudaStream_t s, const char** why) {
+    const int64_t b256 = tile_bound(L, 256);
+    const bool pair = L.pair_mode == 2 ? b256 >= 2 : (L.pair_mode == 1 && b256 >= 4 * (int64_t)num_sms);
+    if (pair) return launch_bn<kFC1, true, 256>(L, num_sms, b256, s, why);
+    // the widest N that still gives every SM two tiles (small batches stream
+    // weights; narrower tiles spread them over more SMs, with deeper rings)
+    if (b256 >= 2 * (int64_t)num_sms) return launch_bn<kFC1, false, 256>(L, num_sms, b256, s, why);
+    const int64_t b128 = tile_bound(L, 128);
+    if (b128 >= 2 * (int64_t)num_sms) return launch_bn<kFC1, false, 128>(L, num_sms, b128, s, why);
+    return launch_bn<kFC1, false, 64>(L, num_sms, tile_bound(L, 64), s, why);
 }
 
 }  // namespace
@@ -596,79 +720,7 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& L, int num_sms, cudaStream_t s
         *why = "too many groups";
         return cudaErrorInvalidValue;
     }
-    const int ow = L.swiglu ? BN / 2 : BN;
-    // upper bound of single-mode tiles; pairs pay off when there are enough of them
-    int64_t bound = 0;
-    if (has_routed) bound += (int64_t)((L.N_out + ow - 1) / ow) * ((L.rows_cap + BM - 1) / BM + L.G);
-    if (has_shared) bound += (int64_t)((L.N_out_sh + ow - 1) / ow) * ((L.T_sh + BM - 1) / BM);
-    const bool pair = L.pair_mode == 2 ? bound >= 2 : (L.pair_mode == 1 && bound >= 4 * (int64_t)num_sms);
-
-    // B boxes: 128 rows (FC1 gate/up halves, or any half in pair mode), else 256
-    const uint32_t brows = (L.swiglu || pair) ? BN / 2 : BN;
-    CUtensorMap mA, mB, mAs, mBs;
-    bool ok = true;
-    if (has_routed) {
-        ok = ok && encode_2d(&mA, L.a, (uint64_t)L.K, (uint64_t)L.rows_cap, BM);
-        ok = ok && encode_3d(&mB, L.b, (uint64_t)L.K, (uint64_t)L.Nb, (uint64_t)L.G, brows);
-    }
-    if (has_shared) {
-        ok = ok && encode_2d(&mAs, L.a_sh, (uint64_t)L.K_sh, (uint64_t)L.T_sh, BM);
-        ok = ok && encode_3d(&mBs, L.b_sh, (uint64_t)L.K_sh, (uint64_t)L.Nb_sh, 1, brows);
-    }
-    if (!ok) {
-        *why = "cuTensorMapEncodeTiled failed";
-        return cudaErrorInvalidValue;
-    }
-    if (!has_routed) {
-        mA = mAs;
-        mB = mBs;
-    }
-    if (!has_shared) {
-        mAs = mA;
-        mBs = mB;
-    }
-    GemmParams p;
-    p.offsets = L.offsets;
-    p.G = has_routed ? L.G : 0;
-    p.K = L.K;
-    p.K_sh = L.K_sh;
-    p.N_out = L.N_out;
-    p.N_out_sh = L.N_out_sh;
-    p.up_off = L.swiglu ? L.Nb / 2 : 0;
-    p.up_off_sh = L.swiglu ? L.Nb_sh / 2 : 0;
-    p.rows_cap = L.rows_cap;
-    p.T_sh = has_shared ? L.T_sh : 0;
-    p.out = L.out;
-    p.out_sh = L.out_sh;
-    p.status = &L.hdr->status;
-    p.timeout_ns = L.timeout_ns;
-
-    KernelInfo info;
-    cudaError_t err;
-    if (L.swiglu)
-        err = pair ? kernel_info<true, true>(num_sms, &info) : kernel_info<true, false>(num_sms, &info);
-    else
-        err = pair ? kernel_info<false, true>(num_sms, &info) : kernel_info<false, false>(num_sms, &info);
-    if (err != cudaSuccess) {
-        *why = "kernel attribute / occupancy query failed";
-        return err;
-    }
-    unsigned grid;
-    if (pair) {
-        const int64_t units = (bound + 1) / 2;
-        const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(units, std::max(1, info.max_clusters)));
-        grid = (unsigned)(2 * clusters);
-    } else {
-        grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(bound, num_sms));
-    }
-    if (L.swiglu)
-        err = pair ? launch_kernel<true, true>(p, mA, mB, mAs, mBs, grid, s)
-                   : launch_kernel<true, false>(p, mA, mB, mAs, mBs, grid, s);
-    else
-        err = pair ? launch_kernel<false, true>(p, mA, mB, mAs, mBs, grid, s)
-                   : launch_kernel<false, false>(p, mA, mB, mAs, mBs, grid, s);
-    if (err != cudaSuccess) *why = "launch failed";
-    return err;
+    return L.swiglu ? dispatch<true>(L, num_sms, s, why) : dispatch<false>(L, num_sms, s, why);
 }
 
 cudaError_t launch_wait_timeout_probe(WsHeader* hdr, uint64_t timeout_ns, cudaStream_t s) {

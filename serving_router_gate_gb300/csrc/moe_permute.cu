@@ -16,19 +16,18 @@
 //    counts, and within a slot pairs keep ascending pair index t*k + j.
 //
 // Pipeline (no atomics decide any output position; results are deterministic):
-//  K1 permute_rank_kernel    one warp per chunk of 256 pairs: slot map + mask
-//                            (writes slot_ids, zeroes masked weights), then the
-//                            stable rank of each pair among the chunk's pairs of
-//                            its slot (__match_any_sync over 32 lanes plus a
-//                            per-warp running count), and the chunk's per-slot
-//                            counts.
-//  K2 permute_scan_kernel    one CTA: counts = column sums, offsets = exclusive
-//                            scan, base[c][s] = offsets[s] + earlier chunks'
-//                            counts of s.
-//  K3 permute_scatter_kernel fully parallel, 8 pairs per warp step:
-//                            row = base[chunk][slot] + rank; writes pair_row
-//                            and perm_src, and the warp copies x[t] into
-//                            x_perm[row] with 16-byte loads/stores.
+//  1 rank    one warp per chunk of 256 pairs: slot map + mask (writes
+//            slot_ids, zeroes masked weights), then the stable rank of each
+//            pair among the chunk's pairs of its slot (__match_any_sync over 32
+//            lanes plus a per-warp running count), and the chunk's counts.
+//  2 scan    one CTA: counts = column sums, offsets = exclusive scan,
+//            base[c][s] = offsets[s] + earlier chunks' counts of s.
+//  3 scatter 8 pairs per warp step: row = base[chunk][slot] + rank; writes
+//            pair_row and perm_src, and the warp copies x[t] into x_perm[row]
+//            with 16-byte loads/stores.
+// Large batches run the phases as three kernels over the whole GPU; batches of
+// at most 8192 pairs run phases 1-2 in one CTA (one launch) separated by
+// barriers, and phase 3 too when its row copy is at most 256 KB.
 #include <stdint.h>
 
 #include <algorithm>
@@ -64,24 +63,26 @@ __device__ __forceinline__ int32_t map_slot(int32_t e, int64_t t, int E, const i
     return s;
 }
 
-__global__ void __launch_bounds__(PM_WARPS * 32) permute_rank_kernel(
-    const int32_t* __restrict__ ids, float* __restrict__ w, int64_t P, int k, int E,
-    const int32_t* __restrict__ rep_offset, const int32_t* __restrict__ rep_slots, int S, int local_start,
-    int local_count, int mode, int S_local, int32_t* __restrict__ slot_ids, int32_t* __restrict__ rank,
-    int32_t* __restrict__ chunk_cnt, int64_t nchunks, int32_t* status) {
-    extern __shared__ int32_t pm_cur[];  // [PM_WARPS][S_local]
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int32_t* cur = pm_cur + (size_t)warp * S_local;
+// ---- the three phases, as device functions shared by the multi-CTA kernels
+// and the one-CTA kernel for small batches ----
+
+// Phase 1, one warp on chunk c (pairs c*PM_CHUNK ..): slot map + mask (writes
+// slot_ids, zeroes masked weights), the stable rank of each pair among the
+// chunk's pairs of its slot, and the chunk's per-slot counts.  `cur` is this
+// warp's S_local shared-memory counters.
+__device__ __forceinline__ void rank_chunk(int64_t c, const int32_t* __restrict__ ids, float* __restrict__ w,
+                                           int64_t P, int k, int E, const int32_t* __restrict__ rep_offset,
+                                           const int32_t* __restrict__ rep_slots, int S, int local_start,
+                                           int local_count, int mode, int S_local, int32_t* __restrict__ slot_ids,
+                                           int32_t* __restrict__ rank, int32_t* __restrict__ chunk_cnt,
+                                           int32_t* cur, int32_t* status) {
+    const int lane = threadIdx.x & 31;
     for (int s = lane; s < S_local; s += 32) cur[s] = 0;
     __syncwarp();
-    const int64_t c = (int64_t)blockIdx.x * PM_WARPS + warp;
-    if (c >= nchunks) return;
     const int64_t p0 = c * PM_CHUNK;
-
-    // slot of each of this lane's pairs (all loads issued before any use)
     int32_t sl[PM_ROUNDS];
 #pragma unroll
-    for (int r = 0; r < PM_ROUNDS; ++r) {
+    for (int r = 0; r < PM_ROUNDS; ++r) {  // all loads in flight before any use
         const int64_t p = p0 + r * 32 + lane;
         sl[r] = (p < P) ? ids[p] : INT32_MIN;
     }
@@ -101,7 +102,6 @@ __global__ void __launch_bounds__(PM_WARPS * 32) permute_rank_kernel(
         slot_ids[p] = s;
         sl[r] = s;
     }
-    // stable rank of each pair among the chunk's pairs of its slot
     const uint32_t lt_mask = (1u << lane) - 1u;
 #pragma unroll
     for (int r = 0; r < PM_ROUNDS; ++r) {
@@ -116,12 +116,11 @@ __global__ void __launch_bounds__(PM_WARPS * 32) permute_rank_kernel(
     for (int s = lane; s < S_local; s += 32) dst[s] = cur[s];
 }
 
-__global__ void __launch_bounds__(PM_SCAN_THREADS) permute_scan_kernel(const int32_t* __restrict__ chunk_cnt,
-                                                                       int64_t nchunks, int S_local,
-                                                                       int32_t* __restrict__ counts,
-                                                                       int32_t* __restrict__ offsets,
-                                                                       int32_t* __restrict__ chunk_base) {
-    __shared__ int32_t s_warp[PM_SCAN_THREADS / 32];
+// Phase 2, one CTA of PM_SCAN_THREADS threads: counts = column sums,
+// offsets = exclusive scan, base[c][s] = offsets[s] + earlier chunks' counts.
+__device__ __forceinline__ void scan_counts(const int32_t* __restrict__ chunk_cnt, int64_t nchunks, int S_local,
+                                            int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                                            int32_t* __restrict__ chunk_base, int32_t* s_warp) {
     const int s = threadIdx.x;
     int32_t tot = 0;
     if (s < S_local) {
@@ -134,7 +133,6 @@ __global__ void __launch_bounds__(PM_SCAN_THREADS) permute_scan_kernel(const int
         for (; c < nchunks; ++c) tot += chunk_cnt[c * S_local + s];
         counts[s] = tot;
     }
-    // block exclusive scan of tot over s
     const int lane = s & 31, warp = s >> 5;
     int32_t incl = tot;
 #pragma unroll
@@ -167,10 +165,64 @@ __global__ void __launch_bounds__(PM_SCAN_THREADS) permute_scan_kernel(const int
     }
 }
 
-// row of each pair = its chunk's base for the slot + its rank inside the chunk.
-// A warp takes 8 pairs per step: lanes 0..7 compute the rows (and write
-// pair_row / perm_src), then the whole warp copies the 8 rows of x.
+// Phase 3, one warp on 8 pairs at pb: row = base[chunk][slot] + rank; lanes
+// 0..7 write pair_row / perm_src, then the warp copies the 8 rows of x.
 constexpr int PS_PAIRS = 8;
+
+__device__ __forceinline__ void scatter_pairs(int64_t pb, const uint16_t* __restrict__ x,
+                                              const int32_t* __restrict__ slot_ids, const int32_t* __restrict__ rank,
+                                              const int32_t* __restrict__ chunk_base, int S_local, int64_t P, int k,
+                                              int H, int32_t* __restrict__ pair_row, int32_t* __restrict__ perm_src,
+                                              uint16_t* __restrict__ x_perm) {
+    const int lane = threadIdx.x & 31;
+    const int vec = H / 8;
+    int32_t row = -1;
+    if (lane < PS_PAIRS && pb + lane < P) {
+        const int64_t p = pb + lane;
+        const int32_t s = slot_ids[p];
+        if (s >= 0) {
+            row = chunk_base[(p / PM_CHUNK) * S_local + s] + rank[p];
+            perm_src[row] = (int32_t)p;
+        }
+        pair_row[p] = row;
+    }
+    const int nj = (int)min((int64_t)PS_PAIRS, P - pb);
+    for (int j = 0; j < nj; ++j) {
+        const int32_t r = __shfl_sync(0xffffffffu, row, j);
+        if (r < 0) continue;
+        const uint4* src = reinterpret_cast<const uint4*>(x + ((pb + j) / k) * H);
+        uint4* dst = reinterpret_cast<uint4*>(x_perm + (int64_t)r * H);
+        for (int v = lane; v < vec; v += 32) dst[v] = __ldg(src + v);
+    }
+}
+
+// ---- multi-CTA kernels ----
+
+__global__ void __launch_bounds__(PM_WARPS * 32) permute_rank_kernel(
+    const int32_t* __restrict__ ids, float* __restrict__ w, int64_t P, int k, int E,
+    const int32_t* __restrict__ rep_offset, const int32_t* __restrict__ rep_slots, int S, int local_start,
+    int local_count, int mode, int S_local, int32_t* __restrict__ slot_ids, int32_t* __restrict__ rank,
+    int32_t* __restrict__ chunk_cnt, int64_t nchunks, int32_t* status) {
+    extern __shared__ int32_t pm_cur[];  // [PM_WARPS][S_local]
+    pdl_wait();
+    pdl_trigger();
+    const int warp = threadIdx.x >> 5;
+    const int64_t c = (int64_t)blockIdx.x * PM_WARPS + warp;
+    if (c >= nchunks) return;
+    rank_chunk(c, ids, w, P, k, E, rep_offset, rep_slots, S, local_start, local_count, mode, S_local, slot_ids, rank,
+               chunk_cnt, pm_cur + (size_t)warp * S_local, status);
+}
+
+__global__ void __launch_bounds__(PM_SCAN_THREADS) permute_scan_kernel(const int32_t* __restrict__ chunk_cnt,
+                                                                       int64_t nchunks, int S_local,
+                                                                       int32_t* __restrict__ counts,
+                                                                       int32_t* __restrict__ offsets,
+                                                                       int32_t* __restrict__ chunk_base) {
+    __shared__ int32_t s_warp[PM_SCAN_THREADS / 32];
+    pdl_wait();
+    pdl_trigger();
+    scan_counts(chunk_cnt, nchunks, S_local, counts, offsets, chunk_base, s_warp);
+}
 
 __global__ void __launch_bounds__(256) permute_scatter_kernel(const uint16_t* __restrict__ x,
                                                               const int32_t* __restrict__ slot_ids,
@@ -180,29 +232,41 @@ __global__ void __launch_bounds__(256) permute_scatter_kernel(const uint16_t* __
                                                               int32_t* __restrict__ pair_row,
                                                               int32_t* __restrict__ perm_src,
                                                               uint16_t* __restrict__ x_perm) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int vec = H / 8;
-    for (int64_t pb = ((int64_t)blockIdx.x * 8 + warp) * PS_PAIRS; pb < P;
-         pb += (int64_t)gridDim.x * 8 * PS_PAIRS) {
-        int32_t row = -1;
-        if (lane < PS_PAIRS && pb + lane < P) {
-            const int64_t p = pb + lane;
-            const int32_t s = slot_ids[p];
-            if (s >= 0) {
-                row = chunk_base[(p / PM_CHUNK) * S_local + s] + rank[p];
-                perm_src[row] = (int32_t)p;
-            }
-            pair_row[p] = row;
-        }
-        const int nj = (int)min((int64_t)PS_PAIRS, P - pb);
-        for (int j = 0; j < nj; ++j) {
-            const int32_t r = __shfl_sync(0xffffffffu, row, j);
-            if (r < 0) continue;
-            const uint4* src = reinterpret_cast<const uint4*>(x + ((pb + j) / k) * H);
-            uint4* dst = reinterpret_cast<uint4*>(x_perm + (int64_t)r * H);
-            for (int v = lane; v < vec; v += 32) dst[v] = __ldg(src + v);
-        }
-    }
+    pdl_wait();
+    pdl_trigger();
+    const int warp = threadIdx.x >> 5;
+    for (int64_t pb = ((int64_t)blockIdx.x * 8 + warp) * PS_PAIRS; pb < P; pb += (int64_t)gridDim.x * 8 * PS_PAIRS)
+        scatter_pairs(pb, x, slot_ids, rank, chunk_base, S_local, P, k, H, pair_row, perm_src, x_perm);
+}
+
+// ---- one CTA for small batches: the three phases with block barriers ----
+constexpr int PM_SMALL_WARPS = PM_SCAN_THREADS / 32;  // 32 warps, one chunk each
+constexpr int64_t PM_SMALL_MAX_P = (int64_t)PM_SMALL_WARPS * PM_CHUNK;
+constexpr int PM_SMALL_MAX_S = 384;
+constexpr int64_t PM_SMALL_COPY = 256 * 1024;  // row bytes one CTA copies itself
+
+__global__ void __launch_bounds__(PM_SCAN_THREADS) permute_small_kernel(
+    const int32_t* __restrict__ ids, float* __restrict__ w, int64_t P, int k, int E,
+    const int32_t* __restrict__ rep_offset, const int32_t* __restrict__ rep_slots, int S, int local_start,
+    int local_count, int mode, int S_local, int32_t* __restrict__ slot_ids, int32_t* __restrict__ rank,
+    int32_t* __restrict__ chunk_cnt, int64_t nchunks, const uint16_t* __restrict__ x, int H,
+    int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ chunk_base,
+    int32_t* __restrict__ pair_row, int32_t* __restrict__ perm_src, uint16_t* __restrict__ x_perm,
+    int with_scatter, int32_t* status) {
+    extern __shared__ int32_t pm_cur[];  // [32 warps][S_local]
+    __shared__ int32_t s_warp[PM_SCAN_THREADS / 32];
+    pdl_wait();
+    pdl_trigger();
+    const int warp = threadIdx.x >> 5;
+    if (warp < nchunks)
+        rank_chunk(warp, ids, w, P, k, E, rep_offset, rep_slots, S, local_start, local_count, mode, S_local,
+                   slot_ids, rank, chunk_cnt, pm_cur + (size_t)warp * S_local, status);
+    __syncthreads();
+    scan_counts(chunk_cnt, nchunks, S_local, counts, offsets, chunk_base, s_warp);
+    if (!with_scatter) return;  // the rows are copied by permute_scatter_kernel over the whole GPU
+    __syncthreads();
+    for (int64_t pb = (int64_t)warp * PS_PAIRS; pb < P; pb += (int64_t)PM_SMALL_WARPS * PS_PAIRS)
+        scatter_pairs(pb, x, slot_ids, rank, chunk_base, S_local, P, k, H, pair_row, perm_src, x_perm);
 }
 
 }  // namespace
@@ -228,23 +292,39 @@ void permute_carve(void* base, int64_t P, int S_local, int32_t** rank, int32_t**
 cudaError_t launch_permute(const PermuteLaunch& L, int num_sms, cudaStream_t s) {
     const int64_t P = L.T * L.k;
     const int64_t nchunks = (P + PM_CHUNK - 1) / PM_CHUNK;
+    int32_t* status = &L.hdr->status;
+    if (P <= PM_SMALL_MAX_P && L.S_local <= PM_SMALL_MAX_S) {
+        const size_t smem_small = (size_t)PM_SMALL_WARPS * L.S_local * sizeof(int32_t);
+        if (smem_small > 48 * 1024) {
+            cudaError_t e = cudaFuncSetAttribute(permute_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)smem_small);
+            if (e != cudaSuccess) return e;
+        }
+        // one CTA copies at most PM_SMALL_COPY bytes of rows; more go to the scatter kernel
+        const bool copy_here = (int64_t)P * L.H * 2 <= PM_SMALL_COPY;
+        cudaError_t e = launch_k(permute_small_kernel, dim3(1), dim3(PM_SCAN_THREADS), smem_small, s, L.ids, L.w, P,
+                                 L.k, L.E, L.rep_offset, L.rep_slots, L.S, L.local_start, L.local_count, L.mode,
+                                 L.S_local, L.slot_ids, L.rank, L.chunk_cnt, nchunks, L.x, L.H, L.counts, L.offsets,
+                                 L.chunk_base, L.pair_row, L.perm_src, L.x_perm, (int)copy_here, status);
+        if (e != cudaSuccess || copy_here) return e;
+        const int64_t want = (P + 8 * PS_PAIRS - 1) / (8 * PS_PAIRS);
+        const unsigned gs = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms * 8));
+        return launch_k(permute_scatter_kernel, dim3(gs), dim3(256), 0, s, L.x, L.slot_ids, L.rank, L.chunk_base,
+                        L.S_local, P, L.k, L.H, L.pair_row, L.perm_src, L.x_perm);
+    }
     const unsigned g1 = (unsigned)((nchunks + PM_WARPS - 1) / PM_WARPS);
     const size_t smem = (size_t)PM_WARPS * L.S_local * sizeof(int32_t);
-    int32_t* status = &L.hdr->status;
-    permute_rank_kernel<<<g1, PM_WARPS * 32, smem, s>>>(L.ids, L.w, P, L.k, L.E, L.rep_offset, L.rep_slots, L.S,
-                                                        L.local_start, L.local_count, L.mode, L.S_local,
-                                                        L.slot_ids, L.rank, L.chunk_cnt, nchunks, status);
-    cudaError_t err = cudaGetLastError();
+    cudaError_t err = launch_k(permute_rank_kernel, dim3(g1), dim3(PM_WARPS * 32), smem, s, L.ids, L.w, P, L.k, L.E,
+                               L.rep_offset, L.rep_slots, L.S, L.local_start, L.local_count, L.mode, L.S_local,
+                               L.slot_ids, L.rank, L.chunk_cnt, nchunks, status);
     if (err != cudaSuccess) return err;
-    permute_scan_kernel<<<1, PM_SCAN_THREADS, 0, s>>>(L.chunk_cnt, nchunks, L.S_local, L.counts, L.offsets,
-                                                      L.chunk_base);
-    err = cudaGetLastError();
+    err = launch_k(permute_scan_kernel, dim3(1), dim3(PM_SCAN_THREADS), 0, s, L.chunk_cnt, nchunks, L.S_local,
+                   L.counts, L.offsets, L.chunk_base);
     if (err != cudaSuccess) return err;
     const int64_t want = (P + 8 * PS_PAIRS - 1) / (8 * PS_PAIRS);
     const unsigned g3 = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms * 8));
-    permute_scatter_kernel<<<g3, 256, 0, s>>>(L.x, L.slot_ids, L.rank, L.chunk_base, L.S_local, P, L.k, L.H,
-                                              L.pair_row, L.perm_src, L.x_perm);
-    return cudaGetLastError();
+    return launch_k(permute_scatter_kernel, dim3(g3), dim3(256), 0, s, L.x, L.slot_ids, L.rank, L.chunk_base,
+                    L.S_local, P, L.k, L.H, L.pair_row, L.perm_src, L.x_perm);
 }
 
 }  // namespace moe

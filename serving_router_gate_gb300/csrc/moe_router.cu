@@ -79,6 +79,8 @@ __global__ void __launch_bounds__(RT_THREADS, 2) router_logits_kernel(const uint
                                                                       float* __restrict__ xsq,
                                                                       float* __restrict__ wsq) {
     extern __shared__ __align__(16) float rt_smem[];
+    pdl_wait();
+    pdl_trigger();
     float (*wsm)[RT_BE][RT_LD] = reinterpret_cast<float (*)[RT_BE][RT_LD]>(rt_smem);
     float (*xs)[RT_BT][RT_LD] = reinterpret_cast<float (*)[RT_BT][RT_LD]>(rt_smem + RT_WSTAGES * RT_BE * RT_LD);
 
@@ -265,6 +267,8 @@ __global__ void __launch_bounds__(RS_WARPS * 32) router_select_kernel(
     int64_t T, int H, int E, int k, int renorm, int32_t* __restrict__ ids, float* __restrict__ wout,
     WsHeader* hdr) {
     extern __shared__ __align__(16) unsigned char rs_smem[];
+    pdl_wait();
+    pdl_trigger();
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     double* s_ref = reinterpret_cast<double*>(rs_smem) + (size_t)warp * E;
@@ -533,8 +537,8 @@ cudaError_t launch_router(const RouterLaunch& L, int num_sms, cudaStream_t s) {
     cudaError_t err = cudaFuncSetAttribute(router_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)RT_SMEM);
     if (err != cudaSuccess) return err;
-    router_logits_kernel<<<grid1, RT_THREADS, RT_SMEM, s>>>(L.x, L.Wg, L.T, L.H, L.E, L.KC, L.part, L.xsq, L.wsq);
-    err = cudaGetLastError();
+    err = launch_k(router_logits_kernel, grid1, dim3(RT_THREADS), RT_SMEM, s, L.x, L.Wg, L.T, L.H, L.E, L.KC, L.part,
+                   L.xsq, L.wsq);
     if (err != cudaSuccess) return err;
 
     // worst-case rounding depth of one logit: 32-term chunk, 8-chunk group,
@@ -559,9 +563,9 @@ cudaError_t launch_router(const RouterLaunch& L, int num_sms, cudaStream_t s) {
                                        (int)smem);                                                               \
             if (err != cudaSuccess) return err;                                                                  \
         }                                                                                                        \
-        router_select_kernel<PLV><<<grid2, RS_WARPS * 32, smem, s>>>(L.part, L.xsq, L.wsq, L.nsplit, thr_coef,   \
-                                                                     L.bias, L.x, L.Wg, L.T, L.H, L.E, L.k,      \
-                                                                     L.renorm, L.ids, L.w, L.hdr);               \
+        err = launch_k(router_select_kernel<PLV>, dim3(grid2), dim3(RS_WARPS * 32), smem, s, L.part, L.xsq,     \
+                       L.wsq, L.nsplit, thr_coef, L.bias, L.x, L.Wg, L.T, L.H, L.E, L.k, L.renorm, L.ids, L.w,    \
+                       L.hdr);                                                                                   \
     } while (0)
     if (L.E <= 32)
         MOE_SELECT(1);
@@ -574,7 +578,7 @@ cudaError_t launch_router(const RouterLaunch& L, int num_sms, cudaStream_t s) {
     else
         MOE_SELECT(16);
 #undef MOE_SELECT
-    return cudaGetLastError();
+    return err;
 }
 
 }  // namespace moe

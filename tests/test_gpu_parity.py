@@ -138,6 +138,21 @@ def test_gemm_tile_modes_single_and_pairs(mode):
         moe.moe_set_gemm_pair_mode(1)
 
 
+def test_programmatic_dependent_launch_on_and_off_agree():
+    inp = mi.make_inputs(MID)
+    layer = layer_from_inputs(inp, "cuda")
+    x = inp["x"].cuda()
+    try:
+        moe.moe_set_pdl(False)
+        a = layer.forward(x).clone()
+        moe.moe_set_pdl(True)
+        b = layer.forward(x).clone()
+    finally:
+        moe.moe_set_pdl(True)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert moe.moe_get_device_status(layer.ws) == 0
+
+
 def test_cuda_graph_replay_matches_eager_launches():
     inp = mi.make_inputs(MID)
     layer = layer_from_inputs(inp, "cuda")
