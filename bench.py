@@ -8,10 +8,11 @@ Prints ONE JSON line (rank 0).  A step is one full layer forward over one
 batch of T tokens.  `value` = tokens of all ranks / max-over-ranks time, with
 inputs resident in HBM; `e2e` = the same through the public API with the
 token activations copied from pinned host memory and the output copied back
-inside the timed region (weights are resident model parameters).  The
+inside the timed region (weights are resident model parameters).  L2 is
+flushed before every timed step, outside the step's own CUDA events.  The
 per-kernel breakdown and the roofline of the dominant kernel come from a
-second timed pass that launches the same kernels stage by stage with CUDA
-events on the launching stream.  With N > 1 (torchrun), every rank runs its
+second timed pass that replays each stage from its own CUDA graph with CUDA
+events on the launching stream between stages.  With N > 1 (torchrun), every rank runs its
 own independent batch (weak scaling, no collective on the data path).
 `--impl reference` times the fp64 CPU oracle on a bounded sample instead.
 """
@@ -110,6 +111,42 @@ class ClockSampler:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
                 "reasons": sorted(reasons)}
+
+
+class L2Flush:
+    """Leaves L2 holding none of a step's data: writes one buffer of at least
+    twice the L2 size, then reads a second one, so no dirty line of the flush is
+    left to be written back inside the next timed step."""
+
+    def __init__(self, dev):
+        l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or (128 << 20))
+        self.nbytes = max(2 * l2, 256 << 20)
+        n = self.nbytes // 4
+        self.w = torch.empty(n, dtype=torch.float32, device=dev)
+        self.r = torch.ones(n, dtype=torch.float32, device=dev)
+        self.sink = torch.empty((), dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.w.fill_(1.0)
+        torch.sum(self.r, 0, out=self.sink)
+
+    def describe(self):
+        return f"write {self.nbytes >> 20} MiB, then read another {self.nbytes >> 20} MiB"
+
+
+def time_steps(fns, K, flush, stream):
+    """K steps; each step flushes L2, then runs fns in order with a CUDA event on
+    `stream` before and after each.  Returns per-fn lists of K times in ms."""
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(fns) + 1)] for _ in range(K)]
+    for i in range(K):
+        flush()
+        e = evs[i]
+        e[0].record(stream)
+        for j, fn in enumerate(fns):
+            fn()
+            e[j + 1].record(stream)
+    torch.cuda.synchronize()
+    return [[e[j].elapsed_time(e[j + 1]) for e in evs] for j in range(len(fns))]
 
 
 def _dist():
@@ -214,6 +251,13 @@ def bench_ours(args):
     if status:
         raise RuntimeError(f"device status {status} after warm-up")
 
+    # launches one layer forward issues (the same kernels a graph replay re-issues)
+    c0 = moe.moe_get_launch_count()
+    layer.forward(x)
+    kernels_per_step = moe.moe_get_launch_count() - c0
+    refined_per_step = moe.moe_get_route_stats(layer.ws) / (W + 1)
+    flush = L2Flush(dev)
+
     # ---- timed pass: the whole layer, K steps (replayed from a CUDA graph of one step) ----
     graph = layer.capture(x) if args.graph else None
     step = graph.replay if graph is not None else (lambda: layer.forward(x))
@@ -223,42 +267,45 @@ def bench_ours(args):
     _barrier(ws_)
     torch.cuda.synchronize()
     clocks.start()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(K):
-        step()
-    e1.record(stream)
+    ms_local = statistics.mean(time_steps([step], K, flush, stream)[0])
     torch.cuda.synchronize()
     clk = clocks.stop()
     _barrier(ws_)
-    value, ms = aggregate_throughput(T, e0.elapsed_time(e1) / K, ws_)
-    kernels_per_step = 2 + 4 + 3  # router 2, permute 4, FC1, FC2, finalize
+    value, ms = aggregate_throughput(T, ms_local, ws_)
 
-    # ---- staged pass: same kernels, events around each stage ----
+    # ---- staged pass: each stage replayed from its own CUDA graph, events between stages ----
     Ish = cfg.n_shared * cfg.I_shared
     P = T * cfg.k
     h = torch.empty((P, cfg.I), dtype=torch.bfloat16, device=dev)
     y = torch.empty((P, H), dtype=torch.bfloat16, device=dev)
     h_sh = torch.empty((T, Ish), dtype=torch.bfloat16, device=dev) if Ish else None
     y_sh = torch.empty((T, H), dtype=torch.bfloat16, device=dev) if Ish else None
-    names = ["route", "permute", "fc1", "fc2", "finalize"]
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
     xs = x if Ish else None
-    for i in range(K + W):
-        e = evs[i - W] if i >= W else None
-        if e: e[0].record(stream)
-        layer.route(x)
-        if e: e[1].record(stream)
-        layer.permute(x)
-        if e: e[2].record(stream)
-        moe.moe_grouped_fc1(layer.x_perm, layer.offsets, layer.W1, xs, layer.W1s, h, h_sh, layer.ws)
-        if e: e[3].record(stream)
-        moe.moe_grouped_fc2(h, layer.offsets, layer.W2, h_sh, layer.W2s, y, y_sh, layer.ws)
-        if e: e[4].record(stream)
-        moe.moe_finalize(y, layer.pair_row, layer.topk_w, y_sh, xs, layer.gate, layer.out, layer.ws)
-        if e: e[5].record(stream)
+    stages = {
+        "route": lambda: layer.route(x),
+        "permute": lambda: layer.permute(x),
+        "fc1": lambda: moe.moe_grouped_fc1(layer.x_perm, layer.offsets, layer.W1, xs, layer.W1s, h, h_sh, layer.ws),
+        "fc2": lambda: moe.moe_grouped_fc2(h, layer.offsets, layer.W2, h_sh, layer.W2s, y, y_sh, layer.ws),
+        "finalize": lambda: moe.moe_finalize(y, layer.pair_row, layer.topk_w, y_sh, xs, layer.gate, layer.out,
+                                             layer.ws),
+    }
+    for fn in stages.values():
+        fn()
     torch.cuda.synchronize()
-    stage_ms = {n: statistics.mean(ev[j].elapsed_time(ev[j + 1]) for ev in evs) for j, n in enumerate(names)}
+    if args.graph:
+        graphs = []
+        for fn in stages.values():
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fn()
+            graphs.append(g.replay)
+    else:
+        graphs = list(stages.values())
+    for _ in range(W):
+        for g in graphs:
+            g()
+    per_stage = time_steps(graphs, K, flush, stream)
+    stage_ms = {n: statistics.mean(t) for n, t in zip(stages, per_stage)}
 
     # ---- e2e pass: host activations in, host output out ----
     x_pin = x.cpu().pin_memory()
@@ -278,12 +325,7 @@ def bench_ours(args):
         e2e_step()
     torch.cuda.synchronize()
     _barrier(ws_)
-    e0.record(stream)
-    for _ in range(K):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms_e2e = max_over_ranks(e0.elapsed_time(e1) / K, ws_)
+    ms_e2e = max_over_ranks(statistics.mean(time_steps([e2e_step], K, flush, stream)[0]), ws_)
     status = moe.moe_get_device_status(layer.ws)
     if status:
         raise RuntimeError(f"device status {status} after the timed runs")
@@ -316,8 +358,8 @@ def bench_ours(args):
         "config": {"workload": cfg.name, "shape": mi.describe(cfg), "tokens_per_gpu": T,
                    "parallelism": f"replicas x{ws_} (independent token batches, no collective)",
                    "cuda_graph": bool(args.graph),
-                   "l2": "inputs larger than L2 (expert weights %.2f GB per step)" % (
-                       (cfg.slots * 3 * cfg.I * H * 2 + 3 * Ish * H * 2) / 1e9)},
+                   "l2": f"flushed before every timed step ({flush.describe()}); each step timed by "
+                         f"its own CUDA events, flush outside them"},
         "roofline": roof,
         "e2e": {"value": total_tokens / (ms_e2e * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2,
                 "d2h_bytes_per_step": T * H * 2, "ms_per_step": ms_e2e},
@@ -326,7 +368,7 @@ def bench_ours(args):
         "kernels_ms": stage_ms,
         "tflops_layer": (wk["fc1_flops"] + wk["fc2_flops"] + wk["gate_flops"]) / (ms * 1e-3) / 1e12,
         "grouped_gemm_tflops": (wk["fc1_flops"] + wk["fc2_flops"]) / ((stage_ms["fc1"] + stage_ms["fc2"]) * 1e-3) / 1e12,
-        "rows": rows, "active_slots": active,
+        "rows": rows, "active_slots": active, "router_fp64_rechecked_tokens": refined_per_step,
     }
     if rank == 0 and ws_ == 1 and not args.no_cpu_baseline:
         base, _ = run_cpu_baseline(inp, cfg, target_s=args.cpu_seconds)

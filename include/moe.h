@@ -286,6 +286,12 @@ MOE_API moe_status_t moe_set_gemm_pair_mode(int mode);
  * order.  Process-wide; results are identical.  MOE_ERR_INVALID_ARG otherwise. */
 MOE_API moe_status_t moe_set_pdl(int enable);
 
+/* Number of kernel launches the library has issued in this process (all
+ * threads, all devices), counted on the host as each launch is made.  A CUDA
+ * graph captured from library calls holds the launches counted during its
+ * capture; replaying it issues them again without counting. */
+MOE_API uint64_t moe_get_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -24,7 +24,7 @@ __all__ = [
     "lib_path", "moe_workspace_size", "moe_workspace_init", "moe_get_device_status", "moe_get_route_stats",
     "moe_route", "moe_permute", "moe_forward", "moe_grouped_fc1", "moe_grouped_fc2", "moe_finalize",
     "moe_debug_wait_timeout", "moe_set_wait_timeout_ns", "moe_route_noalloc", "moe_set_gemm_pair_mode",
-    "moe_set_pdl", "EXPORTED_SYMBOLS",
+    "moe_set_pdl", "moe_get_launch_count", "EXPORTED_SYMBOLS",
 ]
 
 MOE_OK = 0
@@ -41,7 +41,7 @@ EXPORTED_SYMBOLS = (
     "moe_status_string", "moe_workspace_size", "moe_workspace_init", "moe_get_device_status",
     "moe_get_route_stats", "moe_route", "moe_permute", "moe_forward", "moe_grouped_fc1", "moe_grouped_fc2",
     "moe_finalize", "moe_debug_wait_timeout", "moe_set_wait_timeout_ns", "moe_route_noalloc",
-    "moe_set_gemm_pair_mode", "moe_set_pdl",
+    "moe_set_gemm_pair_mode", "moe_set_pdl", "moe_get_launch_count",
 )
 
 
@@ -78,6 +78,7 @@ def _load():
         "moe_route_noalloc": ([P, P, P, i64, i32, i32, i32, i32, P, P, P], i32),
         "moe_set_gemm_pair_mode": ([i32], i32),
         "moe_set_pdl": ([i32], i32),
+        "moe_get_launch_count": ([], ctypes.c_uint64),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -258,6 +259,11 @@ def moe_set_wait_timeout_ns(timeout_ns: int) -> None:
 def moe_set_pdl(enable: bool) -> None:
     """Launch kernels with programmatic dependent launch (default) or in plain stream order."""
     _check("moe_set_pdl", _lib.moe_set_pdl(int(bool(enable))))
+
+
+def moe_get_launch_count() -> int:
+    """Kernel launches the library has issued in this process (counted on the host)."""
+    return int(_lib.moe_get_launch_count())
 
 
 def moe_set_gemm_pair_mode(mode: int) -> None:

@@ -14,6 +14,7 @@ namespace {
 std::atomic<uint64_t> g_timeout_ns{4000000000ull};
 std::atomic<int> g_pair_mode{0};
 std::atomic<int> g_pdl{1};
+std::atomic<uint64_t> g_launches{0};
 
 int device_sms() {
     static std::mutex mu;
@@ -59,6 +60,7 @@ moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE
 }  // namespace
 
 bool moe::pdl_enabled() { return g_pdl.load() != 0; }
+void moe::count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 extern "C" {
 
@@ -77,6 +79,8 @@ const char* moe_status_string(int status) {
 }
 
 void moe_set_wait_timeout_ns(uint64_t timeout_ns) { g_timeout_ns.store(timeout_ns > 0 ? timeout_ns : 1); }
+
+uint64_t moe_get_launch_count(void) { return g_launches.load(); }
 
 moe_status_t moe_set_pdl(int enable) {
     if (enable != 0 && enable != 1) return MOE_ERR_INVALID_ARG;

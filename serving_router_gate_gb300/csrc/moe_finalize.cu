@@ -7,16 +7,22 @@
 // to the routed output (out = routed_out + shared_out).  The shared gate
 // sigmoid(x . w_s) is the Qwen2-MoE-style scaled shared expert.
 //
-// One warp per work unit -- a token's whole row, or (few tokens) a 256-column
-// slice of it -- 8 warps per CTA, grid-stride.  Lane j < k holds pair j's row
-// and weight and broadcasts them with shuffles.  Each lane owns the 16-byte
-// vectors lane, lane+32, ... of the unit; it issues the loads of up to 8 pairs'
-// rows (and then of the shared-expert row) before using them, and accumulates
-// in fp32 in fixed j order:
-//   acc = fma(w_j, y[row_j], acc) for j = 0..k-1 (rows of -1 skipped),
-//   acc = fma(g, y_shared, acc), out = bf16_rn(acc).
-// The gate dot product x . w_s is a per-lane strided partial sum followed by a
-// warp xor-butterfly, so every lane holds the same bit-reproducible value.
+// One CTA (8 warps) per block of TB <= 8 consecutive tokens, grid-stride over
+// blocks.  Per block:
+//   1. the tokens' pair rows and weights go to shared memory (row -1 = pair
+//      skipped; a row outside [-1, rows_cap) is reported and skipped);
+//   2. warp w computes the shared gate g of token w: a lane-strided fp32
+//      partial dot x . w_s, then a warp xor-butterfly, so every lane holds the
+//      same bit-reproducible value;
+//   3. the block's TB x H/8 16-byte output vectors are spread over the 256
+//      threads, consecutive threads on consecutive vectors of a token; each
+//      thread issues the loads of up to 8 pairs' vectors and of the shared
+//      expert's vector before using them and accumulates in fp32 in fixed j
+//      order:
+//        acc = fma(w_j, y[row_j], acc) for j = 0..k-1 (rows of -1 skipped),
+//        acc = fma(g, y_shared, acc), out = bf16_rn(acc).
+// TB is picked on the host so that there are at least two blocks per SM when
+// the batch allows; with one token (TB = 1) all 256 threads share its row.
 #include <algorithm>
 
 #include "moe_internal.cuh"
@@ -25,42 +31,46 @@ namespace moe {
 namespace {
 
 constexpr int FZ_WARPS = 8;
+constexpr int FZ_THREADS = FZ_WARPS * 32;
+constexpr int FZ_TB = 8;     // largest token block (one gate warp per token)
+constexpr int FZ_MAXK = 32;  // k <= 32
+constexpr int FZ_BATCH = 8;  // pair loads issued together
 
-// FZ_UNROLL vectors per lane per pass; FZ_BATCH pairs whose loads are issued
-// together (rows: 2 x 4; slices, one vector per lane: 1 x 8)
-template <int FZ_UNROLL, int FZ_BATCH>
-__global__ void __launch_bounds__(FZ_WARPS * 32, 3) finalize_kernel(
+// Each thread takes one output vector at a time and issues the loads of up to
+// FZ_BATCH pairs' vectors and of the shared-expert vector before using any.
+__global__ void __launch_bounds__(FZ_THREADS, 4) finalize_kernel(
     const uint16_t* __restrict__ y, int64_t rows_cap, const int32_t* __restrict__ pair_row,
-    const float* __restrict__ w, int64_t T, int k, int H, int unit_cols, const uint16_t* __restrict__ y_sh,
+    const float* __restrict__ w, int64_t T, int k, int H, int TB, const uint16_t* __restrict__ y_sh,
     const uint16_t* __restrict__ x, const uint16_t* __restrict__ gate_w, uint16_t* __restrict__ out,
     int32_t* status) {
+    __shared__ int32_t s_row[FZ_TB][FZ_MAXK];
+    __shared__ float s_w[FZ_TB][FZ_MAXK];
+    __shared__ float s_g[FZ_TB];
     pdl_wait();
     pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int vec = H / 8;
-    const int units_per_token = H / unit_cols;
-    const int64_t units = T * units_per_token;
-    for (int64_t un = (int64_t)blockIdx.x * FZ_WARPS + warp; un < units; un += (int64_t)gridDim.x * FZ_WARPS) {
-        const int64_t t = un / units_per_token;
-        const int v_beg = (int)(un % units_per_token) * (unit_cols / 8);
-        const int v_end = v_beg + unit_cols / 8;
-        int64_t my_row = -1;
-        float my_w = 0.f;
-        if (lane < k) {
-            const int32_t r = pair_row[t * k + lane];
-            my_row = r;
+    const bool gated = (y_sh != nullptr) && (gate_w != nullptr);
+    const int64_t nblk = (T + TB - 1) / TB;
+    for (int64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
+        const int64_t t0 = blk * TB;
+        const int nt = (int)min((int64_t)TB, T - t0);
+        for (int i = threadIdx.x; i < nt * k; i += FZ_THREADS) {
+            const int tt = i / k, j = i - tt * k;
+            int32_t r = pair_row[(t0 + tt) * k + j];
             if (r < -1 || (int64_t)r >= rows_cap) {
                 report(status, MOE_ERR_DEVICE_BOUNDS);
-                my_row = -1;
+                r = -1;
             }
-            my_w = w[t * k + lane];
+            s_row[tt][j] = r;
+            s_w[tt][j] = w[(t0 + tt) * k + j];
         }
-        float g = 1.0f;
-        if (y_sh && gate_w) {
-            const uint4* xv = reinterpret_cast<const uint4*>(x + t * H);
+        if (gated && warp < nt) {
+            const uint4* xv = reinterpret_cast<const uint4*>(x + (t0 + warp) * H);
             const uint4* gv = reinterpret_cast<const uint4*>(gate_w);
             float d = 0.f;
+#pragma unroll 4
             for (int v = lane; v < vec; v += 32) {
                 float a[8], b[8];
                 unpack8(__ldg(xv + v), a);
@@ -70,94 +80,67 @@ __global__ void __launch_bounds__(FZ_WARPS * 32, 3) finalize_kernel(
             }
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
-            g = 1.0f / (1.0f + expf(-d));
+            if (lane == 0) s_g[warp] = 1.0f / (1.0f + expf(-d));
         }
-        uint4* orow = reinterpret_cast<uint4*>(out + t * H);
-        const uint4* srow = y_sh ? reinterpret_cast<const uint4*>(y_sh + t * H) : nullptr;
-        for (int v0 = v_beg + lane; v0 < v_end; v0 += 32 * FZ_UNROLL) {
-            float acc[FZ_UNROLL][8];
+        __syncthreads();
+
+        const int items = nt * vec;
+        for (int f = threadIdx.x; f < items; f += FZ_THREADS) {
+            const int tt = f / vec;
+            const int v = f - tt * vec;
+            float acc[8];
 #pragma unroll
-            for (int u = 0; u < FZ_UNROLL; ++u)
-#pragma unroll
-                for (int i = 0; i < 8; ++i) acc[u][i] = 0.f;
-            // pairs in batches of FZ_BATCH: every load of a batch is issued before any use
+            for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+            const uint4 sh = y_sh ? __ldg(reinterpret_cast<const uint4*>(y_sh + (t0 + tt) * H) + v)
+                                  : make_uint4(0, 0, 0, 0);
             for (int j0 = 0; j0 < k; j0 += FZ_BATCH) {
-                uint4 ld[FZ_BATCH][FZ_UNROLL];
-                float wj[FZ_BATCH];
+                uint4 ld[FZ_BATCH];
+                int32_t rr[FZ_BATCH];
 #pragma unroll
                 for (int b = 0; b < FZ_BATCH; ++b) {
                     const int j = j0 + b;
-                    const int64_t r = __shfl_sync(0xffffffffu, my_row, j & 31);
-                    wj[b] = __shfl_sync(0xffffffffu, my_w, j & 31);
-                    const bool use = (j < k) && (r >= 0);
-                    if (!use) wj[b] = 0.f;
-                    const uint4* yrow = reinterpret_cast<const uint4*>(y + (use ? r : 0) * H);
-#pragma unroll
-                    for (int u = 0; u < FZ_UNROLL; ++u) {
-                        const int v = v0 + 32 * u;
-                        ld[b][u] = (use && v < v_end) ? __ldg(yrow + v) : make_uint4(0, 0, 0, 0);
-                    }
+                    rr[b] = j < k ? s_row[tt][j] : -1;
+                    ld[b] = rr[b] >= 0 ? __ldg(reinterpret_cast<const uint4*>(y + (int64_t)rr[b] * H) + v)
+                                       : make_uint4(0, 0, 0, 0);
                 }
 #pragma unroll
                 for (int b = 0; b < FZ_BATCH; ++b) {
-                    if (j0 + b >= k) break;
-                    if (__shfl_sync(0xffffffffu, my_row, (j0 + b) & 31) < 0) continue;
+                    if (rr[b] < 0) continue;
+                    const float wj = s_w[tt][j0 + b];
+                    float fv[8];
+                    unpack8(ld[b], fv);
 #pragma unroll
-                    for (int u = 0; u < FZ_UNROLL; ++u) {
-                        float f[8];
-                        unpack8(ld[b][u], f);
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) acc[u][i] = fmaf(wj[b], f[i], acc[u][i]);
-                    }
+                    for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, fv[i], acc[i]);
                 }
             }
-            if (srow) {
-                uint4 ld[FZ_UNROLL];
+            if (y_sh) {
+                const float g = gated ? s_g[tt] : 1.0f;
+                float fv[8];
+                unpack8(sh, fv);
 #pragma unroll
-                for (int u = 0; u < FZ_UNROLL; ++u) {
-                    const int v = v0 + 32 * u;
-                    ld[u] = v < v_end ? __ldg(srow + v) : make_uint4(0, 0, 0, 0);
-                }
-#pragma unroll
-                for (int u = 0; u < FZ_UNROLL; ++u) {
-                    float f[8];
-                    unpack8(ld[u], f);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) acc[u][i] = fmaf(g, f[i], acc[u][i]);
-                }
+                for (int i = 0; i < 8; ++i) acc[i] = fmaf(g, fv[i], acc[i]);
             }
-#pragma unroll
-            for (int u = 0; u < FZ_UNROLL; ++u) {
-                const int v = v0 + 32 * u;
-                if (v < v_end) {
-                    uint4 o;
-                    o.x = pack_bf16x2(acc[u][0], acc[u][1]);
-                    o.y = pack_bf16x2(acc[u][2], acc[u][3]);
-                    o.z = pack_bf16x2(acc[u][4], acc[u][5]);
-                    o.w = pack_bf16x2(acc[u][6], acc[u][7]);
-                    orow[v] = o;
-                }
-            }
+            uint4 o;
+            o.x = pack_bf16x2(acc[0], acc[1]);
+            o.y = pack_bf16x2(acc[2], acc[3]);
+            o.z = pack_bf16x2(acc[4], acc[5]);
+            o.w = pack_bf16x2(acc[6], acc[7]);
+            reinterpret_cast<uint4*>(out + (t0 + tt) * H)[v] = o;
         }
+        __syncthreads();  // the next block rewrites the shared arrays
     }
 }
 
 }  // namespace
 
 cudaError_t launch_finalize(const FinalizeLaunch& L, int num_sms, cudaStream_t s) {
-    // work unit of one warp: a whole row when there are enough tokens to fill
-    // the GPU, else 256-column slices (each slice recomputes the gate dot)
-    int unit_cols = L.H;
-    if (L.T < 64LL * num_sms && L.H % 256 == 0) unit_cols = 256;
-    const int64_t units = L.T * (L.H / unit_cols);
-    const int64_t want = (units + FZ_WARPS - 1) / FZ_WARPS;
-    const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms * 8));
-    if (unit_cols == L.H)
-        return launch_k(finalize_kernel<2, 4>, dim3(grid), dim3(FZ_WARPS * 32), 0, s, L.y, L.rows_cap, L.pair_row,
-                        L.w, L.T, L.k, L.H, unit_cols, L.y_sh, L.x, L.gate_w, L.out,
-                        L.hdr ? &L.hdr->status : nullptr);
-    return launch_k(finalize_kernel<1, 8>, dim3(grid), dim3(FZ_WARPS * 32), 0, s, L.y, L.rows_cap, L.pair_row, L.w,
-                    L.T, L.k, L.H, unit_cols, L.y_sh, L.x, L.gate_w, L.out, L.hdr ? &L.hdr->status : nullptr);
+    // largest token block that still leaves two blocks per SM
+    int TB = FZ_TB;
+    while (TB > 1 && (L.T + TB - 1) / TB < 2LL * num_sms) TB >>= 1;
+    const int64_t nblk = (L.T + TB - 1) / TB;
+    const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(nblk, (int64_t)num_sms * 4));
+    return launch_k(finalize_kernel, dim3(grid), dim3(FZ_THREADS), 0, s, L.y, L.rows_cap, L.pair_row, L.w, L.T, L.k,
+                    L.H, TB, L.y_sh, L.x, L.gate_w, L.out, L.hdr ? &L.hdr->status : nullptr);
 }
 
 }  // namespace moe

@@ -613,6 +613,7 @@ cudaError_t launch_kernel(const GemmParams& p, const CUtensorMap& mA, const CUte
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
+    count_launch();
     return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<kFC1, kPair, BN>, p, mA, mB, mAs, mBs, mA32, mAs32);
 }
 
@@ -724,6 +725,7 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& L, int num_sms, cudaStream_t s
 }
 
 cudaError_t launch_wait_timeout_probe(WsHeader* hdr, uint64_t timeout_ns, cudaStream_t s) {
+    count_launch();
     wait_probe_kernel<<<1, 32, 0, s>>>(&hdr->status, timeout_ns);
     return cudaGetLastError();
 }

@@ -21,8 +21,11 @@
 //     fixed order, adds the bias, and takes the k+1 largest logits (ties ->
 //     lower id).  Consecutive candidates whose fp32 gap is within twice the
 //     per-token bound form a cluster whose true order fp32 cannot decide; each
-//     cluster that touches the top k is recomputed in fp64 from the exact
-//     bf16 x fp32 products and re-ordered (ties -> lower id).  Then the fp32
+//     cluster that touches the top k is recomputed with a compensated fp32
+//     dot product (about twice fp32's precision, on the fp32 pipes) and
+//     re-ordered; only if those values still leave a gap inside their own
+//     bound is the cluster recomputed in fp64 from the exact bf16 x fp32
+//     products (ties -> lower id).  Then the fp32
 //     softmax (expf) over all E logits, the selected probabilities, and the
 //     optional renormalisation (divide by their sum, in j order).
 #include <float.h>
@@ -226,28 +229,112 @@ __global__ void __launch_bounds__(RT_THREADS, 2) router_logits_kernel(const uint
     if (do_wn && e0 + (tid - 64) < E) wsq[(int64_t)sp * E + e0 + (tid - 64)] = nsq;
 }
 
-// fp64 dot product of one bf16 x row with one fp32 Wg row, by one warp.
-// Every lane returns the same value (xor-butterfly sums are symmetric).
-__device__ double refine_dot(const uint16_t* __restrict__ xrow, const float* __restrict__ wrow, int H, int lane) {
-    double s = 0.0;
-    for (int h0 = lane * 8; h0 < H; h0 += 256) {
-        const uint4 xv = __ldg(reinterpret_cast<const uint4*>(xrow + h0));
-        const float4 w0 = __ldg(reinterpret_cast<const float4*>(wrow + h0));
-        const float4 w1 = __ldg(reinterpret_cast<const float4*>(wrow + h0 + 4));
-        float xf[8];
-        unpack8(xv, xf);
-        s = fma((double)xf[0], (double)w0.x, s);
-        s = fma((double)xf[1], (double)w0.y, s);
-        s = fma((double)xf[2], (double)w0.z, s);
-        s = fma((double)xf[3], (double)w0.w, s);
-        s = fma((double)xf[4], (double)w1.x, s);
-        s = fma((double)xf[5], (double)w1.y, s);
-        s = fma((double)xf[6], (double)w1.z, s);
-        s = fma((double)xf[7], (double)w1.w, s);
+// Compensated (doubled-precision) dot product of one bf16 x row with one fp32
+// Wg row, by one warp, on the fp32 pipes.  Every product x_h * w_h is split
+// exactly into ph + pl (ph = fl(x*w), pl = fma(x, w, -ph)); ph is added to a
+// running sum by the error-free TwoSum, whose rounding error joins pl in a
+// plain fp32 correction sum (the Dot2 scheme of Ogita, Rump and Oishi,
+// "Accurate sum and dot product", 2005).  Lane l keeps four accumulators
+// (piece l + 32 j goes to accumulator j mod 4, H/128 products each); the 128
+// accumulators are then combined by TwoSum (lanes: xor butterfly, so every lane
+// ends with the same pair).  Returned as the fp64 sum hi + lo of the final
+// pair, with no rounding to fp32: |result - exact| <= (gamma_{H/128} +
+// gamma_128)^2 * sum_h |x_h w_h| (no underflow).
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+    s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+__device__ double refine_dot2(const uint16_t* __restrict__ xrow, const float* __restrict__ wrow, int H, int lane) {
+    float hs[4] = {0.f, 0.f, 0.f, 0.f}, cs[4] = {0.f, 0.f, 0.f, 0.f};
+    const int pieces = H / 8;
+    for (int p0 = lane; p0 < pieces; p0 += 128) {
+        uint4 xv[4];
+        float4 w0[4], w1[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int p = p0 + 32 * i;
+            const bool ok = p < pieces;
+            xv[i] = ok ? __ldg(reinterpret_cast<const uint4*>(xrow) + p) : make_uint4(0, 0, 0, 0);
+            w0[i] = ok ? __ldg(reinterpret_cast<const float4*>(wrow) + 2 * p) : make_float4(0.f, 0.f, 0.f, 0.f);
+            w1[i] = ok ? __ldg(reinterpret_cast<const float4*>(wrow) + 2 * p + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float xf[8];
+            unpack8(xv[i], xf);
+            const float wf[8] = {w0[i].x, w0[i].y, w0[i].z, w0[i].w, w1[i].x, w1[i].y, w1[i].z, w1[i].w};
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float ph = __fmul_rn(xf[j], wf[j]);
+                const float pl = fmaf(xf[j], wf[j], -ph);
+                float sn, e;
+                two_sum(hs[i], ph, sn, e);
+                hs[i] = sn;
+                cs[i] = __fadd_rn(cs[i], __fadd_rn(e, pl));
+            }
+        }
+    }
+    float S = hs[0], C = cs[0];
+#pragma unroll
+    for (int i = 1; i < 4; ++i) {
+        float sn, e;
+        two_sum(S, hs[i], sn, e);
+        S = sn;
+        C = __fadd_rn(C, __fadd_rn(e, cs[i]));
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    return s;
+    for (int off = 16; off > 0; off >>= 1) {
+        const float oS = __shfl_xor_sync(0xffffffffu, S, off);
+        const float oC = __shfl_xor_sync(0xffffffffu, C, off);
+        float sn, e;
+        two_sum(S, oS, sn, e);  // exact: e = S + oS - sn on both lanes
+        S = sn;
+        C = __fadd_rn(__fadd_rn(C, oC), e);
+    }
+    return (double)S + (double)C;
+}
+
+// fp64 dot product of one bf16 x row with one fp32 Wg row, by one warp.  Lane
+// l takes the 8-element pieces l, l + 32, ... of the row; the loads of four
+// pieces are issued together and feed four independent fp64 partial sums
+// (piece i into sum i mod 4), added as (s0 + s1) + (s2 + s3) and then summed
+// over the lanes by an xor butterfly.  Every lane returns the same value.
+// Each bf16 x fp32 product is exact in fp64; the sums' rounding stays within
+// gamma_{H+2}(fp64) of the exact dot product (H terms, two more additions).
+__device__ double refine_dot(const uint16_t* __restrict__ xrow, const float* __restrict__ wrow, int H, int lane) {
+    double s[4] = {0.0, 0.0, 0.0, 0.0};
+    const int pieces = H / 8;
+    for (int p0 = lane; p0 < pieces; p0 += 128) {
+        uint4 xv[4];
+        float4 w0[4], w1[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int p = p0 + 32 * i;
+            const bool ok = p < pieces;
+            xv[i] = ok ? __ldg(reinterpret_cast<const uint4*>(xrow) + p) : make_uint4(0, 0, 0, 0);
+            w0[i] = ok ? __ldg(reinterpret_cast<const float4*>(wrow) + 2 * p) : make_float4(0.f, 0.f, 0.f, 0.f);
+            w1[i] = ok ? __ldg(reinterpret_cast<const float4*>(wrow) + 2 * p + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float xf[8];
+            unpack8(xv[i], xf);
+            s[i] = fma((double)xf[0], (double)w0[i].x, s[i]);
+            s[i] = fma((double)xf[1], (double)w0[i].y, s[i]);
+            s[i] = fma((double)xf[2], (double)w0[i].z, s[i]);
+            s[i] = fma((double)xf[3], (double)w0[i].w, s[i]);
+            s[i] = fma((double)xf[4], (double)w1[i].x, s[i]);
+            s[i] = fma((double)xf[5], (double)w1[i].y, s[i]);
+            s[i] = fma((double)xf[6], (double)w1[i].z, s[i]);
+            s[i] = fma((double)xf[7], (double)w1[i].w, s[i]);
+        }
+    }
+    double t = (s[0] + s[1]) + (s[2] + s[3]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+    return t;
 }
 
 template <int PL>
@@ -263,7 +350,7 @@ __device__ __forceinline__ float pick(const float (&l)[PL], int idx) {
 template <int PL>
 __global__ void __launch_bounds__(RS_WARPS * 32) router_select_kernel(
     const float* __restrict__ part, const float* __restrict__ xsq, const float* __restrict__ wsq, int nsplit,
-    float thr_coef, const float* __restrict__ bias, const uint16_t* __restrict__ x, const float* __restrict__ Wg,
+    float thr_coef, float thr2_coef, const float* __restrict__ bias, const uint16_t* __restrict__ x, const float* __restrict__ Wg,
     int64_t T, int H, int E, int k, int renorm, int32_t* __restrict__ ids, float* __restrict__ wout,
     WsHeader* hdr) {
     extern __shared__ __align__(16) unsigned char rs_smem[];
@@ -351,6 +438,8 @@ __global__ void __launch_bounds__(RS_WARPS * 32) router_select_kernel(
         for (int off = 16; off > 0; off >>= 1) xs2 += __shfl_xor_sync(0xffffffffu, xs2, off);
         // two fp32 logits closer than thr may be in either true order
         const float thr = thr_coef * fmaf(sqrtf(xs2), wnorm_max, bias_max);
+        // the same for the compensated values (twice their bound)
+        const float thr2 = thr2_coef * fmaf(sqrtf(xs2), wnorm_max, bias_max);
 
         // extract candidates in (logit desc, id asc) order until the cluster
         // that contains rank k-1 is closed
@@ -402,28 +491,38 @@ __global__ void __launch_bounds__(RS_WARPS * 32) router_select_kernel(
             while (b + 1 < R && (s_v[b] - s_v[b + 1]) <= thr) ++b;
             if (b > a) {
                 refined = true;
-                for (int m = a; m <= b; ++m) {
-                    const int e = s_e[m];
-                    double v = refine_dot(x + t * (int64_t)H, Wg + (int64_t)e * H, H, lane);
-                    if (bias) v += (double)bias[e];
-                    if (lane == 0) s_ref[m] = v;
-                }
-                __syncwarp();
-                if (lane == 0) {  // insertion sort of positions a..b: value desc, id asc
-                    for (int m = a + 1; m <= b; ++m) {
-                        const double v = s_ref[m];
+                // compensated fp32 values first; fp64 only if they still leave a gap
+                // within twice their bound (plus the fp64 rounding of the exact order)
+                for (int pass = 0; pass < 2; ++pass) {
+                    for (int m = a; m <= b; ++m) {
                         const int e = s_e[m];
-                        int q = m - 1;
-                        while (q >= a && (s_ref[q] < v || (s_ref[q] == v && s_e[q] > e))) {
-                            s_ref[q + 1] = s_ref[q];
-                            s_e[q + 1] = s_e[q];
-                            --q;
-                        }
-                        s_ref[q + 1] = v;
-                        s_e[q + 1] = e;
+                        const uint16_t* xr = x + t * (int64_t)H;
+                        const float* wr = Wg + (int64_t)e * H;
+                        double v = pass == 0 ? refine_dot2(xr, wr, H, lane) : refine_dot(xr, wr, H, lane);
+                        if (bias) v += (double)bias[e];
+                        if (lane == 0) s_ref[m] = v;
                     }
+                    __syncwarp();
+                    if (lane == 0) {  // insertion sort of positions a..b: value desc, id asc
+                        for (int m = a + 1; m <= b; ++m) {
+                            const double v = s_ref[m];
+                            const int e = s_e[m];
+                            int q = m - 1;
+                            while (q >= a && (s_ref[q] < v || (s_ref[q] == v && s_e[q] > e))) {
+                                s_ref[q + 1] = s_ref[q];
+                                s_e[q + 1] = s_e[q];
+                                --q;
+                            }
+                            s_ref[q + 1] = v;
+                            s_e[q + 1] = e;
+                        }
+                    }
+                    __syncwarp();
+                    if (pass == 1) break;
+                    bool decided = true;
+                    for (int m = a; m < b; ++m) decided = decided && (s_ref[m] - s_ref[m + 1] > (double)thr2);
+                    if (decided) break;
                 }
-                __syncwarp();
                 for (int m = a; m <= b; ++m) {  // refined values feed the softmax
                     const int e = s_e[m];
                     const float v = (float)s_ref[m];
@@ -553,6 +652,11 @@ cudaError_t launch_router(const RouterLaunch& L, int num_sms, cudaStream_t s) {
     const double g32 = chain_n * u32 / (1.0 - chain_n * u32);
     const double g64 = (L.H + 2.0) * u64 / (1.0 - (L.H + 2.0) * u64);
     const float thr_coef = (float)(2.0 * (g32 + g64) * 1.01);
+    // compensated recheck: (gamma_{ceil(H/128)} + gamma_128)^2 per value, plus
+    // the fp64 rounding of the exact order and of hi + lo + bias
+    const double na = (L.H + 127) / 128, nc = 128.0;
+    const double ga = na * u32 / (1.0 - na * u32), gc = nc * u32 / (1.0 - nc * u32);
+    const float thr2_coef = (float)(2.0 * ((ga + gc) * (ga + gc) + g64 + 3.0 * u64) * 1.01);
     const size_t smem = (size_t)RS_WARPS * L.E * (sizeof(double) + sizeof(int) + sizeof(float));
     const int64_t want = (L.T + RS_WARPS - 1) / RS_WARPS;
     const unsigned grid2 = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms * 8));
@@ -564,7 +668,7 @@ cudaError_t launch_router(const RouterLaunch& L, int num_sms, cudaStream_t s) {
             if (err != cudaSuccess) return err;                                                                  \
         }                                                                                                        \
         err = launch_k(router_select_kernel<PLV>, dim3(grid2), dim3(RS_WARPS * 32), smem, s, L.part, L.xsq,     \
-                       L.wsq, L.nsplit, thr_coef, L.bias, L.x, L.Wg, L.T, L.H, L.E, L.k, L.renorm, L.ids, L.w,    \
+                       L.wsq, L.nsplit, thr_coef, thr2_coef, L.bias, L.x, L.Wg, L.T, L.H, L.E, L.k, L.renorm, L.ids, L.w,    \
                        L.hdr);                                                                                   \
     } while (0)
     if (L.E <= 32)

@@ -128,3 +128,14 @@ def test_binding_rejects_cpu_tensors():
     with pytest.raises(ValueError):
         moe.moe_route(x, torch.zeros(8, 256), None, 2, True, torch.zeros(4, 2, dtype=torch.int32),
                       torch.zeros(4, 2), torch.zeros(1 << 20, dtype=torch.uint8))
+
+
+def test_rejected_calls_launch_nothing():
+    """Calls refused by host validation never reach a kernel launch, so the
+    library's launch count does not move."""
+    before = moe.moe_get_launch_count()
+    assert before >= 0
+    r = moe._lib.moe_route
+    assert r(None, FAKE, None, 16, 256, 8, 2, 1, FAKE, FAKE, FAKE, 1 << 30, None) == moe.MOE_ERR_INVALID_ARG
+    assert r(FAKE, FAKE, None, 16, 256, 8, 2, 1, FAKE, FAKE, FAKE, 64, None) == moe.MOE_ERR_WORKSPACE
+    assert moe.moe_get_launch_count() == before

@@ -157,8 +157,13 @@ def test_cuda_graph_replay_matches_eager_launches():
     inp = mi.make_inputs(MID)
     layer = layer_from_inputs(inp, "cuda")
     x = inp["x"].cuda()
+    c0 = moe.moe_get_launch_count()
     eager = layer.forward(x).clone()
+    per_forward = moe.moe_get_launch_count() - c0
+    assert per_forward >= 5  # router, permute, FC1, FC2, finalize at least
     g = layer.capture(x)
+    # capture runs one forward on a side stream, then records one: both count
+    assert moe.moe_get_launch_count() - c0 == 3 * per_forward
     layer.out.zero_()
     g.replay()
     torch.cuda.synchronize()
