@@ -31,8 +31,20 @@ int device_sms() {
 
 size_t a256(size_t v) { return (v + 255) & ~(size_t)255; }
 
+// Small batches split the shared expert's FC2 into K ranges of about the routed
+// FC2's length, so its tiles do not outlast the routed ones; the fp32 partials
+// are summed by the combine.
+constexpr int64_t kSplitMaxT = 128;
+constexpr int kSplitMax = 8;
+
+int shared_split(int64_t T, int I, int I_sh) {
+    if (I_sh <= 0 || T <= 0 || T > kSplitMaxT) return 1;
+    const int r = I_sh / I;
+    return r < 2 ? 1 : (r > kSplitMax ? kSplitMax : r);
+}
+
 struct ForwardLayout {
-    size_t h, h_sh, y, y_sh, total;
+    size_t h, h_sh, y, y_sh, y_sh_part, total;
 };
 
 ForwardLayout forward_layout(int64_t P_cap, int64_t T, int H, int I, int I_sh) {
@@ -46,6 +58,9 @@ ForwardLayout forward_layout(int64_t P_cap, int64_t T, int H, int I, int I_sh) {
     off += a256((size_t)P_cap * (size_t)H * 2);
     L.y_sh = off;
     off += a256((size_t)(I_sh > 0 ? T : 0) * (size_t)H * 2);
+    L.y_sh_part = off;
+    const int ks = shared_split(T, I, I_sh);
+    off += a256(ks > 1 ? (size_t)ks * (size_t)T * (size_t)H * 4 : 0);
     L.total = off;
     return L;
 }
@@ -102,6 +117,9 @@ size_t moe_workspace_size(int64_t max_T, int H, int I, int E, int S, int k, int 
     size_t need = route_need(max_T, H, E);
     need = std::max(need, permute_need(P, S));
     need = std::max(need, forward_layout(P, max_T, H, I, I_shared_total).total);
+    // a call with fewer tokens may split the shared FC2 (fp32 partials, largest at
+    // T = min(max_T, 128)) where max_T does not; every other region grows with T and P
+    need = std::max(need, forward_layout(P, std::min<int64_t>(max_T, kSplitMaxT), H, I, I_shared_total).total);
     return need;
 }
 
@@ -214,7 +232,7 @@ moe_status_t moe_permute(const int32_t* topk_ids, float* topk_w, int64_t T, int 
 static moe_status_t gemm_call(bool fc1, const moe_bf16_t* a, int64_t rows_cap, const int32_t* offsets, int G,
                               const moe_bf16_t* W, int H, int I, const moe_bf16_t* a_sh, int64_t T,
                               const moe_bf16_t* Ws, int I_sh, moe_bf16_t* out, moe_bf16_t* out_sh, void* ws,
-                              cudaStream_t s) {
+                              cudaStream_t s, float* out_sh_part = nullptr, int ksplit_sh = 1) {
     GemmLaunch L;
     L.swiglu = fc1;
     L.a = a;
@@ -233,6 +251,8 @@ static moe_status_t gemm_call(bool fc1, const moe_bf16_t* a, int64_t rows_cap, c
     L.Nb_sh = fc1 ? 2 * I_sh : H;
     L.N_out_sh = fc1 ? I_sh : H;
     L.out_sh = out_sh;
+    L.out_sh_part = out_sh_part;
+    L.ksplit_sh = ksplit_sh;
     L.hdr = static_cast<WsHeader*>(ws);
     L.timeout_ns = g_timeout_ns.load();
     L.pair_mode = g_pair_mode.load();
@@ -276,6 +296,28 @@ moe_status_t moe_grouped_fc2(const moe_bf16_t* h, int64_t rows_cap, const int32_
                      (cudaStream_t)stream);
 }
 
+static moe_status_t finalize_call(const moe_bf16_t* y, int64_t rows_cap, const int32_t* pair_row,
+                                  const float* topk_w, int64_t T, int k, int H, const moe_bf16_t* y_shared,
+                                  const float* y_shared_part, int ksplit, const moe_bf16_t* x,
+                                  const moe_bf16_t* shared_gate_w, moe_bf16_t* out, void* ws, cudaStream_t s) {
+    FinalizeLaunch L;
+    L.y = y;
+    L.rows_cap = rows_cap;
+    L.pair_row = pair_row;
+    L.w = topk_w;
+    L.T = T;
+    L.k = k;
+    L.H = H;
+    L.y_sh = y_shared;
+    L.y_sh_part = y_shared_part;
+    L.ksplit = ksplit;
+    L.x = x;
+    L.gate_w = shared_gate_w;
+    L.out = out;
+    L.hdr = static_cast<WsHeader*>(ws);
+    return cuda_status(launch_finalize(L, device_sms(), s));
+}
+
 moe_status_t moe_finalize(const moe_bf16_t* y, int64_t rows_cap, const int32_t* pair_row, const float* topk_w,
                           int64_t T, int k, int H, const moe_bf16_t* y_shared, const moe_bf16_t* x,
                           const moe_bf16_t* shared_gate_w, moe_bf16_t* out, void* ws, size_t ws_bytes,
@@ -286,20 +328,8 @@ moe_status_t moe_finalize(const moe_bf16_t* y, int64_t rows_cap, const int32_t* 
     if (!pair_row || !topk_w || !out || (rows_cap > 0 && !y)) return MOE_ERR_INVALID_ARG;
     if (shared_gate_w && (!x || !y_shared)) return MOE_ERR_INVALID_ARG;
     if (!ws || ws_bytes < kWsHeaderBytes) return MOE_ERR_WORKSPACE;
-    FinalizeLaunch L;
-    L.y = y;
-    L.rows_cap = rows_cap;
-    L.pair_row = pair_row;
-    L.w = topk_w;
-    L.T = T;
-    L.k = k;
-    L.H = H;
-    L.y_sh = y_shared;
-    L.x = x;
-    L.gate_w = shared_gate_w;
-    L.out = out;
-    L.hdr = static_cast<WsHeader*>(ws);
-    return cuda_status(launch_finalize(L, device_sms(), (cudaStream_t)stream));
+    return finalize_call(y, rows_cap, pair_row, topk_w, T, k, H, y_shared, nullptr, 0, x, shared_gate_w, out, ws,
+                         (cudaStream_t)stream);
 }
 
 moe_status_t moe_forward(const moe_bf16_t* x_perm, const int32_t* offsets, int S_local, int64_t P_cap,
@@ -327,9 +357,13 @@ moe_status_t moe_forward(const moe_bf16_t* x_perm, const int32_t* offsets, int S
     moe_status_t st = gemm_call(true, x_perm, P_cap, offsets, S_local, W1, H, I, x, T, W1s, I_shared_total, h, h_sh,
                                 ws, s);
     if (st != MOE_OK) return st;
-    st = gemm_call(false, h, P_cap, offsets, S_local, W2, H, I, h_sh, T, W2s, I_shared_total, y, y_sh, ws, s);
+    const int ks = shared_split(T, I, I_shared_total);
+    float* y_sh_part = ks > 1 ? reinterpret_cast<float*>(base + FL.y_sh_part) : nullptr;
+    st = gemm_call(false, h, P_cap, offsets, S_local, W2, H, I, h_sh, T, W2s, I_shared_total, y, y_sh, ws, s,
+                   y_sh_part, ks);
     if (st != MOE_OK) return st;
-    return moe_finalize(y, P_cap, pair_row, topk_w, T, k, H, y_sh, x, shared_gate_w, out, ws, ws_bytes, stream);
+    return finalize_call(y, P_cap, pair_row, topk_w, T, k, H, y_sh_part ? nullptr : y_sh, y_sh_part, ks, x,
+                         shared_gate_w, out, ws, s);
 }
 
 moe_status_t moe_debug_wait_timeout(void* ws, size_t ws_bytes, uint64_t timeout_ns, moe_stream_t stream) {

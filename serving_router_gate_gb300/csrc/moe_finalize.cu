@@ -20,7 +20,9 @@
 //      expert's vector before using them and accumulates in fp32 in fixed j
 //      order:
 //        acc = fma(w_j, y[row_j], acc) for j = 0..k-1 (rows of -1 skipped),
-//        acc = fma(g, y_shared, acc), out = bf16_rn(acc).
+//        acc = fma(g, y_shared, acc), out = bf16_rn(acc),
+//      where y_shared is the bf16 shared-expert row or, when the shared FC2 ran
+//      with its K split, the fp32 sum of its partial rows in range order.
 // TB is picked on the host so that there are at least two blocks per SM when
 // the batch allows; with one token (TB = 1) all 256 threads share its row.
 #include <algorithm>
@@ -41,8 +43,8 @@ constexpr int FZ_BATCH = 8;  // pair loads issued together
 __global__ void __launch_bounds__(FZ_THREADS, 4) finalize_kernel(
     const uint16_t* __restrict__ y, int64_t rows_cap, const int32_t* __restrict__ pair_row,
     const float* __restrict__ w, int64_t T, int k, int H, int TB, const uint16_t* __restrict__ y_sh,
-    const uint16_t* __restrict__ x, const uint16_t* __restrict__ gate_w, uint16_t* __restrict__ out,
-    int32_t* status) {
+    const float* __restrict__ y_sh_part, int ksplit, const uint16_t* __restrict__ x,
+    const uint16_t* __restrict__ gate_w, uint16_t* __restrict__ out, int32_t* status) {
     __shared__ int32_t s_row[FZ_TB][FZ_MAXK];
     __shared__ float s_w[FZ_TB][FZ_MAXK];
     __shared__ float s_g[FZ_TB];
@@ -51,7 +53,8 @@ __global__ void __launch_bounds__(FZ_THREADS, 4) finalize_kernel(
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int vec = H / 8;
-    const bool gated = (y_sh != nullptr) && (gate_w != nullptr);
+    const bool has_sh = (y_sh != nullptr) || (y_sh_part != nullptr);
+    const bool gated = has_sh && (gate_w != nullptr);
     const int64_t nblk = (T + TB - 1) / TB;
     for (int64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
         const int64_t t0 = blk * TB;
@@ -91,8 +94,22 @@ __global__ void __launch_bounds__(FZ_THREADS, 4) finalize_kernel(
             float acc[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-            const uint4 sh = y_sh ? __ldg(reinterpret_cast<const uint4*>(y_sh + (t0 + tt) * H) + v)
-                                  : make_uint4(0, 0, 0, 0);
+            float shf[8];
+            if (y_sh_part) {
+                // split shared expert: fp32 partials of its K ranges, added in range order
+                const float4* pp = reinterpret_cast<const float4*>(y_sh_part + (t0 + tt) * H) + 2 * v;
+                const int64_t stride = T * (int64_t)H / 4;
+                float4 lo = __ldg(pp), hi = __ldg(pp + 1);
+                for (int q = 1; q < ksplit; ++q) {
+                    const float4 a = __ldg(pp + q * stride), b = __ldg(pp + q * stride + 1);
+                    lo.x += a.x; lo.y += a.y; lo.z += a.z; lo.w += a.w;
+                    hi.x += b.x; hi.y += b.y; hi.z += b.z; hi.w += b.w;
+                }
+                shf[0] = lo.x; shf[1] = lo.y; shf[2] = lo.z; shf[3] = lo.w;
+                shf[4] = hi.x; shf[5] = hi.y; shf[6] = hi.z; shf[7] = hi.w;
+            } else if (y_sh) {
+                unpack8(__ldg(reinterpret_cast<const uint4*>(y_sh + (t0 + tt) * H) + v), shf);
+            }
             for (int j0 = 0; j0 < k; j0 += FZ_BATCH) {
                 uint4 ld[FZ_BATCH];
                 int32_t rr[FZ_BATCH];
@@ -113,12 +130,10 @@ __global__ void __launch_bounds__(FZ_THREADS, 4) finalize_kernel(
                     for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, fv[i], acc[i]);
                 }
             }
-            if (y_sh) {
+            if (has_sh) {
                 const float g = gated ? s_g[tt] : 1.0f;
-                float fv[8];
-                unpack8(sh, fv);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) acc[i] = fmaf(g, fv[i], acc[i]);
+                for (int i = 0; i < 8; ++i) acc[i] = fmaf(g, shf[i], acc[i]);
             }
             uint4 o;
             o.x = pack_bf16x2(acc[0], acc[1]);
@@ -140,7 +155,8 @@ cudaError_t launch_finalize(const FinalizeLaunch& L, int num_sms, cudaStream_t s
     const int64_t nblk = (L.T + TB - 1) / TB;
     const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(nblk, (int64_t)num_sms * 4));
     return launch_k(finalize_kernel, dim3(grid), dim3(FZ_THREADS), 0, s, L.y, L.rows_cap, L.pair_row, L.w, L.T, L.k,
-                    L.H, TB, L.y_sh, L.x, L.gate_w, L.out, L.hdr ? &L.hdr->status : nullptr);
+                    L.H, TB, L.y_sh, L.y_sh_part, L.y_sh_part ? L.ksplit : 0, L.x, L.gate_w, L.out,
+                    L.hdr ? &L.hdr->status : nullptr);
 }
 
 }  // namespace moe

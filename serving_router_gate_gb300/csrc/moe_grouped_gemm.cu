@@ -84,6 +84,9 @@ struct GemmParams {
     int64_t T_sh;            // rows of the shared problem (0: none)
     uint16_t* out;
     uint16_t* out_sh;
+    float* out_sh_part;      // FC2, split shared problem: fp32 partials [ksplit_sh, T_sh, N_out_sh]
+    int ksplit_sh;           // K ranges of the shared problem (1: not split)
+    int kb_split_sh;         // K steps per range
     int32_t* status;
     uint64_t timeout_ns;
 };
@@ -112,6 +115,8 @@ struct Tile {
     int nt;          // n-tile
     int row0;        // first row in A / out of this CTA's m-tile
     int rows_valid;  // rows of this CTA's m-tile that belong to the group (may be 0)
+    int ks;          // K range of a split shared tile (0 otherwise)
+    int kb0, kb1;    // K steps [kb0, kb1) of this tile
 };
 
 // work units along M: pairs of m-tiles in pair mode, single m-tiles otherwise
@@ -125,12 +130,17 @@ __device__ __forceinline__ Tile tile_of(int u, const GemmParams& p, const SmemMe
                                         int crank) {
     Tile tl;
     if (u < n_sh_tiles) {
+        // split shared tiles: the K ranges of one output tile are consecutive units
         tl.prob = 1;
         tl.g = 0;
-        tl.nt = u / mu_sh;
-        const int mt = kPair ? 2 * (u % mu_sh) + crank : u % mu_sh;
+        tl.ks = u % p.ksplit_sh;
+        const int v = u / p.ksplit_sh;
+        tl.nt = v / mu_sh;
+        const int mt = kPair ? 2 * (v % mu_sh) + crank : v % mu_sh;
         tl.row0 = mt * BM;
         tl.rows_valid = (int)max((int64_t)0, min((int64_t)BM, p.T_sh - (int64_t)mt * BM));
+        tl.kb0 = tl.ks * p.kb_split_sh;
+        tl.kb1 = min(p.K_sh / BK, tl.kb0 + p.kb_split_sh);
         return tl;
     }
     u -= n_sh_tiles;
@@ -152,6 +162,9 @@ __device__ __forceinline__ Tile tile_of(int u, const GemmParams& p, const SmemMe
     const int mt = kPair ? 2 * (local % MU) + crank : local % MU;
     tl.row0 = m.off[g] + mt * BM;
     tl.rows_valid = max(0, min(BM, M - mt * BM));
+    tl.ks = 0;
+    tl.kb0 = 0;
+    tl.kb1 = p.K / BK;
     return tl;
 }
 
@@ -256,7 +269,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     const uint32_t tmem_base = m.tmem_base;
     const int mu_sh = p.T_sh > 0 ? units_of<kPair>((int)((p.T_sh + BM - 1) / BM)) : 0;
-    const int n_sh_tiles = p.T_sh > 0 ? mu_sh * ((p.N_out_sh + OW - 1) / OW) : 0;
+    const int n_sh_tiles = p.T_sh > 0 ? mu_sh * ((p.N_out_sh + OW - 1) / OW) * p.ksplit_sh : 0;
     const int total_tiles = n_sh_tiles + m.routed_tiles;
     const volatile int* abortp = &m.abort;
 
@@ -273,7 +286,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const bool short_a = tl.rows_valid <= BM_SHORT;
                 const CUtensorMap* mA = tl.prob ? (short_a ? &tmAs32 : &tmAs) : (short_a ? &tmA32 : &tmA);
                 const CUtensorMap* mB = tl.prob ? &tmBs : &tmB;
-                const int nkb = (tl.prob ? p.K_sh : p.K) / BK;
                 const int up = tl.prob ? p.up_off_sh : p.up_off;
                 const uint32_t a_bytes = short_a ? A_SHORT_BYTES : A_BYTES;
                 uint32_t pair_bytes = 0;  // pair mode: bytes of both CTAs, counted by the leader
@@ -281,7 +293,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const Tile other = tile_of<kFC1, kPair>(u, p, m, n_sh_tiles, mu_sh, crank ^ 1);
                     pair_bytes = a_bytes + (other.rows_valid <= BM_SHORT ? A_SHORT_BYTES : A_BYTES) + 2 * B_BYTES;
                 }
-                for (int kb = 0; kb < nkb; ++kb) {
+                for (int kb = tl.kb0; kb < tl.kb1; ++kb) {
                     if (!mbar_wait(&m.empty[stage], phase ^ 1u, p.timeout_ns, abortp)) {
                         failed = true;
                         break;
@@ -340,7 +352,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int i = 0;
             for (int u = unit0; u < total_tiles && !failed; u += nunits, ++i) {
                 const Tile tl = tile_of<kFC1, kPair>(u, p, m, n_sh_tiles, mu_sh, crank);
-                const int nkb = (tl.prob ? p.K_sh : p.K) / BK;
+                const int nkb = tl.kb1 - tl.kb0;
                 const int buf = i & 1;
                 if (!mbar_wait(&m.tempty[buf], (uint32_t)(((i >> 1) & 1) ^ 1), p.timeout_ns, abortp)) {
                     failed = true;
@@ -442,6 +454,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
                             dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                    }
+                }
+            } else if (tl.prob && p.ksplit_sh > 1) {
+                // K range ks of a split shared tile: fp32 partial sums, added up in fixed
+                // range order by the combine
+                float* prow = p.out_sh_part + ((int64_t)tl.ks * p.T_sh + tl.row0 + row_in) * N_out;
+#pragma unroll 1
+                for (int c = 0; c < OW; c += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(taddr + (uint32_t)c, r);
+                    tmem_ld_wait();
+                    const int col = tl.nt * OW + c;
+                    if (valid && col < N_out) {
+                        float4* dst = reinterpret_cast<float4*>(prow + col);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            dst[e] = make_float4(__uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1]),
+                                                 __uint_as_float(r[4 * e + 2]), __uint_as_float(r[4 * e + 3]));
                     }
                 }
             } else {
@@ -661,6 +691,9 @@ cudaError_t launch_bn(const GemmLaunch& L, int num_sms, int64_t bound, cudaStrea
     p.up_off_sh = kFC1 ? L.Nb_sh / 2 : 0;
     p.rows_cap = L.rows_cap;
     p.T_sh = has_shared ? L.T_sh : 0;
+    p.out_sh_part = L.out_sh_part;
+    p.ksplit_sh = (has_shared && !L.swiglu && L.out_sh_part && L.ksplit_sh > 1) ? L.ksplit_sh : 1;
+    p.kb_split_sh = (L.K_sh / BK + p.ksplit_sh - 1) / p.ksplit_sh;
     p.out = L.out;
     p.out_sh = L.out_sh;
     p.status = &L.hdr->status;
@@ -687,6 +720,11 @@ cudaError_t launch_bn(const GemmLaunch& L, int num_sms, int64_t bound, cudaStrea
 
 // Upper bound of the tiles of a launch with MMA N = bn (single CTAs): at most
 // min(G, rows) groups are non-empty, each adding at most one partial m-tile.
+// K ranges of the shared problem: FC2 only, when the caller supplied a partial buffer
+int split_of(const GemmLaunch& L) {
+    return (!L.swiglu && L.out_sh_part && L.ksplit_sh > 1) ? L.ksplit_sh : 1;
+}
+
 int64_t tile_bound(const GemmLaunch& L, int bn) {
     const int ow = L.swiglu ? bn / 2 : bn;
     int64_t bound = 0;
@@ -694,18 +732,22 @@ int64_t tile_bound(const GemmLaunch& L, int bn) {
         bound += (int64_t)((L.N_out + ow - 1) / ow) *
                  ((L.rows_cap + BM - 1) / BM + std::min<int64_t>(L.G, L.rows_cap));
     if (L.T_sh > 0 && L.b_sh != nullptr && L.N_out_sh > 0)
-        bound += (int64_t)((L.N_out_sh + ow - 1) / ow) * ((L.T_sh + BM - 1) / BM);
+        bound += (int64_t)((L.N_out_sh + ow - 1) / ow) * ((L.T_sh + BM - 1) / BM) * split_of(L);
     return bound;
 }
 
 template <bool kFC1>
 cudaError_t dispatch(const GemmLaunch& L, int num_sms, cudaStream_t s, const char** why) {
     const int64_t b256 = tile_bound(L, 256);
-    const bool pair = L.pair_mode == 2 ? b256 >= 2 : (L.pair_mode == 1 && b256 >= 4 * (int64_t)num_sms);
+    const bool pair = split_of(L) == 1 &&
+                      (L.pair_mode == 2 ? b256 >= 2 : (L.pair_mode == 1 && b256 >= 4 * (int64_t)num_sms));
     if (pair) return launch_bn<kFC1, true, 256>(L, num_sms, b256, s, why);
-    // the widest N that still gives every SM two tiles (small batches stream
-    // weights; narrower tiles spread them over more SMs, with deeper rings)
-    if (b256 >= 2 * (int64_t)num_sms) return launch_bn<kFC1, false, 256>(L, num_sms, b256, s, why);
+    // Small batches (at most 1024 routed rows) stream weights: N = 256 moves the
+    // most bytes per pipeline stage, and a stage costs about the same time
+    // whatever its size, so the widest tile wins even with SMs left idle.
+    // Otherwise the widest N that still gives every SM two tiles.
+    if (L.rows_cap <= 1024 || b256 >= 2 * (int64_t)num_sms)
+        return launch_bn<kFC1, false, 256>(L, num_sms, b256, s, why);
     const int64_t b128 = tile_bound(L, 128);
     if (b128 >= 2 * (int64_t)num_sms) return launch_bn<kFC1, false, 128>(L, num_sms, b128, s, why);
     return launch_bn<kFC1, false, 64>(L, num_sms, tile_bound(L, 64), s, why);

@@ -124,20 +124,6 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
-// Bulk prefetch of one tensor-map box into L2 (no shared memory, no barrier).
-__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int c0, int c1) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(c0), "r"(c1)
-                 : "memory");
-}
-__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int c0, int c1, int c2) {
-    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(c0), "r"(c1), "r"(c2)
-                 : "memory");
-}
-
 __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
@@ -399,6 +385,8 @@ struct GemmLaunch {
     const uint16_t* b_sh;      // shared B [Nb_sh, K_sh]
     int K_sh, Nb_sh, N_out_sh;
     uint16_t* out_sh;          // [T_sh, N_out_sh]
+    float* out_sh_part;        // FC2 only, or null: split the shared problem's K into ksplit_sh ranges
+    int ksplit_sh;             // and write fp32 partials [ksplit_sh, T_sh, N_out_sh] here (out_sh unused)
     WsHeader* hdr;
     uint64_t timeout_ns;
     int pair_mode;             // 0 single CTAs only, 1 pairs for large launches, 2 pairs whenever possible
@@ -413,6 +401,8 @@ struct FinalizeLaunch {
     int64_t T;
     int k, H;
     const uint16_t* y_sh;
+    const float* y_sh_part;    // or null: fp32 partials [ksplit, T, H] of the shared expert, summed in order
+    int ksplit;
     const uint16_t* x;
     const uint16_t* gate_w;
     uint16_t* out;

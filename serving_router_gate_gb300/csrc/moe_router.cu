@@ -48,7 +48,6 @@ constexpr int RT_TARGET_MAX = 2048;  // upper bound on CTAs the split plan aims 
 constexpr int RT_MAX_SPLIT = 32;
 
 constexpr int RS_WARPS = 8;      // select: tokens (warps) per CTA
-constexpr int RS_MAXE = 512;
 
 __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc, bool valid) {
     // 16-byte global->shared copy; zero-fills when !valid (source size 0)

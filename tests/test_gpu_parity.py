@@ -227,6 +227,38 @@ def test_stages_fc1_fc2_finalize_against_oracle_rows():
     check_out(out, ref["out"])
 
 
+def test_small_batch_splits_shared_fc2_and_matches_unsplit_stages():
+    """At most 128 tokens: moe_forward splits the shared expert's FC2 over K into
+    fp32 partials (I_sh / I ranges, here 4) summed by the combine.  The result
+    agrees with the unsplit stage-by-stage path (bf16 shared output) to within
+    one bf16 rounding of the shared term, and with the oracle."""
+    cfg = mi.MoEConfig("split", T=37, H=256, I=128, E=9, k=3, renorm=False, n_shared=2, I_shared=256,
+                       shared_gate=True)
+    inp = mi.make_inputs(cfg)
+    g = run_gpu(inp)
+    layer = g["layer"]
+    check_out(g["out"], oracle_layer(to_cpu(inp))["out"])
+    dev = torch.device("cuda")
+    P = cfg.T * cfg.k
+    Ish = cfg.n_shared * cfg.I_shared
+    h = torch.empty((P, cfg.I), dtype=torch.bfloat16, device=dev)
+    y = torch.empty((P, cfg.H), dtype=torch.bfloat16, device=dev)
+    h_sh = torch.empty((cfg.T, Ish), dtype=torch.bfloat16, device=dev)
+    y_sh = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=dev)
+    W1s, W2s = mi.shared_concat(inp["W1s"], inp["W2s"])
+    x = inp["x"].cuda()
+    moe.moe_grouped_fc1(layer.x_perm, layer.offsets, layer.W1, x, W1s.cuda(), h, h_sh, layer.ws)
+    moe.moe_grouped_fc2(h, layer.offsets, layer.W2, h_sh, W2s.cuda(), y, y_sh, layer.ws)
+    moe.moe_finalize(y, layer.pair_row, layer.topk_w, y_sh, x, inp["w_s"].cuda(), out, layer.ws)
+    torch.cuda.synchronize()
+    a, b = out.float(), g["out"].float().to(dev)
+    # the two differ by the bf16 rounding of y_shared (and the output rounding)
+    tol = 2.0 ** -7 * (y_sh.float().abs() + a.abs()) + 1e-6
+    assert bool(((a - b).abs() <= tol).all())
+    assert moe.moe_get_device_status(layer.ws) == 0
+
+
 # --------------------------------------------------------------------------- device-side error paths
 
 def test_out_of_range_expert_ids_are_dropped_and_flagged():
