@@ -39,11 +39,13 @@ METRIC = "MoE-layer tokens/s at 1 GB300; % of BF16 tensor peak (prefill) / HBM B
 DEFAULT_WORKLOAD = "qwen2_moe_like_prefill"
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant kernel,
-# from one ncu capture (profiles/), valid only while the kernel source hashes to
+# from one ncu capture of that workload, valid only while the kernel source hashes to
 # the recorded value.
 NCU_TRAFFIC = {
-    # profiles/grouped_gemm_qwen2_moe_like_prefill.md: 822.35 MB read + 87.58 MB written
-    ("qwen2_moe_like_prefill", "8066cc6a28812a00"): 909.93e6,
+    # FC1 of the first forward, ncu --set full: 822.35 MB read + 88.17 MB written
+    ("qwen2_moe_like_prefill", "e290cf4b326bbfbe"): 910.52e6,
+    # FC1 of the first forward, ncu --set full: 115.41 MB read + 3.18 MB written
+    ("dsv2_lite_like_decode_t1", "e290cf4b326bbfbe"): 118.60e6,
 }
 
 
