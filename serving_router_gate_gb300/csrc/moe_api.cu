@@ -232,7 +232,8 @@ moe_status_t moe_permute(const int32_t* topk_ids, float* topk_w, int64_t T, int 
 static moe_status_t gemm_call(bool fc1, const moe_bf16_t* a, int64_t rows_cap, const int32_t* offsets, int G,
                               const moe_bf16_t* W, int H, int I, const moe_bf16_t* a_sh, int64_t T,
                               const moe_bf16_t* Ws, int I_sh, moe_bf16_t* out, moe_bf16_t* out_sh, void* ws,
-                              cudaStream_t s, float* out_sh_part = nullptr, int ksplit_sh = 1) {
+                              cudaStream_t s, float* out_sh_part = nullptr, int ksplit_sh = 1,
+                              int64_t max_group_rows = -1) {
     GemmLaunch L;
     L.swiglu = fc1;
     L.a = a;
@@ -256,6 +257,8 @@ static moe_status_t gemm_call(bool fc1, const moe_bf16_t* a, int64_t rows_cap, c
     L.hdr = static_cast<WsHeader*>(ws);
     L.timeout_ns = g_timeout_ns.load();
     L.pair_mode = g_pair_mode.load();
+    // a token adds at most one row to a slot, so a group has at most T rows
+    L.max_group_rows = max_group_rows >= 0 ? std::min<int64_t>(max_group_rows, rows_cap) : rows_cap;
     const char* why = nullptr;
     return cuda_status(launch_grouped_gemm(L, device_sms(), s, &why));
 }
@@ -355,12 +358,12 @@ moe_status_t moe_forward(const moe_bf16_t* x_perm, const int32_t* offsets, int S
     moe_bf16_t* y_sh = I_shared_total > 0 ? reinterpret_cast<moe_bf16_t*>(base + FL.y_sh) : nullptr;
     cudaStream_t s = (cudaStream_t)stream;
     moe_status_t st = gemm_call(true, x_perm, P_cap, offsets, S_local, W1, H, I, x, T, W1s, I_shared_total, h, h_sh,
-                                ws, s);
+                                ws, s, nullptr, 1, T);
     if (st != MOE_OK) return st;
     const int ks = shared_split(T, I, I_shared_total);
     float* y_sh_part = ks > 1 ? reinterpret_cast<float*>(base + FL.y_sh_part) : nullptr;
     st = gemm_call(false, h, P_cap, offsets, S_local, W2, H, I, h_sh, T, W2s, I_shared_total, y, y_sh, ws, s,
-                   y_sh_part, ks);
+                   y_sh_part, ks, T);
     if (st != MOE_OK) return st;
     return finalize_call(y, P_cap, pair_row, topk_w, T, k, H, y_sh_part ? nullptr : y_sh, y_sh_part, ks, x,
                          shared_gate_w, out, ws, s);

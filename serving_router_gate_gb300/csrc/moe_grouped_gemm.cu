@@ -59,15 +59,18 @@ constexpr int A_SHORT_BYTES = BM_SHORT * BK * 2;
 constexpr int NUM_THREADS = 192;
 constexpr int MAX_GROUPS = 1024;
 constexpr int MAX_STAGES = 8;
-constexpr int RING_BYTES = 192 * 1024;  // shared memory for the operand ring
+constexpr int RING_BYTES = 216 * 1024;  // shared memory for the operand ring
 constexpr uint16_t PAIR_MASK = 0x3;
 
 // per instantiation: MMA N = BN (256 for large launches, 128 / 64 to spread
 // small ones over more CTAs); a CTA holds all of B (single) or its half (pair)
-template <bool kPair, int BN>
+template <bool kPair, int BN, bool kShort = false>
 struct Cfg {
     static constexpr int B_BYTES = (kPair ? BN / 2 : BN) * BK * 2;
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    // kShort: every tile has at most 32 rows, so an A slot holds 32 rows (the MMA
+    // still reads 128 rows from the slot onward; rows past 32 are never stored)
+    static constexpr int A_SLOT = kShort ? A_SHORT_BYTES : A_BYTES;
+    static constexpr int STAGE_BYTES = A_SLOT + B_BYTES;
     static constexpr int STAGES = RING_BYTES / STAGE_BYTES < MAX_STAGES ? RING_BYTES / STAGE_BYTES : MAX_STAGES;
     static constexpr int TMEM_COLS = 2 * BN;  // two accumulators of BN fp32 columns
     // 2-CTA MMA: M = 256 across the pair
@@ -104,9 +107,10 @@ struct SmemMeta {
     int ts[MAX_GROUPS + 1];
 };
 
-template <bool kPair, int BN>
+template <bool kPair, int BN, bool kShort>
 constexpr size_t smem_bytes() {
-    return 1024 /*alignment slack*/ + (size_t)Cfg<kPair, BN>::STAGES * Cfg<kPair, BN>::STAGE_BYTES + sizeof(SmemMeta);
+    return 1024 /*alignment slack*/ + (size_t)Cfg<kPair, BN, kShort>::STAGES * Cfg<kPair, BN, kShort>::STAGE_BYTES +
+           sizeof(SmemMeta);
 }
 
 struct Tile {
@@ -168,23 +172,25 @@ __device__ __forceinline__ Tile tile_of(int u, const GemmParams& p, const SmemMe
     return tl;
 }
 
-template <bool kFC1, bool kPair, int BN>
+template <bool kFC1, bool kPair, int BN, bool kShort>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmAs,
                         const __grid_constant__ CUtensorMap tmBs, const __grid_constant__ CUtensorMap tmA32,
                         const __grid_constant__ CUtensorMap tmAs32) {
-    constexpr int STAGES = Cfg<kPair, BN>::STAGES;
-    constexpr int B_BYTES = Cfg<kPair, BN>::B_BYTES;
-    constexpr int STAGE_BYTES = Cfg<kPair, BN>::STAGE_BYTES;
-    constexpr uint32_t IDESC = Cfg<kPair, BN>::IDESC;
-    constexpr int TMEM_COLS = Cfg<kPair, BN>::TMEM_COLS;
+    using C = Cfg<kPair, BN, kShort>;
+    constexpr int STAGES = C::STAGES;
+    constexpr int B_BYTES = C::B_BYTES;
+    constexpr int A_SLOT = C::A_SLOT;
+    constexpr uint32_t IDESC = C::IDESC;
+    constexpr int TMEM_COLS = C::TMEM_COLS;
+    static_assert(!kShort || !kPair, "short tiles run in single mode");
     static_assert(!kPair || BN == 256, "pair mode uses N = 256");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t* smA = smem;
-    uint8_t* smB = smem + (size_t)STAGES * A_BYTES;
-    SmemMeta& m = *reinterpret_cast<SmemMeta*>(smem + (size_t)STAGES * STAGE_BYTES);
+    uint8_t* smB = smem + (size_t)STAGES * A_SLOT;
+    SmemMeta& m = *reinterpret_cast<SmemMeta*>(smem + (size_t)STAGES * C::STAGE_BYTES);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -283,7 +289,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const Tile tl = tile_of<kFC1, kPair>(u, p, m, n_sh_tiles, mu_sh, crank);
                 // a tile with at most 32 rows of its group loads only 32 A rows: the MMA
                 // still reads 128, but rows past the group's count are never stored
-                const bool short_a = tl.rows_valid <= BM_SHORT;
+                const bool short_a = kShort || tl.rows_valid <= BM_SHORT;
                 const CUtensorMap* mA = tl.prob ? (short_a ? &tmAs32 : &tmAs) : (short_a ? &tmA32 : &tmA);
                 const CUtensorMap* mB = tl.prob ? &tmBs : &tmB;
                 const int up = tl.prob ? p.up_off_sh : p.up_off;
@@ -298,7 +304,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         failed = true;
                         break;
                     }
-                    uint8_t* a_dst = smA + (size_t)stage * A_BYTES;
+                    uint8_t* a_dst = smA + (size_t)stage * A_SLOT;
                     uint8_t* b_dst = smB + (size_t)stage * B_BYTES;
                     if (kPair) {
                         // this CTA's A rows and its 128-row half of B; the bytes of both
@@ -366,7 +372,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a0 = smem_u32(smA + (size_t)stage * A_BYTES);
+                    const uint32_t a0 = smem_u32(smA + (size_t)stage * A_SLOT);
                     const uint32_t b0 = smem_u32(smB + (size_t)stage * B_BYTES);
 #pragma unroll
                     for (int kk = 0; kk < BK / UMMA_K; ++kk) {
@@ -423,7 +429,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             tc_fence_after();
             const uint32_t taddr = tmem_base + (uint32_t)(buf * BN) + ((uint32_t)(q * 32) << 16);
-            const bool valid = row_in < tl.rows_valid;
+            // short-tile launches hold 32 A rows: a taller tile (a caller's bound was
+            // wrong) is reported and only its first 32 rows are stored
+            if (kShort && tl.rows_valid > BM_SHORT && row_in == 0) report(p.status, MOE_ERR_DEVICE_BOUNDS);
+            const bool valid = row_in < (kShort ? min(tl.rows_valid, BM_SHORT) : tl.rows_valid);
             const int N_out = tl.prob ? p.N_out_sh : p.N_out;
             uint16_t* out = tl.prob ? p.out_sh : p.out;
             uint16_t* orow = out + (int64_t)(tl.row0 + row_in) * N_out;
@@ -582,7 +591,7 @@ struct KernelInfo {
     int max_clusters = 0;
 };
 
-template <bool kFC1, bool kPair, int BN>
+template <bool kFC1, bool kPair, int BN, bool kShort>
 cudaError_t kernel_info(int num_sms, KernelInfo* out) {
     static std::mutex mu;
     static KernelInfo info[64];
@@ -592,15 +601,15 @@ cudaError_t kernel_info(int num_sms, KernelInfo* out) {
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(mu);
     if (!info[dev].ready) {
-        err = cudaFuncSetAttribute(grouped_gemm_kernel<kFC1, kPair, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)smem_bytes<kPair, BN>());
+        err = cudaFuncSetAttribute(grouped_gemm_kernel<kFC1, kPair, BN, kShort>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)smem_bytes<kPair, BN, kShort>());
         if (err != cudaSuccess) return err;
         int clusters = 0;
         if (kPair) {
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(2 * num_sms);
             cfg.blockDim = dim3(NUM_THREADS);
-            cfg.dynamicSmemBytes = smem_bytes<kPair, BN>();
+            cfg.dynamicSmemBytes = smem_bytes<kPair, BN, kShort>();
             cudaLaunchAttribute attr;
             attr.id = cudaLaunchAttributeClusterDimension;
             attr.val.clusterDim.x = 2;
@@ -608,7 +617,7 @@ cudaError_t kernel_info(int num_sms, KernelInfo* out) {
             attr.val.clusterDim.z = 1;
             cfg.attrs = &attr;
             cfg.numAttrs = 1;
-            err = cudaOccupancyMaxActiveClusters(&clusters, grouped_gemm_kernel<kFC1, kPair, BN>, &cfg);
+            err = cudaOccupancyMaxActiveClusters(&clusters, grouped_gemm_kernel<kFC1, kPair, BN, kShort>, &cfg);
             if (err != cudaSuccess) return err;
         }
         info[dev].max_clusters = clusters;
@@ -618,14 +627,14 @@ cudaError_t kernel_info(int num_sms, KernelInfo* out) {
     return cudaSuccess;
 }
 
-template <bool kFC1, bool kPair, int BN>
+template <bool kFC1, bool kPair, int BN, bool kShort>
 cudaError_t launch_kernel(const GemmParams& p, const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mAs,
                           const CUtensorMap& mBs, const CUtensorMap& mA32, const CUtensorMap& mAs32, unsigned grid,
                           cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(NUM_THREADS);
-    cfg.dynamicSmemBytes = smem_bytes<kPair, BN>();
+    cfg.dynamicSmemBytes = smem_bytes<kPair, BN, kShort>();
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     int n = 0;
@@ -644,11 +653,11 @@ cudaError_t launch_kernel(const GemmParams& p, const CUtensorMap& mA, const CUte
     cfg.attrs = attr;
     cfg.numAttrs = n;
     count_launch();
-    return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<kFC1, kPair, BN>, p, mA, mB, mAs, mBs, mA32, mAs32);
+    return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<kFC1, kPair, BN, kShort>, p, mA, mB, mAs, mBs, mA32, mAs32);
 }
 
 // Tensor maps, parameters and grid of one launch with MMA N = BN.
-template <bool kFC1, bool kPair, int BN>
+template <bool kFC1, bool kPair, int BN, bool kShort>
 cudaError_t launch_bn(const GemmLaunch& L, int num_sms, int64_t bound, cudaStream_t s, const char** why) {
     const bool has_routed = L.G > 0 && L.rows_cap > 0;
     const bool has_shared = L.T_sh > 0 && L.b_sh != nullptr && L.N_out_sh > 0;
@@ -700,7 +709,7 @@ cudaError_t launch_bn(const GemmLaunch& L, int num_sms, int64_t bound, cudaStrea
     p.timeout_ns = L.timeout_ns;
 
     KernelInfo info;
-    cudaError_t err = kernel_info<kFC1, kPair, BN>(num_sms, &info);
+    cudaError_t err = kernel_info<kFC1, kPair, BN, kShort>(num_sms, &info);
     if (err != cudaSuccess) {
         *why = "kernel attribute / occupancy query failed";
         return err;
@@ -713,7 +722,7 @@ cudaError_t launch_bn(const GemmLaunch& L, int num_sms, int64_t bound, cudaStrea
     } else {
         grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(bound, num_sms));
     }
-    err = launch_kernel<kFC1, kPair, BN>(p, mA, mB, mAs, mBs, mA32, mAs32, grid, s);
+    err = launch_kernel<kFC1, kPair, BN, kShort>(p, mA, mB, mAs, mBs, mA32, mAs32, grid, s);
     if (err != cudaSuccess) *why = "launch failed";
     return err;
 }
@@ -741,16 +750,19 @@ cudaError_t dispatch(const GemmLaunch& L, int num_sms, cudaStream_t s, const cha
     const int64_t b256 = tile_bound(L, 256);
     const bool pair = split_of(L) == 1 &&
                       (L.pair_mode == 2 ? b256 >= 2 : (L.pair_mode == 1 && b256 >= 4 * (int64_t)num_sms));
-    if (pair) return launch_bn<kFC1, true, 256>(L, num_sms, b256, s, why);
+    if (pair) return launch_bn<kFC1, true, 256, false>(L, num_sms, b256, s, why);
+    // every tile at most 32 rows: 32-row A slots, so more stages fit the ring
+    if (L.max_group_rows <= BM_SHORT && L.T_sh <= BM_SHORT)
+        return launch_bn<kFC1, false, 256, true>(L, num_sms, b256, s, why);
     // Small batches (at most 1024 routed rows) stream weights: N = 256 moves the
     // most bytes per pipeline stage, and a stage costs about the same time
     // whatever its size, so the widest tile wins even with SMs left idle.
     // Otherwise the widest N that still gives every SM two tiles.
     if (L.rows_cap <= 1024 || b256 >= 2 * (int64_t)num_sms)
-        return launch_bn<kFC1, false, 256>(L, num_sms, b256, s, why);
+        return launch_bn<kFC1, false, 256, false>(L, num_sms, b256, s, why);
     const int64_t b128 = tile_bound(L, 128);
-    if (b128 >= 2 * (int64_t)num_sms) return launch_bn<kFC1, false, 128>(L, num_sms, b128, s, why);
-    return launch_bn<kFC1, false, 64>(L, num_sms, tile_bound(L, 64), s, why);
+    if (b128 >= 2 * (int64_t)num_sms) return launch_bn<kFC1, false, 128, false>(L, num_sms, b128, s, why);
+    return launch_bn<kFC1, false, 64, false>(L, num_sms, tile_bound(L, 64), s, why);
 }
 
 }  // namespace

@@ -390,6 +390,7 @@ struct GemmLaunch {
     WsHeader* hdr;
     uint64_t timeout_ns;
     int pair_mode;             // 0 single CTAs only, 1 pairs for large launches, 2 pairs whenever possible
+    int64_t max_group_rows;    // upper bound on the rows of any routed group (tokens of the batch)
 };
 cudaError_t launch_grouped_gemm(const GemmLaunch& L, int num_sms, cudaStream_t s, const char** why);
 
