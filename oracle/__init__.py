@@ -63,6 +63,8 @@ def _load():
         lib.oracle_f64_to_bf16.restype = ctypes.c_uint16
         lib.oracle_route.argtypes = [P, P, P, i64, i32, i32, i32, i32, P, P, P]
         lib.oracle_route.restype = None
+        lib.oracle_route_grouped.argtypes = [P, P, P, i64, i32, i32, i32, i32, i32, i32, P, P, P]
+        lib.oracle_route_grouped.restype = None
         lib.oracle_slot_map.argtypes = [P, i64, i32, P, P, P]
         lib.oracle_slot_map.restype = None
         lib.oracle_local_mask.argtypes = [P, P, i64, i32, i32, i32, P, P, P]
@@ -71,7 +73,7 @@ def _load():
         lib.oracle_permute.restype = None
         lib.oracle_expert_mlp.argtypes = [P, P, P, i32, i32, P, P]
         lib.oracle_expert_mlp.restype = None
-        lib.oracle_moe_tokens.argtypes = [P, i64, i32, P, P, i32, i32, i32, P, P, i32, i32, i32,
+        lib.oracle_moe_tokens.argtypes = [P, i64, i32, P, P, i32, i32, i32, i32, i32, i32, P, P, i32, i32, i32,
                                           P, P, i32, i32, P, P, i32, P, P, i64, P, P, P, P]
         lib.oracle_moe_tokens.restype = None
         lib.oracle_set_threads.argtypes = [i32]
@@ -123,8 +125,9 @@ def f64_to_bf16(v: float) -> int:
     return int(_load().oracle_f64_to_bf16(float(v)))
 
 
-def route(x, Wg, bias, k: int, renorm: bool):
-    """C oracle_route: returns (ids [T,k] int32, w [T,k] float64, logits [T,E] float64)."""
+def route(x, Wg, bias, k: int, renorm: bool, n_group: int = 1, topk_group: int = 1):
+    """C oracle_route (n_group <= 1) or oracle_route_grouped (group-limited top-k):
+    returns (ids [T,k] int32, w [T,k] float64, logits [T,E] float64)."""
     lib = _load()
     x = _u16(x)
     Wg = _np(Wg, np.float32)
@@ -134,8 +137,12 @@ def route(x, Wg, bias, k: int, renorm: bool):
     ids = np.empty((T, k), np.int32)
     w = np.empty((T, k), np.float64)
     logits = np.empty((T, E), np.float64)
-    lib.oracle_route(_ptr(x), _ptr(Wg), _ptr(bias), T, H, E, k, int(bool(renorm)),
-                     _ptr(ids), _ptr(w), _ptr(logits))
+    if n_group > 1:
+        lib.oracle_route_grouped(_ptr(x), _ptr(Wg), _ptr(bias), T, H, E, k, int(bool(renorm)), n_group, topk_group,
+                                 _ptr(ids), _ptr(w), _ptr(logits))
+    else:
+        lib.oracle_route(_ptr(x), _ptr(Wg), _ptr(bias), T, H, E, k, int(bool(renorm)),
+                         _ptr(ids), _ptr(w), _ptr(logits))
     return ids, w, logits
 
 
@@ -196,8 +203,12 @@ def expert_mlp(x_row, W1, W2):
 
 def moe_tokens(x, Wg, bias, k, renorm, W1, W2, tokens=None, rep_offset=None, rep_slots=None,
                local_start=0, local_count=-1, mode=NONLOCAL_SKIP,
-               W1s=None, W2s=None, shared_gate_w=None):
+               W1s=None, W2s=None, shared_gate_w=None, n_group=1, topk_group=1, on_input=False):
     """C oracle_moe_tokens: full layer output (float64) for the listed tokens.
+
+    n_group / topk_group: group-limited top-k (n_group <= 1: plain top-k).
+    on_input: the routing weight scales each expert's input (rounded to bf16)
+    and the expert outputs are summed unweighted.
 
     W1 [S_local, 2I, H], W2 [S_local, H, I] are indexed by local slot.
     W1s [n_shared, 2*I_sh, H] / W2s [n_shared, H, I_sh] (or None).
@@ -230,6 +241,7 @@ def moe_tokens(x, Wg, bias, k, renorm, W1, W2, tokens=None, rep_offset=None, rep
     w = np.empty((n, k), np.float64)
     sl = np.empty((n, k), np.int32)
     lib.oracle_moe_tokens(_ptr(x), T, H, _ptr(Wg), _ptr(bias), E, k, int(bool(renorm)),
+                          int(n_group), int(topk_group), int(bool(on_input)),
                           _ptr(ro), _ptr(rs), local_start, local_count, mode,
                           _ptr(W1), _ptr(W2), I, n_shared, _ptr(W1s), _ptr(W2s), I_sh, _ptr(gw),
                           _ptr(tokens), n, _ptr(out), _ptr(ids), _ptr(w), _ptr(sl))
@@ -238,14 +250,14 @@ def moe_tokens(x, Wg, bias, k, renorm, W1, W2, tokens=None, rep_offset=None, rep
 
 def moe_layer(x, Wg, bias, k, renorm, W1, W2, rep_offset=None, rep_slots=None,
               local_start=0, local_count=-1, mode=NONLOCAL_SKIP,
-              W1s=None, W2s=None, shared_gate_w=None, S=None):
+              W1s=None, W2s=None, shared_gate_w=None, S=None, n_group=1, topk_group=1, on_input=False):
     """The whole layer on a batch: routing, slot map, mask, permutation and outputs.
 
     Composes the C steps in the order the layer runs them; returns a dict with
     ids, w (router weights), slots/w_masked (after slot map and mask), counts,
     offsets, perm_src, pair_row and out [T, H] (float64).
     """
-    ids, w, logits = route(x, Wg, bias, k, renorm)
+    ids, w, logits = route(x, Wg, bias, k, renorm, n_group, topk_group)
     slots = slot_map(ids, rep_offset, rep_slots)
     if S is None:
         S = Wg.shape[0] if rep_offset is None else int(np.asarray(rep_offset)[-1])
@@ -258,7 +270,7 @@ def moe_layer(x, Wg, bias, k, renorm, W1, W2, rep_offset=None, rep_slots=None,
     counts, offsets, perm_src, pair_row = permute(slots_l, S_local)
     res = moe_tokens(x, Wg, bias, k, renorm, W1, W2, None, rep_offset, rep_slots,
                      local_start, local_count if local_count is not None else -1, mode,
-                     W1s, W2s, shared_gate_w)
+                     W1s, W2s, shared_gate_w, n_group, topk_group, on_input)
     return dict(ids=ids, w=w, logits=logits, slots_global=slots, slots=slots_l, w_masked=w_l,
                 mask=mask, counts=counts, offsets=offsets, perm_src=perm_src,
                 pair_row=pair_row.reshape(ids.shape), out=res["out"])

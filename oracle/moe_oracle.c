@@ -101,14 +101,40 @@ uint16_t oracle_f64_to_bf16(double v)
  *   w       [T, k] double out     (p_e, or p_e / sum of the k selected p)
  *   logits  [T, E] double out, or NULL
  */
+void oracle_route_grouped(const uint16_t *x, const float *Wg, const float *bias,
+                          int64_t T, int H, int E, int k, int renorm, int n_group, int topk_group,
+                          int32_t *ids, double *w, double *logits);
+
 void oracle_route(const uint16_t *x, const float *Wg, const float *bias,
                   int64_t T, int H, int E, int k, int renorm,
                   int32_t *ids, double *w, double *logits)
 {
+    oracle_route_grouped(x, Wg, bias, T, H, E, k, renorm, 1, 1, ids, w, logits);
+}
+
+/* Group-limited top-k (the FusedMoE arguments use_grouped_topk,
+ * num_expert_group and topk_group of the vLLM EP FusedMoE patch, _ep_init).
+ * The pages name the arguments only; the reading taken here is the plainest
+ * one, DeepSeek-V2's group-limited routing: the E experts form n_group groups
+ * of E / n_group consecutive ids; a group's score is the largest logit of its
+ * experts; the topk_group groups with the largest scores are kept (ties to
+ * the lower group index); the top-k then runs over the experts of the kept
+ * groups only (same order and tie rule as above).  The softmax still runs over
+ * all E experts, so the weights are the same probabilities as without groups.
+ * n_group <= 1 (or topk_group >= n_group) keeps every expert.
+ */
+void oracle_route_grouped(const uint16_t *x, const float *Wg, const float *bias,
+                          int64_t T, int H, int E, int k, int renorm, int n_group, int topk_group,
+                          int32_t *ids, double *w, double *logits)
+{
+    if (n_group < 1) n_group = 1;
+    const int gsize = E / n_group;
 #pragma omp parallel for schedule(dynamic, 4)
     for (int64_t t = 0; t < T; ++t) {
         double *l = (double *)malloc(sizeof(double) * (size_t)E);
         char *taken = (char *)calloc((size_t)E, 1);
+        char *gkeep = (char *)calloc((size_t)n_group, 1);
+        double *gs = (double *)malloc(sizeof(double) * (size_t)n_group);
         const uint16_t *xt = x + (size_t)t * (size_t)H;
         for (int e = 0; e < E; ++e) {
             const float *we = Wg + (size_t)e * (size_t)H;
@@ -123,6 +149,23 @@ void oracle_route(const uint16_t *x, const float *Wg, const float *bias,
         for (int e = 1; e < E; ++e) if (l[e] > m) m = l[e];
         double z = 0.0;
         for (int e = 0; e < E; ++e) z += exp(l[e] - m);
+        /* groups: score = largest logit of the group; keep topk_group of them */
+        if (n_group > 1 && topk_group < n_group) {
+            for (int g = 0; g < n_group; ++g) {
+                double b = l[g * gsize];
+                for (int e = g * gsize + 1; e < (g + 1) * gsize; ++e) if (l[e] > b) b = l[e];
+                gs[g] = b;
+            }
+            for (int r = 0; r < topk_group; ++r) {
+                int best = -1;
+                for (int g = 0; g < n_group; ++g) {
+                    if (gkeep[g]) continue;
+                    if (best < 0 || gs[g] > gs[best]) best = g;
+                }
+                gkeep[best] = 1;
+            }
+            for (int e = 0; e < E; ++e) if (!gkeep[e / gsize]) taken[e] = 1;  /* excluded */
+        }
         /* top-k: k passes of "largest remaining logit, lowest id on ties" */
         double psum = 0.0;
         for (int j = 0; j < k; ++j) {
@@ -141,6 +184,8 @@ void oracle_route(const uint16_t *x, const float *Wg, const float *bias,
             for (int j = 0; j < k; ++j) w[(size_t)t * (size_t)k + (size_t)j] /= psum;
         free(l);
         free(taken);
+        free(gkeep);
+        free(gs);
     }
 }
 
@@ -310,6 +355,7 @@ void oracle_expert_mlp(const uint16_t *x, const uint16_t *W1, const uint16_t *W2
  */
 void oracle_moe_tokens(const uint16_t *x, int64_t T, int H,
                        const float *Wg, const float *bias, int E, int k, int renorm,
+                       int n_group, int topk_group, int on_input,
                        const int32_t *rep_offset, const int32_t *rep_slots,
                        int local_start, int local_count, int mode,
                        const uint16_t *W1, const uint16_t *W2, int I,
@@ -332,7 +378,7 @@ void oracle_moe_tokens(const uint16_t *x, int64_t T, int H,
         double *o = out + (size_t)q * (size_t)H;
 
         /* steps 1-3 for this one token (the slot map needs its index t) */
-        oracle_route(xt, Wg, bias, 1, H, E, k, renorm, ids, w, NULL);
+        oracle_route_grouped(xt, Wg, bias, 1, H, E, k, renorm, n_group, topk_group, ids, w, NULL);
         for (int j = 0; j < k; ++j) {
             int32_t e = ids[j];
             if (!rep_offset) {
@@ -353,15 +399,27 @@ void oracle_moe_tokens(const uint16_t *x, int64_t T, int H,
             slot_out[(size_t)q * (size_t)k + (size_t)j] = sl2[j];
         }
 
-        /* step 5: weighted sum over the k experts, in order */
+        /* step 5: weighted sum over the k experts, in order.  With on_input the
+         * routing weight scales the expert's input instead (TensorRT-LLM
+         * AutoDeploy MoE PR #10985, review of torch_moe.py: apply_routing_on_input,
+         * "BMM-style routing"): the row w_j * x_t, rounded to bf16, goes through
+         * the expert and the outputs are summed unweighted. */
         for (int hh = 0; hh < H; ++hh) o[hh] = 0.0;
+        uint16_t *xs = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)H);
         for (int j = 0; j < k; ++j) {
             int32_t s = sl2[j];
             if (s < 0) continue;
-            oracle_expert_mlp(xt, W1 + (size_t)s * 2u * (size_t)I * (size_t)H,
+            const uint16_t *xin = xt;
+            if (on_input) {
+                for (int hh = 0; hh < H; ++hh) xs[hh] = oracle_f64_to_bf16(w2[j] * oracle_bf16_to_f64(xt[hh]));
+                xin = xs;
+            }
+            oracle_expert_mlp(xin, W1 + (size_t)s * 2u * (size_t)I * (size_t)H,
                               W2 + (size_t)s * (size_t)H * (size_t)I, H, I, y, NULL);
-            for (int hh = 0; hh < H; ++hh) o[hh] += w2[j] * y[hh];
+            const double wj = on_input ? 1.0 : w2[j];
+            for (int hh = 0; hh < H; ++hh) o[hh] += wj * y[hh];
         }
+        free(xs);
         if (n_shared > 0) {
             double g = 1.0;
             if (shared_gate_w) {

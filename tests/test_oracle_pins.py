@@ -338,3 +338,114 @@ def test_results_do_not_depend_on_thread_count(threads):
         oracle.set_threads(old)
     b = oracle.moe_layer(inp["x"], inp["Wg"], None, 2, True, inp["W1"], inp["W2"])
     assert np.array_equal(a["out"], b["out"])
+
+
+# --------------------------------------------------------------------------- group-limited top-k
+
+def _golden_kv(name):
+    kv = {}
+    for line in open(os.path.join(GOLDEN, name)):
+        line = line.split("#")[0].split()
+        if line:
+            kv[line[0]] = [float(v) for v in line[1:]]
+    return kv
+
+
+def _route_given_logits(logits, k, n_group, topk_group, renorm=False):
+    """x = e_0 (bf16 1.0), Wg[:, 0] = the logits: the oracle's logits are exactly these fp32 values."""
+    E = len(logits)
+    x = torch.zeros((1, 64), dtype=torch.bfloat16)
+    x[0, 0] = 1.0
+    Wg = torch.zeros((E, 64), dtype=torch.float32)
+    Wg[:, 0] = torch.tensor(logits, dtype=torch.float32)
+    return oracle.route(x, Wg, None, k, renorm, n_group, topk_group)
+
+
+def test_grouped_topk_golden_example():
+    g = _golden_kv("grouped_topk_example.txt")
+    logits, k = g["logits"], int(g["k"][0])
+    ids, w, l = _route_given_logits(logits, k, int(g["n_group"][0]), int(g["topk_group"][0]))
+    assert ids[0].tolist() == [int(v) for v in g["grouped_ids"]]
+    p = np.exp(np.array(logits) - max(logits))
+    p /= p.sum()
+    np.testing.assert_allclose(w[0], p[ids[0]], rtol=1e-15)
+    ids_plain, _, _ = _route_given_logits(logits, k, 1, 1)
+    assert ids_plain[0].tolist() == [int(v) for v in g["plain_ids"]]
+    ids_tie, _, _ = _route_given_logits(g["tie_logits"], int(g["tie_k"][0]), int(g["n_group"][0]),
+                                        int(g["tie_topk_group"][0]))
+    assert ids_tie[0].tolist() == [int(v) for v in g["tie_ids"]]
+
+
+def test_grouped_topk_reduces_to_plain_topk():
+    cfg = _small_cfg(T=40, H=64, E=16, k=4)
+    inp = mi.make_inputs(cfg)
+    plain = oracle.route(inp["x"], inp["Wg"], None, 4, True)
+    for n_group, topk_group in ((1, 1), (4, 4), (8, 8)):
+        got = oracle.route(inp["x"], inp["Wg"], None, 4, True, n_group, topk_group)
+        assert np.array_equal(got[0], plain[0]) and np.array_equal(got[1], plain[1])
+
+
+def test_grouped_topk_against_numpy_selection():
+    """Independent numpy selection on the oracle's own fp64 logits: the kept groups are
+    the topk_group largest group maxima (lower index on ties), the ids the k largest
+    logits inside them (lower id on ties), the weights the full-softmax probabilities."""
+    cfg = _small_cfg(T=64, H=64, E=24, k=3)
+    inp = mi.make_inputs(cfg)
+    n_group, topk_group, k = 6, 2, 3
+    ids, w, l = oracle.route(inp["x"], inp["Wg"], None, k, False, n_group, topk_group)
+    gsize = 24 // n_group
+    for t in range(cfg.T):
+        gmax = l[t].reshape(n_group, gsize).max(1)
+        keep = np.lexsort((np.arange(n_group), -gmax))[:topk_group]
+        allowed = np.concatenate([np.arange(g * gsize, (g + 1) * gsize) for g in keep])
+        order = allowed[np.lexsort((allowed, -l[t][allowed]))][:k]
+        assert ids[t].tolist() == order.tolist()
+        assert len({int(e) // gsize for e in ids[t]}) <= topk_group
+        p = np.exp(l[t] - l[t].max())
+        p /= p.sum()
+        np.testing.assert_allclose(w[t], p[ids[t]], rtol=1e-12)
+
+
+# --------------------------------------------------------------------------- routing applied on the input
+
+def test_routing_on_input_top1_renorm_equals_plain_layer():
+    """k = 1 with renorm: w = 1, so scaling the input changes nothing (bitwise)."""
+    cfg = _small_cfg(T=16, H=64, I=64, E=5, k=1, renorm=True)
+    inp = mi.make_inputs(cfg)
+    a = oracle.moe_layer(inp["x"], inp["Wg"], None, 1, True, inp["W1"], inp["W2"])
+    b = oracle.moe_layer(inp["x"], inp["Wg"], None, 1, True, inp["W1"], inp["W2"], on_input=True)
+    assert np.array_equal(a["out"], b["out"])
+
+
+def test_routing_on_input_matches_numpy_mlp_of_scaled_rows():
+    """out_t = sum_j MLP_j(bf16(w_j x_t)), the scaled row rounded through torch's bf16 cast,
+    the MLP a numpy dense product (no oracle arithmetic)."""
+    cfg = _small_cfg(T=12, H=64, I=64, E=6, k=3, renorm=False, n_shared=1, I_shared=32)
+    inp = mi.make_inputs(cfg)
+    res = oracle.moe_layer(inp["x"], inp["Wg"], None, 3, False, inp["W1"], inp["W2"],
+                           W1s=inp["W1s"], W2s=inp["W2s"], on_input=True)
+    x64 = _bf16_np(inp["x"])
+    shared = _numpy_mlp(x64, inp["W1s"][0], inp["W2s"][0])
+    for t in range(cfg.T):
+        ref = shared[t].copy()
+        for j in range(3):
+            e = int(res["ids"][t, j])
+            xs = torch.from_numpy(res["w"][t, j] * x64[t:t + 1]).to(torch.bfloat16).to(torch.float64).numpy()
+            ref += _numpy_mlp(xs, inp["W1"][e], inp["W2"][e])[0]
+        np.testing.assert_allclose(res["out"][t], ref, rtol=0, atol=1e-3 * np.abs(ref).max())
+
+
+def test_routing_on_input_local_ranges_sum_to_full_layer():
+    cfg = _small_cfg(T=30, H=64, I=64, E=8, k=3)
+    inp = mi.make_inputs(cfg)
+    full = oracle.moe_layer(inp["x"], inp["Wg"], None, 3, True, inp["W1"], inp["W2"], on_input=True)
+    acc = np.zeros_like(full["out"])
+    for start in (0, 4):
+        part = oracle.moe_layer(inp["x"], inp["Wg"], None, 3, True, inp["W1"][start:start + 4],
+                                inp["W2"][start:start + 4], local_start=start, local_count=4, on_input=True)
+        mod = oracle.moe_layer(inp["x"], inp["Wg"], None, 3, True, inp["W1"][start:start + 4],
+                               inp["W2"][start:start + 4], local_start=start, local_count=4,
+                               mode=oracle.NONLOCAL_MOD, on_input=True)
+        assert np.array_equal(part["out"], mod["out"])  # a zero-weight input row gives a zero output
+        acc += part["out"]
+    np.testing.assert_allclose(acc, full["out"], rtol=0, atol=1e-12 * np.abs(full["out"]).max())
