@@ -154,6 +154,23 @@ MOE_API moe_status_t moe_route_noalloc(const moe_bf16_t *x, const float *gate_w,
                                int64_t T, int H, int E, int k, int renorm,
                                int32_t *topk_ids, float *topk_w, moe_stream_t stream);
 
+/* moe_route_grouped -- moe_route with group-limited top-k ([VLLM-EP] _ep_init
+ * arguments use_grouped_topk, num_expert_group, topk_group; the pages name them
+ * only, and this is the plainest reading, DeepSeek-V2's group-limited routing):
+ * the E experts form n_group groups of E / n_group consecutive ids; a group's
+ * score is its largest logit; the topk_group best groups are kept (ties to the
+ * lower group index) and the top-k runs over their experts only.  The softmax
+ * still covers all E experts.  The group choice is certified like the top-k:
+ * group scores within the fp32 bound of each other are recomputed
+ * (compensated fp32, then fp64 if needed).
+ * Requires 1 <= n_group <= 32, E % n_group == 0, 1 <= topk_group <= n_group and
+ * k <= topk_group * E / n_group; otherwise MOE_ERR_INVALID_ARG.  Other
+ * arguments, outputs and errors as moe_route. */
+MOE_API moe_status_t moe_route_grouped(const moe_bf16_t *x, const float *gate_w, const float *logit_bias,
+                               int64_t T, int H, int E, int k, int renorm, int n_group, int topk_group,
+                               int32_t *topk_ids, float *topk_w, void *ws, size_t ws_bytes,
+                               moe_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* moe_permute -- slot map, local mask/remap, histogram, scan, scatter.     */
 /* ------------------------------------------------------------------------ */
@@ -189,6 +206,20 @@ MOE_API moe_status_t moe_permute(const int32_t *topk_ids, float *topk_w, int64_t
                          int32_t *perm_src, int32_t *pair_row, moe_bf16_t *x_perm,
                          void *ws, size_t ws_bytes, moe_stream_t stream);
 
+/* moe_permute_on_input -- moe_permute with the routing applied on the input
+ * ([TRT-10985] review of torch_moe.py: apply_routing_on_input, "BMM-style
+ * routing"): every kept pair's row is its token's row scaled by the pair's
+ * routing weight after the mask, rounded once to bf16 (nearest, ties to even):
+ *     x_perm[r] = bf16(topk_w[p] * x[p / k]),  p = perm_src[r].
+ * The expert outputs are then summed unweighted: pass topk_w = NULL to
+ * moe_forward / moe_finalize.  Arguments, outputs and errors as moe_permute. */
+MOE_API moe_status_t moe_permute_on_input(const int32_t *topk_ids, float *topk_w, int64_t T, int k, int E,
+                                  const int32_t *rep_offset, const int32_t *rep_slots, int S, int local_start,
+                                  int local_count, int nonlocal_mode, const moe_bf16_t *x, int H,
+                                  int32_t *slot_ids, int32_t *counts, int32_t *offsets, int32_t *perm_src,
+                                  int32_t *pair_row, moe_bf16_t *x_perm, void *ws, size_t ws_bytes,
+                                  moe_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* moe_forward -- FC1 + SwiGLU, FC2, weighted combine (+ shared expert).    */
 /* ------------------------------------------------------------------------ */
@@ -209,7 +240,8 @@ MOE_API moe_status_t moe_permute(const int32_t *topk_ids, float *topk_w, int64_t
  *   P_cap     rows of x_perm's allocation (>= offsets[S_local]; normally T*k)
  *   W1        [S_local, 2I, H] bf16  per slot: I gate rows, then I up rows
  *   W2        [S_local, H, I] bf16
- *   pair_row  [T, k] int32, topk_w [T, k] fp32 (after the mask)
+ *   pair_row  [T, k] int32, topk_w [T, k] fp32 (after the mask), or NULL: every
+ *             kept pair weighs 1 (routing applied on the input, moe_permute_on_input)
  *   x         [T, H] bf16           input of the shared expert (may be NULL if none)
  *   W1s       [2*I_shared_total, H] bf16 (gate rows then up rows) or NULL
  *   W2s       [H, I_shared_total] bf16 or NULL
@@ -247,7 +279,8 @@ MOE_API moe_status_t moe_grouped_fc2(const moe_bf16_t *h, int64_t rows_cap, cons
                              void *ws, size_t ws_bytes, moe_stream_t stream);
 
 /* Unpermute + weighted combine: out[t] = bf16(sum_j topk_w[t,j] * y[pair_row[t,j]]
- * + g_t * y_shared[t]), fp32 accumulation in fixed j order.  y_shared may be
+ * + g_t * y_shared[t]), fp32 accumulation in fixed j order (topk_w NULL: weight
+ * 1 for every kept pair).  y_shared may be
  * NULL (no shared expert); g_t as in moe_forward (x and shared_gate_w NULL ->
  * g_t = 1).  pair_row entries outside [0, rows_cap) other than -1 are
  * dropped and flagged. */

@@ -57,6 +57,8 @@ class MoEConfig:
     n_shared: int = 0                # shared experts
     I_shared: int = 0                # intermediate size of each shared expert
     shared_gate: bool = False        # scale the shared output by sigmoid(x . w_s)
+    n_group: int = 1                 # group-limited top-k: expert groups (1: plain top-k)
+    topk_group: int = 1              # groups kept per token
     w_std: float = 0.02              # expert weight std
     gate_std: float = 0.02           # router weight std
     seed: int = 0

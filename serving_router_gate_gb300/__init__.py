@@ -24,7 +24,7 @@ __all__ = [
     "lib_path", "moe_workspace_size", "moe_workspace_init", "moe_get_device_status", "moe_get_route_stats",
     "moe_route", "moe_permute", "moe_forward", "moe_grouped_fc1", "moe_grouped_fc2", "moe_finalize",
     "moe_debug_wait_timeout", "moe_set_wait_timeout_ns", "moe_route_noalloc", "moe_set_gemm_pair_mode",
-    "moe_set_pdl", "moe_get_launch_count", "EXPORTED_SYMBOLS",
+    "moe_set_pdl", "moe_get_launch_count", "moe_permute_on_input", "moe_route_grouped", "EXPORTED_SYMBOLS",
 ]
 
 MOE_OK = 0
@@ -41,7 +41,7 @@ EXPORTED_SYMBOLS = (
     "moe_status_string", "moe_workspace_size", "moe_workspace_init", "moe_get_device_status",
     "moe_get_route_stats", "moe_route", "moe_permute", "moe_forward", "moe_grouped_fc1", "moe_grouped_fc2",
     "moe_finalize", "moe_debug_wait_timeout", "moe_set_wait_timeout_ns", "moe_route_noalloc",
-    "moe_set_gemm_pair_mode", "moe_set_pdl", "moe_get_launch_count",
+    "moe_set_gemm_pair_mode", "moe_set_pdl", "moe_get_launch_count", "moe_permute_on_input", "moe_route_grouped",
 )
 
 
@@ -68,7 +68,10 @@ def _load():
         "moe_get_device_status": ([P, P, P], i32),
         "moe_get_route_stats": ([P, P, P], i32),
         "moe_route": ([P, P, P, i64, i32, i32, i32, i32, P, P, P, sz, P], i32),
+        "moe_route_grouped": ([P, P, P, i64, i32, i32, i32, i32, i32, i32, P, P, P, sz, P], i32),
         "moe_permute": ([P, P, i64, i32, i32, P, P, i32, i32, i32, i32, P, i32, P, P, P, P, P, P, P, sz, P], i32),
+        "moe_permute_on_input": ([P, P, i64, i32, i32, P, P, i32, i32, i32, i32, P, i32, P, P, P, P, P, P, P, sz, P],
+                                 i32),
         "moe_forward": ([P, P, i32, i64, P, P, i32, i32, P, P, i64, i32, P, P, P, i32, P, P, P, sz, P], i32),
         "moe_grouped_fc1": ([P, i64, P, i32, P, i32, i32, P, i64, P, i32, P, P, P, sz, P], i32),
         "moe_grouped_fc2": ([P, i64, P, i32, P, i32, i32, P, i64, P, i32, P, P, P, sz, P], i32),
@@ -159,6 +162,18 @@ def moe_route(x, gate_w, logit_bias, k, renorm, topk_ids, topk_w, ws, stream=Non
     _check("moe_route", st)
 
 
+def moe_route_grouped(x, gate_w, logit_bias, k, renorm, n_group, topk_group, topk_ids, topk_w, ws, stream=None):
+    """Group-limited top-k routing: only experts of the topk_group best of n_group groups are eligible."""
+    T, H = x.shape
+    E = gate_w.shape[0]
+    st = _lib.moe_route_grouped(_ptr(x, "x", _bf16, (T, H)), _ptr(gate_w, "gate_w", _f32, (E, H)),
+                                _ptr(logit_bias, "logit_bias", _f32, (E,), allow_none=True), T, H, E, k,
+                                int(bool(renorm)), int(n_group), int(topk_group),
+                                _ptr(topk_ids, "topk_ids", _i32, (T, k)), _ptr(topk_w, "topk_w", _f32, (T, k)),
+                                _ptr(ws, "ws", torch.uint8), ws.numel(), _stream(stream))
+    _check("moe_route_grouped", st)
+
+
 def moe_route_noalloc(x, gate_w, logit_bias, k, renorm, topk_ids, topk_w, stream=None):
     """moe_route without a workspace: scratch in the library's own fixed 16 MiB device array."""
     T, H = x.shape
@@ -171,11 +186,13 @@ def moe_route_noalloc(x, gate_w, logit_bias, k, renorm, topk_ids, topk_w, stream
 
 
 def moe_permute(topk_ids, topk_w, E, rep_offset, rep_slots, S, local_start, local_count, nonlocal_mode, x,
-                slot_ids, counts, offsets, perm_src, pair_row, x_perm, ws, stream=None):
+                slot_ids, counts, offsets, perm_src, pair_row, x_perm, ws, stream=None, on_input=False):
+    """moe_permute, or moe_permute_on_input when on_input (rows scaled by the routing weights)."""
     T, k = topk_ids.shape
     H = x.shape[1]
     S_local = local_count if local_count >= 0 else S
-    st = _lib.moe_permute(_ptr(topk_ids, "topk_ids", _i32, (T, k)), _ptr(topk_w, "topk_w", _f32, (T, k)), T, k, E,
+    fn = _lib.moe_permute_on_input if on_input else _lib.moe_permute
+    st = fn(_ptr(topk_ids, "topk_ids", _i32, (T, k)), _ptr(topk_w, "topk_w", _f32, (T, k)), T, k, E,
                           _ptr(rep_offset, "rep_offset", _i32, (E + 1,), allow_none=True),
                           _ptr(rep_slots, "rep_slots", _i32, (S,), allow_none=True), S, local_start, local_count,
                           nonlocal_mode, _ptr(x, "x", _bf16, (T, H)), H,
@@ -183,7 +200,7 @@ def moe_permute(topk_ids, topk_w, E, rep_offset, rep_slots, S, local_start, loca
                           _ptr(offsets, "offsets", _i32, (S_local + 1,)), _ptr(perm_src, "perm_src", _i32, (T * k,)),
                           _ptr(pair_row, "pair_row", _i32, (T, k)), _ptr(x_perm, "x_perm", _bf16, (T * k, H)),
                           _ptr(ws, "ws", torch.uint8), ws.numel(), _stream(stream))
-    _check("moe_permute", st)
+    _check("moe_permute_on_input" if on_input else "moe_permute", st)
 
 
 def moe_forward(x_perm, offsets, W1, W2, pair_row, topk_w, x, W1s, W2s, shared_gate_w, out, ws, stream=None):
@@ -194,7 +211,8 @@ def moe_forward(x_perm, offsets, W1, W2, pair_row, topk_w, x, W1s, W2s, shared_g
     I_sh = 0 if W2s is None else W2s.shape[1]
     st = _lib.moe_forward(_ptr(x_perm, "x_perm", _bf16), _ptr(offsets, "offsets", _i32), S_local, P_cap,
                           _ptr(W1, "W1", _bf16, (S_local, 2 * I, H)), _ptr(W2, "W2", _bf16, (S_local, H, I)), H, I,
-                          _ptr(pair_row, "pair_row", _i32), _ptr(topk_w, "topk_w", _f32, (T, k)), T, k,
+                          _ptr(pair_row, "pair_row", _i32), _ptr(topk_w, "topk_w", _f32, (T, k), allow_none=True),
+                          T, k,
                           _ptr(x, "x", _bf16, (T, H), allow_none=True),
                           _ptr(W1s, "W1s", _bf16, (2 * I_sh, H), allow_none=True),
                           _ptr(W2s, "W2s", _bf16, (H, I_sh), allow_none=True), I_sh,
@@ -239,7 +257,7 @@ def moe_finalize(y, pair_row, topk_w, y_shared, x, shared_gate_w, out, ws, strea
     rows_cap, H = y.shape
     T, k = pair_row.shape
     st = _lib.moe_finalize(_ptr(y, "y", _bf16), rows_cap, _ptr(pair_row, "pair_row", _i32, (T, k)),
-                           _ptr(topk_w, "topk_w", _f32, (T, k)), T, k, H,
+                           _ptr(topk_w, "topk_w", _f32, (T, k), allow_none=True), T, k, H,
                            _ptr(y_shared, "y_shared", _bf16, (T, H), allow_none=True),
                            _ptr(x, "x", _bf16, (T, H), allow_none=True),
                            _ptr(shared_gate_w, "shared_gate_w", _bf16, (H,), allow_none=True),

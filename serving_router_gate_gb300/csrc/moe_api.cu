@@ -153,9 +153,9 @@ moe_status_t moe_get_route_stats(void* ws, moe_stream_t stream, int64_t* refined
     return MOE_OK;
 }
 
-moe_status_t moe_route(const moe_bf16_t* x, const float* gate_w, const float* logit_bias, int64_t T, int H, int E,
-                       int k, int renorm, int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes,
-                       moe_stream_t stream) {
+static moe_status_t route_impl(const moe_bf16_t* x, const float* gate_w, const float* logit_bias, int64_t T, int H,
+                               int E, int k, int renorm, int n_group, int topk_group, int32_t* topk_ids,
+                               float* topk_w, void* ws, size_t ws_bytes, moe_stream_t stream) {
     if (T < 0 || H <= 0 || E <= 0 || k <= 0 || k > E) return MOE_ERR_INVALID_ARG;
     if (!dim_ok(H) || E > 512 || k > 32 || T * (int64_t)k >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
     if (T == 0) return MOE_OK;
@@ -176,14 +176,32 @@ moe_status_t moe_route(const moe_bf16_t* x, const float* gate_w, const float* lo
     L.hdr = static_cast<WsHeader*>(ws);
     router_carve(static_cast<char*>(ws) + kWsHeaderBytes, T, E, &L.part, &L.xsq, &L.wsq);
     router_plan(T, H, E, sms, &L.nsplit, &L.KC);
+    L.n_group = n_group;
+    L.topk_group = topk_group;
     return cuda_status(launch_router(L, sms, (cudaStream_t)stream));
 }
 
-moe_status_t moe_permute(const int32_t* topk_ids, float* topk_w, int64_t T, int k, int E, const int32_t* rep_offset,
-                         const int32_t* rep_slots, int S, int local_start, int local_count, int nonlocal_mode,
-                         const moe_bf16_t* x, int H, int32_t* slot_ids, int32_t* counts, int32_t* offsets,
-                         int32_t* perm_src, int32_t* pair_row, moe_bf16_t* x_perm, void* ws, size_t ws_bytes,
-                         moe_stream_t stream) {
+moe_status_t moe_route(const moe_bf16_t* x, const float* gate_w, const float* logit_bias, int64_t T, int H, int E,
+                       int k, int renorm, int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes,
+                       moe_stream_t stream) {
+    return route_impl(x, gate_w, logit_bias, T, H, E, k, renorm, 1, 1, topk_ids, topk_w, ws, ws_bytes, stream);
+}
+
+moe_status_t moe_route_grouped(const moe_bf16_t* x, const float* gate_w, const float* logit_bias, int64_t T, int H,
+                               int E, int k, int renorm, int n_group, int topk_group, int32_t* topk_ids,
+                               float* topk_w, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    if (n_group < 1 || n_group > 32 || E % n_group != 0 || topk_group < 1 || topk_group > n_group ||
+        k > topk_group * (E / n_group))
+        return MOE_ERR_INVALID_ARG;
+    return route_impl(x, gate_w, logit_bias, T, H, E, k, renorm, n_group, topk_group, topk_ids, topk_w, ws, ws_bytes,
+                      stream);
+}
+
+static moe_status_t permute_impl(bool scale_rows, const int32_t* topk_ids, float* topk_w, int64_t T, int k, int E,
+                                 const int32_t* rep_offset, const int32_t* rep_slots, int S, int local_start,
+                                 int local_count, int nonlocal_mode, const moe_bf16_t* x, int H, int32_t* slot_ids,
+                                 int32_t* counts, int32_t* offsets, int32_t* perm_src, int32_t* pair_row,
+                                 moe_bf16_t* x_perm, void* ws, size_t ws_bytes, moe_stream_t stream) {
     if (T < 0 || k <= 0 || E <= 0 || S <= 0 || H <= 0) return MOE_ERR_INVALID_ARG;
     if (!rep_offset && S != E) return MOE_ERR_INVALID_ARG;
     if (rep_offset && !rep_slots) return MOE_ERR_INVALID_ARG;
@@ -224,9 +242,30 @@ moe_status_t moe_permute(const int32_t* topk_ids, float* topk_w, int64_t T, int 
     L.perm_src = perm_src;
     L.pair_row = pair_row;
     L.x_perm = x_perm;
+    L.scale_rows = scale_rows;
     L.hdr = static_cast<WsHeader*>(ws);
     permute_carve(static_cast<char*>(ws) + kWsHeaderBytes, P, S_local, &L.rank, &L.chunk_cnt, &L.chunk_base);
     return cuda_status(launch_permute(L, device_sms(), s));
+}
+
+moe_status_t moe_permute(const int32_t* topk_ids, float* topk_w, int64_t T, int k, int E, const int32_t* rep_offset,
+                         const int32_t* rep_slots, int S, int local_start, int local_count, int nonlocal_mode,
+                         const moe_bf16_t* x, int H, int32_t* slot_ids, int32_t* counts, int32_t* offsets,
+                         int32_t* perm_src, int32_t* pair_row, moe_bf16_t* x_perm, void* ws, size_t ws_bytes,
+                         moe_stream_t stream) {
+    return permute_impl(false, topk_ids, topk_w, T, k, E, rep_offset, rep_slots, S, local_start, local_count,
+                        nonlocal_mode, x, H, slot_ids, counts, offsets, perm_src, pair_row, x_perm, ws, ws_bytes,
+                        stream);
+}
+
+moe_status_t moe_permute_on_input(const int32_t* topk_ids, float* topk_w, int64_t T, int k, int E,
+                                  const int32_t* rep_offset, const int32_t* rep_slots, int S, int local_start,
+                                  int local_count, int nonlocal_mode, const moe_bf16_t* x, int H, int32_t* slot_ids,
+                                  int32_t* counts, int32_t* offsets, int32_t* perm_src, int32_t* pair_row,
+                                  moe_bf16_t* x_perm, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    return permute_impl(true, topk_ids, topk_w, T, k, E, rep_offset, rep_slots, S, local_start, local_count,
+                        nonlocal_mode, x, H, slot_ids, counts, offsets, perm_src, pair_row, x_perm, ws, ws_bytes,
+                        stream);
 }
 
 static moe_status_t gemm_call(bool fc1, const moe_bf16_t* a, int64_t rows_cap, const int32_t* offsets, int G,
@@ -328,7 +367,7 @@ moe_status_t moe_finalize(const moe_bf16_t* y, int64_t rows_cap, const int32_t* 
     if (T < 0 || k <= 0 || H <= 0 || rows_cap < 0) return MOE_ERR_INVALID_ARG;
     if (!dim_ok(H) || k > 32) return MOE_ERR_UNSUPPORTED;
     if (T == 0) return MOE_OK;
-    if (!pair_row || !topk_w || !out || (rows_cap > 0 && !y)) return MOE_ERR_INVALID_ARG;
+    if (!pair_row || !out || (rows_cap > 0 && !y)) return MOE_ERR_INVALID_ARG;
     if (shared_gate_w && (!x || !y_shared)) return MOE_ERR_INVALID_ARG;
     if (!ws || ws_bytes < kWsHeaderBytes) return MOE_ERR_WORKSPACE;
     return finalize_call(y, rows_cap, pair_row, topk_w, T, k, H, y_shared, nullptr, 0, x, shared_gate_w, out, ws,
@@ -346,7 +385,7 @@ moe_status_t moe_forward(const moe_bf16_t* x_perm, const int32_t* offsets, int S
         P_cap >= (int64_t(1) << 31))
         return MOE_ERR_UNSUPPORTED;
     if (T == 0) return MOE_OK;
-    if (!x_perm || !offsets || !W1 || !W2 || !pair_row || !topk_w || !out) return MOE_ERR_INVALID_ARG;
+    if (!x_perm || !offsets || !W1 || !W2 || !pair_row || !out) return MOE_ERR_INVALID_ARG;
     if (I_shared_total > 0 && (!x || !W1s || !W2s)) return MOE_ERR_INVALID_ARG;
     if (shared_gate_w && (I_shared_total == 0 || !x)) return MOE_ERR_INVALID_ARG;
     const ForwardLayout FL = forward_layout(P_cap, T, H, I, I_shared_total);

@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(FZ_THREADS, 4) finalize_kernel(
                 r = -1;
             }
             s_row[tt][j] = r;
-            s_w[tt][j] = w[(t0 + tt) * k + j];
+            s_w[tt][j] = w ? w[(t0 + tt) * k + j] : 1.0f;  // no weights: each kept pair counts once
         }
         if (gated && warp < nt) {
             const uint4* xv = reinterpret_cast<const uint4*>(x + (t0 + warp) * H);

@@ -339,6 +339,7 @@ struct RouterLaunch {
     float* xsq;    // [nsplit][T]
     float* wsq;    // [nsplit][E]
     int nsplit, KC;
+    int n_group = 1, topk_group = 1;  // group-limited top-k (n_group <= 1: every expert eligible)
     WsHeader* hdr;
 };
 size_t router_scratch_bytes(int64_t T, int H, int E, int num_sms);
@@ -365,6 +366,7 @@ struct PermuteLaunch {
     int32_t* rank;        // [T*k] rank of each pair among its chunk's pairs of its slot
     int32_t* chunk_cnt;   // [nchunks][S_local]
     int32_t* chunk_base;  // [nchunks][S_local]
+    bool scale_rows;      // x_perm rows = bf16(w * x) (routing applied on the input)
     WsHeader* hdr;
 };
 size_t permute_scratch_bytes(int64_t P, int S_local);

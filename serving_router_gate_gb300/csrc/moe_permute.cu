@@ -169,30 +169,63 @@ __device__ __forceinline__ void scan_counts(const int32_t* __restrict__ chunk_cn
 // 0..7 write pair_row / perm_src, then the warp copies the 8 rows of x.
 constexpr int PS_PAIRS = 8;
 
+// bf16 of the exact product w * x (x a bf16 value), rounded once to nearest,
+// ties to even: fp32 rounds the product to p with an exact remainder e = w*x - p
+// (fma); bf16 rounding points are fp32 values, so p rounds like the exact
+// product unless p sits exactly on a midpoint between two bf16 values, where
+// the sign of e decides.
+__device__ __forceinline__ uint32_t bf16_of_product(float w, float x) {
+    const float p = __fmul_rn(w, x);
+    const float e = fmaf(w, x, -p);
+    const uint32_t b = __float_as_uint(p);
+    if ((b & 0xFFFFu) == 0x8000u && e != 0.0f) {
+        const uint32_t t = b & 0xFFFF0000u;  // toward zero
+        return ((e > 0.0f) == (p > 0.0f) ? t + 0x10000u : t) >> 16;
+    }
+    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(p));
+}
+
+// Copy (or, with wsc, scale by the pair's routing weight) the rows of pairs
+// pb .. pb+7 into their x_perm rows; also writes pair_row and perm_src.
 __device__ __forceinline__ void scatter_pairs(int64_t pb, const uint16_t* __restrict__ x,
                                               const int32_t* __restrict__ slot_ids, const int32_t* __restrict__ rank,
                                               const int32_t* __restrict__ chunk_base, int S_local, int64_t P, int k,
                                               int H, int32_t* __restrict__ pair_row, int32_t* __restrict__ perm_src,
-                                              uint16_t* __restrict__ x_perm) {
+                                              uint16_t* __restrict__ x_perm, const float* __restrict__ wsc) {
     const int lane = threadIdx.x & 31;
     const int vec = H / 8;
     int32_t row = -1;
+    float wp = 1.0f;
     if (lane < PS_PAIRS && pb + lane < P) {
         const int64_t p = pb + lane;
         const int32_t s = slot_ids[p];
         if (s >= 0) {
             row = chunk_base[(p / PM_CHUNK) * S_local + s] + rank[p];
             perm_src[row] = (int32_t)p;
+            if (wsc) wp = wsc[p];
         }
         pair_row[p] = row;
     }
     const int nj = (int)min((int64_t)PS_PAIRS, P - pb);
     for (int j = 0; j < nj; ++j) {
         const int32_t r = __shfl_sync(0xffffffffu, row, j);
+        const float wj = __shfl_sync(0xffffffffu, wp, j);
         if (r < 0) continue;
         const uint4* src = reinterpret_cast<const uint4*>(x + ((pb + j) / k) * H);
         uint4* dst = reinterpret_cast<uint4*>(x_perm + (int64_t)r * H);
-        for (int v = lane; v < vec; v += 32) dst[v] = __ldg(src + v);
+        if (!wsc) {
+            for (int v = lane; v < vec; v += 32) dst[v] = __ldg(src + v);
+        } else {
+            for (int v = lane; v < vec; v += 32) {
+                float f[8];
+                unpack8(__ldg(src + v), f);
+                uint32_t o[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    o[i] = bf16_of_product(wj, f[2 * i]) | (bf16_of_product(wj, f[2 * i + 1]) << 16);
+                dst[v] = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+        }
     }
 }
 
@@ -231,12 +264,13 @@ __global__ void __launch_bounds__(256) permute_scatter_kernel(const uint16_t* __
                                                               int64_t P, int k, int H,
                                                               int32_t* __restrict__ pair_row,
                                                               int32_t* __restrict__ perm_src,
-                                                              uint16_t* __restrict__ x_perm) {
+                                                              uint16_t* __restrict__ x_perm,
+                                                              const float* __restrict__ wsc) {
     pdl_wait();
     pdl_trigger();
     const int warp = threadIdx.x >> 5;
     for (int64_t pb = ((int64_t)blockIdx.x * 8 + warp) * PS_PAIRS; pb < P; pb += (int64_t)gridDim.x * 8 * PS_PAIRS)
-        scatter_pairs(pb, x, slot_ids, rank, chunk_base, S_local, P, k, H, pair_row, perm_src, x_perm);
+        scatter_pairs(pb, x, slot_ids, rank, chunk_base, S_local, P, k, H, pair_row, perm_src, x_perm, wsc);
 }
 
 // ---- one CTA for small batches: the three phases with block barriers ----
@@ -252,7 +286,7 @@ __global__ void __launch_bounds__(PM_SCAN_THREADS) permute_small_kernel(
     int32_t* __restrict__ chunk_cnt, int64_t nchunks, const uint16_t* __restrict__ x, int H,
     int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ chunk_base,
     int32_t* __restrict__ pair_row, int32_t* __restrict__ perm_src, uint16_t* __restrict__ x_perm,
-    int with_scatter, int32_t* status) {
+    const float* __restrict__ wsc, int with_scatter, int32_t* status) {
     extern __shared__ int32_t pm_cur[];  // [32 warps][S_local]
     __shared__ int32_t s_warp[PM_SCAN_THREADS / 32];
     pdl_wait();
@@ -266,7 +300,7 @@ __global__ void __launch_bounds__(PM_SCAN_THREADS) permute_small_kernel(
     if (!with_scatter) return;  // the rows are copied by permute_scatter_kernel over the whole GPU
     __syncthreads();
     for (int64_t pb = (int64_t)warp * PS_PAIRS; pb < P; pb += (int64_t)PM_SMALL_WARPS * PS_PAIRS)
-        scatter_pairs(pb, x, slot_ids, rank, chunk_base, S_local, P, k, H, pair_row, perm_src, x_perm);
+        scatter_pairs(pb, x, slot_ids, rank, chunk_base, S_local, P, k, H, pair_row, perm_src, x_perm, wsc);
 }
 
 }  // namespace
@@ -290,6 +324,8 @@ void permute_carve(void* base, int64_t P, int S_local, int32_t** rank, int32_t**
 }
 
 cudaError_t launch_permute(const PermuteLaunch& L, int num_sms, cudaStream_t s) {
+    // routing applied on the input: rows scaled by the (masked) weights
+    const float* wsc = L.scale_rows ? L.w : nullptr;
     const int64_t P = L.T * L.k;
     const int64_t nchunks = (P + PM_CHUNK - 1) / PM_CHUNK;
     int32_t* status = &L.hdr->status;
@@ -305,12 +341,12 @@ cudaError_t launch_permute(const PermuteLaunch& L, int num_sms, cudaStream_t s) 
         cudaError_t e = launch_k(permute_small_kernel, dim3(1), dim3(PM_SCAN_THREADS), smem_small, s, L.ids, L.w, P,
                                  L.k, L.E, L.rep_offset, L.rep_slots, L.S, L.local_start, L.local_count, L.mode,
                                  L.S_local, L.slot_ids, L.rank, L.chunk_cnt, nchunks, L.x, L.H, L.counts, L.offsets,
-                                 L.chunk_base, L.pair_row, L.perm_src, L.x_perm, (int)copy_here, status);
+                                 L.chunk_base, L.pair_row, L.perm_src, L.x_perm, wsc, (int)copy_here, status);
         if (e != cudaSuccess || copy_here) return e;
         const int64_t want = (P + 8 * PS_PAIRS - 1) / (8 * PS_PAIRS);
         const unsigned gs = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms * 8));
         return launch_k(permute_scatter_kernel, dim3(gs), dim3(256), 0, s, L.x, L.slot_ids, L.rank, L.chunk_base,
-                        L.S_local, P, L.k, L.H, L.pair_row, L.perm_src, L.x_perm);
+                        L.S_local, P, L.k, L.H, L.pair_row, L.perm_src, L.x_perm, wsc);
     }
     const unsigned g1 = (unsigned)((nchunks + PM_WARPS - 1) / PM_WARPS);
     const size_t smem = (size_t)PM_WARPS * L.S_local * sizeof(int32_t);
@@ -324,7 +360,7 @@ cudaError_t launch_permute(const PermuteLaunch& L, int num_sms, cudaStream_t s) 
     const int64_t want = (P + 8 * PS_PAIRS - 1) / (8 * PS_PAIRS);
     const unsigned g3 = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms * 8));
     return launch_k(permute_scatter_kernel, dim3(g3), dim3(256), 0, s, L.x, L.slot_ids, L.rank, L.chunk_base,
-                    L.S_local, P, L.k, L.H, L.pair_row, L.perm_src, L.x_perm);
+                    L.S_local, P, L.k, L.H, L.pair_row, L.perm_src, L.x_perm, wsc);
 }
 
 }  // namespace moe

@@ -336,6 +336,118 @@ __device__ double refine_dot(const uint16_t* __restrict__ xrow, const float* __r
     return t;
 }
 
+// Group-limited top-k, group step (warp-wide; every lane returns the same mask).
+// Groups are n_group runs of E / n_group consecutive experts; a group's score
+// is its largest logit; the topk_group best groups are kept, ties to the lower
+// group index.  With fp32 logits within thr/2 of the exact ones, a group whose
+// fp32 score lies more than thr above the first dropped group's score is kept
+// for certain, one more than thr below the last kept group's is dropped for
+// certain.  The groups in between are decided on recomputed scores: the
+// experts that can be their maximum (fp32 logit within thr of the group's
+// fp32 score) are recomputed with the compensated dot product, and if two of
+// those group scores still lie within thr2 of each other, in fp64.
+template <int PL>
+__device__ __noinline__ uint32_t select_groups(const float (&l)[PL], float* s_l, int* s_cand, double* s_val, int E, int n_group,
+                                  int topk_group, float thr, float thr2, const uint16_t* xrow, const float* Wg,
+                                  const float* bias, int H, int lane) {
+    const int gsize = E / n_group;
+#pragma unroll
+    for (int i = 0; i < PL; ++i)
+        if (lane + 32 * i < E) s_l[lane + 32 * i] = l[i];
+    __syncwarp();
+    float gm = -INFINITY;  // lane g < n_group: score of group g
+    if (lane < n_group)
+        for (int e = lane * gsize; e < (lane + 1) * gsize; ++e) gm = fmaxf(gm, s_l[e]);
+    // rank the groups: topk_group kept, and the score of the first dropped one
+    uint32_t keep = 0;
+    float v_last = 0.f, v_next = -INFINITY;
+    for (int r = 0; r <= topk_group; ++r) {
+        float bv = (lane < n_group && !((keep >> lane) & 1u)) ? gm : -INFINITY;
+        int bg = (lane < n_group && !((keep >> lane) & 1u)) ? lane : INT_MAX;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+            const int og = __shfl_xor_sync(0xffffffffu, bg, off);
+            if (ov > bv || (ov == bv && og < bg)) {
+                bv = ov;
+                bg = og;
+            }
+        }
+        if (r < topk_group) {
+            keep |= 1u << bg;
+            v_last = bv;
+        } else {
+            v_next = bv;
+        }
+    }
+    if (!(v_last - v_next <= thr)) return keep;  // certified (or no finite competitor)
+
+    // undecided groups: score within [v_next - thr, v_last + thr]
+    const float lo = v_next - thr, hi = v_last + thr;
+    const bool sure_in = lane < n_group && gm > hi;
+    const bool undecided = lane < n_group && !sure_in && gm >= lo;
+    const uint32_t und = __ballot_sync(0xffffffffu, undecided);
+    const int n_in = __popc(__ballot_sync(0xffffffffu, sure_in));
+    const int need = topk_group - n_in;
+    // candidates: experts of undecided groups within thr of their group's score
+    int nc = 0;
+    if (lane == 0) {
+        for (int g = 0; g < n_group; ++g) {
+            if (!((und >> g) & 1u)) continue;
+            float m = -INFINITY;
+            for (int e = g * gsize; e < (g + 1) * gsize; ++e) m = fmaxf(m, s_l[e]);
+            for (int e = g * gsize; e < (g + 1) * gsize; ++e)
+                if (s_l[e] >= m - thr) s_cand[nc++] = e;
+        }
+    }
+    nc = __shfl_sync(0xffffffffu, nc, 0);
+    __syncwarp();
+    uint32_t result = 0;
+    for (int pass = 0; pass < 2; ++pass) {
+        for (int c = 0; c < nc; ++c) {
+            const int e = s_cand[c];
+            double v = pass == 0 ? refine_dot2(xrow, Wg + (int64_t)e * H, H, lane)
+                                 : refine_dot(xrow, Wg + (int64_t)e * H, H, lane);
+            if (bias) v += (double)bias[e];
+            if (lane == 0) s_val[c] = v;
+        }
+        __syncwarp();
+        bool decided = true;
+        uint32_t chosen = 0;
+        if (lane == 0) {
+            // recomputed score of each undecided group, then the need best of them
+            double gs[32];
+            for (int g = 0; g < n_group; ++g) gs[g] = -INFINITY;
+            for (int c = 0; c < nc; ++c) {
+                const int g = s_cand[c] / gsize;
+                if (s_val[c] > gs[g]) gs[g] = s_val[c];
+            }
+            double last = 0.0, next = -INFINITY;
+            for (int r = 0; r <= need; ++r) {
+                int bg = -1;
+                for (int g = 0; g < n_group; ++g) {
+                    if (!((und >> g) & 1u) || ((chosen >> g) & 1u)) continue;
+                    if (bg < 0 || gs[g] > gs[bg]) bg = g;
+                }
+                if (bg < 0) break;
+                if (r < need) {
+                    chosen |= 1u << bg;
+                    last = gs[bg];
+                } else {
+                    next = gs[bg];
+                }
+            }
+            decided = pass == 1 || !(last - next <= (double)thr2);
+        }
+        decided = __shfl_sync(0xffffffffu, decided ? 1 : 0, 0) != 0;
+        result = __shfl_sync(0xffffffffu, chosen, 0);
+        __syncwarp();
+        if (decided) break;
+    }
+    const uint32_t sure = __ballot_sync(0xffffffffu, sure_in);
+    return sure | result;
+}
+
 template <int PL>
 __device__ __forceinline__ float pick(const float (&l)[PL], int idx) {
     float v = 0.f;
@@ -349,7 +461,7 @@ __device__ __forceinline__ float pick(const float (&l)[PL], int idx) {
 template <int PL>
 __global__ void __launch_bounds__(RS_WARPS * 32) router_select_kernel(
     const float* __restrict__ part, const float* __restrict__ xsq, const float* __restrict__ wsq, int nsplit,
-    float thr_coef, float thr2_coef, const float* __restrict__ bias, const uint16_t* __restrict__ x, const float* __restrict__ Wg,
+    float thr_coef, float thr2_coef, int n_group, int topk_group, const float* __restrict__ bias, const uint16_t* __restrict__ x, const float* __restrict__ Wg,
     int64_t T, int H, int E, int k, int renorm, int32_t* __restrict__ ids, float* __restrict__ wout,
     WsHeader* hdr) {
     extern __shared__ __align__(16) unsigned char rs_smem[];
@@ -362,6 +474,9 @@ __global__ void __launch_bounds__(RS_WARPS * 32) router_select_kernel(
     float* s_v = reinterpret_cast<float*>(reinterpret_cast<int*>(reinterpret_cast<double*>(rs_smem) +
                                                                  (size_t)RS_WARPS * E) +
                                           (size_t)RS_WARPS * E) +
+                 (size_t)warp * E;
+    // grouped top-k: this warp's fp32 logits, by expert id
+    float* s_l = reinterpret_cast<float*>(rs_smem + (size_t)RS_WARPS * E * (sizeof(double) + sizeof(int) + sizeof(float))) +
                  (size_t)warp * E;
     __shared__ float s_red[2][RS_WARPS];
 
@@ -440,9 +555,21 @@ __global__ void __launch_bounds__(RS_WARPS * 32) router_select_kernel(
         // the same for the compensated values (twice their bound)
         const float thr2 = thr2_coef * fmaf(sqrtf(xs2), wnorm_max, bias_max);
 
+        // group-limited top-k: experts of groups that are not kept start out taken
+        uint32_t taken = 0;
+        if (n_group > 1 && topk_group < n_group) {
+            const uint32_t keep = select_groups(l, s_l, s_e, s_ref, E, n_group, topk_group, thr, thr2,
+                                                x + t * (int64_t)H, Wg, bias, H, lane);
+            const int gsize = E / n_group;
+#pragma unroll
+            for (int i = 0; i < PL; ++i) {
+                const int e = lane + 32 * i;
+                if (e < E && !((keep >> (e / gsize)) & 1u)) taken |= 1u << i;
+            }
+        }
+
         // extract candidates in (logit desc, id asc) order until the cluster
         // that contains rank k-1 is closed
-        uint32_t taken = 0;
         int R = 0;
         float prev_v = 0.f;
         while (R < E) {
@@ -656,7 +783,7 @@ cudaError_t launch_router(const RouterLaunch& L, int num_sms, cudaStream_t s) {
     const double na = (L.H + 127) / 128, nc = 128.0;
     const double ga = na * u32 / (1.0 - na * u32), gc = nc * u32 / (1.0 - nc * u32);
     const float thr2_coef = (float)(2.0 * ((ga + gc) * (ga + gc) + g64 + 3.0 * u64) * 1.01);
-    const size_t smem = (size_t)RS_WARPS * L.E * (sizeof(double) + sizeof(int) + sizeof(float));
+    const size_t smem = (size_t)RS_WARPS * L.E * (sizeof(double) + sizeof(int) + 2 * sizeof(float));
     const int64_t want = (L.T + RS_WARPS - 1) / RS_WARPS;
     const unsigned grid2 = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms * 8));
 #define MOE_SELECT(PLV)                                                                                          \
@@ -667,7 +794,7 @@ cudaError_t launch_router(const RouterLaunch& L, int num_sms, cudaStream_t s) {
             if (err != cudaSuccess) return err;                                                                  \
         }                                                                                                        \
         err = launch_k(router_select_kernel<PLV>, dim3(grid2), dim3(RS_WARPS * 32), smem, s, L.part, L.xsq,     \
-                       L.wsq, L.nsplit, thr_coef, thr2_coef, L.bias, L.x, L.Wg, L.T, L.H, L.E, L.k, L.renorm, L.ids, L.w,    \
+                       L.wsq, L.nsplit, thr_coef, thr2_coef, L.n_group, L.topk_group, L.bias, L.x, L.Wg, L.T, L.H, L.E, L.k, L.renorm, L.ids, L.w,    \
                        L.hdr);                                                                                   \
     } while (0)
     if (L.E <= 32)

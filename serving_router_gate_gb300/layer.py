@@ -14,7 +14,7 @@ from typing import Optional
 
 import torch
 
-from . import (MOE_NONLOCAL_SKIP, moe_forward, moe_permute, moe_route, moe_workspace_init,
+from . import (MOE_NONLOCAL_SKIP, moe_forward, moe_permute, moe_route, moe_route_grouped, moe_workspace_init,
                moe_workspace_size)
 
 
@@ -24,8 +24,13 @@ class MoELayer:
                  rep_offset: Optional[torch.Tensor] = None, rep_slots: Optional[torch.Tensor] = None,
                  S: Optional[int] = None, local_start: int = 0, local_count: int = -1,
                  nonlocal_mode: int = MOE_NONLOCAL_SKIP, W1s: Optional[torch.Tensor] = None,
-                 W2s: Optional[torch.Tensor] = None, shared_gate_w: Optional[torch.Tensor] = None):
+                 W2s: Optional[torch.Tensor] = None, shared_gate_w: Optional[torch.Tensor] = None,
+                 on_input: bool = False, n_group: int = 1, topk_group: int = 1):
         self.Wg, self.W1, self.W2 = Wg, W1, W2
+        # routing applied on the input: rows scaled by the weights, outputs summed unweighted
+        self.on_input = bool(on_input)
+        # group-limited top-k (n_group <= 1: plain top-k)
+        self.n_group, self.topk_group = int(n_group), int(topk_group)
         self.E, self.H = Wg.shape
         self.I = W2.shape[2]
         self.k, self.renorm = int(k), bool(renorm)
@@ -62,19 +67,23 @@ class MoELayer:
 
     def route(self, x: torch.Tensor, stream=None) -> dict:
         v = self.views(x.shape[0])
-        moe_route(x, self.Wg, self.bias, self.k, self.renorm, v["topk_ids"], v["topk_w"], self.ws, stream)
+        if self.n_group > 1:
+            moe_route_grouped(x, self.Wg, self.bias, self.k, self.renorm, self.n_group, self.topk_group,
+                              v["topk_ids"], v["topk_w"], self.ws, stream)
+        else:
+            moe_route(x, self.Wg, self.bias, self.k, self.renorm, v["topk_ids"], v["topk_w"], self.ws, stream)
         return v
 
     def permute(self, x: torch.Tensor, stream=None) -> dict:
         v = self.views(x.shape[0])
         moe_permute(v["topk_ids"], v["topk_w"], self.E, self.rep_offset, self.rep_slots, self.S,
                     self.local_start, self.local_count, self.mode, x, v["slot_ids"], v["counts"], v["offsets"],
-                    v["perm_src"], v["pair_row"], v["x_perm"], self.ws, stream)
+                    v["perm_src"], v["pair_row"], v["x_perm"], self.ws, stream, on_input=self.on_input)
         return v
 
     def expert_forward(self, x: torch.Tensor, stream=None) -> dict:
         v = self.views(x.shape[0])
-        moe_forward(v["x_perm"], v["offsets"], self.W1, self.W2, v["pair_row"], v["topk_w"],
+        moe_forward(v["x_perm"], v["offsets"], self.W1, self.W2, v["pair_row"], None if self.on_input else v["topk_w"],
                     x if (self.I_sh > 0) else None, self.W1s, self.W2s, self.gate, v["out"], self.ws, stream)
         return v
 
@@ -115,7 +124,7 @@ class MoELayer:
 
 
 def layer_from_inputs(inp: dict, device="cuda", max_T: Optional[int] = None, local_start: int = 0,
-                      local_count: int = -1, nonlocal_mode: int = MOE_NONLOCAL_SKIP) -> MoELayer:
+                      local_count: int = -1, nonlocal_mode: int = MOE_NONLOCAL_SKIP, on_input: bool = False) -> MoELayer:
     """A MoELayer over the tensors of moe_inputs.make_inputs() (moved to `device`)."""
     from moe_inputs import shared_concat
     cfg = inp["cfg"]
@@ -133,4 +142,5 @@ def layer_from_inputs(inp: dict, device="cuda", max_T: Optional[int] = None, loc
     return MoELayer(d(inp["Wg"]), d(W1), d(W2), cfg.k, cfg.renorm, max_T or cfg.T, logit_bias=d(inp["bias"]),
                     rep_offset=d(inp["rep_offset"]), rep_slots=d(inp["rep_slots"]), S=cfg.slots,
                     local_start=local_start, local_count=local_count, nonlocal_mode=nonlocal_mode,
-                    W1s=d(W1s), W2s=d(W2s), shared_gate_w=d(inp["w_s"]))
+                    W1s=d(W1s), W2s=d(W2s), shared_gate_w=d(inp["w_s"]), on_input=on_input,
+                    n_group=cfg.n_group, topk_group=cfg.topk_group)

@@ -66,11 +66,11 @@ def check_out(out_gpu: torch.Tensor, ref: np.ndarray, what="out"):
     return float(err.max()), tol
 
 
-def run_gpu(inp: dict, local_start=0, local_count=-1, mode=0, layer=None):
+def run_gpu(inp: dict, local_start=0, local_count=-1, mode=0, layer=None, on_input=False):
     """Route, permute and forward on the GPU; returns CPU copies of every output."""
     if layer is None:
         layer = layer_from_inputs(inp, "cuda", local_start=local_start, local_count=local_count,
-                                  nonlocal_mode=mode)
+                                  nonlocal_mode=mode, on_input=on_input)
     x = inp["x"].cuda()
     out = layer.forward(x)
     torch.cuda.synchronize()
@@ -85,7 +85,7 @@ def run_gpu(inp: dict, local_start=0, local_count=-1, mode=0, layer=None):
     return res
 
 
-def oracle_layer(inp_cpu: dict, local_start=0, local_count=-1, mode=0, tokens=None):
+def oracle_layer(inp_cpu: dict, local_start=0, local_count=-1, mode=0, tokens=None, on_input=False):
     cfg = inp_cpu["cfg"]
     W1, W2 = inp_cpu["W1"], inp_cpu["W2"]
     if local_count >= 0:
@@ -93,7 +93,7 @@ def oracle_layer(inp_cpu: dict, local_start=0, local_count=-1, mode=0, tokens=No
         W2 = W2[local_start:local_start + local_count]
     kw = dict(rep_offset=inp_cpu["rep_offset"], rep_slots=inp_cpu["rep_slots"], local_start=local_start,
               local_count=local_count, mode=mode, W1s=inp_cpu["W1s"], W2s=inp_cpu["W2s"],
-              shared_gate_w=inp_cpu["w_s"])
+              shared_gate_w=inp_cpu["w_s"], n_group=cfg.n_group, topk_group=cfg.topk_group, on_input=on_input)
     if tokens is None:
         return oracle.moe_layer(inp_cpu["x"], inp_cpu["Wg"], inp_cpu["bias"], cfg.k, cfg.renorm, W1, W2,
                                 S=cfg.slots, **kw)
@@ -104,7 +104,8 @@ def oracle_layer(inp_cpu: dict, local_start=0, local_count=-1, mode=0, tokens=No
 def oracle_routing(inp_cpu: dict, local_start=0, local_count=-1, mode=0):
     """Routing + slot map + mask + permutation of every token (no expert MLPs)."""
     cfg = inp_cpu["cfg"]
-    ids, w, _ = oracle.route(inp_cpu["x"], inp_cpu["Wg"], inp_cpu["bias"], cfg.k, cfg.renorm)
+    ids, w, _ = oracle.route(inp_cpu["x"], inp_cpu["Wg"], inp_cpu["bias"], cfg.k, cfg.renorm, cfg.n_group,
+                             cfg.topk_group)
     slots = oracle.slot_map(ids, inp_cpu["rep_offset"], inp_cpu["rep_slots"])
     if local_count >= 0:
         slots, w_m, _ = oracle.local_mask(slots, w, local_start, local_count, mode)

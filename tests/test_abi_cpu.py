@@ -139,3 +139,21 @@ def test_rejected_calls_launch_nothing():
     assert r(None, FAKE, None, 16, 256, 8, 2, 1, FAKE, FAKE, FAKE, 1 << 30, None) == moe.MOE_ERR_INVALID_ARG
     assert r(FAKE, FAKE, None, 16, 256, 8, 2, 1, FAKE, FAKE, FAKE, 64, None) == moe.MOE_ERR_WORKSPACE
     assert moe.moe_get_launch_count() == before
+
+
+def test_route_grouped_rejects_bad_group_parameters_on_host():
+    r = moe._lib.moe_route_grouped
+    args = lambda E, k, ng, tg: (FAKE, FAKE, None, 16, 256, E, k, 1, ng, tg, FAKE, FAKE, FAKE, 1 << 30, None)  # noqa: E731
+    assert r(*args(32, 4, 5, 2)) == moe.MOE_ERR_INVALID_ARG    # E not a multiple of n_group
+    assert r(*args(32, 4, 8, 9)) == moe.MOE_ERR_INVALID_ARG    # topk_group > n_group
+    assert r(*args(32, 9, 8, 2)) == moe.MOE_ERR_INVALID_ARG    # k > topk_group * E / n_group
+    assert r(*args(128, 4, 64, 2)) == moe.MOE_ERR_INVALID_ARG  # n_group > 32
+    assert r(*args(32, 4, 0, 1)) == moe.MOE_ERR_INVALID_ARG
+    assert r(None, None, None, 0, 256, 32, 4, 1, 8, 2, None, None, None, 0, None) == moe.MOE_OK  # T = 0
+
+
+def test_permute_on_input_shares_the_host_validation():
+    p = moe._lib.moe_permute_on_input
+    # S != E without a slot table
+    assert p(FAKE, FAKE, 16, 2, 8, None, None, 9, 0, -1, 0, FAKE, 256, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+             FAKE, 1 << 30, None) == moe.MOE_ERR_INVALID_ARG

@@ -259,6 +259,79 @@ def test_small_batch_splits_shared_fc2_and_matches_unsplit_stages():
     assert moe.moe_get_device_status(layer.ws) == 0
 
 
+# --------------------------------------------------------------------------- group-limited top-k
+
+def test_grouped_topk_layer_full_compare():
+    """moe_route_grouped: ids, weights, permutation and outputs against the oracle's
+    group-limited top-k (8 groups of 4 experts, 3 groups kept)."""
+    cfg = mi.MoEConfig("grouped", T=700, H=512, I=256, E=32, k=4, renorm=True, n_group=8, topk_group=3,
+                       n_shared=1, I_shared=256)
+    inp = mi.make_inputs(cfg)
+    g, ref = _full_check(inp)
+    ids = g["topk_ids"].numpy()
+    assert max(len({int(e) // 4 for e in row}) for row in ids) <= 3
+    # the restriction matters: plain top-k picks other experts for some tokens
+    plain, _, _ = oracle.route(inp["x"], inp["Wg"], None, 4, True)
+    assert not np.array_equal(plain, ids)
+
+
+def test_grouped_topk_exact_group_tie_goes_to_lower_group():
+    """Group 1 is a copy of group 0, so their scores tie exactly for every token: the
+    fp32 gap is zero, the compensated and fp64 rechecks tie too, and the lower group
+    must win (as in the oracle)."""
+    cfg = mi.MoEConfig("gtie", T=300, H=256, I=128, E=16, k=2, renorm=True, n_group=4, topk_group=1)
+    inp = mi.make_inputs(cfg)
+    Wg = inp["Wg"].clone()
+    Wg[4:8] = Wg[0:4]
+    inp["Wg"] = Wg
+    g, ref = _full_check(inp)
+    ids = g["topk_ids"].numpy()
+    assert not (ids // 4 == 1).any()  # group 1 never wins over its copy
+    # group 0 wins for some tokens, and those needed the recheck
+    assert (ids // 4 == 0).any()
+
+
+# --------------------------------------------------------------------------- routing applied on the input
+
+def _on_input_check(inp, local_start=0, local_count=-1, mode=0):
+    g = run_gpu(inp, local_start, local_count, mode, on_input=True)
+    ref = oracle_layer(to_cpu(inp), local_start, local_count, mode, on_input=True)
+    check_routing(g, dict(ids=ref["ids"], w=ref["w"], w_masked=ref["w_masked"], slots=ref["slots"],
+                          counts=ref["counts"], offsets=ref["offsets"], perm_src=ref["perm_src"],
+                          pair_row=ref["pair_row"]), to_cpu(inp), masked=local_count >= 0)
+    # x_perm rows are the routing weight times the token's row, rounded once to bf16:
+    # against the oracle's weight (fp64), so within one bf16 rounding plus the weight error
+    rows = g["rows"]
+    perm = g["perm_src"].numpy()[:rows]
+    k = inp["cfg"].k
+    wm = ref["w_masked"].reshape(-1)[perm]
+    x64 = inp["x"].double().numpy()[perm // k]
+    xp = g["x_perm"][:rows].double().cpu().numpy()
+    exp_rows = wm[:, None] * x64
+    assert np.all(np.abs(xp - exp_rows) <= 2.0 ** -8 * np.abs(exp_rows) + 1e-6 * np.abs(x64) + 1e-30)
+    check_out(g["out"], ref["out"])
+    assert moe.moe_get_device_status(g["layer"].ws) == 0
+    return g, ref
+
+
+def test_routing_on_input_mid_layer():
+    _on_input_check(mi.make_inputs(MID))
+
+
+def test_routing_on_input_local_ranges_skip_mod_and_sum():
+    cfg = mi.MoEConfig("oi_ranges", T=600, H=256, I=256, E=16, k=4, renorm=True)
+    inp = mi.make_inputs(cfg)
+    full, _ = _on_input_check(inp)
+    acc = torch.zeros_like(full["out"], dtype=torch.float64)
+    for start in (0, 8):
+        gs, _ = _on_input_check(inp, start, 8, moe.MOE_NONLOCAL_SKIP)
+        gm, _ = _on_input_check(inp, start, 8, moe.MOE_NONLOCAL_MOD)
+        assert torch.equal(gs["out"].view(torch.int16), gm["out"].view(torch.int16))  # zero rows add nothing
+        acc += gs["out"].double()
+    a, b = acc.numpy(), full["out"].double().numpy()
+    assert np.abs(a - b).max() <= 2.0 ** -7 * np.abs(b).max() + 1e-3
+
+
 # --------------------------------------------------------------------------- device-side error paths
 
 def test_out_of_range_expert_ids_are_dropped_and_flagged():
