@@ -216,7 +216,8 @@ def run_cpu_baseline(inp_dev, cfg, target_s=10.0, T_cap=None):
         t0 = time.perf_counter()
         oracle.moe_layer(cpu["x"][:n], cpu["Wg"], cpu["bias"], cfg.k, cfg.renorm, cpu["W1"], cpu["W2"],
                          rep_offset=cpu["rep_offset"], rep_slots=cpu["rep_slots"], W1s=cpu["W1s"],
-                         W2s=cpu["W2s"], shared_gate_w=cpu["w_s"], S=cfg.slots)
+                         W2s=cpu["W2s"], shared_gate_w=cpu["w_s"], S=cfg.slots, n_group=cfg.n_group,
+                         topk_group=cfg.topk_group, on_input=cfg.on_input)
         return time.perf_counter() - t0
 
     threads = oracle.get_threads()
@@ -288,8 +289,8 @@ def bench_ours(args):
         "permute": lambda: layer.permute(x),
         "fc1": lambda: moe.moe_grouped_fc1(layer.x_perm, layer.offsets, layer.W1, xs, layer.W1s, h, h_sh, layer.ws),
         "fc2": lambda: moe.moe_grouped_fc2(h, layer.offsets, layer.W2, h_sh, layer.W2s, y, y_sh, layer.ws),
-        "finalize": lambda: moe.moe_finalize(y, layer.pair_row, layer.topk_w, y_sh, xs, layer.gate, layer.out,
-                                             layer.ws),
+        "finalize": lambda: moe.moe_finalize(y, layer.pair_row, None if layer.on_input else layer.topk_w, y_sh, xs,
+                                             layer.gate, layer.out, layer.ws),
     }
     for fn in stages.values():
         fn()
@@ -400,7 +401,8 @@ def bench_reference(args):
     def step(n):
         oracle.moe_layer(cpu["x"][:n], cpu["Wg"], cpu["bias"], cfg.k, cfg.renorm, cpu["W1"], cpu["W2"],
                          rep_offset=cpu["rep_offset"], rep_slots=cpu["rep_slots"], W1s=cpu["W1s"],
-                         W2s=cpu["W2s"], shared_gate_w=cpu["w_s"], S=cfg.slots)
+                         W2s=cpu["W2s"], shared_gate_w=cpu["w_s"], S=cfg.slots, n_group=cfg.n_group,
+                         topk_group=cfg.topk_group, on_input=cfg.on_input)
 
     threads = oracle.get_threads()
     n0 = min(cfg.T, max(8, threads))

@@ -59,6 +59,7 @@ class MoEConfig:
     shared_gate: bool = False        # scale the shared output by sigmoid(x . w_s)
     n_group: int = 1                 # group-limited top-k: expert groups (1: plain top-k)
     topk_group: int = 1              # groups kept per token
+    on_input: bool = False           # routing weight applied to the expert input, outputs summed unweighted
     w_std: float = 0.02              # expert weight std
     gate_std: float = 0.02           # router weight std
     seed: int = 0
@@ -80,6 +81,13 @@ CONFIGS = {
     "redundant_slots_prefill": MoEConfig("redundant_slots_prefill", T=16384, H=7168, I=2048, E=256,
                                          k=8, renorm=True, S=288, n_hot=32, zipf_s=1.1, w_std=0.01),
 }
+# the router variants of the next steps, on the Qwen2-like and DeepSeek-V2-Lite-like shapes:
+# group-limited top-k (DeepSeek-V2-style: 8 groups, 3 kept, k = 6 of 64 experts) and the
+# routing weight applied on the expert input
+CONFIGS["grouped_topk_prefill"] = MoEConfig("grouped_topk_prefill", T=4096, H=2048, I=1408, E=64, k=6,
+                                            renorm=False, n_shared=2, I_shared=2816, n_group=8, topk_group=3)
+CONFIGS["routing_on_input_prefill"] = CONFIGS["qwen2_moe_like_prefill"].with_(name="routing_on_input_prefill",
+                                                                              on_input=True)
 for _t in (1, 8, 32, 128):
     CONFIGS[f"dsv2_lite_like_decode_t{_t}"] = MoEConfig(
         f"dsv2_lite_like_decode_t{_t}", T=_t, H=2048, I=1408, E=64, k=6, renorm=False,
@@ -209,6 +217,10 @@ def describe(cfg: MoEConfig) -> str:
         parts.append(f"shared={cfg.n_shared}x{cfg.I_shared}" + ("+sigmoid gate" if cfg.shared_gate else ""))
     if cfg.zipf_s:
         parts.append(f"zipf={cfg.zipf_s}")
+    if cfg.n_group > 1:
+        parts.append(f"grouped top-k {cfg.topk_group} of {cfg.n_group} groups")
+    if cfg.on_input:
+        parts.append("routing on input")
     return ", ".join(parts)
 
 

@@ -124,10 +124,14 @@ class MoELayer:
 
 
 def layer_from_inputs(inp: dict, device="cuda", max_T: Optional[int] = None, local_start: int = 0,
-                      local_count: int = -1, nonlocal_mode: int = MOE_NONLOCAL_SKIP, on_input: bool = False) -> MoELayer:
-    """A MoELayer over the tensors of moe_inputs.make_inputs() (moved to `device`)."""
+                      local_count: int = -1, nonlocal_mode: int = MOE_NONLOCAL_SKIP,
+                      on_input: Optional[bool] = None) -> MoELayer:
+    """A MoELayer over the tensors of moe_inputs.make_inputs() (moved to `device`); the
+    routing variant (groups, routing on the input) follows the workload unless given."""
     from moe_inputs import shared_concat
     cfg = inp["cfg"]
+    if on_input is None:
+        on_input = cfg.on_input
 
     def d(t):
         return None if t is None else t.to(device).contiguous()

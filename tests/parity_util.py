@@ -66,7 +66,7 @@ def check_out(out_gpu: torch.Tensor, ref: np.ndarray, what="out"):
     return float(err.max()), tol
 
 
-def run_gpu(inp: dict, local_start=0, local_count=-1, mode=0, layer=None, on_input=False):
+def run_gpu(inp: dict, local_start=0, local_count=-1, mode=0, layer=None, on_input=None):
     """Route, permute and forward on the GPU; returns CPU copies of every output."""
     if layer is None:
         layer = layer_from_inputs(inp, "cuda", local_start=local_start, local_count=local_count,
@@ -85,8 +85,10 @@ def run_gpu(inp: dict, local_start=0, local_count=-1, mode=0, layer=None, on_inp
     return res
 
 
-def oracle_layer(inp_cpu: dict, local_start=0, local_count=-1, mode=0, tokens=None, on_input=False):
+def oracle_layer(inp_cpu: dict, local_start=0, local_count=-1, mode=0, tokens=None, on_input=None):
     cfg = inp_cpu["cfg"]
+    if on_input is None:
+        on_input = cfg.on_input
     W1, W2 = inp_cpu["W1"], inp_cpu["W2"]
     if local_count >= 0:
         W1 = W1[local_start:local_start + local_count]
