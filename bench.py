@@ -344,9 +344,12 @@ def bench_ours(args):
         per_unit = f"{wk['fc1_bytes']:.0f} algorithmic bytes per launch (active slots' W1 + shared W1 + A rows + h)"
     else:
         achieved = wk["fc1_flops"] / fc1_s / 1e12
+        # burst peak: each step is a fraction of a millisecond between L2 flushes, and the
+        # clocks sampled during the timed region stay at their maximum (no power capping)
         roof = dict(bound="tensor", kernel="grouped_gemm_kernel<FC1+SwiGLU>", achieved=achieved,
-                    peak=peaks["bf16_sustained"], unit="TFLOP/s", frac=achieved / peaks["bf16_sustained"],
-                    peak_kind=f"{peaks['src']} bf16_tflops_sustained (kernel timed inside a seconds-long loop)")
+                    peak=peaks["bf16"], unit="TFLOP/s", frac=achieved / peaks["bf16"],
+                    peak_kind=f"{peaks['src']} bf16_tflops (burst; the kernel is timed in sub-millisecond steps "
+                              f"at full clock)")
         per_unit = f"{wk['fc1_flops']:.4g} flops per launch = 4*H*(rows*I + T*I_shared)"
     key = (args.workload, _src_hash(os.path.join(ROOT, "serving_router_gate_gb300", "csrc", "moe_grouped_gemm.cu")))
     roof["traffic"] = NCU_TRAFFIC.get(key)
