@@ -74,7 +74,16 @@ def _load():
         lib.oracle_expert_mlp.argtypes = [P, P, P, i32, i32, P, P]
         lib.oracle_expert_mlp.restype = None
         lib.oracle_moe_tokens.argtypes = [P, i64, i32, P, P, i32, i32, i32, i32, i32, i32, P, P, i32, i32, i32,
-                                          P, P, i32, i32, P, P, i32, P, P, i64, P, P, P, P]
+                                          P, P, i32, i32, P, P, i32, P, P, P, P, P, P, P, P, P,
+                                          P, i64, P, P, P, P]
+        lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_to_f64.restype = ctypes.c_double
+        lib.oracle_f64_to_e4m3.argtypes = [ctypes.c_double]
+        lib.oracle_f64_to_e4m3.restype = ctypes.c_uint8
+        lib.oracle_quantize_fp8_rows.argtypes = [P, i64, i32, P, P]
+        lib.oracle_quantize_fp8_rows.restype = None
+        lib.oracle_expert_mlp_fp8.argtypes = [P, P, P, P, P, i32, i32, P, P]
+        lib.oracle_expert_mlp_fp8.restype = None
         lib.oracle_moe_tokens.restype = None
         lib.oracle_set_threads.argtypes = [i32]
         lib.oracle_set_threads.restype = None
@@ -201,14 +210,53 @@ def expert_mlp(x_row, W1, W2):
     return y, h
 
 
+def e4m3_to_f64(q: int) -> float:
+    return float(_load().oracle_e4m3_to_f64(int(q)))
+
+
+def f64_to_e4m3(v: float) -> int:
+    """Nearest E4M3 value, ties to even, saturated at +-448; returns the byte."""
+    return int(_load().oracle_f64_to_e4m3(float(v)))
+
+
+def quantize_fp8_rows(w):
+    """C oracle_quantize_fp8_rows on a bf16 matrix [..., K]: returns (q uint8 same shape,
+    scale float32 [...]) with scale = amax/448 per row and q = e4m3(w / scale)."""
+    lib = _load()
+    w16 = _u16(w)
+    shape = w16.shape
+    K = shape[-1]
+    rows = int(np.prod(shape[:-1]))
+    q = np.empty(shape, np.uint8)
+    sc = np.empty(shape[:-1], np.float32)
+    lib.oracle_quantize_fp8_rows(_ptr(np.ascontiguousarray(w16)), rows, K, _ptr(q), _ptr(sc))
+    return q, sc
+
+
+def expert_mlp_fp8(x_row, W1q, s1, W2q, s2):
+    """C oracle_expert_mlp_fp8: one token through one SwiGLU expert with E4M3 weights."""
+    lib = _load()
+    x_row = _u16(x_row).reshape(-1)
+    W1q, W2q = _np(W1q, np.uint8), _np(W2q, np.uint8)
+    s1, s2 = _np(s1, np.float32), _np(s2, np.float32)
+    H = x_row.size
+    I = W1q.shape[0] // 2
+    y = np.empty(H, np.float64)
+    h = np.empty(I, np.uint16)
+    lib.oracle_expert_mlp_fp8(_ptr(x_row), _ptr(W1q), _ptr(s1), _ptr(W2q), _ptr(s2), H, I, _ptr(y), _ptr(h))
+    return y, h
+
+
 def moe_tokens(x, Wg, bias, k, renorm, W1, W2, tokens=None, rep_offset=None, rep_slots=None,
                local_start=0, local_count=-1, mode=NONLOCAL_SKIP,
-               W1s=None, W2s=None, shared_gate_w=None, n_group=1, topk_group=1, on_input=False):
+               W1s=None, W2s=None, shared_gate_w=None, n_group=1, topk_group=1, on_input=False, fp8=None):
     """C oracle_moe_tokens: full layer output (float64) for the listed tokens.
 
     n_group / topk_group: group-limited top-k (n_group <= 1: plain top-k).
     on_input: the routing weight scales each expert's input (rounded to bf16)
     and the expert outputs are summed unweighted.
+    fp8: None, or a dict of E4M3 weights with row scales (W1q, s1, W2q, s2 and,
+    with shared experts, W1sq, s1s, W2sq, s2s) used in place of W1/W2/W1s/W2s.
 
     W1 [S_local, 2I, H], W2 [S_local, H, I] are indexed by local slot.
     W1s [n_shared, 2*I_sh, H] / W2s [n_shared, H, I_sh] (or None).
@@ -240,17 +288,23 @@ def moe_tokens(x, Wg, bias, k, renorm, W1, W2, tokens=None, rep_offset=None, rep
     ids = np.empty((n, k), np.int32)
     w = np.empty((n, k), np.float64)
     sl = np.empty((n, k), np.int32)
+    f = fp8 or {}
+    fq = {key: (_np(f[key], np.uint8) if key.endswith("q") else _np(f[key], np.float32)) if f.get(key) is not None
+          else None for key in ("W1q", "s1", "W2q", "s2", "W1sq", "s1s", "W2sq", "s2s")}
     lib.oracle_moe_tokens(_ptr(x), T, H, _ptr(Wg), _ptr(bias), E, k, int(bool(renorm)),
                           int(n_group), int(topk_group), int(bool(on_input)),
                           _ptr(ro), _ptr(rs), local_start, local_count, mode,
                           _ptr(W1), _ptr(W2), I, n_shared, _ptr(W1s), _ptr(W2s), I_sh, _ptr(gw),
+                          _ptr(fq["W1q"]), _ptr(fq["s1"]), _ptr(fq["W2q"]), _ptr(fq["s2"]),
+                          _ptr(fq["W1sq"]), _ptr(fq["s1s"]), _ptr(fq["W2sq"]), _ptr(fq["s2s"]),
                           _ptr(tokens), n, _ptr(out), _ptr(ids), _ptr(w), _ptr(sl))
     return dict(out=out, ids=ids, w=w, slots=sl)
 
 
 def moe_layer(x, Wg, bias, k, renorm, W1, W2, rep_offset=None, rep_slots=None,
               local_start=0, local_count=-1, mode=NONLOCAL_SKIP,
-              W1s=None, W2s=None, shared_gate_w=None, S=None, n_group=1, topk_group=1, on_input=False):
+              W1s=None, W2s=None, shared_gate_w=None, S=None, n_group=1, topk_group=1, on_input=False,
+              fp8=None):
     """The whole layer on a batch: routing, slot map, mask, permutation and outputs.
 
     Composes the C steps in the order the layer runs them; returns a dict with
@@ -270,7 +324,7 @@ def moe_layer(x, Wg, bias, k, renorm, W1, W2, rep_offset=None, rep_slots=None,
     counts, offsets, perm_src, pair_row = permute(slots_l, S_local)
     res = moe_tokens(x, Wg, bias, k, renorm, W1, W2, None, rep_offset, rep_slots,
                      local_start, local_count if local_count is not None else -1, mode,
-                     W1s, W2s, shared_gate_w, n_group, topk_group, on_input)
+                     W1s, W2s, shared_gate_w, n_group, topk_group, on_input, fp8)
     return dict(ids=ids, w=w, logits=logits, slots_global=slots, slots=slots_l, w_masked=w_l,
                 mask=mask, counts=counts, offsets=offsets, perm_src=perm_src,
                 pair_row=pair_row.reshape(ids.shape), out=res["out"])

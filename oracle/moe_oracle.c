@@ -81,6 +81,87 @@ uint16_t oracle_f64_to_bf16(double v)
 }
 
 /* ------------------------------------------------------------------------- */
+/* FP8 E4M3 weights with one fp32 scale per row                               */
+/* ------------------------------------------------------------------------- */
+
+/* FP8 expert weights (TensorRT-LLM AutoDeploy MoE PR #10985, review of
+ * torch_moe.py: the MoE ops have FP8 and NVFP4 paths).  The pages give no
+ * format; the reading taken is the plainest one: OCP E4M3 ("fn": sign, 4
+ * exponent bits with bias 7, 3 mantissa bits, no infinities, 0x7F / 0xFF NaN,
+ * largest finite 448, subnormal spacing 2^-9) with one fp32 scale per output
+ * row, W[r][c] = scale[r] * e4m3(q[r][c]). */
+double oracle_e4m3_to_f64(uint8_t q)
+{
+    const int sgn = q >> 7, e = (q >> 3) & 0xF, m = q & 7;
+    if (e == 15 && m == 7) return NAN;
+    double v = (e == 0) ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, e - 7);
+    return sgn ? -v : v;
+}
+
+/* Nearest E4M3 value, ties to even, finite results saturated at +-448
+ * (as a saturating conversion does); NaN -> 0x7F. */
+uint8_t oracle_f64_to_e4m3(double v)
+{
+    if (isnan(v)) return 0x7F;
+    const uint8_t sgn = signbit(v) ? 0x80 : 0x00;
+    double a = fabs(v);
+    if (a == 0.0) return sgn;
+    int e;
+    (void)frexp(a, &e);            /* a = f * 2^e, f in [0.5, 1) */
+    int lsb = (e - 1) - 3;         /* weight of the 4th significant bit */
+    if (lsb < -9) lsb = -9;        /* subnormal spacing */
+    double r = ldexp(nearbyint(ldexp(a, -lsb)), lsb);  /* ties to even */
+    if (r > 448.0) r = 448.0;
+    if (r < ldexp(1.0, -6)) {      /* subnormal (or zero): m * 2^-9 */
+        return (uint8_t)(sgn | (uint8_t)ldexp(r, 9));
+    }
+    (void)frexp(r, &e);
+    const int E = e - 1 + 7;       /* r = (1 + m/8) * 2^(e-1) */
+    const int m = (int)(ldexp(r, -(e - 1)) * 8.0) - 8;
+    return (uint8_t)(sgn | (uint8_t)(E << 3) | (uint8_t)m);
+}
+
+/* Row-wise quantisation of a bf16 matrix [rows, K]: scale = amax / 448 (an
+ * IEEE binary32 division), q = e4m3(w / scale) with the division again in
+ * binary32; an all-zero row gets scale 0 and q = 0. */
+void oracle_quantize_fp8_rows(const uint16_t *w, int64_t rows, int K, uint8_t *q, float *scale)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        const uint16_t *wr = w + (size_t)r * (size_t)K;
+        float amax = 0.0f;
+        for (int c = 0; c < K; ++c) {
+            const float f = (float)oracle_bf16_to_f64(wr[c]);
+            if (fabsf(f) > amax) amax = fabsf(f);
+        }
+        volatile float sc = amax / 448.0f;
+        scale[r] = sc;
+        for (int c = 0; c < K; ++c) {
+            if (sc == 0.0f) {
+                q[(size_t)r * (size_t)K + (size_t)c] = 0;
+                continue;
+            }
+            volatile float v = (float)oracle_bf16_to_f64(wr[c]) / sc;
+            q[(size_t)r * (size_t)K + (size_t)c] = oracle_f64_to_e4m3((double)v);
+        }
+    }
+}
+
+/* A weight matrix of the layer: bf16 values, or E4M3 bytes with row scales. */
+typedef struct {
+    const uint16_t *bf;
+    const uint8_t *q;
+    const float *s;
+    size_t K;
+} oracle_wmat;
+
+static double wget(const oracle_wmat *m, size_t row, size_t col)
+{
+    const size_t i = row * m->K + col;
+    return m->q ? (double)m->s[row] * oracle_e4m3_to_f64(m->q[i]) : oracle_bf16_to_f64(m->bf[i]);
+}
+
+/* ------------------------------------------------------------------------- */
 /* 1. Router                                                                  */
 /* ------------------------------------------------------------------------- */
 
@@ -305,28 +386,41 @@ void oracle_permute(const int32_t *slots, int64_t P, int S,
  *   x [H] bf16;  W1 [2I, H] bf16 (rows 0..I-1 gate, I..2I-1 up);  W2 [H, I] bf16
  *   y [H] double out;  h [I] bf16 bits out (or NULL)
  */
-void oracle_expert_mlp(const uint16_t *x, const uint16_t *W1, const uint16_t *W2,
-                       int H, int I, double *y, uint16_t *h_out)
+static void expert_mlp_w(const uint16_t *x, const oracle_wmat *W1, const oracle_wmat *W2,
+                         int H, int I, double *y, uint16_t *h_out)
 {
     double *h = (double *)malloc(sizeof(double) * (size_t)I);
     for (int i = 0; i < I; ++i) {
-        const uint16_t *wg = W1 + (size_t)i * (size_t)H;
-        const uint16_t *wu = W1 + ((size_t)I + (size_t)i) * (size_t)H;
         double g = 0.0, u = 0.0;
-        for (int hh = 0; hh < H; ++hh) g += oracle_bf16_to_f64(wg[hh]) * oracle_bf16_to_f64(x[hh]);
-        for (int hh = 0; hh < H; ++hh) u += oracle_bf16_to_f64(wu[hh]) * oracle_bf16_to_f64(x[hh]);
+        for (int hh = 0; hh < H; ++hh) g += wget(W1, (size_t)i, (size_t)hh) * oracle_bf16_to_f64(x[hh]);
+        for (int hh = 0; hh < H; ++hh) u += wget(W1, (size_t)I + (size_t)i, (size_t)hh) * oracle_bf16_to_f64(x[hh]);
         double a = g / (1.0 + exp(-g)) * u;
         uint16_t b = oracle_f64_to_bf16(a);
         if (h_out) h_out[i] = b;
         h[i] = oracle_bf16_to_f64(b);
     }
     for (int o = 0; o < H; ++o) {
-        const uint16_t *w2 = W2 + (size_t)o * (size_t)I;
         double s = 0.0;
-        for (int i = 0; i < I; ++i) s += oracle_bf16_to_f64(w2[i]) * h[i];
+        for (int i = 0; i < I; ++i) s += wget(W2, (size_t)o, (size_t)i) * h[i];
         y[o] = s;
     }
     free(h);
+}
+
+void oracle_expert_mlp(const uint16_t *x, const uint16_t *W1, const uint16_t *W2,
+                       int H, int I, double *y, uint16_t *h_out)
+{
+    const oracle_wmat w1 = {W1, NULL, NULL, (size_t)H}, w2 = {W2, NULL, NULL, (size_t)I};
+    expert_mlp_w(x, &w1, &w2, H, I, y, h_out);
+}
+
+/* The same MLP with E4M3 weights: W1q [2I, H] with scales s1 [2I], W2q [H, I]
+ * with scales s2 [H] (the dequantised values, exactly, in fp64). */
+void oracle_expert_mlp_fp8(const uint16_t *x, const uint8_t *W1q, const float *s1, const uint8_t *W2q,
+                           const float *s2, int H, int I, double *y, uint16_t *h_out)
+{
+    const oracle_wmat w1 = {NULL, W1q, s1, (size_t)H}, w2 = {NULL, W2q, s2, (size_t)I};
+    expert_mlp_w(x, &w1, &w2, H, I, y, h_out);
 }
 
 /* ------------------------------------------------------------------------- */
@@ -347,6 +441,10 @@ void oracle_expert_mlp(const uint16_t *x, const uint16_t *W1, const uint16_t *W2
  * added to the routed output as in ep_reduce_output of the vLLM EP FusedMoE
  * patch (out = routed_out + shared_out).
  *
+ * Weights: bf16 (W1, W2, W1s, W2s), or, where W1q / W1sq is given, E4M3 bytes
+ * with one fp32 scale per row (W1q [S_local, 2I, H] + s1 [S_local, 2I], W2q
+ * [S_local, H, I] + s2 [S_local, H]; the shared ones alike).
+ *
  * Shared experts: n_shared experts of intermediate size I_sh each; W1s holds
  * them one after another, each [2*I_sh, H] (gate rows, then up rows); W2s holds
  * them one after another, each [H, I_sh].
@@ -361,6 +459,8 @@ void oracle_moe_tokens(const uint16_t *x, int64_t T, int H,
                        const uint16_t *W1, const uint16_t *W2, int I,
                        int n_shared, const uint16_t *W1s, const uint16_t *W2s, int I_sh,
                        const uint16_t *shared_gate_w,
+                       const uint8_t *W1q, const float *s1, const uint8_t *W2q, const float *s2,
+                       const uint8_t *W1sq, const float *s1s, const uint8_t *W2sq, const float *s2s,
                        const int64_t *tok, int64_t n,
                        double *out, int32_t *ids_out, double *w_out, int32_t *slot_out)
 {
@@ -414,8 +514,13 @@ void oracle_moe_tokens(const uint16_t *x, int64_t T, int H,
                 for (int hh = 0; hh < H; ++hh) xs[hh] = oracle_f64_to_bf16(w2[j] * oracle_bf16_to_f64(xt[hh]));
                 xin = xs;
             }
-            oracle_expert_mlp(xin, W1 + (size_t)s * 2u * (size_t)I * (size_t)H,
-                              W2 + (size_t)s * (size_t)H * (size_t)I, H, I, y, NULL);
+            if (W1q)
+                oracle_expert_mlp_fp8(xin, W1q + (size_t)s * 2u * (size_t)I * (size_t)H, s1 + (size_t)s * 2u * (size_t)I,
+                                      W2q + (size_t)s * (size_t)H * (size_t)I, s2 + (size_t)s * (size_t)H, H, I, y,
+                                      NULL);
+            else
+                oracle_expert_mlp(xin, W1 + (size_t)s * 2u * (size_t)I * (size_t)H,
+                                  W2 + (size_t)s * (size_t)H * (size_t)I, H, I, y, NULL);
             const double wj = on_input ? 1.0 : w2[j];
             for (int hh = 0; hh < H; ++hh) o[hh] += wj * y[hh];
         }
@@ -430,8 +535,14 @@ void oracle_moe_tokens(const uint16_t *x, int64_t T, int H,
             }
             double *ysum = (double *)calloc((size_t)H, sizeof(double));
             for (int sidx = 0; sidx < n_shared; ++sidx) {
-                oracle_expert_mlp(xt, W1s + (size_t)sidx * 2u * (size_t)I_sh * (size_t)H,
-                                  W2s + (size_t)sidx * (size_t)H * (size_t)I_sh, H, I_sh, y, NULL);
+                if (W1sq)
+                    oracle_expert_mlp_fp8(xt, W1sq + (size_t)sidx * 2u * (size_t)I_sh * (size_t)H,
+                                          s1s + (size_t)sidx * 2u * (size_t)I_sh,
+                                          W2sq + (size_t)sidx * (size_t)H * (size_t)I_sh, s2s + (size_t)sidx * (size_t)H,
+                                          H, I_sh, y, NULL);
+                else
+                    oracle_expert_mlp(xt, W1s + (size_t)sidx * 2u * (size_t)I_sh * (size_t)H,
+                                      W2s + (size_t)sidx * (size_t)H * (size_t)I_sh, H, I_sh, y, NULL);
                 for (int hh = 0; hh < H; ++hh) ysum[hh] += y[hh];
             }
             for (int hh = 0; hh < H; ++hh) o[hh] += g * ysum[hh];

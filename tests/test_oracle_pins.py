@@ -449,3 +449,100 @@ def test_routing_on_input_local_ranges_sum_to_full_layer():
         assert np.array_equal(part["out"], mod["out"])  # a zero-weight input row gives a zero output
         acc += part["out"]
     np.testing.assert_allclose(acc, full["out"], rtol=0, atol=1e-12 * np.abs(full["out"]).max())
+
+
+# --------------------------------------------------------------------------- E4M3 weights with row scales
+
+def test_e4m3_decode_matches_torch_for_every_byte():
+    q = torch.arange(256, dtype=torch.uint8)
+    ref = q.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle.e4m3_to_f64(int(b)) for b in range(256)])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+def test_e4m3_encode_matches_torch_round_to_nearest_even():
+    g = torch.Generator().manual_seed(5)
+    v = torch.cat([torch.randn(4000, generator=g) * s for s in (1e-3, 0.02, 1.0, 30.0, 120.0)])
+    v = v.clamp(-448, 448)
+    # exact midpoints between neighbouring E4M3 values, normal and subnormal
+    grid = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64)
+    grid = grid[torch.isfinite(grid) & (grid >= 0)].unique().sort().values
+    mids = ((grid[1:] + grid[:-1]) / 2).to(torch.float32)
+    v = torch.cat([v, mids, -mids]).to(torch.float32)
+    ref = v.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.f64_to_e4m3(float(a)) for a in v.numpy()], dtype=np.uint8)
+    assert np.array_equal(got, ref)
+
+
+def test_row_quantisation_bounds_and_largest_value():
+    g = torch.Generator().manual_seed(6)
+    w = (torch.randn(40, 96, generator=g) * 0.02).to(torch.bfloat16)
+    w[3] = 0.0
+    q, sc = oracle.quantize_fp8_rows(w)
+    wf = w.float().numpy()
+    amax = np.abs(wf).max(1)
+    np.testing.assert_array_equal(sc, (amax / np.float32(448.0)).astype(np.float32))
+    deq = sc[:, None].astype(np.float64) * torch.from_numpy(q).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    err = np.abs(deq - wf)
+    # half a unit in the last place: 2^-4 relative for normal values, 2^-10 * scale below 2^-6 * scale
+    bound = np.maximum(2.0 ** -4 * np.abs(wf), 2.0 ** -10 * sc[:, None]) * (1 + 1e-6)
+    assert np.all(err <= bound)
+    assert np.all(q[3] == 0) and sc[3] == 0.0
+    for r in range(40):
+        if r != 3:  # the row's largest |w| maps to +-448 exactly
+            i = int(np.abs(wf[r]).argmax())
+            assert abs(oracle.e4m3_to_f64(int(q[r, i]))) == 448.0
+
+
+def _exact_fp8_weights(shape, gen):
+    """bf16 weights that are exactly scale * e4m3 with scale = 2^-10 (each row holds +-448)."""
+    grid = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float32)
+    grid = grid[torch.isfinite(grid)]
+    idx = torch.randint(0, grid.numel(), shape, generator=gen)
+    w = grid[idx]
+    w[..., 0] = 448.0
+    return (w * 2.0 ** -10).to(torch.bfloat16)
+
+
+def test_fp8_expert_and_layer_equal_bf16_when_weights_are_exact():
+    g = torch.Generator().manual_seed(7)
+    cfg = _small_cfg(T=20, H=64, I=64, E=5, k=2, renorm=True, n_shared=1, I_shared=64)
+    inp = mi.make_inputs(cfg)
+    W1 = _exact_fp8_weights((5, 128, 64), g)
+    W2 = _exact_fp8_weights((5, 64, 64), g)
+    W1s = _exact_fp8_weights((1, 128, 64), g)
+    W2s = _exact_fp8_weights((1, 64, 64), g)
+    q1, s1 = oracle.quantize_fp8_rows(W1)
+    q2, s2 = oracle.quantize_fp8_rows(W2)
+    q1s, s1s = oracle.quantize_fp8_rows(W1s)
+    q2s, s2s = oracle.quantize_fp8_rows(W2s)
+    assert np.all(s1 == 2.0 ** -10) and np.all(s2 == 2.0 ** -10)
+    y8, h8 = oracle.expert_mlp_fp8(inp["x"][0], q1[2], s1[2], q2[2], s2[2])
+    yb, hb = oracle.expert_mlp(inp["x"][0], W1[2], W2[2])
+    assert np.array_equal(y8, yb) and np.array_equal(h8, hb)
+    fp8 = dict(W1q=q1, s1=s1, W2q=q2, s2=s2, W1sq=q1s, s1s=s1s, W2sq=q2s, s2s=s2s)
+    a = oracle.moe_layer(inp["x"], inp["Wg"], None, 2, True, W1, W2, W1s=W1s, W2s=W2s)
+    b = oracle.moe_layer(inp["x"], inp["Wg"], None, 2, True, W1, W2, W1s=W1s, W2s=W2s, fp8=fp8)
+    assert np.array_equal(a["out"], b["out"])
+
+
+def test_fp8_layer_matches_numpy_mlp_of_dequantised_weights():
+    cfg = _small_cfg(T=10, H=64, I=64, E=4, k=1, renorm=True)
+    inp = mi.make_inputs(cfg)
+    q1, s1 = oracle.quantize_fp8_rows(inp["W1"])
+    q2, s2 = oracle.quantize_fp8_rows(inp["W2"])
+    res = oracle.moe_layer(inp["x"], inp["Wg"], None, 1, True, inp["W1"], inp["W2"],
+                           fp8=dict(W1q=q1, s1=s1, W2q=q2, s2=s2))
+    deq = lambda q, s: s[..., None].astype(np.float64) * torch.from_numpy(q).view(  # noqa: E731
+        torch.float8_e4m3fn).to(torch.float64).numpy()
+    D1, D2 = deq(q1, s1), deq(q2, s2)
+    x64 = _bf16_np(inp["x"])
+    for t in range(cfg.T):
+        e = int(res["ids"][t, 0])
+        g = x64[t] @ D1[e][:64].T
+        u = x64[t] @ D1[e][64:].T
+        h = torch.from_numpy(g / (1 + np.exp(-g)) * u).to(torch.bfloat16).to(torch.float64).numpy()
+        ref = h @ D2[e].T
+        np.testing.assert_allclose(res["out"][t], ref, rtol=0, atol=1e-9 * np.abs(ref).max())
