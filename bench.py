@@ -195,8 +195,9 @@ def _work(cfg, rows: int, active_slots: int):
     Ish = cfg.n_shared * cfg.I_shared
     fc1_flops = 4.0 * H * (rows * I + T * Ish)
     fc2_flops = 2.0 * H * (rows * I + T * Ish)
-    w1 = active_slots * 2 * I * H * 2 + 2 * Ish * H * 2
-    w2 = active_slots * H * I * 2 + H * Ish * 2
+    eb = 1 if cfg.fp8 else 2  # bytes per weight (E4M3 adds one fp32 scale per row)
+    w1 = active_slots * 2 * I * (H * eb + (4 if cfg.fp8 else 0)) + 2 * Ish * (H * eb + (4 if cfg.fp8 else 0))
+    w2 = active_slots * H * (I * eb + (4 if cfg.fp8 else 0)) + H * (Ish * eb + (4 if cfg.fp8 else 0))
     fc1_bytes = w1 + (rows + T * (Ish > 0)) * H * 2 + rows * I * 2 + T * Ish * 2
     fc2_bytes = w2 + rows * I * 2 + T * Ish * 2 + rows * H * 2 + (T * H * 2 if Ish else 0)
     return dict(fc1_flops=fc1_flops, fc2_flops=fc2_flops, fc1_bytes=fc1_bytes, fc2_bytes=fc2_bytes,
@@ -287,8 +288,12 @@ def bench_ours(args):
     stages = {
         "route": lambda: layer.route(x),
         "permute": lambda: layer.permute(x),
-        "fc1": lambda: moe.moe_grouped_fc1(layer.x_perm, layer.offsets, layer.W1, xs, layer.W1s, h, h_sh, layer.ws),
-        "fc2": lambda: moe.moe_grouped_fc2(h, layer.offsets, layer.W2, h_sh, layer.W2s, y, y_sh, layer.ws),
+        "fc1": (lambda: moe.moe_grouped_fc1_fp8(layer.x_perm, layer.offsets, layer.W1q, layer.s1, xs, layer.W1sq,
+                                                layer.s1s, h, h_sh, layer.ws)) if layer.fp8 else
+               (lambda: moe.moe_grouped_fc1(layer.x_perm, layer.offsets, layer.W1, xs, layer.W1s, h, h_sh, layer.ws)),
+        "fc2": (lambda: moe.moe_grouped_fc2_fp8(h, layer.offsets, layer.W2q, layer.s2, h_sh, layer.W2sq, layer.s2s,
+                                                y, y_sh, layer.ws)) if layer.fp8 else
+               (lambda: moe.moe_grouped_fc2(h, layer.offsets, layer.W2, h_sh, layer.W2s, y, y_sh, layer.ws)),
         "finalize": lambda: moe.moe_finalize(y, layer.pair_row, None if layer.on_input else layer.topk_w, y_sh, xs,
                                              layer.gate, layer.out, layer.ws),
     }

@@ -256,6 +256,38 @@ MOE_API moe_status_t moe_forward(const moe_bf16_t *x_perm, const int32_t *offset
                          int I_shared_total, const moe_bf16_t *shared_gate_w,
                          moe_bf16_t *out, void *ws, size_t ws_bytes, moe_stream_t stream);
 
+/* moe_forward_fp8 -- moe_forward with E4M3 expert weights ([TRT-10985] review
+ * of torch_moe.py: the MoE ops have FP8 and NVFP4 paths; the pages fix no
+ * format).  Each weight matrix is E4M3 bytes (OCP "fn" encoding) with one fp32
+ * scale per row, W[r][c] = scale[r] * e4m3(q[r][c]) -- see
+ * moe_quantize_fp8_rows.  The tensor cores still compute in bf16: the weights
+ * are widened to bf16 in shared memory (exactly: every E4M3 value is a bf16
+ * value), and each accumulator column is multiplied by its row's scale before
+ * SwiGLU (FC1) or the store (FC2).  Halves the weight bytes each step reads.
+ *
+ *   W1q [S_local, 2I, H] uint8, W1_scale [S_local, 2I] fp32
+ *   W2q [S_local, H, I] uint8,  W2_scale [S_local, H] fp32
+ *   W1sq [2*I_shared_total, H] uint8, W1s_scale [2*I_shared_total] fp32 (or NULL)
+ *   W2sq [H, I_shared_total] uint8,   W2s_scale [H] fp32 (or NULL)
+ * Everything else as moe_forward. */
+MOE_API moe_status_t moe_forward_fp8(const moe_bf16_t *x_perm, const int32_t *offsets, int S_local, int64_t P_cap,
+                             const uint8_t *W1q, const float *W1_scale, const uint8_t *W2q,
+                             const float *W2_scale, int H, int I, const int32_t *pair_row,
+                             const float *topk_w, int64_t T, int k, const moe_bf16_t *x,
+                             const uint8_t *W1sq, const float *W1s_scale, const uint8_t *W2sq,
+                             const float *W2s_scale, int I_shared_total, const moe_bf16_t *shared_gate_w,
+                             moe_bf16_t *out, void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Row-wise E4M3 quantisation of a bf16 matrix w [rows, K] (K a multiple of
+ * 64), for moe_forward_fp8: scale[r] = amax_c |w[r][c]| / 448 and
+ * q[r][c] = e4m3(w[r][c] / scale[r]), both divisions in IEEE binary32 and the
+ * conversion to nearest, ties to even (the row's largest |w| becomes +-448
+ * exactly); an all-zero row gets scale 0 and q = 0.  Expert weights laid out
+ * as [S, R, K] are quantised as one [S*R, K] matrix.  Asynchronous on `stream`;
+ * allocates nothing. */
+MOE_API moe_status_t moe_quantize_fp8_rows(const moe_bf16_t *w, int64_t rows, int K, uint8_t *q, float *scale,
+                                   moe_stream_t stream);
+
 /* ---- the three stages of moe_forward ------------------------------------ */
 
 /* FC1 + SwiGLU on the tcgen05 tensor cores.  Routed problem: for each of the G
@@ -277,6 +309,19 @@ MOE_API moe_status_t moe_grouped_fc2(const moe_bf16_t *h, int64_t rows_cap, cons
                              const moe_bf16_t *h_shared, int64_t T, const moe_bf16_t *W2s,
                              int I_shared_total, moe_bf16_t *y, moe_bf16_t *y_shared,
                              void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/* moe_grouped_fc1 / moe_grouped_fc2 with E4M3 weights and fp32 row scales
+ * (the stages of moe_forward_fp8; layouts as there). */
+MOE_API moe_status_t moe_grouped_fc1_fp8(const moe_bf16_t *a, int64_t rows_cap, const int32_t *offsets, int G,
+                                 const uint8_t *W1q, const float *W1_scale, int H, int I,
+                                 const moe_bf16_t *a_shared, int64_t T, const uint8_t *W1sq,
+                                 const float *W1s_scale, int I_shared_total, moe_bf16_t *h,
+                                 moe_bf16_t *h_shared, void *ws, size_t ws_bytes, moe_stream_t stream);
+MOE_API moe_status_t moe_grouped_fc2_fp8(const moe_bf16_t *h, int64_t rows_cap, const int32_t *offsets, int G,
+                                 const uint8_t *W2q, const float *W2_scale, int H, int I,
+                                 const moe_bf16_t *h_shared, int64_t T, const uint8_t *W2sq,
+                                 const float *W2s_scale, int I_shared_total, moe_bf16_t *y,
+                                 moe_bf16_t *y_shared, void *ws, size_t ws_bytes, moe_stream_t stream);
 
 /* Unpermute + weighted combine: out[t] = bf16(sum_j topk_w[t,j] * y[pair_row[t,j]]
  * + g_t * y_shared[t]), fp32 accumulation in fixed j order (topk_w NULL: weight

@@ -60,6 +60,7 @@ class MoEConfig:
     n_group: int = 1                 # group-limited top-k: expert groups (1: plain top-k)
     topk_group: int = 1              # groups kept per token
     on_input: bool = False           # routing weight applied to the expert input, outputs summed unweighted
+    fp8: bool = False                # E4M3 expert weights with one fp32 scale per row
     w_std: float = 0.02              # expert weight std
     gate_std: float = 0.02           # router weight std
     seed: int = 0
@@ -92,6 +93,10 @@ for _t in (1, 8, 32, 128):
     CONFIGS[f"dsv2_lite_like_decode_t{_t}"] = MoEConfig(
         f"dsv2_lite_like_decode_t{_t}", T=_t, H=2048, I=1408, E=64, k=6, renorm=False,
         n_shared=2, I_shared=2816)
+# E4M3 expert weights (one fp32 scale per row) on the decode and Qwen2-like shapes
+for _name in ["dsv2_lite_like_decode_t1", "dsv2_lite_like_decode_t8", "dsv2_lite_like_decode_t32",
+              "dsv2_lite_like_decode_t128", "qwen2_moe_like_prefill"]:
+    CONFIGS[_name + "_fp8"] = CONFIGS[_name].with_(name=_name + "_fp8", fp8=True)
 
 
 def _gen(device, seed: int, idx: int) -> torch.Generator:
@@ -221,6 +226,8 @@ def describe(cfg: MoEConfig) -> str:
         parts.append(f"grouped top-k {cfg.topk_group} of {cfg.n_group} groups")
     if cfg.on_input:
         parts.append("routing on input")
+    if cfg.fp8:
+        parts.append("E4M3 weights, row scales")
     return ", ".join(parts)
 
 

@@ -272,7 +272,8 @@ static moe_status_t gemm_call(bool fc1, const moe_bf16_t* a, int64_t rows_cap, c
                               const moe_bf16_t* W, int H, int I, const moe_bf16_t* a_sh, int64_t T,
                               const moe_bf16_t* Ws, int I_sh, moe_bf16_t* out, moe_bf16_t* out_sh, void* ws,
                               cudaStream_t s, float* out_sh_part = nullptr, int ksplit_sh = 1,
-                              int64_t max_group_rows = -1) {
+                              int64_t max_group_rows = -1, const float* b_scale = nullptr,
+                              const float* b_scale_sh = nullptr) {
     GemmLaunch L;
     L.swiglu = fc1;
     L.a = a;
@@ -298,6 +299,10 @@ static moe_status_t gemm_call(bool fc1, const moe_bf16_t* a, int64_t rows_cap, c
     L.pair_mode = g_pair_mode.load();
     // a token adds at most one row to a slot, so a group has at most T rows
     L.max_group_rows = max_group_rows >= 0 ? std::min<int64_t>(max_group_rows, rows_cap) : rows_cap;
+    // E4M3 weights come with their row scales (W and Ws then point to bytes)
+    L.b_fp8 = b_scale != nullptr;
+    L.b_scale = b_scale;
+    L.b_scale_sh = b_scale_sh;
     const char* why = nullptr;
     return cuda_status(launch_grouped_gemm(L, device_sms(), s, &why));
 }
@@ -360,6 +365,34 @@ static moe_status_t finalize_call(const moe_bf16_t* y, int64_t rows_cap, const i
     return cuda_status(launch_finalize(L, device_sms(), s));
 }
 
+moe_status_t moe_grouped_fc1_fp8(const moe_bf16_t* a, int64_t rows_cap, const int32_t* offsets, int G,
+                                 const uint8_t* W1q, const float* W1_scale, int H, int I, const moe_bf16_t* a_shared,
+                                 int64_t T, const uint8_t* W1sq, const float* W1s_scale, int I_shared_total,
+                                 moe_bf16_t* h, moe_bf16_t* h_shared, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    moe_status_t st = check_gemm_args(a, rows_cap, offsets, G, reinterpret_cast<const moe_bf16_t*>(W1q), H, I,
+                                      a_shared, T, reinterpret_cast<const moe_bf16_t*>(W1sq), I_shared_total, h,
+                                      h_shared, ws, ws_bytes);
+    if (st != MOE_OK) return st;
+    if (!W1_scale || (I_shared_total > 0 && T > 0 && !W1s_scale)) return MOE_ERR_INVALID_ARG;
+    return gemm_call(true, a, rows_cap, offsets, G, reinterpret_cast<const moe_bf16_t*>(W1q), H, I, a_shared, T,
+                     reinterpret_cast<const moe_bf16_t*>(W1sq), I_shared_total, h, h_shared, ws, (cudaStream_t)stream,
+                     nullptr, 1, -1, W1_scale, W1s_scale);
+}
+
+moe_status_t moe_grouped_fc2_fp8(const moe_bf16_t* h, int64_t rows_cap, const int32_t* offsets, int G,
+                                 const uint8_t* W2q, const float* W2_scale, int H, int I, const moe_bf16_t* h_shared,
+                                 int64_t T, const uint8_t* W2sq, const float* W2s_scale, int I_shared_total,
+                                 moe_bf16_t* y, moe_bf16_t* y_shared, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    moe_status_t st = check_gemm_args(h, rows_cap, offsets, G, reinterpret_cast<const moe_bf16_t*>(W2q), H, I,
+                                      h_shared, T, reinterpret_cast<const moe_bf16_t*>(W2sq), I_shared_total, y,
+                                      y_shared, ws, ws_bytes);
+    if (st != MOE_OK) return st;
+    if (!W2_scale || (I_shared_total > 0 && T > 0 && !W2s_scale)) return MOE_ERR_INVALID_ARG;
+    return gemm_call(false, h, rows_cap, offsets, G, reinterpret_cast<const moe_bf16_t*>(W2q), H, I, h_shared, T,
+                     reinterpret_cast<const moe_bf16_t*>(W2sq), I_shared_total, y, y_shared, ws, (cudaStream_t)stream,
+                     nullptr, 1, -1, W2_scale, W2s_scale);
+}
+
 moe_status_t moe_finalize(const moe_bf16_t* y, int64_t rows_cap, const int32_t* pair_row, const float* topk_w,
                           int64_t T, int k, int H, const moe_bf16_t* y_shared, const moe_bf16_t* x,
                           const moe_bf16_t* shared_gate_w, moe_bf16_t* out, void* ws, size_t ws_bytes,
@@ -374,11 +407,13 @@ moe_status_t moe_finalize(const moe_bf16_t* y, int64_t rows_cap, const int32_t* 
                          (cudaStream_t)stream);
 }
 
-moe_status_t moe_forward(const moe_bf16_t* x_perm, const int32_t* offsets, int S_local, int64_t P_cap,
-                         const moe_bf16_t* W1, const moe_bf16_t* W2, int H, int I, const int32_t* pair_row,
-                         const float* topk_w, int64_t T, int k, const moe_bf16_t* x, const moe_bf16_t* W1s,
-                         const moe_bf16_t* W2s, int I_shared_total, const moe_bf16_t* shared_gate_w, moe_bf16_t* out,
-                         void* ws, size_t ws_bytes, moe_stream_t stream) {
+// moe_forward with bf16 weights (s1 == nullptr) or E4M3 weights with row scales.
+static moe_status_t forward_impl(const moe_bf16_t* x_perm, const int32_t* offsets, int S_local, int64_t P_cap,
+                                 const void* W1, const float* s1, const void* W2, const float* s2, int H, int I,
+                                 const int32_t* pair_row, const float* topk_w, int64_t T, int k,
+                                 const moe_bf16_t* x, const void* W1s, const float* s1s, const void* W2s,
+                                 const float* s2s, int I_shared_total, const moe_bf16_t* shared_gate_w,
+                                 moe_bf16_t* out, void* ws, size_t ws_bytes, moe_stream_t stream) {
     if (T < 0 || k <= 0 || S_local <= 0 || P_cap < 0 || H <= 0 || I <= 0 || I_shared_total < 0)
         return MOE_ERR_INVALID_ARG;
     if (!dim_ok(H) || !dim_ok(I) || (I_shared_total > 0 && !dim_ok(I_shared_total)) || k > 32 || S_local > 1024 ||
@@ -388,6 +423,8 @@ moe_status_t moe_forward(const moe_bf16_t* x_perm, const int32_t* offsets, int S
     if (!x_perm || !offsets || !W1 || !W2 || !pair_row || !out) return MOE_ERR_INVALID_ARG;
     if (I_shared_total > 0 && (!x || !W1s || !W2s)) return MOE_ERR_INVALID_ARG;
     if (shared_gate_w && (I_shared_total == 0 || !x)) return MOE_ERR_INVALID_ARG;
+    const bool fp8 = s1 != nullptr;
+    if (fp8 && (!s2 || (I_shared_total > 0 && (!s1s || !s2s)))) return MOE_ERR_INVALID_ARG;
     const ForwardLayout FL = forward_layout(P_cap, T, H, I, I_shared_total);
     if (!ws || ws_bytes < FL.total) return MOE_ERR_WORKSPACE;
     char* base = static_cast<char*>(ws);
@@ -396,16 +433,47 @@ moe_status_t moe_forward(const moe_bf16_t* x_perm, const int32_t* offsets, int S
     moe_bf16_t* y = reinterpret_cast<moe_bf16_t*>(base + FL.y);
     moe_bf16_t* y_sh = I_shared_total > 0 ? reinterpret_cast<moe_bf16_t*>(base + FL.y_sh) : nullptr;
     cudaStream_t s = (cudaStream_t)stream;
-    moe_status_t st = gemm_call(true, x_perm, P_cap, offsets, S_local, W1, H, I, x, T, W1s, I_shared_total, h, h_sh,
-                                ws, s, nullptr, 1, T);
+    moe_status_t st = gemm_call(true, x_perm, P_cap, offsets, S_local, static_cast<const moe_bf16_t*>(W1), H, I, x,
+                                T, static_cast<const moe_bf16_t*>(W1s), I_shared_total, h, h_sh, ws, s, nullptr, 1, T,
+                                s1, s1s);
     if (st != MOE_OK) return st;
     const int ks = shared_split(T, I, I_shared_total);
     float* y_sh_part = ks > 1 ? reinterpret_cast<float*>(base + FL.y_sh_part) : nullptr;
-    st = gemm_call(false, h, P_cap, offsets, S_local, W2, H, I, h_sh, T, W2s, I_shared_total, y, y_sh, ws, s,
-                   y_sh_part, ks, T);
+    st = gemm_call(false, h, P_cap, offsets, S_local, static_cast<const moe_bf16_t*>(W2), H, I, h_sh, T,
+                   static_cast<const moe_bf16_t*>(W2s), I_shared_total, y, y_sh, ws, s, y_sh_part, ks, T, s2, s2s);
     if (st != MOE_OK) return st;
     return finalize_call(y, P_cap, pair_row, topk_w, T, k, H, y_sh_part ? nullptr : y_sh, y_sh_part, ks, x,
                          shared_gate_w, out, ws, s);
+}
+
+moe_status_t moe_forward(const moe_bf16_t* x_perm, const int32_t* offsets, int S_local, int64_t P_cap,
+                         const moe_bf16_t* W1, const moe_bf16_t* W2, int H, int I, const int32_t* pair_row,
+                         const float* topk_w, int64_t T, int k, const moe_bf16_t* x, const moe_bf16_t* W1s,
+                         const moe_bf16_t* W2s, int I_shared_total, const moe_bf16_t* shared_gate_w, moe_bf16_t* out,
+                         void* ws, size_t ws_bytes, moe_stream_t stream) {
+    return forward_impl(x_perm, offsets, S_local, P_cap, W1, nullptr, W2, nullptr, H, I, pair_row, topk_w, T, k, x,
+                        W1s, nullptr, W2s, nullptr, I_shared_total, shared_gate_w, out, ws, ws_bytes, stream);
+}
+
+moe_status_t moe_forward_fp8(const moe_bf16_t* x_perm, const int32_t* offsets, int S_local, int64_t P_cap,
+                             const uint8_t* W1q, const float* W1_scale, const uint8_t* W2q, const float* W2_scale,
+                             int H, int I, const int32_t* pair_row, const float* topk_w, int64_t T, int k,
+                             const moe_bf16_t* x, const uint8_t* W1sq, const float* W1s_scale, const uint8_t* W2sq,
+                             const float* W2s_scale, int I_shared_total, const moe_bf16_t* shared_gate_w,
+                             moe_bf16_t* out, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    if (!W1_scale || !W2_scale) return MOE_ERR_INVALID_ARG;
+    return forward_impl(x_perm, offsets, S_local, P_cap, W1q, W1_scale, W2q, W2_scale, H, I, pair_row, topk_w, T, k,
+                        x, W1sq, W1s_scale, W2sq, W2s_scale, I_shared_total, shared_gate_w, out, ws, ws_bytes,
+                        stream);
+}
+
+moe_status_t moe_quantize_fp8_rows(const moe_bf16_t* w, int64_t rows, int K, uint8_t* q, float* scale,
+                                   moe_stream_t stream) {
+    if (rows < 0 || K <= 0) return MOE_ERR_INVALID_ARG;
+    if (K % 64 != 0) return MOE_ERR_UNSUPPORTED;
+    if (rows == 0) return MOE_OK;
+    if (!w || !q || !scale) return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_quantize_fp8_rows(w, rows, K, q, scale, device_sms(), (cudaStream_t)stream));
 }
 
 moe_status_t moe_debug_wait_timeout(void* ws, size_t ws_bytes, uint64_t timeout_ns, moe_stream_t stream) {

@@ -57,6 +57,9 @@ constexpr int A_BYTES = BM * BK * 2;
 constexpr int BM_SHORT = 32;                      // A rows loaded for tiles with at most 32 rows
 constexpr int A_SHORT_BYTES = BM_SHORT * BK * 2;
 constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS_FP8 = 448;  // plus warps 6..13: E4M3 -> bf16 converters
+constexpr int CONV_THREADS = 256;
+constexpr int CONV_BARRIER = 1;       // named barrier of the converter warps
 constexpr int MAX_GROUPS = 1024;
 constexpr int MAX_STAGES = 8;
 constexpr int RING_BYTES = 216 * 1024;  // shared memory for the operand ring
@@ -87,6 +90,9 @@ struct GemmParams {
     int64_t T_sh;            // rows of the shared problem (0: none)
     uint16_t* out;
     uint16_t* out_sh;
+    const float* scale;      // E4M3 weights: fp32 scale per B row, [G][Nb] (null: bf16 weights)
+    const float* scale_sh;   // [Nb_sh]
+    int Nb;                  // B rows per group
     float* out_sh_part;      // FC2, split shared problem: fp32 partials [ksplit_sh, T_sh, N_out_sh]
     int ksplit_sh;           // K ranges of the shared problem (1: not split)
     int kb_split_sh;         // K steps per range
@@ -97,11 +103,13 @@ struct GemmParams {
 struct SmemMeta {
     uint64_t full[MAX_STAGES];
     uint64_t empty[MAX_STAGES];
+    uint64_t conv[MAX_STAGES];  // E4M3 weights: stage converted to bf16 (8 converter warps)
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
+    volatile int conv_ok;
     int routed_tiles;
     int off[MAX_GROUPS + 1];
     int ts[MAX_GROUPS + 1];
@@ -172,8 +180,42 @@ __device__ __forceinline__ Tile tile_of(int u, const GemmParams& p, const SmemMe
     return tl;
 }
 
-template <bool kFC1, bool kPair, int BN, bool kShort>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+// Four E4M3 weights (one 32-bit word) -> four bf16 values (two words), exactly,
+// with integer operations on two 16-bit halves at a time.  A normal E4M3 value
+// (exponent field e >= 1) keeps its mantissa and gets the exponent
+// e - 7 + 127: bf16 = (mag << 4) + (120 << 7), sign moved from bit 7 to bit 15.
+// Zeros and subnormals (e = 0: m * 2^-9) are rare; a word holding one takes a
+// slow path that places the byte's fields in binary32 positions and scales by
+// 2^120 (exact, including binary32 subnormal inputs), keeping the top 16 bits.
+__device__ __forceinline__ uint32_t e4m3_small_to_bf16(uint32_t mag) {
+    return __float_as_uint(__uint_as_float(mag << 20) * 0x1p120f) >> 16;
+}
+
+__device__ __forceinline__ uint32_t e4m3x2_normal_to_bf16x2(uint32_t v) {  // bytes at bits 0-7 and 16-23
+    return ((v & 0x007F007Fu) * 16u + 0x3C003C00u) | ((v << 8) & 0x80008000u);
+}
+
+__device__ __forceinline__ uint32_t e4m3x2_any_to_bf16x2(uint32_t v) {
+    const uint32_t lo = v & 0x7Fu, hi = (v >> 16) & 0x7Fu;
+    const uint32_t blo = (lo & 0x78u) ? lo * 16u + 0x3C00u : e4m3_small_to_bf16(lo);
+    const uint32_t bhi = (hi & 0x78u) ? hi * 16u + 0x3C00u : e4m3_small_to_bf16(hi);
+    return (blo | (bhi << 16)) | ((v << 8) & 0x80008000u);
+}
+
+__device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t x, uint32_t& o0, uint32_t& o1) {
+    const uint32_t a = __byte_perm(x, 0u, 0x4140), b = __byte_perm(x, 0u, 0x4342);  // bytes 0,1 and 2,3
+    const uint32_t t = x & 0x78787878u;                                               // exponent fields
+    if (((t - 0x08080808u) & ~t & 0x80808080u) == 0u) {  // no zero exponent field among the four
+        o0 = e4m3x2_normal_to_bf16x2(a);
+        o1 = e4m3x2_normal_to_bf16x2(b);
+    } else {
+        o0 = e4m3x2_any_to_bf16x2(a);
+        o1 = e4m3x2_any_to_bf16x2(b);
+    }
+}
+
+template <bool kFC1, bool kPair, int BN, bool kShort, bool kFp8>
+__global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmAs,
                         const __grid_constant__ CUtensorMap tmBs, const __grid_constant__ CUtensorMap tmA32,
@@ -185,6 +227,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     constexpr uint32_t IDESC = C::IDESC;
     constexpr int TMEM_COLS = C::TMEM_COLS;
     static_assert(!kShort || !kPair, "short tiles run in single mode");
+    static_assert(!kFp8 || (!kPair && BN == 256), "E4M3 weights run in single mode with N = 256");
     static_assert(!kPair || BN == 256, "pair mode uses N = 256");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -204,6 +247,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&m.full[s], 1);   // pair mode: only the leader's, fed by both CTAs' copies
             mbar_init(&m.empty[s], 1);  // released by the (leader's) MMA commit
+            if (kFp8) mbar_init(&m.conv[s], CONV_THREADS / 32);  // one arrival per converter warp
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&m.tfull[b], 1);
@@ -314,6 +358,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const int brow = kFC1 ? (crank ? up : 0) + tl.nt * (BN / 2) : tl.nt * BN + crank * (BN / 2);
                         tma_load_2d_pair(a_dst, mA, lead_full, kb * BK, tl.row0);
                         tma_load_3d_pair(b_dst, mB, lead_full, kb * BK, brow, tl.g);
+                    } else if (kFp8) {
+                        // E4M3 rows of 64 bytes, dense, in the first half of the B slot (FC1:
+                        // the gate rows, then the up rows); the converters widen them in place
+                        mbar_arrive_expect_tx(&m.full[stage], a_bytes + BN * BK);
+                        tma_load_2d(a_dst, mA, &m.full[stage], kb * BK, tl.row0);
+                        if (kFC1) {
+                            tma_load_3d(b_dst, mB, &m.full[stage], kb * BK, tl.nt * (BN / 2), tl.g);
+                            tma_load_3d(b_dst + (BN / 2) * BK, mB, &m.full[stage], kb * BK, up + tl.nt * (BN / 2), tl.g);
+                        } else {
+                            tma_load_3d(b_dst, mB, &m.full[stage], kb * BK, tl.nt * BN, tl.g);
+                        }
                     } else if (kFC1) {
                         mbar_arrive_expect_tx(&m.full[stage], a_bytes + B_BYTES);
                         tma_load_2d(a_dst, mA, &m.full[stage], kb * BK, tl.row0);
@@ -367,7 +422,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(buf * BN);
                 for (int kb = 0; kb < nkb; ++kb) {
-                    if (!mbar_wait(&m.full[stage], phase, p.timeout_ns, abortp)) {
+                    if (!mbar_wait(kFp8 ? &m.conv[stage] : &m.full[stage], phase, p.timeout_ns, abortp)) {
                         failed = true;
                         break;
                     }
@@ -409,7 +464,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tc_commit(&m.drain);
             (void)mbar_wait(&m.drain, 0, p.timeout_ns, nullptr);
         }
-    } else {
+    } else if (warp >= 2 && warp <= 5) {
         // ---------------- epilogue (warps 2..5) ----------------
         const int q = warp & 3;              // TMEM lane quarter of this warp
         const int row_in = q * 32 + lane;    // tile row of this thread
@@ -436,6 +491,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int N_out = tl.prob ? p.N_out_sh : p.N_out;
             uint16_t* out = tl.prob ? p.out_sh : p.out;
             uint16_t* orow = out + (int64_t)(tl.row0 + row_in) * N_out;
+            // E4M3 weights: the accumulator of output column n carries B row n's scale
+            const float* srow = kFp8 ? (tl.prob ? p.scale_sh : p.scale + (int64_t)tl.g * p.Nb) : nullptr;
+            const int sup = tl.prob ? p.up_off_sh : p.up_off;
+            auto bscale = [&](int row) -> float { return kFp8 ? __ldg(srow + row) : 1.0f; };
             if (kFC1) {
 #pragma unroll 1
                 for (int c = 0; c < OW; c += 32) {
@@ -451,8 +510,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             float h2[2];
 #pragma unroll
                             for (int z = 0; z < 2; ++z) {
-                                const float gv = __uint_as_float(g[2 * e + z]);
-                                const float uv = __uint_as_float(v[2 * e + z]);
+                                const float gv = __uint_as_float(g[2 * e + z]) * bscale(col + 2 * e + z);
+                                const float uv = __uint_as_float(v[2 * e + z]) * bscale(sup + col + 2 * e + z);
                                 // silu(g) * u; the product is rounded to bf16 (8 bits),
                                 // far coarser than the approximate exp / divide
                                 h2[z] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
@@ -479,8 +538,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         float4* dst = reinterpret_cast<float4*>(prow + col);
 #pragma unroll
                         for (int e = 0; e < 8; ++e)
-                            dst[e] = make_float4(__uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1]),
-                                                 __uint_as_float(r[4 * e + 2]), __uint_as_float(r[4 * e + 3]));
+                            dst[e] = make_float4(__uint_as_float(r[4 * e]) * bscale(col + 4 * e),
+                                                 __uint_as_float(r[4 * e + 1]) * bscale(col + 4 * e + 1),
+                                                 __uint_as_float(r[4 * e + 2]) * bscale(col + 4 * e + 2),
+                                                 __uint_as_float(r[4 * e + 3]) * bscale(col + 4 * e + 3));
                     }
                 }
             } else {
@@ -494,7 +555,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         uint32_t pk[16];
 #pragma unroll
                         for (int e = 0; e < 16; ++e)
-                            pk[e] = pack_bf16x2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
+                            pk[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * bscale(col + 2 * e),
+                                                __uint_as_float(r[2 * e + 1]) * bscale(col + 2 * e + 1));
                         uint4* dst = reinterpret_cast<uint4*>(orow + col);
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
@@ -510,6 +572,63 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 else
                     mbar_arrive(&m.tempty[buf]);
             }
+        }
+    } else if (kFp8 && warp >= 6) {
+        // ---------------- E4M3 -> bf16 converters (warps 6..13) ----------------
+        // Per K step the B slot holds BN rows of 64 E4M3 bytes (dense); the 256
+        // threads read all of it, meet at a named barrier, then write the rows back
+        // as bf16 in the 128-byte-swizzled layout the MMA reads (16-byte chunk j of
+        // row r at r * 128 + ((j ^ (r & 7)) << 4)), which covers the whole slot.
+        const int ct = threadIdx.x - 6 * 32;  // 0 .. CONV_THREADS - 1
+        constexpr int CPT = (BN * 4 + CONV_THREADS - 1) / CONV_THREADS;  // 16-byte E4M3 chunks per thread
+        uint32_t stage = 0, phase = 0;
+        bool failed = false;
+        for (int u = unit0; u < total_tiles && !failed; u += nunits) {
+            const Tile tl = tile_of<kFC1, kPair>(u, p, m, n_sh_tiles, mu_sh, crank);
+            const int nkb = tl.kb1 - tl.kb0;
+            for (int kb = 0; kb < nkb; ++kb) {
+                // one thread waits for the stage; the named barrier passes its verdict
+                // (and, with it, the visibility of the landed bytes) to all of them, so
+                // the warps always take the same branch and every barrier completes
+                if (ct == 0) m.conv_ok = mbar_wait(&m.full[stage], phase, p.timeout_ns, abortp) ? 1 : 0;
+                asm volatile("bar.sync %0, %1;" ::"n"(CONV_BARRIER), "n"(CONV_THREADS) : "memory");
+                if (!m.conv_ok) {
+                    failed = true;
+                    break;
+                }
+                uint8_t* b_slot = smB + (size_t)stage * B_BYTES;
+                // 16-byte chunk i of the slot's E4M3 rows (row i / 4, bytes 16 (i % 4) ..):
+                // consecutive lanes read consecutive chunks (no bank conflicts)
+                uint4 src[CPT];
+#pragma unroll
+                for (int j = 0; j < CPT; ++j)
+                    src[j] = *reinterpret_cast<const uint4*>(b_slot + (size_t)(ct + j * CONV_THREADS) * 16);
+                asm volatile("bar.sync %0, %1;" ::"n"(CONV_BARRIER), "n"(CONV_THREADS) : "memory");
+#pragma unroll
+                for (int j = 0; j < CPT; ++j) {
+                    const int i = ct + j * CONV_THREADS;
+                    const int r = i >> 2, c = i & 3;
+                    uint8_t* drow = b_slot + (size_t)r * 128;
+                    const uint32_t w4[4] = {src[j].x, src[j].y, src[j].z, src[j].w};
+                    uint32_t o[8];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) e4m3x4_to_bf16x4(w4[e], o[2 * e], o[2 * e + 1]);
+                    *reinterpret_cast<uint4*>(drow + (((2 * c) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+                    *reinterpret_cast<uint4*>(drow + (((2 * c + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+                }
+                // generic-proxy stores -> visible to the tensor core's reads
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&m.conv[stage]);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        if (failed && lane == 0) {
+            m.abort = 1;
+            report(p.status, MOE_ERR_TIMEOUT);
         }
     }
 
@@ -571,6 +690,21 @@ bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t oute
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// E4M3 weights [groups, rows, inner] bytes: boxes of 64 bytes x box_rows rows, no
+// swizzle (dense rows; the converter warps lay them out for the MMA)
+bool encode_3d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t groups,
+                  uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {inner, rows, groups};
+    cuuint64_t strides[2] = {inner, rows * inner};
+    cuuint32_t box[3] = {(cuuint32_t)BK, box_rows, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t groups,
                uint32_t box_rows) {
     auto fn = encode_fn();
@@ -591,7 +725,7 @@ struct KernelInfo {
     int max_clusters = 0;
 };
 
-template <bool kFC1, bool kPair, int BN, bool kShort>
+template <bool kFC1, bool kPair, int BN, bool kShort, bool kFp8>
 cudaError_t kernel_info(int num_sms, KernelInfo* out) {
     static std::mutex mu;
     static KernelInfo info[64];
@@ -601,14 +735,14 @@ cudaError_t kernel_info(int num_sms, KernelInfo* out) {
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(mu);
     if (!info[dev].ready) {
-        err = cudaFuncSetAttribute(grouped_gemm_kernel<kFC1, kPair, BN, kShort>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        err = cudaFuncSetAttribute(grouped_gemm_kernel<kFC1, kPair, BN, kShort, kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    (int)smem_bytes<kPair, BN, kShort>());
         if (err != cudaSuccess) return err;
         int clusters = 0;
         if (kPair) {
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(2 * num_sms);
-            cfg.blockDim = dim3(NUM_THREADS);
+            cfg.blockDim = dim3(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS);
             cfg.dynamicSmemBytes = smem_bytes<kPair, BN, kShort>();
             cudaLaunchAttribute attr;
             attr.id = cudaLaunchAttributeClusterDimension;
@@ -617,7 +751,7 @@ cudaError_t kernel_info(int num_sms, KernelInfo* out) {
             attr.val.clusterDim.z = 1;
             cfg.attrs = &attr;
             cfg.numAttrs = 1;
-            err = cudaOccupancyMaxActiveClusters(&clusters, grouped_gemm_kernel<kFC1, kPair, BN, kShort>, &cfg);
+            err = cudaOccupancyMaxActiveClusters(&clusters, grouped_gemm_kernel<kFC1, kPair, BN, kShort, kFp8>, &cfg);
             if (err != cudaSuccess) return err;
         }
         info[dev].max_clusters = clusters;
@@ -627,13 +761,13 @@ cudaError_t kernel_info(int num_sms, KernelInfo* out) {
     return cudaSuccess;
 }
 
-template <bool kFC1, bool kPair, int BN, bool kShort>
+template <bool kFC1, bool kPair, int BN, bool kShort, bool kFp8>
 cudaError_t launch_kernel(const GemmParams& p, const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mAs,
                           const CUtensorMap& mBs, const CUtensorMap& mA32, const CUtensorMap& mAs32, unsigned grid,
                           cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.blockDim = dim3(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS);
     cfg.dynamicSmemBytes = smem_bytes<kPair, BN, kShort>();
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
@@ -653,11 +787,11 @@ cudaError_t launch_kernel(const GemmParams& p, const CUtensorMap& mA, const CUte
     cfg.attrs = attr;
     cfg.numAttrs = n;
     count_launch();
-    return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<kFC1, kPair, BN, kShort>, p, mA, mB, mAs, mBs, mA32, mAs32);
+    return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<kFC1, kPair, BN, kShort, kFp8>, p, mA, mB, mAs, mBs, mA32, mAs32);
 }
 
 // Tensor maps, parameters and grid of one launch with MMA N = BN.
-template <bool kFC1, bool kPair, int BN, bool kShort>
+template <bool kFC1, bool kPair, int BN, bool kShort, bool kFp8>
 cudaError_t launch_bn(const GemmLaunch& L, int num_sms, int64_t bound, cudaStream_t s, const char** why) {
     const bool has_routed = L.G > 0 && L.rows_cap > 0;
     const bool has_shared = L.T_sh > 0 && L.b_sh != nullptr && L.N_out_sh > 0;
@@ -668,12 +802,14 @@ cudaError_t launch_bn(const GemmLaunch& L, int num_sms, int64_t bound, cudaStrea
     if (has_routed) {
         ok = ok && encode_2d(&mA, L.a, (uint64_t)L.K, (uint64_t)L.rows_cap, BM);
         ok = ok && encode_2d(&mA32, L.a, (uint64_t)L.K, (uint64_t)L.rows_cap, BM_SHORT);
-        ok = ok && encode_3d(&mB, L.b, (uint64_t)L.K, (uint64_t)L.Nb, (uint64_t)L.G, brows);
+        ok = ok && (kFp8 ? encode_3d_u8(&mB, L.b, (uint64_t)L.K, (uint64_t)L.Nb, (uint64_t)L.G, brows)
+                         : encode_3d(&mB, L.b, (uint64_t)L.K, (uint64_t)L.Nb, (uint64_t)L.G, brows));
     }
     if (has_shared) {
         ok = ok && encode_2d(&mAs, L.a_sh, (uint64_t)L.K_sh, (uint64_t)L.T_sh, BM);
         ok = ok && encode_2d(&mAs32, L.a_sh, (uint64_t)L.K_sh, (uint64_t)L.T_sh, BM_SHORT);
-        ok = ok && encode_3d(&mBs, L.b_sh, (uint64_t)L.K_sh, (uint64_t)L.Nb_sh, 1, brows);
+        ok = ok && (kFp8 ? encode_3d_u8(&mBs, L.b_sh, (uint64_t)L.K_sh, (uint64_t)L.Nb_sh, 1, brows)
+                         : encode_3d(&mBs, L.b_sh, (uint64_t)L.K_sh, (uint64_t)L.Nb_sh, 1, brows));
     }
     if (!ok) {
         *why = "cuTensorMapEncodeTiled failed";
@@ -700,6 +836,9 @@ cudaError_t launch_bn(const GemmLaunch& L, int num_sms, int64_t bound, cudaStrea
     p.up_off_sh = kFC1 ? L.Nb_sh / 2 : 0;
     p.rows_cap = L.rows_cap;
     p.T_sh = has_shared ? L.T_sh : 0;
+    p.scale = L.b_scale;
+    p.scale_sh = L.b_scale_sh;
+    p.Nb = L.Nb;
     p.out_sh_part = L.out_sh_part;
     p.ksplit_sh = (has_shared && !L.swiglu && L.out_sh_part && L.ksplit_sh > 1) ? L.ksplit_sh : 1;
     p.kb_split_sh = (L.K_sh / BK + p.ksplit_sh - 1) / p.ksplit_sh;
@@ -709,7 +848,7 @@ cudaError_t launch_bn(const GemmLaunch& L, int num_sms, int64_t bound, cudaStrea
     p.timeout_ns = L.timeout_ns;
 
     KernelInfo info;
-    cudaError_t err = kernel_info<kFC1, kPair, BN, kShort>(num_sms, &info);
+    cudaError_t err = kernel_info<kFC1, kPair, BN, kShort, kFp8>(num_sms, &info);
     if (err != cudaSuccess) {
         *why = "kernel attribute / occupancy query failed";
         return err;
@@ -722,7 +861,7 @@ cudaError_t launch_bn(const GemmLaunch& L, int num_sms, int64_t bound, cudaStrea
     } else {
         grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(bound, num_sms));
     }
-    err = launch_kernel<kFC1, kPair, BN, kShort>(p, mA, mB, mAs, mBs, mA32, mAs32, grid, s);
+    err = launch_kernel<kFC1, kPair, BN, kShort, kFp8>(p, mA, mB, mAs, mBs, mA32, mAs32, grid, s);
     if (err != cudaSuccess) *why = "launch failed";
     return err;
 }
@@ -748,21 +887,27 @@ int64_t tile_bound(const GemmLaunch& L, int bn) {
 template <bool kFC1>
 cudaError_t dispatch(const GemmLaunch& L, int num_sms, cudaStream_t s, const char** why) {
     const int64_t b256 = tile_bound(L, 256);
+    if (L.b_fp8) {
+        // E4M3 weights: N = 256, single CTAs; 32-row A slots when every tile is short
+        if (L.max_group_rows <= BM_SHORT && L.T_sh <= BM_SHORT)
+            return launch_bn<kFC1, false, 256, true, true>(L, num_sms, b256, s, why);
+        return launch_bn<kFC1, false, 256, false, true>(L, num_sms, b256, s, why);
+    }
     const bool pair = split_of(L) == 1 &&
                       (L.pair_mode == 2 ? b256 >= 2 : (L.pair_mode == 1 && b256 >= 4 * (int64_t)num_sms));
-    if (pair) return launch_bn<kFC1, true, 256, false>(L, num_sms, b256, s, why);
+    if (pair) return launch_bn<kFC1, true, 256, false, false>(L, num_sms, b256, s, why);
     // every tile at most 32 rows: 32-row A slots, so more stages fit the ring
     if (L.max_group_rows <= BM_SHORT && L.T_sh <= BM_SHORT)
-        return launch_bn<kFC1, false, 256, true>(L, num_sms, b256, s, why);
+        return launch_bn<kFC1, false, 256, true, false>(L, num_sms, b256, s, why);
     // Small batches (at most 1024 routed rows) stream weights: N = 256 moves the
     // most bytes per pipeline stage, and a stage costs about the same time
     // whatever its size, so the widest tile wins even with SMs left idle.
     // Otherwise the widest N that still gives every SM two tiles.
     if (L.rows_cap <= 1024 || b256 >= 2 * (int64_t)num_sms)
-        return launch_bn<kFC1, false, 256, false>(L, num_sms, b256, s, why);
+        return launch_bn<kFC1, false, 256, false, false>(L, num_sms, b256, s, why);
     const int64_t b128 = tile_bound(L, 128);
-    if (b128 >= 2 * (int64_t)num_sms) return launch_bn<kFC1, false, 128, false>(L, num_sms, b128, s, why);
-    return launch_bn<kFC1, false, 64, false>(L, num_sms, tile_bound(L, 64), s, why);
+    if (b128 >= 2 * (int64_t)num_sms) return launch_bn<kFC1, false, 128, false, false>(L, num_sms, b128, s, why);
+    return launch_bn<kFC1, false, 64, false, false>(L, num_sms, tile_bound(L, 64), s, why);
 }
 
 }  // namespace

@@ -393,6 +393,9 @@ struct GemmLaunch {
     uint64_t timeout_ns;
     int pair_mode;             // 0 single CTAs only, 1 pairs for large launches, 2 pairs whenever possible
     int64_t max_group_rows;    // upper bound on the rows of any routed group (tokens of the batch)
+    bool b_fp8;                // B (weights) are E4M3 bytes with one fp32 scale per row
+    const float* b_scale;      // [G][Nb] row scales of b (E4M3 only)
+    const float* b_scale_sh;   // [Nb_sh] row scales of b_sh (E4M3 only)
 };
 cudaError_t launch_grouped_gemm(const GemmLaunch& L, int num_sms, cudaStream_t s, const char** why);
 
@@ -414,6 +417,10 @@ struct FinalizeLaunch {
 cudaError_t launch_finalize(const FinalizeLaunch& L, int num_sms, cudaStream_t s);
 
 cudaError_t launch_wait_timeout_probe(WsHeader* hdr, uint64_t timeout_ns, cudaStream_t s);
+
+// Row-wise E4M3 quantisation of a bf16 matrix [rows, K] (moe_quantize_fp8_rows).
+cudaError_t launch_quantize_fp8_rows(const uint16_t* w, int64_t rows, int K, uint8_t* q, float* scale, int num_sms,
+                                     cudaStream_t s);
 
 // Whether kernels are launched with programmatic stream serialization (set by
 // moe_set_pdl; defined in moe_api.cu).

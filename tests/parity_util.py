@@ -93,9 +93,26 @@ def oracle_layer(inp_cpu: dict, local_start=0, local_count=-1, mode=0, tokens=No
     if local_count >= 0:
         W1 = W1[local_start:local_start + local_count]
         W2 = W2[local_start:local_start + local_count]
+    W1s, W2s = inp_cpu["W1s"], inp_cpu["W2s"]
+    fp8 = None
+    if cfg.fp8:
+        # the GPU runs the shared experts as one MLP (rows / columns concatenated), and row
+        # scales depend on that layout: the oracle gets the same single MLP
+        if W1s is not None:
+            from moe_inputs import shared_concat
+            c1, c2 = shared_concat(W1s, W2s)
+            W1s, W2s = c1[None], c2[None]
+        q1, s1 = oracle.quantize_fp8_rows(W1)
+        q2, s2 = oracle.quantize_fp8_rows(W2)
+        fp8 = dict(W1q=q1, s1=s1, W2q=q2, s2=s2)
+        if W1s is not None:
+            q1s, s1s = oracle.quantize_fp8_rows(W1s)
+            q2s, s2s = oracle.quantize_fp8_rows(W2s)
+            fp8.update(W1sq=q1s, s1s=s1s, W2sq=q2s, s2s=s2s)
     kw = dict(rep_offset=inp_cpu["rep_offset"], rep_slots=inp_cpu["rep_slots"], local_start=local_start,
-              local_count=local_count, mode=mode, W1s=inp_cpu["W1s"], W2s=inp_cpu["W2s"],
-              shared_gate_w=inp_cpu["w_s"], n_group=cfg.n_group, topk_group=cfg.topk_group, on_input=on_input)
+              local_count=local_count, mode=mode, W1s=W1s, W2s=W2s,
+              shared_gate_w=inp_cpu["w_s"], n_group=cfg.n_group, topk_group=cfg.topk_group, on_input=on_input,
+              fp8=fp8)
     if tokens is None:
         return oracle.moe_layer(inp_cpu["x"], inp_cpu["Wg"], inp_cpu["bias"], cfg.k, cfg.renorm, W1, W2,
                                 S=cfg.slots, **kw)

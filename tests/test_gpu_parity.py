@@ -332,6 +332,74 @@ def test_routing_on_input_local_ranges_skip_mod_and_sum():
     assert np.abs(a - b).max() <= 2.0 ** -7 * np.abs(b).max() + 1e-3
 
 
+# --------------------------------------------------------------------------- E4M3 expert weights
+
+def test_quantize_fp8_rows_bit_exact():
+    g = torch.Generator().manual_seed(11)
+    w = (torch.randn(300, 192, generator=g) * 0.02).to(torch.bfloat16)
+    w[7] = 0.0
+    w[9, 5] = 3.0  # a row with one large value: most others become subnormal E4M3
+    q_ref, s_ref = oracle.quantize_fp8_rows(w)
+    q = torch.empty((300, 192), dtype=torch.uint8, device="cuda")
+    sc = torch.empty(300, dtype=torch.float32, device="cuda")
+    moe.moe_quantize_fp8_rows(w.cuda(), q, sc)
+    torch.cuda.synchronize()
+    assert np.array_equal(q.cpu().numpy(), q_ref)
+    assert np.array_equal(sc.cpu().numpy().view(np.uint32), s_ref.view(np.uint32))
+
+
+FP8_MID = MID.with_(name="mid_fp8", fp8=True)
+
+
+def test_fp8_weights_mid_layer():
+    _full_check(mi.make_inputs(FP8_MID))
+
+
+def test_fp8_weights_with_subnormal_and_zero_values():
+    """One large entry per row of slot 0's W1 pushes that row's other values into the
+    E4M3 subnormal range (and some to zero): the widening to bf16 must stay exact."""
+    inp = mi.make_inputs(FP8_MID)
+    W1 = inp["W1"].clone()
+    W1[0, :, 0] = 1000.0
+    W1[1, :5] = 0.0  # all-zero rows: scale 0
+    inp["W1"] = W1
+    q, _ = oracle.quantize_fp8_rows(W1[0])
+    assert ((q & 0x78) == 0).mean() > 0.3  # many subnormal or zero codes
+    _full_check(inp)
+
+
+def test_fp8_weights_partial_tiles_two_shared_and_short_batch():
+    cfg = mi.MoEConfig("odd_fp8", T=200, H=320, I=320, E=5, k=2, renorm=False, n_shared=2, I_shared=192, fp8=True)
+    _full_check(mi.make_inputs(cfg))
+    # at most 32 tokens: the short-tile variant, and the split shared FC2
+    cfg = mi.MoEConfig("short_fp8", T=24, H=256, I=128, E=9, k=3, renorm=True, n_shared=2, I_shared=256,
+                       shared_gate=True, fp8=True)
+    _full_check(mi.make_inputs(cfg))
+
+
+def test_fp8_stage_gemms_against_oracle_rows():
+    inp = mi.make_inputs(FP8_MID)
+    g = run_gpu(inp)
+    layer = g["layer"]
+    cfg = FP8_MID
+    dev = torch.device("cuda")
+    P = cfg.T * cfg.k
+    h = torch.empty((P, cfg.I), dtype=torch.bfloat16, device=dev)
+    y = torch.empty((P, cfg.H), dtype=torch.bfloat16, device=dev)
+    moe.moe_grouped_fc1_fp8(layer.x_perm, layer.offsets, layer.W1q, layer.s1, None, None, None, h, None, layer.ws)
+    moe.moe_grouped_fc2_fp8(h, layer.offsets, layer.W2q, layer.s2, None, None, None, y, None, layer.ws)
+    torch.cuda.synchronize()
+    q1, s1 = oracle.quantize_fp8_rows(inp["W1"])
+    q2, s2 = oracle.quantize_fp8_rows(inp["W2"])
+    perm = g["perm_src"].numpy()
+    slots = g["slot_ids"].numpy().reshape(-1)
+    for r in sample_tokens(g["rows"], 16, seed=3):
+        p = int(perm[r])
+        t, s = p // cfg.k, int(slots[p])
+        y_ref, _ = oracle.expert_mlp_fp8(inp["x"][t], q1[s], s1[s], q2[s], s2[s])
+        check_out(y[r:r + 1], y_ref[None, :], f"fp8 y row {r}")
+
+
 # --------------------------------------------------------------------------- device-side error paths
 
 def test_out_of_range_expert_ids_are_dropped_and_flagged():
@@ -412,3 +480,9 @@ def test_grouped_topk_prefill_full_size():
 
 def test_routing_on_input_prefill_full_size():
     _full_size("routing_on_input_prefill", 32)
+
+
+@pytest.mark.parametrize("name", ["dsv2_lite_like_decode_t1_fp8", "dsv2_lite_like_decode_t32_fp8",
+                                  "qwen2_moe_like_prefill_fp8"])
+def test_fp8_full_size(name):
+    _full_size(name, 16 if "prefill" in name else 32)
