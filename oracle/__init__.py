@@ -75,7 +75,7 @@ def _load():
         lib.oracle_expert_mlp.restype = None
         lib.oracle_moe_tokens.argtypes = [P, i64, i32, P, P, i32, i32, i32, i32, i32, i32, P, P, i32, i32, i32,
                                           P, P, i32, i32, P, P, i32, P, P, P, P, P, P, P, P, P,
-                                          P, i64, P, P, P, P]
+                                          i32, P, i64, P, P, P, P]
         lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
         lib.oracle_e4m3_to_f64.restype = ctypes.c_double
         lib.oracle_f64_to_e4m3.argtypes = [ctypes.c_double]
@@ -84,6 +84,10 @@ def _load():
         lib.oracle_quantize_fp8_rows.restype = None
         lib.oracle_expert_mlp_fp8.argtypes = [P, P, P, P, P, i32, i32, P, P]
         lib.oracle_expert_mlp_fp8.restype = None
+        lib.oracle_expert_mlp_w8a8.argtypes = [P, P, P, P, P, i32, i32, P, P]
+        lib.oracle_expert_mlp_w8a8.restype = None
+        lib.oracle_quantize_act_rows.argtypes = [P, i64, i32, P, P]
+        lib.oracle_quantize_act_rows.restype = None
         lib.oracle_moe_tokens.restype = None
         lib.oracle_set_threads.argtypes = [i32]
         lib.oracle_set_threads.restype = None
@@ -233,8 +237,24 @@ def quantize_fp8_rows(w):
     return q, sc
 
 
-def expert_mlp_fp8(x_row, W1q, s1, W2q, s2):
-    """C oracle_expert_mlp_fp8: one token through one SwiGLU expert with E4M3 weights."""
+def quantize_act_rows(v):
+    """C oracle_quantize_act_rows on a bf16 matrix [..., K]: returns (q uint8 same shape,
+    scale float32 [...]) with a power-of-two scale 2^e per row, e the smallest integer
+    >= -126 with amax <= 448 * 2^e, and q = e4m3(v / 2^e)."""
+    lib = _load()
+    v16 = np.ascontiguousarray(_u16(v))
+    shape = v16.shape
+    K = shape[-1]
+    rows = int(np.prod(shape[:-1]))
+    q = np.empty(shape, np.uint8)
+    sc = np.empty(shape[:-1], np.float32)
+    lib.oracle_quantize_act_rows(_ptr(v16), rows, K, _ptr(q), _ptr(sc))
+    return q, sc
+
+
+def expert_mlp_fp8(x_row, W1q, s1, W2q, s2, act8=False):
+    """C oracle_expert_mlp_fp8 (or, act8, oracle_expert_mlp_w8a8: x and h quantised to
+    E4M3 per row too): one token through one SwiGLU expert with E4M3 weights."""
     lib = _load()
     x_row = _u16(x_row).reshape(-1)
     W1q, W2q = _np(W1q, np.uint8), _np(W2q, np.uint8)
@@ -243,7 +263,8 @@ def expert_mlp_fp8(x_row, W1q, s1, W2q, s2):
     I = W1q.shape[0] // 2
     y = np.empty(H, np.float64)
     h = np.empty(I, np.uint16)
-    lib.oracle_expert_mlp_fp8(_ptr(x_row), _ptr(W1q), _ptr(s1), _ptr(W2q), _ptr(s2), H, I, _ptr(y), _ptr(h))
+    fn = lib.oracle_expert_mlp_w8a8 if act8 else lib.oracle_expert_mlp_fp8
+    fn(_ptr(x_row), _ptr(W1q), _ptr(s1), _ptr(W2q), _ptr(s2), H, I, _ptr(y), _ptr(h))
     return y, h
 
 
@@ -256,7 +277,8 @@ def moe_tokens(x, Wg, bias, k, renorm, W1, W2, tokens=None, rep_offset=None, rep
     on_input: the routing weight scales each expert's input (rounded to bf16)
     and the expert outputs are summed unweighted.
     fp8: None, or a dict of E4M3 weights with row scales (W1q, s1, W2q, s2 and,
-    with shared experts, W1sq, s1s, W2sq, s2s) used in place of W1/W2/W1s/W2s.
+    with shared experts, W1sq, s1s, W2sq, s2s) used in place of W1/W2/W1s/W2s;
+    with act8=True in it, the activations are quantised to E4M3 per row as well.
 
     W1 [S_local, 2I, H], W2 [S_local, H, I] are indexed by local slot.
     W1s [n_shared, 2*I_sh, H] / W2s [n_shared, H, I_sh] (or None).
@@ -297,7 +319,7 @@ def moe_tokens(x, Wg, bias, k, renorm, W1, W2, tokens=None, rep_offset=None, rep
                           _ptr(W1), _ptr(W2), I, n_shared, _ptr(W1s), _ptr(W2s), I_sh, _ptr(gw),
                           _ptr(fq["W1q"]), _ptr(fq["s1"]), _ptr(fq["W2q"]), _ptr(fq["s2"]),
                           _ptr(fq["W1sq"]), _ptr(fq["s1s"]), _ptr(fq["W2sq"]), _ptr(fq["s2s"]),
-                          _ptr(tokens), n, _ptr(out), _ptr(ids), _ptr(w), _ptr(sl))
+                          int(bool(f.get("act8", False))), _ptr(tokens), n, _ptr(out), _ptr(ids), _ptr(w), _ptr(sl))
     return dict(out=out, ids=ids, w=w, slots=sl)
 
 

@@ -373,6 +373,53 @@ void oracle_permute(const int32_t *slots, int64_t P, int S,
 }
 
 /* ------------------------------------------------------------------------- */
+/* E4M3 activations                                                           */
+/* ------------------------------------------------------------------------- */
+
+/* E4M3 activations as well as weights ("W8A8"; TensorRT-LLM AutoDeploy MoE PR
+ * #10985, review of torch_moe.py, names FP8 paths of the MoE ops and fixes no
+ * format).  Reading: each expert input row and each intermediate row h is
+ * quantised on its own, with a power-of-two scale 2^e, e the smallest integer
+ * >= -126 such that amax <= 448 * 2^e (so amax / scale lies in (224, 448]
+ * unless the clamp applies), and q = e4m3(v / 2^e) to nearest with ties to
+ * even (the division by a power of two is exact).  An all-zero row gets
+ * e = -126 and q = 0. */
+void oracle_quantize_act_row(const uint16_t *v, int K, uint8_t *q, float *scale)
+{
+    double amax = 0.0;
+    for (int c = 0; c < K; ++c) {
+        const double a = fabs(oracle_bf16_to_f64(v[c]));
+        if (a > amax) amax = a;
+    }
+    int e = -126;
+    while (amax > ldexp(448.0, e)) ++e;
+    *scale = (float)ldexp(1.0, e);
+    for (int c = 0; c < K; ++c) q[c] = oracle_f64_to_e4m3(ldexp(oracle_bf16_to_f64(v[c]), -e));
+}
+
+void oracle_quantize_act_rows(const uint16_t *v, int64_t rows, int K, uint8_t *q, float *scale)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r)
+        oracle_quantize_act_row(v + (size_t)r * (size_t)K, K, q + (size_t)r * (size_t)K, scale + r);
+}
+
+/* The row v [K] as fp64 values: bf16 as is, or (act8) its E4M3 quantisation
+ * dequantised exactly, scale * e4m3(q). */
+static void act_values(const uint16_t *v, int K, int act8, double *out)
+{
+    if (!act8) {
+        for (int c = 0; c < K; ++c) out[c] = oracle_bf16_to_f64(v[c]);
+        return;
+    }
+    uint8_t *q = (uint8_t *)malloc((size_t)K);
+    float sc;
+    oracle_quantize_act_row(v, K, q, &sc);
+    for (int c = 0; c < K; ++c) out[c] = (double)sc * oracle_e4m3_to_f64(q[c]);
+    free(q);
+}
+
+/* ------------------------------------------------------------------------- */
 /* 5. Gated MLP (SwiGLU) of one expert on one token                          */
 /* ------------------------------------------------------------------------- */
 
@@ -385,33 +432,40 @@ void oracle_permute(const int32_t *slots, int64_t P, int S,
  *
  *   x [H] bf16;  W1 [2I, H] bf16 (rows 0..I-1 gate, I..2I-1 up);  W2 [H, I] bf16
  *   y [H] double out;  h [I] bf16 bits out (or NULL)
+ * act8: the input row and the bf16 row h are quantised to E4M3 with a
+ * power-of-two scale each (oracle_quantize_act_row) before FC1 and FC2.
  */
 static void expert_mlp_w(const uint16_t *x, const oracle_wmat *W1, const oracle_wmat *W2,
-                         int H, int I, double *y, uint16_t *h_out)
+                         int H, int I, int act8, double *y, uint16_t *h_out)
 {
+    double *xd = (double *)malloc(sizeof(double) * (size_t)H);
     double *h = (double *)malloc(sizeof(double) * (size_t)I);
+    uint16_t *hb = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)I);
+    act_values(x, H, act8, xd);
     for (int i = 0; i < I; ++i) {
         double g = 0.0, u = 0.0;
-        for (int hh = 0; hh < H; ++hh) g += wget(W1, (size_t)i, (size_t)hh) * oracle_bf16_to_f64(x[hh]);
-        for (int hh = 0; hh < H; ++hh) u += wget(W1, (size_t)I + (size_t)i, (size_t)hh) * oracle_bf16_to_f64(x[hh]);
+        for (int hh = 0; hh < H; ++hh) g += wget(W1, (size_t)i, (size_t)hh) * xd[hh];
+        for (int hh = 0; hh < H; ++hh) u += wget(W1, (size_t)I + (size_t)i, (size_t)hh) * xd[hh];
         double a = g / (1.0 + exp(-g)) * u;
-        uint16_t b = oracle_f64_to_bf16(a);
-        if (h_out) h_out[i] = b;
-        h[i] = oracle_bf16_to_f64(b);
+        hb[i] = oracle_f64_to_bf16(a);
+        if (h_out) h_out[i] = hb[i];
     }
+    act_values(hb, I, act8, h);
     for (int o = 0; o < H; ++o) {
         double s = 0.0;
         for (int i = 0; i < I; ++i) s += wget(W2, (size_t)o, (size_t)i) * h[i];
         y[o] = s;
     }
+    free(xd);
     free(h);
+    free(hb);
 }
 
 void oracle_expert_mlp(const uint16_t *x, const uint16_t *W1, const uint16_t *W2,
                        int H, int I, double *y, uint16_t *h_out)
 {
     const oracle_wmat w1 = {W1, NULL, NULL, (size_t)H}, w2 = {W2, NULL, NULL, (size_t)I};
-    expert_mlp_w(x, &w1, &w2, H, I, y, h_out);
+    expert_mlp_w(x, &w1, &w2, H, I, 0, y, h_out);
 }
 
 /* The same MLP with E4M3 weights: W1q [2I, H] with scales s1 [2I], W2q [H, I]
@@ -420,7 +474,15 @@ void oracle_expert_mlp_fp8(const uint16_t *x, const uint8_t *W1q, const float *s
                            const float *s2, int H, int I, double *y, uint16_t *h_out)
 {
     const oracle_wmat w1 = {NULL, W1q, s1, (size_t)H}, w2 = {NULL, W2q, s2, (size_t)I};
-    expert_mlp_w(x, &w1, &w2, H, I, y, h_out);
+    expert_mlp_w(x, &w1, &w2, H, I, 0, y, h_out);
+}
+
+/* E4M3 weights and E4M3 activations (x and h quantised per row). */
+void oracle_expert_mlp_w8a8(const uint16_t *x, const uint8_t *W1q, const float *s1, const uint8_t *W2q,
+                            const float *s2, int H, int I, double *y, uint16_t *h_out)
+{
+    const oracle_wmat w1 = {NULL, W1q, s1, (size_t)H}, w2 = {NULL, W2q, s2, (size_t)I};
+    expert_mlp_w(x, &w1, &w2, H, I, 1, y, h_out);
 }
 
 /* ------------------------------------------------------------------------- */
@@ -443,7 +505,9 @@ void oracle_expert_mlp_fp8(const uint16_t *x, const uint8_t *W1q, const float *s
  *
  * Weights: bf16 (W1, W2, W1s, W2s), or, where W1q / W1sq is given, E4M3 bytes
  * with one fp32 scale per row (W1q [S_local, 2I, H] + s1 [S_local, 2I], W2q
- * [S_local, H, I] + s2 [S_local, H]; the shared ones alike).
+ * [S_local, H, I] + s2 [S_local, H]; the shared ones alike).  act8 (E4M3
+ * weights only): the expert input rows and intermediate rows are quantised to
+ * E4M3 as well (oracle_quantize_act_row), the shared experts' too.
  *
  * Shared experts: n_shared experts of intermediate size I_sh each; W1s holds
  * them one after another, each [2*I_sh, H] (gate rows, then up rows); W2s holds
@@ -461,7 +525,7 @@ void oracle_moe_tokens(const uint16_t *x, int64_t T, int H,
                        const uint16_t *shared_gate_w,
                        const uint8_t *W1q, const float *s1, const uint8_t *W2q, const float *s2,
                        const uint8_t *W1sq, const float *s1s, const uint8_t *W2sq, const float *s2s,
-                       const int64_t *tok, int64_t n,
+                       int act8, const int64_t *tok, int64_t n,
                        double *out, int32_t *ids_out, double *w_out, int32_t *slot_out)
 {
     (void)T;
@@ -515,7 +579,7 @@ void oracle_moe_tokens(const uint16_t *x, int64_t T, int H,
                 xin = xs;
             }
             if (W1q)
-                oracle_expert_mlp_fp8(xin, W1q + (size_t)s * 2u * (size_t)I * (size_t)H, s1 + (size_t)s * 2u * (size_t)I,
+                (act8 ? oracle_expert_mlp_w8a8 : oracle_expert_mlp_fp8)(xin, W1q + (size_t)s * 2u * (size_t)I * (size_t)H, s1 + (size_t)s * 2u * (size_t)I,
                                       W2q + (size_t)s * (size_t)H * (size_t)I, s2 + (size_t)s * (size_t)H, H, I, y,
                                       NULL);
             else
@@ -536,7 +600,7 @@ void oracle_moe_tokens(const uint16_t *x, int64_t T, int H,
             double *ysum = (double *)calloc((size_t)H, sizeof(double));
             for (int sidx = 0; sidx < n_shared; ++sidx) {
                 if (W1sq)
-                    oracle_expert_mlp_fp8(xt, W1sq + (size_t)sidx * 2u * (size_t)I_sh * (size_t)H,
+                    (act8 ? oracle_expert_mlp_w8a8 : oracle_expert_mlp_fp8)(xt, W1sq + (size_t)sidx * 2u * (size_t)I_sh * (size_t)H,
                                           s1s + (size_t)sidx * 2u * (size_t)I_sh,
                                           W2sq + (size_t)sidx * (size_t)H * (size_t)I_sh, s2s + (size_t)sidx * (size_t)H,
                                           H, I_sh, y, NULL);

@@ -546,3 +546,121 @@ def test_fp8_layer_matches_numpy_mlp_of_dequantised_weights():
         h = torch.from_numpy(g / (1 + np.exp(-g)) * u).to(torch.bfloat16).to(torch.float64).numpy()
         ref = h @ D2[e].T
         np.testing.assert_allclose(res["out"][t], ref, rtol=0, atol=1e-9 * np.abs(ref).max())
+
+
+# --------------------------------------------------------------------------- E4M3 activations (W8A8)
+
+def _act_exponent(amax: float) -> int:
+    """Smallest e >= -126 with amax <= 448 * 2^e: a log2 guess corrected by exact compares."""
+    if amax == 0.0:
+        return -126
+    e = max(-126, int(np.ceil(np.log2(amax / 448.0))))
+    while e > -126 and amax <= 448.0 * 2.0 ** (e - 1):
+        e -= 1
+    while amax > 448.0 * 2.0 ** e:
+        e += 1
+    return e
+
+
+def _quant_act_ref(v: torch.Tensor):
+    """Row quantisation through torch's float8_e4m3fn cast: (q bytes, scales, dequantised fp64)."""
+    v64 = v.to(torch.float64).reshape(-1, v.shape[-1]).numpy()
+    qs, scs = [], []
+    for row in v64:
+        e = _act_exponent(float(np.abs(row).max()))
+        scaled = torch.from_numpy(np.ldexp(row, -e)).to(torch.float32)
+        qs.append(scaled.to(torch.float8_e4m3fn).view(torch.uint8).numpy())
+        scs.append(np.float32(2.0 ** e))
+    q = np.stack(qs).reshape(v.shape)
+    sc = np.array(scs, np.float32).reshape(v.shape[:-1])
+    deq = sc[..., None].astype(np.float64) * torch.from_numpy(q).view(torch.float8_e4m3fn).to(
+        torch.float64).numpy()
+    return q, sc, deq
+
+
+def _act_rows():
+    g = torch.Generator().manual_seed(11)
+    rows = [torch.randn(96, generator=g) * s for s in (1e-3, 0.02, 1.0, 300.0, 1e5, 1e-30)]
+    r = torch.randn(96, generator=g)
+    rows.append(torch.zeros(96))                                   # all zero: e = -126, q = 0
+    rows.append(r / r.abs().max() * 3584.0)                        # amax = 448 * 2^3 exactly
+    rows.append(r / r.abs().max() * 3600.0)                        # the next bf16 above it
+    rows.append(torch.full((96,), 2.0 ** -130) * torch.sign(r))    # bf16 subnormals: clamp at 2^-126
+    return torch.stack(rows).to(torch.bfloat16)
+
+
+def test_act_quantisation_matches_torch_cast_with_power_of_two_scale():
+    v = _act_rows()
+    q, sc = oracle.quantize_act_rows(v)
+    q_ref, sc_ref, _ = _quant_act_ref(v)
+    assert np.array_equal(sc, sc_ref)
+    assert np.array_equal(q, q_ref)
+    assert sc[6] == np.float32(2.0 ** -126) and np.all(q[6] == 0)
+    assert sc[7] == 8.0 and sc[8] == 16.0 and sc[9] == np.float32(2.0 ** -126)
+
+
+def test_act_quantisation_bounds_and_power_of_two_equivariance():
+    v = _act_rows()
+    q, sc = oracle.quantize_act_rows(v)
+    vf = v.to(torch.float64).numpy()
+    amax = np.abs(vf).max(1)
+    for r in range(v.shape[0]):
+        if sc[r] > np.float32(2.0 ** -126):
+            assert 224.0 < amax[r] / float(sc[r]) <= 448.0
+    deq = sc[:, None].astype(np.float64) * torch.from_numpy(q).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    bound = np.maximum(2.0 ** -4 * np.abs(vf), 2.0 ** -10 * sc[:, None]) * (1 + 1e-9)
+    assert np.all(np.abs(deq - vf) <= bound)
+    # scaling a row by 2^j (no clamp involved) leaves q alone and scales the scale
+    for j in (-7, 3, 20):
+        keep = [r for r in (0, 1, 2, 3, 7, 8)]
+        q2, sc2 = oracle.quantize_act_rows((v[keep].to(torch.float64) * 2.0 ** j).to(torch.bfloat16))
+        assert np.array_equal(q2, q[keep])
+        assert np.array_equal(sc2.astype(np.float64), sc[keep].astype(np.float64) * 2.0 ** j)
+
+
+def test_w8a8_layer_matches_numpy_mlp_of_quantised_rows():
+    cfg = _small_cfg(T=10, H=64, I=64, E=4, k=1, renorm=True, n_shared=1, I_shared=128)
+    inp = mi.make_inputs(cfg)
+    q1, s1 = oracle.quantize_fp8_rows(inp["W1"])
+    q2, s2 = oracle.quantize_fp8_rows(inp["W2"])
+    q1s, s1s = oracle.quantize_fp8_rows(inp["W1s"])
+    q2s, s2s = oracle.quantize_fp8_rows(inp["W2s"])
+    fp8 = dict(W1q=q1, s1=s1, W2q=q2, s2=s2, W1sq=q1s, s1s=s1s, W2sq=q2s, s2s=s2s, act8=True)
+    res = oracle.moe_layer(inp["x"], inp["Wg"], None, 1, True, inp["W1"], inp["W2"], W1s=inp["W1s"],
+                           W2s=inp["W2s"], fp8=fp8)
+    deq = lambda q, s: s[..., None].astype(np.float64) * torch.from_numpy(q).view(  # noqa: E731
+        torch.float8_e4m3fn).to(torch.float64).numpy()
+    D1, D2, D1s, D2s = deq(q1, s1), deq(q2, s2), deq(q1s, s1s)[0], deq(q2s, s2s)[0]
+    _, _, xq = _quant_act_ref(inp["x"])
+
+    def mlp(xrow, A, B):
+        I = A.shape[0] // 2
+        g, u = xrow @ A[:I].T, xrow @ A[I:].T
+        h = torch.from_numpy(g / (1 + np.exp(-g)) * u).to(torch.bfloat16)
+        return _quant_act_ref(h[None])[2][0] @ B.T
+
+    for t in range(cfg.T):
+        e = int(res["ids"][t, 0])
+        ref = mlp(xq[t], D1[e], D2[e]) + mlp(xq[t], D1s, D2s)
+        np.testing.assert_allclose(res["out"][t], ref, rtol=0, atol=1e-9 * np.abs(ref).max())
+    # and the activations really are quantised: the weight-only result differs
+    w16 = oracle.moe_layer(inp["x"], inp["Wg"], None, 1, True, inp["W1"], inp["W2"], W1s=inp["W1s"],
+                           W2s=inp["W2s"], fp8={k: v for k, v in fp8.items() if k != "act8"})
+    assert not np.array_equal(w16["out"], res["out"])
+
+
+def test_w8a8_single_expert_with_routing_on_input_quantises_the_scaled_row():
+    cfg = _small_cfg(T=6, H=64, I=64, E=3, k=2, renorm=True)
+    inp = mi.make_inputs(cfg)
+    q1, s1 = oracle.quantize_fp8_rows(inp["W1"])
+    q2, s2 = oracle.quantize_fp8_rows(inp["W2"])
+    fp8 = dict(W1q=q1, s1=s1, W2q=q2, s2=s2, act8=True)
+    res = oracle.moe_layer(inp["x"], inp["Wg"], None, 2, True, inp["W1"], inp["W2"], on_input=True, fp8=fp8)
+    for t in range(cfg.T):
+        acc = np.zeros(cfg.H)
+        for j in range(2):
+            e, w = int(res["ids"][t, j]), float(res["w"][t, j])
+            xs = torch.from_numpy(w * _bf16_np(inp["x"][t])).to(torch.bfloat16)
+            y, _ = oracle.expert_mlp_fp8(xs, q1[e], s1[e], q2[e], s2[e], act8=True)
+            acc += y
+        np.testing.assert_allclose(res["out"][t], acc, rtol=0, atol=1e-12 * np.abs(acc).max())
