@@ -198,10 +198,29 @@ def _work(cfg, rows: int, active_slots: int):
     eb = 1 if cfg.fp8 else 2  # bytes per weight (E4M3 adds one fp32 scale per row)
     w1 = active_slots * 2 * I * (H * eb + (4 if cfg.fp8 else 0)) + 2 * Ish * (H * eb + (4 if cfg.fp8 else 0))
     w2 = active_slots * H * (I * eb + (4 if cfg.fp8 else 0)) + H * (Ish * eb + (4 if cfg.fp8 else 0))
-    fc1_bytes = w1 + (rows + T * (Ish > 0)) * H * 2 + rows * I * 2 + T * Ish * 2
-    fc2_bytes = w2 + rows * I * 2 + T * Ish * 2 + rows * H * 2 + (T * H * 2 if Ish else 0)
+    ab = 1 if cfg.act8 else 2  # bytes per GEMM input activation (E4M3 adds one fp32 scale per row)
+    a_rows = rows + T * (Ish > 0)
+    fc1_bytes = w1 + a_rows * (H * ab + (4 if cfg.act8 else 0)) + rows * I * 2 + T * Ish * 2
+    fc2_bytes = (w2 + rows * (I * ab + (4 if cfg.act8 else 0)) + T * (Ish * ab + (4 if cfg.act8 and Ish else 0))
+                 + rows * H * 2 + (T * H * 2 if Ish else 0))
     return dict(fc1_flops=fc1_flops, fc2_flops=fc2_flops, fc1_bytes=fc1_bytes, fc2_bytes=fc2_bytes,
                 gate_flops=2.0 * T * H * cfg.E)
+
+
+def _oracle_fp8(oracle, cfg, cpu):
+    """E4M3 workloads: the oracle's own quantisation of the weights (done once, untimed),
+    the shared experts as the one concatenated MLP the layer runs."""
+    if not cfg.fp8:
+        return None
+    q1, s1 = oracle.quantize_fp8_rows(cpu["W1"])
+    q2, s2 = oracle.quantize_fp8_rows(cpu["W2"])
+    f = dict(W1q=q1, s1=s1, W2q=q2, s2=s2, act8=cfg.act8)
+    if cpu["W1s"] is not None:
+        c1, c2 = mi.shared_concat(cpu["W1s"], cpu["W2s"])
+        cpu["W1s"], cpu["W2s"] = c1[None], c2[None]
+        f["W1sq"], f["s1s"] = oracle.quantize_fp8_rows(cpu["W1s"])
+        f["W2sq"], f["s2s"] = oracle.quantize_fp8_rows(cpu["W2s"])
+    return f
 
 
 def run_cpu_baseline(inp_dev, cfg, target_s=10.0, T_cap=None):
@@ -213,12 +232,14 @@ def run_cpu_baseline(inp_dev, cfg, target_s=10.0, T_cap=None):
     oracle.set_threads(os.cpu_count() or 1)
     cpu = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in inp_dev.items()}
 
+    fp8 = _oracle_fp8(oracle, cfg, cpu)
+
     def run(n):
         t0 = time.perf_counter()
         oracle.moe_layer(cpu["x"][:n], cpu["Wg"], cpu["bias"], cfg.k, cfg.renorm, cpu["W1"], cpu["W2"],
                          rep_offset=cpu["rep_offset"], rep_slots=cpu["rep_slots"], W1s=cpu["W1s"],
                          W2s=cpu["W2s"], shared_gate_w=cpu["w_s"], S=cfg.slots, n_group=cfg.n_group,
-                         topk_group=cfg.topk_group, on_input=cfg.on_input)
+                         topk_group=cfg.topk_group, on_input=cfg.on_input, fp8=fp8)
         return time.perf_counter() - t0
 
     threads = oracle.get_threads()
@@ -285,18 +306,44 @@ def bench_ours(args):
     h_sh = torch.empty((T, Ish), dtype=torch.bfloat16, device=dev) if Ish else None
     y_sh = torch.empty((T, H), dtype=torch.bfloat16, device=dev) if Ish else None
     xs = x if Ish else None
-    stages = {
-        "route": lambda: layer.route(x),
-        "permute": lambda: layer.permute(x),
-        "fc1": (lambda: moe.moe_grouped_fc1_fp8(layer.x_perm, layer.offsets, layer.W1q, layer.s1, xs, layer.W1sq,
-                                                layer.s1s, h, h_sh, layer.ws)) if layer.fp8 else
-               (lambda: moe.moe_grouped_fc1(layer.x_perm, layer.offsets, layer.W1, xs, layer.W1s, h, h_sh, layer.ws)),
-        "fc2": (lambda: moe.moe_grouped_fc2_fp8(h, layer.offsets, layer.W2q, layer.s2, h_sh, layer.W2sq, layer.s2s,
-                                                y, y_sh, layer.ws)) if layer.fp8 else
-               (lambda: moe.moe_grouped_fc2(h, layer.offsets, layer.W2, h_sh, layer.W2s, y, y_sh, layer.ws)),
-        "finalize": lambda: moe.moe_finalize(y, layer.pair_row, None if layer.on_input else layer.topk_w, y_sh, xs,
-                                             layer.gate, layer.out, layer.ws),
-    }
+    stages = {"route": lambda: layer.route(x), "permute": lambda: layer.permute(x)}
+    if layer.act8:
+        xq = torch.empty((P, H), dtype=torch.uint8, device=dev)
+        sx = torch.empty(P, dtype=torch.float32, device=dev)
+        xsq = torch.empty((T, H), dtype=torch.uint8, device=dev) if Ish else None
+        sxs = torch.empty(T, dtype=torch.float32, device=dev) if Ish else None
+        hq = torch.empty((P, cfg.I), dtype=torch.uint8, device=dev)
+        shq = torch.empty(P, dtype=torch.float32, device=dev)
+        hsq = torch.empty((T, Ish), dtype=torch.uint8, device=dev) if Ish else None
+        shs = torch.empty(T, dtype=torch.float32, device=dev) if Ish else None
+
+        def quant_x():
+            moe.moe_quantize_act_rows(layer.x_perm, xq, sx)
+            if Ish:
+                moe.moe_quantize_act_rows(x, xsq, sxs)
+
+        def quant_h():
+            moe.moe_quantize_act_rows(h, hq, shq)
+            if Ish:
+                moe.moe_quantize_act_rows(h_sh, hsq, shs)
+
+        stages["quant_x"] = quant_x
+        stages["fc1"] = lambda: moe.moe_grouped_fc1_w8a8(xq, sx, layer.offsets, layer.W1q, layer.s1, xsq, sxs,
+                                                         layer.W1sq, layer.s1s, h, h_sh, layer.ws)
+        stages["quant_h"] = quant_h
+        stages["fc2"] = lambda: moe.moe_grouped_fc2_w8a8(hq, shq, layer.offsets, layer.W2q, layer.s2, hsq, shs,
+                                                         layer.W2sq, layer.s2s, y, y_sh, layer.ws)
+    elif layer.fp8:
+        stages["fc1"] = lambda: moe.moe_grouped_fc1_fp8(layer.x_perm, layer.offsets, layer.W1q, layer.s1, xs,
+                                                        layer.W1sq, layer.s1s, h, h_sh, layer.ws)
+        stages["fc2"] = lambda: moe.moe_grouped_fc2_fp8(h, layer.offsets, layer.W2q, layer.s2, h_sh, layer.W2sq,
+                                                        layer.s2s, y, y_sh, layer.ws)
+    else:
+        stages["fc1"] = lambda: moe.moe_grouped_fc1(layer.x_perm, layer.offsets, layer.W1, xs, layer.W1s, h, h_sh,
+                                                    layer.ws)
+        stages["fc2"] = lambda: moe.moe_grouped_fc2(h, layer.offsets, layer.W2, h_sh, layer.W2s, y, y_sh, layer.ws)
+    stages["finalize"] = lambda: moe.moe_finalize(y, layer.pair_row, None if layer.on_input else layer.topk_w, y_sh,
+                                                  xs, layer.gate, layer.out, layer.ws)
     for fn in stages.values():
         fn()
     torch.cuda.synchronize()
@@ -350,11 +397,13 @@ def bench_ours(args):
     else:
         achieved = wk["fc1_flops"] / fc1_s / 1e12
         # burst peak: each step is a fraction of a millisecond between L2 flushes, and the
-        # clocks sampled during the timed region stay at their maximum (no power capping)
+        # clocks sampled during the timed region stay at their maximum (no power capping);
+        # E4M3 operands: the measured bf16 peak times the nominal fp8 / bf16 ratio (4.5 / 2.25)
+        peak = peaks["bf16"] * (2.0 if cfg.act8 else 1.0)
         roof = dict(bound="tensor", kernel="grouped_gemm_kernel<FC1+SwiGLU>", achieved=achieved,
-                    peak=peaks["bf16"], unit="TFLOP/s", frac=achieved / peaks["bf16"],
+                    peak=peak, unit="TFLOP/s", frac=achieved / peak,
                     peak_kind=f"{peaks['src']} bf16_tflops (burst; the kernel is timed in sub-millisecond steps "
-                              f"at full clock)")
+                              f"at full clock)" + (" x 2, the nominal e4m3 / bf16 rate ratio" if cfg.act8 else ""))
         per_unit = f"{wk['fc1_flops']:.4g} flops per launch = 4*H*(rows*I + T*I_shared)"
     key = (args.workload, _src_hash(os.path.join(ROOT, "serving_router_gate_gb300", "csrc", "moe_grouped_gemm.cu")))
     roof["traffic"] = NCU_TRAFFIC.get(key)
@@ -364,7 +413,7 @@ def bench_ours(args):
     res = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws_, "steps": K,
         "warmup": W, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic: seeded N(0,1) activations, N(0,sigma) random-init weights of the "
+        "dtype": "e4m3" if cfg.act8 else "bf16", "data": "synthetic: seeded N(0,1) activations, N(0,sigma) random-init weights of the "
                                  "workload's shapes (no checkpoint)",
         "config": {"workload": cfg.name, "shape": mi.describe(cfg), "tokens_per_gpu": T,
                    "parallelism": f"replicas x{ws_} (independent token batches, no collective)",
@@ -406,11 +455,13 @@ def bench_reference(args):
     inp = mi.make_inputs(cfg, device=dev)
     cpu = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
 
+    fp8 = _oracle_fp8(oracle, cfg, cpu)
+
     def step(n):
         oracle.moe_layer(cpu["x"][:n], cpu["Wg"], cpu["bias"], cfg.k, cfg.renorm, cpu["W1"], cpu["W2"],
                          rep_offset=cpu["rep_offset"], rep_slots=cpu["rep_slots"], W1s=cpu["W1s"],
                          W2s=cpu["W2s"], shared_gate_w=cpu["w_s"], S=cfg.slots, n_group=cfg.n_group,
-                         topk_group=cfg.topk_group, on_input=cfg.on_input)
+                         topk_group=cfg.topk_group, on_input=cfg.on_input, fp8=fp8)
 
     threads = oracle.get_threads()
     n0 = min(cfg.T, max(8, threads))

@@ -288,6 +288,33 @@ MOE_API moe_status_t moe_forward_fp8(const moe_bf16_t *x_perm, const int32_t *of
 MOE_API moe_status_t moe_quantize_fp8_rows(const moe_bf16_t *w, int64_t rows, int K, uint8_t *q, float *scale,
                                    moe_stream_t stream);
 
+/* moe_forward_w8a8 -- moe_forward_fp8 with E4M3 activations as well (the same
+ * source, the same silence on the format).  Each expert input row (a row of
+ * x_perm) and each bf16 intermediate row h is quantised on its own with a
+ * power-of-two scale (moe_quantize_act_rows); the shared experts' input is x,
+ * quantised the same way per token.  FC1 and FC2 then run on E4M3 operands
+ * (tcgen05.mma kind::f8f6f4, fp32 accumulation), and each accumulator is
+ * multiplied by its A row's and its B row's scale.  Launches two quantisation
+ * kernels besides moe_forward's three.  The workspace regions for the
+ * quantised rows are part of moe_workspace_size.  Arguments, layouts,
+ * ownership and errors as moe_forward_fp8. */
+MOE_API moe_status_t moe_forward_w8a8(const moe_bf16_t *x_perm, const int32_t *offsets, int S_local, int64_t P_cap,
+                              const uint8_t *W1q, const float *W1_scale, const uint8_t *W2q,
+                              const float *W2_scale, int H, int I, const int32_t *pair_row,
+                              const float *topk_w, int64_t T, int k, const moe_bf16_t *x,
+                              const uint8_t *W1sq, const float *W1s_scale, const uint8_t *W2sq,
+                              const float *W2s_scale, int I_shared_total, const moe_bf16_t *shared_gate_w,
+                              moe_bf16_t *out, void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Row-wise E4M3 quantisation of activations v [rows, K] bf16 (K a multiple of
+ * 64), as moe_forward_w8a8 does: per row, scale = 2^e with e the smallest
+ * integer >= -126 such that amax_c |v[r][c]| <= 448 * 2^e, and
+ * q[r][c] = e4m3(v[r][c] / 2^e) to nearest, ties to even (the division is
+ * exact).  An all-zero row gets scale 2^-126 and q = 0.  Asynchronous on
+ * `stream`; allocates nothing. */
+MOE_API moe_status_t moe_quantize_act_rows(const moe_bf16_t *v, int64_t rows, int K, uint8_t *q, float *scale,
+                                   moe_stream_t stream);
+
 /* ---- the three stages of moe_forward ------------------------------------ */
 
 /* FC1 + SwiGLU on the tcgen05 tensor cores.  Routed problem: for each of the G
@@ -322,6 +349,23 @@ MOE_API moe_status_t moe_grouped_fc2_fp8(const moe_bf16_t *h, int64_t rows_cap, 
                                  const moe_bf16_t *h_shared, int64_t T, const uint8_t *W2sq,
                                  const float *W2s_scale, int I_shared_total, moe_bf16_t *y,
                                  moe_bf16_t *y_shared, void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/* The GEMM stages of moe_forward_w8a8: A operands are E4M3 rows with one fp32
+ * scale per row (aq [rows_cap, H] + a_scale [rows_cap], a_shared_q [T, H] +
+ * a_shared_scale [T]; for FC2 hq [rows_cap, I] + h_scale, h_shared_q
+ * [T, I_shared_total] + h_shared_scale), weights as moe_forward_fp8. */
+MOE_API moe_status_t moe_grouped_fc1_w8a8(const uint8_t *aq, const float *a_scale, int64_t rows_cap,
+                                  const int32_t *offsets, int G, const uint8_t *W1q, const float *W1_scale,
+                                  int H, int I, const uint8_t *a_shared_q, const float *a_shared_scale,
+                                  int64_t T, const uint8_t *W1sq, const float *W1s_scale, int I_shared_total,
+                                  moe_bf16_t *h, moe_bf16_t *h_shared, void *ws, size_t ws_bytes,
+                                  moe_stream_t stream);
+MOE_API moe_status_t moe_grouped_fc2_w8a8(const uint8_t *hq, const float *h_scale, int64_t rows_cap,
+                                  const int32_t *offsets, int G, const uint8_t *W2q, const float *W2_scale,
+                                  int H, int I, const uint8_t *h_shared_q, const float *h_shared_scale,
+                                  int64_t T, const uint8_t *W2sq, const float *W2s_scale, int I_shared_total,
+                                  moe_bf16_t *y, moe_bf16_t *y_shared, void *ws, size_t ws_bytes,
+                                  moe_stream_t stream);
 
 /* Unpermute + weighted combine: out[t] = bf16(sum_j topk_w[t,j] * y[pair_row[t,j]]
  * + g_t * y_shared[t]), fp32 accumulation in fixed j order (topk_w NULL: weight

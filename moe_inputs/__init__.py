@@ -61,6 +61,7 @@ class MoEConfig:
     topk_group: int = 1              # groups kept per token
     on_input: bool = False           # routing weight applied to the expert input, outputs summed unweighted
     fp8: bool = False                # E4M3 expert weights with one fp32 scale per row
+    act8: bool = False               # and E4M3 activations, one power-of-two scale per row
     w_std: float = 0.02              # expert weight std
     gate_std: float = 0.02           # router weight std
     seed: int = 0
@@ -97,6 +98,8 @@ for _t in (1, 8, 32, 128):
 for _name in ["dsv2_lite_like_decode_t1", "dsv2_lite_like_decode_t8", "dsv2_lite_like_decode_t32",
               "dsv2_lite_like_decode_t128", "qwen2_moe_like_prefill"]:
     CONFIGS[_name + "_fp8"] = CONFIGS[_name].with_(name=_name + "_fp8", fp8=True)
+    # E4M3 weights and activations (tcgen05 kind::f8f6f4)
+    CONFIGS[_name + "_w8a8"] = CONFIGS[_name].with_(name=_name + "_w8a8", fp8=True, act8=True)
 
 
 def _gen(device, seed: int, idx: int) -> torch.Generator:
@@ -227,7 +230,8 @@ def describe(cfg: MoEConfig) -> str:
     if cfg.on_input:
         parts.append("routing on input")
     if cfg.fp8:
-        parts.append("E4M3 weights, row scales")
+        parts.append("E4M3 weights, row scales" + (" + E4M3 activations, power-of-two row scales"
+                                                   if cfg.act8 else ""))
     return ", ".join(parts)
 
 

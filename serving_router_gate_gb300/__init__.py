@@ -25,7 +25,8 @@ __all__ = [
     "moe_route", "moe_permute", "moe_forward", "moe_grouped_fc1", "moe_grouped_fc2", "moe_finalize",
     "moe_debug_wait_timeout", "moe_set_wait_timeout_ns", "moe_route_noalloc", "moe_set_gemm_pair_mode",
     "moe_set_pdl", "moe_get_launch_count", "moe_permute_on_input", "moe_route_grouped", "moe_forward_fp8",
-    "moe_quantize_fp8_rows", "EXPORTED_SYMBOLS",
+    "moe_quantize_fp8_rows", "moe_forward_w8a8", "moe_quantize_act_rows", "moe_grouped_fc1_fp8",
+    "moe_grouped_fc2_fp8", "moe_grouped_fc1_w8a8", "moe_grouped_fc2_w8a8", "EXPORTED_SYMBOLS",
 ]
 
 MOE_OK = 0
@@ -44,6 +45,7 @@ EXPORTED_SYMBOLS = (
     "moe_finalize", "moe_debug_wait_timeout", "moe_set_wait_timeout_ns", "moe_route_noalloc",
     "moe_set_gemm_pair_mode", "moe_set_pdl", "moe_get_launch_count", "moe_permute_on_input", "moe_route_grouped",
     "moe_forward_fp8", "moe_quantize_fp8_rows", "moe_grouped_fc1_fp8", "moe_grouped_fc2_fp8",
+    "moe_forward_w8a8", "moe_quantize_act_rows", "moe_grouped_fc1_w8a8", "moe_grouped_fc2_w8a8",
 )
 
 
@@ -78,6 +80,11 @@ def _load():
         "moe_forward_fp8": ([P, P, i32, i64, P, P, P, P, i32, i32, P, P, i64, i32, P, P, P, P, P, i32, P, P, P, sz, P],
                             i32),
         "moe_quantize_fp8_rows": ([P, i64, i32, P, P, P], i32),
+        "moe_forward_w8a8": ([P, P, i32, i64, P, P, P, P, i32, i32, P, P, i64, i32, P, P, P, P, P, i32, P, P, P, sz,
+                              P], i32),
+        "moe_quantize_act_rows": ([P, i64, i32, P, P, P], i32),
+        "moe_grouped_fc1_w8a8": ([P, P, i64, P, i32, P, P, i32, i32, P, P, i64, P, P, i32, P, P, P, sz, P], i32),
+        "moe_grouped_fc2_w8a8": ([P, P, i64, P, i32, P, P, i32, i32, P, P, i64, P, P, i32, P, P, P, sz, P], i32),
         "moe_grouped_fc1_fp8": ([P, i64, P, i32, P, P, i32, i32, P, i64, P, P, i32, P, P, P, sz, P], i32),
         "moe_grouped_fc2_fp8": ([P, i64, P, i32, P, P, i32, i32, P, i64, P, P, i32, P, P, P, sz, P], i32),
         "moe_grouped_fc1": ([P, i64, P, i32, P, i32, i32, P, i64, P, i32, P, P, P, sz, P], i32),
@@ -232,13 +239,26 @@ def moe_forward(x_perm, offsets, W1, W2, pair_row, topk_w, x, W1s, W2s, shared_g
 def moe_forward_fp8(x_perm, offsets, W1q, s1, W2q, s2, pair_row, topk_w, x, W1sq, s1s, W2sq, s2s, shared_gate_w,
                     out, ws, stream=None):
     """moe_forward with E4M3 weights (uint8 tensors) and fp32 row scales (moe_quantize_fp8_rows)."""
+    _forward_q("moe_forward_fp8", x_perm, offsets, W1q, s1, W2q, s2, pair_row, topk_w, x, W1sq, s1s, W2sq, s2s,
+               shared_gate_w, out, ws, stream)
+
+
+def moe_forward_w8a8(x_perm, offsets, W1q, s1, W2q, s2, pair_row, topk_w, x, W1sq, s1s, W2sq, s2s, shared_gate_w,
+                     out, ws, stream=None):
+    """moe_forward_fp8 with the activations quantised to E4M3 per row as well (moe_quantize_act_rows)."""
+    _forward_q("moe_forward_w8a8", x_perm, offsets, W1q, s1, W2q, s2, pair_row, topk_w, x, W1sq, s1s, W2sq, s2s,
+               shared_gate_w, out, ws, stream)
+
+
+def _forward_q(fn, x_perm, offsets, W1q, s1, W2q, s2, pair_row, topk_w, x, W1sq, s1s, W2sq, s2s, shared_gate_w,
+               out, ws, stream):
     P_cap, H = x_perm.shape
     S_local = offsets.shape[0] - 1
     I = W2q.shape[2]
     T, k = pair_row.shape
     I_sh = 0 if W2sq is None else W2sq.shape[1]
     u8 = torch.uint8
-    st = _lib.moe_forward_fp8(_ptr(x_perm, "x_perm", _bf16), _ptr(offsets, "offsets", _i32), S_local, P_cap,
+    st = getattr(_lib, fn)(_ptr(x_perm, "x_perm", _bf16), _ptr(offsets, "offsets", _i32), S_local, P_cap,
                               _ptr(W1q, "W1q", u8, (S_local, 2 * I, H)), _ptr(s1, "W1_scale", _f32, (S_local, 2 * I)),
                               _ptr(W2q, "W2q", u8, (S_local, H, I)), _ptr(s2, "W2_scale", _f32, (S_local, H)), H, I,
                               _ptr(pair_row, "pair_row", _i32), _ptr(topk_w, "topk_w", _f32, (T, k), allow_none=True),
@@ -250,7 +270,7 @@ def moe_forward_fp8(x_perm, offsets, W1q, s1, W2q, s2, pair_row, topk_w, x, W1sq
                               _ptr(shared_gate_w, "shared_gate_w", _bf16, (H,), allow_none=True),
                               _ptr(out, "out", _bf16, (T, H)), _ptr(ws, "ws", torch.uint8), ws.numel(),
                               _stream(stream))
-    _check("moe_forward_fp8", st)
+    _check(fn, st)
 
 
 def moe_grouped_fc1_fp8(a, offsets, W1q, s1, a_shared, W1sq, s1s, h, h_shared, ws, stream=None):
@@ -287,6 +307,60 @@ def moe_grouped_fc2_fp8(h, offsets, W2q, s2, h_shared, W2sq, s2s, y, y_shared, w
                                   _ptr(y_shared, "y_shared", _bf16, (T, H), allow_none=True),
                                   _ptr(ws, "ws", torch.uint8), ws.numel(), _stream(stream))
     _check("moe_grouped_fc2_fp8", st)
+
+
+def moe_grouped_fc1_w8a8(aq, a_scale, offsets, W1q, s1, a_shared_q, a_shared_scale, W1sq, s1s, h, h_shared, ws,
+                         stream=None):
+    """FC1 + SwiGLU on E4M3 activation rows (with their scales) and E4M3 weights."""
+    rows_cap, H = aq.shape
+    G = offsets.shape[0] - 1
+    I = W1q.shape[1] // 2
+    T = 0 if a_shared_q is None else a_shared_q.shape[0]
+    I_sh = 0 if W1sq is None else W1sq.shape[0] // 2
+    u8 = torch.uint8
+    st = _lib.moe_grouped_fc1_w8a8(_ptr(aq, "aq", u8), _ptr(a_scale, "a_scale", _f32, (rows_cap,)), rows_cap,
+                                   _ptr(offsets, "offsets", _i32), G,
+                                   _ptr(W1q, "W1q", u8, (G, 2 * I, H)), _ptr(s1, "W1_scale", _f32, (G, 2 * I)), H, I,
+                                   _ptr(a_shared_q, "a_shared_q", u8, (T, H), allow_none=True),
+                                   _ptr(a_shared_scale, "a_shared_scale", _f32, (T,), allow_none=True), T,
+                                   _ptr(W1sq, "W1sq", u8, (2 * I_sh, H), allow_none=True),
+                                   _ptr(s1s, "W1s_scale", _f32, (2 * I_sh,), allow_none=True), I_sh,
+                                   _ptr(h, "h", _bf16, (rows_cap, I)),
+                                   _ptr(h_shared, "h_shared", _bf16, (T, I_sh), allow_none=True),
+                                   _ptr(ws, "ws", torch.uint8), ws.numel(), _stream(stream))
+    _check("moe_grouped_fc1_w8a8", st)
+
+
+def moe_grouped_fc2_w8a8(hq, h_scale, offsets, W2q, s2, h_shared_q, h_shared_scale, W2sq, s2s, y, y_shared, ws,
+                         stream=None):
+    """FC2 on E4M3 intermediate rows (with their scales) and E4M3 weights."""
+    rows_cap, I = hq.shape
+    G = offsets.shape[0] - 1
+    H = W2q.shape[1]
+    T = 0 if h_shared_q is None else h_shared_q.shape[0]
+    I_sh = 0 if W2sq is None else W2sq.shape[1]
+    u8 = torch.uint8
+    st = _lib.moe_grouped_fc2_w8a8(_ptr(hq, "hq", u8), _ptr(h_scale, "h_scale", _f32, (rows_cap,)), rows_cap,
+                                   _ptr(offsets, "offsets", _i32), G,
+                                   _ptr(W2q, "W2q", u8, (G, H, I)), _ptr(s2, "W2_scale", _f32, (G, H)), H, I,
+                                   _ptr(h_shared_q, "h_shared_q", u8, (T, I_sh), allow_none=True),
+                                   _ptr(h_shared_scale, "h_shared_scale", _f32, (T,), allow_none=True), T,
+                                   _ptr(W2sq, "W2sq", u8, (H, I_sh), allow_none=True),
+                                   _ptr(s2s, "W2s_scale", _f32, (H,), allow_none=True), I_sh,
+                                   _ptr(y, "y", _bf16, (rows_cap, H)),
+                                   _ptr(y_shared, "y_shared", _bf16, (T, H), allow_none=True),
+                                   _ptr(ws, "ws", torch.uint8), ws.numel(), _stream(stream))
+    _check("moe_grouped_fc2_w8a8", st)
+
+
+def moe_quantize_act_rows(v, q, scale, stream=None):
+    """Row-wise E4M3 quantisation of activations [..., K] bf16 with power-of-two scales into q (uint8, same
+    shape) and scale ([...] fp32)."""
+    K = v.shape[-1]
+    rows = v.numel() // K
+    st = _lib.moe_quantize_act_rows(_ptr(v, "v", _bf16), rows, K, _ptr(q, "q", torch.uint8, tuple(v.shape)),
+                                    _ptr(scale, "scale", _f32, tuple(v.shape[:-1])), _stream(stream))
+    _check("moe_quantize_act_rows", st)
 
 
 def moe_quantize_fp8_rows(w, q, scale, stream=None):

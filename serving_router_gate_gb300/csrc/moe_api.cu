@@ -44,7 +44,10 @@ int shared_split(int64_t T, int I, int I_sh) {
 }
 
 struct ForwardLayout {
-    size_t h, h_sh, y, y_sh, y_sh_part, total;
+    size_t h, h_sh, y, y_sh, y_sh_part;
+    // E4M3 activations: quantised expert inputs, shared input, intermediates, and scales
+    size_t xq, sxq, xsq, sxs, hq, shq, hsq, shs;
+    size_t total;
 };
 
 ForwardLayout forward_layout(int64_t P_cap, int64_t T, int H, int I, int I_sh) {
@@ -61,6 +64,23 @@ ForwardLayout forward_layout(int64_t P_cap, int64_t T, int H, int I, int I_sh) {
     L.y_sh_part = off;
     const int ks = shared_split(T, I, I_sh);
     off += a256(ks > 1 ? (size_t)ks * (size_t)T * (size_t)H * 4 : 0);
+    const size_t T_sh = I_sh > 0 ? (size_t)T : 0;
+    L.xq = off;
+    off += a256((size_t)P_cap * (size_t)H);
+    L.sxq = off;
+    off += a256((size_t)P_cap * 4);
+    L.xsq = off;
+    off += a256(T_sh * (size_t)H);
+    L.sxs = off;
+    off += a256(T_sh * 4);
+    L.hq = off;
+    off += a256((size_t)P_cap * (size_t)I);
+    L.shq = off;
+    off += a256((size_t)P_cap * 4);
+    L.hsq = off;
+    off += a256(T_sh * (size_t)(I_sh > 0 ? I_sh : 0));
+    L.shs = off;
+    off += a256(T_sh * 4);
     L.total = off;
     return L;
 }
@@ -273,7 +293,8 @@ static moe_status_t gemm_call(bool fc1, const moe_bf16_t* a, int64_t rows_cap, c
                               const moe_bf16_t* Ws, int I_sh, moe_bf16_t* out, moe_bf16_t* out_sh, void* ws,
                               cudaStream_t s, float* out_sh_part = nullptr, int ksplit_sh = 1,
                               int64_t max_group_rows = -1, const float* b_scale = nullptr,
-                              const float* b_scale_sh = nullptr) {
+                              const float* b_scale_sh = nullptr, const float* a_scale = nullptr,
+                              const float* a_scale_sh = nullptr) {
     GemmLaunch L;
     L.swiglu = fc1;
     L.a = a;
@@ -299,10 +320,13 @@ static moe_status_t gemm_call(bool fc1, const moe_bf16_t* a, int64_t rows_cap, c
     L.pair_mode = g_pair_mode.load();
     // a token adds at most one row to a slot, so a group has at most T rows
     L.max_group_rows = max_group_rows >= 0 ? std::min<int64_t>(max_group_rows, rows_cap) : rows_cap;
-    // E4M3 weights come with their row scales (W and Ws then point to bytes)
-    L.b_fp8 = b_scale != nullptr;
+    // E4M3 weights come with their row scales (W and Ws then point to bytes), E4M3
+    // activations with theirs (a and a_sh then point to bytes)
+    L.quant = a_scale ? GEMM_W8A8 : (b_scale ? GEMM_W8 : GEMM_BF16);
     L.b_scale = b_scale;
     L.b_scale_sh = b_scale_sh;
+    L.a_scale = a_scale;
+    L.a_scale_sh = a_scale_sh;
     const char* why = nullptr;
     return cuda_status(launch_grouped_gemm(L, device_sms(), s, &why));
 }
@@ -393,6 +417,42 @@ moe_status_t moe_grouped_fc2_fp8(const moe_bf16_t* h, int64_t rows_cap, const in
                      nullptr, 1, -1, W2_scale, W2s_scale);
 }
 
+moe_status_t moe_grouped_fc1_w8a8(const uint8_t* aq, const float* a_scale, int64_t rows_cap, const int32_t* offsets,
+                                  int G, const uint8_t* W1q, const float* W1_scale, int H, int I,
+                                  const uint8_t* a_shared_q, const float* a_shared_scale, int64_t T, const uint8_t* W1sq,
+                                  const float* W1s_scale, int I_shared_total, moe_bf16_t* h, moe_bf16_t* h_shared,
+                                  void* ws, size_t ws_bytes, moe_stream_t stream) {
+    const moe_bf16_t* a = reinterpret_cast<const moe_bf16_t*>(aq);
+    const moe_bf16_t* a_sh = reinterpret_cast<const moe_bf16_t*>(a_shared_q);
+    moe_status_t st = check_gemm_args(a, rows_cap, offsets, G, reinterpret_cast<const moe_bf16_t*>(W1q), H, I, a_sh, T,
+                                      reinterpret_cast<const moe_bf16_t*>(W1sq), I_shared_total, h, h_shared, ws,
+                                      ws_bytes);
+    if (st != MOE_OK) return st;
+    if (!W1_scale || !a_scale || (I_shared_total > 0 && T > 0 && (!W1s_scale || !a_shared_scale)))
+        return MOE_ERR_INVALID_ARG;
+    return gemm_call(true, a, rows_cap, offsets, G, reinterpret_cast<const moe_bf16_t*>(W1q), H, I, a_sh, T,
+                     reinterpret_cast<const moe_bf16_t*>(W1sq), I_shared_total, h, h_shared, ws, (cudaStream_t)stream,
+                     nullptr, 1, -1, W1_scale, W1s_scale, a_scale, a_shared_scale);
+}
+
+moe_status_t moe_grouped_fc2_w8a8(const uint8_t* hq, const float* h_scale, int64_t rows_cap, const int32_t* offsets,
+                                  int G, const uint8_t* W2q, const float* W2_scale, int H, int I,
+                                  const uint8_t* h_shared_q, const float* h_shared_scale, int64_t T,
+                                  const uint8_t* W2sq, const float* W2s_scale, int I_shared_total, moe_bf16_t* y,
+                                  moe_bf16_t* y_shared, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    const moe_bf16_t* a = reinterpret_cast<const moe_bf16_t*>(hq);
+    const moe_bf16_t* a_sh = reinterpret_cast<const moe_bf16_t*>(h_shared_q);
+    moe_status_t st = check_gemm_args(a, rows_cap, offsets, G, reinterpret_cast<const moe_bf16_t*>(W2q), H, I, a_sh, T,
+                                      reinterpret_cast<const moe_bf16_t*>(W2sq), I_shared_total, y, y_shared, ws,
+                                      ws_bytes);
+    if (st != MOE_OK) return st;
+    if (!W2_scale || !h_scale || (I_shared_total > 0 && T > 0 && (!W2s_scale || !h_shared_scale)))
+        return MOE_ERR_INVALID_ARG;
+    return gemm_call(false, a, rows_cap, offsets, G, reinterpret_cast<const moe_bf16_t*>(W2q), H, I, a_sh, T,
+                     reinterpret_cast<const moe_bf16_t*>(W2sq), I_shared_total, y, y_shared, ws, (cudaStream_t)stream,
+                     nullptr, 1, -1, W2_scale, W2s_scale, h_scale, h_shared_scale);
+}
+
 moe_status_t moe_finalize(const moe_bf16_t* y, int64_t rows_cap, const int32_t* pair_row, const float* topk_w,
                           int64_t T, int k, int H, const moe_bf16_t* y_shared, const moe_bf16_t* x,
                           const moe_bf16_t* shared_gate_w, moe_bf16_t* out, void* ws, size_t ws_bytes,
@@ -407,13 +467,15 @@ moe_status_t moe_finalize(const moe_bf16_t* y, int64_t rows_cap, const int32_t* 
                          (cudaStream_t)stream);
 }
 
-// moe_forward with bf16 weights (s1 == nullptr) or E4M3 weights with row scales.
+// moe_forward with bf16 weights (s1 == nullptr) or E4M3 weights with row scales,
+// and (act8) E4M3 activations.
 static moe_status_t forward_impl(const moe_bf16_t* x_perm, const int32_t* offsets, int S_local, int64_t P_cap,
                                  const void* W1, const float* s1, const void* W2, const float* s2, int H, int I,
                                  const int32_t* pair_row, const float* topk_w, int64_t T, int k,
                                  const moe_bf16_t* x, const void* W1s, const float* s1s, const void* W2s,
                                  const float* s2s, int I_shared_total, const moe_bf16_t* shared_gate_w,
-                                 moe_bf16_t* out, void* ws, size_t ws_bytes, moe_stream_t stream) {
+                                 moe_bf16_t* out, void* ws, size_t ws_bytes, moe_stream_t stream,
+                                 bool act8 = false) {
     if (T < 0 || k <= 0 || S_local <= 0 || P_cap < 0 || H <= 0 || I <= 0 || I_shared_total < 0)
         return MOE_ERR_INVALID_ARG;
     if (!dim_ok(H) || !dim_ok(I) || (I_shared_total > 0 && !dim_ok(I_shared_total)) || k > 32 || S_local > 1024 ||
@@ -433,14 +495,41 @@ static moe_status_t forward_impl(const moe_bf16_t* x_perm, const int32_t* offset
     moe_bf16_t* y = reinterpret_cast<moe_bf16_t*>(base + FL.y);
     moe_bf16_t* y_sh = I_shared_total > 0 ? reinterpret_cast<moe_bf16_t*>(base + FL.y_sh) : nullptr;
     cudaStream_t s = (cudaStream_t)stream;
-    moe_status_t st = gemm_call(true, x_perm, P_cap, offsets, S_local, static_cast<const moe_bf16_t*>(W1), H, I, x,
-                                T, static_cast<const moe_bf16_t*>(W1s), I_shared_total, h, h_sh, ws, s, nullptr, 1, T,
-                                s1, s1s);
-    if (st != MOE_OK) return st;
     const int ks = shared_split(T, I, I_shared_total);
     float* y_sh_part = ks > 1 ? reinterpret_cast<float*>(base + FL.y_sh_part) : nullptr;
-    st = gemm_call(false, h, P_cap, offsets, S_local, static_cast<const moe_bf16_t*>(W2), H, I, h_sh, T,
-                   static_cast<const moe_bf16_t*>(W2s), I_shared_total, y, y_sh, ws, s, y_sh_part, ks, T, s2, s2s);
+    moe_status_t st;
+    if (act8) {
+        // E4M3 activations: quantise the expert input rows (as many as offsets[S_local]
+        // says, read on the device) and the shared experts' input, run FC1 on them,
+        // quantise the intermediate rows, run FC2
+        const int sms = device_sms();
+        const int64_t T_sh = I_shared_total > 0 ? T : 0;
+        auto u8 = [&](size_t off) { return reinterpret_cast<uint8_t*>(base + off); };
+        auto f32 = [&](size_t off) { return reinterpret_cast<float*>(base + off); };
+        const ActQuantSeg qx[2] = {{x_perm, P_cap, offsets + S_local, H, u8(FL.xq), f32(FL.sxq)},
+                                   {x, T_sh, nullptr, H, u8(FL.xsq), f32(FL.sxs)}};
+        st = cuda_status(launch_quantize_act_rows(qx, 2, sms, s));
+        if (st != MOE_OK) return st;
+        st = gemm_call(true, reinterpret_cast<const moe_bf16_t*>(u8(FL.xq)), P_cap, offsets, S_local,
+                       static_cast<const moe_bf16_t*>(W1), H, I, reinterpret_cast<const moe_bf16_t*>(u8(FL.xsq)), T,
+                       static_cast<const moe_bf16_t*>(W1s), I_shared_total, h, h_sh, ws, s, nullptr, 1, T, s1, s1s,
+                       f32(FL.sxq), f32(FL.sxs));
+        if (st != MOE_OK) return st;
+        const ActQuantSeg qh[2] = {{h, P_cap, offsets + S_local, I, u8(FL.hq), f32(FL.shq)},
+                                   {h_sh, T_sh, nullptr, I_shared_total, u8(FL.hsq), f32(FL.shs)}};
+        st = cuda_status(launch_quantize_act_rows(qh, 2, sms, s));
+        if (st != MOE_OK) return st;
+        st = gemm_call(false, reinterpret_cast<const moe_bf16_t*>(u8(FL.hq)), P_cap, offsets, S_local,
+                       static_cast<const moe_bf16_t*>(W2), H, I, reinterpret_cast<const moe_bf16_t*>(u8(FL.hsq)), T,
+                       static_cast<const moe_bf16_t*>(W2s), I_shared_total, y, y_sh, ws, s, y_sh_part, ks, T, s2,
+                       s2s, f32(FL.shq), f32(FL.shs));
+    } else {
+        st = gemm_call(true, x_perm, P_cap, offsets, S_local, static_cast<const moe_bf16_t*>(W1), H, I, x, T,
+                       static_cast<const moe_bf16_t*>(W1s), I_shared_total, h, h_sh, ws, s, nullptr, 1, T, s1, s1s);
+        if (st != MOE_OK) return st;
+        st = gemm_call(false, h, P_cap, offsets, S_local, static_cast<const moe_bf16_t*>(W2), H, I, h_sh, T,
+                       static_cast<const moe_bf16_t*>(W2s), I_shared_total, y, y_sh, ws, s, y_sh_part, ks, T, s2, s2s);
+    }
     if (st != MOE_OK) return st;
     return finalize_call(y, P_cap, pair_row, topk_w, T, k, H, y_sh_part ? nullptr : y_sh, y_sh_part, ks, x,
                          shared_gate_w, out, ws, s);
@@ -465,6 +554,28 @@ moe_status_t moe_forward_fp8(const moe_bf16_t* x_perm, const int32_t* offsets, i
     return forward_impl(x_perm, offsets, S_local, P_cap, W1q, W1_scale, W2q, W2_scale, H, I, pair_row, topk_w, T, k,
                         x, W1sq, W1s_scale, W2sq, W2s_scale, I_shared_total, shared_gate_w, out, ws, ws_bytes,
                         stream);
+}
+
+moe_status_t moe_forward_w8a8(const moe_bf16_t* x_perm, const int32_t* offsets, int S_local, int64_t P_cap,
+                              const uint8_t* W1q, const float* W1_scale, const uint8_t* W2q, const float* W2_scale,
+                              int H, int I, const int32_t* pair_row, const float* topk_w, int64_t T, int k,
+                              const moe_bf16_t* x, const uint8_t* W1sq, const float* W1s_scale, const uint8_t* W2sq,
+                              const float* W2s_scale, int I_shared_total, const moe_bf16_t* shared_gate_w,
+                              moe_bf16_t* out, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    if (!W1_scale || !W2_scale) return MOE_ERR_INVALID_ARG;
+    return forward_impl(x_perm, offsets, S_local, P_cap, W1q, W1_scale, W2q, W2_scale, H, I, pair_row, topk_w, T, k,
+                        x, W1sq, W1s_scale, W2sq, W2s_scale, I_shared_total, shared_gate_w, out, ws, ws_bytes,
+                        stream, true);
+}
+
+moe_status_t moe_quantize_act_rows(const moe_bf16_t* v, int64_t rows, int K, uint8_t* q, float* scale,
+                                   moe_stream_t stream) {
+    if (rows < 0 || K <= 0) return MOE_ERR_INVALID_ARG;
+    if (K % 64 != 0) return MOE_ERR_UNSUPPORTED;
+    if (rows == 0) return MOE_OK;
+    if (!v || !q || !scale) return MOE_ERR_INVALID_ARG;
+    const ActQuantSeg seg = {v, rows, nullptr, K, q, scale};
+    return cuda_status(launch_quantize_act_rows(&seg, 1, device_sms(), (cudaStream_t)stream));
 }
 
 moe_status_t moe_quantize_fp8_rows(const moe_bf16_t* w, int64_t rows, int K, uint8_t* q, float* scale,

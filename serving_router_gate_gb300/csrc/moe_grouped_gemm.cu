@@ -33,6 +33,12 @@
 // consecutive m-tiles of one (slot, n-tile); an odd leftover m-tile leaves the
 // second CTA without rows (its half is computed and discarded).  Single mode
 // (one CTA per tile, 4 stages of 48 KB) serves small launches.
+// E4M3 weights (quant GEMM_W8): 8 more warps widen each E4M3 weight tile to bf16
+// in shared memory before the MMA reads it.  E4M3 weights and activations
+// (GEMM_W8A8): the TMA loads 128-byte rows of E4M3 bytes (128 elements per K
+// step instead of 64, same bytes per stage), tcgen05.mma.kind::f8f6f4 (K = 32)
+// consumes them directly, and the epilogue scales each accumulator by its A
+// row's and its B row's scale.
 // Tiles: an optional dense "shared expert" problem (M = T) first, then the
 // routed problem, whose ragged per-slot row counts are read on the device from
 // the offsets array (no host synchronisation): slot g has ceil(M_g / 128)
@@ -78,6 +84,7 @@ struct Cfg {
     static constexpr int TMEM_COLS = 2 * BN;  // two accumulators of BN fp32 columns
     // 2-CTA MMA: M = 256 across the pair
     static constexpr uint32_t IDESC = idesc_bf16_f32(kPair ? 2 * BM : BM, BN);
+    static constexpr uint32_t IDESC8 = idesc_e4m3_f32(BM, BN);
 };
 
 struct GemmParams {
@@ -92,6 +99,9 @@ struct GemmParams {
     uint16_t* out_sh;
     const float* scale;      // E4M3 weights: fp32 scale per B row, [G][Nb] (null: bf16 weights)
     const float* scale_sh;   // [Nb_sh]
+    const float* a_scale;    // E4M3 activations: fp32 scale per A row, [rows_cap]
+    const float* a_scale_sh; // [T_sh]
+    int kb_total, kb_total_sh;  // K steps of the routed and the shared problem
     int Nb;                  // B rows per group
     float* out_sh_part;      // FC2, split shared problem: fp32 partials [ksplit_sh, T_sh, N_out_sh]
     int ksplit_sh;           // K ranges of the shared problem (1: not split)
@@ -152,7 +162,7 @@ __device__ __forceinline__ Tile tile_of(int u, const GemmParams& p, const SmemMe
         tl.row0 = mt * BM;
         tl.rows_valid = (int)max((int64_t)0, min((int64_t)BM, p.T_sh - (int64_t)mt * BM));
         tl.kb0 = tl.ks * p.kb_split_sh;
-        tl.kb1 = min(p.K_sh / BK, tl.kb0 + p.kb_split_sh);
+        tl.kb1 = min(p.kb_total_sh, tl.kb0 + p.kb_split_sh);
         return tl;
     }
     u -= n_sh_tiles;
@@ -176,7 +186,7 @@ __device__ __forceinline__ Tile tile_of(int u, const GemmParams& p, const SmemMe
     tl.rows_valid = max(0, min(BM, M - mt * BM));
     tl.ks = 0;
     tl.kb0 = 0;
-    tl.kb1 = p.K / BK;
+    tl.kb1 = p.kb_total;
     return tl;
 }
 
@@ -214,8 +224,8 @@ __device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t x, uint32_t& o0, uint3
     }
 }
 
-template <bool kFC1, bool kPair, int BN, bool kShort, bool kFp8>
-__global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
+template <bool kFC1, bool kPair, int BN, bool kShort, int kQ>
+__global__ void __launch_bounds__(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmAs,
                         const __grid_constant__ CUtensorMap tmBs, const __grid_constant__ CUtensorMap tmA32,
@@ -227,7 +237,11 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
     constexpr uint32_t IDESC = C::IDESC;
     constexpr int TMEM_COLS = C::TMEM_COLS;
     static_assert(!kShort || !kPair, "short tiles run in single mode");
+    constexpr bool kFp8 = kQ == GEMM_W8;      // E4M3 weights widened by converter warps
+    constexpr bool kA8 = kQ == GEMM_W8A8;     // E4M3 A and B on kind::f8f6f4
+    constexpr int KE = kA8 ? 2 * BK : BK;     // elements per K step (one 128-byte row)
     static_assert(!kFp8 || (!kPair && BN == 256), "E4M3 weights run in single mode with N = 256");
+    static_assert(!kA8 || !kPair, "E4M3 activations run in single mode");
     static_assert(!kPair || BN == 256, "pair mode uses N = 256");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -356,28 +370,28 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
                         const uint32_t lead_full = mapa_shared(&m.full[stage], 0);
                         if (crank == 0) mbar_arrive_expect_tx(&m.full[stage], pair_bytes);
                         const int brow = kFC1 ? (crank ? up : 0) + tl.nt * (BN / 2) : tl.nt * BN + crank * (BN / 2);
-                        tma_load_2d_pair(a_dst, mA, lead_full, kb * BK, tl.row0);
-                        tma_load_3d_pair(b_dst, mB, lead_full, kb * BK, brow, tl.g);
+                        tma_load_2d_pair(a_dst, mA, lead_full, kb * KE, tl.row0);
+                        tma_load_3d_pair(b_dst, mB, lead_full, kb * KE, brow, tl.g);
                     } else if (kFp8) {
                         // E4M3 rows of 64 bytes, dense, in the first half of the B slot (FC1:
                         // the gate rows, then the up rows); the converters widen them in place
                         mbar_arrive_expect_tx(&m.full[stage], a_bytes + BN * BK);
-                        tma_load_2d(a_dst, mA, &m.full[stage], kb * BK, tl.row0);
+                        tma_load_2d(a_dst, mA, &m.full[stage], kb * KE, tl.row0);
                         if (kFC1) {
-                            tma_load_3d(b_dst, mB, &m.full[stage], kb * BK, tl.nt * (BN / 2), tl.g);
-                            tma_load_3d(b_dst + (BN / 2) * BK, mB, &m.full[stage], kb * BK, up + tl.nt * (BN / 2), tl.g);
+                            tma_load_3d(b_dst, mB, &m.full[stage], kb * KE, tl.nt * (BN / 2), tl.g);
+                            tma_load_3d(b_dst + (BN / 2) * BK, mB, &m.full[stage], kb * KE, up + tl.nt * (BN / 2), tl.g);
                         } else {
-                            tma_load_3d(b_dst, mB, &m.full[stage], kb * BK, tl.nt * BN, tl.g);
+                            tma_load_3d(b_dst, mB, &m.full[stage], kb * KE, tl.nt * BN, tl.g);
                         }
                     } else if (kFC1) {
                         mbar_arrive_expect_tx(&m.full[stage], a_bytes + B_BYTES);
-                        tma_load_2d(a_dst, mA, &m.full[stage], kb * BK, tl.row0);
-                        tma_load_3d(b_dst, mB, &m.full[stage], kb * BK, tl.nt * (BN / 2), tl.g);
-                        tma_load_3d(b_dst + B_BYTES / 2, mB, &m.full[stage], kb * BK, up + tl.nt * (BN / 2), tl.g);
+                        tma_load_2d(a_dst, mA, &m.full[stage], kb * KE, tl.row0);
+                        tma_load_3d(b_dst, mB, &m.full[stage], kb * KE, tl.nt * (BN / 2), tl.g);
+                        tma_load_3d(b_dst + B_BYTES / 2, mB, &m.full[stage], kb * KE, up + tl.nt * (BN / 2), tl.g);
                     } else {
                         mbar_arrive_expect_tx(&m.full[stage], a_bytes + B_BYTES);
-                        tma_load_2d(a_dst, mA, &m.full[stage], kb * BK, tl.row0);
-                        tma_load_3d(b_dst, mB, &m.full[stage], kb * BK, tl.nt * BN, tl.g);
+                        tma_load_2d(a_dst, mA, &m.full[stage], kb * KE, tl.row0);
+                        tma_load_3d(b_dst, mB, &m.full[stage], kb * KE, tl.nt * BN, tl.g);
                     }
                     ++issued;
                     if (++stage == STAGES) {
@@ -431,10 +445,13 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
                     const uint32_t b0 = smem_u32(smB + (size_t)stage * B_BYTES);
 #pragma unroll
                     for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                        // 32 bytes of each 128-byte row per MMA: K = 16 bf16 or 32 E4M3
                         const uint64_t ad = sw128_kmajor_desc(a0 + kk * UMMA_K * 2);
                         const uint64_t bd = sw128_kmajor_desc(b0 + kk * UMMA_K * 2);
                         if (kPair)
                             tc_mma_bf16_pair(d, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+                        else if (kA8)
+                            tc_mma_e4m3(d, ad, bd, C::IDESC8, (kb | kk) != 0 ? 1u : 0u);
                         else
                             tc_mma_bf16(d, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
                     }
@@ -491,10 +508,13 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
             const int N_out = tl.prob ? p.N_out_sh : p.N_out;
             uint16_t* out = tl.prob ? p.out_sh : p.out;
             uint16_t* orow = out + (int64_t)(tl.row0 + row_in) * N_out;
-            // E4M3 weights: the accumulator of output column n carries B row n's scale
-            const float* srow = kFp8 ? (tl.prob ? p.scale_sh : p.scale + (int64_t)tl.g * p.Nb) : nullptr;
+            // E4M3 weights: the accumulator of output column n carries B row n's scale;
+            // E4M3 activations: and its A row's scale (a power of two)
+            const float* srow = (kFp8 || kA8) ? (tl.prob ? p.scale_sh : p.scale + (int64_t)tl.g * p.Nb) : nullptr;
             const int sup = tl.prob ? p.up_off_sh : p.up_off;
-            auto bscale = [&](int row) -> float { return kFp8 ? __ldg(srow + row) : 1.0f; };
+            const float asc =
+                (kA8 && valid) ? __ldg((tl.prob ? p.a_scale_sh : p.a_scale) + tl.row0 + row_in) : 1.0f;
+            auto bscale = [&](int row) -> float { return (kFp8 || kA8) ? __ldg(srow + row) : 1.0f; };
             if (kFC1) {
 #pragma unroll 1
                 for (int c = 0; c < OW; c += 32) {
@@ -510,8 +530,8 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
                             float h2[2];
 #pragma unroll
                             for (int z = 0; z < 2; ++z) {
-                                const float gv = __uint_as_float(g[2 * e + z]) * bscale(col + 2 * e + z);
-                                const float uv = __uint_as_float(v[2 * e + z]) * bscale(sup + col + 2 * e + z);
+                                const float gv = __uint_as_float(g[2 * e + z]) * bscale(col + 2 * e + z) * asc;
+                                const float uv = __uint_as_float(v[2 * e + z]) * bscale(sup + col + 2 * e + z) * asc;
                                 // silu(g) * u; the product is rounded to bf16 (8 bits),
                                 // far coarser than the approximate exp / divide
                                 h2[z] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
@@ -526,8 +546,10 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
                 }
             } else if (tl.prob && p.ksplit_sh > 1) {
                 // K range ks of a split shared tile: fp32 partial sums, added up in fixed
-                // range order by the combine
+                // range order by the combine; a range past the last K step (more ranges
+                // than K steps allow) issued no MMA and contributes zeros
                 float* prow = p.out_sh_part + ((int64_t)tl.ks * p.T_sh + tl.row0 + row_in) * N_out;
+                const float kz = tl.kb1 > tl.kb0 ? 1.0f : 0.0f;
 #pragma unroll 1
                 for (int c = 0; c < OW; c += 32) {
                     uint32_t r[32];
@@ -538,10 +560,12 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
                         float4* dst = reinterpret_cast<float4*>(prow + col);
 #pragma unroll
                         for (int e = 0; e < 8; ++e)
-                            dst[e] = make_float4(__uint_as_float(r[4 * e]) * bscale(col + 4 * e),
-                                                 __uint_as_float(r[4 * e + 1]) * bscale(col + 4 * e + 1),
-                                                 __uint_as_float(r[4 * e + 2]) * bscale(col + 4 * e + 2),
-                                                 __uint_as_float(r[4 * e + 3]) * bscale(col + 4 * e + 3));
+                            dst[e] = kz == 0.0f
+                                         ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                         : make_float4(__uint_as_float(r[4 * e]) * bscale(col + 4 * e) * asc,
+                                                       __uint_as_float(r[4 * e + 1]) * bscale(col + 4 * e + 1) * asc,
+                                                       __uint_as_float(r[4 * e + 2]) * bscale(col + 4 * e + 2) * asc,
+                                                       __uint_as_float(r[4 * e + 3]) * bscale(col + 4 * e + 3) * asc);
                     }
                 }
             } else {
@@ -555,8 +579,8 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
                         uint32_t pk[16];
 #pragma unroll
                         for (int e = 0; e < 16; ++e)
-                            pk[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * bscale(col + 2 * e),
-                                                __uint_as_float(r[2 * e + 1]) * bscale(col + 2 * e + 1));
+                            pk[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * bscale(col + 2 * e) * asc,
+                                                __uint_as_float(r[2 * e + 1]) * bscale(col + 2 * e + 1) * asc);
                         uint4* dst = reinterpret_cast<uint4*>(orow + col);
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
@@ -678,14 +702,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+// bf16 (u8 = false) or byte (u8 = true) matrix [outer, inner]: boxes of one
+// 128-byte row (64 bf16 or 128 bytes) x box_outer rows, 128-byte swizzle
+bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer,
+               bool u8 = false) {
     auto fn = encode_fn();
     if (!fn) return false;
+    const uint64_t es_bytes = u8 ? 1 : 2;
     cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {inner * 2};
-    cuuint32_t box[2] = {(cuuint32_t)BK, box_outer};
+    cuuint64_t strides[1] = {inner * es_bytes};
+    cuuint32_t box[2] = {(cuuint32_t)(128 / es_bytes), box_outer};
     cuuint32_t es[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+    return fn(map, u8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -705,15 +733,18 @@ bool encode_3d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t r
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// bf16 or byte matrices [groups, rows, inner]: boxes of one 128-byte row x
+// box_rows rows of one group, 128-byte swizzle
 bool encode_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t groups,
-               uint32_t box_rows) {
+               uint32_t box_rows, bool u8 = false) {
     auto fn = encode_fn();
     if (!fn) return false;
+    const uint64_t es_bytes = u8 ? 1 : 2;
     cuuint64_t dims[3] = {inner, rows, groups};
-    cuuint64_t strides[2] = {inner * 2, rows * inner * 2};
-    cuuint32_t box[3] = {(cuuint32_t)BK, box_rows, 1};
+    cuuint64_t strides[2] = {inner * es_bytes, rows * inner * es_bytes};
+    cuuint32_t box[3] = {(cuuint32_t)(128 / es_bytes), box_rows, 1};
     cuuint32_t es[3] = {1, 1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+    return fn(map, u8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -725,7 +756,7 @@ struct KernelInfo {
     int max_clusters = 0;
 };
 
-template <bool kFC1, bool kPair, int BN, bool kShort, bool kFp8>
+template <bool kFC1, bool kPair, int BN, bool kShort, int kQ>
 cudaError_t kernel_info(int num_sms, KernelInfo* out) {
     static std::mutex mu;
     static KernelInfo info[64];
@@ -735,14 +766,14 @@ cudaError_t kernel_info(int num_sms, KernelInfo* out) {
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(mu);
     if (!info[dev].ready) {
-        err = cudaFuncSetAttribute(grouped_gemm_kernel<kFC1, kPair, BN, kShort, kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        err = cudaFuncSetAttribute(grouped_gemm_kernel<kFC1, kPair, BN, kShort, kQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    (int)smem_bytes<kPair, BN, kShort>());
         if (err != cudaSuccess) return err;
         int clusters = 0;
         if (kPair) {
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(2 * num_sms);
-            cfg.blockDim = dim3(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS);
+            cfg.blockDim = dim3(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS);
             cfg.dynamicSmemBytes = smem_bytes<kPair, BN, kShort>();
             cudaLaunchAttribute attr;
             attr.id = cudaLaunchAttributeClusterDimension;
@@ -751,7 +782,7 @@ cudaError_t kernel_info(int num_sms, KernelInfo* out) {
             attr.val.clusterDim.z = 1;
             cfg.attrs = &attr;
             cfg.numAttrs = 1;
-            err = cudaOccupancyMaxActiveClusters(&clusters, grouped_gemm_kernel<kFC1, kPair, BN, kShort, kFp8>, &cfg);
+            err = cudaOccupancyMaxActiveClusters(&clusters, grouped_gemm_kernel<kFC1, kPair, BN, kShort, kQ>, &cfg);
             if (err != cudaSuccess) return err;
         }
         info[dev].max_clusters = clusters;
@@ -761,13 +792,13 @@ cudaError_t kernel_info(int num_sms, KernelInfo* out) {
     return cudaSuccess;
 }
 
-template <bool kFC1, bool kPair, int BN, bool kShort, bool kFp8>
+template <bool kFC1, bool kPair, int BN, bool kShort, int kQ>
 cudaError_t launch_kernel(const GemmParams& p, const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mAs,
                           const CUtensorMap& mBs, const CUtensorMap& mA32, const CUtensorMap& mAs32, unsigned grid,
                           cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS);
+    cfg.blockDim = dim3(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS);
     cfg.dynamicSmemBytes = smem_bytes<kPair, BN, kShort>();
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
@@ -787,11 +818,11 @@ cudaError_t launch_kernel(const GemmParams& p, const CUtensorMap& mA, const CUte
     cfg.attrs = attr;
     cfg.numAttrs = n;
     count_launch();
-    return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<kFC1, kPair, BN, kShort, kFp8>, p, mA, mB, mAs, mBs, mA32, mAs32);
+    return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<kFC1, kPair, BN, kShort, kQ>, p, mA, mB, mAs, mBs, mA32, mAs32);
 }
 
 // Tensor maps, parameters and grid of one launch with MMA N = BN.
-template <bool kFC1, bool kPair, int BN, bool kShort, bool kFp8>
+template <bool kFC1, bool kPair, int BN, bool kShort, int kQ>
 cudaError_t launch_bn(const GemmLaunch& L, int num_sms, int64_t bound, cudaStream_t s, const char** why) {
     const bool has_routed = L.G > 0 && L.rows_cap > 0;
     const bool has_shared = L.T_sh > 0 && L.b_sh != nullptr && L.N_out_sh > 0;
@@ -799,17 +830,18 @@ cudaError_t launch_bn(const GemmLaunch& L, int num_sms, int64_t bound, cudaStrea
     const uint32_t brows = kFC1 ? BN / 2 : (kPair ? BN / 2 : BN);
     CUtensorMap mA, mB, mAs, mBs, mA32, mAs32;
     bool ok = true;
+    constexpr bool a8 = kQ == GEMM_W8A8;
     if (has_routed) {
-        ok = ok && encode_2d(&mA, L.a, (uint64_t)L.K, (uint64_t)L.rows_cap, BM);
-        ok = ok && encode_2d(&mA32, L.a, (uint64_t)L.K, (uint64_t)L.rows_cap, BM_SHORT);
-        ok = ok && (kFp8 ? encode_3d_u8(&mB, L.b, (uint64_t)L.K, (uint64_t)L.Nb, (uint64_t)L.G, brows)
-                         : encode_3d(&mB, L.b, (uint64_t)L.K, (uint64_t)L.Nb, (uint64_t)L.G, brows));
+        ok = ok && encode_2d(&mA, L.a, (uint64_t)L.K, (uint64_t)L.rows_cap, BM, a8);
+        ok = ok && encode_2d(&mA32, L.a, (uint64_t)L.K, (uint64_t)L.rows_cap, BM_SHORT, a8);
+        ok = ok && (kQ == GEMM_W8 ? encode_3d_u8(&mB, L.b, (uint64_t)L.K, (uint64_t)L.Nb, (uint64_t)L.G, brows)
+                                  : encode_3d(&mB, L.b, (uint64_t)L.K, (uint64_t)L.Nb, (uint64_t)L.G, brows, a8));
     }
     if (has_shared) {
-        ok = ok && encode_2d(&mAs, L.a_sh, (uint64_t)L.K_sh, (uint64_t)L.T_sh, BM);
-        ok = ok && encode_2d(&mAs32, L.a_sh, (uint64_t)L.K_sh, (uint64_t)L.T_sh, BM_SHORT);
-        ok = ok && (kFp8 ? encode_3d_u8(&mBs, L.b_sh, (uint64_t)L.K_sh, (uint64_t)L.Nb_sh, 1, brows)
-                         : encode_3d(&mBs, L.b_sh, (uint64_t)L.K_sh, (uint64_t)L.Nb_sh, 1, brows));
+        ok = ok && encode_2d(&mAs, L.a_sh, (uint64_t)L.K_sh, (uint64_t)L.T_sh, BM, a8);
+        ok = ok && encode_2d(&mAs32, L.a_sh, (uint64_t)L.K_sh, (uint64_t)L.T_sh, BM_SHORT, a8);
+        ok = ok && (kQ == GEMM_W8 ? encode_3d_u8(&mBs, L.b_sh, (uint64_t)L.K_sh, (uint64_t)L.Nb_sh, 1, brows)
+                                  : encode_3d(&mBs, L.b_sh, (uint64_t)L.K_sh, (uint64_t)L.Nb_sh, 1, brows, a8));
     }
     if (!ok) {
         *why = "cuTensorMapEncodeTiled failed";
@@ -838,17 +870,24 @@ cudaError_t launch_bn(const GemmLaunch& L, int num_sms, int64_t bound, cudaStrea
     p.T_sh = has_shared ? L.T_sh : 0;
     p.scale = L.b_scale;
     p.scale_sh = L.b_scale_sh;
+    p.a_scale = L.a_scale;
+    p.a_scale_sh = L.a_scale_sh;
+    // K steps: 64 bf16 or 128 E4M3 elements (one 128-byte row); a ragged last step
+    // of E4M3 operands is zero-filled by the TMA past K
+    const int ke = a8 ? 2 * BK : BK;
+    p.kb_total = (L.K + ke - 1) / ke;
+    p.kb_total_sh = (L.K_sh + ke - 1) / ke;
     p.Nb = L.Nb;
     p.out_sh_part = L.out_sh_part;
     p.ksplit_sh = (has_shared && !L.swiglu && L.out_sh_part && L.ksplit_sh > 1) ? L.ksplit_sh : 1;
-    p.kb_split_sh = (L.K_sh / BK + p.ksplit_sh - 1) / p.ksplit_sh;
+    p.kb_split_sh = (p.kb_total_sh + p.ksplit_sh - 1) / p.ksplit_sh;
     p.out = L.out;
     p.out_sh = L.out_sh;
     p.status = &L.hdr->status;
     p.timeout_ns = L.timeout_ns;
 
     KernelInfo info;
-    cudaError_t err = kernel_info<kFC1, kPair, BN, kShort, kFp8>(num_sms, &info);
+    cudaError_t err = kernel_info<kFC1, kPair, BN, kShort, kQ>(num_sms, &info);
     if (err != cudaSuccess) {
         *why = "kernel attribute / occupancy query failed";
         return err;
@@ -861,7 +900,7 @@ cudaError_t launch_bn(const GemmLaunch& L, int num_sms, int64_t bound, cudaStrea
     } else {
         grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(bound, num_sms));
     }
-    err = launch_kernel<kFC1, kPair, BN, kShort, kFp8>(p, mA, mB, mAs, mBs, mA32, mAs32, grid, s);
+    err = launch_kernel<kFC1, kPair, BN, kShort, kQ>(p, mA, mB, mAs, mBs, mA32, mAs32, grid, s);
     if (err != cudaSuccess) *why = "launch failed";
     return err;
 }
@@ -887,27 +926,38 @@ int64_t tile_bound(const GemmLaunch& L, int bn) {
 template <bool kFC1>
 cudaError_t dispatch(const GemmLaunch& L, int num_sms, cudaStream_t s, const char** why) {
     const int64_t b256 = tile_bound(L, 256);
-    if (L.b_fp8) {
+    if (L.quant == GEMM_W8) {
         // E4M3 weights: N = 256, single CTAs; 32-row A slots when every tile is short
         if (L.max_group_rows <= BM_SHORT && L.T_sh <= BM_SHORT)
-            return launch_bn<kFC1, false, 256, true, true>(L, num_sms, b256, s, why);
-        return launch_bn<kFC1, false, 256, false, true>(L, num_sms, b256, s, why);
+            return launch_bn<kFC1, false, 256, true, GEMM_W8>(L, num_sms, b256, s, why);
+        return launch_bn<kFC1, false, 256, false, GEMM_W8>(L, num_sms, b256, s, why);
+    }
+    if (L.quant == GEMM_W8A8) {
+        // E4M3 operands: single CTAs, tile widths chosen as for bf16
+        if (L.max_group_rows <= BM_SHORT && L.T_sh <= BM_SHORT)
+            return launch_bn<kFC1, false, 256, true, GEMM_W8A8>(L, num_sms, b256, s, why);
+        if (L.rows_cap <= 1024 || b256 >= 2 * (int64_t)num_sms)
+            return launch_bn<kFC1, false, 256, false, GEMM_W8A8>(L, num_sms, b256, s, why);
+        const int64_t b128 = tile_bound(L, 128);
+        if (b128 >= 2 * (int64_t)num_sms)
+            return launch_bn<kFC1, false, 128, false, GEMM_W8A8>(L, num_sms, b128, s, why);
+        return launch_bn<kFC1, false, 64, false, GEMM_W8A8>(L, num_sms, tile_bound(L, 64), s, why);
     }
     const bool pair = split_of(L) == 1 &&
                       (L.pair_mode == 2 ? b256 >= 2 : (L.pair_mode == 1 && b256 >= 4 * (int64_t)num_sms));
-    if (pair) return launch_bn<kFC1, true, 256, false, false>(L, num_sms, b256, s, why);
+    if (pair) return launch_bn<kFC1, true, 256, false, GEMM_BF16>(L, num_sms, b256, s, why);
     // every tile at most 32 rows: 32-row A slots, so more stages fit the ring
     if (L.max_group_rows <= BM_SHORT && L.T_sh <= BM_SHORT)
-        return launch_bn<kFC1, false, 256, true, false>(L, num_sms, b256, s, why);
+        return launch_bn<kFC1, false, 256, true, GEMM_BF16>(L, num_sms, b256, s, why);
     // Small batches (at most 1024 routed rows) stream weights: N = 256 moves the
     // most bytes per pipeline stage, and a stage costs about the same time
     // whatever its size, so the widest tile wins even with SMs left idle.
     // Otherwise the widest N that still gives every SM two tiles.
     if (L.rows_cap <= 1024 || b256 >= 2 * (int64_t)num_sms)
-        return launch_bn<kFC1, false, 256, false, false>(L, num_sms, b256, s, why);
+        return launch_bn<kFC1, false, 256, false, GEMM_BF16>(L, num_sms, b256, s, why);
     const int64_t b128 = tile_bound(L, 128);
-    if (b128 >= 2 * (int64_t)num_sms) return launch_bn<kFC1, false, 128, false, false>(L, num_sms, b128, s, why);
-    return launch_bn<kFC1, false, 64, false, false>(L, num_sms, tile_bound(L, 64), s, why);
+    if (b128 >= 2 * (int64_t)num_sms) return launch_bn<kFC1, false, 128, false, GEMM_BF16>(L, num_sms, b128, s, why);
+    return launch_bn<kFC1, false, 64, false, GEMM_BF16>(L, num_sms, tile_bound(L, 64), s, why);
 }
 
 }  // namespace

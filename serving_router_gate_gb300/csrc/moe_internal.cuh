@@ -233,6 +233,18 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, ui
         : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem]^T, E4M3 inputs (kind::f8f6f4, K = 32 per
+// instruction: 32 bytes of a 128-byte row, as for bf16), fp32 accumulation.
+__device__ __forceinline__ void tc_mma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on `bar` when all tcgen05 operations issued so far by this thread complete.
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -324,6 +336,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
            | ((uint32_t)(M >> 4) << 24);          // M / 16
 }
 
+// Instruction descriptor of tcgen05.mma.kind::f8f6f4: E4M3 A and B (format
+// code 0 in both fields, both K-major), fp32 D, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+    return (1u << 4)                              // D format: f32
+           | ((uint32_t)(N >> 3) << 17)           // N / 8
+           | ((uint32_t)(M >> 4) << 24);          // M / 16
+}
+
 // ---------------------------------------------------------------------------
 // Internal launchers (defined in the kernel files, called by moe_api.cu)
 // ---------------------------------------------------------------------------
@@ -393,10 +413,13 @@ struct GemmLaunch {
     uint64_t timeout_ns;
     int pair_mode;             // 0 single CTAs only, 1 pairs for large launches, 2 pairs whenever possible
     int64_t max_group_rows;    // upper bound on the rows of any routed group (tokens of the batch)
-    bool b_fp8;                // B (weights) are E4M3 bytes with one fp32 scale per row
-    const float* b_scale;      // [G][Nb] row scales of b (E4M3 only)
-    const float* b_scale_sh;   // [Nb_sh] row scales of b_sh (E4M3 only)
+    int quant;                 // GEMM_BF16, GEMM_W8 (E4M3 B, bf16 A) or GEMM_W8A8 (E4M3 A and B)
+    const float* b_scale;      // [G][Nb] row scales of b (E4M3 B only)
+    const float* b_scale_sh;   // [Nb_sh] row scales of b_sh (E4M3 B only)
+    const float* a_scale;      // [rows_cap] row scales of a (GEMM_W8A8 only)
+    const float* a_scale_sh;   // [T_sh] row scales of a_sh (GEMM_W8A8 only)
 };
+enum { GEMM_BF16 = 0, GEMM_W8 = 1, GEMM_W8A8 = 2 };
 cudaError_t launch_grouped_gemm(const GemmLaunch& L, int num_sms, cudaStream_t s, const char** why);
 
 struct FinalizeLaunch {
@@ -419,6 +442,17 @@ cudaError_t launch_finalize(const FinalizeLaunch& L, int num_sms, cudaStream_t s
 cudaError_t launch_wait_timeout_probe(WsHeader* hdr, uint64_t timeout_ns, cudaStream_t s);
 
 // Row-wise E4M3 quantisation of a bf16 matrix [rows, K] (moe_quantize_fp8_rows).
+// E4M3 activation rows with power-of-two scales: up to two row sets per launch;
+// a set with rows_dev takes min(rows, *rows_dev) rows, read on the device.
+struct ActQuantSeg {
+    const uint16_t* src;       // [rows, K] bf16
+    int64_t rows;
+    const int32_t* rows_dev;   // or null
+    int K;
+    uint8_t* dst;              // [rows, K]
+    float* scale;              // [rows]
+};
+cudaError_t launch_quantize_act_rows(const ActQuantSeg* seg, int nseg, int num_sms, cudaStream_t s);
 cudaError_t launch_quantize_fp8_rows(const uint16_t* w, int64_t rows, int K, uint8_t* q, float* scale, int num_sms,
                                      cudaStream_t s);
 

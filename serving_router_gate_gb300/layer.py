@@ -14,8 +14,8 @@ from typing import Optional
 
 import torch
 
-from . import (MOE_NONLOCAL_SKIP, moe_forward, moe_forward_fp8, moe_permute, moe_quantize_fp8_rows, moe_route,
-               moe_route_grouped, moe_workspace_init, moe_workspace_size)
+from . import (MOE_NONLOCAL_SKIP, moe_forward, moe_forward_fp8, moe_forward_w8a8, moe_permute,
+               moe_quantize_fp8_rows, moe_route, moe_route_grouped, moe_workspace_init, moe_workspace_size)
 
 
 class MoELayer:
@@ -25,7 +25,8 @@ class MoELayer:
                  S: Optional[int] = None, local_start: int = 0, local_count: int = -1,
                  nonlocal_mode: int = MOE_NONLOCAL_SKIP, W1s: Optional[torch.Tensor] = None,
                  W2s: Optional[torch.Tensor] = None, shared_gate_w: Optional[torch.Tensor] = None,
-                 on_input: bool = False, n_group: int = 1, topk_group: int = 1, fp8: bool = False):
+                 on_input: bool = False, n_group: int = 1, topk_group: int = 1, fp8: bool = False,
+                 act8: bool = False):
         self.Wg, self.W1, self.W2 = Wg, W1, W2
         # routing applied on the input: rows scaled by the weights, outputs summed unweighted
         self.on_input = bool(on_input)
@@ -60,6 +61,10 @@ class MoELayer:
         moe_workspace_init(self.ws)
         # E4M3 expert weights with one fp32 scale per row, quantised once here
         self.fp8 = bool(fp8)
+        # E4M3 activations as well (per row, power-of-two scales, inside moe_forward_w8a8)
+        self.act8 = bool(act8)
+        if self.act8 and not self.fp8:
+            raise ValueError("E4M3 activations need E4M3 weights (fp8=True)")
         self.W1q = self.s1 = self.W2q = self.s2 = self.W1sq = self.s1s = self.W2sq = self.s2s = None
         if self.fp8:
             def quant(w):
@@ -100,7 +105,8 @@ class MoELayer:
         w = None if self.on_input else v["topk_w"]
         xs = x if (self.I_sh > 0) else None
         if self.fp8:
-            moe_forward_fp8(v["x_perm"], v["offsets"], self.W1q, self.s1, self.W2q, self.s2, v["pair_row"], w, xs,
+            fwd = moe_forward_w8a8 if self.act8 else moe_forward_fp8
+            fwd(v["x_perm"], v["offsets"], self.W1q, self.s1, self.W2q, self.s2, v["pair_row"], w, xs,
                             self.W1sq, self.s1s, self.W2sq, self.s2s, self.gate, v["out"], self.ws, stream)
         else:
             moe_forward(v["x_perm"], v["offsets"], self.W1, self.W2, v["pair_row"], w, xs, self.W1s, self.W2s,
@@ -167,4 +173,4 @@ def layer_from_inputs(inp: dict, device="cuda", max_T: Optional[int] = None, loc
                     rep_offset=d(inp["rep_offset"]), rep_slots=d(inp["rep_slots"]), S=cfg.slots,
                     local_start=local_start, local_count=local_count, nonlocal_mode=nonlocal_mode,
                     W1s=d(W1s), W2s=d(W2s), shared_gate_w=d(inp["w_s"]), on_input=on_input,
-                    n_group=cfg.n_group, topk_group=cfg.topk_group, fp8=cfg.fp8)
+                    n_group=cfg.n_group, topk_group=cfg.topk_group, fp8=cfg.fp8, act8=cfg.act8)

@@ -104,7 +104,7 @@ def oracle_layer(inp_cpu: dict, local_start=0, local_count=-1, mode=0, tokens=No
             W1s, W2s = c1[None], c2[None]
         q1, s1 = oracle.quantize_fp8_rows(W1)
         q2, s2 = oracle.quantize_fp8_rows(W2)
-        fp8 = dict(W1q=q1, s1=s1, W2q=q2, s2=s2)
+        fp8 = dict(W1q=q1, s1=s1, W2q=q2, s2=s2, act8=cfg.act8)
         if W1s is not None:
             q1s, s1s = oracle.quantize_fp8_rows(W1s)
             q2s, s2s = oracle.quantize_fp8_rows(W2s)

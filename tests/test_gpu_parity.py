@@ -400,6 +400,93 @@ def test_fp8_stage_gemms_against_oracle_rows():
         check_out(y[r:r + 1], y_ref[None, :], f"fp8 y row {r}")
 
 
+# --------------------------------------------------------------------------- E4M3 weights and activations
+
+def test_quantize_act_rows_bit_exact():
+    g = torch.Generator().manual_seed(12)
+    rows = [torch.randn(40, 192, generator=g) * sc for sc in (1e-3, 0.02, 1.0, 300.0)]
+    v = torch.cat(rows)
+    v[3] = 0.0                                        # all zero: scale 2^-126, q = 0
+    v[5] = v[5] / v[5].abs().max() * 3584.0           # amax = 448 * 2^3 exactly
+    v[6] = v[6] / v[6].abs().max() * 3600.0           # the next bf16 above
+    v[7] = torch.full((192,), 2.0 ** -130)            # bf16 subnormals: the scale clamps at 2^-126
+    v[8, 0] = 1e30                                    # one huge value: the rest round to zero
+    v = v.to(torch.bfloat16)
+    for K, vv in ((192, v), (7168, torch.randn(33, 7168, generator=g).to(torch.bfloat16))):
+        q_ref, s_ref = oracle.quantize_act_rows(vv)
+        q = torch.empty(vv.shape, dtype=torch.uint8, device="cuda")
+        sc = torch.empty(vv.shape[0], dtype=torch.float32, device="cuda")
+        moe.moe_quantize_act_rows(vv.cuda(), q, sc)
+        torch.cuda.synchronize()
+        assert np.array_equal(q.cpu().numpy(), q_ref), K
+        assert np.array_equal(sc.cpu().numpy().view(np.uint32), s_ref.view(np.uint32)), K
+
+
+W8A8_MID = MID.with_(name="mid_w8a8", fp8=True, act8=True)
+
+
+def test_w8a8_mid_layer():
+    _full_check(mi.make_inputs(W8A8_MID))
+
+
+def test_w8a8_ragged_k_partial_tiles_two_shared_and_short_batch():
+    # H = 320, I = 320, I_shared = 192: K is not a multiple of the 128-element E4M3 step
+    cfg = mi.MoEConfig("odd_w8a8", T=200, H=320, I=320, E=5, k=2, renorm=False, n_shared=2, I_shared=192,
+                       fp8=True, act8=True)
+    _full_check(mi.make_inputs(cfg))
+    # at most 32 tokens: the short-tile variant, and the split shared FC2
+    cfg = mi.MoEConfig("short_w8a8", T=24, H=256, I=128, E=9, k=3, renorm=True, n_shared=2, I_shared=256,
+                       shared_gate=True, fp8=True, act8=True)
+    _full_check(mi.make_inputs(cfg))
+
+
+@pytest.mark.parametrize("act8", [False, True])
+def test_shared_split_with_more_ranges_than_k_steps(act8):
+    # I = 64 and 576 shared columns: the shared FC2 splits into 8 K ranges, more than
+    # its K steps fill (9 bf16 steps of 64 or 5 E4M3 steps of 128); empty ranges add zeros
+    cfg = mi.MoEConfig("split_empty", T=16, H=128, I=64, E=4, k=2, renorm=True, n_shared=1, I_shared=576,
+                       fp8=act8, act8=act8)
+    _full_check(mi.make_inputs(cfg))
+
+
+def test_w8a8_local_ranges_and_routing_on_input():
+    inp = mi.make_inputs(W8A8_MID)
+    # a local range: fewer routed rows than the buffers hold (the quantiser reads the count on the device)
+    _full_check(inp, 4, 5, moe.MOE_NONLOCAL_SKIP)
+    _full_check(inp, 4, 5, moe.MOE_NONLOCAL_MOD)
+    _on_input_check(mi.make_inputs(W8A8_MID.with_(on_input=True)))
+
+
+def test_w8a8_stage_gemms_against_oracle_rows():
+    inp = mi.make_inputs(W8A8_MID)
+    g = run_gpu(inp)
+    layer = g["layer"]
+    cfg = W8A8_MID
+    dev = torch.device("cuda")
+    P = cfg.T * cfg.k
+    xq = torch.empty((P, cfg.H), dtype=torch.uint8, device=dev)
+    sx = torch.empty(P, dtype=torch.float32, device=dev)
+    h = torch.empty((P, cfg.I), dtype=torch.bfloat16, device=dev)
+    hq = torch.empty((P, cfg.I), dtype=torch.uint8, device=dev)
+    sh = torch.empty(P, dtype=torch.float32, device=dev)
+    y = torch.empty((P, cfg.H), dtype=torch.bfloat16, device=dev)
+    moe.moe_quantize_act_rows(layer.x_perm, xq, sx)
+    moe.moe_grouped_fc1_w8a8(xq, sx, layer.offsets, layer.W1q, layer.s1, None, None, None, None, h, None, layer.ws)
+    moe.moe_quantize_act_rows(h, hq, sh)
+    moe.moe_grouped_fc2_w8a8(hq, sh, layer.offsets, layer.W2q, layer.s2, None, None, None, None, y, None, layer.ws)
+    torch.cuda.synchronize()
+    q1, s1 = oracle.quantize_fp8_rows(inp["W1"])
+    q2, s2 = oracle.quantize_fp8_rows(inp["W2"])
+    perm = g["perm_src"].numpy()
+    slots = g["slot_ids"].numpy().reshape(-1)
+    for r in sample_tokens(g["rows"], 16, seed=4):
+        p = int(perm[r])
+        t, s = p // cfg.k, int(slots[p])
+        y_ref, _ = oracle.expert_mlp_fp8(inp["x"][t], q1[s], s1[s], q2[s], s2[s], act8=True)
+        check_out(y[r:r + 1], y_ref[None, :], f"w8a8 y row {r}")
+    assert moe.moe_get_device_status(layer.ws) == 0
+
+
 # --------------------------------------------------------------------------- device-side error paths
 
 def test_out_of_range_expert_ids_are_dropped_and_flagged():
@@ -485,4 +572,10 @@ def test_routing_on_input_prefill_full_size():
 @pytest.mark.parametrize("name", ["dsv2_lite_like_decode_t1_fp8", "dsv2_lite_like_decode_t32_fp8",
                                   "qwen2_moe_like_prefill_fp8"])
 def test_fp8_full_size(name):
+    _full_size(name, 16 if "prefill" in name else 32)
+
+
+@pytest.mark.parametrize("name", ["dsv2_lite_like_decode_t1_w8a8", "dsv2_lite_like_decode_t32_w8a8",
+                                  "qwen2_moe_like_prefill_w8a8"])
+def test_w8a8_full_size(name):
     _full_size(name, 16 if "prefill" in name else 32)
