@@ -68,8 +68,6 @@ __global__ void __launch_bounds__(QZ_WARPS * 32) quantize_fp8_rows_kernel(const 
 struct ActQuantArgs {
     ActQuantSeg seg[2];
     int nseg;
-    int64_t rows0;  // rows of seg[0] (its bound): rows of the launch's index space before seg[1]
-    int64_t rows_total;
 };
 
 __device__ __forceinline__ int act_exponent(float amax) {
@@ -78,46 +76,138 @@ __device__ __forceinline__ int act_exponent(float amax) {
     return e < -126 ? -126 : e;
 }
 
-__global__ void __launch_bounds__(QZ_WARPS * 32) quantize_act_rows_kernel(const __grid_constant__ ActQuantArgs a) {
+// One CTA of 256 threads quantises R = 8 / VPT rows at a time, each thread
+// holding VPT 16-byte vectors (8 bf16) of every one of those rows: all loads of
+// an iteration are issued before any is used, so a CTA keeps R rows in flight.
+// Rows longer than 256 * 8 * 8 elements take a two-pass loop instead.
+constexpr int QA_THREADS = 256;
+constexpr int QA_WARPS = QA_THREADS / 32;
+
+__device__ __forceinline__ uint32_t e4m3x4(const float* f, float inv) {
+    return (uint32_t)__nv_cvt_float_to_fp8(f[0] * inv, __NV_SATFINITE, __NV_E4M3) |
+           ((uint32_t)__nv_cvt_float_to_fp8(f[1] * inv, __NV_SATFINITE, __NV_E4M3) << 8) |
+           ((uint32_t)__nv_cvt_float_to_fp8(f[2] * inv, __NV_SATFINITE, __NV_E4M3) << 16) |
+           ((uint32_t)__nv_cvt_float_to_fp8(f[3] * inv, __NV_SATFINITE, __NV_E4M3) << 24);
+}
+
+// |v| of a finite bf16 value orders like its bit pattern with the sign cleared,
+// so a row's amax is an unsigned maximum of those 15-bit patterns (two per word)
+__device__ __forceinline__ uint32_t absmax_bf16x8(uint32_t m, const uint4& v) {
+    m = __vmaxu2(m, v.x & 0x7FFF7FFFu);
+    m = __vmaxu2(m, v.y & 0x7FFF7FFFu);
+    m = __vmaxu2(m, v.z & 0x7FFF7FFFu);
+    return __vmaxu2(m, v.w & 0x7FFF7FFFu);
+}
+
+// amax over the CTA for each of the R rows (packed per-thread maxima in, binary32
+// amax out); red: [R][QA_WARPS] shared words
+template <int R>
+__device__ __forceinline__ void block_amax(const uint32_t (&pk)[R], float (&am)[R], uint32_t* red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int rr = 0; rr < R; ++rr) {
+        const uint32_t m = __reduce_max_sync(0xffffffffu, max(pk[rr] & 0xFFFFu, pk[rr] >> 16));
+        if (lane == 0) red[rr * QA_WARPS + warp] = m;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int rr = 0; rr < R; ++rr) {
+        uint32_t m = red[rr * QA_WARPS];
+#pragma unroll
+        for (int w = 1; w < QA_WARPS; ++w) m = max(m, red[rr * QA_WARPS + w]);
+        am[rr] = __uint_as_float(m << 16);
+    }
+    __syncthreads();  // red is rewritten by the next iteration
+}
+
+template <int VPT>
+__device__ __forceinline__ void quantize_rows_regs(const ActQuantSeg& sg, int64_t lim, uint32_t* red, int cta) {
+    constexpr int R = 8 / VPT;
+    const int vec = sg.K / 8;
+    for (int64_t base = (int64_t)cta * R; base < lim; base += (int64_t)gridDim.x * R) {
+        uint4 v[R][VPT];
+        uint32_t pk[R];
+        float am[R];
+#pragma unroll
+        for (int rr = 0; rr < R; ++rr) {
+            const int64_t row = base + rr;
+            const uint4* src = reinterpret_cast<const uint4*>(sg.src + row * sg.K);
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                const int idx = threadIdx.x + j * QA_THREADS;
+                v[rr][j] = (row < lim && idx < vec) ? __ldg(src + idx) : make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+#pragma unroll
+        for (int rr = 0; rr < R; ++rr) {
+            pk[rr] = 0u;
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) pk[rr] = absmax_bf16x8(pk[rr], v[rr][j]);
+        }
+        block_amax<R>(pk, am, red);
+#pragma unroll
+        for (int rr = 0; rr < R; ++rr) {
+            const int64_t row = base + rr;
+            if (row >= lim) break;
+            const int e = act_exponent(am[rr]);
+            const float inv = __uint_as_float((uint32_t)(127 - e) << 23);
+            if (threadIdx.x == 0) sg.scale[row] = __uint_as_float((uint32_t)(127 + e) << 23);
+            uint2* dst = reinterpret_cast<uint2*>(sg.dst + row * sg.K);
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                const int idx = threadIdx.x + j * QA_THREADS;
+                if (idx < vec) {
+                    float f[8];
+                    unpack8(v[rr][j], f);
+                    dst[idx] = make_uint2(e4m3x4(f, inv), e4m3x4(f + 4, inv));
+                }
+            }
+        }
+    }
+}
+
+// long rows: one row per CTA iteration, read twice (amax, then quantise)
+__device__ __forceinline__ void quantize_rows_loop(const ActQuantSeg& sg, int64_t lim, uint32_t* red, int cta) {
+    const int vec = sg.K / 8;
+    for (int64_t row = cta; row < lim; row += gridDim.x) {
+        const uint4* src = reinterpret_cast<const uint4*>(sg.src + row * sg.K);
+        uint32_t pk[1] = {0u};
+        float am[1];
+        for (int idx = threadIdx.x; idx < vec; idx += QA_THREADS) pk[0] = absmax_bf16x8(pk[0], __ldg(src + idx));
+        block_amax<1>(pk, am, red);
+        const int e = act_exponent(am[0]);
+        const float inv = __uint_as_float((uint32_t)(127 - e) << 23);
+        if (threadIdx.x == 0) sg.scale[row] = __uint_as_float((uint32_t)(127 + e) << 23);
+        uint2* dst = reinterpret_cast<uint2*>(sg.dst + row * sg.K);
+        for (int idx = threadIdx.x; idx < vec; idx += QA_THREADS) {
+            float f[8];
+            unpack8(__ldg(src + idx), f);
+            dst[idx] = make_uint2(e4m3x4(f, inv), e4m3x4(f + 4, inv));
+        }
+    }
+}
+
+__global__ void __launch_bounds__(QA_THREADS) quantize_act_rows_kernel(const __grid_constant__ ActQuantArgs a) {
+    __shared__ uint32_t red[8 * QA_WARPS];
     pdl_wait();
     pdl_trigger();
-    const int lane = threadIdx.x & 31;
-    int64_t lim[2];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        lim[i] = i < a.nseg ? a.seg[i].rows : 0;
-        if (i < a.nseg && a.seg[i].rows_dev) lim[i] = min(lim[i], (int64_t)max(0, __ldg(a.seg[i].rows_dev)));
-    }
-    for (int64_t gr = (int64_t)blockIdx.x * QZ_WARPS + (threadIdx.x >> 5); gr < a.rows_total;
-         gr += (int64_t)gridDim.x * QZ_WARPS) {
-        const int si = gr < a.rows0 ? 0 : 1;
-        const int64_t r = si ? gr - a.rows0 : gr;
-        if (r >= lim[si]) continue;
+    for (int si = 0; si < a.nseg; ++si) {
         const ActQuantSeg& sg = a.seg[si];
-        const int vec = sg.K / 8;
-        const uint4* src = reinterpret_cast<const uint4*>(sg.src + r * sg.K);
-        float amax = 0.f;
-        for (int v = lane; v < vec; v += 32) {
-            float f[8];
-            unpack8(__ldg(src + v), f);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-        const int e = act_exponent(amax);
-        const float inv = __uint_as_float((uint32_t)(127 - e) << 23);
-        if (lane == 0) sg.scale[r] = __uint_as_float((uint32_t)(127 + e) << 23);
-        uint2* dst = reinterpret_cast<uint2*>(sg.dst + r * sg.K);
-        for (int v = lane; v < vec; v += 32) {
-            float f[8];
-            unpack8(__ldg(src + v), f);
-            uint32_t b[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) b[i] = (uint32_t)__nv_cvt_float_to_fp8(f[i] * inv, __NV_SATFINITE, __NV_E4M3);
-            dst[v] = make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24),
-                                b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
-        }
+        int64_t lim = sg.rows;
+        if (sg.rows_dev) lim = min(lim, (int64_t)max(0, __ldg(sg.rows_dev)));
+        const int vpt = (sg.K / 8 + QA_THREADS - 1) / QA_THREADS;
+        // the second row set starts from the last CTA, so small launches run both at once
+        const int cta = si ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
+        if (vpt <= 1)
+            quantize_rows_regs<1>(sg, lim, red, cta);
+        else if (vpt <= 2)
+            quantize_rows_regs<2>(sg, lim, red, cta);
+        else if (vpt <= 4)
+            quantize_rows_regs<4>(sg, lim, red, cta);
+        else if (vpt <= 8)
+            quantize_rows_regs<8>(sg, lim, red, cta);
+        else
+            quantize_rows_loop(sg, lim, red, cta);
     }
 }
 
@@ -129,11 +219,16 @@ cudaError_t launch_quantize_act_rows(const ActQuantSeg* seg, int nseg, int num_s
     for (int i = 0; i < nseg && i < 2; ++i)
         if (seg[i].rows > 0) a.seg[a.nseg++] = seg[i];
     if (a.nseg == 0) return cudaSuccess;
-    a.rows0 = a.seg[0].rows;
-    a.rows_total = a.rows0 + (a.nseg > 1 ? a.seg[1].rows : 0);
-    const int64_t want = (a.rows_total + QZ_WARPS - 1) / QZ_WARPS;
-    const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms * 8));
-    return launch_k(quantize_act_rows_kernel, dim3(grid), dim3(QZ_WARPS * 32), 0, s, a);
+    // one CTA per row group of the two row sets together, at most the resident
+    // CTAs (3 per SM)
+    int64_t want = 0;
+    for (int i = 0; i < a.nseg; ++i) {
+        const int vpt = (a.seg[i].K / 8 + QA_THREADS - 1) / QA_THREADS;
+        const int R = vpt <= 1 ? 8 : vpt <= 2 ? 4 : vpt <= 4 ? 2 : 1;
+        want += (a.seg[i].rows + R - 1) / R;
+    }
+    const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms * 3));
+    return launch_k(quantize_act_rows_kernel, dim3(grid), dim3(QA_THREADS), 0, s, a);
 }
 
 cudaError_t launch_quantize_fp8_rows(const uint16_t* w, int64_t rows, int K, uint8_t* q, float* scale, int num_sms,
