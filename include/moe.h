@@ -283,7 +283,8 @@ MOE_API moe_status_t moe_forward_fp8(const moe_bf16_t *x_perm, const int32_t *of
  * q[r][c] = e4m3(w[r][c] / scale[r]), both divisions in IEEE binary32 and the
  * conversion to nearest, ties to even (the row's largest |w| becomes +-448
  * exactly); an all-zero row gets scale 0 and q = 0.  Expert weights laid out
- * as [S, R, K] are quantised as one [S*R, K] matrix.  Asynchronous on `stream`;
+ * as [S, R, K] are quantised as one [S*R, K] matrix.  w must be 16-byte and q
+ * 8-byte aligned (MOE_ERR_INVALID_ARG otherwise).  Asynchronous on `stream`;
  * allocates nothing. */
 MOE_API moe_status_t moe_quantize_fp8_rows(const moe_bf16_t *w, int64_t rows, int K, uint8_t *q, float *scale,
                                    moe_stream_t stream);
@@ -310,7 +311,8 @@ MOE_API moe_status_t moe_forward_w8a8(const moe_bf16_t *x_perm, const int32_t *o
  * 64), as moe_forward_w8a8 does: per row, scale = 2^e with e the smallest
  * integer >= -126 such that amax_c |v[r][c]| <= 448 * 2^e, and
  * q[r][c] = e4m3(v[r][c] / 2^e) to nearest, ties to even (the division is
- * exact).  An all-zero row gets scale 2^-126 and q = 0.  Asynchronous on
+ * exact).  An all-zero row gets scale 2^-126 and q = 0.  v must be 16-byte
+ * and q 8-byte aligned (MOE_ERR_INVALID_ARG otherwise).  Asynchronous on
  * `stream`; allocates nothing. */
 MOE_API moe_status_t moe_quantize_act_rows(const moe_bf16_t *v, int64_t rows, int K, uint8_t *q, float *scale,
                                    moe_stream_t stream);

@@ -90,6 +90,8 @@ size_t permute_need(int64_t P, int S_local) { return kWsHeaderBytes + permute_sc
 
 bool dim_ok(int v) { return v > 0 && v % 64 == 0 && v <= (1 << 20); }
 
+bool aligned(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+
 moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 }  // namespace
@@ -499,6 +501,7 @@ static moe_status_t forward_impl(const moe_bf16_t* x_perm, const int32_t* offset
     float* y_sh_part = ks > 1 ? reinterpret_cast<float*>(base + FL.y_sh_part) : nullptr;
     moe_status_t st;
     if (act8) {
+        if (!aligned(x_perm, 16) || (I_shared_total > 0 && !aligned(x, 16))) return MOE_ERR_INVALID_ARG;
         // E4M3 activations: quantise the expert input rows (as many as offsets[S_local]
         // says, read on the device) and the shared experts' input, run FC1 on them,
         // quantise the intermediate rows, run FC2
@@ -574,6 +577,7 @@ moe_status_t moe_quantize_act_rows(const moe_bf16_t* v, int64_t rows, int K, uin
     if (K % 64 != 0) return MOE_ERR_UNSUPPORTED;
     if (rows == 0) return MOE_OK;
     if (!v || !q || !scale) return MOE_ERR_INVALID_ARG;
+    if (!aligned(v, 16) || !aligned(q, 8)) return MOE_ERR_INVALID_ARG;
     const ActQuantSeg seg = {v, rows, nullptr, K, q, scale};
     return cuda_status(launch_quantize_act_rows(&seg, 1, device_sms(), (cudaStream_t)stream));
 }
@@ -584,6 +588,7 @@ moe_status_t moe_quantize_fp8_rows(const moe_bf16_t* w, int64_t rows, int K, uin
     if (K % 64 != 0) return MOE_ERR_UNSUPPORTED;
     if (rows == 0) return MOE_OK;
     if (!w || !q || !scale) return MOE_ERR_INVALID_ARG;
+    if (!aligned(w, 16) || !aligned(q, 8)) return MOE_ERR_INVALID_ARG;
     return cuda_status(launch_quantize_fp8_rows(w, rows, K, q, scale, device_sms(), (cudaStream_t)stream));
 }
 

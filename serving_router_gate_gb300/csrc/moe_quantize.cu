@@ -14,6 +14,7 @@
 #include <cuda_fp8.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "moe_internal.cuh"
 
@@ -76,18 +77,30 @@ __device__ __forceinline__ int act_exponent(float amax) {
     return e < -126 ? -126 : e;
 }
 
-// One CTA of 256 threads quantises R = 8 / VPT rows at a time, each thread
-// holding VPT 16-byte vectors (8 bf16) of every one of those rows: all loads of
-// an iteration are issued before any is used, so a CTA keeps R rows in flight.
-// Rows longer than 256 * 8 * 8 elements take a two-pass loop instead.
+// One CTA of 256 threads quantises a group of R = 4 / VPT consecutive rows at a
+// time, each thread owning VPT 16-byte vectors (8 bf16) of every one of those
+// rows.  The vectors arrive by cp.async in a double-buffered shared-memory
+// staging area: the copies of the next group are issued before the current one
+// is reduced and stored, and each thread reads back only its own vectors (no
+// barrier besides the reduction's).  Rows longer than 256 * 4 * 8 values take a
+// two-pass loop instead.
 constexpr int QA_THREADS = 256;
 constexpr int QA_WARPS = QA_THREADS / 32;
+constexpr int QA_VEC = 4;  // 16-byte vectors per thread per row group
 
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)), "l"(gsrc),
+                 "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_one() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+// four values scaled by inv (a power of two) -> four E4M3 bytes, two per conversion
 __device__ __forceinline__ uint32_t e4m3x4(const float* f, float inv) {
-    return (uint32_t)__nv_cvt_float_to_fp8(f[0] * inv, __NV_SATFINITE, __NV_E4M3) |
-           ((uint32_t)__nv_cvt_float_to_fp8(f[1] * inv, __NV_SATFINITE, __NV_E4M3) << 8) |
-           ((uint32_t)__nv_cvt_float_to_fp8(f[2] * inv, __NV_SATFINITE, __NV_E4M3) << 16) |
-           ((uint32_t)__nv_cvt_float_to_fp8(f[3] * inv, __NV_SATFINITE, __NV_E4M3) << 24);
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(f[0] * inv, f[1] * inv), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(f[2] * inv, f[3] * inv), __NV_SATFINITE, __NV_E4M3);
+    return lo | (hi << 16);
 }
 
 // |v| of a finite bf16 value orders like its bit pattern with the sign cleared,
@@ -117,56 +130,83 @@ __device__ __forceinline__ void block_amax(const uint32_t (&pk)[R], float (&am)[
         for (int w = 1; w < QA_WARPS; ++w) m = max(m, red[rr * QA_WARPS + w]);
         am[rr] = __uint_as_float(m << 16);
     }
-    __syncthreads();  // red is rewritten by the next iteration
+    __syncthreads();  // red is rewritten by the next group
+}
+
+// stage[buf][i * QA_THREADS + thread]: vector i = rr * VPT + j of the group
+template <int VPT>
+__device__ __forceinline__ void issue_group(uint4* stage, const ActQuantSeg& sg, int64_t base, int64_t lim) {
+    constexpr int R = QA_VEC / VPT;
+    const int vec = sg.K / 8;
+#pragma unroll
+    for (int rr = 0; rr < R; ++rr) {
+        const int64_t row = base + rr;
+        const uint4* src = reinterpret_cast<const uint4*>(sg.src + (row < lim ? row : 0) * sg.K);
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int idx = threadIdx.x + j * QA_THREADS;
+            cp_async16(stage + (rr * VPT + j) * QA_THREADS + threadIdx.x, src + (idx < vec ? idx : 0),
+                       row < lim && idx < vec);
+        }
+    }
+    cp_async_commit();
 }
 
 template <int VPT>
-__device__ __forceinline__ void quantize_rows_regs(const ActQuantSeg& sg, int64_t lim, uint32_t* red, int cta) {
-    constexpr int R = 8 / VPT;
+__device__ __forceinline__ void quantize_rows_staged(const ActQuantSeg& sg, int64_t lim, uint32_t* red, uint4* stage,
+                                                     int cta) {
+    constexpr int R = QA_VEC / VPT;
     const int vec = sg.K / 8;
-    for (int64_t base = (int64_t)cta * R; base < lim; base += (int64_t)gridDim.x * R) {
+    const int64_t stride = (int64_t)gridDim.x * R;
+    int64_t base = (int64_t)cta * R;
+    if (base >= lim) return;
+    issue_group<VPT>(stage, sg, base, lim);
+    for (int it = 0; base < lim; base += stride, ++it) {
+        uint4* cur = stage + (it & 1) * QA_VEC * QA_THREADS;
+        uint4* nxt = stage + ((it & 1) ^ 1) * QA_VEC * QA_THREADS;
+        if (base + stride < lim)
+            issue_group<VPT>(nxt, sg, base + stride, lim);
+        else
+            cp_async_commit();  // an empty group keeps the wait count uniform
+        cp_async_wait_one();    // this thread's copies of the current group have landed
         uint4 v[R][VPT];
         uint32_t pk[R];
         float am[R];
 #pragma unroll
         for (int rr = 0; rr < R; ++rr) {
-            const int64_t row = base + rr;
-            const uint4* src = reinterpret_cast<const uint4*>(sg.src + row * sg.K);
-#pragma unroll
-            for (int j = 0; j < VPT; ++j) {
-                const int idx = threadIdx.x + j * QA_THREADS;
-                v[rr][j] = (row < lim && idx < vec) ? __ldg(src + idx) : make_uint4(0u, 0u, 0u, 0u);
-            }
-        }
-#pragma unroll
-        for (int rr = 0; rr < R; ++rr) {
             pk[rr] = 0u;
 #pragma unroll
-            for (int j = 0; j < VPT; ++j) pk[rr] = absmax_bf16x8(pk[rr], v[rr][j]);
+            for (int j = 0; j < VPT; ++j) {
+                v[rr][j] = cur[(rr * VPT + j) * QA_THREADS + threadIdx.x];
+                pk[rr] = absmax_bf16x8(pk[rr], v[rr][j]);
+            }
         }
         block_amax<R>(pk, am, red);
 #pragma unroll
         for (int rr = 0; rr < R; ++rr) {
             const int64_t row = base + rr;
-            if (row >= lim) break;
-            const int e = act_exponent(am[rr]);
-            const float inv = __uint_as_float((uint32_t)(127 - e) << 23);
-            if (threadIdx.x == 0) sg.scale[row] = __uint_as_float((uint32_t)(127 + e) << 23);
-            uint2* dst = reinterpret_cast<uint2*>(sg.dst + row * sg.K);
+            if (row < lim) {
+                const int e = act_exponent(am[rr]);
+                const float inv = __uint_as_float((uint32_t)(127 - e) << 23);
+                if (threadIdx.x == 0) sg.scale[row] = __uint_as_float((uint32_t)(127 + e) << 23);
+                uint2* dst = reinterpret_cast<uint2*>(sg.dst + row * sg.K);
 #pragma unroll
-            for (int j = 0; j < VPT; ++j) {
-                const int idx = threadIdx.x + j * QA_THREADS;
-                if (idx < vec) {
-                    float f[8];
-                    unpack8(v[rr][j], f);
-                    dst[idx] = make_uint2(e4m3x4(f, inv), e4m3x4(f + 4, inv));
+                for (int j = 0; j < VPT; ++j) {
+                    const int idx = threadIdx.x + j * QA_THREADS;
+                    if (idx < vec) {
+                        float f[8];
+                        unpack8(v[rr][j], f);
+                        dst[idx] = make_uint2(e4m3x4(f, inv), e4m3x4(f + 4, inv));
+                    }
                 }
             }
         }
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
-// long rows: one row per CTA iteration, read twice (amax, then quantise)
+// long rows (more than 8192 values): one row per CTA iteration, read twice (amax,
+// then quantise)
 __device__ __forceinline__ void quantize_rows_loop(const ActQuantSeg& sg, int64_t lim, uint32_t* red, int cta) {
     const int vec = sg.K / 8;
     for (int64_t row = cta; row < lim; row += gridDim.x) {
@@ -188,7 +228,8 @@ __device__ __forceinline__ void quantize_rows_loop(const ActQuantSeg& sg, int64_
 }
 
 __global__ void __launch_bounds__(QA_THREADS) quantize_act_rows_kernel(const __grid_constant__ ActQuantArgs a) {
-    __shared__ uint32_t red[8 * QA_WARPS];
+    __shared__ uint32_t red[QA_VEC * QA_WARPS];
+    __shared__ uint4 stage[2 * QA_VEC * QA_THREADS];  // 32 KB: two row groups
     pdl_wait();
     pdl_trigger();
     for (int si = 0; si < a.nseg; ++si) {
@@ -199,13 +240,11 @@ __global__ void __launch_bounds__(QA_THREADS) quantize_act_rows_kernel(const __g
         // the second row set starts from the last CTA, so small launches run both at once
         const int cta = si ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
         if (vpt <= 1)
-            quantize_rows_regs<1>(sg, lim, red, cta);
+            quantize_rows_staged<1>(sg, lim, red, stage, cta);
         else if (vpt <= 2)
-            quantize_rows_regs<2>(sg, lim, red, cta);
+            quantize_rows_staged<2>(sg, lim, red, stage, cta);
         else if (vpt <= 4)
-            quantize_rows_regs<4>(sg, lim, red, cta);
-        else if (vpt <= 8)
-            quantize_rows_regs<8>(sg, lim, red, cta);
+            quantize_rows_staged<4>(sg, lim, red, stage, cta);
         else
             quantize_rows_loop(sg, lim, red, cta);
     }
@@ -219,15 +258,26 @@ cudaError_t launch_quantize_act_rows(const ActQuantSeg* seg, int nseg, int num_s
     for (int i = 0; i < nseg && i < 2; ++i)
         if (seg[i].rows > 0) a.seg[a.nseg++] = seg[i];
     if (a.nseg == 0) return cudaSuccess;
-    // one CTA per row group of the two row sets together, at most the resident
-    // CTAs (3 per SM)
+    // one CTA per row group of the two row sets together, at most one wave of
+    // resident CTAs (several per SM: 32 KB of staging each, so the largest
+    // shared-memory carve-out)
+    static std::once_flag once;
+    static int per_sm = 1;
+    std::call_once(once, [] {
+        cudaFuncSetAttribute(quantize_act_rows_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quantize_act_rows_kernel, QA_THREADS, 0) ==
+                cudaSuccess &&
+            n > 0)
+            per_sm = n;
+    });
     int64_t want = 0;
     for (int i = 0; i < a.nseg; ++i) {
         const int vpt = (a.seg[i].K / 8 + QA_THREADS - 1) / QA_THREADS;
-        const int R = vpt <= 1 ? 8 : vpt <= 2 ? 4 : vpt <= 4 ? 2 : 1;
+        const int R = vpt <= 1 ? 4 : vpt <= 2 ? 2 : 1;
         want += (a.seg[i].rows + R - 1) / R;
     }
-    const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms * 3));
+    const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms * per_sm));
     return launch_k(quantize_act_rows_kernel, dim3(grid), dim3(QA_THREADS), 0, s, a);
 }
 

@@ -412,10 +412,10 @@ def test_quantize_act_rows_bit_exact():
     v[7] = torch.full((192,), 2.0 ** -130)            # bf16 subnormals: the scale clamps at 2^-126
     v[8, 0] = 1e30                                    # one huge value: the rest round to zero
     v = v.to(torch.bfloat16)
-    # row lengths for each register layout of the kernel (1, 2, 4, 8 vectors of 8 per
-    # thread) and for its two-pass loop (more than 16384 values)
+    # row lengths for each staging layout of the kernel (1, 2, 4 vectors of 8 values
+    # per thread and row) and for its two-pass loop (more than 8192 values)
     sets = [(192, v)] + [(K, (torch.randn(n, K, generator=g) * 3).to(torch.bfloat16))
-                         for K, n in ((3072, 21), (7168, 33), (16384, 5), (16448, 3))]
+                         for K, n in ((3072, 21), (7168, 33), (8192, 6), (8256, 4), (16448, 3))]
     for K, vv in sets:
         q_ref, s_ref = oracle.quantize_act_rows(vv)
         q = torch.empty(vv.shape, dtype=torch.uint8, device="cuda")
