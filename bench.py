@@ -42,10 +42,12 @@ DEFAULT_WORKLOAD = "qwen2_moe_like_prefill"
 # from one ncu capture of that workload, valid only while the kernel source hashes to
 # the recorded value.
 NCU_TRAFFIC = {
-    # FC1 of the first forward, ncu --set full: 822.35 MB read + 88.17 MB written
-    ("qwen2_moe_like_prefill", "e290cf4b326bbfbe"): 910.52e6,
-    # FC1 of the first forward, ncu --set full: 115.41 MB read + 3.18 MB written
-    ("dsv2_lite_like_decode_t1", "e290cf4b326bbfbe"): 118.60e6,
+    # FC1 of the first forward, ncu --set full: 822.21 MB read + 87.64 MB written
+    ("qwen2_moe_like_prefill", "696982a70cb38b2f"): 909.85e6,
+    # FC1 of the first forward, ncu --set full: 115.41 MB read + 3.26 MB written
+    ("dsv2_lite_like_decode_t1", "696982a70cb38b2f"): 118.67e6,
+    # FC1 (E4M3 operands) of the first forward, ncu --set full: 412.00 MB read + 81.62 MB written
+    ("qwen2_moe_like_prefill_w8a8", "696982a70cb38b2f"): 493.62e6,
 }
 
 
