@@ -49,6 +49,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <climits>
 #include <mutex>
 
 #include "moe_internal.cuh"
@@ -117,6 +118,7 @@ struct SmemMeta {
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t drain;
+    uint64_t ready;   // the routed tile prefix (off, ts, routed_tiles) is written
     uint32_t tmem_base;
     int abort;
     volatile int conv_ok;
@@ -268,6 +270,7 @@ __global__ void __launch_bounds__(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS,
             mbar_init(&m.tempty[b], kPair ? 8 : 4);  // pair mode: the epilogue warps of both CTAs
         }
         mbar_init(&m.drain, 1);
+        mbar_init(&m.ready, 1);
         m.abort = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmA);
@@ -286,7 +289,35 @@ __global__ void __launch_bounds__(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS,
             tmem_relinquish();
         }
     }
-    // everything above touches no memory of earlier kernels; from here on it may
+    tc_fence_before();
+    if (kPair) {
+        __syncwarp();        // barrier.cluster.*.aligned: each warp arrives converged
+        cluster_sync_all();  // the peer's multicasts may target this CTA's barriers from here on
+    } else {
+        __syncthreads();
+    }
+    tc_fence_after();
+
+    const uint32_t tmem_base = m.tmem_base;
+    const int mu_sh = p.T_sh > 0 ? units_of<kPair>((int)((p.T_sh + BM - 1) / BM)) : 0;
+    const int n_sh_tiles = p.T_sh > 0 ? mu_sh * ((p.N_out_sh + OW - 1) / OW) * p.ksplit_sh : 0;
+    const volatile int* abortp = &m.abort;
+    // units below n_sh_tiles need no prefix; the bound for the others is known once
+    // m.ready has completed (-1: the wait gave up)
+    auto unit_bound = [&](int u, bool& have) -> int {
+        if (u < n_sh_tiles) return INT_MAX;
+        if (!have) {
+            if (!mbar_wait(&m.ready, 0, p.timeout_ns, abortp)) return -1;
+            have = true;
+        }
+        return n_sh_tiles + m.routed_tiles;
+    };
+
+    // everything above touches no memory of earlier kernels; from here on it may.
+    // The shared problem's units need only their operands, so the roles start on
+    // them at once; warp 2 meanwhile builds the routed tile prefix from the offsets
+    // and publishes it on m.ready, which every role waits for before its first
+    // routed unit.
     pdl_wait();
     pdl_trigger();
     if (warp == 2) {
@@ -321,21 +352,9 @@ __global__ void __launch_bounds__(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS,
             m.routed_tiles = total;
             if (!ok) report(p.status, MOE_ERR_DEVICE_BOUNDS);
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&m.ready);
     }
-    tc_fence_before();
-    if (kPair) {
-        __syncwarp();        // barrier.cluster.*.aligned: each warp arrives converged
-        cluster_sync_all();  // the peer's multicasts may target this CTA's barriers from here on
-    } else {
-        __syncthreads();
-    }
-    tc_fence_after();
-
-    const uint32_t tmem_base = m.tmem_base;
-    const int mu_sh = p.T_sh > 0 ? units_of<kPair>((int)((p.T_sh + BM - 1) / BM)) : 0;
-    const int n_sh_tiles = p.T_sh > 0 ? mu_sh * ((p.N_out_sh + OW - 1) / OW) * p.ksplit_sh : 0;
-    const int total_tiles = n_sh_tiles + m.routed_tiles;
-    const volatile int* abortp = &m.abort;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -343,7 +362,14 @@ __global__ void __launch_bounds__(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS,
             uint32_t stage = 0, phase = 0;
             int64_t issued = 0;
             bool failed = false;
-            for (int u = unit0; u < total_tiles && !failed; u += nunits) {
+            bool have = false;
+            for (int u = unit0; !failed; u += nunits) {
+                const int bound = unit_bound(u, have);
+                if (bound < 0) {
+                    failed = true;
+                    break;
+                }
+                if (u >= bound) break;
                 const Tile tl = tile_of<kFC1, kPair>(u, p, m, n_sh_tiles, mu_sh, crank);
                 // a tile with at most 32 rows of its group loads only 32 A rows: the MMA
                 // still reads 128, but rows past the group's count are never stored
@@ -425,7 +451,14 @@ __global__ void __launch_bounds__(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS,
             uint32_t stage = 0, phase = 0;
             bool failed = false;
             int i = 0;
-            for (int u = unit0; u < total_tiles && !failed; u += nunits, ++i) {
+            bool have = false;
+            for (int u = unit0; !failed; u += nunits, ++i) {
+                const int bound = unit_bound(u, have);
+                if (bound < 0) {
+                    failed = true;
+                    break;
+                }
+                if (u >= bound) break;
                 const Tile tl = tile_of<kFC1, kPair>(u, p, m, n_sh_tiles, mu_sh, crank);
                 const int nkb = tl.kb1 - tl.kb0;
                 const int buf = i & 1;
@@ -486,7 +519,18 @@ __global__ void __launch_bounds__(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS,
         const int q = warp & 3;              // TMEM lane quarter of this warp
         const int row_in = q * 32 + lane;    // tile row of this thread
         int i = 0;
-        for (int u = unit0; u < total_tiles; u += nunits, ++i) {
+        bool have = false;
+        for (int u = unit0;; u += nunits, ++i) {
+            // every lane waits; the warp goes on only if all of them saw the prefix
+            const int bound = unit_bound(u, have);
+            if (!__all_sync(0xffffffffu, bound >= 0)) {
+                if (lane == 0) {
+                    m.abort = 1;
+                    report(p.status, MOE_ERR_TIMEOUT);
+                }
+                break;
+            }
+            if (u >= bound) break;
             const Tile tl = tile_of<kFC1, kPair>(u, p, m, n_sh_tiles, mu_sh, crank);
             const int buf = i & 1;
             // every lane polls; the warp proceeds (reconverged, as tcgen05.ld
@@ -607,6 +651,12 @@ __global__ void __launch_bounds__(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS,
         constexpr int CPT = (BN * 4 + CONV_THREADS - 1) / CONV_THREADS;  // 16-byte E4M3 chunks per thread
         uint32_t stage = 0, phase = 0;
         bool failed = false;
+        // the tile sequence of all units is needed up front (one thread waits for the
+        // prefix; the named barrier passes its verdict on)
+        if (ct == 0) m.conv_ok = mbar_wait(&m.ready, 0, p.timeout_ns, abortp) ? 1 : 0;
+        asm volatile("bar.sync %0, %1;" ::"n"(CONV_BARRIER), "n"(CONV_THREADS) : "memory");
+        failed = !m.conv_ok;
+        const int total_tiles = n_sh_tiles + m.routed_tiles;
         for (int u = unit0; u < total_tiles && !failed; u += nunits) {
             const Tile tl = tile_of<kFC1, kPair>(u, p, m, n_sh_tiles, mu_sh, crank);
             const int nkb = tl.kb1 - tl.kb0;
