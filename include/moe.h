@@ -295,8 +295,12 @@ MOE_API moe_status_t moe_quantize_fp8_rows(const moe_bf16_t *w, int64_t rows, in
  * power-of-two scale (moe_quantize_act_rows); the shared experts' input is x,
  * quantised the same way per token.  FC1 and FC2 then run on E4M3 operands
  * (tcgen05.mma kind::f8f6f4, fp32 accumulation), and each accumulator is
- * multiplied by its A row's and its B row's scale.  Launches two quantisation
- * kernels besides moe_forward's three.  The workspace regions for the
+ * multiplied by its A row's and its B row's scale.  With topk_w given (weights
+ * applied at the output) the rows of x_perm must be the copies of token rows
+ * that moe_permute writes: for batches of more than 64 tokens the call then
+ * quantises each row of x once and places its codes at the token's pair rows
+ * (pair_row) without reading x_perm; otherwise, and with topk_w = NULL
+ * (moe_permute_on_input) or x = NULL, it quantises the rows of x_perm.  Launches two quantisation kernels besides moe_forward's three.  The workspace regions for the
  * quantised rows are part of moe_workspace_size.  Arguments, layouts,
  * ownership and errors as moe_forward_fp8. */
 MOE_API moe_status_t moe_forward_w8a8(const moe_bf16_t *x_perm, const int32_t *offsets, int S_local, int64_t P_cap,

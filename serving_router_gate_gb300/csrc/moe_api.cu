@@ -509,9 +509,23 @@ static moe_status_t forward_impl(const moe_bf16_t* x_perm, const int32_t* offset
         const int64_t T_sh = I_shared_total > 0 ? T : 0;
         auto u8 = [&](size_t off) { return reinterpret_cast<uint8_t*>(base + off); };
         auto f32 = [&](size_t off) { return reinterpret_cast<float*>(base + off); };
-        const ActQuantSeg qx[2] = {{x_perm, P_cap, offsets + S_local, H, u8(FL.xq), f32(FL.sxq)},
-                                   {x, T_sh, nullptr, H, u8(FL.xsq), f32(FL.sxs)}};
-        st = cuda_status(launch_quantize_act_rows(qx, 2, sms, s));
+        if (topk_w && x && T > 64) {
+            // weights applied at the output: the expert input rows are copies of token
+            // rows, so each token row is quantised once and its codes are placed at its
+            // pairs' rows (and kept for the shared experts); small batches quantise the
+            // rows themselves, spread over more CTAs
+            ActQuantSeg q = {x, T, nullptr, H, T_sh > 0 ? u8(FL.xsq) : nullptr, f32(FL.sxs)};
+            q.pair_row = pair_row;
+            q.k = k;
+            q.dst2 = u8(FL.xq);
+            q.scale2 = f32(FL.sxq);
+            q.dst2_rows = P_cap;
+            st = cuda_status(launch_quantize_act_rows(&q, 1, sms, s));
+        } else {
+            const ActQuantSeg qx[2] = {{x_perm, P_cap, offsets + S_local, H, u8(FL.xq), f32(FL.sxq)},
+                                       {x, T_sh, nullptr, H, u8(FL.xsq), f32(FL.sxs)}};
+            st = cuda_status(launch_quantize_act_rows(qx, 2, sms, s));
+        }
         if (st != MOE_OK) return st;
         st = gemm_call(true, reinterpret_cast<const moe_bf16_t*>(u8(FL.xq)), P_cap, offsets, S_local,
                        static_cast<const moe_bf16_t*>(W1), H, I, reinterpret_cast<const moe_bf16_t*>(u8(FL.xsq)), T,

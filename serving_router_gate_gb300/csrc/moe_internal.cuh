@@ -449,8 +449,15 @@ struct ActQuantSeg {
     int64_t rows;
     const int32_t* rows_dev;   // or null
     int K;
-    uint8_t* dst;              // [rows, K]
+    uint8_t* dst;              // [rows, K], or null
     float* scale;              // [rows]
+    // optional: row t's codes and scale also go to rows pair_row[t * k + j] (j < k;
+    // -1 and rows past dst2_rows skipped) of dst2 / scale2
+    const int32_t* pair_row;
+    int k;
+    uint8_t* dst2;
+    float* scale2;
+    int64_t dst2_rows;
 };
 cudaError_t launch_quantize_act_rows(const ActQuantSeg* seg, int nseg, int num_sms, cudaStream_t s);
 cudaError_t launch_quantize_fp8_rows(const uint16_t* w, int64_t rows, int K, uint8_t* q, float* scale, int num_sms,

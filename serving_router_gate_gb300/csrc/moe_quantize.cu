@@ -133,6 +133,35 @@ __device__ __forceinline__ void block_amax(const uint32_t (&pk)[R], float (&am)[
     __syncthreads();  // red is rewritten by the next group
 }
 
+// The codes of source row `row` (vector j of this thread: q[j]) and its scale go
+// to row `row` of dst and, with pair_row, to each pair row of dst2.
+template <int VPT>
+__device__ __forceinline__ void store_row(const ActQuantSeg& sg, int64_t row, const uint2 (&q)[VPT], float scale) {
+    const int vec = sg.K / 8;
+    if (sg.dst) {
+        if (threadIdx.x == 0) sg.scale[row] = scale;
+        uint2* dst = reinterpret_cast<uint2*>(sg.dst + row * sg.K);
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int idx = threadIdx.x + j * QA_THREADS;
+            if (idx < vec) dst[idx] = q[j];
+        }
+    }
+    if (sg.pair_row) {
+        for (int jj = 0; jj < sg.k; ++jj) {
+            const int32_t r = __ldg(sg.pair_row + row * sg.k + jj);
+            if (r < 0 || (int64_t)r >= sg.dst2_rows) continue;
+            if (threadIdx.x == 0) sg.scale2[r] = scale;
+            uint2* dst = reinterpret_cast<uint2*>(sg.dst2 + (int64_t)r * sg.K);
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                const int idx = threadIdx.x + j * QA_THREADS;
+                if (idx < vec) dst[idx] = q[j];
+            }
+        }
+    }
+}
+
 // stage[buf][i * QA_THREADS + thread]: vector i = rr * VPT + j of the group
 template <int VPT>
 __device__ __forceinline__ void issue_group(uint4* stage, const ActQuantSeg& sg, int64_t base, int64_t lim) {
@@ -188,17 +217,14 @@ __device__ __forceinline__ void quantize_rows_staged(const ActQuantSeg& sg, int6
             if (row < lim) {
                 const int e = act_exponent(am[rr]);
                 const float inv = __uint_as_float((uint32_t)(127 - e) << 23);
-                if (threadIdx.x == 0) sg.scale[row] = __uint_as_float((uint32_t)(127 + e) << 23);
-                uint2* dst = reinterpret_cast<uint2*>(sg.dst + row * sg.K);
+                uint2 q[VPT];
 #pragma unroll
                 for (int j = 0; j < VPT; ++j) {
-                    const int idx = threadIdx.x + j * QA_THREADS;
-                    if (idx < vec) {
-                        float f[8];
-                        unpack8(v[rr][j], f);
-                        dst[idx] = make_uint2(e4m3x4(f, inv), e4m3x4(f + 4, inv));
-                    }
+                    float f[8];
+                    unpack8(v[rr][j], f);
+                    q[j] = make_uint2(e4m3x4(f, inv), e4m3x4(f + 4, inv));
                 }
+                store_row<VPT>(sg, row, q, __uint_as_float((uint32_t)(127 + e) << 23));
             }
         }
     }
@@ -217,12 +243,26 @@ __device__ __forceinline__ void quantize_rows_loop(const ActQuantSeg& sg, int64_
         block_amax<1>(pk, am, red);
         const int e = act_exponent(am[0]);
         const float inv = __uint_as_float((uint32_t)(127 - e) << 23);
-        if (threadIdx.x == 0) sg.scale[row] = __uint_as_float((uint32_t)(127 + e) << 23);
-        uint2* dst = reinterpret_cast<uint2*>(sg.dst + row * sg.K);
+        const float sc = __uint_as_float((uint32_t)(127 + e) << 23);
+        if (threadIdx.x == 0) {
+            if (sg.dst) sg.scale[row] = sc;
+            if (sg.pair_row)
+                for (int jj = 0; jj < sg.k; ++jj) {
+                    const int32_t r = __ldg(sg.pair_row + row * sg.k + jj);
+                    if (r >= 0 && (int64_t)r < sg.dst2_rows) sg.scale2[r] = sc;
+                }
+        }
         for (int idx = threadIdx.x; idx < vec; idx += QA_THREADS) {
             float f[8];
             unpack8(__ldg(src + idx), f);
-            dst[idx] = make_uint2(e4m3x4(f, inv), e4m3x4(f + 4, inv));
+            const uint2 q = make_uint2(e4m3x4(f, inv), e4m3x4(f + 4, inv));
+            if (sg.dst) reinterpret_cast<uint2*>(sg.dst + row * sg.K)[idx] = q;
+            if (sg.pair_row)
+                for (int jj = 0; jj < sg.k; ++jj) {
+                    const int32_t r = __ldg(sg.pair_row + row * sg.k + jj);
+                    if (r >= 0 && (int64_t)r < sg.dst2_rows)
+                        reinterpret_cast<uint2*>(sg.dst2 + (int64_t)r * sg.K)[idx] = q;
+                }
         }
     }
 }

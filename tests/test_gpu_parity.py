@@ -377,6 +377,13 @@ def test_fp8_weights_partial_tiles_two_shared_and_short_batch():
     _full_check(mi.make_inputs(cfg))
 
 
+def test_fp8_weights_with_routing_on_input():
+    # the quantised expert paths keep apply_routing_on_input (the TensorRT-LLM PR #10985
+    # review notes quantised MoE ops that drop it): rows scaled before FC1, outputs summed
+    # with weight 1
+    _on_input_check(mi.make_inputs(FP8_MID.with_(on_input=True)))
+
+
 def test_fp8_stage_gemms_against_oracle_rows():
     inp = mi.make_inputs(FP8_MID)
     g = run_gpu(inp)
@@ -441,6 +448,9 @@ def test_w8a8_ragged_k_partial_tiles_two_shared_and_short_batch():
     # at most 32 tokens: the short-tile variant, and the split shared FC2
     cfg = mi.MoEConfig("short_w8a8", T=24, H=256, I=128, E=9, k=3, renorm=True, n_shared=2, I_shared=256,
                        shared_gate=True, fp8=True, act8=True)
+    _full_check(mi.make_inputs(cfg))
+    # no shared expert: the token rows' codes go to the pair rows only
+    cfg = mi.MoEConfig("noshared_w8a8", T=300, H=256, I=256, E=6, k=2, renorm=True, fp8=True, act8=True)
     _full_check(mi.make_inputs(cfg))
 
 
