@@ -250,9 +250,16 @@ def run_cpu_baseline(inp_dev, cfg, target_s=10.0, T_cap=None):
     n = int(max(n0, min(T_cap or cfg.T, n0 * target_s / max(t0, 1e-3))))
     n = max(1, min(n, cfg.T))
     t = run(n)
+    # the same oracle on one thread, on a sample of about a quarter of that time
+    oracle.set_threads(1)
+    n1 = max(1, min(cfg.T, int(n / t * target_s / 4 / max(threads, 1))))
+    t1 = run(n1)
+    oracle.set_threads(threads)
     return dict(value=n / t, unit="tokens/s", cores=threads, kind="oracle",
                 sample=f"first {n} of the {cfg.T} tokens of {cfg.name}, whole layer in fp64 "
-                       f"({t:.1f} s, {threads} OpenMP threads)"), t
+                       f"({t:.1f} s, {threads} OpenMP threads)",
+                single_thread_value=n1 / t1,
+                single_thread_sample=f"first {n1} tokens, {t1:.1f} s on one thread"), t
 
 
 def bench_ours(args):
