@@ -42,12 +42,12 @@ DEFAULT_WORKLOAD = "qwen2_moe_like_prefill"
 # from one ncu capture of that workload, valid only while the kernel source hashes to
 # the recorded value.
 NCU_TRAFFIC = {
-    # FC1 of the first forward, ncu --set full: 822.21 MB read + 87.64 MB written
-    ("qwen2_moe_like_prefill", "696982a70cb38b2f"): 909.85e6,
-    # FC1 of the first forward, ncu --set full: 115.41 MB read + 3.26 MB written
-    ("dsv2_lite_like_decode_t1", "696982a70cb38b2f"): 118.67e6,
-    # FC1 (E4M3 operands) of the first forward, ncu --set full: 412.00 MB read + 81.62 MB written
-    ("qwen2_moe_like_prefill_w8a8", "696982a70cb38b2f"): 493.62e6,
+    # FC1 of the first forward, ncu --set full: 822.22 MB read + 87.97 MB written
+    ("qwen2_moe_like_prefill", "2d15891afb042227"): 910.20e6,
+    # FC1 of the first forward, ncu --set full: 115.42 MB read + 3.24 MB written
+    ("dsv2_lite_like_decode_t1", "2d15891afb042227"): 118.66e6,
+    # FC1 (E4M3 operands) of the first forward, ncu --set full: 411.94 MB read + 81.72 MB written
+    ("qwen2_moe_like_prefill_w8a8", "2d15891afb042227"): 493.66e6,
 }
 
 
