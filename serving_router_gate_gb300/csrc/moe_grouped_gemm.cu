@@ -49,7 +49,6 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
-#include <climits>
 #include <mutex>
 
 #include "moe_internal.cuh"
@@ -302,15 +301,40 @@ __global__ void __launch_bounds__(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS,
     const int mu_sh = p.T_sh > 0 ? units_of<kPair>((int)((p.T_sh + BM - 1) / BM)) : 0;
     const int n_sh_tiles = p.T_sh > 0 ? mu_sh * ((p.N_out_sh + OW - 1) / OW) * p.ksplit_sh : 0;
     const volatile int* abortp = &m.abort;
-    // units below n_sh_tiles need no prefix; the bound for the others is known once
-    // m.ready has completed (-1: the wait gave up)
-    auto unit_bound = [&](int u, bool& have) -> int {
-        if (u < n_sh_tiles) return INT_MAX;
+    // This CTA's units, in order: its shared-problem units unit0 + j * nunits first
+    // (they need no prefix), then routed units, once m.ready has published the prefix.
+    // Where the shared units split unevenly over the CTAs, each CTA with one shared unit
+    // fewer first takes q routed units (q = the shared-to-routed K-step ratio, rounded),
+    // so the K steps per CTA even out; the remaining routed units go round-robin.  With
+    // q = 1, or fewer than q routed units per CTA (streaming launches, where spreading
+    // the units over more SMs matters more), this is plain round-robin over all units.  next_unit(i) returns the
+    // i-th unit, -1 past the last, -2 if the wait for the prefix gave up.
+    const int n_long = unit0 < n_sh_tiles ? (n_sh_tiles - unit0 + nunits - 1) / nunits : 0;
+    const int light0 = n_sh_tiles % nunits;  // first CTA with one shared unit fewer
+    const int len_sh = p.ksplit_sh > 1 ? p.kb_split_sh : p.kb_total_sh;
+    const int len_rt = max(1, p.kb_total);
+    const int bonus_q = light0 == 0 ? 0 : max(1, (len_sh + len_rt / 2) / len_rt);
+    auto next_unit = [&](int i, bool& have) -> int {
+        if (i < n_long) return unit0 + i * nunits;
         if (!have) {
-            if (!mbar_wait(&m.ready, 0, p.timeout_ns, abortp)) return -1;
+            if (!mbar_wait(&m.ready, 0, p.timeout_ns, abortp)) return -2;
             have = true;
         }
-        return n_sh_tiles + m.routed_tiles;
+        const int routed = m.routed_tiles;
+        int j = i - n_long;
+        int bonus_total = 0;
+        if (bonus_q > 0) {
+            const int q = routed >= nunits * bonus_q ? bonus_q : 1;
+            bonus_total = min((nunits - light0) * q, routed);
+            if (unit0 >= light0) {
+                const int b0 = (unit0 - light0) * q;
+                const int nb = max(0, min(q, bonus_total - b0));
+                if (j < nb) return n_sh_tiles + b0 + j;
+                j -= nb;
+            }
+        }
+        const int r = bonus_total + unit0 + j * nunits;
+        return r < routed ? n_sh_tiles + r : -1;
     };
 
     // everything above touches no memory of earlier kernels; from here on it may.
@@ -363,13 +387,13 @@ __global__ void __launch_bounds__(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS,
             int64_t issued = 0;
             bool failed = false;
             bool have = false;
-            for (int u = unit0; !failed; u += nunits) {
-                const int bound = unit_bound(u, have);
-                if (bound < 0) {
+            for (int iu = 0; !failed; ++iu) {
+                const int u = next_unit(iu, have);
+                if (u == -2) {
                     failed = true;
                     break;
                 }
-                if (u >= bound) break;
+                if (u < 0) break;
                 const Tile tl = tile_of<kFC1, kPair>(u, p, m, n_sh_tiles, mu_sh, crank);
                 // a tile with at most 32 rows of its group loads only 32 A rows: the MMA
                 // still reads 128, but rows past the group's count are never stored
@@ -452,13 +476,13 @@ __global__ void __launch_bounds__(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS,
             bool failed = false;
             int i = 0;
             bool have = false;
-            for (int u = unit0; !failed; u += nunits, ++i) {
-                const int bound = unit_bound(u, have);
-                if (bound < 0) {
+            for (;; ++i) {
+                const int u = next_unit(i, have);
+                if (u == -2) {
                     failed = true;
                     break;
                 }
-                if (u >= bound) break;
+                if (u < 0) break;
                 const Tile tl = tile_of<kFC1, kPair>(u, p, m, n_sh_tiles, mu_sh, crank);
                 const int nkb = tl.kb1 - tl.kb0;
                 const int buf = i & 1;
@@ -520,17 +544,17 @@ __global__ void __launch_bounds__(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS,
         const int row_in = q * 32 + lane;    // tile row of this thread
         int i = 0;
         bool have = false;
-        for (int u = unit0;; u += nunits, ++i) {
+        for (;; ++i) {
             // every lane waits; the warp goes on only if all of them saw the prefix
-            const int bound = unit_bound(u, have);
-            if (!__all_sync(0xffffffffu, bound >= 0)) {
+            const int u = next_unit(i, have);
+            if (!__all_sync(0xffffffffu, u != -2)) {
                 if (lane == 0) {
                     m.abort = 1;
                     report(p.status, MOE_ERR_TIMEOUT);
                 }
                 break;
             }
-            if (u >= bound) break;
+            if (u < 0) break;
             const Tile tl = tile_of<kFC1, kPair>(u, p, m, n_sh_tiles, mu_sh, crank);
             const int buf = i & 1;
             // every lane polls; the warp proceeds (reconverged, as tcgen05.ld
@@ -656,8 +680,10 @@ __global__ void __launch_bounds__(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS,
         if (ct == 0) m.conv_ok = mbar_wait(&m.ready, 0, p.timeout_ns, abortp) ? 1 : 0;
         asm volatile("bar.sync %0, %1;" ::"n"(CONV_BARRIER), "n"(CONV_THREADS) : "memory");
         failed = !m.conv_ok;
-        const int total_tiles = n_sh_tiles + m.routed_tiles;
-        for (int u = unit0; u < total_tiles && !failed; u += nunits) {
+        bool have = true;  // the prefix is published (waited for above)
+        for (int iu = 0; !failed; ++iu) {
+            const int u = next_unit(iu, have);
+            if (u < 0) break;
             const Tile tl = tile_of<kFC1, kPair>(u, p, m, n_sh_tiles, mu_sh, crank);
             const int nkb = tl.kb1 - tl.kb0;
             for (int kb = 0; kb < nkb; ++kb) {
