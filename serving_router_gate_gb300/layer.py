@@ -106,8 +106,10 @@ class MoELayer:
         xs = x if (self.I_sh > 0) else None
         if self.fp8:
             fwd = moe_forward_w8a8 if self.act8 else moe_forward_fp8
-            fwd(v["x_perm"], v["offsets"], self.W1q, self.s1, self.W2q, self.s2, v["pair_row"], w, xs,
-                            self.W1sq, self.s1s, self.W2sq, self.s2s, self.gate, v["out"], self.ws, stream)
+            # E4M3 activations: x also lets large batches quantise each token row once
+            xa = x if self.act8 else xs
+            fwd(v["x_perm"], v["offsets"], self.W1q, self.s1, self.W2q, self.s2, v["pair_row"], w, xa,
+                self.W1sq, self.s1s, self.W2sq, self.s2s, self.gate, v["out"], self.ws, stream)
         else:
             moe_forward(v["x_perm"], v["offsets"], self.W1, self.W2, v["pair_row"], w, xs, self.W1s, self.W2s,
                         self.gate, v["out"], self.ws, stream)
