@@ -43,7 +43,11 @@
 // routed problem, whose ragged per-slot row counts are read on the device from
 // the offsets array (no host synchronisation): slot g has ceil(M_g / 128)
 // m-tiles; within a slot, tiles run n-tile-major so consecutive CTAs share the
-// same weight tile through L2.  Every wait is bounded: on a timeout the CTA
+// same weight tile through L2.  The CTAs take tiles round-robin; when the shared
+// tiles are longer than the routed ones, a CTA with one shared tile fewer first
+// takes as many routed tiles as make up the difference.  The shared tiles start
+// before the routed prefix is built (it arrives on an mbarrier).  Every wait is
+// bounded: on a timeout the CTA
 // records MOE_ERR_TIMEOUT, drains its in-flight copies and MMAs, frees its
 // tensor memory and exits.
 #include <cudaTypedefs.h>
