@@ -214,8 +214,12 @@ __device__ __forceinline__ void scatter_pairs(int64_t pb, const uint16_t* __rest
         const uint4* src = reinterpret_cast<const uint4*>(x + ((pb + j) / k) * H);
         uint4* dst = reinterpret_cast<uint4*>(x_perm + (int64_t)r * H);
         if (!wsc) {
+#pragma unroll 4
             for (int v = lane; v < vec; v += 32) dst[v] = __ldg(src + v);
         } else {
+            // unrolled so the loads of several vectors are in flight before the first
+            // one's products are rounded
+#pragma unroll 4
             for (int v = lane; v < vec; v += 32) {
                 float f[8];
                 unpack8(__ldg(src + v), f);
