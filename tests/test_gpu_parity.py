@@ -471,6 +471,34 @@ def test_w8a8_local_ranges_and_routing_on_input():
     _on_input_check(mi.make_inputs(W8A8_MID.with_(on_input=True)))
 
 
+def test_w8a8_replica_slots_grouped_topk_and_k_extremes():
+    rep = mi.MoEConfig("rep_w8a8", T=700, H=256, I=256, E=10, S=13, n_hot=3, zipf_s=1.1, k=4, renorm=True,
+                       fp8=True, act8=True)
+    _full_check(mi.make_inputs(rep))
+    grp = mi.MoEConfig("grp_w8a8", T=300, H=256, I=192, E=16, k=4, renorm=False, n_group=4, topk_group=2,
+                       n_shared=1, I_shared=256, fp8=True, act8=True)
+    _full_check(mi.make_inputs(grp))
+    for k in (1, 6):  # top-1, and every expert of the batch
+        cfg = mi.MoEConfig(f"k{k}_w8a8", T=130, H=256, I=128, E=6, k=k, renorm=True, fp8=True, act8=True)
+        _full_check(mi.make_inputs(cfg))
+
+
+def test_w8a8_empty_range_zero_tokens_and_determinism():
+    cfg = mi.MoEConfig("empty_w8a8", T=100, H=256, I=256, E=8, k=2, renorm=True, fp8=True, act8=True)
+    inp = mi.make_inputs(cfg)
+    inp["bias"] = torch.zeros(cfg.E)
+    inp["bias"][:4] = 60.0  # experts 4..7 are never chosen
+    g, _ = _full_check(inp, 4, 4, moe.MOE_NONLOCAL_SKIP)
+    assert g["rows"] == 0 and torch.count_nonzero(g["out"].float()) == 0
+    layer = layer_from_inputs(mi.make_inputs(W8A8_MID), "cuda")
+    assert layer.forward(torch.zeros((0, W8A8_MID.H), dtype=torch.bfloat16, device="cuda")).shape[0] == 0
+    x = mi.make_inputs(W8A8_MID)["x"].cuda()
+    a = layer.forward(x).clone()
+    b = layer.forward(x).clone()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert moe.moe_get_device_status(layer.ws) == 0
+
+
 def test_w8a8_stage_gemms_against_oracle_rows():
     inp = mi.make_inputs(W8A8_MID)
     g = run_gpu(inp)
