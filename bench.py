@@ -42,12 +42,12 @@ DEFAULT_WORKLOAD = "qwen2_moe_like_prefill"
 # from one ncu capture of that workload, valid only while the kernel source hashes to
 # the recorded value.
 NCU_TRAFFIC = {
-    # FC1 of the first forward, ncu --set full: 822.20 MB read + 87.75 MB written
-    ("qwen2_moe_like_prefill", "d3f758dbc935add5"): 909.94e6,
-    # FC1 of the first forward, ncu --set full: 115.42 MB read + 3.22 MB written
-    ("dsv2_lite_like_decode_t1", "d3f758dbc935add5"): 118.64e6,
-    # FC1 (E4M3 operands) of the first forward, ncu --set full: 412.00 MB read + 82.14 MB written
-    ("qwen2_moe_like_prefill_w8a8", "d3f758dbc935add5"): 494.14e6,
+    # FC1 of the first forward, ncu --set full: 822.22 MB read + 87.98 MB written
+    ("qwen2_moe_like_prefill", "815b23aea88b128d"): 910.20e6,
+    # FC1 of the first forward, ncu --set full: 115.42 MB read + 3.04 MB written
+    ("dsv2_lite_like_decode_t1", "815b23aea88b128d"): 118.46e6,
+    # FC1 (E4M3 operands) of the first forward, ncu --set full: 411.94 MB read + 81.70 MB written
+    ("qwen2_moe_like_prefill_w8a8", "815b23aea88b128d"): 493.63e6,
 }
 
 
@@ -75,6 +75,7 @@ class ClockSampler:
         self.dev = device_index
         self.proc = None
         self.path = None
+        self.n_before = 0
 
     def start(self):
         try:
@@ -86,6 +87,20 @@ class ClockSampler:
                                          stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            return
+        # nvidia-smi takes a moment to start: let its first sample land before the
+        # timed region opens, then remember how many samples predate the region
+        t_end = time.time() + 5.0
+        while time.time() < t_end and self._lines() == 0:
+            time.sleep(0.01)
+        self.n_before = self._lines()
+
+    def _lines(self):
+        try:
+            with open(self.path) as f:
+                return sum(1 for ln in f if ln.endswith("\n"))
+        except OSError:
+            return 0
 
     def stop(self):
         if self.proc is None:
@@ -98,7 +113,10 @@ class ClockSampler:
         self.f.close()
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
+        lines = open(self.path).readlines()
+        # the samples taken inside the region, plus the last one before it opened
+        n_in = max(0, len(lines) - self.n_before)
+        for line in lines[max(0, self.n_before - 1):]:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -114,7 +132,7 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+                "samples_in_region": n_in, "interval_ms": 50, "reasons": sorted(reasons)}
 
 
 class L2Flush:
@@ -151,6 +169,58 @@ def time_steps(fns, K, flush, stream):
             e[j + 1].record(stream)
     torch.cuda.synchronize()
     return [[e[j].elapsed_time(e[j + 1]) for e in evs] for j in range(len(fns))]
+
+
+def kernel_breakdown(layer, x, n_launch, K, W, flush, stream):
+    """Each kernel of one layer forward timed on its own: the forward is captured
+    into a CUDA graph with the library's launch-event hook armed, so an event
+    node precedes every kernel it launches and a mark follows the last, and the
+    kernels run without programmatic overlap.  The graph holds exactly the
+    launches of the timed forward (same kernels, tile variants and splits).
+    Returns the kernels' labels and, per kernel, K times in ms (each replay after
+    an L2 flush; the host waits after every replay to read the events)."""
+    import serving_router_gate_gb300 as moe
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_launch + 1)]
+    for e in evs:
+        e.record(stream)  # creates the CUDA events
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    moe.moe_launch_events_arm(evs)
+    try:
+        with torch.cuda.graph(g):
+            layer.forward(x)
+            moe.moe_launch_events_mark()
+        labels = moe.moe_launch_events_used()
+    finally:
+        moe.moe_launch_events_arm(None)
+    if len(labels) != n_launch + 1 or labels[-1] != "mark":
+        raise RuntimeError(f"launch-event hook saw {labels}, expected {n_launch} launches and a mark")
+    for _ in range(W):
+        g.replay()
+    times = [[] for _ in range(n_launch)]
+    for _ in range(K):
+        flush()
+        g.replay()
+        torch.cuda.synchronize()
+        for i in range(n_launch):
+            times[i].append(evs[i].elapsed_time(evs[i + 1]))
+    return labels[:-1], times
+
+
+def _stage_of(label, seen):
+    """The layer stage a kernel label belongs to (E4M3 activation quantisers:
+    the first one quantises the GEMM inputs, the second the intermediates)."""
+    if label.startswith("router_"):
+        return "route"
+    if label.startswith("permute_"):
+        return "permute"
+    if label.startswith("grouped_gemm_fc1"):
+        return "fc1"
+    if label.startswith("grouped_gemm_fc2"):
+        return "fc2"
+    if label == "quantize_act_rows":
+        return "quant_h" if "fc1" in seen else "quant_x"
+    return label
 
 
 def _dist():
@@ -205,8 +275,12 @@ def _work(cfg, rows: int, active_slots: int):
     fc1_bytes = w1 + a_rows * (H * ab + (4 if cfg.act8 else 0)) + rows * I * 2 + T * Ish * 2
     fc2_bytes = (w2 + rows * (I * ab + (4 if cfg.act8 else 0)) + T * (Ish * ab + (4 if cfg.act8 and Ish else 0))
                  + rows * H * 2 + (T * H * 2 if Ish else 0))
+    # the whole layer: both GEMMs' bytes plus the router's x and fp32 gate weights, the
+    # permuted rows written, the expert outputs read back by the combine, and out
+    layer_bytes = (fc1_bytes + fc2_bytes + cfg.E * H * 4 + T * H * 2 + rows * H * 2 + rows * H * 2
+                   + (T * H * 2 if Ish else 0) + T * H * 2)
     return dict(fc1_flops=fc1_flops, fc2_flops=fc2_flops, fc1_bytes=fc1_bytes, fc2_bytes=fc2_bytes,
-                gate_flops=2.0 * T * H * cfg.E)
+                gate_flops=2.0 * T * H * cfg.E, layer_bytes=layer_bytes)
 
 
 def _oracle_fp8(oracle, cfg, cpu):
@@ -307,69 +381,13 @@ def bench_ours(args):
     _barrier(ws_)
     value, ms = aggregate_throughput(T, ms_local, ws_)
 
-    # ---- staged pass: each stage replayed from its own CUDA graph, events between stages ----
-    Ish = cfg.n_shared * cfg.I_shared
-    P = T * cfg.k
-    h = torch.empty((P, cfg.I), dtype=torch.bfloat16, device=dev)
-    y = torch.empty((P, H), dtype=torch.bfloat16, device=dev)
-    h_sh = torch.empty((T, Ish), dtype=torch.bfloat16, device=dev) if Ish else None
-    y_sh = torch.empty((T, H), dtype=torch.bfloat16, device=dev) if Ish else None
-    xs = x if Ish else None
-    stages = {"route": lambda: layer.route(x), "permute": lambda: layer.permute(x)}
-    if layer.act8:
-        xq = torch.empty((P, H), dtype=torch.uint8, device=dev)
-        sx = torch.empty(P, dtype=torch.float32, device=dev)
-        xsq = torch.empty((T, H), dtype=torch.uint8, device=dev) if Ish else None
-        sxs = torch.empty(T, dtype=torch.float32, device=dev) if Ish else None
-        hq = torch.empty((P, cfg.I), dtype=torch.uint8, device=dev)
-        shq = torch.empty(P, dtype=torch.float32, device=dev)
-        hsq = torch.empty((T, Ish), dtype=torch.uint8, device=dev) if Ish else None
-        shs = torch.empty(T, dtype=torch.float32, device=dev) if Ish else None
-
-        def quant_x():
-            moe.moe_quantize_act_rows(layer.x_perm, xq, sx)
-            if Ish:
-                moe.moe_quantize_act_rows(x, xsq, sxs)
-
-        def quant_h():
-            moe.moe_quantize_act_rows(h, hq, shq)
-            if Ish:
-                moe.moe_quantize_act_rows(h_sh, hsq, shs)
-
-        stages["quant_x"] = quant_x
-        stages["fc1"] = lambda: moe.moe_grouped_fc1_w8a8(xq, sx, layer.offsets, layer.W1q, layer.s1, xsq, sxs,
-                                                         layer.W1sq, layer.s1s, h, h_sh, layer.ws)
-        stages["quant_h"] = quant_h
-        stages["fc2"] = lambda: moe.moe_grouped_fc2_w8a8(hq, shq, layer.offsets, layer.W2q, layer.s2, hsq, shs,
-                                                         layer.W2sq, layer.s2s, y, y_sh, layer.ws)
-    elif layer.fp8:
-        stages["fc1"] = lambda: moe.moe_grouped_fc1_fp8(layer.x_perm, layer.offsets, layer.W1q, layer.s1, xs,
-                                                        layer.W1sq, layer.s1s, h, h_sh, layer.ws)
-        stages["fc2"] = lambda: moe.moe_grouped_fc2_fp8(h, layer.offsets, layer.W2q, layer.s2, h_sh, layer.W2sq,
-                                                        layer.s2s, y, y_sh, layer.ws)
-    else:
-        stages["fc1"] = lambda: moe.moe_grouped_fc1(layer.x_perm, layer.offsets, layer.W1, xs, layer.W1s, h, h_sh,
-                                                    layer.ws)
-        stages["fc2"] = lambda: moe.moe_grouped_fc2(h, layer.offsets, layer.W2, h_sh, layer.W2s, y, y_sh, layer.ws)
-    stages["finalize"] = lambda: moe.moe_finalize(y, layer.pair_row, None if layer.on_input else layer.topk_w, y_sh,
-                                                  xs, layer.gate, layer.out, layer.ws)
-    for fn in stages.values():
-        fn()
-    torch.cuda.synchronize()
-    if args.graph:
-        graphs = []
-        for fn in stages.values():
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):
-                fn()
-            graphs.append(g.replay)
-    else:
-        graphs = list(stages.values())
-    for _ in range(W):
-        for g in graphs:
-            g()
-    per_stage = time_steps(graphs, K, flush, stream)
-    stage_ms = {n: statistics.mean(t) for n, t in zip(stages, per_stage)}
+    # ---- per-kernel pass: the same forward, every kernel between its own events ----
+    labels, per_kernel = kernel_breakdown(layer, x, kernels_per_step, K, W, flush, stream)
+    kernel_ms = {}
+    for lab, t in zip(labels, per_kernel):
+        st = _stage_of(lab, kernel_ms)
+        kernel_ms[st] = kernel_ms.get(st, 0.0) + statistics.mean(t)
+    launches_ms = [{"kernel": lab, "ms": statistics.mean(t)} for lab, t in zip(labels, per_kernel)]
 
     # ---- e2e pass: host activations in, host output out ----
     x_pin = x.cpu().pin_memory()
@@ -397,7 +415,7 @@ def bench_ours(args):
     peaks = _peaks()
     wk = _work(cfg, rows, active)
     decode = T <= 256
-    fc1_s = stage_ms["fc1"] * 1e-3
+    fc1_s = kernel_ms["fc1"] * 1e-3
     if decode:
         achieved = wk["fc1_bytes"] / fc1_s / 1e9
         roof = dict(bound="hbm", kernel="grouped_gemm_kernel<FC1+SwiGLU>", achieved=achieved, peak=peaks["hbm"],
@@ -416,6 +434,11 @@ def bench_ours(args):
         per_unit = f"{wk['fc1_flops']:.4g} flops per launch = 4*H*(rows*I + T*I_shared)"
     key = (args.workload, _src_hash(os.path.join(ROOT, "serving_router_gate_gb300", "csrc", "moe_grouped_gemm.cu")))
     roof["traffic"] = NCU_TRAFFIC.get(key)
+    fc1_label = next(lab for lab in labels if lab.startswith("grouped_gemm_fc1"))
+    roof["kernel"] = f"grouped_gemm_kernel<FC1+SwiGLU> ({fc1_label})"
+    roof["timing"] = ("CUDA events recorded on the launching stream right before and after the FC1 kernel, "
+                      "as nodes of a CUDA graph of the whole forward (library launch-event hook), mean of the "
+                      "timed steps, each after an L2 flush")
     roof["work"] = per_unit
 
     total_tokens = T * ws_
@@ -434,9 +457,13 @@ def bench_ours(args):
                 "d2h_bytes_per_step": T * H * 2, "ms_per_step": ms_e2e},
         "gpu_launches": kernels_per_step * K,
         "clocks": clk,
-        "kernels_ms": stage_ms,
+        "kernels_ms": kernel_ms,
+        "launches_ms": launches_ms,
         "tflops_layer": (wk["fc1_flops"] + wk["fc2_flops"] + wk["gate_flops"]) / (ms * 1e-3) / 1e12,
-        "grouped_gemm_tflops": (wk["fc1_flops"] + wk["fc2_flops"]) / ((stage_ms["fc1"] + stage_ms["fc2"]) * 1e-3) / 1e12,
+        "layer_hbm": {"bytes": wk["layer_bytes"], "gbs": wk["layer_bytes"] / (ms * 1e-3) / 1e9,
+                      "frac": wk["layer_bytes"] / (ms * 1e-3) / 1e9 / peaks["hbm"],
+                      "what": "algorithmic bytes of the whole layer step / step time, of the measured HBM peak"},
+        "grouped_gemm_tflops": (wk["fc1_flops"] + wk["fc2_flops"]) / ((kernel_ms["fc1"] + kernel_ms["fc2"]) * 1e-3) / 1e12,
         "rows": rows, "active_slots": active, "router_fp64_rechecked_tokens": refined_per_step,
     }
     if rank == 0 and ws_ == 1 and not args.no_cpu_baseline:
@@ -500,7 +527,7 @@ def bench_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(mi.CONFIGS))

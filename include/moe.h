@@ -420,6 +420,33 @@ MOE_API moe_status_t moe_set_pdl(int enable);
  * capture; replaying it issues them again without counting. */
 MOE_API uint64_t moe_get_launch_count(void);
 
+/* Per-kernel timing of the library's own launches (diagnostics).
+ *
+ * moe_launch_events_arm(events, n): `events` holds n CUDA event handles
+ * (cudaEvent_t, created by the caller with timing enabled; they stay the
+ * caller's and must outlive their use).  While armed, each kernel launch the
+ * library issues first records the next unused event on the launch's stream,
+ * and moe_launch_events_mark records the next one on `stream` with no launch
+ * (to close the last kernel's interval).  Under stream capture the record is
+ * captured as an external event node, so every replay of the graph records the
+ * event again.  While armed, kernels go without programmatic dependent launch,
+ * so the time between consecutive events is one kernel (plus the record).
+ * Once the n events are used, further launches and marks record nothing.
+ * n = 0 (events may be NULL) disarms and forgets the events; arming again
+ * starts from the first event.  Process-wide: arm it only while one host thread
+ * issues library calls.  MOE_ERR_INVALID_ARG for n < 0 or a NULL array with
+ * n > 0; MOE_ERR_CUDA if a record failed (the launch is then not made).
+ *
+ * moe_launch_events_used(names, cap): how many events have been recorded since
+ * arming; when `names` is not NULL, copies the first min(count, cap) labels into
+ * it, MOE_LAUNCH_LABEL_BYTES (48) bytes each, zero-terminated: the kernel's name for a launch (grouped
+ * GEMMs carry their tile variant, e.g. "grouped_gemm_fc1_n256_short"), "mark"
+ * for a mark. */
+#define MOE_LAUNCH_LABEL_BYTES 48
+MOE_API moe_status_t moe_launch_events_arm(void *const *events, int n);
+MOE_API moe_status_t moe_launch_events_mark(moe_stream_t stream);
+MOE_API int moe_launch_events_used(char *names, int cap);
+
 #ifdef __cplusplus
 }
 #endif

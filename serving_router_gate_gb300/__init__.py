@@ -26,7 +26,8 @@ __all__ = [
     "moe_debug_wait_timeout", "moe_set_wait_timeout_ns", "moe_route_noalloc", "moe_set_gemm_pair_mode",
     "moe_set_pdl", "moe_get_launch_count", "moe_permute_on_input", "moe_route_grouped", "moe_forward_fp8",
     "moe_quantize_fp8_rows", "moe_forward_w8a8", "moe_quantize_act_rows", "moe_grouped_fc1_fp8",
-    "moe_grouped_fc2_fp8", "moe_grouped_fc1_w8a8", "moe_grouped_fc2_w8a8", "EXPORTED_SYMBOLS",
+    "moe_grouped_fc2_fp8", "moe_grouped_fc1_w8a8", "moe_grouped_fc2_w8a8", "moe_launch_events_arm",
+    "moe_launch_events_mark", "moe_launch_events_used", "EXPORTED_SYMBOLS",
 ]
 
 MOE_OK = 0
@@ -38,6 +39,7 @@ MOE_ERR_DEVICE_BOUNDS = 8
 MOE_ERR_TIMEOUT = 16
 MOE_NONLOCAL_SKIP = 0
 MOE_NONLOCAL_MOD = 1
+MOE_LAUNCH_LABEL_BYTES = 48  # bytes per label written by moe_launch_events_used
 
 EXPORTED_SYMBOLS = (
     "moe_status_string", "moe_workspace_size", "moe_workspace_init", "moe_get_device_status",
@@ -46,6 +48,7 @@ EXPORTED_SYMBOLS = (
     "moe_set_gemm_pair_mode", "moe_set_pdl", "moe_get_launch_count", "moe_permute_on_input", "moe_route_grouped",
     "moe_forward_fp8", "moe_quantize_fp8_rows", "moe_grouped_fc1_fp8", "moe_grouped_fc2_fp8",
     "moe_forward_w8a8", "moe_quantize_act_rows", "moe_grouped_fc1_w8a8", "moe_grouped_fc2_w8a8",
+    "moe_launch_events_arm", "moe_launch_events_mark", "moe_launch_events_used",
 )
 
 
@@ -96,6 +99,9 @@ def _load():
         "moe_set_gemm_pair_mode": ([i32], i32),
         "moe_set_pdl": ([i32], i32),
         "moe_get_launch_count": ([], ctypes.c_uint64),
+        "moe_launch_events_arm": ([P, i32], i32),
+        "moe_launch_events_mark": ([P], i32),
+        "moe_launch_events_used": ([P, i32], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -432,6 +438,41 @@ def moe_set_pdl(enable: bool) -> None:
 def moe_get_launch_count() -> int:
     """Kernel launches the library has issued in this process (counted on the host)."""
     return int(_lib.moe_get_launch_count())
+
+
+_armed_events: list = []
+
+
+def moe_launch_events_arm(events) -> None:
+    """Arm the per-launch timing hook with torch.cuda.Event objects created with
+    enable_timing=True; each must have been recorded once (torch creates the CUDA
+    event on first record).  While armed, every library launch first records the
+    next event on its stream.  None or an empty list disarms."""
+    global _armed_events
+    evs = list(events or [])
+    handles = []
+    for e in evs:
+        h = int(e.cuda_event)
+        if not h:
+            raise ValueError("record each event once before arming it (its CUDA event is created on first record)")
+        handles.append(h)
+    arr = (ctypes.c_void_p * len(handles))(*handles) if handles else None
+    _check("moe_launch_events_arm", _lib.moe_launch_events_arm(arr, len(handles)))
+    _armed_events = evs  # the events must outlive their use by the library
+
+
+def moe_launch_events_mark(stream=None) -> None:
+    """Record the next armed event on `stream` now (closes the last launch's interval)."""
+    _check("moe_launch_events_mark", _lib.moe_launch_events_mark(_stream(stream)))
+
+
+def moe_launch_events_used() -> list:
+    """Labels of the events recorded since arming: kernel names, and "mark" for marks."""
+    n = int(_lib.moe_launch_events_used(None, 0))
+    w = MOE_LAUNCH_LABEL_BYTES
+    buf = ctypes.create_string_buffer(w * max(1, n))
+    _lib.moe_launch_events_used(buf, n)
+    return [buf.raw[w * i:w * (i + 1)].split(b"\0", 1)[0].decode() for i in range(n)]
 
 
 def moe_set_gemm_pair_mode(mode: int) -> None:

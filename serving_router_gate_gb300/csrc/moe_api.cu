@@ -3,7 +3,10 @@
 // (except the two explicit status readers).
 #include <algorithm>
 #include <atomic>
+#include <cstring>
 #include <mutex>
+#include <string>
+#include <vector>
 
 #include "moe_internal.cuh"
 
@@ -15,6 +18,30 @@ std::atomic<uint64_t> g_timeout_ns{4000000000ull};
 std::atomic<int> g_pair_mode{0};
 std::atomic<int> g_pdl{1};
 std::atomic<uint64_t> g_launches{0};
+
+// Launch-event hook (moe_launch_events_arm): the caller's events, how many are
+// used, and the label of each used one.
+struct LaunchEvents {
+    std::mutex mu;
+    std::vector<cudaEvent_t> events;
+    std::vector<std::string> labels;
+};
+LaunchEvents g_ev;
+std::atomic<int> g_ev_armed{0};
+
+// Records the next armed event on s (an external node under stream capture).
+cudaError_t record_next_event(const char* label, cudaStream_t s) {
+    std::lock_guard<std::mutex> lock(g_ev.mu);
+    if (g_ev.labels.size() >= g_ev.events.size()) return cudaSuccess;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(s, &cs);
+    if (e != cudaSuccess) return e;
+    e = cudaEventRecordWithFlags(g_ev.events[g_ev.labels.size()], s,
+                                 cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault);
+    if (e != cudaSuccess) return e;
+    g_ev.labels.emplace_back(label);
+    return cudaSuccess;
+}
 
 int device_sms() {
     static std::mutex mu;
@@ -96,8 +123,12 @@ moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE
 
 }  // namespace
 
-bool moe::pdl_enabled() { return g_pdl.load() != 0; }
-void moe::count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+bool moe::pdl_enabled() { return g_pdl.load() != 0 && g_ev_armed.load() == 0; }
+
+cudaError_t moe::note_launch(const char* name, cudaStream_t s) {
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return g_ev_armed.load() ? record_next_event(name, s) : cudaSuccess;
+}
 
 extern "C" {
 
@@ -123,6 +154,33 @@ moe_status_t moe_set_pdl(int enable) {
     if (enable != 0 && enable != 1) return MOE_ERR_INVALID_ARG;
     g_pdl.store(enable);
     return MOE_OK;
+}
+
+moe_status_t moe_launch_events_arm(void* const* events, int n) {
+    if (n < 0 || (n > 0 && !events)) return MOE_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_ev.mu);
+    g_ev.events.clear();
+    g_ev.labels.clear();
+    for (int i = 0; i < n; ++i) g_ev.events.push_back(static_cast<cudaEvent_t>(events[i]));
+    g_ev_armed.store(n > 0 ? 1 : 0);
+    return MOE_OK;
+}
+
+moe_status_t moe_launch_events_mark(moe_stream_t stream) {
+    if (!g_ev_armed.load()) return MOE_OK;
+    return cuda_status(record_next_event("mark", (cudaStream_t)stream));
+}
+
+int moe_launch_events_used(char* names, int cap) {
+    std::lock_guard<std::mutex> lock(g_ev.mu);
+    const int used = (int)g_ev.labels.size();
+    if (names)
+        for (int i = 0; i < std::min(used, cap); ++i) {
+            char* dst = names + (size_t)i * MOE_LAUNCH_LABEL_BYTES;
+            std::memset(dst, 0, MOE_LAUNCH_LABEL_BYTES);
+            std::strncpy(dst, g_ev.labels[i].c_str(), MOE_LAUNCH_LABEL_BYTES - 1);
+        }
+    return used;
 }
 
 moe_status_t moe_set_gemm_pair_mode(int mode) {

@@ -154,8 +154,8 @@ cudaError_t launch_finalize(const FinalizeLaunch& L, int num_sms, cudaStream_t s
     while (TB > 1 && (L.T + TB - 1) / TB < 2LL * num_sms) TB >>= 1;
     const int64_t nblk = (L.T + TB - 1) / TB;
     const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(nblk, (int64_t)num_sms * 4));
-    return launch_k(finalize_kernel, dim3(grid), dim3(FZ_THREADS), 0, s, L.y, L.rows_cap, L.pair_row, L.w, L.T, L.k,
-                    L.H, TB, L.y_sh, L.y_sh_part, L.y_sh_part ? L.ksplit : 0, L.x, L.gate_w, L.out,
+    return launch_k("finalize", finalize_kernel, dim3(grid), dim3(FZ_THREADS), 0, s, L.y, L.rows_cap, L.pair_row, L.w,
+                    L.T, L.k, L.H, TB, L.y_sh, L.y_sh_part, L.y_sh_part ? L.ksplit : 0, L.x, L.gate_w, L.out,
                     L.hdr ? &L.hdr->status : nullptr);
 }
 

@@ -53,6 +53,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstdio>
 #include <mutex>
 
 #include "moe_internal.cuh"
@@ -897,7 +898,11 @@ cudaError_t launch_kernel(const GemmParams& p, const CUtensorMap& mA, const CUte
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
-    count_launch();
+    char name[32];
+    snprintf(name, sizeof(name), "grouped_gemm_%s_n%d%s%s%s", kFC1 ? "fc1" : "fc2", BN, kShort ? "_short" : "",
+             kPair ? "_pair" : "", kQ == GEMM_W8 ? "_w8" : (kQ == GEMM_W8A8 ? "_w8a8" : ""));
+    const cudaError_t e = note_launch(name, s);
+    if (e != cudaSuccess) return e;
     return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<kFC1, kPair, BN, kShort, kQ>, p, mA, mB, mAs, mBs, mA32, mAs32);
 }
 
@@ -1054,7 +1059,8 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& L, int num_sms, cudaStream_t s
 }
 
 cudaError_t launch_wait_timeout_probe(WsHeader* hdr, uint64_t timeout_ns, cudaStream_t s) {
-    count_launch();
+    const cudaError_t e = note_launch("wait_probe", s);
+    if (e != cudaSuccess) return e;
     wait_probe_kernel<<<1, 32, 0, s>>>(&hdr->status, timeout_ns);
     return cudaGetLastError();
 }

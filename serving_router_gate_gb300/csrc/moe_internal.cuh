@@ -466,12 +466,16 @@ cudaError_t launch_quantize_fp8_rows(const uint16_t* w, int64_t rows, int K, uin
 // Whether kernels are launched with programmatic stream serialization (set by
 // moe_set_pdl; defined in moe_api.cu).
 bool pdl_enabled();
-// adds one to the library's count of kernel launches issued (moe_get_launch_count)
-void count_launch();
+// Called right before each kernel launch: adds one to the library's count of
+// launches (moe_get_launch_count) and, while the launch-event hook is armed,
+// records its next event on `s` labelled `name` (moe_launch_events_arm).  A
+// non-success return means the launch must not be made.
+cudaError_t note_launch(const char* name, cudaStream_t s);
 
 // Launch `kernel` on `s`, with programmatic stream serialization when enabled.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args&&... args) {
+cudaError_t launch_k(const char* name, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                     Args&&... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
@@ -482,7 +486,8 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
     attr.val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = pdl_enabled() ? 1 : 0;
-    count_launch();
+    const cudaError_t e = note_launch(name, s);
+    if (e != cudaSuccess) return e;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 

@@ -342,29 +342,29 @@ cudaError_t launch_permute(const PermuteLaunch& L, int num_sms, cudaStream_t s) 
         }
         // one CTA copies at most PM_SMALL_COPY bytes of rows; more go to the scatter kernel
         const bool copy_here = (int64_t)P * L.H * 2 <= PM_SMALL_COPY;
-        cudaError_t e = launch_k(permute_small_kernel, dim3(1), dim3(PM_SCAN_THREADS), smem_small, s, L.ids, L.w, P,
-                                 L.k, L.E, L.rep_offset, L.rep_slots, L.S, L.local_start, L.local_count, L.mode,
+        cudaError_t e = launch_k("permute_small", permute_small_kernel, dim3(1), dim3(PM_SCAN_THREADS), smem_small,
+                                 s, L.ids, L.w, P, L.k, L.E, L.rep_offset, L.rep_slots, L.S, L.local_start, L.local_count, L.mode,
                                  L.S_local, L.slot_ids, L.rank, L.chunk_cnt, nchunks, L.x, L.H, L.counts, L.offsets,
                                  L.chunk_base, L.pair_row, L.perm_src, L.x_perm, wsc, (int)copy_here, status);
         if (e != cudaSuccess || copy_here) return e;
         const int64_t want = (P + 8 * PS_PAIRS - 1) / (8 * PS_PAIRS);
         const unsigned gs = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms * 8));
-        return launch_k(permute_scatter_kernel, dim3(gs), dim3(256), 0, s, L.x, L.slot_ids, L.rank, L.chunk_base,
-                        L.S_local, P, L.k, L.H, L.pair_row, L.perm_src, L.x_perm, wsc);
+        return launch_k("permute_scatter", permute_scatter_kernel, dim3(gs), dim3(256), 0, s, L.x, L.slot_ids,
+                        L.rank, L.chunk_base, L.S_local, P, L.k, L.H, L.pair_row, L.perm_src, L.x_perm, wsc);
     }
     const unsigned g1 = (unsigned)((nchunks + PM_WARPS - 1) / PM_WARPS);
     const size_t smem = (size_t)PM_WARPS * L.S_local * sizeof(int32_t);
-    cudaError_t err = launch_k(permute_rank_kernel, dim3(g1), dim3(PM_WARPS * 32), smem, s, L.ids, L.w, P, L.k, L.E,
-                               L.rep_offset, L.rep_slots, L.S, L.local_start, L.local_count, L.mode, L.S_local,
+    cudaError_t err = launch_k("permute_rank", permute_rank_kernel, dim3(g1), dim3(PM_WARPS * 32), smem, s, L.ids,
+                               L.w, P, L.k, L.E, L.rep_offset, L.rep_slots, L.S, L.local_start, L.local_count, L.mode, L.S_local,
                                L.slot_ids, L.rank, L.chunk_cnt, nchunks, status);
     if (err != cudaSuccess) return err;
-    err = launch_k(permute_scan_kernel, dim3(1), dim3(PM_SCAN_THREADS), 0, s, L.chunk_cnt, nchunks, L.S_local,
-                   L.counts, L.offsets, L.chunk_base);
+    err = launch_k("permute_scan", permute_scan_kernel, dim3(1), dim3(PM_SCAN_THREADS), 0, s, L.chunk_cnt, nchunks,
+                   L.S_local, L.counts, L.offsets, L.chunk_base);
     if (err != cudaSuccess) return err;
     const int64_t want = (P + 8 * PS_PAIRS - 1) / (8 * PS_PAIRS);
     const unsigned g3 = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms * 8));
-    return launch_k(permute_scatter_kernel, dim3(g3), dim3(256), 0, s, L.x, L.slot_ids, L.rank, L.chunk_base,
-                    L.S_local, P, L.k, L.H, L.pair_row, L.perm_src, L.x_perm, wsc);
+    return launch_k("permute_scatter", permute_scatter_kernel, dim3(g3), dim3(256), 0, s, L.x, L.slot_ids, L.rank,
+                    L.chunk_base, L.S_local, P, L.k, L.H, L.pair_row, L.perm_src, L.x_perm, wsc);
 }
 
 }  // namespace moe

@@ -318,14 +318,15 @@ cudaError_t launch_quantize_act_rows(const ActQuantSeg* seg, int nseg, int num_s
         want += (a.seg[i].rows + R - 1) / R;
     }
     const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms * per_sm));
-    return launch_k(quantize_act_rows_kernel, dim3(grid), dim3(QA_THREADS), 0, s, a);
+    return launch_k("quantize_act_rows", quantize_act_rows_kernel, dim3(grid), dim3(QA_THREADS), 0, s, a);
 }
 
 cudaError_t launch_quantize_fp8_rows(const uint16_t* w, int64_t rows, int K, uint8_t* q, float* scale, int num_sms,
                                      cudaStream_t s) {
     const int64_t want = (rows + QZ_WARPS - 1) / QZ_WARPS;
     const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms * 8));
-    return launch_k(quantize_fp8_rows_kernel, dim3(grid), dim3(QZ_WARPS * 32), 0, s, w, rows, K, q, scale);
+    return launch_k("quantize_fp8_rows", quantize_fp8_rows_kernel, dim3(grid), dim3(QZ_WARPS * 32), 0, s, w, rows, K,
+                    q, scale);
 }
 
 }  // namespace moe

@@ -762,8 +762,8 @@ cudaError_t launch_router(const RouterLaunch& L, int num_sms, cudaStream_t s) {
     cudaError_t err = cudaFuncSetAttribute(router_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)RT_SMEM);
     if (err != cudaSuccess) return err;
-    err = launch_k(router_logits_kernel, grid1, dim3(RT_THREADS), RT_SMEM, s, L.x, L.Wg, L.T, L.H, L.E, L.KC, L.part,
-                   L.xsq, L.wsq);
+    err = launch_k("router_logits", router_logits_kernel, grid1, dim3(RT_THREADS), RT_SMEM, s, L.x, L.Wg, L.T, L.H,
+                   L.E, L.KC, L.part, L.xsq, L.wsq);
     if (err != cudaSuccess) return err;
 
     // worst-case rounding depth of one logit: 32-term chunk, 8-chunk group,
@@ -793,9 +793,9 @@ cudaError_t launch_router(const RouterLaunch& L, int num_sms, cudaStream_t s) {
                                        (int)smem);                                                               \
             if (err != cudaSuccess) return err;                                                                  \
         }                                                                                                        \
-        err = launch_k(router_select_kernel<PLV>, dim3(grid2), dim3(RS_WARPS * 32), smem, s, L.part, L.xsq,     \
-                       L.wsq, L.nsplit, thr_coef, thr2_coef, L.n_group, L.topk_group, L.bias, L.x, L.Wg, L.T, L.H, L.E, L.k, L.renorm, L.ids, L.w,    \
-                       L.hdr);                                                                                   \
+        err = launch_k("router_select", router_select_kernel<PLV>, dim3(grid2), dim3(RS_WARPS * 32), smem, s,    \
+                       L.part, L.xsq, L.wsq, L.nsplit, thr_coef, thr2_coef, L.n_group, L.topk_group, L.bias, L.x,   \
+                       L.Wg, L.T, L.H, L.E, L.k, L.renorm, L.ids, L.w, L.hdr);                                   \
     } while (0)
     if (L.E <= 32)
         MOE_SELECT(1);

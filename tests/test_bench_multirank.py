@@ -47,3 +47,34 @@ def test_single_rank_is_local_time():
     import bench
     value, ms = bench.aggregate_throughput(100, 2.0, 1)
     assert ms == 2.0 and value == pytest.approx(100 / 2e-3)
+
+
+def test_kernel_labels_map_to_layer_stages():
+    import bench
+    labels = ["router_logits", "router_select", "permute_rank", "permute_scan", "permute_scatter",
+              "quantize_act_rows", "grouped_gemm_fc1_n256_w8a8", "quantize_act_rows",
+              "grouped_gemm_fc2_n256_short_w8a8", "finalize"]
+    seen = {}
+    stages = []
+    for lab in labels:
+        st = bench._stage_of(lab, seen)
+        seen[st] = seen.get(st, 0.0) + 1.0
+        stages.append(st)
+    assert stages == ["route", "route", "permute", "permute", "permute", "quant_x", "fc1", "quant_h", "fc2",
+                      "finalize"]
+
+
+def test_layer_bytes_count_each_tensor_once():
+    import bench
+    import moe_inputs as mi
+    cfg = mi.MoEConfig("b", T=2, H=64, I=128, E=4, k=2, renorm=False, n_shared=1, I_shared=64)
+    rows, active = 4, 3
+    wk = bench._work(cfg, rows, active)
+    H, I, Ish, T = 64, 128, 64, 2
+    w1 = active * 2 * I * H * 2 + 2 * Ish * H * 2
+    w2 = active * H * I * 2 + H * Ish * 2
+    fc1 = w1 + (rows + T) * H * 2 + rows * I * 2 + T * Ish * 2          # A rows in, h out
+    fc2 = w2 + rows * I * 2 + T * Ish * 2 + rows * H * 2 + T * H * 2     # h in, y out
+    assert wk["fc1_bytes"] == fc1 and wk["fc2_bytes"] == fc2
+    # + fp32 gate weights, x for the router, x_perm written, y and y_shared read back, out
+    assert wk["layer_bytes"] == fc1 + fc2 + 4 * H * 4 + T * H * 2 + rows * H * 2 + rows * H * 2 + T * H * 2 + T * H * 2
