@@ -92,6 +92,19 @@ def test_one_hot_expert_gets_every_token():
     assert int(g["counts"][5]) == cfg.T
 
 
+def test_supported_envelope_extremes():
+    # 512 experts (16 logits per lane in the select kernel, its shared memory above 48 KB),
+    # k = 32, and the smallest hidden and intermediate sizes (one K step per GEMM)
+    _full_check(mi.make_inputs(mi.MoEConfig("e512k32", T=150, H=64, I=64, E=512, k=32, renorm=True)))
+    # 1024 slots (each of 512 experts replicated): 1024 GEMM groups, most of them with rows
+    g, _ = _full_check(mi.make_inputs(mi.MoEConfig("s1024", T=400, H=128, I=64, E=512, S=1024, n_hot=512, k=8,
+                                                   renorm=False)))
+    assert int((g["counts"] > 0).sum()) > 900
+    # 128 experts (4 logits per lane) with a gated shared expert
+    _full_check(mi.make_inputs(mi.MoEConfig("e128", T=300, H=192, I=128, E=128, k=6, renorm=True, n_shared=1,
+                                            I_shared=64, shared_gate=True)))
+
+
 def test_local_range_without_pairs_gives_zero():
     cfg = mi.MoEConfig("empty", T=64, H=256, I=256, E=8, k=2, renorm=True)
     inp = mi.make_inputs(cfg)
