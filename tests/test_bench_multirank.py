@@ -78,3 +78,31 @@ def test_layer_bytes_count_each_tensor_once():
     assert wk["fc1_bytes"] == fc1 and wk["fc2_bytes"] == fc2
     # + fp32 gate weights, x for the router, x_perm written, y and y_shared read back, out
     assert wk["layer_bytes"] == fc1 + fc2 + 4 * H * 4 + T * H * 2 + rows * H * 2 + rows * H * 2 + T * H * 2 + T * H * 2
+
+
+def test_clock_sampler_keeps_region_samples_and_reasons(tmp_path):
+    import bench
+    cs = bench.ClockSampler(0)
+    path = tmp_path / "clocks.csv"
+    # index, sm, max sm, power, active mask, hw_slowdown, hw_thermal, sw_thermal, sw_power_cap
+    lines = ["0, 1200, 2070, 300.0, 0x0, Not Active, Not Active, Not Active, Not Active",   # before the region
+             "0, 2070, 2070, 900.5, 0x0, Not Active, Not Active, Not Active, Not Active",   # last one before
+             "0, 2055, 2070, 1350.0, 0x4, Not Active, Not Active, Not Active, Active",      # inside the region
+             "0, 1980, 2070, 1390.0, 0x20, Not Active, Not Active, Active, Not Active",     # inside the region
+             "garbled line"]
+    path.write_text("\n".join(lines) + "\n")
+
+    class _Done:
+        def terminate(self):
+            pass
+
+        def wait(self, timeout=None):
+            return 0
+
+    cs.path, cs.proc, cs.n_before = str(path), _Done(), 2
+    cs.f = open(tmp_path / "unused", "w")
+    rec = cs.stop()
+    assert rec["samples_in_region"] == 2  # parsed samples after the region opened
+    assert rec["samples"] == 3            # the last sample before it plus the two inside
+    assert rec["sm_mhz"] == 2055.0 and rec["sm_max_mhz"] == 2070.0
+    assert rec["reasons"] == ["sw_power_cap", "sw_thermal_slowdown"]
