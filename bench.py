@@ -42,12 +42,13 @@ DEFAULT_WORKLOAD = "qwen2_moe_like_prefill"
 # from one ncu capture of that workload, valid only while the kernel source hashes to
 # the recorded value.
 NCU_TRAFFIC = {
-    # FC1 of the first forward, ncu --set full: 822.22 MB read + 87.98 MB written
-    ("qwen2_moe_like_prefill", "815b23aea88b128d"): 910.20e6,
-    # FC1 of the first forward, ncu --set full: 115.42 MB read + 3.04 MB written
-    ("dsv2_lite_like_decode_t1", "815b23aea88b128d"): 118.46e6,
-    # FC1 (E4M3 operands) of the first forward, ncu --set full: 411.94 MB read + 81.70 MB written
-    ("qwen2_moe_like_prefill_w8a8", "815b23aea88b128d"): 493.63e6,
+    # FC1 of the first forward, ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum:
+    # 822.21 MB read + 87.42 MB written
+    ("qwen2_moe_like_prefill", "7e9e213e91d0e978"): 909.63e6,
+    # 115.46 MB read + 2.99 MB written
+    ("dsv2_lite_like_decode_t1", "7e9e213e91d0e978"): 118.46e6,
+    # FC1 (E4M3 operands): 411.93 MB read + 81.52 MB written
+    ("qwen2_moe_like_prefill_w8a8", "7e9e213e91d0e978"): 493.45e6,
 }
 
 
