@@ -11,9 +11,10 @@ token activations copied from pinned host memory and the output copied back
 inside the timed region (weights are resident model parameters).  L2 is
 flushed before every timed step, outside the step's own CUDA events.  The
 per-kernel breakdown and the roofline of the dominant kernel come from a
-second timed pass that replays each stage from its own CUDA graph with CUDA
-events on the launching stream between stages.  With N > 1 (torchrun), every rank runs its
-own independent batch (weak scaling, no collective on the data path).
+second pass that replays a CUDA graph of the same forward captured with the
+library's launch-event hook armed: a CUDA event node on the launching stream
+right before every kernel and one after the last.  With N > 1 (torchrun), every
+rank runs its own independent batch (weak scaling, no collective on the data path).
 `--impl reference` times the fp64 CPU oracle on a bounded sample instead.
 """
 from __future__ import annotations
