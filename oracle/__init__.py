@@ -10,9 +10,10 @@ ctypes.  Each wrapper names the C function it calls; the C file cites the
 passage of the source pages each step follows.
 
 Parity status of each function (see tests/test_oracle_pins.py for the pins):
-  route, slot_map, local_mask, permute, expert_mlp, moe_tokens, bf16 rounding:
-  pinned (closed forms, brute force, invariants, independent numpy/torch
-  routines).  No function here is "parity unpinned".
+  route, slot_map, local_mask, permute, expert_mlp, moe_tokens, bf16 rounding,
+  the E4M3 and NVFP4 quantisers and expert MLPs: pinned (closed forms, brute
+  force, invariants, independent numpy/torch routines).  No function here is
+  "parity unpinned".  The NVFP4 functions serve a GPU path not built yet.
 """
 from __future__ import annotations
 
@@ -88,6 +89,14 @@ def _load():
         lib.oracle_expert_mlp_w8a8.restype = None
         lib.oracle_quantize_act_rows.argtypes = [P, i64, i32, P, P]
         lib.oracle_quantize_act_rows.restype = None
+        lib.oracle_e2m1_to_f64.argtypes = [ctypes.c_uint8]
+        lib.oracle_e2m1_to_f64.restype = ctypes.c_double
+        lib.oracle_f64_to_e2m1.argtypes = [ctypes.c_double]
+        lib.oracle_f64_to_e2m1.restype = ctypes.c_uint8
+        lib.oracle_quantize_nvfp4_rows.argtypes = [P, i64, i32, i32, P, P, P]
+        lib.oracle_quantize_nvfp4_rows.restype = None
+        lib.oracle_expert_mlp_nvfp4.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, P, P]
+        lib.oracle_expert_mlp_nvfp4.restype = None
         lib.oracle_moe_tokens.restype = None
         lib.oracle_set_threads.argtypes = [i32]
         lib.oracle_set_threads.restype = None
@@ -265,6 +274,54 @@ def expert_mlp_fp8(x_row, W1q, s1, W2q, s2, act8=False):
     h = np.empty(I, np.uint16)
     fn = lib.oracle_expert_mlp_w8a8 if act8 else lib.oracle_expert_mlp_fp8
     fn(_ptr(x_row), _ptr(W1q), _ptr(s1), _ptr(W2q), _ptr(s2), H, I, _ptr(y), _ptr(h))
+    return y, h
+
+
+def e2m1_to_f64(q: int) -> float:
+    return float(_load().oracle_e2m1_to_f64(int(q)))
+
+
+def f64_to_e2m1(v: float) -> int:
+    """Nearest E2M1 value, ties to even, saturated at +-6; returns the 4-bit code."""
+    return int(_load().oracle_f64_to_e2m1(float(v)))
+
+
+def quantize_nvfp4_rows(v, pow2=False):
+    """C oracle_quantize_nvfp4_rows on a bf16 matrix [..., K] (K a multiple of 16):
+    returns (q uint8 [..., K] E2M1 codes, sb uint8 [..., K/16] E4M3 block scales,
+    s float32 [...] row scales), s = amax / 2688 (pow2, for activations: the
+    smallest 2^e, e >= -126, with amax <= 2688 * 2^e), sb = e4m3(amax_b / (6 s)),
+    q = e2m1(v / (sb s)); the value of an element is e2m1(q) * sb * s."""
+    lib = _load()
+    v16 = np.ascontiguousarray(_u16(v))
+    shape = v16.shape
+    K = shape[-1]
+    assert K % 16 == 0, "NVFP4 rows hold whole 16-element blocks"
+    rows = int(np.prod(shape[:-1]))
+    q = np.empty(shape, np.uint8)
+    sb = np.empty(shape[:-1] + (K // 16,), np.uint8)
+    sc = np.empty(shape[:-1], np.float32)
+    lib.oracle_quantize_nvfp4_rows(_ptr(v16), rows, K, int(bool(pow2)), _ptr(q), _ptr(sb), _ptr(sc))
+    return q, sb, sc
+
+
+def expert_mlp_nvfp4(x_row, W1q, W1sb, s1, W2q, W2sb, s2, act4=False):
+    """C oracle_expert_mlp_nvfp4: one token through one SwiGLU expert with NVFP4
+    weights (codes, block scales, row scales as quantize_nvfp4_rows returns them);
+    act4: x and h quantised to NVFP4 per row as well (power-of-two row scales).  Returns (y [H] f64, h [I] bf16 bits)."""
+    lib = _load()
+    x_row = _u16(x_row).reshape(-1)
+    W1q, W2q = _np(W1q, np.uint8), _np(W2q, np.uint8)
+    W1sb, W2sb = _np(W1sb, np.uint8), _np(W2sb, np.uint8)
+    s1, s2 = _np(s1, np.float32), _np(s2, np.float32)
+    H = x_row.size
+    I = W1q.shape[0] // 2
+    assert W1q.shape == (2 * I, H) and W2q.shape == (H, I) and H % 16 == 0 and I % 16 == 0
+    assert W1sb.shape == (2 * I, H // 16) and W2sb.shape == (H, I // 16)
+    y = np.empty(H, np.float64)
+    h = np.empty(I, np.uint16)
+    lib.oracle_expert_mlp_nvfp4(_ptr(x_row), _ptr(W1q), _ptr(W1sb), _ptr(s1), _ptr(W2q), _ptr(W2sb), _ptr(s2),
+                                H, I, int(bool(act4)), _ptr(y), _ptr(h))
     return y, h
 
 

@@ -147,17 +147,122 @@ void oracle_quantize_fp8_rows(const uint16_t *w, int64_t rows, int K, uint8_t *q
     }
 }
 
-/* A weight matrix of the layer: bf16 values, or E4M3 bytes with row scales. */
+/* ------------------------------------------------------------------------- */
+/* NVFP4 values: E2M1 elements, an E4M3 scale per 16 consecutive elements of a */
+/* row, and an fp32 scale per row                                             */
+/* ------------------------------------------------------------------------- */
+
+/* E2M1 code (bit 3 sign, bits 2-1 exponent with bias 1, bit 0 mantissa): the
+ * magnitudes 0, 0.5 (exponent field 0: m * 0.5), 1, 1.5, 2, 3, 4, 6. */
+double oracle_e2m1_to_f64(uint8_t q)
+{
+    const int sgn = (q >> 3) & 1, e = (q >> 1) & 3, m = q & 1;
+    const double v = (e == 0) ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return sgn ? -v : v;
+}
+
+/* Nearest E2M1 value, ties to even (the code whose mantissa bit is 0), finite
+ * results saturated at +-6; returns the 4-bit code.  Inputs are finite. */
+uint8_t oracle_f64_to_e2m1(double v)
+{
+    const uint8_t sgn = signbit(v) ? 8 : 0;
+    const double a = fabs(v);
+    if (a == 0.0) return sgn;
+    int e;
+    (void)frexp(a, &e);            /* a = f * 2^e, f in [0.5, 1) */
+    int lsb = (e - 1) - 1;         /* weight of the 2nd significant bit */
+    if (lsb < -1) lsb = -1;        /* subnormal spacing 0.5 */
+    double r = ldexp(nearbyint(ldexp(a, -lsb)), lsb);  /* ties to even */
+    if (r > 6.0) r = 6.0;
+    if (r < 1.0) return (uint8_t)(sgn | (uint8_t)(r * 2.0));  /* 0 or 0.5 */
+    (void)frexp(r, &e);
+    const int E = e;               /* r = (1 + m/2) * 2^(e-1), exponent field e - 1 + 1 */
+    const int m = (int)(ldexp(r, -(e - 1)) * 2.0) - 2;
+    return (uint8_t)(sgn | (uint8_t)(E << 1) | (uint8_t)m);
+}
+
+/* NVFP4 quantisation of one bf16 row [K], K a multiple of 16.  The pages name
+ * NVFP4 expert weights (TensorRT-LLM PR #10985, review of torch_moe.py, which
+ * names the FP8 and NVFP4 paths of the MoE ops) and define no encoding.
+ * Reading: the row's fp32 scale is s = amax / (6 * 448), one binary32 division
+ * (6 * 448 = 2688 is exact); each block of 16 consecutive elements gets the
+ * E4M3 scale sb = e4m3(amax_b / (6 * s)), the product 6 * s and the division in
+ * binary32, rounded to E4M3 to nearest with ties to even and saturated at 448;
+ * each element q = e2m1(v / (sb * s)), the product sb * s and the division in
+ * binary32.  The value is e2m1(q) * sb * s.  An all-zero row gets s = 0, zero
+ * block scales and zero codes; a block whose scale rounds to 0 gets zero codes.
+ * q holds one code per element (0..15); sb one E4M3 byte per block.
+ *
+ * pow2 (activations): the row scale is instead the power of two s = 2^e, e the
+ * smallest integer >= -126 with amax <= 2688 * 2^e (an all-zero row gets
+ * 2^-126), for the reason E4M3 activations use one: the GPU's bf16 rows can
+ * differ from the oracle's in a rare last bit, and a scale set by amax itself
+ * would then move every block scale and code of the row. */
+void oracle_quantize_nvfp4_row(const uint16_t *v, int K, int pow2, uint8_t *q, uint8_t *sb, float *scale)
+{
+    float amax = 0.0f;
+    for (int c = 0; c < K; ++c) {
+        const float f = fabsf((float)oracle_bf16_to_f64(v[c]));
+        if (f > amax) amax = f;
+    }
+    volatile float s = amax / 2688.0f;
+    if (pow2) {
+        int e = -126;
+        while ((double)amax > ldexp(2688.0, e)) ++e;
+        s = (float)ldexp(1.0, e);
+    }
+    *scale = s;
+    for (int b = 0; b < K / 16; ++b) {
+        float bmax = 0.0f;
+        for (int c = 16 * b; c < 16 * b + 16; ++c) {
+            const float f = fabsf((float)oracle_bf16_to_f64(v[c]));
+            if (f > bmax) bmax = f;
+        }
+        uint8_t code = 0;
+        if (s != 0.0f) {
+            volatile float six_s = 6.0f * s;
+            volatile float d = bmax / six_s;
+            code = oracle_f64_to_e4m3((double)d);
+        }
+        sb[b] = code;
+        const float sbv = (float)oracle_e4m3_to_f64(code);
+        volatile float denom = sbv * s;
+        for (int c = 16 * b; c < 16 * b + 16; ++c) {
+            if (denom == 0.0f) {
+                q[c] = 0;
+                continue;
+            }
+            volatile float x = (float)oracle_bf16_to_f64(v[c]) / denom;
+            q[c] = oracle_f64_to_e2m1((double)x);
+        }
+    }
+}
+
+void oracle_quantize_nvfp4_rows(const uint16_t *v, int64_t rows, int K, int pow2, uint8_t *q, uint8_t *sb,
+                                float *scale)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r)
+        oracle_quantize_nvfp4_row(v + (size_t)r * (size_t)K, K, pow2, q + (size_t)r * (size_t)K,
+                                  sb + (size_t)r * (size_t)(K / 16), scale + r);
+}
+
+/* A weight matrix of the layer: bf16 values, E4M3 bytes with row scales, or
+ * (sb given) NVFP4 codes with block and row scales. */
 typedef struct {
     const uint16_t *bf;
     const uint8_t *q;
     const float *s;
     size_t K;
+    const uint8_t *sb;
 } oracle_wmat;
 
 static double wget(const oracle_wmat *m, size_t row, size_t col)
 {
     const size_t i = row * m->K + col;
+    if (m->sb)
+        return (double)m->s[row] * oracle_e4m3_to_f64(m->sb[row * (m->K / 16) + col / 16]) *
+               oracle_e2m1_to_f64(m->q[i]);
     return m->q ? (double)m->s[row] * oracle_e4m3_to_f64(m->q[i]) : oracle_bf16_to_f64(m->bf[i]);
 }
 
@@ -404,18 +509,27 @@ void oracle_quantize_act_rows(const uint16_t *v, int64_t rows, int K, uint8_t *q
         oracle_quantize_act_row(v + (size_t)r * (size_t)K, K, q + (size_t)r * (size_t)K, scale + r);
 }
 
-/* The row v [K] as fp64 values: bf16 as is, or (act8) its E4M3 quantisation
- * dequantised exactly, scale * e4m3(q). */
-static void act_values(const uint16_t *v, int K, int act8, double *out)
+/* The row v [K] as fp64 values: bf16 as is (act 0), its E4M3 quantisation
+ * dequantised exactly, scale * e4m3(q) (act 1), or its NVFP4 quantisation
+ * dequantised exactly, s * sb * e2m1(q), with a power-of-two s (act 2). */
+static void act_values(const uint16_t *v, int K, int act, double *out)
 {
-    if (!act8) {
+    if (act == 0) {
         for (int c = 0; c < K; ++c) out[c] = oracle_bf16_to_f64(v[c]);
         return;
     }
     uint8_t *q = (uint8_t *)malloc((size_t)K);
     float sc;
-    oracle_quantize_act_row(v, K, q, &sc);
-    for (int c = 0; c < K; ++c) out[c] = (double)sc * oracle_e4m3_to_f64(q[c]);
+    if (act == 1) {
+        oracle_quantize_act_row(v, K, q, &sc);
+        for (int c = 0; c < K; ++c) out[c] = (double)sc * oracle_e4m3_to_f64(q[c]);
+    } else {
+        uint8_t *sb = (uint8_t *)malloc((size_t)(K / 16));
+        oracle_quantize_nvfp4_row(v, K, 1, q, sb, &sc);
+        for (int c = 0; c < K; ++c)
+            out[c] = (double)sc * oracle_e4m3_to_f64(sb[c / 16]) * oracle_e2m1_to_f64(q[c]);
+        free(sb);
+    }
     free(q);
 }
 
@@ -433,7 +547,9 @@ static void act_values(const uint16_t *v, int K, int act8, double *out)
  *   x [H] bf16;  W1 [2I, H] bf16 (rows 0..I-1 gate, I..2I-1 up);  W2 [H, I] bf16
  *   y [H] double out;  h [I] bf16 bits out (or NULL)
  * act8: the input row and the bf16 row h are quantised to E4M3 with a
- * power-of-two scale each (oracle_quantize_act_row) before FC1 and FC2.
+ * power-of-two scale each (oracle_quantize_act_row) before FC1 and FC2; act8 =
+ * 2: to NVFP4 with a power-of-two row scale (oracle_quantize_nvfp4_row, pow2)
+ * instead.
  */
 static void expert_mlp_w(const uint16_t *x, const oracle_wmat *W1, const oracle_wmat *W2,
                          int H, int I, int act8, double *y, uint16_t *h_out)
@@ -464,7 +580,7 @@ static void expert_mlp_w(const uint16_t *x, const oracle_wmat *W1, const oracle_
 void oracle_expert_mlp(const uint16_t *x, const uint16_t *W1, const uint16_t *W2,
                        int H, int I, double *y, uint16_t *h_out)
 {
-    const oracle_wmat w1 = {W1, NULL, NULL, (size_t)H}, w2 = {W2, NULL, NULL, (size_t)I};
+    const oracle_wmat w1 = {W1, NULL, NULL, (size_t)H, NULL}, w2 = {W2, NULL, NULL, (size_t)I, NULL};
     expert_mlp_w(x, &w1, &w2, H, I, 0, y, h_out);
 }
 
@@ -473,7 +589,7 @@ void oracle_expert_mlp(const uint16_t *x, const uint16_t *W1, const uint16_t *W2
 void oracle_expert_mlp_fp8(const uint16_t *x, const uint8_t *W1q, const float *s1, const uint8_t *W2q,
                            const float *s2, int H, int I, double *y, uint16_t *h_out)
 {
-    const oracle_wmat w1 = {NULL, W1q, s1, (size_t)H}, w2 = {NULL, W2q, s2, (size_t)I};
+    const oracle_wmat w1 = {NULL, W1q, s1, (size_t)H, NULL}, w2 = {NULL, W2q, s2, (size_t)I, NULL};
     expert_mlp_w(x, &w1, &w2, H, I, 0, y, h_out);
 }
 
@@ -481,8 +597,19 @@ void oracle_expert_mlp_fp8(const uint16_t *x, const uint8_t *W1q, const float *s
 void oracle_expert_mlp_w8a8(const uint16_t *x, const uint8_t *W1q, const float *s1, const uint8_t *W2q,
                             const float *s2, int H, int I, double *y, uint16_t *h_out)
 {
-    const oracle_wmat w1 = {NULL, W1q, s1, (size_t)H}, w2 = {NULL, W2q, s2, (size_t)I};
+    const oracle_wmat w1 = {NULL, W1q, s1, (size_t)H, NULL}, w2 = {NULL, W2q, s2, (size_t)I, NULL};
     expert_mlp_w(x, &w1, &w2, H, I, 1, y, h_out);
+}
+
+/* NVFP4 weights: W1q [2I, H] codes with block scales W1sb [2I, H/16] and row
+ * scales s1 [2I], W2q [H, I] with W2sb [H, I/16] and s2 [H] (the dequantised
+ * values, exactly, in fp64); act4: x and h quantised to NVFP4 per row too. */
+void oracle_expert_mlp_nvfp4(const uint16_t *x, const uint8_t *W1q, const uint8_t *W1sb, const float *s1,
+                             const uint8_t *W2q, const uint8_t *W2sb, const float *s2, int H, int I, int act4,
+                             double *y, uint16_t *h_out)
+{
+    const oracle_wmat w1 = {NULL, W1q, s1, (size_t)H, W1sb}, w2 = {NULL, W2q, s2, (size_t)I, W2sb};
+    expert_mlp_w(x, &w1, &w2, H, I, act4 ? 2 : 0, y, h_out);
 }
 
 /* ------------------------------------------------------------------------- */

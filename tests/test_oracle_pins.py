@@ -664,3 +664,174 @@ def test_w8a8_single_expert_with_routing_on_input_quantises_the_scaled_row():
             y, _ = oracle.expert_mlp_fp8(xs, q1[e], s1[e], q2[e], s2[e], act8=True)
             acc += y
         np.testing.assert_allclose(res["out"][t], acc, rtol=0, atol=1e-12 * np.abs(acc).max())
+
+
+# --------------------------------------------------------------------------- NVFP4 (E2M1 + block scales)
+
+# E2M1 magnitudes by code (bit 0 = mantissa bit): the format's value table, written out
+_E2M1 = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def _e2m1_brute(v: float) -> int:
+    """Nearest E2M1 code by exhaustive search over the 8 magnitudes; a tie goes to the
+    code with mantissa bit 0; beyond 6 the magnitude saturates."""
+    a = abs(v)
+    best = min(range(8), key=lambda c: (abs(_E2M1[c] - a), c & 1))
+    return best | (8 if np.signbit(v) else 0)
+
+
+def _e4m3_np(codes: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.ascontiguousarray(codes)).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def _nvfp4_deq(q, sb, s):
+    """Dequantised NVFP4 values from the value table, torch's E4M3 decode and the row scales."""
+    mag = np.array(_E2M1)[q & 7] * np.where(q & 8, -1.0, 1.0)
+    blk = np.repeat(_e4m3_np(sb), 16, axis=-1)
+    return mag * blk * s[..., None].astype(np.float64)
+
+
+def test_e2m1_decode_and_encode_match_the_value_table():
+    for c in range(16):
+        v = oracle.e2m1_to_f64(c)
+        assert abs(v) == _E2M1[c & 7] and (np.signbit(v) == bool(c & 8))
+        assert oracle.f64_to_e2m1(v) == c
+    g = np.random.default_rng(11)
+    mids = [(a + b) / 2 for a, b in zip(_E2M1[:-1], _E2M1[1:])]
+    vals = list(g.uniform(-8, 8, 3000)) + mids + [-m for m in mids] + [6.0001, 7.0, 1e9, 1e-9, -1e-9, 0.2499]
+    for v in vals:
+        assert oracle.f64_to_e2m1(v) == _e2m1_brute(v), v
+
+
+def _nvfp4_rows():
+    g = torch.Generator().manual_seed(12)
+    v = torch.randn(24, 256, generator=g)
+    v[1] *= 1e-3                       # small row
+    v[2, :16] *= 1e-4                  # a block far below the row's maximum
+    v[3] = 0.0                         # all-zero row
+    v[4] = 0.0
+    v[4, 37] = -3.25                   # a single non-zero element
+    v[5, 64:80] = 0.0                  # an all-zero block
+    return v.to(torch.bfloat16)
+
+
+def test_nvfp4_quantisation_closed_forms():
+    v = _nvfp4_rows()
+    q, sb, s = oracle.quantize_nvfp4_rows(v)
+    assert q.shape == (24, 256) and sb.shape == (24, 16) and s.shape == (24,)
+    # the zero row: scale 0, zero codes and block scales
+    assert s[3] == 0.0 and np.all(q[3] == 0) and np.all(sb[3] == 0)
+    # a single non-zero element: its block scale is 448, its code -6, its value the element
+    assert _e4m3_np(sb[4, 2:3])[0] == 448.0 and q[4, 37] == (8 | 7)
+    assert np.all(q[4, np.arange(256) != 37] == 0)
+    assert np.all(sb[4, np.arange(16) != 2] == 0)
+    deq = _nvfp4_deq(q, sb, s)
+    assert abs(deq[4, 37] - (-3.25)) <= 2.0 ** -21 * 3.25
+    # an all-zero block: scale 0, codes 0
+    assert sb[5, 4] == 0 and np.all(q[5, 64:80] == 0)
+    # every non-zero row: its largest |v| has magnitude code 6 (value 6) in a block of scale 448
+    vf = v.float().numpy()
+    for r in range(24):
+        if r == 3:
+            continue
+        i = int(np.abs(vf[r]).argmax())
+        assert (q[r, i] & 7) == 7 and _e4m3_np(sb[r, i // 16:i // 16 + 1])[0] == 448.0
+
+
+def test_nvfp4_values_are_exact_for_representable_rows():
+    # rows built as e2m1 * sb * s with E4M3 block scales whose block maxima are 6 * sb:
+    # the quantiser must give back exactly these codes and scales
+    g = np.random.default_rng(13)
+    grid_sb = _e4m3_np(np.arange(0x30, 0x7F, dtype=np.uint8))    # block scales 2^-3 .. 448
+    for trial in range(20):
+        s = 2.0 ** int(g.integers(-20, -8))                         # the row scale, a power of two
+        sbv = g.choice(grid_sb, 8)
+        sbv[int(g.integers(0, 8))] = 448.0                         # one block carries the row maximum
+        codes = g.integers(0, 16, (8, 16))
+        codes[:, 0] = 7 | (8 * g.integers(0, 2, 8))                # each block holds +-6
+        vals = np.array(_E2M1)[codes & 7] * np.where(codes & 8, -1.0, 1.0) * sbv[:, None] * s
+        row = torch.from_numpy(vals.reshape(1, -1)).to(torch.bfloat16)
+        assert np.array_equal(row.to(torch.float64).numpy().reshape(8, 16), vals)  # bf16-exact
+        q, sb, sc = oracle.quantize_nvfp4_rows(row)
+        # s = amax / 2688 with amax = 6 * 448 * s exactly
+        assert sc[0] == np.float32(s)
+        np.testing.assert_array_equal(_e4m3_np(sb[0]), sbv)
+        deq = _nvfp4_deq(q, sb, sc)
+        np.testing.assert_array_equal(deq.reshape(8, 16), vals)
+
+
+def test_nvfp4_bounds_and_power_of_two_equivariance():
+    v = _nvfp4_rows()
+    q, sb, s = oracle.quantize_nvfp4_rows(v)
+    vf = v.to(torch.float64).numpy()
+    deq = _nvfp4_deq(q, sb, s)
+    blk = np.repeat(_e4m3_np(sb), 16, axis=-1) * s[:, None].astype(np.float64)
+    live = blk > 0
+    # each element: within half an E2M1 step of its scaled value (the step is 0.5 below 2,
+    # 1 below 4, 2 up to 6), or saturated at 6 block units
+    t = np.where(live, np.abs(vf) / np.where(live, blk, 1.0), 0.0)
+    half = np.where(t < 2.0, 0.25, np.where(t < 4.0, 0.5, 1.0))
+    bound = np.where(t <= 6.0, half, t - 6.0) * blk * (1 + 1e-6) + 1e-300
+    assert np.all(np.abs(deq - vf)[live] <= bound[live])
+    # blocks whose scale rounds to zero hold zeros only
+    assert np.all(deq[~live] == 0.0)
+    # scaling a row by 2^j scales s by 2^j and keeps every code and block scale
+    for j in (-7, -1, 3, 9):
+        q2, sb2, s2 = oracle.quantize_nvfp4_rows((v.float() * 2.0 ** j).to(torch.bfloat16))
+        keep = np.arange(24) != 3
+        assert np.array_equal(q2, q) and np.array_equal(sb2, sb)
+        np.testing.assert_array_equal(s2[keep], (s[keep].astype(np.float64) * 2.0 ** j).astype(np.float32))
+
+
+def test_nvfp4_expert_mlp_matches_numpy_of_dequantised_values():
+    cfg = _small_cfg(T=6, H=64, I=64, E=1, k=1, renorm=True)
+    inp = mi.make_inputs(cfg)
+    q1, sb1, s1 = oracle.quantize_nvfp4_rows(inp["W1"][0])
+    q2, sb2, s2 = oracle.quantize_nvfp4_rows(inp["W2"][0])
+    D1, D2 = _nvfp4_deq(q1, sb1, s1), _nvfp4_deq(q2, sb2, s2)
+    for t in range(cfg.T):
+        xrow = inp["x"][t]
+        for act4 in (False, True):
+            y, h = oracle.expert_mlp_nvfp4(xrow, q1, sb1, s1, q2, sb2, s2, act4=act4)
+            if act4:
+                xq, xsb, xs = oracle.quantize_nvfp4_rows(xrow[None], pow2=True)
+                x64 = _nvfp4_deq(xq, xsb, xs)[0]
+            else:
+                x64 = _bf16_np(xrow)
+            g = x64 @ D1[:64].T
+            u = x64 @ D1[64:].T
+            hb = torch.from_numpy(g / (1 + np.exp(-g)) * u).to(torch.bfloat16)
+            assert np.array_equal(h, hb.view(torch.int16).numpy().view(np.uint16))
+            if act4:
+                hq, hsb, hs = oracle.quantize_nvfp4_rows(hb[None], pow2=True)
+                h64 = _nvfp4_deq(hq, hsb, hs)[0]
+            else:
+                h64 = hb.to(torch.float64).numpy()
+            ref = h64 @ D2.T
+            np.testing.assert_allclose(y, ref, rtol=0, atol=1e-12 * np.abs(ref).max())
+
+
+def test_nvfp4_power_of_two_row_scale_for_activations():
+    v = _nvfp4_rows()
+    q, sb, s = oracle.quantize_nvfp4_rows(v, pow2=True)
+    vf = np.abs(v.to(torch.float64).numpy())
+    for r in range(24):
+        amax = vf[r].max()
+        # the smallest e >= -126 with amax <= 2688 * 2^e, by exact comparisons
+        e = -126
+        while amax > 2688.0 * 2.0 ** e:
+            e += 1
+        assert s[r] == np.float32(2.0 ** e)
+        if amax > 0:
+            assert amax > 2688.0 * 2.0 ** (e - 1) or e == -126
+    deq = _nvfp4_deq(q, sb, s)
+    blk = np.repeat(_e4m3_np(sb), 16, axis=-1) * s[:, None].astype(np.float64)
+    live = blk > 0
+    t = np.where(live, vf / np.where(live, blk, 1.0), 0.0)
+    half = np.where(t < 2.0, 0.25, np.where(t < 4.0, 0.5, 1.0))
+    bound = np.where(t <= 6.0, half, t - 6.0) * blk * (1 + 1e-6)
+    vs = v.to(torch.float64).numpy()
+    assert np.all(np.abs(deq - vs)[live] <= bound[live] + 1e-300)
+    # with a power-of-two row scale, rows equal up to a power of two give the same codes
+    q2, sb2, s2 = oracle.quantize_nvfp4_rows((v.float() * 2.0 ** 5).to(torch.bfloat16), pow2=True)
+    assert np.array_equal(q2, q) and np.array_equal(sb2, sb)
