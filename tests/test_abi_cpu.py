@@ -157,3 +157,18 @@ def test_permute_on_input_shares_the_host_validation():
     # S != E without a slot table
     assert p(FAKE, FAKE, 16, 2, 8, None, None, 9, 0, -1, 0, FAKE, 256, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
              FAKE, 1 << 30, None) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_launch_event_hook_host_side():
+    lib = moe._lib
+    assert lib.moe_launch_events_arm(None, -1) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_launch_events_arm(None, 3) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_launch_events_arm(None, 0) == moe.MOE_OK
+    assert lib.moe_launch_events_mark(None) == moe.MOE_OK      # disarmed: records nothing, calls no CUDA
+    assert lib.moe_launch_events_used(None, 0) == 0
+    # arming only stores the handles (no CUDA call); nothing is recorded until a launch or a mark
+    handles = (ctypes.c_void_p * 2)(0x1000, 0x2000)
+    assert lib.moe_launch_events_arm(handles, 2) == moe.MOE_OK
+    assert lib.moe_launch_events_used(None, 0) == 0
+    assert lib.moe_launch_events_arm(None, 0) == moe.MOE_OK
+    assert moe.moe_launch_events_used() == []
