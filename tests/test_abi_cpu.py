@@ -172,3 +172,25 @@ def test_launch_event_hook_host_side():
     assert lib.moe_launch_events_used(None, 0) == 0
     assert lib.moe_launch_events_arm(None, 0) == moe.MOE_OK
     assert moe.moe_launch_events_used() == []
+
+
+def test_import_without_the_built_library_fails_loudly(tmp_path):
+    # a copy of the Python package with no compiled library next to it: the import must
+    # raise ImportError (no fallback path exists)
+    import shutil
+    import subprocess
+    import sys
+    src = os.path.join(ROOT, "serving_router_gate_gb300")
+    dst = tmp_path / "serving_router_gate_gb300"
+    dst.mkdir()
+    for name in os.listdir(src):
+        if name.endswith(".py"):
+            shutil.copy(os.path.join(src, name), dst / name)
+    code = ("import sys; sys.path.insert(0, sys.argv[1])\n"
+            "try:\n    import serving_router_gate_gb300\nexcept ImportError as e:\n"
+            "    print('ImportError:', e); sys.exit(0)\n"
+            "sys.exit(3)\n")
+    r = subprocess.run([sys.executable, "-c", code, str(tmp_path)], capture_output=True, text=True, timeout=300,
+                       cwd=str(tmp_path))
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "not built" in r.stdout
