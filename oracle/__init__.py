@@ -76,7 +76,7 @@ def _load():
         lib.oracle_expert_mlp.restype = None
         lib.oracle_moe_tokens.argtypes = [P, i64, i32, P, P, i32, i32, i32, i32, i32, i32, P, P, i32, i32, i32,
                                           P, P, i32, i32, P, P, i32, P, P, P, P, P, P, P, P, P,
-                                          i32, P, i64, P, P, P, P]
+                                          P, P, P, P, i32, P, i64, P, P, P, P]
         lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
         lib.oracle_e4m3_to_f64.restype = ctypes.c_double
         lib.oracle_f64_to_e4m3.argtypes = [ctypes.c_double]
@@ -327,7 +327,8 @@ def expert_mlp_nvfp4(x_row, W1q, W1sb, s1, W2q, W2sb, s2, act4=False):
 
 def moe_tokens(x, Wg, bias, k, renorm, W1, W2, tokens=None, rep_offset=None, rep_slots=None,
                local_start=0, local_count=-1, mode=NONLOCAL_SKIP,
-               W1s=None, W2s=None, shared_gate_w=None, n_group=1, topk_group=1, on_input=False, fp8=None):
+               W1s=None, W2s=None, shared_gate_w=None, n_group=1, topk_group=1, on_input=False, fp8=None,
+               nvfp4=None):
     """C oracle_moe_tokens: full layer output (float64) for the listed tokens.
 
     n_group / topk_group: group-limited top-k (n_group <= 1: plain top-k).
@@ -336,6 +337,9 @@ def moe_tokens(x, Wg, bias, k, renorm, W1, W2, tokens=None, rep_offset=None, rep
     fp8: None, or a dict of E4M3 weights with row scales (W1q, s1, W2q, s2 and,
     with shared experts, W1sq, s1s, W2sq, s2s) used in place of W1/W2/W1s/W2s;
     with act8=True in it, the activations are quantised to E4M3 per row as well.
+    nvfp4: None, or a dict of NVFP4 weights as quantize_nvfp4_rows returns them (W1q,
+    W1sb, s1, W2q, W2sb, s2 and, with shared experts, W1sq, W1ssb, s1s, W2sq, W2ssb,
+    s2s); with act4=True in it, the activations are quantised to NVFP4 per row as well.
 
     W1 [S_local, 2I, H], W2 [S_local, H, I] are indexed by local slot.
     W1s [n_shared, 2*I_sh, H] / W2s [n_shared, H, I_sh] (or None).
@@ -367,23 +371,27 @@ def moe_tokens(x, Wg, bias, k, renorm, W1, W2, tokens=None, rep_offset=None, rep
     ids = np.empty((n, k), np.int32)
     w = np.empty((n, k), np.float64)
     sl = np.empty((n, k), np.int32)
-    f = fp8 or {}
-    fq = {key: (_np(f[key], np.uint8) if key.endswith("q") else _np(f[key], np.float32)) if f.get(key) is not None
-          else None for key in ("W1q", "s1", "W2q", "s2", "W1sq", "s1s", "W2sq", "s2s")}
+    assert fp8 is None or nvfp4 is None, "one weight format at a time"
+    f = fp8 or nvfp4 or {}
+    keys = ("W1q", "s1", "W2q", "s2", "W1sq", "s1s", "W2sq", "s2s", "W1sb", "W2sb", "W1ssb", "W2ssb")
+    fq = {key: (_np(f[key], np.float32) if key.startswith("s") else _np(f[key], np.uint8))
+          if f.get(key) is not None else None for key in keys}
+    act = bool(f.get("act4", False)) if nvfp4 is not None else bool(f.get("act8", False))
     lib.oracle_moe_tokens(_ptr(x), T, H, _ptr(Wg), _ptr(bias), E, k, int(bool(renorm)),
                           int(n_group), int(topk_group), int(bool(on_input)),
                           _ptr(ro), _ptr(rs), local_start, local_count, mode,
                           _ptr(W1), _ptr(W2), I, n_shared, _ptr(W1s), _ptr(W2s), I_sh, _ptr(gw),
                           _ptr(fq["W1q"]), _ptr(fq["s1"]), _ptr(fq["W2q"]), _ptr(fq["s2"]),
                           _ptr(fq["W1sq"]), _ptr(fq["s1s"]), _ptr(fq["W2sq"]), _ptr(fq["s2s"]),
-                          int(bool(f.get("act8", False))), _ptr(tokens), n, _ptr(out), _ptr(ids), _ptr(w), _ptr(sl))
+                          _ptr(fq["W1sb"]), _ptr(fq["W2sb"]), _ptr(fq["W1ssb"]), _ptr(fq["W2ssb"]),
+                          int(act), _ptr(tokens), n, _ptr(out), _ptr(ids), _ptr(w), _ptr(sl))
     return dict(out=out, ids=ids, w=w, slots=sl)
 
 
 def moe_layer(x, Wg, bias, k, renorm, W1, W2, rep_offset=None, rep_slots=None,
               local_start=0, local_count=-1, mode=NONLOCAL_SKIP,
               W1s=None, W2s=None, shared_gate_w=None, S=None, n_group=1, topk_group=1, on_input=False,
-              fp8=None):
+              fp8=None, nvfp4=None):
     """The whole layer on a batch: routing, slot map, mask, permutation and outputs.
 
     Composes the C steps in the order the layer runs them; returns a dict with
@@ -403,7 +411,7 @@ def moe_layer(x, Wg, bias, k, renorm, W1, W2, rep_offset=None, rep_slots=None,
     counts, offsets, perm_src, pair_row = permute(slots_l, S_local)
     res = moe_tokens(x, Wg, bias, k, renorm, W1, W2, None, rep_offset, rep_slots,
                      local_start, local_count if local_count is not None else -1, mode,
-                     W1s, W2s, shared_gate_w, n_group, topk_group, on_input, fp8)
+                     W1s, W2s, shared_gate_w, n_group, topk_group, on_input, fp8, nvfp4)
     return dict(ids=ids, w=w, logits=logits, slots_global=slots, slots=slots_l, w_masked=w_l,
                 mask=mask, counts=counts, offsets=offsets, perm_src=perm_src,
                 pair_row=pair_row.reshape(ids.shape), out=res["out"])

@@ -634,7 +634,10 @@ void oracle_expert_mlp_nvfp4(const uint16_t *x, const uint8_t *W1q, const uint8_
  * with one fp32 scale per row (W1q [S_local, 2I, H] + s1 [S_local, 2I], W2q
  * [S_local, H, I] + s2 [S_local, H]; the shared ones alike).  act8 (E4M3
  * weights only): the expert input rows and intermediate rows are quantised to
- * E4M3 as well (oracle_quantize_act_row), the shared experts' too.
+ * E4M3 as well (oracle_quantize_act_row), the shared experts' too.  Where the
+ * block scales W1sb [S_local, 2I, H/16] / W2sb [S_local, H, I/16] (W1ssb /
+ * W2ssb for the shared experts) are given, W1q ... hold NVFP4 codes instead
+ * (oracle_expert_mlp_nvfp4), and act8 quantises the activations to NVFP4.
  *
  * Shared experts: n_shared experts of intermediate size I_sh each; W1s holds
  * them one after another, each [2*I_sh, H] (gate rows, then up rows); W2s holds
@@ -652,6 +655,7 @@ void oracle_moe_tokens(const uint16_t *x, int64_t T, int H,
                        const uint16_t *shared_gate_w,
                        const uint8_t *W1q, const float *s1, const uint8_t *W2q, const float *s2,
                        const uint8_t *W1sq, const float *s1s, const uint8_t *W2sq, const float *s2s,
+                       const uint8_t *W1sb, const uint8_t *W2sb, const uint8_t *W1ssb, const uint8_t *W2ssb,
                        int act8, const int64_t *tok, int64_t n,
                        double *out, int32_t *ids_out, double *w_out, int32_t *slot_out)
 {
@@ -705,7 +709,13 @@ void oracle_moe_tokens(const uint16_t *x, int64_t T, int H,
                 for (int hh = 0; hh < H; ++hh) xs[hh] = oracle_f64_to_bf16(w2[j] * oracle_bf16_to_f64(xt[hh]));
                 xin = xs;
             }
-            if (W1q)
+            if (W1q && W1sb)
+                oracle_expert_mlp_nvfp4(xin, W1q + (size_t)s * 2u * (size_t)I * (size_t)H,
+                                        W1sb + (size_t)s * 2u * (size_t)I * (size_t)(H / 16), s1 + (size_t)s * 2u * (size_t)I,
+                                        W2q + (size_t)s * (size_t)H * (size_t)I,
+                                        W2sb + (size_t)s * (size_t)H * (size_t)(I / 16), s2 + (size_t)s * (size_t)H,
+                                        H, I, act8, y, NULL);
+            else if (W1q)
                 (act8 ? oracle_expert_mlp_w8a8 : oracle_expert_mlp_fp8)(xin, W1q + (size_t)s * 2u * (size_t)I * (size_t)H, s1 + (size_t)s * 2u * (size_t)I,
                                       W2q + (size_t)s * (size_t)H * (size_t)I, s2 + (size_t)s * (size_t)H, H, I, y,
                                       NULL);
@@ -726,7 +736,14 @@ void oracle_moe_tokens(const uint16_t *x, int64_t T, int H,
             }
             double *ysum = (double *)calloc((size_t)H, sizeof(double));
             for (int sidx = 0; sidx < n_shared; ++sidx) {
-                if (W1sq)
+                if (W1sq && W1ssb)
+                    oracle_expert_mlp_nvfp4(xt, W1sq + (size_t)sidx * 2u * (size_t)I_sh * (size_t)H,
+                                            W1ssb + (size_t)sidx * 2u * (size_t)I_sh * (size_t)(H / 16),
+                                            s1s + (size_t)sidx * 2u * (size_t)I_sh,
+                                            W2sq + (size_t)sidx * (size_t)H * (size_t)I_sh,
+                                            W2ssb + (size_t)sidx * (size_t)H * (size_t)(I_sh / 16),
+                                            s2s + (size_t)sidx * (size_t)H, H, I_sh, act8, y, NULL);
+                else if (W1sq)
                     (act8 ? oracle_expert_mlp_w8a8 : oracle_expert_mlp_fp8)(xt, W1sq + (size_t)sidx * 2u * (size_t)I_sh * (size_t)H,
                                           s1s + (size_t)sidx * 2u * (size_t)I_sh,
                                           W2sq + (size_t)sidx * (size_t)H * (size_t)I_sh, s2s + (size_t)sidx * (size_t)H,

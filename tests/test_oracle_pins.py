@@ -835,3 +835,73 @@ def test_nvfp4_power_of_two_row_scale_for_activations():
     # with a power-of-two row scale, rows equal up to a power of two give the same codes
     q2, sb2, s2 = oracle.quantize_nvfp4_rows((v.float() * 2.0 ** 5).to(torch.bfloat16), pow2=True)
     assert np.array_equal(q2, q) and np.array_equal(sb2, sb)
+
+
+def _exact_nvfp4_rows(n_rows, K, gen):
+    """bf16 rows that are exactly e2m1 * sb * s with s = 2^-12, E4M3 block scales, and a
+    +-6 in every block (so each block's scale and the row's largest block, 448, come back)."""
+    grid_sb = _e4m3_np(np.arange(0x30, 0x7F, dtype=np.uint8))
+    sbv = gen.choice(grid_sb, (n_rows, K // 16))
+    sbv[:, 0] = 448.0
+    codes = gen.integers(0, 16, (n_rows, K // 16, 16))
+    codes[..., 0] = 7 | (8 * gen.integers(0, 2, (n_rows, K // 16)))
+    vals = np.array(_E2M1)[codes & 7] * np.where(codes & 8, -1.0, 1.0) * sbv[..., None] * 2.0 ** -12
+    return torch.from_numpy(vals.reshape(n_rows, K)).to(torch.bfloat16)
+
+
+def _nvfp4_dict(W1, W2, W1s=None, W2s=None, act4=False):
+    d = {}
+    d["W1q"], d["W1sb"], d["s1"] = oracle.quantize_nvfp4_rows(W1)
+    d["W2q"], d["W2sb"], d["s2"] = oracle.quantize_nvfp4_rows(W2)
+    if W1s is not None:
+        d["W1sq"], d["W1ssb"], d["s1s"] = oracle.quantize_nvfp4_rows(W1s)
+        d["W2sq"], d["W2ssb"], d["s2s"] = oracle.quantize_nvfp4_rows(W2s)
+    d["act4"] = act4
+    return d
+
+
+def test_nvfp4_layer_equals_bf16_when_weights_are_exact():
+    g = np.random.default_rng(14)
+    cfg = _small_cfg(T=20, H=64, I=64, E=5, k=2, renorm=True, n_shared=1, I_shared=64)
+    inp = mi.make_inputs(cfg)
+    W1 = _exact_nvfp4_rows(5 * 128, 64, g).reshape(5, 128, 64)
+    W2 = _exact_nvfp4_rows(5 * 64, 64, g).reshape(5, 64, 64)
+    W1s = _exact_nvfp4_rows(128, 64, g)[None]
+    W2s = _exact_nvfp4_rows(64, 64, g)[None]
+    d = _nvfp4_dict(W1, W2, W1s, W2s)
+    assert np.all(d["s1"] == np.float32(2.0 ** -12)) and np.all(d["s2"] == np.float32(2.0 ** -12))
+    y4, h4 = oracle.expert_mlp_nvfp4(inp["x"][0], d["W1q"][2], d["W1sb"][2], d["s1"][2], d["W2q"][2],
+                                     d["W2sb"][2], d["s2"][2])
+    yb, hb = oracle.expert_mlp(inp["x"][0], W1[2], W2[2])
+    assert np.array_equal(y4, yb) and np.array_equal(h4, hb)
+    a = oracle.moe_layer(inp["x"], inp["Wg"], None, 2, True, W1, W2, W1s=W1s, W2s=W2s)
+    b = oracle.moe_layer(inp["x"], inp["Wg"], None, 2, True, W1, W2, W1s=W1s, W2s=W2s, nvfp4=d)
+    assert np.array_equal(a["out"], b["out"])
+
+
+def test_nvfp4_layer_matches_numpy_mlp_of_dequantised_values():
+    cfg = _small_cfg(T=8, H=64, I=64, E=4, k=1, renorm=True, n_shared=1, I_shared=64)
+    inp = mi.make_inputs(cfg)
+    for act4 in (False, True):
+        d = _nvfp4_dict(inp["W1"], inp["W2"], inp["W1s"], inp["W2s"], act4=act4)
+        res = oracle.moe_layer(inp["x"], inp["Wg"], None, 1, True, inp["W1"], inp["W2"], W1s=inp["W1s"],
+                               W2s=inp["W2s"], nvfp4=d)
+        D1, D2 = _nvfp4_deq(d["W1q"], d["W1sb"], d["s1"]), _nvfp4_deq(d["W2q"], d["W2sb"], d["s2"])
+        S1, S2 = _nvfp4_deq(d["W1sq"], d["W1ssb"], d["s1s"])[0], _nvfp4_deq(d["W2sq"], d["W2ssb"], d["s2s"])[0]
+
+        def act(row_bf16):
+            if not act4:
+                return row_bf16.to(torch.float64).numpy()
+            q, sb, s = oracle.quantize_nvfp4_rows(row_bf16[None], pow2=True)
+            return _nvfp4_deq(q, sb, s)[0]
+
+        def mlp(xr, A, B):
+            x64 = act(xr)
+            gt, up = x64 @ A[:64].T, x64 @ A[64:].T
+            h = torch.from_numpy(gt / (1 + np.exp(-gt)) * up).to(torch.bfloat16)
+            return act(h) @ B.T
+
+        for t in range(cfg.T):
+            e = int(res["ids"][t, 0])
+            ref = mlp(inp["x"][t], D1[e], D2[e]) + mlp(inp["x"][t], S1, S2)
+            np.testing.assert_allclose(res["out"][t], ref, rtol=0, atol=1e-9 * np.abs(ref).max())
