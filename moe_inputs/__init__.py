@@ -83,6 +83,10 @@ CONFIGS = {
     "redundant_slots_prefill": MoEConfig("redundant_slots_prefill", T=16384, H=7168, I=2048, E=256,
                                          k=8, renorm=True, S=288, n_hot=32, zipf_s=1.1, w_std=0.01),
 }
+# a cut-down redundant-slot layer (same H and I, 16 slots of about 512 rows, a few GB on the
+# device) on which the FC1 DRAM traffic of the full workload is captured and scaled per slot
+CONFIGS["redundant_slots_cut16"] = MoEConfig("redundant_slots_cut16", T=1024, H=7168, I=2048, E=16, k=8,
+                                             renorm=True, w_std=0.01)
 # the router variants of the next steps, on the Qwen2-like and DeepSeek-V2-Lite-like shapes:
 # group-limited top-k (DeepSeek-V2-style: 8 groups, 3 kept, k = 6 of 64 experts) and the
 # routing weight applied on the expert input

@@ -15,8 +15,10 @@
 // each device looks its address up with cudaGetSymbolAddress (with that device
 // current) and caches it; that first call should therefore come before any
 // stream capture.  Every call uses the same array and overwrites every entry
-// it later reads, so nothing has to be cleared between calls; calls that
-// overlap on the GPU (two streams, or two devices' calls are fine) race on it.
+// it later reads, so nothing has to be cleared between calls.  Calls that
+// overlap on one device (on two streams, or two graph replays in flight) race
+// on it; calls ordered on one stream do not, and calls on different devices
+// use separate copies of the array.
 #include <algorithm>
 #include <mutex>
 
@@ -80,7 +82,10 @@ extern "C" MOE_API moe_status_t moe_route_noalloc(const moe_bf16_t* x, const flo
     moe_status_t st = device_scratch(&base, &sms);
     if (st != MOE_OK) return st;
 
-    // the split moe_route would use, reduced until its scratch fits the array
+    // the split moe_route would use, reduced until its scratch fits the array.  Each
+    // pass lowers nsplit by at least one (ranges of ceil(H / (nsplit - 1)) rounded up
+    // to 32), so the loop ends with a layout that fits: either the test failed, or
+    // nsplit reached 1, whose size was checked above.
     int nsplit = 1, KC = H;
     moe::router_plan(T, H, E, sms, &nsplit, &KC);
     while (nsplit > 1 && scratch_bytes(T, E, nsplit) > kNoallocScratchBytes) {
@@ -88,10 +93,6 @@ extern "C" MOE_API moe_status_t moe_route_noalloc(const moe_bf16_t* x, const flo
         kc = (kc + 31) / 32 * 32;
         KC = kc;
         nsplit = (H + kc - 1) / kc;
-    }
-    if (scratch_bytes(T, E, nsplit) > kNoallocScratchBytes) {
-        nsplit = 1;
-        KC = H;
     }
 
     moe::RouterLaunch L;

@@ -134,9 +134,10 @@ def test_two_runs_are_bitwise_identical():
 
 @pytest.mark.parametrize("mode", [0, 2])
 def test_gemm_tile_modes_single_and_pairs(mode):
-    # pairs of CTAs sharing weight tiles by multicast (mode 2 forces them on a
-    # mid-size layer: groups with odd and even m-tile counts, shared problem
-    # with an odd count) and single CTAs must give the same results
+    # CTA pairs running 2-SM MMAs, each CTA loading its own half of the weight
+    # tile (mode 2 forces them on a mid-size layer: groups with odd and even
+    # m-tile counts, shared problem with an odd count), and single CTAs must
+    # give the same results
     cfg = mi.MoEConfig("pairs", T=1400, H=512, I=384, E=6, k=3, renorm=True, n_shared=1, I_shared=384,
                        shared_gate=True)
     inp = mi.make_inputs(cfg)
@@ -577,7 +578,19 @@ def test_decode_workload_full(T):
     _full_check(make(f"dsv2_lite_like_decode_t{T}"))
 
 
-def _full_size(name, n_samples, local_ranges=None):
+def _tail_tile_tokens(g, k, n):
+    """Tokens with a pair in the last m-tile of its slot, where that tile is partial (fewer
+    than 128 rows): the last row of up to n such slots, spread over the slot range."""
+    off = g["offsets"].numpy().astype(np.int64)
+    perm = g["perm_src"].numpy()
+    cnt = off[1:] - off[:-1]
+    slots = np.flatnonzero((cnt > 0) & (cnt % 128 != 0))
+    if len(slots) > n:
+        slots = slots[np.linspace(0, len(slots) - 1, n).astype(np.int64)]
+    return np.unique(perm[off[slots + 1] - 1] // k).astype(np.int64)
+
+
+def _full_size(name, n_samples, local_ranges=None, n_tail=0):
     cfg = mi.CONFIGS[name]
     inp = mi.make_inputs(cfg, device="cpu", weights_device="cuda")
     inp_cpu = to_cpu(inp)
@@ -587,6 +600,8 @@ def _full_size(name, n_samples, local_ranges=None):
     if not cfg.on_input:  # rows scaled by the weights are checked in the routing-on-input tests
         check_x_perm(g, inp["x"].cuda(), cfg.k)
     tok = sample_tokens(cfg.T, n_samples)
+    if n_tail:
+        tok = np.union1d(tok, _tail_tile_tokens(g, cfg.k, n_tail))
     part = oracle_layer(inp_cpu, tokens=tok)
     check_out(g["out"][tok], part["out"])
     assert moe.moe_get_device_status(g["layer"].ws) == 0
@@ -609,11 +624,11 @@ def test_qwen2_moe_like_prefill_full_size():
 
 
 def test_large_expert_prefill_full_size_and_local_ranges():
-    _full_size("large_expert_prefill", 16, local_ranges=[(0, 64), (64, 64), (128, 64), (192, 64)])
+    _full_size("large_expert_prefill", 64, local_ranges=[(0, 64), (64, 64), (128, 64), (192, 64)], n_tail=16)
 
 
 def test_redundant_slots_prefill_full_size():
-    _full_size("redundant_slots_prefill", 16)
+    _full_size("redundant_slots_prefill", 64, n_tail=16)
 
 
 def test_grouped_topk_prefill_full_size():

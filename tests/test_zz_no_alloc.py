@@ -50,6 +50,52 @@ def test_noalloc_route_matches_route_on_two_calls_in_a_row():
     _route_both(cfg2)
 
 
+def _router_plan_splits(T, H, E, sms):
+    """The number of K ranges moe_route's split plan picks (its cost model: CTAs run in
+    waves of two per SM; a CTA costs its range plus about three 32-wide chunks)."""
+    tiles = -(-T // 64) * -(-E // 64)
+    slots = max(1, min(2 * sms, 2048))
+    best, best_ns = None, 1
+    for kc in range(32, H + 1, 32):
+        ns = -(-H // kc)
+        if ns > 32 or (ns - 1) * kc >= H or tiles * ns > 2048 + tiles:
+            continue
+        cost = -(-(tiles * ns) // slots) * (kc + 96)
+        if best is None or cost < best:
+            best, best_ns = cost, ns
+    return best_ns
+
+
+def test_noalloc_route_lowers_the_split_to_fit_and_still_matches_route():
+    # 153 x 4 token/expert tiles: moe_route splits H = 7168 into several K ranges whose
+    # partial logits (nsplit * T * E fp32) outgrow the 16 MiB array; the no-alloc call
+    # lowers the split until one fits (here down to a single range) and must still give
+    # moe_route's ids bit for bit and its weights within the certified bound
+    T, H, E, k = 153 * 64, 7168, 256, 8
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    ns = _router_plan_splits(T, H, E, sms)
+    assert ns > 1 and ns * T * E * 4 > 16 << 20, (ns, sms)
+    g = torch.Generator().manual_seed(11)
+    x = torch.randn((T, H), generator=g).to(torch.bfloat16)
+    Wg = torch.randn((E, H), generator=g) * 0.02
+    ids_a = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    w_a = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    ws = torch.empty(moe.moe_workspace_size(T, H, 64, E, E, k, 0), dtype=torch.uint8, device="cuda")
+    moe.moe_workspace_init(ws)
+    xd, Wd = x.cuda(), Wg.cuda()
+    moe.moe_route(xd, Wd, None, k, True, ids_a, w_a, ws)
+    for _ in range(2):
+        ids_b = torch.full((T, k), -7, dtype=torch.int32, device="cuda")
+        w_b = torch.full((T, k), float("nan"), dtype=torch.float32, device="cuda")
+        moe.moe_route_noalloc(xd, Wd, None, k, True, ids_b, w_b)
+        torch.cuda.synchronize()
+        assert torch.equal(ids_a, ids_b)
+        B = router_bound(x, Wg, None, H)
+        rel = np.expm1(4.0 * B)[:, None] + 128 * 2.0 ** -24
+        wa, wb = w_a.cpu().double().numpy(), w_b.cpu().double().numpy()
+        assert np.all(np.abs(wa - wb) <= rel * np.abs(wa) + 1e-7)
+
+
 def test_noalloc_route_rejects_sizes_beyond_its_scratch():
     T, H, E = 20000, 64, 256  # T*(E+1) floats > 16 MiB even with a single K range
     x = torch.zeros((T, H), dtype=torch.bfloat16, device="cuda")
