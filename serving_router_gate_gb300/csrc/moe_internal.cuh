@@ -20,6 +20,8 @@ struct WsHeader {
     int32_t status;              // OR of MOE_ERR_DEVICE_BOUNDS / MOE_ERR_TIMEOUT
     int32_t pad0;
     unsigned long long refined;  // tokens whose top-k needed the fp64 recheck
+    unsigned int route_ticket;   // small-batch router: CTAs of the running launch that have
+                                 // written their logits (back to 0 when the launch ends)
 };
 
 __device__ __forceinline__ void report(int32_t* status, int32_t code) {
@@ -123,6 +125,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Pull `bytes` (a multiple of 16, from a 16-byte-aligned address) of global memory
+// into L2 (no shared memory, no completion to wait for).
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+                 : "memory");
 }
 
 // Pull one box of a tensor into L2 (no shared memory, no completion to wait for).
@@ -415,6 +424,13 @@ struct GemmLaunch {
     const float* b_scale_sh;   // [Nb_sh] row scales of b_sh (E4M3 B only)
     const float* a_scale;      // [rows_cap] row scales of a (GEMM_W8A8 only)
     const float* a_scale_sh;   // [T_sh] row scales of a_sh (GEMM_W8A8 only)
+    // FC1 of a small batch: the weights the next GEMM (FC2) will stream, pulled into L2
+    // by each CTA once it has issued its last load (null: none).  Group g's bytes are
+    // next_b + g * next_b_group_bytes, for the groups that have rows; then the shared ones.
+    const void* next_b = nullptr;
+    int64_t next_b_group_bytes = 0;
+    const void* next_b_sh = nullptr;
+    int64_t next_b_sh_bytes = 0;
 };
 enum { GEMM_BF16 = 0, GEMM_W8 = 1, GEMM_W8A8 = 2 };
 cudaError_t launch_grouped_gemm(const GemmLaunch& L, int num_sms, cudaStream_t s, const char** why);

@@ -42,6 +42,15 @@ constexpr int PM_ROUNDS = PM_CHUNK / 32;
 constexpr int PM_WARPS = 8;       // warps per CTA in K1 / K3
 constexpr int PM_SCAN_THREADS = 1024;
 
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ int32_t map_slot(int32_t e, int64_t t, int E, const int32_t* __restrict__ rep_offset,
                                             const int32_t* __restrict__ rep_slots, int S, int32_t* status) {
     if (e < 0 || e >= E) {
@@ -307,6 +316,149 @@ __global__ void __launch_bounds__(PM_SCAN_THREADS) permute_small_kernel(
         scatter_pairs(pb, x, slot_ids, rank, chunk_base, S_local, P, k, H, pair_row, perm_src, x_perm, wsc);
 }
 
+// ---- one CTA for tiny batches (at most one chunk of pairs): every phase in shared
+// memory, no scratch in global memory ----
+//
+// The token rows are staged in shared memory while warp 0 maps, masks and ranks
+// the pairs (as rank_chunk does, ranks kept in shared memory); the block then
+// scans the counts, places every pair and writes the rows of x_perm from the
+// staged copy.  The kernel lets the next one on the stream launch as soon as it
+// starts: the grouped GEMM that follows prefetches weights (which no kernel
+// writes) before it waits for this one to finish.
+constexpr int PT_THREADS = 512;
+constexpr int PT_WARPS = PT_THREADS / 32;
+constexpr int64_t PT_MAX_X_BYTES = 96 * 1024;
+
+__global__ void __launch_bounds__(PT_THREADS) permute_tiny_kernel(
+    const int32_t* __restrict__ ids, float* __restrict__ w, int T, int k, int E,
+    const int32_t* __restrict__ rep_offset, const int32_t* __restrict__ rep_slots, int S, int local_start,
+    int local_count, int mode, int S_local, const uint16_t* __restrict__ x, int H, int32_t* __restrict__ slot_ids,
+    int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ perm_src,
+    int32_t* __restrict__ pair_row, uint16_t* __restrict__ x_perm, int scale_rows, int32_t* status) {
+    extern __shared__ __align__(16) unsigned char pt_smem[];
+    uint16_t* xs = reinterpret_cast<uint16_t*>(pt_smem);                      // [T][H]
+    int32_t* cnt = reinterpret_cast<int32_t*>(pt_smem + (size_t)T * H * 2);   // [S_local]
+    int32_t* off = cnt + S_local;                                             // [S_local]
+    const int P = T * k;
+    int32_t* s_slot = off + S_local;                                          // [P]
+    int32_t* s_rank = s_slot + P;                                             // [P]
+    int32_t* s_row = s_rank + P;                                              // [P]
+    float* s_w = reinterpret_cast<float*>(s_row + P);                         // [P]
+    __shared__ int32_t s_wsum[PT_WARPS];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_trigger();
+    pdl_wait();
+
+    const int vec = H / 8;
+    for (int i = tid; i < T * vec; i += PT_THREADS) cp_async16(xs + (size_t)i * 8, x + (size_t)i * 8);
+    cp_async_commit();
+    for (int s = tid; s < S_local; s += PT_THREADS) cnt[s] = 0;
+    __syncthreads();
+
+    if (warp == 0) {
+        // slot map + mask, then the stable rank of each pair among the pairs of its slot
+        int32_t sl[PM_ROUNDS];
+#pragma unroll
+        for (int r = 0; r < PM_ROUNDS; ++r) {
+            const int p = r * 32 + lane;
+            sl[r] = p < P ? ids[p] : INT32_MIN;
+        }
+#pragma unroll
+        for (int r = 0; r < PM_ROUNDS; ++r) {
+            const int p = r * 32 + lane;
+            if (p >= P) {
+                sl[r] = -2;
+                continue;
+            }
+            int32_t sv = map_slot(sl[r], p / k, E, rep_offset, rep_slots, S, status);
+            float wp = w[p];
+            if (local_count >= 0) {
+                const bool local = (sv >= local_start) && (sv < local_start + local_count);
+                wp = wp * (local ? 1.0f : 0.0f);
+                w[p] = wp;
+                if (sv >= 0) sv = local ? sv - local_start : (mode == MOE_NONLOCAL_MOD ? sv % local_count : -1);
+            }
+            slot_ids[p] = sv;
+            s_slot[p] = sv;
+            s_w[p] = wp;
+            sl[r] = sv;
+        }
+        const uint32_t lt_mask = (1u << lane) - 1u;
+#pragma unroll
+        for (int r = 0; r < PM_ROUNDS; ++r) {
+            const int32_t sv = sl[r];
+            const uint32_t peers = __match_any_sync(0xffffffffu, sv);
+            if (sv >= 0) s_rank[r * 32 + lane] = cnt[sv] + __popc(peers & lt_mask);
+            __syncwarp();
+            if (sv >= 0 && lane == 31 - __clz(peers)) cnt[sv] += __popc(peers);
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+
+    // counts and their exclusive scan: thread i takes slots 2i and 2i + 1
+    const int s0 = 2 * tid;
+    const int32_t c0 = s0 < S_local ? cnt[s0] : 0, c1 = s0 + 1 < S_local ? cnt[s0 + 1] : 0;
+    int32_t incl = c0 + c1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) s_wsum[warp] = incl;
+    __syncthreads();
+    int32_t before = 0;
+    for (int i = 0; i < warp; ++i) before += s_wsum[i];
+    const int32_t ex = before + incl - (c0 + c1);
+    if (s0 < S_local) {
+        counts[s0] = c0;
+        offsets[s0] = ex;
+        off[s0] = ex;
+    }
+    if (s0 + 1 < S_local) {
+        counts[s0 + 1] = c1;
+        offsets[s0 + 1] = ex + c0;
+        off[s0 + 1] = ex + c0;
+    }
+    if (tid == PT_THREADS - 1) {
+        int32_t total = 0;
+        for (int i = 0; i < PT_WARPS; ++i) total += s_wsum[i];
+        offsets[S_local] = total;
+    }
+    __syncthreads();
+
+    for (int p = tid; p < P; p += PT_THREADS) {
+        const int32_t sv = s_slot[p];
+        const int32_t row = sv >= 0 ? off[sv] + s_rank[p] : -1;
+        pair_row[p] = row;
+        if (row >= 0) perm_src[row] = p;
+        s_row[p] = row;
+    }
+    cp_async_wait_group<0>();
+    __syncthreads();
+
+    // rows of x_perm from the staged token rows (or, with the routing applied on
+    // the input, bf16(w * x))
+    for (int f = tid; f < P * vec; f += PT_THREADS) {
+        const int p = f / vec, v = f - p * vec;
+        const int32_t row = s_row[p];
+        if (row < 0) continue;
+        const uint4 src = *reinterpret_cast<const uint4*>(xs + (size_t)(p / k) * H + (size_t)v * 8);
+        uint4* dst = reinterpret_cast<uint4*>(x_perm + (int64_t)row * H) + v;
+        if (!scale_rows) {
+            *dst = src;
+        } else {
+            const float wj = s_w[p];
+            float fx[8];
+            unpack8(src, fx);
+            uint32_t o[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) o[i] = bf16_of_product(wj, fx[2 * i]) | (bf16_of_product(wj, fx[2 * i + 1]) << 16);
+            *dst = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    }
+}
+
 }  // namespace
 
 static size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
@@ -333,6 +485,17 @@ cudaError_t launch_permute(const PermuteLaunch& L, int num_sms, cudaStream_t s) 
     const int64_t P = L.T * L.k;
     const int64_t nchunks = (P + PM_CHUNK - 1) / PM_CHUNK;
     int32_t* status = &L.hdr->status;
+    if (P <= PM_CHUNK && L.S_local <= 2 * PT_THREADS && L.T * (int64_t)L.H * 2 <= PT_MAX_X_BYTES) {
+        const size_t smem = (size_t)L.T * L.H * 2 + (size_t)2 * L.S_local * sizeof(int32_t) +
+                            (size_t)4 * P * sizeof(int32_t);
+        cudaError_t e = cudaFuncSetAttribute(permute_tiny_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (e != cudaSuccess) return e;
+        return launch_k("permute_tiny", permute_tiny_kernel, dim3(1), dim3(PT_THREADS), smem, s, L.ids, L.w,
+                        (int)L.T, L.k, L.E, L.rep_offset, L.rep_slots, L.S, L.local_start, L.local_count, L.mode,
+                        L.S_local, L.x, L.H, L.slot_ids, L.counts, L.offsets, L.perm_src, L.pair_row, L.x_perm,
+                        (int)L.scale_rows, status);
+    }
     if (P <= PM_SMALL_MAX_P && L.S_local <= PM_SMALL_MAX_S) {
         const size_t smem_small = (size_t)PM_SMALL_WARPS * L.S_local * sizeof(int32_t);
         if (smem_small > 48 * 1024) {

@@ -457,6 +457,199 @@ __device__ __forceinline__ float pick(const float (&l)[PL], int idx) {
     return v;
 }
 
+// Selection of one token by one warp, from its fp32 logits l (lane holds experts
+// lane + 32 i; bias added, NaN already -inf, experts >= E at -inf): the group step
+// (if any), the candidates in (logit desc, id asc) order until the cluster that
+// holds rank k-1 closes, the certified rechecks of near-tied clusters that touch
+// ranks 0..k-1, then the fp32 softmax over all E and the k (renormalised)
+// probabilities.  thr / thr2: gaps below which two fp32 / compensated values may
+// be in either true order.  Scratch: this warp's s_ref (double), s_e (int), s_v
+// (float), s_l (float), E entries each.  Writes ids[0..k) and wout[0..k).
+template <int PL>
+__device__ __forceinline__ void select_token(float (&l)[PL], float thr, float thr2, int n_group, int topk_group,
+                                             const float* __restrict__ bias, const uint16_t* __restrict__ xrow,
+                                             const float* __restrict__ Wg, int H, int E, int k, int renorm,
+                                             double* s_ref, int* s_e, float* s_v, float* s_l, int lane,
+                                             int32_t* __restrict__ ids, float* __restrict__ wout, WsHeader* hdr) {
+    // group-limited top-k: experts of groups that are not kept start out taken
+    uint32_t taken = 0;
+    if (n_group > 1 && topk_group < n_group) {
+        const uint32_t keep = select_groups(l, s_l, s_e, s_ref, E, n_group, topk_group, thr, thr2, xrow, Wg, bias,
+                                            H, lane);
+        const int gsize = E / n_group;
+#pragma unroll
+        for (int i = 0; i < PL; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E && !((keep >> (e / gsize)) & 1u)) taken |= 1u << i;
+        }
+    }
+
+    // extract candidates in (logit desc, id asc) order until the cluster
+    // that contains rank k-1 is closed
+    int R = 0;
+    float prev_v = 0.f;
+    while (R < E) {
+        float bv = -INFINITY;
+        int be = INT_MAX;
+#pragma unroll
+        for (int i = 0; i < PL; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E && !((taken >> i) & 1u)) {
+                if (l[i] > bv || (l[i] == bv && e < be)) {
+                    bv = l[i];
+                    be = e;
+                }
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+            const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+            if (ov > bv || (ov == bv && oe < be)) {
+                bv = ov;
+                be = oe;
+            }
+        }
+        if (be == INT_MAX) break;
+        if ((be & 31) == lane) taken |= 1u << (be >> 5);
+        if (lane == 0) {
+            s_e[R] = be;
+            s_v[R] = bv;
+        }
+        ++R;
+        if (R >= k + 1) {
+            const float gap = prev_v - bv;
+            if (!(gap <= thr)) break;
+        }
+        prev_v = bv;
+    }
+    __syncwarp();
+
+    // refine each ambiguous cluster that touches ranks 0..k-1
+    bool refined = false;
+    int a = 0;
+    while (a < R && a < k) {
+        int b = a;
+        while (b + 1 < R && (s_v[b] - s_v[b + 1]) <= thr) ++b;
+        if (b > a) {
+            refined = true;
+            // compensated fp32 values first; fp64 only if they still leave a gap
+            // within twice their bound (plus the fp64 rounding of the exact order)
+            for (int pass = 0; pass < 2; ++pass) {
+                for (int m = a; m <= b; ++m) {
+                    const int e = s_e[m];
+                    const float* wr = Wg + (int64_t)e * H;
+                    double v = pass == 0 ? refine_dot2(xrow, wr, H, lane) : refine_dot(xrow, wr, H, lane);
+                    if (bias) v += (double)bias[e];
+                    if (lane == 0) s_ref[m] = v;
+                }
+                __syncwarp();
+                if (lane == 0) {  // insertion sort of positions a..b: value desc, id asc
+                    for (int m = a + 1; m <= b; ++m) {
+                        const double v = s_ref[m];
+                        const int e = s_e[m];
+                        int q = m - 1;
+                        while (q >= a && (s_ref[q] < v || (s_ref[q] == v && s_e[q] > e))) {
+                            s_ref[q + 1] = s_ref[q];
+                            s_e[q + 1] = s_e[q];
+                            --q;
+                        }
+                        s_ref[q + 1] = v;
+                        s_e[q + 1] = e;
+                    }
+                }
+                __syncwarp();
+                if (pass == 1) break;
+                bool decided = true;
+                for (int m = a; m < b; ++m) decided = decided && (s_ref[m] - s_ref[m + 1] > (double)thr2);
+                if (decided) break;
+            }
+            for (int m = a; m <= b; ++m) {  // refined values feed the softmax
+                const int e = s_e[m];
+                const float v = (float)s_ref[m];
+                if ((e & 31) == lane) {
+#pragma unroll
+                    for (int i = 0; i < PL; ++i)
+                        if (i == (e >> 5)) l[i] = v;
+                }
+            }
+        }
+        a = b + 1;
+    }
+    if (refined && lane == 0 && hdr) atomicAdd(&hdr->refined, 1ull);
+
+    // softmax over all E, probabilities of the selected k
+    float mx = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < PL; ++i)
+        if (lane + 32 * i < E) mx = fmaxf(mx, l[i]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    float z = 0.f;
+#pragma unroll
+    for (int i = 0; i < PL; ++i)
+        if (lane + 32 * i < E) z += expf(l[i] - mx);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+
+    float psum = 0.f, my_p = 0.f;
+    int my_e = 0;
+    for (int j = 0; j < k; ++j) {
+        const int e = s_e[j];
+        const float v = __shfl_sync(0xffffffffu, pick(l, e >> 5), e & 31);
+        const float p = expf(v - mx) / z;
+        psum += p;
+        if (j == lane) {
+            my_p = p;
+            my_e = e;
+        }
+    }
+    if (lane < k) {
+        ids[lane] = my_e;
+        wout[lane] = renorm ? my_p / psum : my_p;
+    }
+    __syncwarp();
+}
+
+// max_e ||w_e|| and max_e |b_e| from the split partial squared norms wsq
+// [nsplit][E] (block-wide; every thread returns the same values).
+__device__ __forceinline__ void weight_norm_max(const float* __restrict__ wsq, int nsplit, int E,
+                                                const float* __restrict__ bias, float (*s_red)[32],
+                                                float& wnorm_max, float& bias_max) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    float wm = 0.f, bm = 0.f;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        float v[RT_MAX_SPLIT];  // all loads in flight before the (ordered) sum
+#pragma unroll
+        for (int q = 0; q < RT_MAX_SPLIT; ++q) v[q] = q < nsplit ? __ldcg(wsq + (int64_t)q * E + e) : 0.f;
+        float s = 0.f;
+#pragma unroll
+        for (int q = 0; q < RT_MAX_SPLIT; ++q) s += v[q];
+        wm = fmaxf(wm, s);
+        if (bias) bm = fmaxf(bm, fabsf(__ldg(bias + e)));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, off));
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, off));
+    }
+    if (lane == 0) {
+        s_red[0][warp] = wm;
+        s_red[1][warp] = bm;
+    }
+    __syncthreads();
+    wm = 0.f;
+    bm = 0.f;
+    for (int i = 0; i < nw; ++i) {
+        wm = fmaxf(wm, s_red[0][i]);
+        bm = fmaxf(bm, s_red[1][i]);
+    }
+    // fp32 bound arithmetic: the threshold coefficients carry a 1 % margin, far above
+    // the relative rounding (< 2^-20) of the few fp32 operations on these values
+    wnorm_max = sqrtf(wm);
+    bias_max = bm;
+}
+
 // PL = experts per lane (E <= 32 * PL); lane holds experts lane + 32*i.
 template <int PL>
 __global__ void __launch_bounds__(RS_WARPS * 32) router_select_kernel(
@@ -478,40 +671,11 @@ __global__ void __launch_bounds__(RS_WARPS * 32) router_select_kernel(
     // grouped top-k: this warp's fp32 logits, by expert id
     float* s_l = reinterpret_cast<float*>(rs_smem + (size_t)RS_WARPS * E * (sizeof(double) + sizeof(int) + sizeof(float))) +
                  (size_t)warp * E;
-    __shared__ float s_red[2][RS_WARPS];
+    __shared__ float s_red[2][32];
 
-    // CTA prologue: max_e ||w_e||^2 and max_e |b_e|
-    float wm = 0.f, bm = 0.f;
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        float v[RT_MAX_SPLIT];  // all loads in flight before the (ordered) sum
-#pragma unroll
-        for (int q = 0; q < RT_MAX_SPLIT; ++q) v[q] = q < nsplit ? __ldg(wsq + (int64_t)q * E + e) : 0.f;
-        float s = 0.f;
-#pragma unroll
-        for (int q = 0; q < RT_MAX_SPLIT; ++q) s += v[q];
-        wm = fmaxf(wm, s);
-        if (bias) bm = fmaxf(bm, fabsf(__ldg(bias + e)));
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, off));
-        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, off));
-    }
-    if (lane == 0) {
-        s_red[0][warp] = wm;
-        s_red[1][warp] = bm;
-    }
-    __syncthreads();
-    wm = 0.f;
-    bm = 0.f;
-    for (int i = 0; i < RS_WARPS; ++i) {
-        wm = fmaxf(wm, s_red[0][i]);
-        bm = fmaxf(bm, s_red[1][i]);
-    }
-    // fp32 bound arithmetic: thr_coef already carries a 1 % margin, far above the
-    // relative rounding (< 2^-20) of the few fp32 operations below
-    const float wnorm_max = sqrtf(wm);
-    const float bias_max = bm;
+    // CTA prologue: max_e ||w_e|| and max_e |b_e|
+    float wnorm_max, bias_max;
+    weight_norm_max(wsq, nsplit, E, bias, s_red, wnorm_max, bias_max);
 
     for (int64_t t = (int64_t)blockIdx.x * RS_WARPS + warp; t < T; t += (int64_t)gridDim.x * RS_WARPS) {
         // fp32 logits of this token: sum of the split partials in split order, then the bias
@@ -554,147 +718,168 @@ __global__ void __launch_bounds__(RS_WARPS * 32) router_select_kernel(
         const float thr = thr_coef * fmaf(sqrtf(xs2), wnorm_max, bias_max);
         // the same for the compensated values (twice their bound)
         const float thr2 = thr2_coef * fmaf(sqrtf(xs2), wnorm_max, bias_max);
-
-        // group-limited top-k: experts of groups that are not kept start out taken
-        uint32_t taken = 0;
-        if (n_group > 1 && topk_group < n_group) {
-            const uint32_t keep = select_groups(l, s_l, s_e, s_ref, E, n_group, topk_group, thr, thr2,
-                                                x + t * (int64_t)H, Wg, bias, H, lane);
-            const int gsize = E / n_group;
-#pragma unroll
-            for (int i = 0; i < PL; ++i) {
-                const int e = lane + 32 * i;
-                if (e < E && !((keep >> (e / gsize)) & 1u)) taken |= 1u << i;
-            }
-        }
-
-        // extract candidates in (logit desc, id asc) order until the cluster
-        // that contains rank k-1 is closed
-        int R = 0;
-        float prev_v = 0.f;
-        while (R < E) {
-            float bv = -INFINITY;
-            int be = INT_MAX;
-#pragma unroll
-            for (int i = 0; i < PL; ++i) {
-                const int e = lane + 32 * i;
-                if (e < E && !((taken >> i) & 1u)) {
-                    if (l[i] > bv || (l[i] == bv && e < be)) {
-                        bv = l[i];
-                        be = e;
-                    }
-                }
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-                const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-                if (ov > bv || (ov == bv && oe < be)) {
-                    bv = ov;
-                    be = oe;
-                }
-            }
-            if (be == INT_MAX) break;
-            if ((be & 31) == lane) taken |= 1u << (be >> 5);
-            if (lane == 0) {
-                s_e[R] = be;
-                s_v[R] = bv;
-            }
-            ++R;
-            if (R >= k + 1) {
-                const float gap = prev_v - bv;
-                if (!(gap <= thr)) break;
-            }
-            prev_v = bv;
-        }
-        __syncwarp();
-
-        // refine each ambiguous cluster that touches ranks 0..k-1
-        bool refined = false;
-        int a = 0;
-        while (a < R && a < k) {
-            int b = a;
-            while (b + 1 < R && (s_v[b] - s_v[b + 1]) <= thr) ++b;
-            if (b > a) {
-                refined = true;
-                // compensated fp32 values first; fp64 only if they still leave a gap
-                // within twice their bound (plus the fp64 rounding of the exact order)
-                for (int pass = 0; pass < 2; ++pass) {
-                    for (int m = a; m <= b; ++m) {
-                        const int e = s_e[m];
-                        const uint16_t* xr = x + t * (int64_t)H;
-                        const float* wr = Wg + (int64_t)e * H;
-                        double v = pass == 0 ? refine_dot2(xr, wr, H, lane) : refine_dot(xr, wr, H, lane);
-                        if (bias) v += (double)bias[e];
-                        if (lane == 0) s_ref[m] = v;
-                    }
-                    __syncwarp();
-                    if (lane == 0) {  // insertion sort of positions a..b: value desc, id asc
-                        for (int m = a + 1; m <= b; ++m) {
-                            const double v = s_ref[m];
-                            const int e = s_e[m];
-                            int q = m - 1;
-                            while (q >= a && (s_ref[q] < v || (s_ref[q] == v && s_e[q] > e))) {
-                                s_ref[q + 1] = s_ref[q];
-                                s_e[q + 1] = s_e[q];
-                                --q;
-                            }
-                            s_ref[q + 1] = v;
-                            s_e[q + 1] = e;
-                        }
-                    }
-                    __syncwarp();
-                    if (pass == 1) break;
-                    bool decided = true;
-                    for (int m = a; m < b; ++m) decided = decided && (s_ref[m] - s_ref[m + 1] > (double)thr2);
-                    if (decided) break;
-                }
-                for (int m = a; m <= b; ++m) {  // refined values feed the softmax
-                    const int e = s_e[m];
-                    const float v = (float)s_ref[m];
-                    if ((e & 31) == lane) {
-#pragma unroll
-                        for (int i = 0; i < PL; ++i)
-                            if (i == (e >> 5)) l[i] = v;
-                    }
-                }
-            }
-            a = b + 1;
-        }
-        if (refined && lane == 0 && hdr) atomicAdd(&hdr->refined, 1ull);
-
-        // softmax over all E, probabilities of the selected k
-        float mx = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < PL; ++i)
-            if (lane + 32 * i < E) mx = fmaxf(mx, l[i]);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        float z = 0.f;
-#pragma unroll
-        for (int i = 0; i < PL; ++i)
-            if (lane + 32 * i < E) z += expf(l[i] - mx);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
-
-        float psum = 0.f, my_p = 0.f;
-        int my_e = 0;
-        for (int j = 0; j < k; ++j) {
-            const int e = s_e[j];
-            const float v = __shfl_sync(0xffffffffu, pick(l, e >> 5), e & 31);
-            const float p = expf(v - mx) / z;
-            psum += p;
-            if (j == lane) {
-                my_p = p;
-                my_e = e;
-            }
-        }
-        if (lane < k) {
-            ids[t * k + lane] = my_e;
-            wout[t * k + lane] = renorm ? my_p / psum : my_p;
-        }
-        __syncwarp();
+        select_token<PL>(l, thr, thr2, n_group, topk_group, bias, x + t * (int64_t)H, Wg, H, E, k, renorm, s_ref,
+                         s_e, s_v, s_l, lane, ids + t * k, wout + t * k, hdr);
     }
+}
+
+// ---------------------------------------------------------------------------
+// Small batches (decode): one launch for logits and selection.
+//
+// Each CTA (16 warps) stages the T <= 16 token rows in shared memory, then
+// computes the complete logits of `epb` experts: warp w takes expert
+// epb * blockIdx.x + (w % epb) over part (w / epb) of the QN = 16 / epb parts of
+// H.  Lane l of a part takes its 8-element pieces l, l + 32, ...; piece i of a
+// lane feeds accumulator (i & 1) of each token with 8 chained fmas; the two
+// accumulators are added, the lanes summed by an xor butterfly, and the parts in
+// part order, so a logit's rounding depth is n = 8 ceil(npl / 2) + 1 + 5 +
+// (QN - 1) (+ 1 for the bias), npl = pieces per lane.  The squared row norms of
+// Wg come out of the same loads.  The logits and norms go to the workspace; the
+// CTA that finishes last (a ticket in the workspace header) runs the selection
+// of every token -- one warp per token, as router_select_kernel does -- with the
+// bound of this depth.  Non-last CTAs simply exit; the last one puts the ticket
+// back to 0 before it lets the next kernel launch, so launches never overlap
+// on the ticket.
+constexpr int RSM_WARPS = 16;
+constexpr int RSM_THREADS = RSM_WARPS * 32;
+constexpr int RSM_MAX_T = 16;
+constexpr int RSM_MAX_NPL = 8;  // pieces per lane: all of a lane's weight loads in flight at once
+
+template <int PL>
+__global__ void __launch_bounds__(RSM_THREADS, 1) router_small_kernel(
+    const uint16_t* __restrict__ x, const float* __restrict__ Wg, const float* __restrict__ bias, int T, int H,
+    int E, int k, int renorm, int epb, float thr_coef, float thr2_coef, int n_group, int topk_group,
+    float* __restrict__ lg, float* __restrict__ wsq, int32_t* __restrict__ ids, float* __restrict__ wout,
+    WsHeader* hdr) {
+    extern __shared__ __align__(16) unsigned char rsm[];
+    uint16_t* xs = reinterpret_cast<uint16_t*>(rsm);                              // [T][H]
+    float* part = reinterpret_cast<float*>(rsm + (size_t)T * H * 2);             // [RSM_WARPS][T]
+    float* wpart = part + RSM_WARPS * RSM_MAX_T;                                 // [RSM_WARPS]
+    unsigned char* sel = reinterpret_cast<unsigned char*>(wpart + RSM_WARPS);   // select scratch
+    __shared__ float s_red[2][32];
+    __shared__ int s_last;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_wait();
+
+    // token rows -> shared memory (one round trip for all of them)
+    const int nvec = T * H / 8;
+    for (int i = tid; i < nvec; i += RSM_THREADS) cp_async16(xs + (size_t)i * 8, x + (size_t)i * 8, true);
+    cp_async_commit();
+
+    const int QN = RSM_WARPS / epb;
+    const int jw = warp % epb, q = warp / epb;
+    const int e = blockIdx.x * epb + jw;
+    const int NP = H / 8;
+    const int pb = (int)((int64_t)NP * q / QN), pe = (int)((int64_t)NP * (q + 1) / QN);
+    // this lane's weight pieces, all loads issued before the first use
+    float4 wv[RSM_MAX_NPL][2];
+    const float* wrow = Wg + (int64_t)(e < E ? e : 0) * H;
+#pragma unroll
+    for (int i = 0; i < RSM_MAX_NPL; ++i) {
+        const int pc = pb + lane + 32 * i;
+        const bool ok = e < E && pc < pe;
+        wv[i][0] = ok ? __ldg(reinterpret_cast<const float4*>(wrow) + 2 * pc) : make_float4(0.f, 0.f, 0.f, 0.f);
+        wv[i][1] = ok ? __ldg(reinterpret_cast<const float4*>(wrow) + 2 * pc + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float wn = 0.f;
+#pragma unroll
+    for (int i = 0; i < RSM_MAX_NPL; ++i) {
+        wn = fmaf(wv[i][0].x, wv[i][0].x, wn); wn = fmaf(wv[i][0].y, wv[i][0].y, wn);
+        wn = fmaf(wv[i][0].z, wv[i][0].z, wn); wn = fmaf(wv[i][0].w, wv[i][0].w, wn);
+        wn = fmaf(wv[i][1].x, wv[i][1].x, wn); wn = fmaf(wv[i][1].y, wv[i][1].y, wn);
+        wn = fmaf(wv[i][1].z, wv[i][1].z, wn); wn = fmaf(wv[i][1].w, wv[i][1].w, wn);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) wn += __shfl_xor_sync(0xffffffffu, wn, off);
+    cp_async_wait_group<0>();
+    __syncthreads();
+
+    for (int t = 0; t < T; ++t) {
+        const uint16_t* xr = xs + (size_t)t * H;
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int i = 0; i < RSM_MAX_NPL; ++i) {
+            const int pc = pb + lane + 32 * i;
+            if (pc < pe) {
+                float xf[8];
+                unpack8(*reinterpret_cast<const uint4*>(xr + (size_t)pc * 8), xf);
+                float a = (i & 1) ? a1 : a0;
+                a = fmaf(xf[0], wv[i][0].x, a); a = fmaf(xf[1], wv[i][0].y, a);
+                a = fmaf(xf[2], wv[i][0].z, a); a = fmaf(xf[3], wv[i][0].w, a);
+                a = fmaf(xf[4], wv[i][1].x, a); a = fmaf(xf[5], wv[i][1].y, a);
+                a = fmaf(xf[6], wv[i][1].z, a); a = fmaf(xf[7], wv[i][1].w, a);
+                if (i & 1) a1 = a; else a0 = a;
+            }
+        }
+        float v = a0 + a1;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+        if (lane == 0) part[warp * RSM_MAX_T + t] = v;
+    }
+    if (lane == 0) wpart[warp] = wn;
+    __syncthreads();
+    // the parts of each logit in part order (warp jw + epb * q holds part q of expert jw)
+    for (int i = tid; i < epb * T; i += RSM_THREADS) {
+        const int jj = i % epb, t = i / epb, ee = blockIdx.x * epb + jj;
+        if (ee >= E) continue;
+        float v = part[jj * RSM_MAX_T + t];
+        for (int qq = 1; qq < QN; ++qq) v += part[(jj + epb * qq) * RSM_MAX_T + t];
+        lg[(int64_t)t * E + ee] = v;
+    }
+    if (tid < epb && blockIdx.x * epb + tid < E) {
+        float v = wpart[tid];
+        for (int qq = 1; qq < QN; ++qq) v += wpart[tid + epb * qq];
+        wsq[blockIdx.x * epb + tid] = v;
+    }
+    // publish, then take a ticket; the last CTA to arrive sees every CTA's writes
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = atomicAdd(&hdr->route_ticket, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (!s_last) return;
+    if (tid == 0) hdr->route_ticket = 0u;  // every CTA of this launch has taken its ticket
+    __threadfence();
+    pdl_trigger();
+
+    // ---- selection, one warp per token (the last CTA only) ----
+    float wnorm_max, bias_max;
+    weight_norm_max(wsq, 1, E, bias, s_red, wnorm_max, bias_max);
+    double* s_ref = reinterpret_cast<double*>(sel) + (size_t)warp * E;
+    int* s_e = reinterpret_cast<int*>(reinterpret_cast<double*>(sel) + (size_t)RSM_WARPS * E) + (size_t)warp * E;
+    float* s_v = reinterpret_cast<float*>(reinterpret_cast<int*>(reinterpret_cast<double*>(sel) +
+                                                                 (size_t)RSM_WARPS * E) +
+                                          (size_t)RSM_WARPS * E) +
+                 (size_t)warp * E;
+    float* s_l = reinterpret_cast<float*>(sel + (size_t)RSM_WARPS * E * (sizeof(double) + sizeof(int) + sizeof(float))) +
+                 (size_t)warp * E;
+    if (warp >= T) return;
+    const int t = warp;
+    float l[PL];
+#pragma unroll
+    for (int i = 0; i < PL; ++i) {
+        const int ee = lane + 32 * i;
+        float v = -INFINITY;
+        if (ee < E) {
+            v = __ldcg(lg + (int64_t)t * E + ee);
+            if (bias) v += bias[ee];
+            if (v != v) v = -INFINITY;  // NaN logits never win
+        }
+        l[i] = v;
+    }
+    // squared norm of x_t: only bounds the error (inflated by 1.01), order is immaterial
+    float xs2 = 0.f;
+    for (int pc = lane; pc < NP; pc += 32) {
+        float xf[8];
+        unpack8(*reinterpret_cast<const uint4*>(xs + (size_t)t * H + (size_t)pc * 8), xf);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) xs2 = fmaf(xf[i], xf[i], xs2);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) xs2 += __shfl_xor_sync(0xffffffffu, xs2, off);
+    const float thr = thr_coef * fmaf(sqrtf(xs2), wnorm_max, bias_max);
+    const float thr2 = thr2_coef * fmaf(sqrtf(xs2), wnorm_max, bias_max);
+    select_token<PL>(l, thr, thr2, n_group, topk_group, bias, x + (int64_t)t * H, Wg, H, E, k, renorm, s_ref, s_e,
+                     s_v, s_l, lane, ids + (int64_t)t * k, wout + (int64_t)t * k, hdr);
 }
 
 }  // namespace
@@ -755,7 +940,67 @@ void router_carve(void* base, int64_t T, int E, float** part, float** xsq, float
     *wsq = reinterpret_cast<float*>(p + a + b);
 }
 
+// Plan of the small-batch router: experts per CTA (epb) and parts of H per
+// expert (16 / epb), or false if the batch does not fit its envelope.
+static bool small_router_plan(const RouterLaunch& L, int* epb, size_t* smem) {
+    if (!L.hdr || L.T < 1 || L.T > RSM_MAX_T) return false;
+    const int NP = L.H / 8;
+    int qn_min = 1;
+    while (qn_min < RSM_WARPS && (NP + qn_min - 1) / qn_min > 32 * RSM_MAX_NPL) qn_min <<= 1;
+    if ((NP + qn_min - 1) / qn_min > 32 * RSM_MAX_NPL) return false;
+    int e = 1;
+    while (e * 2 <= RSM_WARPS / qn_min && e * 2 * 16 <= L.E) e <<= 1;
+    *epb = e;
+    *smem = (size_t)L.T * L.H * 2 + sizeof(float) * (RSM_WARPS * RSM_MAX_T + RSM_WARPS) +
+            (size_t)RSM_WARPS * L.E * (sizeof(double) + sizeof(int) + 2 * sizeof(float));
+    return *smem <= 200 * 1024;
+}
+
 cudaError_t launch_router(const RouterLaunch& L, int num_sms, cudaStream_t s) {
+    const double u32 = 1.0 / 16777216.0, u64 = 1.0 / 9007199254740992.0;
+    const double g64 = (L.H + 2.0) * u64 / (1.0 - (L.H + 2.0) * u64);
+    // compensated recheck: (gamma_{ceil(H/128)} + gamma_128)^2 per value, plus
+    // the fp64 rounding of the exact order and of hi + lo + bias
+    const double na = (L.H + 127) / 128, nc = 128.0;
+    const double ga = na * u32 / (1.0 - na * u32), gc = nc * u32 / (1.0 - nc * u32);
+    const float thr2_coef = (float)(2.0 * ((ga + gc) * (ga + gc) + g64 + 3.0 * u64) * 1.01);
+
+    int epb = 1;
+    size_t smem_small = 0;
+    if (small_router_plan(L, &epb, &smem_small)) {
+        // rounding depth of the small kernel: the fma chains of one accumulator (8 per
+        // piece), the two accumulators, the lane butterfly, the parts of H, the bias
+        const int QN = RSM_WARPS / epb;
+        const int NP = L.H / 8;
+        const int npl = ((NP + QN - 1) / QN + 31) / 32;
+        const int chain_n = 8 * ((npl + 1) / 2) + 1 + 5 + (QN - 1) + 1;
+        const double g32 = chain_n * u32 / (1.0 - chain_n * u32);
+        const float thr_coef = (float)(2.0 * (g32 + g64) * 1.01);
+        const unsigned grid = (unsigned)((L.E + epb - 1) / epb);
+        cudaError_t err = cudaSuccess;
+#define MOE_SMALL(PLV)                                                                                           \
+    do {                                                                                                         \
+        err = cudaFuncSetAttribute(router_small_kernel<PLV>, cudaFuncAttributeMaxDynamicSharedMemorySize,        \
+                                   (int)smem_small);                                                             \
+        if (err != cudaSuccess) return err;                                                                      \
+        err = launch_k("router_small", router_small_kernel<PLV>, dim3(grid), dim3(RSM_THREADS), smem_small, s,   \
+                       L.x, L.Wg, L.bias, (int)L.T, L.H, L.E, L.k, L.renorm, epb, thr_coef, thr2_coef, L.n_group, \
+                       L.topk_group, L.part, L.wsq, L.ids, L.w, L.hdr);                                          \
+    } while (0)
+        if (L.E <= 32)
+            MOE_SMALL(1);
+        else if (L.E <= 64)
+            MOE_SMALL(2);
+        else if (L.E <= 128)
+            MOE_SMALL(4);
+        else if (L.E <= 256)
+            MOE_SMALL(8);
+        else
+            MOE_SMALL(16);
+#undef MOE_SMALL
+        return err;
+    }
+
     const int64_t tT = (L.T + RT_BT - 1) / RT_BT;
     const int tE = (L.E + RT_BE - 1) / RT_BE;
     dim3 grid1((unsigned)tT, (unsigned)tE, (unsigned)L.nsplit);
@@ -774,15 +1019,8 @@ cudaError_t launch_router(const RouterLaunch& L, int num_sms, cudaStream_t s) {
     const int chain_n = RT_BK / 2 + 1 + RT_GROUP + groups + L.nsplit + 1;
     // per-logit bound B_t = (gamma_n(fp32) + gamma_{H+2}(fp64)) * (||x_t|| max||w_e|| + max|b_e|);
     // threshold on a gap = 2 B_t, with a 1 % margin that covers the fp32 evaluation
-    const double u32 = 1.0 / 16777216.0, u64 = 1.0 / 9007199254740992.0;
     const double g32 = chain_n * u32 / (1.0 - chain_n * u32);
-    const double g64 = (L.H + 2.0) * u64 / (1.0 - (L.H + 2.0) * u64);
     const float thr_coef = (float)(2.0 * (g32 + g64) * 1.01);
-    // compensated recheck: (gamma_{ceil(H/128)} + gamma_128)^2 per value, plus
-    // the fp64 rounding of the exact order and of hi + lo + bias
-    const double na = (L.H + 127) / 128, nc = 128.0;
-    const double ga = na * u32 / (1.0 - na * u32), gc = nc * u32 / (1.0 - nc * u32);
-    const float thr2_coef = (float)(2.0 * ((ga + gc) * (ga + gc) + g64 + 3.0 * u64) * 1.01);
     const size_t smem = (size_t)RS_WARPS * L.E * (sizeof(double) + sizeof(int) + 2 * sizeof(float));
     const int64_t want = (L.T + RS_WARPS - 1) / RS_WARPS;
     const unsigned grid2 = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms * 8));
