@@ -93,14 +93,8 @@ MOE_API const char *moe_status_string(int status);
  * caller will pass, as [TRT-10985] sizes its workspace by max_num_tokens. */
 MOE_API size_t moe_workspace_size(int64_t max_T, int H, int I, int E, int S, int k, int I_shared_total);
 
-/* The first MOE_WS_HEADER_BYTES bytes of every workspace are its header: the
- * device status word, counters and the tickets of tiles split over K.  Kernels
- * leave every counter and ticket at zero when they finish, so the header is
- * zeroed only once, by moe_workspace_init; a caller never writes it. */
-#define MOE_WS_HEADER_BYTES 4096
-
-/* Zero the workspace's header (status word, counters, tickets).  Call once
- * after allocating ws, before the first call that uses it. */
+/* Zero the workspace's header (status word and counters).  Call once after
+ * allocating ws, before the first call that uses it. */
 MOE_API moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, moe_stream_t stream);
 
 /* Read the device status word (an OR of MOE_ERR_DEVICE_BOUNDS /

@@ -40,7 +40,6 @@ MOE_ERR_TIMEOUT = 16
 MOE_NONLOCAL_SKIP = 0
 MOE_NONLOCAL_MOD = 1
 MOE_LAUNCH_LABEL_BYTES = 48  # bytes per label written by moe_launch_events_used
-MOE_WS_HEADER_BYTES = 4096   # the workspace header (status word, counters, tickets) a caller never writes
 
 EXPORTED_SYMBOLS = (
     "moe_status_string", "moe_workspace_size", "moe_workspace_init", "moe_get_device_status",

@@ -62,6 +62,8 @@ size_t a256(size_t v) { return (v + 255) & ~(size_t)255; }
 // FC2's length, so its tiles do not outlast the routed ones; the fp32 partials
 // are summed by the combine.
 constexpr int64_t kSplitMaxT = 128;
+// batches of at most this many tokens pull FC2's weights into L2 from FC1
+constexpr int64_t kPrefetchNextMaxT = 64;
 constexpr int kSplitMax = 8;
 
 int shared_split(int64_t T, int I, int I_sh) {
@@ -70,30 +72,14 @@ int shared_split(int64_t T, int I, int I_sh) {
     return r < 2 ? 1 : (r > kSplitMax ? kSplitMax : r);
 }
 
-// FC1 of batches of at most this many tokens may split its routed tiles over K
-// (at most 4 ranges) when the batch has at most kSplitRtMaxTiles routed tiles;
-// the fp32 partials of a range are [32 rows][256 columns].
-constexpr int64_t kSplitRtMaxT = 32;
-constexpr int64_t kSplitRtMaxTiles = 128;
-constexpr int64_t kSplitRtUnitBytes = 32 * 256 * 4;
-
-// Upper bound of FC1's routed 256-column tiles for P pair rows in S_local groups.
-int64_t fc1_tile_bound(int64_t P, int S_local, int I) {
-    return (int64_t)((I + 127) / 128) * ((P + 127) / 128 + std::min<int64_t>(S_local, P));
-}
-
 struct ForwardLayout {
     size_t h, h_sh, y, y_sh, y_sh_part;
     // E4M3 activations: quantised expert inputs, shared input, intermediates, and scales
     size_t xq, sxq, xsq, sxs, hq, shq, hsq, shs;
     size_t total;
-    // after total: FC1's split-K partials of small batches (rt_units of them; 0: none)
-    size_t rt_part;
-    int64_t rt_units;
-    size_t total_split;
 };
 
-ForwardLayout forward_layout(int64_t P_cap, int64_t T, int H, int I, int I_sh, int S_local) {
+ForwardLayout forward_layout(int64_t P_cap, int64_t T, int H, int I, int I_sh) {
     ForwardLayout L;
     size_t off = kWsHeaderBytes;
     L.h = off;
@@ -125,11 +111,6 @@ ForwardLayout forward_layout(int64_t P_cap, int64_t T, int H, int I, int I_sh, i
     L.shs = off;
     off += a256(T_sh * 4);
     L.total = off;
-    const int64_t tiles = fc1_tile_bound(P_cap, S_local, I);
-    L.rt_units = (T <= kSplitRtMaxT && tiles <= kSplitRtMaxTiles) ? 4 * tiles : 0;
-    L.rt_part = off;
-    off += a256((size_t)L.rt_units * kSplitRtUnitBytes);
-    L.total_split = off;
     return L;
 }
 
@@ -217,13 +198,10 @@ size_t moe_workspace_size(int64_t max_T, int H, int I, int E, int S, int k, int 
     const int64_t P = max_T * k;
     size_t need = route_need(max_T, H, E);
     need = std::max(need, permute_need(P, S));
-    need = std::max(need, forward_layout(P, max_T, H, I, I_shared_total, S).total_split);
+    need = std::max(need, forward_layout(P, max_T, H, I, I_shared_total).total);
     // a call with fewer tokens may split the shared FC2 (fp32 partials, largest at
     // T = min(max_T, 128)) where max_T does not; every other region grows with T and P
-    need = std::max(need, forward_layout(P, std::min<int64_t>(max_T, kSplitMaxT), H, I, I_shared_total, S).total_split);
-    // and batches of at most 32 tokens may split FC1's routed tiles over K
-    for (int64_t t = 1; t <= std::min<int64_t>(max_T, kSplitRtMaxT); ++t)
-        need = std::max(need, forward_layout(t * k, t, H, I, I_shared_total, S).total_split);
+    need = std::max(need, forward_layout(P, std::min<int64_t>(max_T, kSplitMaxT), H, I, I_shared_total).total);
     return need;
 }
 
@@ -378,8 +356,9 @@ static moe_status_t gemm_call(bool fc1, const moe_bf16_t* a, int64_t rows_cap, c
                               cudaStream_t s, float* out_sh_part = nullptr, int ksplit_sh = 1,
                               int64_t max_group_rows = -1, const float* b_scale = nullptr,
                               const float* b_scale_sh = nullptr, const float* a_scale = nullptr,
-                              const float* a_scale_sh = nullptr, float* rt_part = nullptr,
-                              int64_t rt_units_cap = 0) {
+                              const float* a_scale_sh = nullptr, const void* next_b = nullptr,
+                              int64_t next_b_group_bytes = 0, const void* next_b_sh = nullptr,
+                              int64_t next_b_sh_bytes = 0) {
     GemmLaunch L;
     L.swiglu = fc1;
     L.a = a;
@@ -412,8 +391,10 @@ static moe_status_t gemm_call(bool fc1, const moe_bf16_t* a, int64_t rows_cap, c
     L.b_scale_sh = b_scale_sh;
     L.a_scale = a_scale;
     L.a_scale_sh = a_scale_sh;
-    L.rt_part = rt_part;
-    L.rt_units_cap = rt_units_cap;
+    L.next_b = next_b;
+    L.next_b_group_bytes = next_b_group_bytes;
+    L.next_b_sh = next_b_sh;
+    L.next_b_sh_bytes = next_b_sh_bytes;
     const char* why = nullptr;
     return cuda_status(launch_grouped_gemm(L, device_sms(), s, &why));
 }
@@ -574,14 +555,8 @@ static moe_status_t forward_impl(const moe_bf16_t* x_perm, const int32_t* offset
     if (shared_gate_w && (I_shared_total == 0 || !x)) return MOE_ERR_INVALID_ARG;
     const bool fp8 = s1 != nullptr;
     if (fp8 && (!s2 || (I_shared_total > 0 && (!s1s || !s2s)))) return MOE_ERR_INVALID_ARG;
-    const ForwardLayout FL = forward_layout(P_cap, T, H, I, I_shared_total, S_local);
+    const ForwardLayout FL = forward_layout(P_cap, T, H, I, I_shared_total);
     if (!ws || ws_bytes < FL.total) return MOE_ERR_WORKSPACE;
-    // FC1 of a small batch may split its routed tiles over K, if the workspace has room
-    // for the partials (moe_workspace_size always leaves it)
-    float* rt_part = (FL.rt_units > 0 && ws_bytes >= FL.total_split)
-                         ? reinterpret_cast<float*>(static_cast<char*>(ws) + FL.rt_part)
-                         : nullptr;
-    const int64_t rt_units = rt_part ? FL.rt_units : 0;
     char* base = static_cast<char*>(ws);
     moe_bf16_t* h = reinterpret_cast<moe_bf16_t*>(base + FL.h);
     moe_bf16_t* h_sh = I_shared_total > 0 ? reinterpret_cast<moe_bf16_t*>(base + FL.h_sh) : nullptr;
@@ -590,6 +565,14 @@ static moe_status_t forward_impl(const moe_bf16_t* x_perm, const int32_t* offset
     cudaStream_t s = (cudaStream_t)stream;
     const int ks = shared_split(T, I, I_shared_total);
     float* y_sh_part = ks > 1 ? reinterpret_cast<float*>(base + FL.y_sh_part) : nullptr;
+    // Small batches stream weights: once an FC1 CTA has issued its last load it pulls
+    // its share of FC2's weights (the slots with rows, then the shared expert's) into
+    // L2, so FC2's stream starts during FC1's tail.
+    const bool pf = T <= kPrefetchNextMaxT;
+    const int64_t wb = fp8 ? 1 : 2;  // bytes per weight
+    const void* nb = pf ? W2 : nullptr;
+    const void* nbs = pf && I_shared_total > 0 ? W2s : nullptr;
+    const int64_t nb_bytes = (int64_t)H * I * wb, nbs_bytes = (int64_t)H * I_shared_total * wb;
     moe_status_t st;
     if (act8) {
         if (!aligned(x_perm, 16) || (I_shared_total > 0 && !aligned(x, 16))) return MOE_ERR_INVALID_ARG;
@@ -621,7 +604,7 @@ static moe_status_t forward_impl(const moe_bf16_t* x_perm, const int32_t* offset
         st = gemm_call(true, reinterpret_cast<const moe_bf16_t*>(u8(FL.xq)), P_cap, offsets, S_local,
                        static_cast<const moe_bf16_t*>(W1), H, I, reinterpret_cast<const moe_bf16_t*>(u8(FL.xsq)), T,
                        static_cast<const moe_bf16_t*>(W1s), I_shared_total, h, h_sh, ws, s, nullptr, 1, T, s1, s1s,
-                       f32(FL.sxq), f32(FL.sxs), rt_part, rt_units);
+                       f32(FL.sxq), f32(FL.sxs), nb, nb_bytes, nbs, nbs_bytes);
         if (st != MOE_OK) return st;
         const ActQuantSeg qh[2] = {{h, P_cap, offsets + S_local, I, u8(FL.hq), f32(FL.shq)},
                                    {h_sh, T_sh, nullptr, I_shared_total, u8(FL.hsq), f32(FL.shs)}};
@@ -634,7 +617,7 @@ static moe_status_t forward_impl(const moe_bf16_t* x_perm, const int32_t* offset
     } else {
         st = gemm_call(true, x_perm, P_cap, offsets, S_local, static_cast<const moe_bf16_t*>(W1), H, I, x, T,
                        static_cast<const moe_bf16_t*>(W1s), I_shared_total, h, h_sh, ws, s, nullptr, 1, T, s1, s1s,
-                       nullptr, nullptr, rt_part, rt_units);
+                       nullptr, nullptr, nb, nb_bytes, nbs, nbs_bytes);
         if (st != MOE_OK) return st;
         st = gemm_call(false, h, P_cap, offsets, S_local, static_cast<const moe_bf16_t*>(W2), H, I, h_sh, T,
                        static_cast<const moe_bf16_t*>(W2s), I_shared_total, y, y_sh, ws, s, y_sh_part, ks, T, s2, s2s);

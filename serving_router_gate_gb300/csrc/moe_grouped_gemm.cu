@@ -113,11 +113,10 @@ struct GemmParams {
     int kb_split_sh;         // K steps per range
     int prefetch_sh;         // FC1: pull this CTA's shared-problem weights into L2 before
                              // waiting on the previous kernel (shared problems of <= 64 rows)
-    int ksplit_rt;           // FC1, short tiles: K ranges per routed tile (1: not split)
-    int kb_split_rt;         // K steps per range
-    float* rt_part;          // fp32 partials [routed tile * ksplit_rt + range][32][BN]
-    unsigned int* rt_ticket; // per routed tile: ranges finished (back to 0 by the last one)
-    int rt_cap_tiles;        // routed tiles the partials and tickets have room for
+    const uint8_t* next_b;   // FC1 of a small batch: FC2's weights, pulled into L2 once this
+    int64_t next_b_group_bytes;  // CTA has issued its last load (see GemmLaunch)
+    const uint8_t* next_b_sh;
+    int64_t next_b_sh_bytes;
     int32_t* status;
     uint64_t timeout_ns;
 };
@@ -150,9 +149,8 @@ struct Tile {
     int nt;          // n-tile
     int row0;        // first row in A / out of this CTA's m-tile
     int rows_valid;  // rows of this CTA's m-tile that belong to the group (may be 0)
-    int ks;          // K range of a split shared or routed tile (0 otherwise)
+    int ks;          // K range of a split shared tile (0 otherwise)
     int kb0, kb1;    // K steps [kb0, kb1) of this tile
-    int rt;          // routed tile index (split routed tiles)
 };
 
 // work units along M: pairs of m-tiles in pair mode, single m-tiles otherwise
@@ -177,13 +175,9 @@ __device__ __forceinline__ Tile tile_of(int u, const GemmParams& p, const SmemMe
         tl.rows_valid = (int)max((int64_t)0, min((int64_t)BM, p.T_sh - (int64_t)mt * BM));
         tl.kb0 = tl.ks * p.kb_split_sh;
         tl.kb1 = min(p.kb_total_sh, tl.kb0 + p.kb_split_sh);
-        tl.rt = 0;
         return tl;
     }
     u -= n_sh_tiles;
-    // split routed tiles: the K ranges of one tile are consecutive units
-    const int ks = u % p.ksplit_rt;
-    u /= p.ksplit_rt;
     int lo = 0, hi = p.G;
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
@@ -202,10 +196,9 @@ __device__ __forceinline__ Tile tile_of(int u, const GemmParams& p, const SmemMe
     const int mt = kPair ? 2 * (local % MU) + crank : local % MU;
     tl.row0 = m.off[g] + mt * BM;
     tl.rows_valid = max(0, min(BM, M - mt * BM));
-    tl.ks = ks;
-    tl.rt = u;
-    tl.kb0 = ks * p.kb_split_rt;
-    tl.kb1 = min(p.kb_total, tl.kb0 + p.kb_split_rt);
+    tl.ks = 0;
+    tl.kb0 = 0;
+    tl.kb1 = p.kb_total;
     return tl;
 }
 
@@ -330,7 +323,7 @@ __global__ void __launch_bounds__(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS,
     const int n_long = unit0 < n_sh_tiles ? (n_sh_tiles - unit0 + nunits - 1) / nunits : 0;
     const int light0 = n_sh_tiles % nunits;  // first CTA with one shared unit fewer
     const int len_sh = p.ksplit_sh > 1 ? p.kb_split_sh : p.kb_total_sh;
-    const int len_rt = max(1, p.ksplit_rt > 1 ? p.kb_split_rt : p.kb_total);
+    const int len_rt = max(1, p.kb_total);
     const int bonus_q = light0 == 0 ? 0 : max(1, (len_sh + len_rt / 2) / len_rt);
     auto next_unit = [&](int i, bool& have) -> int {
         if (i < n_long) return unit0 + i * nunits;
@@ -409,7 +402,7 @@ __global__ void __launch_bounds__(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS,
         const int total = __shfl_sync(0xffffffffu, incl, 31);
         if (lane == 0) {
             m.ts[G] = total;
-            m.routed_tiles = total * p.ksplit_rt;
+            m.routed_tiles = total;
             if (!ok) report(p.status, MOE_ERR_DEVICE_BOUNDS);
         }
         __syncwarp();
@@ -485,6 +478,26 @@ __global__ void __launch_bounds__(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS,
                         phase ^= 1u;
                     }
                 }
+            }
+            if (!failed && (p.next_b || p.next_b_sh) && have && (!kPair || crank == 0)) {
+                // this CTA's share of the next GEMM's weights (the groups with rows, then the
+                // shared ones), pulled into L2 while the tiles still in the ring finish
+                int64_t total = p.next_b_sh ? p.next_b_sh_bytes : 0;
+                if (p.next_b)
+                    for (int g = 0; g < p.G; ++g) total += m.off[g + 1] > m.off[g] ? p.next_b_group_bytes : 0;
+                const int64_t lo = total * unit0 / nunits / 256 * 256;
+                const int64_t hi = unit0 + 1 == nunits ? total : total * (unit0 + 1) / nunits / 256 * 256;
+                int64_t base = 0;
+                auto seg = [&](const uint8_t* ptr, int64_t n) {
+                    const int64_t a = max(lo, base), b = min(hi, base + n);
+                    for (int64_t c = a; c < b; c += 65536)
+                        prefetch_l2_bulk(ptr + (c - base), (uint32_t)min((int64_t)65536, b - c));
+                    base += n;
+                };
+                if (p.next_b)
+                    for (int g = 0; g < p.G && base < hi; ++g)
+                        if (m.off[g + 1] > m.off[g]) seg(p.next_b + g * p.next_b_group_bytes, p.next_b_group_bytes);
+                if (p.next_b_sh && base < hi) seg(p.next_b_sh, p.next_b_sh_bytes);
             }
             if (failed) {
                 m.abort = 1;
@@ -619,32 +632,7 @@ __global__ void __launch_bounds__(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS,
             const float asc =
                 (kA8 && valid) ? __ldg((tl.prob ? p.a_scale_sh : p.a_scale) + tl.row0 + row_in) : 1.0f;
             auto bscale = [&](int row) -> float { return (kFp8 || kA8) ? __ldg(srow + row) : 1.0f; };
-            // K range tl.ks of a routed tile split over K (FC1, short tiles): its rows, at
-            // most 32 and all in the warp of lane quarter 0, store the raw fp32
-            // accumulators; a range past the last K step issued no MMA and stores zeros
-            const bool rsplit = kFC1 && kShort && !tl.prob && p.ksplit_rt > 1;
-            const bool rs_ok = rsplit && tl.rt < p.rt_cap_tiles;
-            if (rsplit && !rs_ok && row_in == 0) report(p.status, MOE_ERR_DEVICE_BOUNDS);
-            if (rsplit) {
-                if (q == 0 && rs_ok) {
-                    float* prow = p.rt_part + ((int64_t)(tl.rt * p.ksplit_rt + tl.ks) * BM_SHORT + lane) * BN;
-                    const bool kz = tl.kb1 > tl.kb0;
-#pragma unroll 1
-                    for (int c = 0; c < BN; c += 32) {
-                        uint32_t r[32];
-                        tmem_ld32(taddr + (uint32_t)c, r);
-                        tmem_ld_wait();
-                        if (valid) {
-                            float4* dst = reinterpret_cast<float4*>(prow + c);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e)
-                                dst[e] = kz ? make_float4(__uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1]),
-                                                          __uint_as_float(r[4 * e + 2]), __uint_as_float(r[4 * e + 3]))
-                                            : make_float4(0.f, 0.f, 0.f, 0.f);
-                        }
-                    }
-                }
-            } else if (kFC1) {
+            if (kFC1) {
 #pragma unroll 1
                 for (int c = 0; c < OW; c += 32) {
                     uint32_t g[32], v[32];
@@ -724,62 +712,6 @@ __global__ void __launch_bounds__(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS,
                     mbar_arrive_cluster(mapa_shared(&m.tempty[buf], 0));  // the leader's barrier
                 else
                     mbar_arrive(&m.tempty[buf]);
-            }
-            if (rs_ok && q == 0) {
-                // the tile's ranges take tickets; the last one sums the partials in range
-                // order (each written before its range's ticket), then applies the SwiGLU
-                __threadfence();
-                __syncwarp();
-                unsigned int old = 0;
-                if (lane == 0) old = atomicAdd(p.rt_ticket + tl.rt, 1u);
-                old = __shfl_sync(0xffffffffu, old, 0);
-                if (old == (unsigned int)p.ksplit_rt - 1u) {
-                    if (lane == 0) p.rt_ticket[tl.rt] = 0u;  // every range of the tile has arrived
-                    __threadfence();
-                    if (valid) {
-                        const float* pr0 = p.rt_part + ((int64_t)tl.rt * p.ksplit_rt * BM_SHORT + lane) * BN;
-                        const int N_out = p.N_out;
-                        uint16_t* orow = p.out + (int64_t)(tl.row0 + row_in) * N_out;
-                        const float* srow = (kFp8 || kA8) ? p.scale + (int64_t)tl.g * p.Nb : nullptr;
-                        const float asc = kA8 ? __ldg(p.a_scale + tl.row0 + row_in) : 1.0f;
-                        auto bscale = [&](int row) -> float { return (kFp8 || kA8) ? __ldg(srow + row) : 1.0f; };
-#pragma unroll 1
-                        for (int c = 0; c < OW; c += 32) {
-                            const int col = tl.nt * OW + c;
-                            if (col >= N_out) break;
-                            float gs[32], us[32];
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) gs[i] = us[i] = 0.f;
-#pragma unroll 1
-                            for (int kk = 0; kk < p.ksplit_rt; ++kk) {
-                                const float4* gp = reinterpret_cast<const float4*>(pr0 + (int64_t)kk * BM_SHORT * BN + c);
-                                const float4* up = reinterpret_cast<const float4*>(pr0 + (int64_t)kk * BM_SHORT * BN + BN / 2 + c);
-#pragma unroll
-                                for (int e = 0; e < 8; ++e) {
-                                    const float4 a = __ldcg(gp + e), b = __ldcg(up + e);
-                                    gs[4 * e] += a.x; gs[4 * e + 1] += a.y; gs[4 * e + 2] += a.z; gs[4 * e + 3] += a.w;
-                                    us[4 * e] += b.x; us[4 * e + 1] += b.y; us[4 * e + 2] += b.z; us[4 * e + 3] += b.w;
-                                }
-                            }
-                            uint32_t pk[16];
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) {
-                                float h2[2];
-#pragma unroll
-                                for (int z = 0; z < 2; ++z) {
-                                    const float gv = gs[2 * e + z] * bscale(col + 2 * e + z) * asc;
-                                    const float uv = us[2 * e + z] * bscale(p.up_off + col + 2 * e + z) * asc;
-                                    h2[z] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
-                                }
-                                pk[e] = pack_bf16x2(h2[0], h2[1]);
-                            }
-                            uint4* dst = reinterpret_cast<uint4*>(orow + col);
-#pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
-                        }
-                    }
-                }
             }
         }
     } else if (kFp8 && warp >= 6) {
@@ -1081,29 +1013,10 @@ cudaError_t launch_bn(const GemmLaunch& L, int num_sms, int64_t bound, cudaStrea
     // (measured: one token 6 % off the layer step, 8 and 32 tokens 1-2 %; at 128 tokens the
     // shared stream no longer fits in the window and the prefetch costs about 1 %)
     p.prefetch_sh = (kFC1 && has_shared && L.T_sh <= 64) ? 1 : 0;
-    // Small batches: too few routed tiles to keep every SM streaming weights, and a CTA
-    // streams at a fixed rate (the bytes its ring keeps in flight over the memory
-    // latency), so each routed tile's K is split into ranges until the routed units
-    // about match the SMs; the last range of a tile to finish sums the partials
-    p.ksplit_rt = 1;
-    p.kb_split_rt = p.kb_total;
-    p.rt_part = nullptr;
-    p.rt_ticket = nullptr;
-    p.rt_cap_tiles = 0;
-    if (kFC1 && kShort && !kPair && has_routed && L.rt_part) {
-        const int64_t nt = (L.N_out + BN / 2 - 1) / (BN / 2);
-        const int64_t tiles = nt * ((L.rows_cap + BM - 1) / BM + std::min<int64_t>(L.G, L.rows_cap));
-        int ks = (int)std::min<int64_t>(4, (num_sms + tiles / 2) / std::max<int64_t>(1, tiles));
-        ks = std::min(ks, p.kb_total);
-        while (ks > 1 && (tiles * ks > L.rt_units_cap || tiles > kMaxTickets)) --ks;
-        if (ks > 1) {
-            p.ksplit_rt = ks;
-            p.kb_split_rt = (p.kb_total + ks - 1) / ks;
-            p.rt_part = L.rt_part;
-            p.rt_ticket = reinterpret_cast<unsigned int*>(reinterpret_cast<char*>(L.hdr) + kTicketOffset);
-            p.rt_cap_tiles = (int)tiles;
-        }
-    }
+    p.next_b = kFC1 && has_routed ? static_cast<const uint8_t*>(L.next_b) : nullptr;
+    p.next_b_group_bytes = L.next_b_group_bytes;
+    p.next_b_sh = kFC1 && has_shared ? static_cast<const uint8_t*>(L.next_b_sh) : nullptr;
+    p.next_b_sh_bytes = L.next_b_sh_bytes;
     p.out = L.out;
     p.out_sh = L.out_sh;
     p.status = &L.hdr->status;
@@ -1121,8 +1034,7 @@ cudaError_t launch_bn(const GemmLaunch& L, int num_sms, int64_t bound, cudaStrea
         const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(units, std::max(1, info.max_clusters)));
         grid = (unsigned)(2 * clusters);
     } else {
-        const int64_t units = bound + (int64_t)(p.ksplit_rt - 1) * p.rt_cap_tiles;
-        grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(units, num_sms));
+        grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(bound, num_sms));
     }
     err = launch_kernel<kFC1, kPair, BN, kShort, kQ>(p, mA, mB, mAs, mBs, mA32, mAs32, grid, s);
     if (err != cudaSuccess) *why = "launch failed";

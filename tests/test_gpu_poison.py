@@ -4,8 +4,7 @@ and initialisation checker, which this GPU pool does not offer).
 Every buffer of a layer that a forward writes before it reads -- routing
 outputs, permutation outputs, x_perm, out, and the workspace body behind its
 header (router partials, permutation scratch, h, h_shared, y, y_shared, the
-split shared FC2's fp32 partials, FC1's split-K partials, the E4M3 rows and
-scales) -- is filled with
+split shared FC2's fp32 partials, the E4M3 rows and scales) -- is filled with
 all-ones bytes (a NaN in bf16 and fp32, -1 in int32) before a forward, and the
 forward must reproduce bitwise what it gives on zero-filled buffers.  A kernel
 that read a row, a partial or a scale nobody wrote would carry the NaN (or a
@@ -26,7 +25,7 @@ _BUFS = ("topk_ids", "topk_w", "slot_ids", "counts", "offsets", "perm_src", "pai
 def _fill(layer, byte):
     for name in _BUFS:
         getattr(layer, name).view(torch.uint8).fill_(byte)
-    layer.ws[moe.MOE_WS_HEADER_BYTES:].fill_(byte)  # the header (status word, counters, tickets) stays
+    layer.ws[256:].fill_(byte)  # the header (status word, counters) stays
 
 
 def _forward(layer, x, byte):
@@ -51,9 +50,6 @@ CASES = {
     # a small batch: the shared FC2 runs split over K into fp32 partials summed by the combine
     "split_shared_fc2": mi.MoEConfig("poison_split", T=40, H=512, I=256, E=8, k=2, renorm=False, n_shared=2,
                                      I_shared=512),
-    # one token: FC1's routed tiles split over K, their partials summed by the last range
-    "split_fc1": mi.MoEConfig("poison_split_fc1", T=1, H=1024, I=256, E=16, k=4, renorm=True, n_shared=1,
-                              I_shared=512),
     # E4M3 weights and activations: quantised rows and scales in the workspace
     "w8a8": mi.MoEConfig("poison_w8a8", T=1000, H=512, I=384, E=12, k=3, renorm=True, n_shared=1,
                          I_shared=256, shared_gate=True, fp8=True, act8=True),

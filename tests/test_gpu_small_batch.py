@@ -158,20 +158,3 @@ def test_small_batch_back_to_back_calls_reuse_the_ticket():
     torch.cuda.synchronize()
     assert torch.equal(layer.topk_ids[:cfg.T], first)
     assert moe.moe_get_device_status(layer.ws) == 0
-
-
-def test_small_batch_split_k_with_an_empty_range():
-    # one token, H = 320 (5 K steps): FC1 splits each routed tile into 4 K ranges of 2
-    # steps, the last of them empty (it issues no MMA and contributes zeros)
-    cfg = mi.MoEConfig("sb_kempty", T=1, H=320, I=128, E=8, k=2, renorm=True, n_shared=1, I_shared=128)
-    _check(mi.make_inputs(cfg))
-    # and the same layer over several calls: the tiles' tickets return to 0 every time
-    inp = mi.make_inputs(cfg)
-    g, _ = _check(inp)
-    layer = g["layer"]
-    x = inp["x"].cuda()
-    first = layer.forward(x).clone()
-    for _ in range(4):
-        again = layer.forward(x)
-    torch.cuda.synchronize()
-    assert torch.equal(first.view(torch.int16), again.view(torch.int16))
