@@ -62,8 +62,6 @@ size_t a256(size_t v) { return (v + 255) & ~(size_t)255; }
 // FC2's length, so its tiles do not outlast the routed ones; the fp32 partials
 // are summed by the combine.
 constexpr int64_t kSplitMaxT = 128;
-// batches of at most this many tokens pull FC2's weights into L2 from FC1
-constexpr int64_t kPrefetchNextMaxT = 64;
 constexpr int kSplitMax = 8;
 
 int shared_split(int64_t T, int I, int I_sh) {
@@ -356,9 +354,7 @@ static moe_status_t gemm_call(bool fc1, const moe_bf16_t* a, int64_t rows_cap, c
                               cudaStream_t s, float* out_sh_part = nullptr, int ksplit_sh = 1,
                               int64_t max_group_rows = -1, const float* b_scale = nullptr,
                               const float* b_scale_sh = nullptr, const float* a_scale = nullptr,
-                              const float* a_scale_sh = nullptr, const void* next_b = nullptr,
-                              int64_t next_b_group_bytes = 0, const void* next_b_sh = nullptr,
-                              int64_t next_b_sh_bytes = 0) {
+                              const float* a_scale_sh = nullptr) {
     GemmLaunch L;
     L.swiglu = fc1;
     L.a = a;
@@ -391,10 +387,6 @@ static moe_status_t gemm_call(bool fc1, const moe_bf16_t* a, int64_t rows_cap, c
     L.b_scale_sh = b_scale_sh;
     L.a_scale = a_scale;
     L.a_scale_sh = a_scale_sh;
-    L.next_b = next_b;
-    L.next_b_group_bytes = next_b_group_bytes;
-    L.next_b_sh = next_b_sh;
-    L.next_b_sh_bytes = next_b_sh_bytes;
     const char* why = nullptr;
     return cuda_status(launch_grouped_gemm(L, device_sms(), s, &why));
 }
@@ -565,14 +557,6 @@ static moe_status_t forward_impl(const moe_bf16_t* x_perm, const int32_t* offset
     cudaStream_t s = (cudaStream_t)stream;
     const int ks = shared_split(T, I, I_shared_total);
     float* y_sh_part = ks > 1 ? reinterpret_cast<float*>(base + FL.y_sh_part) : nullptr;
-    // Small batches stream weights: once an FC1 CTA has issued its last load it pulls
-    // its share of FC2's weights (the slots with rows, then the shared expert's) into
-    // L2, so FC2's stream starts during FC1's tail.
-    const bool pf = T <= kPrefetchNextMaxT;
-    const int64_t wb = fp8 ? 1 : 2;  // bytes per weight
-    const void* nb = pf ? W2 : nullptr;
-    const void* nbs = pf && I_shared_total > 0 ? W2s : nullptr;
-    const int64_t nb_bytes = (int64_t)H * I * wb, nbs_bytes = (int64_t)H * I_shared_total * wb;
     moe_status_t st;
     if (act8) {
         if (!aligned(x_perm, 16) || (I_shared_total > 0 && !aligned(x, 16))) return MOE_ERR_INVALID_ARG;
@@ -604,7 +588,7 @@ static moe_status_t forward_impl(const moe_bf16_t* x_perm, const int32_t* offset
         st = gemm_call(true, reinterpret_cast<const moe_bf16_t*>(u8(FL.xq)), P_cap, offsets, S_local,
                        static_cast<const moe_bf16_t*>(W1), H, I, reinterpret_cast<const moe_bf16_t*>(u8(FL.xsq)), T,
                        static_cast<const moe_bf16_t*>(W1s), I_shared_total, h, h_sh, ws, s, nullptr, 1, T, s1, s1s,
-                       f32(FL.sxq), f32(FL.sxs), nb, nb_bytes, nbs, nbs_bytes);
+                       f32(FL.sxq), f32(FL.sxs));
         if (st != MOE_OK) return st;
         const ActQuantSeg qh[2] = {{h, P_cap, offsets + S_local, I, u8(FL.hq), f32(FL.shq)},
                                    {h_sh, T_sh, nullptr, I_shared_total, u8(FL.hsq), f32(FL.shs)}};
@@ -616,8 +600,7 @@ static moe_status_t forward_impl(const moe_bf16_t* x_perm, const int32_t* offset
                        s2s, f32(FL.shq), f32(FL.shs));
     } else {
         st = gemm_call(true, x_perm, P_cap, offsets, S_local, static_cast<const moe_bf16_t*>(W1), H, I, x, T,
-                       static_cast<const moe_bf16_t*>(W1s), I_shared_total, h, h_sh, ws, s, nullptr, 1, T, s1, s1s,
-                       nullptr, nullptr, nb, nb_bytes, nbs, nbs_bytes);
+                       static_cast<const moe_bf16_t*>(W1s), I_shared_total, h, h_sh, ws, s, nullptr, 1, T, s1, s1s);
         if (st != MOE_OK) return st;
         st = gemm_call(false, h, P_cap, offsets, S_local, static_cast<const moe_bf16_t*>(W2), H, I, h_sh, T,
                        static_cast<const moe_bf16_t*>(W2s), I_shared_total, y, y_sh, ws, s, y_sh_part, ks, T, s2, s2s);

@@ -113,10 +113,6 @@ struct GemmParams {
     int kb_split_sh;         // K steps per range
     int prefetch_sh;         // FC1: pull this CTA's shared-problem weights into L2 before
                              // waiting on the previous kernel (shared problems of <= 64 rows)
-    const uint8_t* next_b;   // FC1 of a small batch: FC2's weights, pulled into L2 once this
-    int64_t next_b_group_bytes;  // CTA has issued its last load (see GemmLaunch)
-    const uint8_t* next_b_sh;
-    int64_t next_b_sh_bytes;
     int32_t* status;
     uint64_t timeout_ns;
 };
@@ -478,26 +474,6 @@ __global__ void __launch_bounds__(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS,
                         phase ^= 1u;
                     }
                 }
-            }
-            if (!failed && (p.next_b || p.next_b_sh) && have && (!kPair || crank == 0)) {
-                // this CTA's share of the next GEMM's weights (the groups with rows, then the
-                // shared ones), pulled into L2 while the tiles still in the ring finish
-                int64_t total = p.next_b_sh ? p.next_b_sh_bytes : 0;
-                if (p.next_b)
-                    for (int g = 0; g < p.G; ++g) total += m.off[g + 1] > m.off[g] ? p.next_b_group_bytes : 0;
-                const int64_t lo = total * unit0 / nunits / 256 * 256;
-                const int64_t hi = unit0 + 1 == nunits ? total : total * (unit0 + 1) / nunits / 256 * 256;
-                int64_t base = 0;
-                auto seg = [&](const uint8_t* ptr, int64_t n) {
-                    const int64_t a = max(lo, base), b = min(hi, base + n);
-                    for (int64_t c = a; c < b; c += 65536)
-                        prefetch_l2_bulk(ptr + (c - base), (uint32_t)min((int64_t)65536, b - c));
-                    base += n;
-                };
-                if (p.next_b)
-                    for (int g = 0; g < p.G && base < hi; ++g)
-                        if (m.off[g + 1] > m.off[g]) seg(p.next_b + g * p.next_b_group_bytes, p.next_b_group_bytes);
-                if (p.next_b_sh && base < hi) seg(p.next_b_sh, p.next_b_sh_bytes);
             }
             if (failed) {
                 m.abort = 1;
@@ -1013,10 +989,6 @@ cudaError_t launch_bn(const GemmLaunch& L, int num_sms, int64_t bound, cudaStrea
     // (measured: one token 6 % off the layer step, 8 and 32 tokens 1-2 %; at 128 tokens the
     // shared stream no longer fits in the window and the prefetch costs about 1 %)
     p.prefetch_sh = (kFC1 && has_shared && L.T_sh <= 64) ? 1 : 0;
-    p.next_b = kFC1 && has_routed ? static_cast<const uint8_t*>(L.next_b) : nullptr;
-    p.next_b_group_bytes = L.next_b_group_bytes;
-    p.next_b_sh = kFC1 && has_shared ? static_cast<const uint8_t*>(L.next_b_sh) : nullptr;
-    p.next_b_sh_bytes = L.next_b_sh_bytes;
     p.out = L.out;
     p.out_sh = L.out_sh;
     p.status = &L.hdr->status;

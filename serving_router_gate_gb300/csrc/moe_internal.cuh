@@ -424,13 +424,6 @@ struct GemmLaunch {
     const float* b_scale_sh;   // [Nb_sh] row scales of b_sh (E4M3 B only)
     const float* a_scale;      // [rows_cap] row scales of a (GEMM_W8A8 only)
     const float* a_scale_sh;   // [T_sh] row scales of a_sh (GEMM_W8A8 only)
-    // FC1 of a small batch: the weights the next GEMM (FC2) will stream, pulled into L2
-    // by each CTA once it has issued its last load (null: none).  Group g's bytes are
-    // next_b + g * next_b_group_bytes, for the groups that have rows; then the shared ones.
-    const void* next_b = nullptr;
-    int64_t next_b_group_bytes = 0;
-    const void* next_b_sh = nullptr;
-    int64_t next_b_sh_bytes = 0;
 };
 enum { GEMM_BF16 = 0, GEMM_W8 = 1, GEMM_W8A8 = 2 };
 cudaError_t launch_grouped_gemm(const GemmLaunch& L, int num_sms, cudaStream_t s, const char** why);

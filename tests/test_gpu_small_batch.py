@@ -2,9 +2,8 @@
 
 Batches of at most 16 tokens route in one launch (logits over many CTAs, the
 selection by the CTA that finishes last), and batches of at most 256 pairs
-permute in one CTA entirely in shared memory; FC1 splits the routed tiles of
-such batches over K (the last K range of a tile sums the partials).  Every
-routing variant those paths serve is compared here in full:
+permute in one CTA entirely in shared memory.  Every routing variant those
+paths serve is compared here in full:
 plain and renormalised top-k, replica slots with a Zipf bias, local ranges
 (SKIP and MOD, summing to the full layer), routing on the input, group-limited
 top-k, 512 experts with k = 32, exact logit ties, E4M3 weights and activations,
