@@ -77,13 +77,17 @@ constexpr int RING_BYTES = 216 * 1024;  // shared memory for the operand ring
 constexpr uint16_t PAIR_MASK = 0x3;
 
 // per instantiation: MMA N = BN (256 for large launches, 128 / 64 to spread
-// small ones over more CTAs); a CTA holds all of B (single) or its half (pair)
-template <bool kPair, int BN, bool kShort = false>
+// small ones over more CTAs); a CTA holds all of B (single) or its half (pair).
+// A stage holds KS consecutive K chunks of 64 bf16 (one 128-byte swizzle row per
+// operand row each): chunk c of A at c * A_CHUNK, of B at c * B_CHUNK.
+template <bool kPair, int BN, bool kShort = false, int KS = 1>
 struct Cfg {
-    static constexpr int B_BYTES = (kPair ? BN / 2 : BN) * BK * 2;
-    // kShort: every tile has at most 32 rows, so an A slot holds 32 rows (the MMA
-    // still reads 128 rows from the slot onward; rows past 32 are never stored)
-    static constexpr int A_SLOT = kShort ? A_SHORT_BYTES : A_BYTES;
+    static constexpr int B_CHUNK = (kPair ? BN / 2 : BN) * BK * 2;
+    static constexpr int B_BYTES = B_CHUNK * KS;
+    // kShort: every tile has at most 32 rows, so an A slot holds 32 rows per chunk (the
+    // MMA still reads 128 rows from the chunk onward; rows past 32 are never stored)
+    static constexpr int A_CHUNK = kShort ? A_SHORT_BYTES : A_BYTES;
+    static constexpr int A_SLOT = A_CHUNK * KS;
     static constexpr int STAGE_BYTES = A_SLOT + B_BYTES;
     static constexpr int STAGES = RING_BYTES / STAGE_BYTES < MAX_STAGES ? RING_BYTES / STAGE_BYTES : MAX_STAGES;
     static constexpr int TMEM_COLS = 2 * BN;  // two accumulators of BN fp32 columns
@@ -133,9 +137,17 @@ struct SmemMeta {
     int ts[MAX_GROUPS + 1];
 };
 
-template <bool kPair, int BN, bool kShort>
+// K chunks per stage: two for short-tile (small-batch) bf16 launches, whose CTAs
+// stream weights at a pace set by the number of pipeline stages they issue, not by
+// the bytes; one otherwise
+template <bool kShort, int kQ>
+constexpr int chunks_per_stage() {
+    return (kShort && kQ == 0) ? 2 : 1;
+}
+
+template <bool kPair, int BN, bool kShort, int KS>
 constexpr size_t smem_bytes() {
-    return 1024 /*alignment slack*/ + (size_t)Cfg<kPair, BN, kShort>::STAGES * Cfg<kPair, BN, kShort>::STAGE_BYTES +
+    return 1024 /*alignment slack*/ + (size_t)Cfg<kPair, BN, kShort, KS>::STAGES * Cfg<kPair, BN, kShort, KS>::STAGE_BYTES +
            sizeof(SmemMeta);
 }
 
@@ -238,7 +250,8 @@ __global__ void __launch_bounds__(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS,
                         const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmAs,
                         const __grid_constant__ CUtensorMap tmBs, const __grid_constant__ CUtensorMap tmA32,
                         const __grid_constant__ CUtensorMap tmAs32) {
-    using C = Cfg<kPair, BN, kShort>;
+    constexpr int KSC = chunks_per_stage<kShort, kQ>();
+    using C = Cfg<kPair, BN, kShort, KSC>;
     constexpr int STAGES = C::STAGES;
     constexpr int B_BYTES = C::B_BYTES;
     constexpr int A_SLOT = C::A_SLOT;
@@ -432,7 +445,7 @@ __global__ void __launch_bounds__(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS,
                     const Tile other = tile_of<kFC1, kPair>(u, p, m, n_sh_tiles, mu_sh, crank ^ 1);
                     pair_bytes = a_bytes + (other.rows_valid <= BM_SHORT ? A_SHORT_BYTES : A_BYTES) + 2 * B_BYTES;
                 }
-                for (int kb = tl.kb0; kb < tl.kb1; ++kb) {
+                for (int kb = tl.kb0; kb < tl.kb1; kb += KSC) {
                     if (!mbar_wait(&m.empty[stage], phase ^ 1u, p.timeout_ns, abortp)) {
                         failed = true;
                         break;
@@ -458,15 +471,22 @@ __global__ void __launch_bounds__(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS,
                         } else {
                             tma_load_3d(b_dst, mB, &m.full[stage], kb * KE, tl.nt * BN, tl.g);
                         }
-                    } else if (kFC1) {
-                        mbar_arrive_expect_tx(&m.full[stage], a_bytes + B_BYTES);
-                        tma_load_2d(a_dst, mA, &m.full[stage], kb * KE, tl.row0);
-                        tma_load_3d(b_dst, mB, &m.full[stage], kb * KE, tl.nt * (BN / 2), tl.g);
-                        tma_load_3d(b_dst + B_BYTES / 2, mB, &m.full[stage], kb * KE, up + tl.nt * (BN / 2), tl.g);
                     } else {
-                        mbar_arrive_expect_tx(&m.full[stage], a_bytes + B_BYTES);
-                        tma_load_2d(a_dst, mA, &m.full[stage], kb * KE, tl.row0);
-                        tma_load_3d(b_dst, mB, &m.full[stage], kb * KE, tl.nt * BN, tl.g);
+                        // KSC chunks: a chunk past the range's end lies past K (ranges of
+                        // split tiles are multiples of KSC), where the TMA fills zeros
+                        mbar_arrive_expect_tx(&m.full[stage], KSC * (a_bytes + C::B_CHUNK));
+#pragma unroll
+                        for (int c = 0; c < KSC; ++c) {
+                            const int kc = (kb + c) * KE;
+                            tma_load_2d(a_dst + c * C::A_CHUNK, mA, &m.full[stage], kc, tl.row0);
+                            uint8_t* bc = b_dst + c * C::B_CHUNK;
+                            if (kFC1) {
+                                tma_load_3d(bc, mB, &m.full[stage], kc, tl.nt * (BN / 2), tl.g);
+                                tma_load_3d(bc + C::B_CHUNK / 2, mB, &m.full[stage], kc, up + tl.nt * (BN / 2), tl.g);
+                            } else {
+                                tma_load_3d(bc, mB, &m.full[stage], kc, tl.nt * BN, tl.g);
+                            }
+                        }
                     }
                     ++issued;
                     if (++stage == STAGES) {
@@ -509,7 +529,7 @@ __global__ void __launch_bounds__(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS,
                 }
                 if (u < 0) break;
                 const Tile tl = tile_of<kFC1, kPair>(u, p, m, n_sh_tiles, mu_sh, crank);
-                const int nkb = tl.kb1 - tl.kb0;
+                const int nkb = (tl.kb1 - tl.kb0 + KSC - 1) / KSC;  // stages of this tile
                 const int buf = i & 1;
                 if (!mbar_wait(&m.tempty[buf], (uint32_t)(((i >> 1) & 1) ^ 1), p.timeout_ns, abortp)) {
                     failed = true;
@@ -526,17 +546,20 @@ __global__ void __launch_bounds__(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS,
                     const uint32_t a0 = smem_u32(smA + (size_t)stage * A_SLOT);
                     const uint32_t b0 = smem_u32(smB + (size_t)stage * B_BYTES);
 #pragma unroll
-                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                        // 32 bytes of each 128-byte row per MMA: K = 16 bf16 or 32 E4M3
-                        const uint64_t ad = sw128_kmajor_desc(a0 + kk * UMMA_K * 2);
-                        const uint64_t bd = sw128_kmajor_desc(b0 + kk * UMMA_K * 2);
-                        if (kPair)
-                            tc_mma_bf16_pair(d, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
-                        else if (kA8)
-                            tc_mma_e4m3(d, ad, bd, C::IDESC8, (kb | kk) != 0 ? 1u : 0u);
-                        else
-                            tc_mma_bf16(d, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
-                    }
+                    for (int c = 0; c < KSC; ++c)
+#pragma unroll
+                        for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                            // 32 bytes of each 128-byte row per MMA: K = 16 bf16 or 32 E4M3
+                            const uint64_t ad = sw128_kmajor_desc(a0 + c * C::A_CHUNK + kk * UMMA_K * 2);
+                            const uint64_t bd = sw128_kmajor_desc(b0 + c * C::B_CHUNK + kk * UMMA_K * 2);
+                            const uint32_t acc = (kb | c | kk) != 0 ? 1u : 0u;
+                            if (kPair)
+                                tc_mma_bf16_pair(d, ad, bd, IDESC, acc);
+                            else if (kA8)
+                                tc_mma_e4m3(d, ad, bd, C::IDESC8, acc);
+                            else
+                                tc_mma_bf16(d, ad, bd, IDESC, acc);
+                        }
                     if (kPair)
                         tc_commit_pair_multicast(&m.empty[stage], PAIR_MASK);
                     else
@@ -868,14 +891,14 @@ cudaError_t kernel_info(int num_sms, KernelInfo* out) {
     std::lock_guard<std::mutex> lock(mu);
     if (!info[dev].ready) {
         err = cudaFuncSetAttribute(grouped_gemm_kernel<kFC1, kPair, BN, kShort, kQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)smem_bytes<kPair, BN, kShort>());
+                                   (int)smem_bytes<kPair, BN, kShort, chunks_per_stage<kShort, kQ>()>());
         if (err != cudaSuccess) return err;
         int clusters = 0;
         if (kPair) {
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(2 * num_sms);
             cfg.blockDim = dim3(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS);
-            cfg.dynamicSmemBytes = smem_bytes<kPair, BN, kShort>();
+            cfg.dynamicSmemBytes = smem_bytes<kPair, BN, kShort, chunks_per_stage<kShort, kQ>()>();
             cudaLaunchAttribute attr;
             attr.id = cudaLaunchAttributeClusterDimension;
             attr.val.clusterDim.x = 2;
@@ -900,7 +923,7 @@ cudaError_t launch_kernel(const GemmParams& p, const CUtensorMap& mA, const CUte
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS);
-    cfg.dynamicSmemBytes = smem_bytes<kPair, BN, kShort>();
+    cfg.dynamicSmemBytes = smem_bytes<kPair, BN, kShort, chunks_per_stage<kShort, kQ>()>();
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     int n = 0;
@@ -985,7 +1008,10 @@ cudaError_t launch_bn(const GemmLaunch& L, int num_sms, int64_t bound, cudaStrea
     p.Nb = L.Nb;
     p.out_sh_part = L.out_sh_part;
     p.ksplit_sh = (has_shared && !L.swiglu && L.out_sh_part && L.ksplit_sh > 1) ? L.ksplit_sh : 1;
+    // ranges of a split shared tile hold whole stages (KSC chunks each)
+    constexpr int KSC = chunks_per_stage<kShort, kQ>();
     p.kb_split_sh = (p.kb_total_sh + p.ksplit_sh - 1) / p.ksplit_sh;
+    p.kb_split_sh = (p.kb_split_sh + KSC - 1) / KSC * KSC;
     // (measured: one token 6 % off the layer step, 8 and 32 tokens 1-2 %; at 128 tokens the
     // shared stream no longer fits in the window and the prefetch costs about 1 %)
     p.prefetch_sh = (kFC1 && has_shared && L.T_sh <= 64) ? 1 : 0;
