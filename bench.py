@@ -181,6 +181,16 @@ class L2Flush:
         return f"write {self.nbytes >> 20} MiB, then read another {self.nbytes >> 20} MiB"
 
 
+def _external_events():
+    """Two timing events that can be recorded as nodes of a captured CUDA graph (None
+    where this PyTorch cannot make them)."""
+    try:
+        return (torch.cuda.Event(enable_timing=True, external=True),
+                torch.cuda.Event(enable_timing=True, external=True))
+    except TypeError:
+        return None
+
+
 def time_steps(fns, K, flush, stream):
     """K steps; each step flushes L2, then runs fns in order with a CUDA event on
     `stream` before and after each.  Returns per-fn lists of K times in ms."""
@@ -392,32 +402,57 @@ def bench_ours(args):
     flush = L2Flush(dev)
 
     # ---- timed pass: the whole layer, K steps (replayed from a CUDA graph of one step) ----
-    graph = layer.capture(x) if args.graph else None
+    # The graph holds two external event nodes, one before the forward's first kernel
+    # and one after its last: their interval is the forward's device time.  Events
+    # recorded on the stream around each replay also time the graph's own launch, a
+    # cost a model-level graph pays once per model step rather than once per layer;
+    # both are reported.
+    inner = _external_events() if args.graph else None
+    if args.graph:
+        pre = (lambda: inner[0].record()) if inner else None
+        post = (lambda: inner[1].record()) if inner else None
+        graph = layer.capture(x, pre=pre, post=post)
+    else:
+        graph = None
     step = graph.replay if graph is not None else (lambda: layer.forward(x))
     for _ in range(W):
         step()
+
     def timed_region():
         clocks = ClockSampler(torch.cuda.current_device())
         _barrier(ws_)
         torch.cuda.synchronize()
         clocks.start()
-        t = statistics.mean(time_steps([step], K, flush, stream)[0])
+        outer, inside = [], []
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for _ in range(K):
+            flush()
+            e0.record(stream)
+            step()
+            e1.record(stream)
+            torch.cuda.synchronize()  # the in-graph events are re-recorded by the next replay
+            outer.append(e0.elapsed_time(e1))
+            if inner:
+                inside.append(inner[0].elapsed_time(inner[1]))
         torch.cuda.synchronize()
         rec = clocks.stop()
         _barrier(ws_)
-        return t, rec
+        t_out = statistics.mean(outer)
+        t_in = statistics.mean(inside) if inside else t_out
+        return (t_in, t_out), rec
 
-    ms_local, clk = timed_region()
+    (ms_local, ms_replay_local), clk = timed_region()
     # a region that saw a hardware or thermal slowdown is measured once more (power
     # capping is kept: it is the part's normal state under a dense load); decided over
     # all ranks, so that every rank measures the same number of regions
     bad = bool(clk and set(clk["reasons"]) & {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"})
     if max_over_ranks(float(bad), ws_) > 0:
         first = clk
-        ms_local, clk = timed_region()
+        (ms_local, ms_replay_local), clk = timed_region()
         if clk is not None:
             clk["remeasured_after"] = first
     value, ms = aggregate_throughput(T, ms_local, ws_)
+    ms_replay = max_over_ranks(ms_replay_local, ws_)
 
     # ---- per-kernel pass: the same forward, every kernel between its own events ----
     labels, per_kernel = kernel_breakdown(layer, x, kernels_per_step, K, W, flush, stream)
@@ -490,6 +525,11 @@ def bench_ours(args):
     res = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws_, "steps": K,
         "warmup": W, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "step_timing": ("device time of one forward: CUDA events recorded by external event nodes at the "
+                        "head and tail of the forward's graph, mean of the K steps" if inner else
+                        "CUDA events on the stream around each step"),
+        "ms_per_step_with_graph_launch": ms_replay,
+        "value_with_graph_launch": T * ws_ / (ms_replay * 1e-3),
         "dtype": "e4m3" if cfg.act8 else "bf16", "data": "synthetic: seeded N(0,1) activations, N(0,sigma) random-init weights of the "
                                  "workload's shapes (no checkpoint)",
         "config": {"workload": cfg.name, "shape": mi.describe(cfg), "tokens_per_gpu": T,
