@@ -87,6 +87,10 @@ CONFIGS = {
 # device) on which the FC1 DRAM traffic of the full workload is captured and scaled per slot
 CONFIGS["redundant_slots_cut16"] = MoEConfig("redundant_slots_cut16", T=1024, H=7168, I=2048, E=16, k=8,
                                              renorm=True, w_std=0.01)
+# the router of the large-expert and redundant-slot layers (H = 7168, E = 256, Zipf bias) on
+# 8192 tokens with small experts: about 2 GB on the device, for router captures
+CONFIGS["router_h7168_e256_cut"] = MoEConfig("router_h7168_e256_cut", T=8192, H=7168, I=64, E=256, k=8,
+                                             renorm=True, zipf_s=1.1, w_std=0.01)
 # the router variants of the next steps, on the Qwen2-like and DeepSeek-V2-Lite-like shapes:
 # group-limited top-k (DeepSeek-V2-style: 8 groups, 3 kept, k = 6 of 64 experts) and the
 # routing weight applied on the expert input

@@ -322,9 +322,7 @@ __global__ void __launch_bounds__(PM_SCAN_THREADS) permute_small_kernel(
 // The token rows are staged in shared memory while warp 0 maps, masks and ranks
 // the pairs (as rank_chunk does, ranks kept in shared memory); the block then
 // scans the counts, places every pair and writes the rows of x_perm from the
-// staged copy.  The kernel lets the next one on the stream launch as soon as it
-// starts: the grouped GEMM that follows prefetches weights (which no kernel
-// writes) before it waits for this one to finish.
+// staged copy.
 constexpr int PT_THREADS = 512;
 constexpr int PT_WARPS = PT_THREADS / 32;
 constexpr int64_t PT_MAX_X_BYTES = 96 * 1024;
@@ -346,8 +344,8 @@ __global__ void __launch_bounds__(PT_THREADS) permute_tiny_kernel(
     float* s_w = reinterpret_cast<float*>(s_row + P);                         // [P]
     __shared__ int32_t s_wsum[PT_WARPS];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    pdl_trigger();
     pdl_wait();
+    pdl_trigger();
 
     const int vec = H / 8;
     for (int i = tid; i < T * vec; i += PT_THREADS) cp_async16(xs + (size_t)i * 8, x + (size_t)i * 8);

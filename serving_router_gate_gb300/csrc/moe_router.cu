@@ -10,12 +10,12 @@
 //
 // Two kernels:
 //  1. router_logits_kernel: partial logits l[t,e] over a K range per CTA.
-//     Tile 64 tokens x 64 experts x K-range; each thread owns 4x4 outputs,
-//     read as float4 along k from padded k-contiguous shared-memory rows.
-//     Accumulation is nested (even/odd-k chains of 16 terms per 32-k chunk ->
-//     groups of 8 chunks -> the CTA's range), which keeps the worst-case
-//     rounding error of every logit below gamma_n * (||x_t|| ||w_e|| + |b_e|)
-//     with a small n (about 60 for H = 7168) instead of n = H.  The CTAs of the first token/expert tile
+//     Tile 128 tokens x 64 experts x K-range; each thread owns 8x4 outputs,
+//     read from k-major shared-memory tiles.  Accumulation is nested (32-term
+//     chains per 32-k chunk -> groups of 8 chunks -> the CTA's range), which
+//     keeps the worst-case rounding error of every logit below
+//     gamma_n * (||x_t|| ||w_e|| + |b_e|) with a small n (about 70 for
+//     H = 7168) instead of n = H.  The CTAs of the first token/expert tile
 //     also emit the partial squared norms of x rows and Wg rows.
 //  2. router_select_kernel: one warp per token.  Sums the split partials in
 //     fixed order, adds the bias, and takes the k+1 largest logits (ties ->
@@ -39,7 +39,7 @@
 namespace moe {
 namespace {
 
-constexpr int RT_BT = 64;        // tokens per CTA
+constexpr int RT_BT = 128;       // tokens per CTA
 constexpr int RT_BE = 64;        // experts per CTA
 constexpr int RT_BK = 32;        // K per shared-memory chunk (level-1 sum length)
 constexpr int RT_GROUP = 8;      // chunks per level-2 group
@@ -61,20 +61,25 @@ __device__ __forceinline__ void cp_async_wait_group() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// Tile: 64 tokens x 64 experts x a K range per CTA, 256 threads, 4x4 outputs
-// per thread.  Shared memory holds k-contiguous rows padded to 36 floats, so
-// the float4 reads along k are bank-conflict-free.  Wg chunks arrive through a
-// 4-stage cp.async ring; x chunks are loaded two chunks ahead into registers,
-// converted to fp32 and stored into a double-buffered tile.  Thread (tg, eg)
-// owns tokens tg + 16 i and experts eg + 16 j (i, j < 4).  Each logit's sum:
-// per 32-k chunk (one stage), two interleaved chains -- even k and odd k, each
-// in ascending k, advanced together by packed fp32 FMAs -- then their sum;
-// chunks summed in groups of 8, groups summed over the CTA's range.
-constexpr int RT_LD = RT_BK + 4;  // padded row length (floats)
-constexpr int RT_WSTAGES = 4;
-constexpr size_t RT_SMEM = sizeof(float) * RT_LD * (RT_WSTAGES * RT_BE + 2 * RT_BT);
+// Tile: 128 tokens x 64 experts x a K range per CTA, 256 threads, 8 x 4 outputs
+// per thread (tokens 4 tg .. 4 tg + 3 and 64 + 4 tg .. + 3, experts 4 eg .. 4 eg + 3).
+// Both operands sit k-major in shared memory (xs[k][token], ws[k][expert], fp32),
+// so per k a thread reads its 8 token values and 4 expert values with three 16-byte
+// loads -- two of them broadcast to half a warp, one spread over 16 lanes -- and
+// issues 32 FMAs.  Chunks of 32 k are staged through registers loaded two chunks
+// ahead: a lane reads 8 consecutive k of one token row (bf16) or 4 of one Wg row,
+// the 32 lanes of a warp consecutive rows, and stores them transposed, conflict-free,
+// into the buffer the next chunk reads (two buffers, one barrier per chunk).  Each
+// logit's sum: per 32-k chunk one chain in ascending k, chunks summed in groups of 8,
+// groups summed over the CTA's range -- a rounding depth of 32 + 8 + groups per range.
+// The expert tiles of one token tile are adjacent CTAs, so they share the token rows
+// through L2.  CTAs of expert tile 0 also emit the partial squared norms of their
+// token rows, CTAs of token tile 0 those of their Wg rows.
+constexpr int RT_XW = RT_BT;  // xs row (floats)
+constexpr int RT_WW = RT_BE;  // ws row (floats)
+constexpr size_t RT_SMEM = sizeof(float) * 2 * RT_BK * (RT_XW + RT_WW);
 
-__global__ void __launch_bounds__(RT_THREADS, 2) router_logits_kernel(const uint16_t* __restrict__ x,
+__global__ void __launch_bounds__(RT_THREADS, 1) router_logits_kernel(const uint16_t* __restrict__ x,
                                                                       const float* __restrict__ Wg, int64_t T,
                                                                       int H, int E, int KC,
                                                                       float* __restrict__ part,
@@ -83,149 +88,152 @@ __global__ void __launch_bounds__(RT_THREADS, 2) router_logits_kernel(const uint
     extern __shared__ __align__(16) float rt_smem[];
     pdl_wait();
     pdl_trigger();
-    float (*wsm)[RT_BE][RT_LD] = reinterpret_cast<float (*)[RT_BE][RT_LD]>(rt_smem);
-    float (*xs)[RT_BT][RT_LD] = reinterpret_cast<float (*)[RT_BT][RT_LD]>(rt_smem + RT_WSTAGES * RT_BE * RT_LD);
+    float (*xs)[RT_BK][RT_XW] = reinterpret_cast<float (*)[RT_BK][RT_XW]>(rt_smem);
+    float (*ws)[RT_BK][RT_WW] = reinterpret_cast<float (*)[RT_BK][RT_WW]>(rt_smem + 2 * RT_BK * RT_XW);
 
     const int tid = threadIdx.x;
-    const int64_t t0 = (int64_t)blockIdx.x * RT_BT;
-    const int e0 = blockIdx.y * RT_BE;
+    const int e0 = blockIdx.x * RT_BE;               // expert tiles vary fastest
+    const int64_t t0 = (int64_t)blockIdx.y * RT_BT;
     const int sp = blockIdx.z;
     const int kbeg = sp * KC;
     const int kend = min(H, kbeg + KC);
     const int nchunk = (kend - kbeg) / RT_BK;
 
-    // x loader: row tid/4 of the tile, 8 consecutive k at (tid%4)*8
-    const int xr = tid >> 2, xk = (tid & 3) * 8;
-    const bool xvalid = t0 + xr < T;
-    const uint16_t* xsrc = x + (xvalid ? t0 + xr : 0) * (int64_t)H + kbeg + xk;
-    // Wg loader: 64 rows x 32 floats = 512 16-byte pieces, two per thread
-    const int wr0 = tid >> 3, wk0 = (tid & 7) * 4;
-    const int wr1 = wr0 + 32;
-    const bool wv0 = e0 + wr0 < E, wv1 = e0 + wr1 < E;
-    const float* wsrc0 = Wg + (int64_t)(wv0 ? e0 + wr0 : 0) * H + kbeg + wk0;
-    const float* wsrc1 = Wg + (int64_t)(wv1 ? e0 + wr1 : 0) * H + kbeg + wk0;
+    // staging: x vector j of this thread is token xt, k offset xk[j] (8 bf16);
+    // Wg vector j is expert we, k offset wk[j] (4 fp32)
+    const int xt = tid & (RT_BT - 1);
+    const int xk0 = (tid >> 7) * 8;                  // 0 or 8; vector 1 adds 16
+    const bool xv = t0 + xt < T;
+    const uint16_t* xsrc = x + (xv ? t0 + xt : 0) * (int64_t)H + kbeg + xk0;
+    const int we = tid & (RT_BE - 1);
+    const int wk0 = (tid >> 6) * 4;                  // 0, 4, 8, 12; vector 1 adds 16
+    const bool wvl = e0 + we < E;
+    const float* wsrc = Wg + (int64_t)(wvl ? e0 + we : 0) * H + kbeg + wk0;
 
-    auto issue_w = [&](int c) {  // always commits a group (empty past the end) so counts stay uniform
+    struct Stage {
+        uint4 xa, xb;
+        float4 wa, wb;
+    };
+    auto load = [&](int c, Stage& st) {
         if (c < nchunk) {
-            const int st = c % RT_WSTAGES;
-            cp_async16(&wsm[st][wr0][wk0], wsrc0 + c * RT_BK, wv0);
-            cp_async16(&wsm[st][wr1][wk0], wsrc1 + c * RT_BK, wv1);
+            const int ko = c * RT_BK;
+            st.xa = xv ? __ldg(reinterpret_cast<const uint4*>(xsrc + ko)) : make_uint4(0, 0, 0, 0);
+            st.xb = xv ? __ldg(reinterpret_cast<const uint4*>(xsrc + ko + 16)) : make_uint4(0, 0, 0, 0);
+            st.wa = wvl ? __ldg(reinterpret_cast<const float4*>(wsrc + ko)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            st.wb = wvl ? __ldg(reinterpret_cast<const float4*>(wsrc + ko + 16)) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        cp_async_commit();
     };
-    auto load_x = [&](int c) -> uint4 {
-        return (xvalid && c < nchunk) ? __ldg(reinterpret_cast<const uint4*>(xsrc + c * RT_BK))
-                                      : make_uint4(0, 0, 0, 0);
-    };
-    auto store_x = [&](int buf, const uint4& v) {
+    float nx = 0.f, nw = 0.f;  // partial squared norms of row xt / we (this thread's k)
+    auto store = [&](int buf, const Stage& st) {
         float f[8];
-        unpack8(v, f);
-        *reinterpret_cast<float4*>(&xs[buf][xr][xk]) = make_float4(f[0], f[1], f[2], f[3]);
-        *reinterpret_cast<float4*>(&xs[buf][xr][xk + 4]) = make_float4(f[4], f[5], f[6], f[7]);
+        unpack8(st.xa, f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            xs[buf][xk0 + i][xt] = f[i];
+            nx = fmaf(f[i], f[i], nx);
+        }
+        unpack8(st.xb, f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            xs[buf][xk0 + 16 + i][xt] = f[i];
+            nx = fmaf(f[i], f[i], nx);
+        }
+        const float w8[8] = {st.wa.x, st.wa.y, st.wa.z, st.wa.w, st.wb.x, st.wb.y, st.wb.z, st.wb.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            ws[buf][wk0 + i][we] = w8[i];
+            ws[buf][wk0 + 16 + i][we] = w8[4 + i];
+            nw = fmaf(w8[i], w8[i], nw);
+            nw = fmaf(w8[4 + i], w8[4 + i], nw);
+        }
     };
 
-    // warp w covers token groups 4*(w/2) .. +3 and expert groups 8*(w%2) .. +7:
-    // per load instruction 4 distinct x rows and 8 distinct Wg rows (one
-    // shared-memory wavefront each)
-    const int wid = tid >> 5, ln = tid & 31;
-    const int tg = (wid >> 1) * 4 + (ln >> 3);
-    const int eg = (wid & 1) * 8 + (ln & 7);
-    const bool do_xn = (blockIdx.y == 0) && (tid < RT_BT);
-    const bool do_wn = (blockIdx.x == 0) && (tid >= 64) && (tid < 64 + RT_BE);
-    // level 1: one packed pair per output -- (sum over even k, sum over odd k)
-    // of the chunk, advanced by __ffma2_rn (two independent round-to-nearest
-    // fmas); levels 2 and 3: fp32
-    float2 a1[4][4];
-    float a2[4][4], a3[4][4];
+    // compute layout: warp w, lane: expert group eg = lane & 15, token group tg = 2 w + lane / 16
+    const int lane = tid & 31, wid = tid >> 5;
+    const int eg = lane & 15;
+    const int tg = 2 * wid + (lane >> 4);
+    float a1[8][4], a2[8][4], a3[8][4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            a1[i][j] = make_float2(0.f, 0.f);
-            a2[i][j] = a3[i][j] = 0.f;
-        }
-    float nsq = 0.f;
+        for (int j = 0; j < 4; ++j) a2[i][j] = a3[i][j] = 0.f;
 
-    // prologue: Wg chunks 0..2 in flight, x chunk 0 in shared memory, x chunks 1, 2 in registers
-    for (int c = 0; c < RT_WSTAGES - 1; ++c) issue_w(c);
-    store_x(0, load_x(0));
-    uint4 xn1 = load_x(1), xn2 = load_x(2);
-    cp_async_wait_group<RT_WSTAGES - 2>();
-    __syncthreads();
-
-    for (int c = 0; c < nchunk; ++c) {
+    // chunk c: computed from buffer c & 1; the registers of chunk c + 1 (loaded one
+    // chunk earlier) go to the other buffer after it; chunk c + 2 is loaded into the
+    // registers chunk c came from
+    auto step = [&](int c, Stage& nxt, Stage& far) {
         const int buf = c & 1;
-        const int st = c % RT_WSTAGES;
-        issue_w(c + RT_WSTAGES - 1);
-        const uint4 xn3 = load_x(c + 3);
-#pragma unroll 2
-        for (int kk = 0; kk < RT_BK; kk += 4) {
-            float4 xa[4], wb[4];
+        load(c + 2, far);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) xa[i] = *reinterpret_cast<const float4*>(&xs[buf][tg + 16 * i][kk]);
+        for (int i = 0; i < 8; ++i)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) wb[j] = *reinterpret_cast<const float4*>(&wsm[st][eg + 16 * j][kk]);
+            for (int j = 0; j < 4; ++j) a1[i][j] = 0.f;
+#pragma unroll 4
+        for (int k = 0; k < RT_BK; ++k) {
+            const float4 xlo = *reinterpret_cast<const float4*>(&xs[buf][k][4 * tg]);
+            const float4 xhi = *reinterpret_cast<const float4*>(&xs[buf][k][64 + 4 * tg]);
+            const float4 wv = *reinterpret_cast<const float4*>(&ws[buf][k][4 * eg]);
+            const float xv8[8] = {xlo.x, xlo.y, xlo.z, xlo.w, xhi.x, xhi.y, xhi.z, xhi.w};
+            const float wv4[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+            for (int i = 0; i < 8; ++i)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    a1[i][j] = __ffma2_rn(make_float2(xa[i].x, xa[i].y), make_float2(wb[j].x, wb[j].y), a1[i][j]);
-                    a1[i][j] = __ffma2_rn(make_float2(xa[i].z, xa[i].w), make_float2(wb[j].z, wb[j].w), a1[i][j]);
-                }
-        }
-        if (do_xn) {
-#pragma unroll 8
-            for (int kk = 0; kk < RT_BK; ++kk) {
-                const float v = xs[buf][tid][kk];
-                nsq = fmaf(v, v, nsq);
-            }
-        } else if (do_wn) {
-#pragma unroll 8
-            for (int kk = 0; kk < RT_BK; ++kk) {
-                const float v = wsm[st][tid - 64][kk];
-                nsq = fmaf(v, v, nsq);
-            }
+                for (int j = 0; j < 4; ++j) a1[i][j] = fmaf(xv8[i], wv4[j], a1[i][j]);
         }
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < 8; ++i)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                a2[i][j] += a1[i][j].x + a1[i][j].y;
-                a1[i][j] = make_float2(0.f, 0.f);
-            }
+            for (int j = 0; j < 4; ++j) a2[i][j] += a1[i][j];
         if ((c % RT_GROUP) == RT_GROUP - 1) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+            for (int i = 0; i < 8; ++i)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     a3[i][j] += a2[i][j];
                     a2[i][j] = 0.f;
                 }
         }
-        store_x(buf ^ 1, xn1);
-        xn1 = xn2;
-        xn2 = xn3;
-        cp_async_wait_group<RT_WSTAGES - 2>();  // Wg chunk c+1 has landed
+        if (c + 1 < nchunk) store(buf ^ 1, nxt);
         __syncthreads();
+    };
+    Stage s0, s1;
+    load(0, s0);
+    load(1, s1);
+    if (nchunk > 0) store(0, s0);
+    __syncthreads();
+    for (int c = 0; c < nchunk; c += 2) {
+        step(c, s1, s0);
+        if (c + 1 < nchunk) step(c + 1, s0, s1);
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 8; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) a3[i][j] += a2[i][j];
 
+    const int ebase = e0 + 4 * eg;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int64_t t = t0 + tg + 16 * i;
+    for (int i = 0; i < 8; ++i) {
+        const int64_t t = t0 + (i < 4 ? 4 * tg + i : 64 + 4 * tg + (i - 4));
         if (t >= T) continue;
-        float* dst = part + ((int64_t)sp * T + t) * E;
+        float* dst = part + ((int64_t)sp * T + t) * E + ebase;
+        if (ebase + 3 < E && (E & 3) == 0) {
+            *reinterpret_cast<float4*>(dst) = make_float4(a3[i][0], a3[i][1], a3[i][2], a3[i][3]);
+        } else {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int e = e0 + eg + 16 * j;
-            if (e < E) dst[e] = a3[i][j];
+            for (int j = 0; j < 4; ++j)
+                if (ebase + j < E) dst[j] = a3[i][j];
         }
     }
-    if (do_xn && t0 + tid < T) xsq[(int64_t)sp * T + t0 + tid] = nsq;
-    if (do_wn && e0 + (tid - 64) < E) wsq[(int64_t)sp * E + e0 + (tid - 64)] = nsq;
+    // squared norms: two threads hold parts of each token row, four of each Wg row
+    float* red = rt_smem;  // the buffers are no longer read
+    red[tid] = nx;
+    red[RT_THREADS + tid] = nw;
+    __syncthreads();
+    if (blockIdx.x == 0 && tid < RT_BT && t0 + tid < T)
+        xsq[(int64_t)sp * T + t0 + tid] = red[tid] + red[tid + RT_BT];
+    if (blockIdx.y == 0 && tid < RT_BE && e0 + tid < E)
+        wsq[(int64_t)sp * E + e0 + tid] = (red[RT_THREADS + tid] + red[RT_THREADS + tid + 64]) +
+                                          (red[RT_THREADS + tid + 128] + red[RT_THREADS + tid + 192]);
 }
 
 // Compensated (doubled-precision) dot product of one bf16 x row with one fp32
@@ -884,14 +892,14 @@ __global__ void __launch_bounds__(RSM_THREADS, 1) router_small_kernel(
 
 }  // namespace
 
-// Split of H into K ranges: the CTAs run in waves of (resident CTAs per SM x
-// SMs), so pick the range length that minimises waves x (range + a fixed
-// per-CTA overhead of about three chunks).
+// Split of H into K ranges: the CTAs run in waves of one CTA per SM, so pick the
+// range length that minimises waves x (range + a fixed per-CTA overhead of about
+// three chunks).
 void router_plan(int64_t T, int H, int E, int num_sms, int* nsplit, int* KC) {
     const int64_t tT = (T + RT_BT - 1) / RT_BT;
     const int64_t tE = (E + RT_BE - 1) / RT_BE;
     const int64_t base = tT * tE;
-    const int64_t slots = std::max<int64_t>(1, std::min<int64_t>(2 * (int64_t)num_sms, RT_TARGET_MAX));
+    const int64_t slots = std::max<int64_t>(1, std::min<int64_t>((int64_t)num_sms, RT_TARGET_MAX));
     int best_kc = H, best_ns = 1;
     int64_t best_cost = INT64_MAX;
     for (int kc = RT_BK; kc <= H; kc += RT_BK) {
@@ -914,7 +922,7 @@ void router_plan(int64_t T, int H, int E, int num_sms, int* nsplit, int* KC) {
 static size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 // Scratch of the router for up to T tokens, for any split plan router_plan can
-// choose: nsplit * ceil(T/64) * ceil(E/64) < RT_TARGET_MAX + ceil(T/64) * ceil(E/64).
+// choose: nsplit * ceil(T/128) * ceil(E/64) < RT_TARGET_MAX + ceil(T/128) * ceil(E/64).
 static void router_sizes(int64_t T, int E, size_t* part, size_t* xs, size_t* ws) {
     const int64_t tT = (T + RT_BT - 1) / RT_BT;
     const int64_t tE = (E + RT_BE - 1) / RT_BE;
@@ -1003,7 +1011,7 @@ cudaError_t launch_router(const RouterLaunch& L, int num_sms, cudaStream_t s) {
 
     const int64_t tT = (L.T + RT_BT - 1) / RT_BT;
     const int tE = (L.E + RT_BE - 1) / RT_BE;
-    dim3 grid1((unsigned)tT, (unsigned)tE, (unsigned)L.nsplit);
+    dim3 grid1((unsigned)tE, (unsigned)tT, (unsigned)L.nsplit);
     cudaError_t err = cudaFuncSetAttribute(router_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)RT_SMEM);
     if (err != cudaSuccess) return err;
@@ -1014,9 +1022,9 @@ cudaError_t launch_router(const RouterLaunch& L, int num_sms, cudaStream_t s) {
     // worst-case rounding depth of one logit: 32-term chunk, 8-chunk group,
     // groups in the CTA range, split partials, bias
     const int groups = (L.KC + RT_BK * RT_GROUP - 1) / (RT_BK * RT_GROUP);
-    // rounding depth: the even/odd 16-term chains of a chunk, their sum, 8 chunks
-    // of a group, the groups of the range, the split partials, the bias
-    const int chain_n = RT_BK / 2 + 1 + RT_GROUP + groups + L.nsplit + 1;
+    // rounding depth: the 32-term chain of a chunk, 8 chunks of a group, the groups
+    // of the range, the split partials, the bias
+    const int chain_n = RT_BK + RT_GROUP + groups + L.nsplit + 1;
     // per-logit bound B_t = (gamma_n(fp32) + gamma_{H+2}(fp64)) * (||x_t|| max||w_e|| + max|b_e|);
     // threshold on a gap = 2 B_t, with a 1 % margin that covers the fp32 evaluation
     const double g32 = chain_n * u32 / (1.0 - chain_n * u32);
