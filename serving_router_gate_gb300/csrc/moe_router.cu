@@ -164,21 +164,31 @@ __global__ void __launch_bounds__(RT_THREADS, 1) router_logits_kernel(const uint
     auto step = [&](int c, Stage& nxt, Stage& far) {
         const int buf = c & 1;
         load(c + 2, far);
+        // the operands of k + 1 are loaded while the 32 FMAs of k issue; the chain of
+        // each chunk starts with the rounded product of its first k
+        float4 cxl = *reinterpret_cast<const float4*>(&xs[buf][0][4 * tg]);
+        float4 cxh = *reinterpret_cast<const float4*>(&xs[buf][0][64 + 4 * tg]);
+        float4 cw = *reinterpret_cast<const float4*>(&ws[buf][0][4 * eg]);
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) a1[i][j] = 0.f;
-#pragma unroll 4
         for (int k = 0; k < RT_BK; ++k) {
-            const float4 xlo = *reinterpret_cast<const float4*>(&xs[buf][k][4 * tg]);
-            const float4 xhi = *reinterpret_cast<const float4*>(&xs[buf][k][64 + 4 * tg]);
-            const float4 wv = *reinterpret_cast<const float4*>(&ws[buf][k][4 * eg]);
-            const float xv8[8] = {xlo.x, xlo.y, xlo.z, xlo.w, xhi.x, xhi.y, xhi.z, xhi.w};
-            const float wv4[4] = {wv.x, wv.y, wv.z, wv.w};
+            float4 nxl, nxh, nw4;
+            if (k + 1 < RT_BK) {
+                nxl = *reinterpret_cast<const float4*>(&xs[buf][k + 1][4 * tg]);
+                nxh = *reinterpret_cast<const float4*>(&xs[buf][k + 1][64 + 4 * tg]);
+                nw4 = *reinterpret_cast<const float4*>(&ws[buf][k + 1][4 * eg]);
+            }
+            const float xv8[8] = {cxl.x, cxl.y, cxl.z, cxl.w, cxh.x, cxh.y, cxh.z, cxh.w};
+            const float wv4[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
             for (int i = 0; i < 8; ++i)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) a1[i][j] = fmaf(xv8[i], wv4[j], a1[i][j]);
+                for (int j = 0; j < 4; ++j)
+                    a1[i][j] = k == 0 ? __fmul_rn(xv8[i], wv4[j]) : fmaf(xv8[i], wv4[j], a1[i][j]);
+            if (k + 1 < RT_BK) {
+                cxl = nxl;
+                cxh = nxh;
+                cw = nw4;
+            }
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i)
