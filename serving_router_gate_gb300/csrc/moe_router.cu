@@ -66,7 +66,7 @@ __device__ __forceinline__ void cp_async_wait_group() {
 // Both operands sit k-major in shared memory (xs[k][token], ws[k][expert], fp32),
 // so per k a thread reads its 8 token values and 4 expert values with three 16-byte
 // loads -- two of them broadcast to half a warp, one spread over 16 lanes -- and
-// issues 32 FMAs.  Chunks of 32 k are staged through registers loaded two chunks
+// issues 32 FMAs.  Chunks of 32 k are staged through registers loaded one chunk
 // ahead: a lane reads 8 consecutive k of one token row (bf16) or 4 of one Wg row,
 // the 32 lanes of a warp consecutive rows, and stores them transposed, conflict-free,
 // into the buffer the next chunk reads (two buffers, one barrier per chunk).  Each
@@ -77,9 +77,10 @@ __device__ __forceinline__ void cp_async_wait_group() {
 // token rows, CTAs of token tile 0 those of their Wg rows.
 constexpr int RT_XW = RT_BT;  // xs row (floats)
 constexpr int RT_WW = RT_BE;  // ws row (floats)
-constexpr size_t RT_SMEM = sizeof(float) * 2 * RT_BK * (RT_XW + RT_WW);
+// two tile buffers, then the range-level sums of every thread's 32 outputs
+constexpr size_t RT_SMEM = sizeof(float) * (2 * RT_BK * (RT_XW + RT_WW) + 32 * RT_THREADS);
 
-__global__ void __launch_bounds__(RT_THREADS, 1) router_logits_kernel(const uint16_t* __restrict__ x,
+__global__ void __launch_bounds__(RT_THREADS, 2) router_logits_kernel(const uint16_t* __restrict__ x,
                                                                       const float* __restrict__ Wg, int64_t T,
                                                                       int H, int E, int KC,
                                                                       float* __restrict__ part,
@@ -152,18 +153,23 @@ __global__ void __launch_bounds__(RT_THREADS, 1) router_logits_kernel(const uint
     const int lane = tid & 31, wid = tid >> 5;
     const int eg = lane & 15;
     const int tg = 2 * wid + (lane >> 4);
-    float a1[8][4], a2[8][4], a3[8][4];
+    // level 3 (the range) lives in shared memory: it changes once per 8 chunks
+    float* a3s = rt_smem + 2 * RT_BK * (RT_XW + RT_WW) + tid;  // element q at a3s[q * RT_THREADS]
+    float a1[8][4], a2[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) a2[i][j] = a3[i][j] = 0.f;
+        for (int j = 0; j < 4; ++j) {
+            a2[i][j] = 0.f;
+            a3s[(i * 4 + j) * RT_THREADS] = 0.f;
+        }
 
-    // chunk c: computed from buffer c & 1; the registers of chunk c + 1 (loaded one
-    // chunk earlier) go to the other buffer after it; chunk c + 2 is loaded into the
-    // registers chunk c came from
-    auto step = [&](int c, Stage& nxt, Stage& far) {
+    // chunk c: computed from buffer c & 1 while the registers load chunk c + 1, which
+    // goes to the other buffer after the compute
+    Stage sn;
+    auto step = [&](int c) {
         const int buf = c & 1;
-        load(c + 2, far);
+        load(c + 1, sn);
         // the operands of k + 1 are loaded while the 32 FMAs of k issue; the chain of
         // each chunk starts with the rounded product of its first k
         float4 cxl = *reinterpret_cast<const float4*>(&xs[buf][0][4 * tg]);
@@ -199,26 +205,22 @@ __global__ void __launch_bounds__(RT_THREADS, 1) router_logits_kernel(const uint
             for (int i = 0; i < 8; ++i)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    a3[i][j] += a2[i][j];
+                    a3s[(i * 4 + j) * RT_THREADS] += a2[i][j];
                     a2[i][j] = 0.f;
                 }
         }
-        if (c + 1 < nchunk) store(buf ^ 1, nxt);
+        if (c + 1 < nchunk) store(buf ^ 1, sn);
         __syncthreads();
     };
-    Stage s0, s1;
-    load(0, s0);
-    load(1, s1);
-    if (nchunk > 0) store(0, s0);
+    load(0, sn);
+    if (nchunk > 0) store(0, sn);
     __syncthreads();
-    for (int c = 0; c < nchunk; c += 2) {
-        step(c, s1, s0);
-        if (c + 1 < nchunk) step(c + 1, s0, s1);
-    }
+    for (int c = 0; c < nchunk; ++c) step(c);
+    float a3[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) a3[i][j] += a2[i][j];
+        for (int j = 0; j < 4; ++j) a3[i][j] = a3s[(i * 4 + j) * RT_THREADS] + a2[i][j];
 
     const int ebase = e0 + 4 * eg;
 #pragma unroll
@@ -902,14 +904,14 @@ __global__ void __launch_bounds__(RSM_THREADS, 1) router_small_kernel(
 
 }  // namespace
 
-// Split of H into K ranges: the CTAs run in waves of one CTA per SM, so pick the
+// Split of H into K ranges: the CTAs run in waves of two CTAs per SM, so pick the
 // range length that minimises waves x (range + a fixed per-CTA overhead of about
 // three chunks).
 void router_plan(int64_t T, int H, int E, int num_sms, int* nsplit, int* KC) {
     const int64_t tT = (T + RT_BT - 1) / RT_BT;
     const int64_t tE = (E + RT_BE - 1) / RT_BE;
     const int64_t base = tT * tE;
-    const int64_t slots = std::max<int64_t>(1, std::min<int64_t>((int64_t)num_sms, RT_TARGET_MAX));
+    const int64_t slots = std::max<int64_t>(1, std::min<int64_t>(2 * (int64_t)num_sms, RT_TARGET_MAX));
     int best_kc = H, best_ns = 1;
     int64_t best_cost = INT64_MAX;
     for (int kc = RT_BK; kc <= H; kc += RT_BK) {

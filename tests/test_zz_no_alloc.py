@@ -52,10 +52,10 @@ def test_noalloc_route_matches_route_on_two_calls_in_a_row():
 
 def _router_plan_splits(T, H, E, sms):
     """The number of K ranges moe_route's split plan picks (its cost model: CTAs of
-    128 tokens x 64 experts run in waves of one per SM; a CTA costs its range plus
+    128 tokens x 64 experts run in waves of two per SM; a CTA costs its range plus
     about three 32-wide chunks)."""
     tiles = -(-T // 128) * -(-E // 64)
-    slots = max(1, min(sms, 2048))
+    slots = max(1, min(2 * sms, 2048))
     best, best_ns = None, 1
     for kc in range(32, H + 1, 32):
         ns = -(-H // kc)
