@@ -302,13 +302,18 @@ def _work(cfg, rows: int, active_slots: int):
     Ish = cfg.n_shared * cfg.I_shared
     fc1_flops = 4.0 * H * (rows * I + T * Ish)
     fc2_flops = 2.0 * H * (rows * I + T * Ish)
-    eb = 1 if cfg.fp8 else 2  # bytes per weight (E4M3 adds one fp32 scale per row)
-    w1 = active_slots * 2 * I * (H * eb + (4 if cfg.fp8 else 0)) + 2 * Ish * (H * eb + (4 if cfg.fp8 else 0))
-    w2 = active_slots * H * (I * eb + (4 if cfg.fp8 else 0)) + H * (Ish * eb + (4 if cfg.fp8 else 0))
-    ab = 1 if cfg.act8 else 2  # bytes per GEMM input activation (E4M3 adds one fp32 scale per row)
+    # bytes per weight, per row of weights: bf16; E4M3 + an fp32 row scale; NVFP4: half a
+    # byte + one E4M3 block scale per 16 elements + an fp32 row scale
+    eb = 0.5 + 1.0 / 16 if cfg.fp4 else (1 if cfg.fp8 else 2)
+    er = 4 if (cfg.fp8 or cfg.fp4) else 0
+    w1 = active_slots * 2 * I * (H * eb + er) + 2 * Ish * (H * eb + er)
+    w2 = active_slots * H * (I * eb + er) + H * (Ish * eb + er)
+    # the same per GEMM input activation
+    ab = 0.5 + 1.0 / 16 if cfg.fp4 else (1 if cfg.act8 else 2)
+    ar = 4 if (cfg.act8 or cfg.fp4) else 0
     a_rows = rows + T * (Ish > 0)
-    fc1_bytes = w1 + a_rows * (H * ab + (4 if cfg.act8 else 0)) + rows * I * 2 + T * Ish * 2
-    fc2_bytes = (w2 + rows * (I * ab + (4 if cfg.act8 else 0)) + T * (Ish * ab + (4 if cfg.act8 and Ish else 0))
+    fc1_bytes = w1 + a_rows * (H * ab + ar) + rows * I * 2 + T * Ish * 2
+    fc2_bytes = (w2 + rows * (I * ab + ar) + T * (Ish * ab + (ar if Ish else 0))
                  + rows * H * 2 + (T * H * 2 if Ish else 0))
     # the whole layer: both GEMMs' bytes plus the router's x and fp32 gate weights, the
     # permuted rows written, the expert outputs read back by the combine, and out
@@ -316,6 +321,23 @@ def _work(cfg, rows: int, active_slots: int):
                    + (T * H * 2 if Ish else 0) + T * H * 2)
     return dict(fc1_flops=fc1_flops, fc2_flops=fc2_flops, fc1_bytes=fc1_bytes, fc2_bytes=fc2_bytes,
                 gate_flops=2.0 * T * H * cfg.E, layer_bytes=layer_bytes)
+
+
+def _oracle_nvfp4(oracle, cfg, cpu):
+    """NVFP4 workloads: the oracle's own quantisation of the weights (done once, untimed),
+    the shared experts as the one concatenated MLP the layer runs, NVFP4 activations."""
+    if not cfg.fp4:
+        return None
+    d = {}
+    d["W1q"], d["W1sb"], d["s1"] = oracle.quantize_nvfp4_rows(cpu["W1"])
+    d["W2q"], d["W2sb"], d["s2"] = oracle.quantize_nvfp4_rows(cpu["W2"])
+    if cpu["W1s"] is not None:
+        c1, c2 = mi.shared_concat(cpu["W1s"], cpu["W2s"])
+        cpu["W1s"], cpu["W2s"] = c1[None], c2[None]
+        d["W1sq"], d["W1ssb"], d["s1s"] = oracle.quantize_nvfp4_rows(cpu["W1s"])
+        d["W2sq"], d["W2ssb"], d["s2s"] = oracle.quantize_nvfp4_rows(cpu["W2s"])
+    d["act4"] = True
+    return d
 
 
 def _oracle_fp8(oracle, cfg, cpu):
@@ -344,13 +366,14 @@ def run_cpu_baseline(inp_dev, cfg, target_s=10.0, T_cap=None):
     cpu = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in inp_dev.items()}
 
     fp8 = _oracle_fp8(oracle, cfg, cpu)
+    fp4 = _oracle_nvfp4(oracle, cfg, cpu)
 
     def run(n):
         t0 = time.perf_counter()
         oracle.moe_layer(cpu["x"][:n], cpu["Wg"], cpu["bias"], cfg.k, cfg.renorm, cpu["W1"], cpu["W2"],
                          rep_offset=cpu["rep_offset"], rep_slots=cpu["rep_slots"], W1s=cpu["W1s"],
                          W2s=cpu["W2s"], shared_gate_w=cpu["w_s"], S=cfg.slots, n_group=cfg.n_group,
-                         topk_group=cfg.topk_group, on_input=cfg.on_input, fp8=fp8)
+                         topk_group=cfg.topk_group, on_input=cfg.on_input, fp8=fp8, nvfp4=fp4)
         return time.perf_counter() - t0
 
     threads = oracle.get_threads()
@@ -499,7 +522,8 @@ def bench_ours(args):
         # E4M3 operands: the measured bf16 peak times the nominal fp8 / bf16 ratio (4.5 / 2.25).
         # A timed region that ran under the power cap (sw_power_cap among the sampled reasons)
         # is held to the sustained peak, measured under the same cap; otherwise to the burst one.
-        ratio = 2.0 if cfg.act8 else 1.0
+        # nominal dense rates: bf16 2.25, fp8 4.5, fp4 13.5 PFLOP/s
+        ratio = 6.0 if cfg.fp4 else (2.0 if cfg.act8 else 1.0)
         capped = bool(clk and "sw_power_cap" in clk.get("reasons", []))
         burst, sustained = peaks["bf16"] * ratio, peaks["bf16_sustained"] * ratio
         peak = sustained if capped else burst
@@ -509,7 +533,8 @@ def bench_ours(args):
                     peak=peak, unit="TFLOP/s", frac=achieved / peak,
                     frac_of_burst=achieved / burst, frac_of_sustained=achieved / sustained,
                     peak_kind=f"{peaks['src']} {which}" + (" x 2, the nominal e4m3 / bf16 rate ratio"
-                                                            if cfg.act8 else ""))
+                                                            if cfg.act8 else "")
+                    + (" x 6, the nominal fp4 / bf16 rate ratio" if cfg.fp4 else ""))
         per_unit = f"{wk['fc1_flops']:.4g} flops per launch = 4*H*(rows*I + T*I_shared)"
     key = (args.workload, _src_hash(os.path.join(ROOT, "serving_router_gate_gb300", "csrc", "moe_grouped_gemm.cu")))
     roof["traffic"], roof["traffic_source"] = _traffic(key[0], key[1], wk["fc1_bytes"])
@@ -530,7 +555,7 @@ def bench_ours(args):
                         "CUDA events on the stream around each step"),
         "ms_per_step_with_graph_launch": ms_replay,
         "value_with_graph_launch": T * ws_ / (ms_replay * 1e-3),
-        "dtype": "e4m3" if cfg.act8 else "bf16", "data": "synthetic: seeded N(0,1) activations, N(0,sigma) random-init weights of the "
+        "dtype": "nvfp4" if cfg.fp4 else ("e4m3" if cfg.act8 else "bf16"), "data": "synthetic: seeded N(0,1) activations, N(0,sigma) random-init weights of the "
                                  "workload's shapes (no checkpoint)",
         "config": {"workload": cfg.name, "shape": mi.describe(cfg), "tokens_per_gpu": T,
                    "parallelism": f"replicas x{ws_} (independent token batches, no collective)",
@@ -577,12 +602,13 @@ def bench_reference(args):
     cpu = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
 
     fp8 = _oracle_fp8(oracle, cfg, cpu)
+    fp4 = _oracle_nvfp4(oracle, cfg, cpu)
 
     def step(n):
         oracle.moe_layer(cpu["x"][:n], cpu["Wg"], cpu["bias"], cfg.k, cfg.renorm, cpu["W1"], cpu["W2"],
                          rep_offset=cpu["rep_offset"], rep_slots=cpu["rep_slots"], W1s=cpu["W1s"],
                          W2s=cpu["W2s"], shared_gate_w=cpu["w_s"], S=cfg.slots, n_group=cfg.n_group,
-                         topk_group=cfg.topk_group, on_input=cfg.on_input, fp8=fp8)
+                         topk_group=cfg.topk_group, on_input=cfg.on_input, fp8=fp8, nvfp4=fp4)
 
     threads = oracle.get_threads()
     n0 = min(cfg.T, max(8, threads))

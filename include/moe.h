@@ -93,6 +93,12 @@ MOE_API const char *moe_status_string(int status);
  * caller will pass, as [TRT-10985] sizes its workspace by max_num_tokens. */
 MOE_API size_t moe_workspace_size(int64_t max_T, int H, int I, int E, int S, int k, int I_shared_total);
 
+/* The first MOE_WS_HEADER_BYTES bytes of every workspace are its header: the
+ * device status word and counters.  Kernels leave the small-batch router's
+ * counter at zero when they finish, so the header is zeroed only once, by
+ * moe_workspace_init; a caller never writes it. */
+#define MOE_WS_HEADER_BYTES 256
+
 /* Zero the workspace's header (status word and counters).  Call once after
  * allocating ws, before the first call that uses it. */
 MOE_API moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, moe_stream_t stream);
@@ -320,6 +326,57 @@ MOE_API moe_status_t moe_forward_w8a8(const moe_bf16_t *x_perm, const int32_t *o
  * `stream`; allocates nothing. */
 MOE_API moe_status_t moe_quantize_act_rows(const moe_bf16_t *v, int64_t rows, int K, uint8_t *q, float *scale,
                                    moe_stream_t stream);
+
+/* moe_forward_nvfp4 -- moe_forward with NVFP4 experts: E2M1 weights and
+ * activations with E4M3 block scales ([TRT-10985] review of torch_moe.py: the
+ * MoE ops have FP8 and NVFP4 paths; the pages fix no encoding).  Every expert
+ * matrix and every activation row is stored as moe_quantize_nvfp4_rows writes
+ * it: the weights with row scales amax / 2688 (pow2 = 0); the expert input rows
+ * (of x_perm), the shared experts' input x and the bf16 intermediates h are
+ * quantised inside the call with power-of-two row scales (pow2 = 1).  FC1 and
+ * FC2 run on tcgen05.mma kind::mxf4nvf4 (one E4M3 scale per 16 elements of
+ * both operands, fp32 accumulation); each accumulator is then multiplied by
+ * its A row's and its B row's fp32 scale.
+ *
+ *   W1q [S_local, 2I, H/2] uint8, W1_sf [S_local, 2I, MOE_NVFP4_SF_ROW_BYTES(H)],
+ *       W1_scale [S_local, 2I] fp32
+ *   W2q [S_local, H, I/2] uint8,  W2_sf [S_local, H, MOE_NVFP4_SF_ROW_BYTES(I)],
+ *       W2_scale [S_local, H] fp32
+ *   W1sq [2*I_shared_total, H/2], W1s_sf, W1s_scale; W2sq [H, I_shared_total/2],
+ *       W2s_sf, W2s_scale (the shared experts as one concatenated MLP; NULL if none)
+ * x_perm must be 16-byte aligned.  Launches two quantisation kernels besides
+ * moe_forward's three; their scratch is part of moe_workspace_size.  Everything
+ * else as moe_forward. */
+MOE_API moe_status_t moe_forward_nvfp4(const moe_bf16_t *x_perm, const int32_t *offsets, int S_local, int64_t P_cap,
+                               const uint8_t *W1q, const uint8_t *W1_sf, const float *W1_scale,
+                               const uint8_t *W2q, const uint8_t *W2_sf, const float *W2_scale, int H, int I,
+                               const int32_t *pair_row, const float *topk_w, int64_t T, int k,
+                               const moe_bf16_t *x, const uint8_t *W1sq, const uint8_t *W1s_sf,
+                               const float *W1s_scale, const uint8_t *W2sq, const uint8_t *W2s_sf,
+                               const float *W2s_scale, int I_shared_total, const moe_bf16_t *shared_gate_w,
+                               moe_bf16_t *out, void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Bytes of one row of NVFP4 block scales of K elements: one E4M3 byte per 16
+ * elements, padded with zero bytes to a multiple of 16 bytes (one 16-byte piece
+ * per 256 elements). */
+#define MOE_NVFP4_SF_ROW_BYTES(K) (16 * (((K) + 255) / 256))
+
+/* NVFP4 quantisation of a bf16 matrix v [rows, K] (K a multiple of 64), as
+ * moe_forward_nvfp4 reads it.  Per row: the row scale s = amax / 2688 (one
+ * binary32 division; pow2 = 0, for weights) or the smallest power of two 2^e,
+ * e >= -126, with amax <= 2688 * 2^e (pow2 = 1, for activations); per block of
+ * 16 elements sb = e4m3(bmax / (6 s)) and per element q = e2m1(v / (sb * s)),
+ * every product and division in binary32 and every conversion to nearest with
+ * ties to even, saturating (E4M3 at 448, E2M1 at 6).  An all-zero row gets zero
+ * codes and block scales (and s = 0 for weights).
+ *   q     [rows, K/2] uint8 out    codes, element 2i in the low nibble of byte i
+ *   sb    [rows, MOE_NVFP4_SF_ROW_BYTES(K)] uint8 out  E4M3 block scales, then zeros
+ *   scale [rows] fp32 out          row scales
+ * Expert weights [S, R, K] are quantised as one [S*R, K] matrix.  v must be
+ * 16-byte and q 8-byte aligned (MOE_ERR_INVALID_ARG otherwise).  Asynchronous on
+ * `stream`; allocates nothing. */
+MOE_API moe_status_t moe_quantize_nvfp4_rows(const moe_bf16_t *v, int64_t rows, int K, int pow2, uint8_t *q,
+                                     uint8_t *sb, float *scale, moe_stream_t stream);
 
 /* ---- the three stages of moe_forward ------------------------------------ */
 

@@ -62,6 +62,7 @@ class MoEConfig:
     on_input: bool = False           # routing weight applied to the expert input, outputs summed unweighted
     fp8: bool = False                # E4M3 expert weights with one fp32 scale per row
     act8: bool = False               # and E4M3 activations, one power-of-two scale per row
+    fp4: bool = False                # NVFP4 expert weights and activations (E2M1, E4M3 block scales)
     w_std: float = 0.02              # expert weight std
     gate_std: float = 0.02           # router weight std
     seed: int = 0
@@ -108,6 +109,8 @@ for _name in ["dsv2_lite_like_decode_t1", "dsv2_lite_like_decode_t8", "dsv2_lite
     CONFIGS[_name + "_fp8"] = CONFIGS[_name].with_(name=_name + "_fp8", fp8=True)
     # E4M3 weights and activations (tcgen05 kind::f8f6f4)
     CONFIGS[_name + "_w8a8"] = CONFIGS[_name].with_(name=_name + "_w8a8", fp8=True, act8=True)
+    # NVFP4 weights and activations (tcgen05 kind::mxf4nvf4)
+    CONFIGS[_name + "_nvfp4"] = CONFIGS[_name].with_(name=_name + "_nvfp4", fp4=True)
 
 
 def _gen(device, seed: int, idx: int) -> torch.Generator:
@@ -240,6 +243,8 @@ def describe(cfg: MoEConfig) -> str:
     if cfg.fp8:
         parts.append("E4M3 weights, row scales" + (" + E4M3 activations, power-of-two row scales"
                                                    if cfg.act8 else ""))
+    if cfg.fp4:
+        parts.append("NVFP4 weights and activations (E2M1, E4M3 scale per 16 elements, fp32 row scale)")
     return ", ".join(parts)
 
 

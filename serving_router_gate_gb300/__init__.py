@@ -26,6 +26,7 @@ __all__ = [
     "moe_debug_wait_timeout", "moe_set_wait_timeout_ns", "moe_route_noalloc", "moe_set_gemm_pair_mode",
     "moe_set_pdl", "moe_get_launch_count", "moe_permute_on_input", "moe_route_grouped", "moe_forward_fp8",
     "moe_quantize_fp8_rows", "moe_forward_w8a8", "moe_quantize_act_rows", "moe_grouped_fc1_fp8",
+    "moe_forward_nvfp4", "moe_quantize_nvfp4_rows", "nvfp4_sf_row_bytes", "MOE_WS_HEADER_BYTES",
     "moe_grouped_fc2_fp8", "moe_grouped_fc1_w8a8", "moe_grouped_fc2_w8a8", "moe_launch_events_arm",
     "moe_launch_events_mark", "moe_launch_events_used", "EXPORTED_SYMBOLS",
 ]
@@ -40,6 +41,7 @@ MOE_ERR_TIMEOUT = 16
 MOE_NONLOCAL_SKIP = 0
 MOE_NONLOCAL_MOD = 1
 MOE_LAUNCH_LABEL_BYTES = 48  # bytes per label written by moe_launch_events_used
+MOE_WS_HEADER_BYTES = 256    # the workspace header (status word, counters) a caller never writes
 
 EXPORTED_SYMBOLS = (
     "moe_status_string", "moe_workspace_size", "moe_workspace_init", "moe_get_device_status",
@@ -47,6 +49,7 @@ EXPORTED_SYMBOLS = (
     "moe_finalize", "moe_debug_wait_timeout", "moe_set_wait_timeout_ns", "moe_route_noalloc",
     "moe_set_gemm_pair_mode", "moe_set_pdl", "moe_get_launch_count", "moe_permute_on_input", "moe_route_grouped",
     "moe_forward_fp8", "moe_quantize_fp8_rows", "moe_grouped_fc1_fp8", "moe_grouped_fc2_fp8",
+    "moe_forward_nvfp4", "moe_quantize_nvfp4_rows",
     "moe_forward_w8a8", "moe_quantize_act_rows", "moe_grouped_fc1_w8a8", "moe_grouped_fc2_w8a8",
     "moe_launch_events_arm", "moe_launch_events_mark", "moe_launch_events_used",
 )
@@ -86,6 +89,9 @@ def _load():
         "moe_forward_w8a8": ([P, P, i32, i64, P, P, P, P, i32, i32, P, P, i64, i32, P, P, P, P, P, i32, P, P, P, sz,
                               P], i32),
         "moe_quantize_act_rows": ([P, i64, i32, P, P, P], i32),
+        "moe_forward_nvfp4": ([P, P, i32, i64, P, P, P, P, P, P, i32, i32, P, P, i64, i32, P, P, P, P, P, P, P, i32,
+                               P, P, P, sz, P], i32),
+        "moe_quantize_nvfp4_rows": ([P, i64, i32, i32, P, P, P, P], i32),
         "moe_grouped_fc1_w8a8": ([P, P, i64, P, i32, P, P, i32, i32, P, P, i64, P, P, i32, P, P, P, sz, P], i32),
         "moe_grouped_fc2_w8a8": ([P, P, i64, P, i32, P, P, i32, i32, P, P, i64, P, P, i32, P, P, P, sz, P], i32),
         "moe_grouped_fc1_fp8": ([P, i64, P, i32, P, P, i32, i32, P, i64, P, P, i32, P, P, P, sz, P], i32),
@@ -367,6 +373,54 @@ def moe_quantize_act_rows(v, q, scale, stream=None):
     st = _lib.moe_quantize_act_rows(_ptr(v, "v", _bf16), rows, K, _ptr(q, "q", torch.uint8, tuple(v.shape)),
                                     _ptr(scale, "scale", _f32, tuple(v.shape[:-1])), _stream(stream))
     _check("moe_quantize_act_rows", st)
+
+
+def nvfp4_sf_row_bytes(K: int) -> int:
+    """Bytes of one row of NVFP4 block scales of K elements (MOE_NVFP4_SF_ROW_BYTES)."""
+    return 16 * ((K + 255) // 256)
+
+
+def moe_quantize_nvfp4_rows(v, q, sb, scale, pow2=False, stream=None):
+    """NVFP4 quantisation of a bf16 tensor [..., K]: q [..., K/2] uint8 (packed E2M1 codes), sb
+    [..., nvfp4_sf_row_bytes(K)] uint8 (E4M3 block scales, zero-padded), scale [...] fp32 row scales
+    (amax / 2688, or powers of two with pow2)."""
+    K = v.shape[-1]
+    rows = v.numel() // K
+    lead = tuple(v.shape[:-1])
+    st = _lib.moe_quantize_nvfp4_rows(_ptr(v, "v", _bf16), rows, K, int(bool(pow2)),
+                                      _ptr(q, "q", torch.uint8, lead + (K // 2,)),
+                                      _ptr(sb, "sb", torch.uint8, lead + (nvfp4_sf_row_bytes(K),)),
+                                      _ptr(scale, "scale", _f32, lead), _stream(stream))
+    _check("moe_quantize_nvfp4_rows", st)
+
+
+def moe_forward_nvfp4(x_perm, offsets, W1q, W1sf, s1, W2q, W2sf, s2, pair_row, topk_w, x, W1sq, W1ssf, s1s,
+                      W2sq, W2ssf, s2s, shared_gate_w, out, ws, stream=None):
+    """moe_forward with NVFP4 weights (moe_quantize_nvfp4_rows, pow2=False) and NVFP4 activations."""
+    P_cap, H = x_perm.shape
+    S_local = offsets.shape[0] - 1
+    I = 2 * W2q.shape[2]
+    T, k = pair_row.shape
+    I_sh = 0 if W2sq is None else 2 * W2sq.shape[1]
+    u8 = torch.uint8
+    fh, fi, fs = nvfp4_sf_row_bytes(H), nvfp4_sf_row_bytes(I), nvfp4_sf_row_bytes(I_sh) if I_sh else 0
+    st = _lib.moe_forward_nvfp4(
+        _ptr(x_perm, "x_perm", _bf16), _ptr(offsets, "offsets", _i32), S_local, P_cap,
+        _ptr(W1q, "W1q", u8, (S_local, 2 * I, H // 2)), _ptr(W1sf, "W1_sf", u8, (S_local, 2 * I, fh)),
+        _ptr(s1, "W1_scale", _f32, (S_local, 2 * I)),
+        _ptr(W2q, "W2q", u8, (S_local, H, I // 2)), _ptr(W2sf, "W2_sf", u8, (S_local, H, fi)),
+        _ptr(s2, "W2_scale", _f32, (S_local, H)), H, I,
+        _ptr(pair_row, "pair_row", _i32), _ptr(topk_w, "topk_w", _f32, (T, k), allow_none=True), T, k,
+        _ptr(x, "x", _bf16, (T, H), allow_none=True),
+        _ptr(W1sq, "W1sq", u8, (2 * I_sh, H // 2), allow_none=True),
+        _ptr(W1ssf, "W1s_sf", u8, (2 * I_sh, fh), allow_none=True),
+        _ptr(s1s, "W1s_scale", _f32, (2 * I_sh,), allow_none=True),
+        _ptr(W2sq, "W2sq", u8, (H, I_sh // 2), allow_none=True),
+        _ptr(W2ssf, "W2s_sf", u8, (H, fs), allow_none=True),
+        _ptr(s2s, "W2s_scale", _f32, (H,), allow_none=True), I_sh,
+        _ptr(shared_gate_w, "shared_gate_w", _bf16, (H,), allow_none=True),
+        _ptr(out, "out", _bf16, (T, H)), _ptr(ws, "ws", torch.uint8), ws.numel(), _stream(stream))
+    _check("moe_forward_nvfp4", st)
 
 
 def moe_quantize_fp8_rows(w, q, scale, stream=None):

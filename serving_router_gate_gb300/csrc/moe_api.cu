@@ -73,7 +73,10 @@ int shared_split(int64_t T, int I, int I_sh) {
 struct ForwardLayout {
     size_t h, h_sh, y, y_sh, y_sh_part;
     // E4M3 activations: quantised expert inputs, shared input, intermediates, and scales
+    // (NVFP4 activations keep their packed codes and row scales in the same regions)
     size_t xq, sxq, xsq, sxs, hq, shq, hsq, shs;
+    // NVFP4 activations: block scales of the expert inputs, shared input, intermediates
+    size_t xsf, xssf, hsf, hssf;
     size_t total;
 };
 
@@ -108,6 +111,14 @@ ForwardLayout forward_layout(int64_t P_cap, int64_t T, int H, int I, int I_sh) {
     off += a256(T_sh * (size_t)(I_sh > 0 ? I_sh : 0));
     L.shs = off;
     off += a256(T_sh * 4);
+    L.xsf = off;
+    off += a256((size_t)P_cap * (size_t)nvfp4_sf_row_bytes(H));
+    L.xssf = off;
+    off += a256(T_sh * (size_t)nvfp4_sf_row_bytes(H));
+    L.hsf = off;
+    off += a256((size_t)P_cap * (size_t)nvfp4_sf_row_bytes(I));
+    L.hssf = off;
+    off += a256(T_sh * (size_t)(I_sh > 0 ? nvfp4_sf_row_bytes(I_sh) : 0));
     L.total = off;
     return L;
 }
@@ -641,6 +652,127 @@ moe_status_t moe_forward_w8a8(const moe_bf16_t* x_perm, const int32_t* offsets, 
     return forward_impl(x_perm, offsets, S_local, P_cap, W1q, W1_scale, W2q, W2_scale, H, I, pair_row, topk_w, T, k,
                         x, W1sq, W1s_scale, W2sq, W2s_scale, I_shared_total, shared_gate_w, out, ws, ws_bytes,
                         stream, true);
+}
+
+// One grouped GEMM on NVFP4 operands (packed E2M1 codes, E4M3 block scales, fp32
+// row scales): the routed problem (A rows a, weights b per group) and the shared
+// one (a_sh, b_sh).
+struct Nvfp4Operands {
+    const uint8_t *a, *a_sf;
+    const float* a_scale;
+    const uint8_t *b, *b_sf;
+    const float* b_scale;
+    const uint8_t *a_sh, *a_sh_sf;
+    const float* a_sh_scale;
+    const uint8_t *b_sh, *b_sh_sf;
+    const float* b_sh_scale;
+};
+
+static moe_status_t gemm_call_nvfp4(bool fc1, const Nvfp4Operands& o, int64_t rows_cap, const int32_t* offsets,
+                                    int G, int H, int I, int64_t T, int I_sh, moe_bf16_t* out, moe_bf16_t* out_sh,
+                                    void* ws, cudaStream_t s, float* out_sh_part, int ksplit_sh) {
+    GemmLaunch L;
+    L.swiglu = fc1;
+    L.a = reinterpret_cast<const uint16_t*>(o.a);
+    L.rows_cap = rows_cap;
+    L.offsets = offsets;
+    L.G = G;
+    L.b = reinterpret_cast<const uint16_t*>(o.b);
+    L.K = fc1 ? H : I;
+    L.Nb = fc1 ? 2 * I : H;
+    L.N_out = fc1 ? I : H;
+    L.out = out;
+    L.a_sh = reinterpret_cast<const uint16_t*>(o.a_sh);
+    L.T_sh = I_sh > 0 ? T : 0;
+    L.b_sh = reinterpret_cast<const uint16_t*>(o.b_sh);
+    L.K_sh = fc1 ? H : I_sh;
+    L.Nb_sh = fc1 ? 2 * I_sh : H;
+    L.N_out_sh = fc1 ? I_sh : H;
+    L.out_sh = out_sh;
+    L.out_sh_part = out_sh_part;
+    L.ksplit_sh = ksplit_sh;
+    L.hdr = static_cast<WsHeader*>(ws);
+    L.timeout_ns = g_timeout_ns.load();
+    L.pair_mode = 0;
+    L.max_group_rows = std::min<int64_t>(T, rows_cap);
+    L.quant = GEMM_NVFP4;
+    L.b_scale = o.b_scale;
+    L.b_scale_sh = o.b_sh_scale;
+    L.a_scale = o.a_scale;
+    L.a_scale_sh = o.a_sh_scale;
+    L.a_sf = o.a_sf;
+    L.a_sf_sh = o.a_sh_sf;
+    L.b_sf = o.b_sf;
+    L.b_sf_sh = o.b_sh_sf;
+    const char* why = nullptr;
+    return cuda_status(launch_grouped_gemm(L, device_sms(), s, &why));
+}
+
+moe_status_t moe_quantize_nvfp4_rows(const moe_bf16_t* v, int64_t rows, int K, int pow2, uint8_t* q, uint8_t* sb,
+                                     float* scale, moe_stream_t stream) {
+    if (rows < 0 || K <= 0 || (pow2 != 0 && pow2 != 1)) return MOE_ERR_INVALID_ARG;
+    if (K % 64 != 0) return MOE_ERR_UNSUPPORTED;
+    if (rows == 0) return MOE_OK;
+    if (!v || !q || !sb || !scale) return MOE_ERR_INVALID_ARG;
+    if (!aligned(v, 16) || !aligned(q, 8)) return MOE_ERR_INVALID_ARG;
+    const Nvfp4QuantSeg seg = {v, rows, nullptr, K, pow2, q, sb, scale};
+    return cuda_status(launch_quantize_nvfp4_rows(&seg, 1, device_sms(), (cudaStream_t)stream));
+}
+
+moe_status_t moe_forward_nvfp4(const moe_bf16_t* x_perm, const int32_t* offsets, int S_local, int64_t P_cap,
+                               const uint8_t* W1q, const uint8_t* W1_sf, const float* W1_scale, const uint8_t* W2q,
+                               const uint8_t* W2_sf, const float* W2_scale, int H, int I, const int32_t* pair_row,
+                               const float* topk_w, int64_t T, int k, const moe_bf16_t* x, const uint8_t* W1sq,
+                               const uint8_t* W1s_sf, const float* W1s_scale, const uint8_t* W2sq,
+                               const uint8_t* W2s_sf, const float* W2s_scale, int I_shared_total,
+                               const moe_bf16_t* shared_gate_w, moe_bf16_t* out, void* ws, size_t ws_bytes,
+                               moe_stream_t stream) {
+    if (T < 0 || k <= 0 || S_local <= 0 || P_cap < 0 || H <= 0 || I <= 0 || I_shared_total < 0)
+        return MOE_ERR_INVALID_ARG;
+    if (!dim_ok(H) || !dim_ok(I) || (I_shared_total > 0 && !dim_ok(I_shared_total)) || k > 32 || S_local > 1024 ||
+        P_cap >= (int64_t(1) << 31))
+        return MOE_ERR_UNSUPPORTED;
+    if (T == 0) return MOE_OK;
+    if (!x_perm || !offsets || !W1q || !W1_sf || !W1_scale || !W2q || !W2_sf || !W2_scale || !pair_row || !out)
+        return MOE_ERR_INVALID_ARG;
+    if (I_shared_total > 0 && (!x || !W1sq || !W1s_sf || !W1s_scale || !W2sq || !W2s_sf || !W2s_scale))
+        return MOE_ERR_INVALID_ARG;
+    if (shared_gate_w && (I_shared_total == 0 || !x)) return MOE_ERR_INVALID_ARG;
+    if (!aligned(x_perm, 16) || (I_shared_total > 0 && !aligned(x, 16))) return MOE_ERR_INVALID_ARG;
+    const ForwardLayout FL = forward_layout(P_cap, T, H, I, I_shared_total);
+    if (!ws || ws_bytes < FL.total) return MOE_ERR_WORKSPACE;
+    char* base = static_cast<char*>(ws);
+    auto u8 = [&](size_t off) { return reinterpret_cast<uint8_t*>(base + off); };
+    auto f32 = [&](size_t off) { return reinterpret_cast<float*>(base + off); };
+    moe_bf16_t* h = reinterpret_cast<moe_bf16_t*>(base + FL.h);
+    moe_bf16_t* h_sh = I_shared_total > 0 ? reinterpret_cast<moe_bf16_t*>(base + FL.h_sh) : nullptr;
+    moe_bf16_t* y = reinterpret_cast<moe_bf16_t*>(base + FL.y);
+    moe_bf16_t* y_sh = I_shared_total > 0 ? reinterpret_cast<moe_bf16_t*>(base + FL.y_sh) : nullptr;
+    cudaStream_t s = (cudaStream_t)stream;
+    const int ks = shared_split(T, I, I_shared_total);
+    float* y_sh_part = ks > 1 ? reinterpret_cast<float*>(base + FL.y_sh_part) : nullptr;
+    const int sms = device_sms();
+    const int64_t T_sh = I_shared_total > 0 ? T : 0;
+    // the expert input rows (as many as offsets[S_local] says, read on the device) and the
+    // shared experts' input, to NVFP4 with power-of-two row scales
+    const Nvfp4QuantSeg qx[2] = {{x_perm, P_cap, offsets + S_local, H, 1, u8(FL.xq), u8(FL.xsf), f32(FL.sxq)},
+                                 {x, T_sh, nullptr, H, 1, u8(FL.xsq), u8(FL.xssf), f32(FL.sxs)}};
+    moe_status_t st = cuda_status(launch_quantize_nvfp4_rows(qx, T_sh > 0 ? 2 : 1, sms, s));
+    if (st != MOE_OK) return st;
+    const Nvfp4Operands o1 = {u8(FL.xq), u8(FL.xsf), f32(FL.sxq), W1q, W1_sf, W1_scale,
+                              u8(FL.xsq), u8(FL.xssf), f32(FL.sxs), W1sq, W1s_sf, W1s_scale};
+    st = gemm_call_nvfp4(true, o1, P_cap, offsets, S_local, H, I, T, I_shared_total, h, h_sh, ws, s, nullptr, 1);
+    if (st != MOE_OK) return st;
+    const Nvfp4QuantSeg qh[2] = {{h, P_cap, offsets + S_local, I, 1, u8(FL.hq), u8(FL.hsf), f32(FL.shq)},
+                                 {h_sh, T_sh, nullptr, I_shared_total, 1, u8(FL.hsq), u8(FL.hssf), f32(FL.shs)}};
+    st = cuda_status(launch_quantize_nvfp4_rows(qh, T_sh > 0 ? 2 : 1, sms, s));
+    if (st != MOE_OK) return st;
+    const Nvfp4Operands o2 = {u8(FL.hq), u8(FL.hsf), f32(FL.shq), W2q, W2_sf, W2_scale,
+                              u8(FL.hsq), u8(FL.hssf), f32(FL.shs), W2sq, W2s_sf, W2s_scale};
+    st = gemm_call_nvfp4(false, o2, P_cap, offsets, S_local, H, I, T, I_shared_total, y, y_sh, ws, s, y_sh_part, ks);
+    if (st != MOE_OK) return st;
+    return finalize_call(y, P_cap, pair_row, topk_w, T, k, H, y_sh_part ? nullptr : y_sh, y_sh_part, ks, x,
+                         shared_gate_w, out, ws, s);
 }
 
 moe_status_t moe_quantize_act_rows(const moe_bf16_t* v, int64_t rows, int K, uint8_t* q, float* scale,

@@ -69,6 +69,9 @@ constexpr int BM_SHORT = 32;                      // A rows loaded for tiles wit
 constexpr int A_SHORT_BYTES = BM_SHORT * BK * 2;
 constexpr int NUM_THREADS = 192;
 constexpr int NUM_THREADS_FP8 = 448;  // plus warps 6..13: E4M3 -> bf16 converters
+constexpr int NUM_THREADS_F4 = 256;   // plus warps 6..7: NVFP4 block-scale layout converters
+constexpr int F4_CONV_THREADS = 64;
+constexpr int SF_STAGE_BYTES = 4096;  // NVFP4: the A and the B block scales of a stage, 2 KB each
 constexpr int CONV_THREADS = 256;
 constexpr int CONV_BARRIER = 1;       // named barrier of the converter warps
 constexpr int MAX_GROUPS = 1024;
@@ -80,7 +83,7 @@ constexpr uint16_t PAIR_MASK = 0x3;
 // small ones over more CTAs); a CTA holds all of B (single) or its half (pair).
 // A stage holds KS consecutive K chunks of 64 bf16 (one 128-byte swizzle row per
 // operand row each): chunk c of A at c * A_CHUNK, of B at c * B_CHUNK.
-template <bool kPair, int BN, bool kShort = false, int KS = 1>
+template <bool kPair, int BN, bool kShort = false, int KS = 1, int SFB = 0>
 struct Cfg {
     static constexpr int B_CHUNK = (kPair ? BN / 2 : BN) * BK * 2;
     static constexpr int B_BYTES = B_CHUNK * KS;
@@ -88,12 +91,11 @@ struct Cfg {
     // MMA still reads 128 rows from the chunk onward; rows past 32 are never stored)
     static constexpr int A_CHUNK = kShort ? A_SHORT_BYTES : A_BYTES;
     static constexpr int A_SLOT = A_CHUNK * KS;
-    static constexpr int STAGE_BYTES = A_SLOT + B_BYTES;
+    static constexpr int STAGE_BYTES = A_SLOT + B_BYTES + SFB;  // SFB: NVFP4 block scales
     static constexpr int STAGES = RING_BYTES / STAGE_BYTES < MAX_STAGES ? RING_BYTES / STAGE_BYTES : MAX_STAGES;
     static constexpr int TMEM_COLS = 2 * BN;  // two accumulators of BN fp32 columns
     // 2-CTA MMA: M = 256 across the pair
     static constexpr uint32_t IDESC = idesc_bf16_f32(kPair ? 2 * BM : BM, BN);
-    static constexpr uint32_t IDESC8 = idesc_e4m3_f32(BM, BN);
 };
 
 struct GemmParams {
@@ -145,9 +147,21 @@ constexpr int chunks_per_stage() {
     return (kShort && kQ == 0) ? 2 : 1;
 }
 
-template <bool kPair, int BN, bool kShort, int KS>
+// block-scale bytes of a pipeline stage
+template <int kQ>
+constexpr int sf_stage_bytes() {
+    return kQ == GEMM_NVFP4 ? SF_STAGE_BYTES : 0;
+}
+
+template <int kQ>
+constexpr int threads_of() {
+    return kQ == GEMM_W8 ? NUM_THREADS_FP8 : (kQ == GEMM_NVFP4 ? NUM_THREADS_F4 : NUM_THREADS);
+}
+
+template <bool kPair, int BN, bool kShort, int KS, int SFB>
 constexpr size_t smem_bytes() {
-    return 1024 /*alignment slack*/ + (size_t)Cfg<kPair, BN, kShort, KS>::STAGES * Cfg<kPair, BN, kShort, KS>::STAGE_BYTES +
+    return 1024 /*alignment slack*/ +
+           (size_t)Cfg<kPair, BN, kShort, KS, SFB>::STAGES * Cfg<kPair, BN, kShort, KS, SFB>::STAGE_BYTES +
            sizeof(SmemMeta);
 }
 
@@ -245,22 +259,29 @@ __device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t x, uint32_t& o0, uint3
 }
 
 template <bool kFC1, bool kPair, int BN, bool kShort, int kQ>
-__global__ void __launch_bounds__(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
+__global__ void __launch_bounds__(threads_of<kQ>(), 1)
     grouped_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmAs,
                         const __grid_constant__ CUtensorMap tmBs, const __grid_constant__ CUtensorMap tmA32,
-                        const __grid_constant__ CUtensorMap tmAs32) {
+                        const __grid_constant__ CUtensorMap tmAs32, const __grid_constant__ CUtensorMap tmSFA,
+                        const __grid_constant__ CUtensorMap tmSFB, const __grid_constant__ CUtensorMap tmSFAs,
+                        const __grid_constant__ CUtensorMap tmSFBs) {
     constexpr int KSC = chunks_per_stage<kShort, kQ>();
-    using C = Cfg<kPair, BN, kShort, KSC>;
+    using C = Cfg<kPair, BN, kShort, KSC, sf_stage_bytes<kQ>()>;
     constexpr int STAGES = C::STAGES;
     constexpr int B_BYTES = C::B_BYTES;
     constexpr int A_SLOT = C::A_SLOT;
     constexpr uint32_t IDESC = C::IDESC;
+    constexpr uint32_t IDESC4 = idesc_nvfp4(BM, BN);
     constexpr int TMEM_COLS = C::TMEM_COLS;
     static_assert(!kShort || !kPair, "short tiles run in single mode");
     constexpr bool kFp8 = kQ == GEMM_W8;      // E4M3 weights widened by converter warps
     constexpr bool kA8 = kQ == GEMM_W8A8;     // E4M3 A and B on kind::f8f6f4
-    constexpr int KE = kA8 ? 2 * BK : BK;     // elements per K step (one 128-byte row)
+    constexpr bool kF4 = kQ == GEMM_NVFP4;    // E2M1 A and B with E4M3 block scales on kind::mxf4nvf4
+    constexpr int KE = kF4 ? 4 * BK : (kA8 ? 2 * BK : BK);  // elements per K step (one 128-byte row)
+    // NVFP4: two accumulators, then two sets (stage parity) of 32 block-scale columns
+    constexpr int TMEM_ALLOC = kF4 ? 512 : TMEM_COLS;
+    static_assert(!kF4 || (!kPair && BN == 128 && 2 * BN + 64 <= TMEM_ALLOC), "NVFP4 runs single CTAs with N = 128");
     static_assert(!kFp8 || (!kPair && BN == 256), "E4M3 weights run in single mode with N = 256");
     static_assert(!kA8 || !kPair, "E4M3 activations run in single mode");
     static_assert(!kPair || BN == 256, "pair mode uses N = 256");
@@ -268,6 +289,7 @@ __global__ void __launch_bounds__(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS,
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t* smA = smem;
     uint8_t* smB = smem + (size_t)STAGES * A_SLOT;
+    uint8_t* smSF = smB + (size_t)STAGES * B_BYTES;  // NVFP4: [stage][A scales 2 KB][B scales 2 KB]
     SmemMeta& m = *reinterpret_cast<SmemMeta*>(smem + (size_t)STAGES * C::STAGE_BYTES);
 
     const int warp = threadIdx.x >> 5;
@@ -283,6 +305,7 @@ __global__ void __launch_bounds__(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS,
             mbar_init(&m.full[s], 1);   // pair mode: only the leader's, fed by both CTAs' copies
             mbar_init(&m.empty[s], 1);  // released by the (leader's) MMA commit
             if (kFp8) mbar_init(&m.conv[s], CONV_THREADS / 32);  // one arrival per converter warp
+            if (kF4) mbar_init(&m.conv[s], F4_CONV_THREADS / 32);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&m.tfull[b], 1);
@@ -298,13 +321,19 @@ __global__ void __launch_bounds__(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS,
         tma_prefetch_desc(&tmBs);
         tma_prefetch_desc(&tmA32);
         tma_prefetch_desc(&tmAs32);
+        if (kF4) {
+            tma_prefetch_desc(&tmSFA);
+            tma_prefetch_desc(&tmSFB);
+            tma_prefetch_desc(&tmSFAs);
+            tma_prefetch_desc(&tmSFBs);
+        }
     }
     if (warp == 1) {
         if (kPair) {
             tmem_alloc_pair(&m.tmem_base, TMEM_COLS);
             tmem_relinquish_pair();
         } else {
-            tmem_alloc(&m.tmem_base, TMEM_COLS);
+            tmem_alloc(&m.tmem_base, TMEM_ALLOC);
             tmem_relinquish();
         }
     }
@@ -368,8 +397,9 @@ __global__ void __launch_bounds__(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS,
             for (int i = 0; i < n_long; ++i) {
                 const Tile tl = tile_of<kFC1, kPair>(unit0 + i * nunits, p, m, n_sh_tiles, mu_sh, crank);
                 for (int kb = tl.kb0; kb < tl.kb1; ++kb) {
-                    tma_prefetch_l2_3d(&tmBs, kb * KE, tl.nt * (BN / 2), 0);
-                    tma_prefetch_l2_3d(&tmBs, kb * KE, p.up_off_sh + tl.nt * (BN / 2), 0);
+                    const int kx = kF4 ? kb * 128 : kb * KE;  // x in bytes: packed E2M1 holds two per byte
+                    tma_prefetch_l2_3d(&tmBs, kx, tl.nt * (BN / 2), 0);
+                    tma_prefetch_l2_3d(&tmBs, kx, p.up_off_sh + tl.nt * (BN / 2), 0);
                 }
             }
         }
@@ -471,6 +501,28 @@ __global__ void __launch_bounds__(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS,
                         } else {
                             tma_load_3d(b_dst, mB, &m.full[stage], kb * KE, tl.nt * BN, tl.g);
                         }
+                    } else if (kF4) {
+                        // 128-byte rows of packed E2M1 codes (256 elements) and, for the same
+                        // 256 elements, 16 bytes of block scales per row: A's tile rows from
+                        // row0, B's rows as the codes (FC1: gate rows, then up rows)
+                        const CUtensorMap* mSA = tl.prob ? &tmSFAs : &tmSFA;
+                        const CUtensorMap* mSB = tl.prob ? &tmSFBs : &tmSFB;
+                        constexpr uint32_t SFA_BOX = (kShort ? BM_SHORT : BM) * 16;
+                        mbar_arrive_expect_tx(&m.full[stage], a_bytes + B_BYTES + SFA_BOX + BN * 16);
+                        const int kx = kb * 128, ks = kb * 16;
+                        uint8_t* sfa = smSF + (size_t)stage * SF_STAGE_BYTES;
+                        uint8_t* sfb = sfa + SF_STAGE_BYTES / 2;
+                        tma_load_2d(a_dst, mA, &m.full[stage], kx, tl.row0);
+                        tma_load_3d(sfa, mSA, &m.full[stage], ks, tl.row0, 0);
+                        if (kFC1) {
+                            tma_load_3d(b_dst, mB, &m.full[stage], kx, tl.nt * (BN / 2), tl.g);
+                            tma_load_3d(b_dst + B_BYTES / 2, mB, &m.full[stage], kx, up + tl.nt * (BN / 2), tl.g);
+                            tma_load_3d(sfb, mSB, &m.full[stage], ks, tl.nt * (BN / 2), tl.g);
+                            tma_load_3d(sfb + (BN / 2) * 16, mSB, &m.full[stage], ks, up + tl.nt * (BN / 2), tl.g);
+                        } else {
+                            tma_load_3d(b_dst, mB, &m.full[stage], kx, tl.nt * BN, tl.g);
+                            tma_load_3d(sfb, mSB, &m.full[stage], ks, tl.nt * BN, tl.g);
+                        }
                     } else {
                         // KSC chunks: a chunk past the range's end lies past K (ranges of
                         // split tiles are multiples of KSC), where the TMA fills zeros
@@ -518,6 +570,7 @@ __global__ void __launch_bounds__(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS,
         if (lane == 0 && crank == 0) {
             // ---------------- MMA issuer (the pair's leader in pair mode) ----------------
             uint32_t stage = 0, phase = 0;
+            uint32_t sfp = 0;  // NVFP4: block-scale columns of this stage (two sets, alternating)
             bool failed = false;
             int i = 0;
             bool have = false;
@@ -538,13 +591,28 @@ __global__ void __launch_bounds__(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS,
                 tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(buf * BN);
                 for (int kb = 0; kb < nkb; ++kb) {
-                    if (!mbar_wait(kFp8 ? &m.conv[stage] : &m.full[stage], phase, p.timeout_ns, abortp)) {
+                    if (!mbar_wait((kFp8 || kF4) ? &m.conv[stage] : &m.full[stage], phase, p.timeout_ns, abortp)) {
                         failed = true;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t a0 = smem_u32(smA + (size_t)stage * A_SLOT);
                     const uint32_t b0 = smem_u32(smB + (size_t)stage * B_BYTES);
+                    if constexpr (kF4) {
+                        // per MMA of 64 elements: the A and B block scales of its 4 blocks
+                        // (laid out by the converter warps) into tensor memory, then the MMA
+                        const uint32_t sf0 = smem_u32(smSF + (size_t)stage * SF_STAGE_BYTES);
+                        const uint32_t col = tmem_base + (uint32_t)(2 * BN) + (sfp & 1u) * 32u;
+#pragma unroll
+                        for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                            tc_copy_32x128b_x4(col + kk * 4, sf0 + kk * 512);
+                            tc_copy_32x128b_x4(col + 16 + kk * 4, sf0 + SF_STAGE_BYTES / 2 + kk * 512);
+                            const uint64_t ad = sw128_kmajor_desc(a0 + kk * UMMA_K * 2);
+                            const uint64_t bd = sw128_kmajor_desc(b0 + kk * UMMA_K * 2);
+                            tc_mma_nvfp4(d, ad, bd, IDESC4, col + kk * 4, col + 16 + kk * 4, (kb | kk) != 0 ? 1u : 0u);
+                        }
+                        ++sfp;
+                    } else {
 #pragma unroll
                     for (int c = 0; c < KSC; ++c)
 #pragma unroll
@@ -556,10 +624,11 @@ __global__ void __launch_bounds__(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS,
                             if (kPair)
                                 tc_mma_bf16_pair(d, ad, bd, IDESC, acc);
                             else if (kA8)
-                                tc_mma_e4m3(d, ad, bd, C::IDESC8, acc);
+                                tc_mma_e4m3(d, ad, bd, idesc_e4m3_f32(BM, BN), acc);
                             else
                                 tc_mma_bf16(d, ad, bd, IDESC, acc);
                         }
+                    }
                     if (kPair)
                         tc_commit_pair_multicast(&m.empty[stage], PAIR_MASK);
                     else
@@ -626,11 +695,12 @@ __global__ void __launch_bounds__(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS,
             uint16_t* orow = out + (int64_t)(tl.row0 + row_in) * N_out;
             // E4M3 weights: the accumulator of output column n carries B row n's scale;
             // E4M3 activations: and its A row's scale (a power of two)
-            const float* srow = (kFp8 || kA8) ? (tl.prob ? p.scale_sh : p.scale + (int64_t)tl.g * p.Nb) : nullptr;
+            constexpr bool kRowScaleB = kFp8 || kA8 || kF4, kRowScaleA = kA8 || kF4;
+            const float* srow = kRowScaleB ? (tl.prob ? p.scale_sh : p.scale + (int64_t)tl.g * p.Nb) : nullptr;
             const int sup = tl.prob ? p.up_off_sh : p.up_off;
             const float asc =
-                (kA8 && valid) ? __ldg((tl.prob ? p.a_scale_sh : p.a_scale) + tl.row0 + row_in) : 1.0f;
-            auto bscale = [&](int row) -> float { return (kFp8 || kA8) ? __ldg(srow + row) : 1.0f; };
+                (kRowScaleA && valid) ? __ldg((tl.prob ? p.a_scale_sh : p.a_scale) + tl.row0 + row_in) : 1.0f;
+            auto bscale = [&](int row) -> float { return kRowScaleB ? __ldg(srow + row) : 1.0f; };
             if (kFC1) {
 #pragma unroll 1
                 for (int c = 0; c < OW; c += 32) {
@@ -778,6 +848,67 @@ __global__ void __launch_bounds__(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS,
             m.abort = 1;
             report(p.status, MOE_ERR_TIMEOUT);
         }
+    } else if (kF4 && warp >= 6) {
+        // ---------------- NVFP4 block-scale layout (warps 6..7) ----------------
+        // A stage's block scales arrive row-major: row r's 16 bytes (the 16 blocks of
+        // the stage's 256 elements) at 16 r, A rows then B rows, 2 KB each.  The MMA of
+        // elements 64 kk .. 64 kk + 63 takes them as 512 bytes per operand: lane l's 16
+        // bytes hold the 4 scales (blocks 4 kk .. 4 kk + 3) of rows l, 32 + l, 64 + l
+        // and 96 + l.  Thread (l, pair) moves chunks 2 pair and 2 pair + 1 of both
+        // operands: it reads all its words, the 64 threads meet, then write in place.
+        const int ct = threadIdx.x - 6 * 32;  // 0 .. F4_CONV_THREADS - 1
+        const int l = ct & 31, kp = (ct >> 5) * 2;
+        uint32_t stage = 0, phase = 0;
+        bool failed = false;
+        if (ct == 0) m.conv_ok = mbar_wait(&m.ready, 0, p.timeout_ns, abortp) ? 1 : 0;
+        asm volatile("bar.sync %0, %1;" ::"n"(CONV_BARRIER), "n"(F4_CONV_THREADS) : "memory");
+        failed = !m.conv_ok;
+        bool have = true;  // the prefix is published (waited for above)
+        for (int iu = 0; !failed; ++iu) {
+            const int u = next_unit(iu, have);
+            if (u < 0) break;
+            const Tile tl = tile_of<kFC1, kPair>(u, p, m, n_sh_tiles, mu_sh, crank);
+            const int nkb = tl.kb1 - tl.kb0;
+            for (int kb = 0; kb < nkb; ++kb) {
+                if (ct == 0) m.conv_ok = mbar_wait(&m.full[stage], phase, p.timeout_ns, abortp) ? 1 : 0;
+                asm volatile("bar.sync %0, %1;" ::"n"(CONV_BARRIER), "n"(F4_CONV_THREADS) : "memory");
+                if (!m.conv_ok) {
+                    failed = true;
+                    break;
+                }
+                uint8_t* sfa = smSF + (size_t)stage * SF_STAGE_BYTES;
+                const uint32_t* ra = reinterpret_cast<const uint32_t*>(sfa);
+                const uint32_t* rb = reinterpret_cast<const uint32_t*>(sfa + SF_STAGE_BYTES / 2);
+                uint32_t wa[2][4], wb[2][4];
+#pragma unroll
+                for (int c = 0; c < 2; ++c)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        wa[c][q] = ra[(32 * q + l) * 4 + kp + c];
+                        wb[c][q] = rb[(32 * q + l) * 4 + kp + c];
+                    }
+                asm volatile("bar.sync %0, %1;" ::"n"(CONV_BARRIER), "n"(F4_CONV_THREADS) : "memory");
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    *reinterpret_cast<uint4*>(sfa + (kp + c) * 512 + l * 16) =
+                        make_uint4(wa[c][0], wa[c][1], wa[c][2], wa[c][3]);
+                    *reinterpret_cast<uint4*>(sfa + SF_STAGE_BYTES / 2 + (kp + c) * 512 + l * 16) =
+                        make_uint4(wb[c][0], wb[c][1], wb[c][2], wb[c][3]);
+                }
+                // generic-proxy stores -> visible to the tensor core's copies
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&m.conv[stage]);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        if (failed && lane == 0) {
+            m.abort = 1;
+            report(p.status, MOE_ERR_TIMEOUT);
+        }
     }
 
     // ---------------- teardown ----------------
@@ -794,7 +925,7 @@ __global__ void __launch_bounds__(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS,
         if (kPair)
             tmem_dealloc_pair(tmem_base, TMEM_COLS);
         else
-            tmem_dealloc(tmem_base, TMEM_COLS);
+            tmem_dealloc(tmem_base, TMEM_ALLOC);
     }
 }
 
@@ -873,6 +1004,22 @@ bool encode_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// NVFP4 block scales [groups][rows][row_bytes] bytes (row_bytes a multiple of
+// 16): boxes of 16 bytes (one pipeline stage's 16 blocks) x box_rows rows, no
+// swizzle (the converter warps lay them out for the tensor core)
+bool encode_sf(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows, uint64_t groups,
+               uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {row_bytes, rows, groups};
+    cuuint64_t strides[2] = {row_bytes, rows * row_bytes};
+    cuuint32_t box[3] = {16, box_rows, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Per-device launch facts of one kernel instantiation: shared-memory limit set,
 // and (pair mode) how many 2-CTA clusters can be resident at once.
 struct KernelInfo {
@@ -891,14 +1038,14 @@ cudaError_t kernel_info(int num_sms, KernelInfo* out) {
     std::lock_guard<std::mutex> lock(mu);
     if (!info[dev].ready) {
         err = cudaFuncSetAttribute(grouped_gemm_kernel<kFC1, kPair, BN, kShort, kQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)smem_bytes<kPair, BN, kShort, chunks_per_stage<kShort, kQ>()>());
+                                   (int)smem_bytes<kPair, BN, kShort, chunks_per_stage<kShort, kQ>(), sf_stage_bytes<kQ>()>());
         if (err != cudaSuccess) return err;
         int clusters = 0;
         if (kPair) {
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(2 * num_sms);
-            cfg.blockDim = dim3(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS);
-            cfg.dynamicSmemBytes = smem_bytes<kPair, BN, kShort, chunks_per_stage<kShort, kQ>()>();
+            cfg.blockDim = dim3(threads_of<kQ>());
+            cfg.dynamicSmemBytes = smem_bytes<kPair, BN, kShort, chunks_per_stage<kShort, kQ>(), sf_stage_bytes<kQ>()>();
             cudaLaunchAttribute attr;
             attr.id = cudaLaunchAttributeClusterDimension;
             attr.val.clusterDim.x = 2;
@@ -918,12 +1065,14 @@ cudaError_t kernel_info(int num_sms, KernelInfo* out) {
 
 template <bool kFC1, bool kPair, int BN, bool kShort, int kQ>
 cudaError_t launch_kernel(const GemmParams& p, const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mAs,
-                          const CUtensorMap& mBs, const CUtensorMap& mA32, const CUtensorMap& mAs32, unsigned grid,
+                          const CUtensorMap& mBs, const CUtensorMap& mA32, const CUtensorMap& mAs32,
+                          const CUtensorMap& mSFA, const CUtensorMap& mSFB, const CUtensorMap& mSFAs,
+                          const CUtensorMap& mSFBs, unsigned grid,
                           cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kQ == GEMM_W8 ? NUM_THREADS_FP8 : NUM_THREADS);
-    cfg.dynamicSmemBytes = smem_bytes<kPair, BN, kShort, chunks_per_stage<kShort, kQ>()>();
+    cfg.blockDim = dim3(threads_of<kQ>());
+    cfg.dynamicSmemBytes = smem_bytes<kPair, BN, kShort, chunks_per_stage<kShort, kQ>(), sf_stage_bytes<kQ>()>();
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     int n = 0;
@@ -941,12 +1090,14 @@ cudaError_t launch_kernel(const GemmParams& p, const CUtensorMap& mA, const CUte
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
-    char name[32];
+    char name[MOE_LAUNCH_LABEL_BYTES];
     snprintf(name, sizeof(name), "grouped_gemm_%s_n%d%s%s%s", kFC1 ? "fc1" : "fc2", BN, kShort ? "_short" : "",
-             kPair ? "_pair" : "", kQ == GEMM_W8 ? "_w8" : (kQ == GEMM_W8A8 ? "_w8a8" : ""));
+             kPair ? "_pair" : "",
+             kQ == GEMM_W8 ? "_w8" : (kQ == GEMM_W8A8 ? "_w8a8" : (kQ == GEMM_NVFP4 ? "_nvfp4" : "")));
     const cudaError_t e = note_launch(name, s);
     if (e != cudaSuccess) return e;
-    return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<kFC1, kPair, BN, kShort, kQ>, p, mA, mB, mAs, mBs, mA32, mAs32);
+    return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<kFC1, kPair, BN, kShort, kQ>, p, mA, mB, mAs, mBs, mA32, mAs32,
+                              mSFA, mSFB, mSFAs, mSFBs);
 }
 
 // Tensor maps, parameters and grid of one launch with MMA N = BN.
@@ -956,20 +1107,34 @@ cudaError_t launch_bn(const GemmLaunch& L, int num_sms, int64_t bound, cudaStrea
     const bool has_shared = L.T_sh > 0 && L.b_sh != nullptr && L.N_out_sh > 0;
     // B boxes: FC1 loads gate and up halves of BN/2 rows; FC2 BN rows (pair: 128)
     const uint32_t brows = kFC1 ? BN / 2 : (kPair ? BN / 2 : BN);
-    CUtensorMap mA, mB, mAs, mBs, mA32, mAs32;
+    CUtensorMap mA, mB, mAs, mBs, mA32, mAs32, mSFA, mSFB, mSFAs, mSFBs;
     bool ok = true;
     constexpr bool a8 = kQ == GEMM_W8A8;
+    constexpr bool f4 = kQ == GEMM_NVFP4;
+    // operand rows in bytes: K bf16 / E4M3 elements, or K / 2 bytes of packed E2M1
+    const uint64_t ka = f4 ? (uint64_t)L.K / 2 : (uint64_t)L.K;
+    const uint64_t ka_sh = f4 ? (uint64_t)L.K_sh / 2 : (uint64_t)L.K_sh;
+    const bool u8 = a8 || f4;
+    const uint32_t sfa_rows = kShort ? BM_SHORT : BM;
     if (has_routed) {
-        ok = ok && encode_2d(&mA, L.a, (uint64_t)L.K, (uint64_t)L.rows_cap, BM, a8);
-        ok = ok && encode_2d(&mA32, L.a, (uint64_t)L.K, (uint64_t)L.rows_cap, BM_SHORT, a8);
+        ok = ok && encode_2d(&mA, L.a, ka, (uint64_t)L.rows_cap, BM, u8);
+        ok = ok && encode_2d(&mA32, L.a, ka, (uint64_t)L.rows_cap, BM_SHORT, u8);
         ok = ok && (kQ == GEMM_W8 ? encode_3d_u8(&mB, L.b, (uint64_t)L.K, (uint64_t)L.Nb, (uint64_t)L.G, brows)
-                                  : encode_3d(&mB, L.b, (uint64_t)L.K, (uint64_t)L.Nb, (uint64_t)L.G, brows, a8));
+                                  : encode_3d(&mB, L.b, ka, (uint64_t)L.Nb, (uint64_t)L.G, brows, u8));
+        if (f4) {
+            ok = ok && encode_sf(&mSFA, L.a_sf, nvfp4_sf_row_bytes(L.K), (uint64_t)L.rows_cap, 1, sfa_rows);
+            ok = ok && encode_sf(&mSFB, L.b_sf, nvfp4_sf_row_bytes(L.K), (uint64_t)L.Nb, (uint64_t)L.G, brows);
+        }
     }
     if (has_shared) {
-        ok = ok && encode_2d(&mAs, L.a_sh, (uint64_t)L.K_sh, (uint64_t)L.T_sh, BM, a8);
-        ok = ok && encode_2d(&mAs32, L.a_sh, (uint64_t)L.K_sh, (uint64_t)L.T_sh, BM_SHORT, a8);
+        ok = ok && encode_2d(&mAs, L.a_sh, ka_sh, (uint64_t)L.T_sh, BM, u8);
+        ok = ok && encode_2d(&mAs32, L.a_sh, ka_sh, (uint64_t)L.T_sh, BM_SHORT, u8);
         ok = ok && (kQ == GEMM_W8 ? encode_3d_u8(&mBs, L.b_sh, (uint64_t)L.K_sh, (uint64_t)L.Nb_sh, 1, brows)
-                                  : encode_3d(&mBs, L.b_sh, (uint64_t)L.K_sh, (uint64_t)L.Nb_sh, 1, brows, a8));
+                                  : encode_3d(&mBs, L.b_sh, ka_sh, (uint64_t)L.Nb_sh, 1, brows, u8));
+        if (f4) {
+            ok = ok && encode_sf(&mSFAs, L.a_sf_sh, nvfp4_sf_row_bytes(L.K_sh), (uint64_t)L.T_sh, 1, sfa_rows);
+            ok = ok && encode_sf(&mSFBs, L.b_sf_sh, nvfp4_sf_row_bytes(L.K_sh), (uint64_t)L.Nb_sh, 1, brows);
+        }
     }
     if (!ok) {
         *why = "cuTensorMapEncodeTiled failed";
@@ -979,11 +1144,22 @@ cudaError_t launch_bn(const GemmLaunch& L, int num_sms, int64_t bound, cudaStrea
         mA = mAs;
         mA32 = mAs32;
         mB = mBs;
+        if (f4) {
+            mSFA = mSFAs;
+            mSFB = mSFBs;
+        }
     }
     if (!has_shared) {
         mAs = mA;
         mAs32 = mA32;
         mBs = mB;
+        if (f4) {
+            mSFAs = mSFA;
+            mSFBs = mSFB;
+        }
+    }
+    if (!f4) {  // unused by the other formats
+        mSFA = mSFB = mSFAs = mSFBs = mA;
     }
     GemmParams p;
     p.offsets = L.offsets;
@@ -1002,7 +1178,7 @@ cudaError_t launch_bn(const GemmLaunch& L, int num_sms, int64_t bound, cudaStrea
     p.a_scale_sh = L.a_scale_sh;
     // K steps: 64 bf16 or 128 E4M3 elements (one 128-byte row); a ragged last step
     // of E4M3 operands is zero-filled by the TMA past K
-    const int ke = a8 ? 2 * BK : BK;
+    const int ke = f4 ? 4 * BK : (a8 ? 2 * BK : BK);
     p.kb_total = (L.K + ke - 1) / ke;
     p.kb_total_sh = (L.K_sh + ke - 1) / ke;
     p.Nb = L.Nb;
@@ -1034,7 +1210,8 @@ cudaError_t launch_bn(const GemmLaunch& L, int num_sms, int64_t bound, cudaStrea
     } else {
         grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(bound, num_sms));
     }
-    err = launch_kernel<kFC1, kPair, BN, kShort, kQ>(p, mA, mB, mAs, mBs, mA32, mAs32, grid, s);
+    err = launch_kernel<kFC1, kPair, BN, kShort, kQ>(p, mA, mB, mAs, mBs, mA32, mAs32, mSFA, mSFB, mSFAs, mSFBs, grid,
+                                                    s);
     if (err != cudaSuccess) *why = "launch failed";
     return err;
 }
@@ -1065,6 +1242,14 @@ cudaError_t dispatch(const GemmLaunch& L, int num_sms, cudaStream_t s, const cha
         if (L.max_group_rows <= BM_SHORT && L.T_sh <= BM_SHORT)
             return launch_bn<kFC1, false, 256, true, GEMM_W8>(L, num_sms, b256, s, why);
         return launch_bn<kFC1, false, 256, false, GEMM_W8>(L, num_sms, b256, s, why);
+    }
+    if (L.quant == GEMM_NVFP4) {
+        // E2M1 operands with block scales: single CTAs, N = 128 (the accumulators and
+        // the scales' tensor-memory columns fit one allocation)
+        const int64_t b128 = tile_bound(L, 128);
+        if (L.max_group_rows <= BM_SHORT && L.T_sh <= BM_SHORT)
+            return launch_bn<kFC1, false, 128, true, GEMM_NVFP4>(L, num_sms, b128, s, why);
+        return launch_bn<kFC1, false, 128, false, GEMM_NVFP4>(L, num_sms, b128, s, why);
     }
     if (L.quant == GEMM_W8A8) {
         // E4M3 operands: single CTAs, tile widths chosen as for bf16

@@ -15,7 +15,7 @@ namespace moe {
 // ---------------------------------------------------------------------------
 // Workspace header (first kWsHeaderBytes bytes of every workspace)
 // ---------------------------------------------------------------------------
-constexpr size_t kWsHeaderBytes = 256;
+constexpr size_t kWsHeaderBytes = MOE_WS_HEADER_BYTES;
 struct WsHeader {
     int32_t status;              // OR of MOE_ERR_DEVICE_BOUNDS / MOE_ERR_TIMEOUT
     int32_t pad0;
@@ -239,6 +239,34 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, ui
         : "memory");
 }
 
+// D[tmem] (+)= (A x SFA)[smem] * (B x SFB)[smem]^T, packed E2M1 inputs with one
+// E4M3 scale per 16 elements (kind::mxf4nvf4, scale_vec::4X; K = 64 per
+// instruction: 32 bytes of a 128-byte row), fp32 accumulation.  The scales of
+// the instruction's 4 K blocks sit in 4 tensor-memory columns from sfa / sfb:
+// row r's four scale bytes (K-block order) in lane r % 32 of every lane
+// quarter, column r / 32.
+__device__ __forceinline__ void tc_mma_nvfp4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Copy 32 rows x 16 bytes of shared memory (rows contiguous, from a 16-byte
+// aligned address) into 4 tensor-memory columns from `taddr`, row i to lane i of
+// every lane quarter.
+__device__ __forceinline__ void tc_copy_32x128b_x4(uint32_t taddr, uint32_t smem_addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)(128 >> 4) << 32;  // 8-row core matrices of 16-byte rows, 128 bytes apart
+    d |= (uint64_t)1 << 46;           // descriptor version
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(d) : "memory");
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T, E4M3 inputs (kind::f8f6f4, K = 32 per
 // instruction: 32 bytes of a 128-byte row, as for bf16), fp32 accumulation.
 __device__ __forceinline__ void tc_mma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
@@ -342,6 +370,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
            | ((uint32_t)(M >> 4) << 24);          // M / 16
 }
 
+// Instruction descriptor of tcgen05.mma.kind::mxf4nvf4: E2M1 A and B (format
+// code 1, K-major), E4M3 block scales (scale format 0), fp32 D, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_nvfp4(int M, int N) {
+    return (1u << 7)                              // A format: E2M1
+           | (1u << 10)                           // B format: E2M1
+           | ((uint32_t)(N >> 3) << 17)           // N / 8
+           | ((uint32_t)(M >> 4) << 24);          // M / 16
+}
+
 // Instruction descriptor of tcgen05.mma.kind::f8f6f4: E4M3 A and B (format
 // code 0 in both fields, both K-major), fp32 D, shape M x N.
 __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
@@ -424,8 +461,15 @@ struct GemmLaunch {
     const float* b_scale_sh;   // [Nb_sh] row scales of b_sh (E4M3 B only)
     const float* a_scale;      // [rows_cap] row scales of a (GEMM_W8A8 only)
     const float* a_scale_sh;   // [T_sh] row scales of a_sh (GEMM_W8A8 only)
+    // GEMM_NVFP4: a, b, a_sh, b_sh hold packed E2M1 codes ([rows][K/2] bytes), these
+    // their E4M3 block scales ([rows][nvfp4_sf_row_bytes(K)] bytes); b_scale / a_scale
+    // hold the fp32 row scales
+    const uint8_t* a_sf = nullptr;
+    const uint8_t* a_sf_sh = nullptr;
+    const uint8_t* b_sf = nullptr;
+    const uint8_t* b_sf_sh = nullptr;
 };
-enum { GEMM_BF16 = 0, GEMM_W8 = 1, GEMM_W8A8 = 2 };
+enum { GEMM_BF16 = 0, GEMM_W8 = 1, GEMM_W8A8 = 2, GEMM_NVFP4 = 3 };
 cudaError_t launch_grouped_gemm(const GemmLaunch& L, int num_sms, cudaStream_t s, const char** why);
 
 struct FinalizeLaunch {
@@ -468,6 +512,25 @@ struct ActQuantSeg {
 cudaError_t launch_quantize_act_rows(const ActQuantSeg* seg, int nseg, int num_sms, cudaStream_t s);
 cudaError_t launch_quantize_fp8_rows(const uint16_t* w, int64_t rows, int K, uint8_t* q, float* scale, int num_sms,
                                      cudaStream_t s);
+
+// NVFP4 quantisation of bf16 rows [rows, K] (K a multiple of 64): packed E2M1
+// codes [rows][K/2], E4M3 block scales [rows][16 * ceil(K / 256)] (zero past
+// K / 16) and fp32 row scales [rows]; pow2: power-of-two row scales
+// (activations), else amax / 2688 (weights).  A segment with rows_dev takes
+// min(rows, *rows_dev) rows, read on the device.
+struct Nvfp4QuantSeg {
+    const uint16_t* src;
+    int64_t rows;
+    const int32_t* rows_dev;
+    int K;
+    int pow2;
+    uint8_t* q;
+    uint8_t* sb;
+    float* scale;
+};
+cudaError_t launch_quantize_nvfp4_rows(const Nvfp4QuantSeg* seg, int nseg, int num_sms, cudaStream_t s);
+// bytes of one row of NVFP4 block scales
+__host__ __device__ constexpr int nvfp4_sf_row_bytes(int K) { return 16 * ((K + 255) / 256); }
 
 // Whether kernels are launched with programmatic stream serialization (set by
 // moe_set_pdl; defined in moe_api.cu).

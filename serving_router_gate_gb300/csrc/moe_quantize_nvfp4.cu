@@ -1,0 +1,139 @@
+// moe_quantize_nvfp4.cu -- NVFP4 quantisation of expert weights and of expert
+// activations, rows at a time.
+//
+// The TensorRT-LLM AutoDeploy MoE PR #10985 (review of torch_moe.py) names NVFP4
+// paths of the MoE ops and defines no encoding.  Reading: E2M1 elements, one
+// E4M3 scale per 16 consecutive elements of a row, one fp32 scale per row.
+// For a row with largest magnitude amax the row scale is s = amax / 2688 (one
+// binary32 division; 2688 = 6 * 448) -- or, for activations, the power of two
+// s = 2^e with e the smallest integer >= -126 such that amax <= 2688 * 2^e.
+// Each block b of 16 elements gets sb = e4m3(bmax / (6 s)) (the product and the
+// division in binary32, to nearest with ties to even, saturating at 448), and
+// each element q = e2m1(v / (sb * s)) (the product and the division in
+// binary32, to nearest with ties to the even code, saturating at 6).  An
+// all-zero row gets s = 0 (weights) and zero scales and codes; a block whose
+// scale rounds to zero gets zero codes.
+//
+// Layout written: codes [rows][K/2] bytes, element 2i in the low nibble of byte
+// i and 2i + 1 in the high one; block scales [rows][SFW] bytes with
+// SFW = 16 * ceil(K / 256) (blocks past K/16 are zero: a row of block scales is
+// a whole number of 16-byte pieces, one per 256 elements, the unit a GEMM
+// pipeline stage reads); row scales [rows] fp32.
+//
+// One warp per row: the row maximum (an unsigned maximum of the bf16 patterns
+// with the sign cleared), then lane l takes blocks l, l + 32, ...: two 16-byte
+// loads of its 16 values, the block maximum, the block scale and 16 codes
+// written as 8 bytes.
+#include <cuda_fp4.h>
+#include <cuda_fp8.h>
+
+#include <algorithm>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int Q4_WARPS = 8;
+
+__device__ __forceinline__ uint32_t absmax_bf16x8(uint32_t m, const uint4& v) {
+    m = __vmaxu2(m, v.x & 0x7FFF7FFFu);
+    m = __vmaxu2(m, v.y & 0x7FFF7FFFu);
+    m = __vmaxu2(m, v.z & 0x7FFF7FFFu);
+    return __vmaxu2(m, v.w & 0x7FFF7FFFu);
+}
+
+__device__ __forceinline__ float packed_max_to_float(uint32_t m) {
+    const uint32_t hi = m >> 16, lo = m & 0xFFFFu;
+    return __uint_as_float((hi > lo ? hi : lo) << 16);
+}
+
+// the power of two 2^e, e the smallest integer >= -126 with amax <= 2688 * 2^e:
+// with amax = f * 2^E (1 <= f < 2) and 2688 = 1.3125 * 2^11, e = E - 11 when
+// f <= 1.3125, else E - 10
+__device__ __forceinline__ float pow2_row_scale(float amax) {
+    const uint32_t b = __float_as_uint(amax);
+    int e = (int)(b >> 23) - 127 - 11 + ((b & 0x7FFFFFu) > 0x280000u ? 1 : 0);
+    if (e < -126) e = -126;
+    return __uint_as_float((uint32_t)(e + 127) << 23);
+}
+
+__device__ __forceinline__ float e4m3_value(uint8_t code) {
+    const __half_raw h = __nv_cvt_fp8_to_halfraw(code, __NV_E4M3);
+    return __half2float(__half(h));
+}
+
+// two values -> two E2M1 codes in one byte (the first in the low nibble)
+__device__ __forceinline__ uint32_t e2m1x2(float a, float b) {
+    return (uint32_t)__nv_cvt_float2_to_fp4x2(make_float2(a, b), __NV_E2M1, cudaRoundNearest);
+}
+
+__global__ void __launch_bounds__(Q4_WARPS * 32) quantize_nvfp4_rows_kernel(const __grid_constant__ Nvfp4QuantSeg seg0,
+                                                                           const __grid_constant__ Nvfp4QuantSeg seg1,
+                                                                           int nseg) {
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = (int64_t)blockIdx.x * Q4_WARPS + (threadIdx.x >> 5);
+    const int64_t nw = (int64_t)gridDim.x * Q4_WARPS;
+    for (int sidx = 0; sidx < nseg; ++sidx) {
+        const Nvfp4QuantSeg& sg = sidx == 0 ? seg0 : seg1;
+        int64_t rows = sg.rows;
+        if (sg.rows_dev) rows = min(rows, (int64_t)max(0, *sg.rows_dev));
+        const int K = sg.K;
+        const int nblk = K / 16;
+        const int sfw = nvfp4_sf_row_bytes(K);
+        for (int64_t r = gw; r < rows; r += nw) {
+            const uint4* src = reinterpret_cast<const uint4*>(sg.src + r * K);
+            uint32_t pm = 0;
+            for (int v = lane; v < K / 8; v += 32) pm = absmax_bf16x8(pm, __ldg(src + v));
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) pm = __vmaxu2(pm, __shfl_xor_sync(0xffffffffu, pm, off));
+            const float amax = packed_max_to_float(pm);
+            const float s = sg.pow2 ? pow2_row_scale(amax) : __fdiv_rn(amax, 2688.0f);
+            if (lane == 0) sg.scale[r] = s;
+            uint8_t* qrow = sg.q + r * (K / 2);
+            uint8_t* sbrow = sg.sb + r * sfw;
+            for (int b = lane; b < sfw; b += 32) {
+                if (b >= nblk) {  // padding of the block-scale row
+                    sbrow[b] = 0;
+                    continue;
+                }
+                const uint4 v0 = __ldg(src + 2 * b), v1 = __ldg(src + 2 * b + 1);
+                const float bmax = packed_max_to_float(absmax_bf16x8(absmax_bf16x8(0u, v0), v1));
+                uint8_t code = 0;
+                if (s != 0.0f) code = __nv_cvt_float_to_fp8(__fdiv_rn(bmax, __fmul_rn(6.0f, s)), __NV_SATFINITE, __NV_E4M3);
+                sbrow[b] = code;
+                const float denom = __fmul_rn(e4m3_value(code), s);
+                float f[16];
+                unpack8(v0, f);
+                unpack8(v1, f + 8);
+                uint32_t w[2] = {0u, 0u};
+                if (denom != 0.0f) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const uint32_t byte = e2m1x2(__fdiv_rn(f[2 * i], denom), __fdiv_rn(f[2 * i + 1], denom));
+                        w[i >> 2] |= byte << (8 * (i & 3));
+                    }
+                }
+                *reinterpret_cast<uint2*>(qrow + 8 * b) = make_uint2(w[0], w[1]);
+            }
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_nvfp4_rows(const Nvfp4QuantSeg* seg, int nseg, int num_sms, cudaStream_t s) {
+    if (nseg < 1 || nseg > 2) return cudaErrorInvalidValue;
+    int64_t rows = 0;
+    for (int i = 0; i < nseg; ++i) rows = std::max<int64_t>(rows, seg[i].rows);
+    if (rows <= 0) return cudaSuccess;
+    const int64_t want = (rows + Q4_WARPS - 1) / Q4_WARPS;
+    const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms * 8));
+    const Nvfp4QuantSeg empty = seg[0];
+    return launch_k("quantize_nvfp4_rows", quantize_nvfp4_rows_kernel, dim3(grid), dim3(Q4_WARPS * 32), 0, s, seg[0],
+                    nseg > 1 ? seg[1] : empty, nseg);
+}
+
+}  // namespace moe

@@ -14,8 +14,9 @@ from typing import Optional
 
 import torch
 
-from . import (MOE_NONLOCAL_SKIP, moe_forward, moe_forward_fp8, moe_forward_w8a8, moe_permute,
-               moe_quantize_fp8_rows, moe_route, moe_route_grouped, moe_workspace_init, moe_workspace_size)
+from . import (MOE_NONLOCAL_SKIP, moe_forward, moe_forward_fp8, moe_forward_nvfp4, moe_forward_w8a8, moe_permute,
+               moe_quantize_fp8_rows, moe_quantize_nvfp4_rows, moe_route, moe_route_grouped, moe_workspace_init,
+               moe_workspace_size, nvfp4_sf_row_bytes)
 
 
 class MoELayer:
@@ -26,7 +27,7 @@ class MoELayer:
                  nonlocal_mode: int = MOE_NONLOCAL_SKIP, W1s: Optional[torch.Tensor] = None,
                  W2s: Optional[torch.Tensor] = None, shared_gate_w: Optional[torch.Tensor] = None,
                  on_input: bool = False, n_group: int = 1, topk_group: int = 1, fp8: bool = False,
-                 act8: bool = False):
+                 act8: bool = False, fp4: bool = False):
         self.Wg, self.W1, self.W2 = Wg, W1, W2
         # routing applied on the input: rows scaled by the weights, outputs summed unweighted
         self.on_input = bool(on_input)
@@ -77,6 +78,25 @@ class MoELayer:
             if W1s is not None:
                 self.W1sq, self.s1s = quant(W1s)
                 self.W2sq, self.s2s = quant(W2s)
+        # NVFP4 experts (E2M1 codes, E4M3 block scales, fp32 row scales), quantised once here;
+        # the activations are quantised inside moe_forward_nvfp4
+        self.fp4 = bool(fp4)
+        if self.fp4 and self.fp8:
+            raise ValueError("one weight format at a time")
+        self.W1f = self.W2f = self.W1sf = self.W2sf = None
+        if self.fp4:
+            def quant4(w):
+                K = w.shape[-1]
+                q = torch.empty(w.shape[:-1] + (K // 2,), dtype=torch.uint8, device=dev)
+                sb = torch.empty(w.shape[:-1] + (nvfp4_sf_row_bytes(K),), dtype=torch.uint8, device=dev)
+                sc = torch.empty(w.shape[:-1], dtype=torch.float32, device=dev)
+                moe_quantize_nvfp4_rows(w, q, sb, sc, pow2=False)
+                return q, sb, sc
+            self.W1f = quant4(W1)
+            self.W2f = quant4(W2)
+            if W1s is not None:
+                self.W1sf = quant4(W1s)
+                self.W2sf = quant4(W2s)
 
     def views(self, T: int) -> dict:
         k = self.k
@@ -104,7 +124,14 @@ class MoELayer:
         v = self.views(x.shape[0])
         w = None if self.on_input else v["topk_w"]
         xs = x if (self.I_sh > 0) else None
-        if self.fp8:
+        if self.fp4:
+            (q1, f1, s1), (q2, f2, s2) = self.W1f, self.W2f
+            q1s = f1s = s1s = q2s = f2s = s2s = None
+            if self.W1sf is not None:
+                (q1s, f1s, s1s), (q2s, f2s, s2s) = self.W1sf, self.W2sf
+            moe_forward_nvfp4(v["x_perm"], v["offsets"], q1, f1, s1, q2, f2, s2, v["pair_row"], w, xs, q1s, f1s, s1s,
+                              q2s, f2s, s2s, self.gate, v["out"], self.ws, stream)
+        elif self.fp8:
             fwd = moe_forward_w8a8 if self.act8 else moe_forward_fp8
             # E4M3 activations: x also lets large batches quantise each token row once
             xa = x if self.act8 else xs
@@ -175,4 +202,4 @@ def layer_from_inputs(inp: dict, device="cuda", max_T: Optional[int] = None, loc
                     rep_offset=d(inp["rep_offset"]), rep_slots=d(inp["rep_slots"]), S=cfg.slots,
                     local_start=local_start, local_count=local_count, nonlocal_mode=nonlocal_mode,
                     W1s=d(W1s), W2s=d(W2s), shared_gate_w=d(inp["w_s"]), on_input=on_input,
-                    n_group=cfg.n_group, topk_group=cfg.topk_group, fp8=cfg.fp8, act8=cfg.act8)
+                    n_group=cfg.n_group, topk_group=cfg.topk_group, fp8=cfg.fp8, act8=cfg.act8, fp4=cfg.fp4)

@@ -109,15 +109,47 @@ def oracle_layer(inp_cpu: dict, local_start=0, local_count=-1, mode=0, tokens=No
             q1s, s1s = oracle.quantize_fp8_rows(W1s)
             q2s, s2s = oracle.quantize_fp8_rows(W2s)
             fp8.update(W1sq=q1s, s1s=s1s, W2sq=q2s, s2s=s2s)
+    nvfp4 = None
+    if cfg.fp4:
+        nvfp4 = nvfp4_weights(W1, W2, W1s, W2s)
+        if W1s is not None:
+            from moe_inputs import shared_concat
+            c1, c2 = shared_concat(W1s, W2s)
+            W1s, W2s = c1[None], c2[None]
     kw = dict(rep_offset=inp_cpu["rep_offset"], rep_slots=inp_cpu["rep_slots"], local_start=local_start,
               local_count=local_count, mode=mode, W1s=W1s, W2s=W2s,
               shared_gate_w=inp_cpu["w_s"], n_group=cfg.n_group, topk_group=cfg.topk_group, on_input=on_input,
-              fp8=fp8)
+              fp8=fp8, nvfp4=nvfp4)
     if tokens is None:
         return oracle.moe_layer(inp_cpu["x"], inp_cpu["Wg"], inp_cpu["bias"], cfg.k, cfg.renorm, W1, W2,
                                 S=cfg.slots, **kw)
     return oracle.moe_tokens(inp_cpu["x"], inp_cpu["Wg"], inp_cpu["bias"], cfg.k, cfg.renorm, W1, W2,
                              tokens=tokens, **kw)
+
+
+def nvfp4_weights(W1, W2, W1s=None, W2s=None):
+    """The oracle's NVFP4 quantisation of the expert weights (the shared experts as the one
+    concatenated MLP the GPU runs: its row and block scales depend on that layout), with
+    NVFP4 activations."""
+    d = {}
+    d["W1q"], d["W1sb"], d["s1"] = oracle.quantize_nvfp4_rows(W1)
+    d["W2q"], d["W2sb"], d["s2"] = oracle.quantize_nvfp4_rows(W2)
+    if W1s is not None:
+        from moe_inputs import shared_concat
+        c1, c2 = shared_concat(W1s, W2s)
+        d["W1sq"], d["W1ssb"], d["s1s"] = oracle.quantize_nvfp4_rows(c1[None])
+        d["W2sq"], d["W2ssb"], d["s2s"] = oracle.quantize_nvfp4_rows(c2[None])
+    d["act4"] = True
+    return d
+
+
+def unpack_e2m1(q: np.ndarray) -> np.ndarray:
+    """Packed E2M1 bytes [..., K/2] -> one code per element [..., K] (low nibble first)."""
+    q = np.asarray(q, np.uint8)
+    out = np.empty(q.shape[:-1] + (2 * q.shape[-1],), np.uint8)
+    out[..., 0::2] = q & 0xF
+    out[..., 1::2] = q >> 4
+    return out
 
 
 def oracle_routing(inp_cpu: dict, local_start=0, local_count=-1, mode=0):

@@ -1,0 +1,145 @@
+"""GPU parity of the NVFP4 experts (E2M1 weights and activations, E4M3 scales per
+16 elements, fp32 row scales; tcgen05.mma kind::mxf4nvf4) against the fp64 oracle.
+
+The quantiser must reproduce the oracle's codes, block scales and row scales
+bit for bit (weights with amax / 2688 row scales, activations with power-of-two
+ones).  The layer runs every routing variant on NVFP4 experts and must match
+the oracle's NVFP4 layer (which quantises the same activation rows) within the
+output tolerance of tests/parity_util.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as mi
+import oracle
+import serving_router_gate_gb300 as moe
+from serving_router_gate_gb300.layer import layer_from_inputs
+
+from parity_util import (check_out, check_routing, check_x_perm, make, oracle_layer, oracle_threads, run_gpu,
+                         sample_tokens, to_cpu, unpack_e2m1)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True, scope="module")
+def _threads():
+    oracle_threads()
+
+
+def _check(inp, local_start=0, local_count=-1, mode=0):
+    g = run_gpu(inp, local_start, local_count, mode)
+    ref = oracle_layer(to_cpu(inp), local_start, local_count, mode)
+    check_routing(g, dict(ids=ref["ids"], w=ref["w"], w_masked=ref["w_masked"], slots=ref["slots"],
+                          counts=ref["counts"], offsets=ref["offsets"], perm_src=ref["perm_src"],
+                          pair_row=ref["pair_row"]), to_cpu(inp), masked=local_count >= 0)
+    if not inp["cfg"].on_input:
+        check_x_perm(g, inp["x"].cuda(), inp["cfg"].k)
+    check_out(g["out"], ref["out"])
+    st = moe.moe_get_device_status(g["layer"].ws)
+    assert st == 0, f"device status {st}"
+    return g, ref
+
+
+def _quantize_gpu(v, pow2):
+    K = v.shape[-1]
+    d = v.cuda()
+    q = torch.empty(v.shape[:-1] + (K // 2,), dtype=torch.uint8, device="cuda")
+    sb = torch.full(v.shape[:-1] + (moe.nvfp4_sf_row_bytes(K),), 0xAB, dtype=torch.uint8, device="cuda")
+    sc = torch.empty(v.shape[:-1], dtype=torch.float32, device="cuda")
+    moe.moe_quantize_nvfp4_rows(d, q, sb, sc, pow2=pow2)
+    torch.cuda.synchronize()
+    return q.cpu().numpy(), sb.cpu().numpy(), sc.cpu().numpy()
+
+
+def _special_rows(K, g):
+    v = torch.randn(12, K, generator=g) * 0.02
+    v[0] = 0.0                                              # an all-zero row
+    v[1, : K // 2] = 0.0                                    # zero blocks in a live row
+    v[2] = torch.randn(K, generator=g) * 3000.0             # large values
+    v[3] = torch.full((K,), 2.0 ** -130)                    # bf16 subnormals
+    v[4] = torch.linspace(-6.0, 6.0, K)                     # many E2M1 ties at scale 1
+    v[5, 0] = 1.0                                           # one element dominating its row
+    v[6] = torch.randn(K, generator=g) * 1e-30
+    return v.to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("K", [64, 192, 1408, 2048])
+@pytest.mark.parametrize("pow2", [False, True])
+def test_quantize_nvfp4_rows_bit_exact(K, pow2):
+    g = torch.Generator().manual_seed(K + (1000 if pow2 else 0))
+    v = torch.cat([_special_rows(K, g), (torch.randn(100, K, generator=g) * 0.05).to(torch.bfloat16)])
+    q, sb, sc = _quantize_gpu(v, pow2)
+    rq, rsb, rsc = oracle.quantize_nvfp4_rows(v, pow2=pow2)
+    assert np.array_equal(unpack_e2m1(q), rq), "E2M1 codes differ"
+    assert np.array_equal(sb[:, : K // 16], rsb), "block scales differ"
+    assert not sb[:, K // 16:].any(), "block-scale padding is not zero"
+    assert np.array_equal(sc.view(np.uint32), rsc.view(np.uint32)), "row scales differ"
+
+
+def test_quantize_nvfp4_expert_stack_as_one_matrix():
+    inp = mi.make_inputs(mi.MoEConfig("q4stack", T=4, H=256, I=128, E=3, k=1, renorm=True))
+    q, sb, sc = _quantize_gpu(inp["W1"], False)
+    rq, rsb, rsc = oracle.quantize_nvfp4_rows(inp["W1"])
+    assert np.array_equal(unpack_e2m1(q), rq) and np.array_equal(sb[..., :16], rsb)
+    assert np.array_equal(sc.view(np.uint32), rsc.view(np.uint32))
+
+
+NV_MID = mi.MoEConfig("mid_nvfp4", T=1000, H=512, I=384, E=12, k=3, renorm=True, n_shared=1, I_shared=256,
+                      shared_gate=True, fp4=True)
+
+
+def test_nvfp4_mid_layer():
+    _check(mi.make_inputs(NV_MID))
+
+
+def test_nvfp4_ragged_k_partial_tiles_two_shared_experts():
+    # FC2's K = I = 320: a stage of 256 elements and a second one zero-filled past K;
+    # H = 320: partial N tiles; two shared experts
+    cfg = mi.MoEConfig("odd_nvfp4", T=200, H=320, I=320, E=5, k=2, renorm=False, n_shared=2, I_shared=192,
+                       fp4=True)
+    _check(mi.make_inputs(cfg))
+
+
+@pytest.mark.parametrize("T", [1, 5, 32])
+def test_nvfp4_small_batches(T):
+    cfg = mi.MoEConfig(f"sb_nvfp4_{T}", T=T, H=512, I=256, E=16, k=4, renorm=True, n_shared=2, I_shared=256,
+                       fp4=True)
+    _check(mi.make_inputs(cfg))
+
+
+def test_nvfp4_local_ranges_routing_on_input_and_replicas():
+    inp = mi.make_inputs(NV_MID)
+    _check(inp, 4, 5, moe.MOE_NONLOCAL_SKIP)
+    _check(inp, 4, 5, moe.MOE_NONLOCAL_MOD)
+    _check(mi.make_inputs(NV_MID.with_(name="mid_nvfp4_oi", on_input=True)))
+    rep = mi.MoEConfig("rep_nvfp4", T=700, H=256, I=256, E=10, S=13, n_hot=3, zipf_s=1.1, k=4, renorm=True,
+                       fp4=True)
+    _check(mi.make_inputs(rep))
+
+
+def test_nvfp4_zero_tokens_determinism_and_poisoned_workspace():
+    layer = layer_from_inputs(mi.make_inputs(NV_MID), "cuda")
+    assert layer.forward(torch.zeros((0, NV_MID.H), dtype=torch.bfloat16, device="cuda")).shape[0] == 0
+    x = mi.make_inputs(NV_MID)["x"].cuda()
+    a = layer.forward(x).clone()
+    layer.ws[moe.MOE_WS_HEADER_BYTES:].fill_(0xFF)  # nothing the forward reads may come from before it
+    b = layer.forward(x).clone()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert moe.moe_get_device_status(layer.ws) == 0
+
+
+@pytest.mark.parametrize("name", ["dsv2_lite_like_decode_t1_nvfp4", "dsv2_lite_like_decode_t32_nvfp4"])
+def test_nvfp4_decode_full(name):
+    _check(make(name))
+
+
+def test_nvfp4_qwen2_moe_like_prefill_full_size():
+    cfg = mi.CONFIGS["qwen2_moe_like_prefill_nvfp4"]
+    inp = mi.make_inputs(cfg, device="cpu", weights_device="cuda")
+    inp_cpu = to_cpu(inp)
+    g = run_gpu(inp)
+    tok = sample_tokens(cfg.T, 32)
+    part = oracle_layer(inp_cpu, tokens=tok)
+    check_out(g["out"][tok], part["out"])
+    assert moe.moe_get_device_status(g["layer"].ws) == 0

@@ -25,7 +25,7 @@ _BUFS = ("topk_ids", "topk_w", "slot_ids", "counts", "offsets", "perm_src", "pai
 def _fill(layer, byte):
     for name in _BUFS:
         getattr(layer, name).view(torch.uint8).fill_(byte)
-    layer.ws[256:].fill_(byte)  # the header (status word, counters) stays
+    layer.ws[moe.MOE_WS_HEADER_BYTES:].fill_(byte)  # the header (status word, counters) stays
 
 
 def _forward(layer, x, byte):
