@@ -344,6 +344,7 @@ MOE_API moe_status_t moe_quantize_act_rows(const moe_bf16_t *v, int64_t rows, in
  *       W2_scale [S_local, H] fp32
  *   W1sq [2*I_shared_total, H/2], W1s_sf, W1s_scale; W2sq [H, I_shared_total/2],
  *       W2s_sf, W2s_scale (the shared experts as one concatenated MLP; NULL if none)
+ * H, I and I_shared_total at most 16384 (MOE_ERR_UNSUPPORTED otherwise).
  * x_perm must be 16-byte aligned.  Launches two quantisation kernels besides
  * moe_forward's three; their scratch is part of moe_workspace_size.  Everything
  * else as moe_forward. */
@@ -361,7 +362,8 @@ MOE_API moe_status_t moe_forward_nvfp4(const moe_bf16_t *x_perm, const int32_t *
  * per 256 elements). */
 #define MOE_NVFP4_SF_ROW_BYTES(K) (16 * (((K) + 255) / 256))
 
-/* NVFP4 quantisation of a bf16 matrix v [rows, K] (K a multiple of 64), as
+/* NVFP4 quantisation of a bf16 matrix v [rows, K] (K a multiple of 64, at most
+ * 16384; MOE_ERR_UNSUPPORTED otherwise), as
  * moe_forward_nvfp4 reads it.  Per row: the row scale s = amax / 2688 (one
  * binary32 division; pow2 = 0, for weights) or the smallest power of two 2^e,
  * e >= -126, with amax <= 2688 * 2^e (pow2 = 1, for activations); per block of

@@ -654,6 +654,9 @@ moe_status_t moe_forward_w8a8(const moe_bf16_t* x_perm, const int32_t* offsets, 
                         stream, true);
 }
 
+// longest row the NVFP4 quantiser takes (its CTA holds a row in registers)
+constexpr int kNvfp4MaxK = 16384;
+
 // One grouped GEMM on NVFP4 operands (packed E2M1 codes, E4M3 block scales, fp32
 // row scales): the routed problem (A rows a, weights b per group) and the shared
 // one (a_sh, b_sh).
@@ -711,7 +714,7 @@ static moe_status_t gemm_call_nvfp4(bool fc1, const Nvfp4Operands& o, int64_t ro
 moe_status_t moe_quantize_nvfp4_rows(const moe_bf16_t* v, int64_t rows, int K, int pow2, uint8_t* q, uint8_t* sb,
                                      float* scale, moe_stream_t stream) {
     if (rows < 0 || K <= 0 || (pow2 != 0 && pow2 != 1)) return MOE_ERR_INVALID_ARG;
-    if (K % 64 != 0) return MOE_ERR_UNSUPPORTED;
+    if (K % 64 != 0 || K > kNvfp4MaxK) return MOE_ERR_UNSUPPORTED;
     if (rows == 0) return MOE_OK;
     if (!v || !q || !sb || !scale) return MOE_ERR_INVALID_ARG;
     if (!aligned(v, 16) || !aligned(q, 8)) return MOE_ERR_INVALID_ARG;
@@ -730,7 +733,7 @@ moe_status_t moe_forward_nvfp4(const moe_bf16_t* x_perm, const int32_t* offsets,
     if (T < 0 || k <= 0 || S_local <= 0 || P_cap < 0 || H <= 0 || I <= 0 || I_shared_total < 0)
         return MOE_ERR_INVALID_ARG;
     if (!dim_ok(H) || !dim_ok(I) || (I_shared_total > 0 && !dim_ok(I_shared_total)) || k > 32 || S_local > 1024 ||
-        P_cap >= (int64_t(1) << 31))
+        P_cap >= (int64_t(1) << 31) || H > kNvfp4MaxK || I > kNvfp4MaxK || I_shared_total > kNvfp4MaxK)
         return MOE_ERR_UNSUPPORTED;
     if (T == 0) return MOE_OK;
     if (!x_perm || !offsets || !W1q || !W1_sf || !W1_scale || !W2q || !W2_sf || !W2_scale || !pair_row || !out)

@@ -20,10 +20,10 @@
 // a whole number of 16-byte pieces, one per 256 elements, the unit a GEMM
 // pipeline stage reads); row scales [rows] fp32.
 //
-// One warp per row: the row maximum (an unsigned maximum of the bf16 patterns
-// with the sign cleared), then lane l takes blocks l, l + 32, ...: two 16-byte
-// loads of its 16 values, the block maximum, the block scale and 16 codes
-// written as 8 bytes.
+// One CTA per row: each thread loads whole blocks (two 16-byte loads of 16
+// values), the row maximum is an unsigned maximum of the bf16 patterns with the
+// sign cleared (block-reduced), then each thread writes its blocks' scales and
+// codes (16 codes as 8 bytes).
 #include <cuda_fp4.h>
 #include <cuda_fp8.h>
 
@@ -33,8 +33,6 @@
 
 namespace moe {
 namespace {
-
-constexpr int Q4_WARPS = 8;
 
 __device__ __forceinline__ uint32_t absmax_bf16x8(uint32_t m, const uint4& v) {
     m = __vmaxu2(m, v.x & 0x7FFF7FFFu);
@@ -68,14 +66,19 @@ __device__ __forceinline__ uint32_t e2m1x2(float a, float b) {
     return (uint32_t)__nv_cvt_float2_to_fp4x2(make_float2(a, b), __NV_E2M1, cudaRoundNearest);
 }
 
-__global__ void __launch_bounds__(Q4_WARPS * 32) quantize_nvfp4_rows_kernel(const __grid_constant__ Nvfp4QuantSeg seg0,
-                                                                           const __grid_constant__ Nvfp4QuantSeg seg1,
-                                                                           int nseg) {
+// One CTA per row (grid-stride over rows): thread i holds blocks i, i + 256, ... of
+// the row in registers (up to Q4_MAXB of them), so a single pass over global memory
+// gives the row maximum (a block reduction), the block scales and the codes.
+constexpr int Q4_THREADS = 256;
+constexpr int Q4_MAXB = 4;  // blocks per thread: rows of up to 4 * 256 * 16 = 16384 elements
+
+__global__ void __launch_bounds__(Q4_THREADS) quantize_nvfp4_rows_kernel(const __grid_constant__ Nvfp4QuantSeg seg0,
+                                                                        const __grid_constant__ Nvfp4QuantSeg seg1,
+                                                                        int nseg) {
+    __shared__ uint32_t red[Q4_THREADS / 32];
     pdl_wait();
     pdl_trigger();
-    const int lane = threadIdx.x & 31;
-    const int64_t gw = (int64_t)blockIdx.x * Q4_WARPS + (threadIdx.x >> 5);
-    const int64_t nw = (int64_t)gridDim.x * Q4_WARPS;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int sidx = 0; sidx < nseg; ++sidx) {
         const Nvfp4QuantSeg& sg = sidx == 0 ? seg0 : seg1;
         int64_t rows = sg.rows;
@@ -83,40 +86,59 @@ __global__ void __launch_bounds__(Q4_WARPS * 32) quantize_nvfp4_rows_kernel(cons
         const int K = sg.K;
         const int nblk = K / 16;
         const int sfw = nvfp4_sf_row_bytes(K);
-        for (int64_t r = gw; r < rows; r += nw) {
+        for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
             const uint4* src = reinterpret_cast<const uint4*>(sg.src + r * K);
+            uint4 v[Q4_MAXB][2];
+            uint32_t bm[Q4_MAXB];
             uint32_t pm = 0;
-            for (int v = lane; v < K / 8; v += 32) pm = absmax_bf16x8(pm, __ldg(src + v));
+#pragma unroll
+            for (int j = 0; j < Q4_MAXB; ++j) {
+                const int b = tid + j * Q4_THREADS;
+                if (b < nblk) {
+                    v[j][0] = __ldg(src + 2 * b);
+                    v[j][1] = __ldg(src + 2 * b + 1);
+                    bm[j] = absmax_bf16x8(absmax_bf16x8(0u, v[j][0]), v[j][1]);
+                    pm = __vmaxu2(pm, bm[j]);
+                }
+            }
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) pm = __vmaxu2(pm, __shfl_xor_sync(0xffffffffu, pm, off));
+            if (lane == 0) red[warp] = pm;
+            __syncthreads();
+            pm = red[0];
+#pragma unroll
+            for (int w = 1; w < Q4_THREADS / 32; ++w) pm = __vmaxu2(pm, red[w]);
+            __syncthreads();  // red is rewritten for the next row
             const float amax = packed_max_to_float(pm);
             const float s = sg.pow2 ? pow2_row_scale(amax) : __fdiv_rn(amax, 2688.0f);
-            if (lane == 0) sg.scale[r] = s;
+            if (tid == 0) sg.scale[r] = s;
             uint8_t* qrow = sg.q + r * (K / 2);
             uint8_t* sbrow = sg.sb + r * sfw;
-            for (int b = lane; b < sfw; b += 32) {
+#pragma unroll
+            for (int j = 0; j < Q4_MAXB; ++j) {
+                const int b = tid + j * Q4_THREADS;
+                if (b >= sfw) continue;
                 if (b >= nblk) {  // padding of the block-scale row
                     sbrow[b] = 0;
                     continue;
                 }
-                const uint4 v0 = __ldg(src + 2 * b), v1 = __ldg(src + 2 * b + 1);
-                const float bmax = packed_max_to_float(absmax_bf16x8(absmax_bf16x8(0u, v0), v1));
+                const float bmax = packed_max_to_float(bm[j]);
                 uint8_t code = 0;
                 if (s != 0.0f) code = __nv_cvt_float_to_fp8(__fdiv_rn(bmax, __fmul_rn(6.0f, s)), __NV_SATFINITE, __NV_E4M3);
                 sbrow[b] = code;
                 const float denom = __fmul_rn(e4m3_value(code), s);
                 float f[16];
-                unpack8(v0, f);
-                unpack8(v1, f + 8);
-                uint32_t w[2] = {0u, 0u};
+                unpack8(v[j][0], f);
+                unpack8(v[j][1], f + 8);
+                uint32_t w2[2] = {0u, 0u};
                 if (denom != 0.0f) {
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const uint32_t byte = e2m1x2(__fdiv_rn(f[2 * i], denom), __fdiv_rn(f[2 * i + 1], denom));
-                        w[i >> 2] |= byte << (8 * (i & 3));
+                        w2[i >> 2] |= byte << (8 * (i & 3));
                     }
                 }
-                *reinterpret_cast<uint2*>(qrow + 8 * b) = make_uint2(w[0], w[1]);
+                *reinterpret_cast<uint2*>(qrow + 8 * b) = make_uint2(w2[0], w2[1]);
             }
         }
     }
@@ -129,10 +151,11 @@ cudaError_t launch_quantize_nvfp4_rows(const Nvfp4QuantSeg* seg, int nseg, int n
     int64_t rows = 0;
     for (int i = 0; i < nseg; ++i) rows = std::max<int64_t>(rows, seg[i].rows);
     if (rows <= 0) return cudaSuccess;
-    const int64_t want = (rows + Q4_WARPS - 1) / Q4_WARPS;
-    const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms * 8));
+    for (int i = 0; i < nseg; ++i)
+        if (seg[i].K / 16 > Q4_THREADS * Q4_MAXB) return cudaErrorInvalidValue;
+    const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(rows, (int64_t)num_sms * 8));
     const Nvfp4QuantSeg empty = seg[0];
-    return launch_k("quantize_nvfp4_rows", quantize_nvfp4_rows_kernel, dim3(grid), dim3(Q4_WARPS * 32), 0, s, seg[0],
+    return launch_k("quantize_nvfp4_rows", quantize_nvfp4_rows_kernel, dim3(grid), dim3(Q4_THREADS), 0, s, seg[0],
                     nseg > 1 ? seg[1] : empty, nseg);
 }
 
