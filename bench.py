@@ -13,8 +13,12 @@ flushed before every timed step, outside the step's own CUDA events.  The
 per-kernel breakdown and the roofline of the dominant kernel come from a
 second pass that replays a CUDA graph of the same forward captured with the
 library's launch-event hook armed: a CUDA event node on the launching stream
-right before every kernel and one after the last.  With N > 1 (torchrun), every
-rank runs its own independent batch (weak scaling, no collective on the data path).
+right before every kernel and one after the last.  With N > 1 (torchrun, or
+started by this script), the ranks split the layer by experts (--partition ep,
+the default: every rank routes the same batch, computes its contiguous slot
+range and its shard of the shared experts, and one all-reduce sums the
+partials; strong scaling) or run independent batches (--partition replicas;
+weak scaling, no collective).
 `--impl reference` times the fp64 CPU oracle on a bounded sample instead.
 """
 from __future__ import annotations
@@ -394,6 +398,19 @@ def run_cpu_baseline(inp_dev, cfg, target_s=10.0, T_cap=None):
                 single_thread_sample=f"first {n1} tokens, {t1:.1f} s on one thread"), t
 
 
+def _ep_layer(inp, cfg, world, rank, dev):
+    """This rank's expert-parallel layer over the workload's inputs."""
+    from serving_router_gate_gb300.expert_parallel import EPMoELayer
+    W1s = W2s = None
+    if inp["W1s"] is not None:
+        W1s, W2s = mi.shared_concat(inp["W1s"], inp["W2s"])
+    d = lambda t: None if t is None else t.to(dev).contiguous()  # noqa: E731
+    return EPMoELayer(d(inp["Wg"]), d(inp["W1"]), d(inp["W2"]), cfg.k, cfg.renorm, cfg.T, world, rank,
+                      logit_bias=d(inp["bias"]), rep_offset=d(inp["rep_offset"]), rep_slots=d(inp["rep_slots"]),
+                      W1s=d(W1s), W2s=d(W2s), shared_gate_w=d(inp["w_s"]), on_input=cfg.on_input,
+                      n_group=cfg.n_group, topk_group=cfg.topk_group, fp8=cfg.fp8, act8=cfg.act8, fp4=cfg.fp4)
+
+
 def bench_ours(args):
     import serving_router_gate_gb300 as moe
     from serving_router_gate_gb300.layer import layer_from_inputs
@@ -402,7 +419,11 @@ def bench_ours(args):
     cfg = mi.CONFIGS[args.workload]
     dev = torch.device("cuda", local)
     inp = mi.make_inputs(cfg, device=dev)
-    layer = layer_from_inputs(inp, dev)
+    # expert parallelism (more than one rank): every rank routes the whole batch, computes
+    # its slot range and shared shard, and one all-reduce sums the partials; otherwise
+    # (replicas) every rank runs its own batch through the whole layer
+    ep = _ep_layer(inp, cfg, ws_, rank, dev) if (args.partition == "ep" and ws_ > 1) else None
+    layer = ep.layer if ep is not None else layer_from_inputs(inp, dev)
     x = inp["x"]
     T, H = cfg.T, cfg.H
     stream = torch.cuda.current_stream()
@@ -430,14 +451,16 @@ def bench_ours(args):
     # recorded on the stream around each replay also time the graph's own launch, a
     # cost a model-level graph pays once per model step rather than once per layer;
     # both are reported.
-    inner = _external_events() if args.graph else None
-    if args.graph:
+    graph_ok = args.graph and ep is None  # the expert-parallel step runs eagerly (NCCL in the step)
+    inner = _external_events() if graph_ok else None
+    if graph_ok:
         pre = (lambda: inner[0].record()) if inner else None
         post = (lambda: inner[1].record()) if inner else None
         graph = layer.capture(x, pre=pre, post=post)
     else:
         graph = None
-    step = graph.replay if graph is not None else (lambda: layer.forward(x))
+    step = graph.replay if graph is not None else ((lambda: ep.forward(x)) if ep is not None
+                                                   else (lambda: layer.forward(x)))
     for _ in range(W):
         step()
 
@@ -474,7 +497,12 @@ def bench_ours(args):
         (ms_local, ms_replay_local), clk = timed_region()
         if clk is not None:
             clk["remeasured_after"] = first
-    value, ms = aggregate_throughput(T, ms_local, ws_)
+    if ep is not None:
+        # one batch of T tokens for the whole job (strong scaling)
+        ms = max_over_ranks(ms_local, ws_)
+        value = T / (ms * 1e-3)
+    else:
+        value, ms = aggregate_throughput(T, ms_local, ws_)
     ms_replay = max_over_ranks(ms_replay_local, ws_)
 
     # ---- per-kernel pass: the same forward, every kernel between its own events ----
@@ -491,13 +519,16 @@ def bench_ours(args):
     x_dev = torch.empty_like(x)
     h2d = lambda: x_dev.copy_(x_pin, non_blocking=True)  # noqa: E731
     d2h = lambda: out_pin.copy_(layer.out[:T], non_blocking=True)  # noqa: E731
-    if args.graph:
+    if graph_ok:
         g_e2e = layer.capture(x_dev, pre=h2d, post=d2h)
         e2e_step = g_e2e.replay
     else:
         def e2e_step():
             h2d()
-            layer.forward(x_dev)
+            if ep is not None:
+                layer.out[:T].copy_(ep.forward(x_dev))
+            else:
+                layer.forward(x_dev)
             d2h()
     for _ in range(W):
         e2e_step()
@@ -546,10 +577,11 @@ def bench_ours(args):
                       "timed steps, each after an L2 flush")
     roof["work"] = per_unit
 
-    total_tokens = T * ws_
+    total_tokens = T if ep is not None else T * ws_
     res = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws_, "steps": K,
-        "warmup": W, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "warmup": W, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "strong" if ep is not None else "weak", "vs_baseline": None,
         "step_timing": ("device time of one forward: CUDA events recorded by external event nodes at the "
                         "head and tail of the forward's graph, mean of the K steps" if inner else
                         "CUDA events on the stream around each step"),
@@ -558,8 +590,10 @@ def bench_ours(args):
         "dtype": "nvfp4" if cfg.fp4 else ("e4m3" if cfg.act8 else "bf16"), "data": "synthetic: seeded N(0,1) activations, N(0,sigma) random-init weights of the "
                                  "workload's shapes (no checkpoint)",
         "config": {"workload": cfg.name, "shape": mi.describe(cfg), "tokens_per_gpu": T,
-                   "parallelism": f"replicas x{ws_} (independent token batches, no collective)",
-                   "cuda_graph": bool(args.graph),
+                   "parallelism": (f"expert parallel x{ws_} (contiguous slot ranges, shared-expert shards, one "
+                                   f"fp32 all-reduce of the partials)" if ep is not None else
+                                   f"replicas x{ws_} (independent token batches, no collective)"),
+                   "cuda_graph": bool(graph_ok),
                    "l2": f"flushed before every timed step ({flush.describe()}); each step timed by "
                          f"its own CUDA events, flush outside them"},
         "roofline": roof,
@@ -646,6 +680,9 @@ def main():
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="launch every step from Python instead of replaying a CUDA graph of one step")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--partition", choices=["ep", "replicas"], default="ep",
+                    help="with more than one rank: expert parallelism over one batch (default) or independent "
+                         "replicas, each with its own batch")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
