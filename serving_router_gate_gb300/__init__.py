@@ -62,13 +62,15 @@ class MoEError(RuntimeError):
 
 
 def lib_path() -> str:
-    return _build.LIB_PATH
+    """The library this process loads: the bounds-checked build when MOE_CHECKED=1."""
+    return _build.CHECKED_LIB_PATH if os.environ.get("MOE_CHECKED") == "1" else _build.LIB_PATH
 
 
 def _load():
-    path = _build.LIB_PATH
+    path = lib_path()
     if not os.path.exists(path):
-        raise ImportError(f"CUDA library not built: {path} is missing (run serving_router_gate_gb300._build.build())")
+        raise ImportError(f"CUDA library not built: {path} is missing (run serving_router_gate_gb300._build.build("
+                          f"{'checked=True' if path == _build.CHECKED_LIB_PATH else ''}))")
     lib = ctypes.CDLL(path)
     P, i32, i64, sz, u64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_uint64
     sig = {

@@ -2,7 +2,11 @@
 
 Each translation unit under csrc/ is compiled in parallel, then linked into one
 shared library next to this file (_lib/libmoe_gb300.so).  Rebuilds only when a
-source or header is newer than the library.
+source or header is newer than the library.  build(checked=True) makes the
+bounds-checked variant (_lib/libmoe_gb300_checked.so, compiled with
+-DMOE_CHECKED: kernels test data-dependent global indexes and report
+MOE_ERR_DEVICE_BOUNDS instead of accessing out of range), which the binding
+loads when the environment variable MOE_CHECKED is 1.
 """
 from __future__ import annotations
 
@@ -18,6 +22,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_lib")
 LIB_PATH = os.path.join(OUT_DIR, "libmoe_gb300.so")
+CHECKED_LIB_PATH = os.path.join(OUT_DIR, "libmoe_gb300_checked.so")
 OBJ_DIR = os.path.join(HERE, "_build")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -40,23 +45,26 @@ def _deps():
     return _sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+def up_to_date(lib: str = LIB_PATH) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
-    if not force and up_to_date():
-        return LIB_PATH
+def build(force: bool = False, verbose: bool = False, extra_flags=None, checked: bool = False) -> str:
+    lib = CHECKED_LIB_PATH if checked else LIB_PATH
+    if not force and up_to_date(lib):
+        return lib
     nvcc = _nvcc()
+    obj_dir = OBJ_DIR + ("_checked" if checked else "")
     os.makedirs(OUT_DIR, exist_ok=True)
-    os.makedirs(OBJ_DIR, exist_ok=True)
-    flags = ARCH + NVCC_FLAGS + ["-I", INCLUDE, "-I", CSRC] + list(extra_flags or [])
+    os.makedirs(obj_dir, exist_ok=True)
+    flags = ARCH + NVCC_FLAGS + ["-I", INCLUDE, "-I", CSRC] + list(extra_flags or []) + (
+        ["-DMOE_CHECKED"] if checked else [])
 
     def compile_one(src):
-        obj = os.path.join(OBJ_DIR, os.path.basename(src) + ".o")
+        obj = os.path.join(obj_dir, os.path.basename(src) + ".o")
         cmd = [nvcc, *flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -68,13 +76,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
     srcs = _sources()
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 4))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-Xcompiler", "-fPIC", "-cudart", "static", *objs, "-o", tmp]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -8,6 +8,8 @@
 #include <string>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "moe_internal.cuh"
 
 using namespace moe;
@@ -134,6 +136,16 @@ moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE
 
 }  // namespace
 
+// An NVTX range around each entry point of the ABI (a profiler's timeline shows
+// which call enqueued which kernels; without a tool attached it costs a check).
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
+#define MOE_NVTX(name) NvtxRange moe_nvtx_range_(name)
+
 bool moe::pdl_enabled() { return g_pdl.load() != 0 && g_ev_armed.load() == 0; }
 
 cudaError_t moe::note_launch(const char* name, cudaStream_t s) {
@@ -215,11 +227,13 @@ size_t moe_workspace_size(int64_t max_T, int H, int I, int E, int S, int k, int 
 }
 
 moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream) {
+    MOE_NVTX("moe_workspace_init");
     if (!ws || ws_bytes < kWsHeaderBytes) return MOE_ERR_WORKSPACE;
     return cuda_status(cudaMemsetAsync(ws, 0, kWsHeaderBytes, (cudaStream_t)stream));
 }
 
 moe_status_t moe_get_device_status(void* ws, moe_stream_t stream, int32_t* device_status) {
+    MOE_NVTX("moe_get_device_status");
     if (!ws || !device_status) return MOE_ERR_INVALID_ARG;
     WsHeader* hdr = static_cast<WsHeader*>(ws);
     int32_t v = 0;
@@ -233,6 +247,7 @@ moe_status_t moe_get_device_status(void* ws, moe_stream_t stream, int32_t* devic
 }
 
 moe_status_t moe_get_route_stats(void* ws, moe_stream_t stream, int64_t* refined_tokens) {
+    MOE_NVTX("moe_get_route_stats");
     if (!ws || !refined_tokens) return MOE_ERR_INVALID_ARG;
     WsHeader* hdr = static_cast<WsHeader*>(ws);
     unsigned long long v = 0;
@@ -275,12 +290,14 @@ static moe_status_t route_impl(const moe_bf16_t* x, const float* gate_w, const f
 moe_status_t moe_route(const moe_bf16_t* x, const float* gate_w, const float* logit_bias, int64_t T, int H, int E,
                        int k, int renorm, int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes,
                        moe_stream_t stream) {
+    MOE_NVTX("moe_route");
     return route_impl(x, gate_w, logit_bias, T, H, E, k, renorm, 1, 1, topk_ids, topk_w, ws, ws_bytes, stream);
 }
 
 moe_status_t moe_route_grouped(const moe_bf16_t* x, const float* gate_w, const float* logit_bias, int64_t T, int H,
                                int E, int k, int renorm, int n_group, int topk_group, int32_t* topk_ids,
                                float* topk_w, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    MOE_NVTX("moe_route_grouped");
     if (n_group < 1 || n_group > 32 || E % n_group != 0 || topk_group < 1 || topk_group > n_group ||
         k > topk_group * (E / n_group))
         return MOE_ERR_INVALID_ARG;
@@ -344,6 +361,7 @@ moe_status_t moe_permute(const int32_t* topk_ids, float* topk_w, int64_t T, int 
                          const moe_bf16_t* x, int H, int32_t* slot_ids, int32_t* counts, int32_t* offsets,
                          int32_t* perm_src, int32_t* pair_row, moe_bf16_t* x_perm, void* ws, size_t ws_bytes,
                          moe_stream_t stream) {
+    MOE_NVTX("moe_permute");
     return permute_impl(false, topk_ids, topk_w, T, k, E, rep_offset, rep_slots, S, local_start, local_count,
                         nonlocal_mode, x, H, slot_ids, counts, offsets, perm_src, pair_row, x_perm, ws, ws_bytes,
                         stream);
@@ -354,6 +372,7 @@ moe_status_t moe_permute_on_input(const int32_t* topk_ids, float* topk_w, int64_
                                   int local_count, int nonlocal_mode, const moe_bf16_t* x, int H, int32_t* slot_ids,
                                   int32_t* counts, int32_t* offsets, int32_t* perm_src, int32_t* pair_row,
                                   moe_bf16_t* x_perm, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    MOE_NVTX("moe_permute_on_input");
     return permute_impl(true, topk_ids, topk_w, T, k, E, rep_offset, rep_slots, S, local_start, local_count,
                         nonlocal_mode, x, H, slot_ids, counts, offsets, perm_src, pair_row, x_perm, ws, ws_bytes,
                         stream);
@@ -420,6 +439,7 @@ moe_status_t moe_grouped_fc1(const moe_bf16_t* a, int64_t rows_cap, const int32_
                              const moe_bf16_t* W1, int H, int I, const moe_bf16_t* a_shared, int64_t T,
                              const moe_bf16_t* W1s, int I_shared_total, moe_bf16_t* h, moe_bf16_t* h_shared,
                              void* ws, size_t ws_bytes, moe_stream_t stream) {
+    MOE_NVTX("moe_grouped_fc1");
     moe_status_t st = check_gemm_args(a, rows_cap, offsets, G, W1, H, I, a_shared, T, W1s, I_shared_total, h,
                                       h_shared, ws, ws_bytes);
     if (st != MOE_OK) return st;
@@ -431,6 +451,7 @@ moe_status_t moe_grouped_fc2(const moe_bf16_t* h, int64_t rows_cap, const int32_
                              const moe_bf16_t* W2, int H, int I, const moe_bf16_t* h_shared, int64_t T,
                              const moe_bf16_t* W2s, int I_shared_total, moe_bf16_t* y, moe_bf16_t* y_shared,
                              void* ws, size_t ws_bytes, moe_stream_t stream) {
+    MOE_NVTX("moe_grouped_fc2");
     moe_status_t st = check_gemm_args(h, rows_cap, offsets, G, W2, H, I, h_shared, T, W2s, I_shared_total, y,
                                       y_shared, ws, ws_bytes);
     if (st != MOE_OK) return st;
@@ -464,6 +485,7 @@ moe_status_t moe_grouped_fc1_fp8(const moe_bf16_t* a, int64_t rows_cap, const in
                                  const uint8_t* W1q, const float* W1_scale, int H, int I, const moe_bf16_t* a_shared,
                                  int64_t T, const uint8_t* W1sq, const float* W1s_scale, int I_shared_total,
                                  moe_bf16_t* h, moe_bf16_t* h_shared, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    MOE_NVTX("moe_grouped_fc1_fp8");
     moe_status_t st = check_gemm_args(a, rows_cap, offsets, G, reinterpret_cast<const moe_bf16_t*>(W1q), H, I,
                                       a_shared, T, reinterpret_cast<const moe_bf16_t*>(W1sq), I_shared_total, h,
                                       h_shared, ws, ws_bytes);
@@ -478,6 +500,7 @@ moe_status_t moe_grouped_fc2_fp8(const moe_bf16_t* h, int64_t rows_cap, const in
                                  const uint8_t* W2q, const float* W2_scale, int H, int I, const moe_bf16_t* h_shared,
                                  int64_t T, const uint8_t* W2sq, const float* W2s_scale, int I_shared_total,
                                  moe_bf16_t* y, moe_bf16_t* y_shared, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    MOE_NVTX("moe_grouped_fc2_fp8");
     moe_status_t st = check_gemm_args(h, rows_cap, offsets, G, reinterpret_cast<const moe_bf16_t*>(W2q), H, I,
                                       h_shared, T, reinterpret_cast<const moe_bf16_t*>(W2sq), I_shared_total, y,
                                       y_shared, ws, ws_bytes);
@@ -493,6 +516,7 @@ moe_status_t moe_grouped_fc1_w8a8(const uint8_t* aq, const float* a_scale, int64
                                   const uint8_t* a_shared_q, const float* a_shared_scale, int64_t T, const uint8_t* W1sq,
                                   const float* W1s_scale, int I_shared_total, moe_bf16_t* h, moe_bf16_t* h_shared,
                                   void* ws, size_t ws_bytes, moe_stream_t stream) {
+    MOE_NVTX("moe_grouped_fc1_w8a8");
     const moe_bf16_t* a = reinterpret_cast<const moe_bf16_t*>(aq);
     const moe_bf16_t* a_sh = reinterpret_cast<const moe_bf16_t*>(a_shared_q);
     moe_status_t st = check_gemm_args(a, rows_cap, offsets, G, reinterpret_cast<const moe_bf16_t*>(W1q), H, I, a_sh, T,
@@ -511,6 +535,7 @@ moe_status_t moe_grouped_fc2_w8a8(const uint8_t* hq, const float* h_scale, int64
                                   const uint8_t* h_shared_q, const float* h_shared_scale, int64_t T,
                                   const uint8_t* W2sq, const float* W2s_scale, int I_shared_total, moe_bf16_t* y,
                                   moe_bf16_t* y_shared, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    MOE_NVTX("moe_grouped_fc2_w8a8");
     const moe_bf16_t* a = reinterpret_cast<const moe_bf16_t*>(hq);
     const moe_bf16_t* a_sh = reinterpret_cast<const moe_bf16_t*>(h_shared_q);
     moe_status_t st = check_gemm_args(a, rows_cap, offsets, G, reinterpret_cast<const moe_bf16_t*>(W2q), H, I, a_sh, T,
@@ -528,6 +553,7 @@ moe_status_t moe_finalize(const moe_bf16_t* y, int64_t rows_cap, const int32_t* 
                           int64_t T, int k, int H, const moe_bf16_t* y_shared, const moe_bf16_t* x,
                           const moe_bf16_t* shared_gate_w, moe_bf16_t* out, void* ws, size_t ws_bytes,
                           moe_stream_t stream) {
+    MOE_NVTX("moe_finalize");
     if (T < 0 || k <= 0 || H <= 0 || rows_cap < 0) return MOE_ERR_INVALID_ARG;
     if (!dim_ok(H) || k > 32) return MOE_ERR_UNSUPPORTED;
     if (T == 0) return MOE_OK;
@@ -626,6 +652,7 @@ moe_status_t moe_forward(const moe_bf16_t* x_perm, const int32_t* offsets, int S
                          const float* topk_w, int64_t T, int k, const moe_bf16_t* x, const moe_bf16_t* W1s,
                          const moe_bf16_t* W2s, int I_shared_total, const moe_bf16_t* shared_gate_w, moe_bf16_t* out,
                          void* ws, size_t ws_bytes, moe_stream_t stream) {
+    MOE_NVTX("moe_forward");
     return forward_impl(x_perm, offsets, S_local, P_cap, W1, nullptr, W2, nullptr, H, I, pair_row, topk_w, T, k, x,
                         W1s, nullptr, W2s, nullptr, I_shared_total, shared_gate_w, out, ws, ws_bytes, stream);
 }
@@ -636,6 +663,7 @@ moe_status_t moe_forward_fp8(const moe_bf16_t* x_perm, const int32_t* offsets, i
                              const moe_bf16_t* x, const uint8_t* W1sq, const float* W1s_scale, const uint8_t* W2sq,
                              const float* W2s_scale, int I_shared_total, const moe_bf16_t* shared_gate_w,
                              moe_bf16_t* out, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    MOE_NVTX("moe_forward_fp8");
     if (!W1_scale || !W2_scale) return MOE_ERR_INVALID_ARG;
     return forward_impl(x_perm, offsets, S_local, P_cap, W1q, W1_scale, W2q, W2_scale, H, I, pair_row, topk_w, T, k,
                         x, W1sq, W1s_scale, W2sq, W2s_scale, I_shared_total, shared_gate_w, out, ws, ws_bytes,
@@ -648,6 +676,7 @@ moe_status_t moe_forward_w8a8(const moe_bf16_t* x_perm, const int32_t* offsets, 
                               const moe_bf16_t* x, const uint8_t* W1sq, const float* W1s_scale, const uint8_t* W2sq,
                               const float* W2s_scale, int I_shared_total, const moe_bf16_t* shared_gate_w,
                               moe_bf16_t* out, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    MOE_NVTX("moe_forward_w8a8");
     if (!W1_scale || !W2_scale) return MOE_ERR_INVALID_ARG;
     return forward_impl(x_perm, offsets, S_local, P_cap, W1q, W1_scale, W2q, W2_scale, H, I, pair_row, topk_w, T, k,
                         x, W1sq, W1s_scale, W2sq, W2s_scale, I_shared_total, shared_gate_w, out, ws, ws_bytes,
@@ -713,6 +742,7 @@ static moe_status_t gemm_call_nvfp4(bool fc1, const Nvfp4Operands& o, int64_t ro
 
 moe_status_t moe_quantize_nvfp4_rows(const moe_bf16_t* v, int64_t rows, int K, int pow2, uint8_t* q, uint8_t* sb,
                                      float* scale, moe_stream_t stream) {
+    MOE_NVTX("moe_quantize_nvfp4_rows");
     if (rows < 0 || K <= 0 || (pow2 != 0 && pow2 != 1)) return MOE_ERR_INVALID_ARG;
     if (K % 64 != 0 || K > kNvfp4MaxK) return MOE_ERR_UNSUPPORTED;
     if (rows == 0) return MOE_OK;
@@ -730,6 +760,7 @@ moe_status_t moe_forward_nvfp4(const moe_bf16_t* x_perm, const int32_t* offsets,
                                const uint8_t* W2s_sf, const float* W2s_scale, int I_shared_total,
                                const moe_bf16_t* shared_gate_w, moe_bf16_t* out, void* ws, size_t ws_bytes,
                                moe_stream_t stream) {
+    MOE_NVTX("moe_forward_nvfp4");
     if (T < 0 || k <= 0 || S_local <= 0 || P_cap < 0 || H <= 0 || I <= 0 || I_shared_total < 0)
         return MOE_ERR_INVALID_ARG;
     if (!dim_ok(H) || !dim_ok(I) || (I_shared_total > 0 && !dim_ok(I_shared_total)) || k > 32 || S_local > 1024 ||
@@ -780,6 +811,7 @@ moe_status_t moe_forward_nvfp4(const moe_bf16_t* x_perm, const int32_t* offsets,
 
 moe_status_t moe_quantize_act_rows(const moe_bf16_t* v, int64_t rows, int K, uint8_t* q, float* scale,
                                    moe_stream_t stream) {
+    MOE_NVTX("moe_quantize_act_rows");
     if (rows < 0 || K <= 0) return MOE_ERR_INVALID_ARG;
     if (K % 64 != 0) return MOE_ERR_UNSUPPORTED;
     if (rows == 0) return MOE_OK;
@@ -791,6 +823,7 @@ moe_status_t moe_quantize_act_rows(const moe_bf16_t* v, int64_t rows, int K, uin
 
 moe_status_t moe_quantize_fp8_rows(const moe_bf16_t* w, int64_t rows, int K, uint8_t* q, float* scale,
                                    moe_stream_t stream) {
+    MOE_NVTX("moe_quantize_fp8_rows");
     if (rows < 0 || K <= 0) return MOE_ERR_INVALID_ARG;
     if (K % 64 != 0) return MOE_ERR_UNSUPPORTED;
     if (rows == 0) return MOE_OK;

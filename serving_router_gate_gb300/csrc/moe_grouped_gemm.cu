@@ -689,7 +689,8 @@ __global__ void __launch_bounds__(threads_of<kQ>(), 1)
             // short-tile launches hold 32 A rows: a taller tile (a caller's bound was
             // wrong) is reported and only its first 32 rows are stored
             if (kShort && tl.rows_valid > BM_SHORT && row_in == 0) report(p.status, MOE_ERR_DEVICE_BOUNDS);
-            const bool valid = row_in < (kShort ? min(tl.rows_valid, BM_SHORT) : tl.rows_valid);
+            const bool valid = row_in < (kShort ? min(tl.rows_valid, BM_SHORT) : tl.rows_valid) &&
+                               in_bounds(tl.row0 + row_in, tl.prob ? p.T_sh : p.rows_cap, p.status);
             const int N_out = tl.prob ? p.N_out_sh : p.N_out;
             uint16_t* out = tl.prob ? p.out_sh : p.out;
             uint16_t* orow = out + (int64_t)(tl.row0 + row_in) * N_out;

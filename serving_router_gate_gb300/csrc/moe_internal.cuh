@@ -28,6 +28,20 @@ __device__ __forceinline__ void report(int32_t* status, int32_t code) {
     if (status) atomicOr(status, code);
 }
 
+// Bounds check of a global index that data (offsets, ranks, ids) decides.  The
+// library built with MOE_CHECKED tests 0 <= i < n, reports MOE_ERR_DEVICE_BOUNDS
+// and skips the access when it fails; the regular build assumes it (every such
+// index is derived from values the kernels validate where they are read).
+#ifdef MOE_CHECKED
+__device__ __forceinline__ bool in_bounds(int64_t i, int64_t n, int32_t* status) {
+    if (i >= 0 && i < n) return true;
+    report(status, MOE_ERR_DEVICE_BOUNDS);
+    return false;
+}
+#else
+__device__ __forceinline__ bool in_bounds(int64_t, int64_t, int32_t*) { return true; }
+#endif
+
 // ---------------------------------------------------------------------------
 // bf16 helpers (bit patterns in uint16_t)
 // ---------------------------------------------------------------------------

@@ -200,7 +200,8 @@ __device__ __forceinline__ void scatter_pairs(int64_t pb, const uint16_t* __rest
                                               const int32_t* __restrict__ slot_ids, const int32_t* __restrict__ rank,
                                               const int32_t* __restrict__ chunk_base, int S_local, int64_t P, int k,
                                               int H, int32_t* __restrict__ pair_row, int32_t* __restrict__ perm_src,
-                                              uint16_t* __restrict__ x_perm, const float* __restrict__ wsc) {
+                                              uint16_t* __restrict__ x_perm, const float* __restrict__ wsc,
+                                              int32_t* status) {
     const int lane = threadIdx.x & 31;
     const int vec = H / 8;
     int32_t row = -1;
@@ -210,6 +211,9 @@ __device__ __forceinline__ void scatter_pairs(int64_t pb, const uint16_t* __rest
         const int32_t s = slot_ids[p];
         if (s >= 0) {
             row = chunk_base[(p / PM_CHUNK) * S_local + s] + rank[p];
+            if (!in_bounds(row, P, status)) row = -1;
+        }
+        if (row >= 0) {
             perm_src[row] = (int32_t)p;
             if (wsc) wp = wsc[p];
         }
@@ -278,12 +282,12 @@ __global__ void __launch_bounds__(256) permute_scatter_kernel(const uint16_t* __
                                                               int32_t* __restrict__ pair_row,
                                                               int32_t* __restrict__ perm_src,
                                                               uint16_t* __restrict__ x_perm,
-                                                              const float* __restrict__ wsc) {
+                                                              const float* __restrict__ wsc, int32_t* status) {
     pdl_wait();
     pdl_trigger();
     const int warp = threadIdx.x >> 5;
     for (int64_t pb = ((int64_t)blockIdx.x * 8 + warp) * PS_PAIRS; pb < P; pb += (int64_t)gridDim.x * 8 * PS_PAIRS)
-        scatter_pairs(pb, x, slot_ids, rank, chunk_base, S_local, P, k, H, pair_row, perm_src, x_perm, wsc);
+        scatter_pairs(pb, x, slot_ids, rank, chunk_base, S_local, P, k, H, pair_row, perm_src, x_perm, wsc, status);
 }
 
 // ---- one CTA for small batches: the three phases with block barriers ----
@@ -313,7 +317,7 @@ __global__ void __launch_bounds__(PM_SCAN_THREADS) permute_small_kernel(
     if (!with_scatter) return;  // the rows are copied by permute_scatter_kernel over the whole GPU
     __syncthreads();
     for (int64_t pb = (int64_t)warp * PS_PAIRS; pb < P; pb += (int64_t)PM_SMALL_WARPS * PS_PAIRS)
-        scatter_pairs(pb, x, slot_ids, rank, chunk_base, S_local, P, k, H, pair_row, perm_src, x_perm, wsc);
+        scatter_pairs(pb, x, slot_ids, rank, chunk_base, S_local, P, k, H, pair_row, perm_src, x_perm, wsc, status);
 }
 
 // ---- one CTA for tiny batches (at most one chunk of pairs): every phase in shared
@@ -427,7 +431,8 @@ __global__ void __launch_bounds__(PT_THREADS) permute_tiny_kernel(
 
     for (int p = tid; p < P; p += PT_THREADS) {
         const int32_t sv = s_slot[p];
-        const int32_t row = sv >= 0 ? off[sv] + s_rank[p] : -1;
+        int32_t row = sv >= 0 ? off[sv] + s_rank[p] : -1;
+        if (row >= 0 && !in_bounds(row, P, status)) row = -1;
         pair_row[p] = row;
         if (row >= 0) perm_src[row] = p;
         s_row[p] = row;
@@ -511,7 +516,7 @@ cudaError_t launch_permute(const PermuteLaunch& L, int num_sms, cudaStream_t s) 
         const int64_t want = (P + 8 * PS_PAIRS - 1) / (8 * PS_PAIRS);
         const unsigned gs = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms * 8));
         return launch_k("permute_scatter", permute_scatter_kernel, dim3(gs), dim3(256), 0, s, L.x, L.slot_ids,
-                        L.rank, L.chunk_base, L.S_local, P, L.k, L.H, L.pair_row, L.perm_src, L.x_perm, wsc);
+                        L.rank, L.chunk_base, L.S_local, P, L.k, L.H, L.pair_row, L.perm_src, L.x_perm, wsc, status);
     }
     const unsigned g1 = (unsigned)((nchunks + PM_WARPS - 1) / PM_WARPS);
     const size_t smem = (size_t)PM_WARPS * L.S_local * sizeof(int32_t);
@@ -525,7 +530,7 @@ cudaError_t launch_permute(const PermuteLaunch& L, int num_sms, cudaStream_t s) 
     const int64_t want = (P + 8 * PS_PAIRS - 1) / (8 * PS_PAIRS);
     const unsigned g3 = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms * 8));
     return launch_k("permute_scatter", permute_scatter_kernel, dim3(g3), dim3(256), 0, s, L.x, L.slot_ids, L.rank,
-                    L.chunk_base, L.S_local, P, L.k, L.H, L.pair_row, L.perm_src, L.x_perm, wsc);
+                    L.chunk_base, L.S_local, P, L.k, L.H, L.pair_row, L.perm_src, L.x_perm, wsc, status);
 }
 
 }  // namespace moe
