@@ -20,10 +20,10 @@
 // a whole number of 16-byte pieces, one per 256 elements, the unit a GEMM
 // pipeline stage reads); row scales [rows] fp32.
 //
-// One CTA per row: each thread loads whole blocks (two 16-byte loads of 16
-// values), the row maximum is an unsigned maximum of the bf16 patterns with the
-// sign cleared (block-reduced), then each thread writes its blocks' scales and
-// codes (16 codes as 8 bytes).
+// A group of threads per row: each thread loads whole blocks (two 16-byte loads
+// of 16 values), the row maximum is an unsigned maximum of the bf16 patterns
+// with the sign cleared (reduced over the group), then each thread writes its
+// blocks' scales and codes (16 codes as 8 bytes).
 #include <cuda_fp4.h>
 #include <cuda_fp8.h>
 
@@ -66,9 +66,12 @@ __device__ __forceinline__ uint32_t e2m1x2(float a, float b) {
     return (uint32_t)__nv_cvt_float2_to_fp4x2(make_float2(a, b), __NV_E2M1, cudaRoundNearest);
 }
 
-// One CTA per row (grid-stride over rows): thread i holds blocks i, i + 256, ... of
-// the row in registers (up to Q4_MAXB of them), so a single pass over global memory
-// gives the row maximum (a block reduction), the block scales and the codes.
+// A group of G threads per row (G the row's block count rounded up to a multiple
+// of 32, at most 256; 256 / G rows per CTA): thread i of a group holds blocks
+// i, i + G, ... of its row in registers (up to Q4_MAXB of them), so a single pass
+// over global memory gives the row maximum (reduced over the group's warps), the
+// block scales and the codes.  Every thread runs the same number of row rounds, so
+// every barrier is reached by the whole CTA.
 constexpr int Q4_THREADS = 256;
 constexpr int Q4_MAXB = 4;  // blocks per thread: rows of up to 4 * 256 * 16 = 16384 elements
 
@@ -86,15 +89,22 @@ __global__ void __launch_bounds__(Q4_THREADS) quantize_nvfp4_rows_kernel(const _
         const int K = sg.K;
         const int nblk = K / 16;
         const int sfw = nvfp4_sf_row_bytes(K);
-        for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
-            const uint4* src = reinterpret_cast<const uint4*>(sg.src + r * K);
+        const int G = min(Q4_THREADS, (nblk + 31) / 32 * 32);  // threads per row
+        const int rpc = Q4_THREADS / G;                        // rows per CTA round
+        const int gi = tid / G, gt = tid - gi * G;             // this thread's group and place in it
+        const int w0 = gi * (G / 32), nwg = G / 32;            // the group's warps
+        for (int64_t r0 = (int64_t)blockIdx.x * rpc; r0 < rows; r0 += (int64_t)gridDim.x * rpc) {
+            const int64_t r = r0 + gi;
+            const bool live = gi < rpc && r < rows;
+            const uint4* src = reinterpret_cast<const uint4*>(sg.src + (live ? r : 0) * K);
             uint4 v[Q4_MAXB][2];
             uint32_t bm[Q4_MAXB];
             uint32_t pm = 0;
 #pragma unroll
             for (int j = 0; j < Q4_MAXB; ++j) {
-                const int b = tid + j * Q4_THREADS;
-                if (b < nblk) {
+                const int b = gt + j * G;
+                bm[j] = 0;
+                if (live && b < nblk) {
                     v[j][0] = __ldg(src + 2 * b);
                     v[j][1] = __ldg(src + 2 * b + 1);
                     bm[j] = absmax_bf16x8(absmax_bf16x8(0u, v[j][0]), v[j][1]);
@@ -105,18 +115,18 @@ __global__ void __launch_bounds__(Q4_THREADS) quantize_nvfp4_rows_kernel(const _
             for (int off = 16; off > 0; off >>= 1) pm = __vmaxu2(pm, __shfl_xor_sync(0xffffffffu, pm, off));
             if (lane == 0) red[warp] = pm;
             __syncthreads();
-            pm = red[0];
-#pragma unroll
-            for (int w = 1; w < Q4_THREADS / 32; ++w) pm = __vmaxu2(pm, red[w]);
-            __syncthreads();  // red is rewritten for the next row
+            pm = 0;
+            for (int w = 0; w < nwg; ++w) pm = __vmaxu2(pm, red[min(w0 + w, Q4_THREADS / 32 - 1)]);
+            __syncthreads();  // red is rewritten in the next round
+            if (!live) continue;
             const float amax = packed_max_to_float(pm);
             const float s = sg.pow2 ? pow2_row_scale(amax) : __fdiv_rn(amax, 2688.0f);
-            if (tid == 0) sg.scale[r] = s;
+            if (gt == 0) sg.scale[r] = s;
             uint8_t* qrow = sg.q + r * (K / 2);
             uint8_t* sbrow = sg.sb + r * sfw;
 #pragma unroll
             for (int j = 0; j < Q4_MAXB; ++j) {
-                const int b = tid + j * Q4_THREADS;
+                const int b = gt + j * G;
                 if (b >= sfw) continue;
                 if (b >= nblk) {  // padding of the block-scale row
                     sbrow[b] = 0;
@@ -153,7 +163,14 @@ cudaError_t launch_quantize_nvfp4_rows(const Nvfp4QuantSeg* seg, int nseg, int n
     if (rows <= 0) return cudaSuccess;
     for (int i = 0; i < nseg; ++i)
         if (seg[i].K / 16 > Q4_THREADS * Q4_MAXB) return cudaErrorInvalidValue;
-    const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(rows, (int64_t)num_sms * 8));
+    // rows per CTA round of the segment with the most rounds
+    int64_t rounds = 1;
+    for (int i = 0; i < nseg; ++i) {
+        const int nblk = seg[i].K / 16;
+        const int rpc = Q4_THREADS / std::min(Q4_THREADS, (nblk + 31) / 32 * 32);
+        rounds = std::max<int64_t>(rounds, (seg[i].rows + rpc - 1) / rpc);
+    }
+    const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(rounds, (int64_t)num_sms * 8));
     const Nvfp4QuantSeg empty = seg[0];
     return launch_k("quantize_nvfp4_rows", quantize_nvfp4_rows_kernel, dim3(grid), dim3(Q4_THREADS), 0, s, seg[0],
                     nseg > 1 ? seg[1] : empty, nseg);
