@@ -48,12 +48,12 @@ DEFAULT_WORKLOAD = "redundant_slots_prefill"
 # the recorded value.
 NCU_TRAFFIC = {
     # FC1 of the first forward, ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum:
-    # 822.21 MB read + 87.42 MB written
-    ("qwen2_moe_like_prefill", "7e9e213e91d0e978"): 909.63e6,
-    # 115.46 MB read + 2.99 MB written
-    ("dsv2_lite_like_decode_t1", "7e9e213e91d0e978"): 118.46e6,
-    # FC1 (E4M3 operands): 411.93 MB read + 81.52 MB written
-    ("qwen2_moe_like_prefill_w8a8", "7e9e213e91d0e978"): 493.45e6,
+    # 822.31 MB read + 87.85 MB written (algorithmic 914.36 MB)
+    ("qwen2_moe_like_prefill", "158e60acb8eccf05"): 910.16e6,
+    # 115.52 MB read + 2.81 MB written (algorithmic 115.40 MB)
+    ("dsv2_lite_like_decode_t1", "158e60acb8eccf05"): 118.33e6,
+    # 1105.56 MB read + 32.93 MB written (algorithmic 1090.52 MB)
+    ("redundant_slots_cut16", "158e60acb8eccf05"): 1138.49e6,
 }
 
 
@@ -62,7 +62,11 @@ NCU_TRAFFIC = {
 # dram bytes, its algorithmic FC1 bytes), applied to the full launch's algorithmic bytes.
 # Traffic grows in proportion: every slot's weight tile is streamed once and its A rows
 # stay in L2 across the slot's n-tiles, at either size.
-NCU_TRAFFIC_SCALED = {}
+NCU_TRAFFIC_SCALED = {
+    ("redundant_slots_prefill", "158e60acb8eccf05"): (
+        1138.49e6, 1090.52e6,
+        "one capture of FC1 on the 16-slot cut (T=1024, H=7168, I=2048, E=16, k=8: 512 rows per slot)"),
+}
 
 
 def _traffic(workload, src_hash, fc1_bytes):
