@@ -11,7 +11,7 @@
 // Two kernels:
 //  1. router_logits_kernel: partial logits l[t,e] over a K range per CTA.
 //     Tile 128 tokens x 64 experts x K-range; each thread owns 8x4 outputs,
-//     read from k-major shared-memory tiles.  Accumulation is nested (32-term
+//     read from row-major padded shared-memory tiles.  Accumulation is nested (32-term
 //     chains per 32-k chunk -> groups of 8 chunks -> the CTA's range), which
 //     keeps the worst-case rounding error of every logit below
 //     gamma_n * (||x_t|| ||w_e|| + |b_e|) with a small n (about 70 for
@@ -62,23 +62,26 @@ __device__ __forceinline__ void cp_async_wait_group() {
 }
 
 // Tile: 128 tokens x 64 experts x a K range per CTA, 256 threads, 8 x 4 outputs
-// per thread (tokens 4 tg .. 4 tg + 3 and 64 + 4 tg .. + 3, experts 4 eg .. 4 eg + 3).
-// Both operands sit k-major in shared memory (xs[k][token], ws[k][expert], fp32),
-// so per k a thread reads its 8 token values and 4 expert values with three 16-byte
-// loads -- two of them broadcast to half a warp, one spread over 16 lanes -- and
-// issues 32 FMAs.  Chunks of 32 k are staged through registers loaded one chunk
-// ahead: a lane reads 8 consecutive k of one token row (bf16) or 4 of one Wg row,
-// the 32 lanes of a warp consecutive rows, and stores them transposed, conflict-free,
-// into the buffer the next chunk reads (two buffers, one barrier per chunk).  Each
-// logit's sum: per 32-k chunk one chain in ascending k, chunks summed in groups of 8,
-// groups summed over the CTA's range -- a rounding depth of 32 + 8 + groups per range.
-// The expert tiles of one token tile are adjacent CTAs, so they share the token rows
-// through L2.  CTAs of expert tile 0 also emit the partial squared norms of their
-// token rows, CTAs of token tile 0 those of their Wg rows.
-constexpr int RT_XW = RT_BT;  // xs row (floats)
-constexpr int RT_WW = RT_BE;  // ws row (floats)
+// per thread (tokens 4 tg .. 4 tg + 3 and 64 + 4 tg .. + 3, experts eg + 16 j).
+// Both operands sit row-major in shared memory in rows padded to 36 floats:
+// xs[token][k] (fp32, widened from bf16 once by the thread that stages it) and
+// ws[expert][k] (copied as it is by cp.async).  Per 4 k a thread reads its 8 token
+// quads and its 4 expert quads with 12 16-byte loads -- a token quad is broadcast to
+// half a warp, the 16 expert rows of a warp fall on all 8 bank quads (two wavefronts)
+// -- and issues 128 FMAs.  The staging reads are coalesced: per warp instruction 8
+// token rows x 64 contiguous bytes, or 4 Wg rows x 128 bytes; the widened token
+// pieces go to shared memory as two 16-byte stores that cover all 32 banks per 8
+// lanes.  Chunk c is computed from buffer c & 1 while the next chunk's token pieces
+// load into registers and its Wg pieces copy into the other buffer; one barrier per
+// chunk.  Each logit's sum: per 32-k chunk one chain in ascending k whose first term
+// is the rounded product, chunks summed in groups of 8, groups summed over the CTA's
+// range -- a rounding depth of 32 + 8 + groups per range.  The expert tiles of one
+// token tile are adjacent CTAs, so they share the token rows through L2.  CTAs of
+// expert tile 0 also emit the partial squared norms of their token rows, CTAs of
+// token tile 0 those of their Wg rows.
+constexpr int RT_LD = RT_BK + 4;  // padded row (floats): 144 bytes, 16-byte aligned
 // two tile buffers, then the range-level sums of every thread's 32 outputs
-constexpr size_t RT_SMEM = sizeof(float) * (2 * RT_BK * (RT_XW + RT_WW) + 32 * RT_THREADS);
+constexpr size_t RT_SMEM = sizeof(float) * (2 * RT_LD * (RT_BT + RT_BE) + 32 * RT_THREADS);
 
 __global__ void __launch_bounds__(RT_THREADS, 2) router_logits_kernel(const uint16_t* __restrict__ x,
                                                                       const float* __restrict__ Wg, int64_t T,
@@ -89,8 +92,8 @@ __global__ void __launch_bounds__(RT_THREADS, 2) router_logits_kernel(const uint
     extern __shared__ __align__(16) float rt_smem[];
     pdl_wait();
     pdl_trigger();
-    float (*xs)[RT_BK][RT_XW] = reinterpret_cast<float (*)[RT_BK][RT_XW]>(rt_smem);
-    float (*ws)[RT_BK][RT_WW] = reinterpret_cast<float (*)[RT_BK][RT_WW]>(rt_smem + 2 * RT_BK * RT_XW);
+    float (*xs)[RT_BT][RT_LD] = reinterpret_cast<float (*)[RT_BT][RT_LD]>(rt_smem);
+    float (*ws)[RT_BE][RT_LD] = reinterpret_cast<float (*)[RT_BE][RT_LD]>(rt_smem + 2 * RT_BT * RT_LD);
 
     const int tid = threadIdx.x;
     const int e0 = blockIdx.x * RT_BE;               // expert tiles vary fastest
@@ -100,53 +103,47 @@ __global__ void __launch_bounds__(RT_THREADS, 2) router_logits_kernel(const uint
     const int kend = min(H, kbeg + KC);
     const int nchunk = (kend - kbeg) / RT_BK;
 
-    // staging: x vector j of this thread is token xt, k offset xk[j] (8 bf16);
-    // Wg vector j is expert we, k offset wk[j] (4 fp32)
-    const int xt = tid & (RT_BT - 1);
-    const int xk0 = (tid >> 7) * 8;                  // 0 or 8; vector 1 adds 16
-    const bool xv = t0 + xt < T;
-    const uint16_t* xsrc = x + (xv ? t0 + xt : 0) * (int64_t)H + kbeg + xk0;
-    const int we = tid & (RT_BE - 1);
-    const int wk0 = (tid >> 6) * 4;                  // 0, 4, 8, 12; vector 1 adds 16
-    const bool wvl = e0 + we < E;
-    const float* wsrc = Wg + (int64_t)(wvl ? e0 + we : 0) * H + kbeg + wk0;
+    // staging: token pieces tid and tid + 256 of a chunk's 512 (token p / 4, k 8 (p % 4)
+    // .. + 7, bf16); Wg pieces tid and tid + 256 (expert p / 8, k 4 (p % 8) .. + 3, fp32)
+    const int xq = tid & 3;
+    const int xt = tid >> 2;                         // tokens xt and xt + 64
+    const bool xv0 = t0 + xt < T, xv1 = t0 + xt + 64 < T;
+    const uint16_t* xsrc0 = x + (xv0 ? t0 + xt : 0) * (int64_t)H + kbeg + 8 * xq;
+    const uint16_t* xsrc1 = x + (xv1 ? t0 + xt + 64 : 0) * (int64_t)H + kbeg + 8 * xq;
+    const int wq = tid & 7;
+    const int we = tid >> 3;                         // experts we and we + 32
+    const bool wv0 = e0 + we < E, wv1 = e0 + we + 32 < E;
+    const float* wsrc0 = Wg + (int64_t)(wv0 ? e0 + we : 0) * H + kbeg + 4 * wq;
+    const float* wsrc1 = Wg + (int64_t)(wv1 ? e0 + we + 32 : 0) * H + kbeg + 4 * wq;
+    const bool wnorm = blockIdx.y == 0;              // this CTA emits the Wg row norms
 
-    struct Stage {
-        uint4 xa, xb;
-        float4 wa, wb;
-    };
-    auto load = [&](int c, Stage& st) {
+    uint4 sx0, sx1;                                  // the next chunk's token pieces
+    auto load_x = [&](int c) {
         if (c < nchunk) {
-            const int ko = c * RT_BK;
-            st.xa = xv ? __ldg(reinterpret_cast<const uint4*>(xsrc + ko)) : make_uint4(0, 0, 0, 0);
-            st.xb = xv ? __ldg(reinterpret_cast<const uint4*>(xsrc + ko + 16)) : make_uint4(0, 0, 0, 0);
-            st.wa = wvl ? __ldg(reinterpret_cast<const float4*>(wsrc + ko)) : make_float4(0.f, 0.f, 0.f, 0.f);
-            st.wb = wvl ? __ldg(reinterpret_cast<const float4*>(wsrc + ko + 16)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            sx0 = xv0 ? __ldg(reinterpret_cast<const uint4*>(xsrc0 + c * RT_BK)) : make_uint4(0, 0, 0, 0);
+            sx1 = xv1 ? __ldg(reinterpret_cast<const uint4*>(xsrc1 + c * RT_BK)) : make_uint4(0, 0, 0, 0);
         }
     };
-    float nx = 0.f, nw = 0.f;  // partial squared norms of row xt / we (this thread's k)
-    auto store = [&](int buf, const Stage& st) {
+    auto copy_w = [&](int c, int buf) {
+        if (c < nchunk) {
+            cp_async16(&ws[buf][we][4 * wq], wsrc0 + c * RT_BK, wv0);
+            cp_async16(&ws[buf][we + 32][4 * wq], wsrc1 + c * RT_BK, wv1);
+        }
+        cp_async_commit();
+    };
+    float nx0 = 0.f, nx1 = 0.f, nw0 = 0.f, nw1 = 0.f;  // partial squared norms (this thread's k)
+    auto store_x = [&](int buf) {
         float f[8];
-        unpack8(st.xa, f);
+        unpack8(sx0, f);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            xs[buf][xk0 + i][xt] = f[i];
-            nx = fmaf(f[i], f[i], nx);
-        }
-        unpack8(st.xb, f);
+        for (int i = 0; i < 8; ++i) nx0 = fmaf(f[i], f[i], nx0);
+        *reinterpret_cast<float4*>(&xs[buf][xt][8 * xq]) = make_float4(f[0], f[1], f[2], f[3]);
+        *reinterpret_cast<float4*>(&xs[buf][xt][8 * xq + 4]) = make_float4(f[4], f[5], f[6], f[7]);
+        unpack8(sx1, f);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            xs[buf][xk0 + 16 + i][xt] = f[i];
-            nx = fmaf(f[i], f[i], nx);
-        }
-        const float w8[8] = {st.wa.x, st.wa.y, st.wa.z, st.wa.w, st.wb.x, st.wb.y, st.wb.z, st.wb.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            ws[buf][wk0 + i][we] = w8[i];
-            ws[buf][wk0 + 16 + i][we] = w8[4 + i];
-            nw = fmaf(w8[i], w8[i], nw);
-            nw = fmaf(w8[4 + i], w8[4 + i], nw);
-        }
+        for (int i = 0; i < 8; ++i) nx1 = fmaf(f[i], f[i], nx1);
+        *reinterpret_cast<float4*>(&xs[buf][xt + 64][8 * xq]) = make_float4(f[0], f[1], f[2], f[3]);
+        *reinterpret_cast<float4*>(&xs[buf][xt + 64][8 * xq + 4]) = make_float4(f[4], f[5], f[6], f[7]);
     };
 
     // compute layout: warp w, lane: expert group eg = lane & 15, token group tg = 2 w + lane / 16
@@ -154,7 +151,7 @@ __global__ void __launch_bounds__(RT_THREADS, 2) router_logits_kernel(const uint
     const int eg = lane & 15;
     const int tg = 2 * wid + (lane >> 4);
     // level 3 (the range) lives in shared memory: it changes once per 8 chunks
-    float* a3s = rt_smem + 2 * RT_BK * (RT_XW + RT_WW) + tid;  // element q at a3s[q * RT_THREADS]
+    float* a3s = rt_smem + 2 * RT_LD * (RT_BT + RT_BE) + tid;  // element q at a3s[q * RT_THREADS]
     float a1[8][4], a2[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
@@ -164,36 +161,34 @@ __global__ void __launch_bounds__(RT_THREADS, 2) router_logits_kernel(const uint
             a3s[(i * 4 + j) * RT_THREADS] = 0.f;
         }
 
-    // chunk c: computed from buffer c & 1 while the registers load chunk c + 1, which
-    // goes to the other buffer after the compute
-    Stage sn;
     auto step = [&](int c) {
         const int buf = c & 1;
-        load(c + 1, sn);
-        // the operands of k + 1 are loaded while the 32 FMAs of k issue; the chain of
-        // each chunk starts with the rounded product of its first k
-        float4 cxl = *reinterpret_cast<const float4*>(&xs[buf][0][4 * tg]);
-        float4 cxh = *reinterpret_cast<const float4*>(&xs[buf][0][64 + 4 * tg]);
-        float4 cw = *reinterpret_cast<const float4*>(&ws[buf][0][4 * eg]);
+        load_x(c + 1);
+        copy_w(c + 1, buf ^ 1);  // the other buffer was last read by chunk c - 1
+        if (wnorm) {
+            const float4 p = *reinterpret_cast<const float4*>(&ws[buf][we][4 * wq]);
+            const float4 q = *reinterpret_cast<const float4*>(&ws[buf][we + 32][4 * wq]);
+            nw0 = fmaf(p.x, p.x, fmaf(p.y, p.y, fmaf(p.z, p.z, fmaf(p.w, p.w, nw0))));
+            nw1 = fmaf(q.x, q.x, fmaf(q.y, q.y, fmaf(q.z, q.z, fmaf(q.w, q.w, nw1))));
+        }
 #pragma unroll
-        for (int k = 0; k < RT_BK; ++k) {
-            float4 nxl, nxh, nw4;
-            if (k + 1 < RT_BK) {
-                nxl = *reinterpret_cast<const float4*>(&xs[buf][k + 1][4 * tg]);
-                nxh = *reinterpret_cast<const float4*>(&xs[buf][k + 1][64 + 4 * tg]);
-                nw4 = *reinterpret_cast<const float4*>(&ws[buf][k + 1][4 * eg]);
-            }
-            const float xv8[8] = {cxl.x, cxl.y, cxl.z, cxl.w, cxh.x, cxh.y, cxh.z, cxh.w};
-            const float wv4[4] = {cw.x, cw.y, cw.z, cw.w};
+        for (int kq = 0; kq < RT_BK / 4; ++kq) {
+            float4 w4[4];
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
+            for (int j = 0; j < 4; ++j) w4[j] = *reinterpret_cast<const float4*>(&ws[buf][eg + 16 * j][4 * kq]);
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    a1[i][j] = k == 0 ? __fmul_rn(xv8[i], wv4[j]) : fmaf(xv8[i], wv4[j], a1[i][j]);
-            if (k + 1 < RT_BK) {
-                cxl = nxl;
-                cxh = nxh;
-                cw = nw4;
+            for (int i = 0; i < 8; ++i) {
+                const int row = (i < 4 ? 0 : 64) + 4 * tg + (i & 3);
+                const float4 x4 = *reinterpret_cast<const float4*>(&xs[buf][row][4 * kq]);
+                const float xv[4] = {x4.x, x4.y, x4.z, x4.w};
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float wv = kk == 0 ? w4[j].x : kk == 1 ? w4[j].y : kk == 2 ? w4[j].z : w4[j].w;
+                        a1[i][j] = (kq == 0 && kk == 0) ? __fmul_rn(xv[kk], wv) : fmaf(xv[kk], wv, a1[i][j]);
+                    }
+                }
             }
         }
 #pragma unroll
@@ -209,11 +204,14 @@ __global__ void __launch_bounds__(RT_THREADS, 2) router_logits_kernel(const uint
                     a2[i][j] = 0.f;
                 }
         }
-        if (c + 1 < nchunk) store(buf ^ 1, sn);
+        if (c + 1 < nchunk) store_x(buf ^ 1);
+        cp_async_wait_group<0>();
         __syncthreads();
     };
-    load(0, sn);
-    if (nchunk > 0) store(0, sn);
+    load_x(0);
+    copy_w(0, 0);
+    if (nchunk > 0) store_x(0);
+    cp_async_wait_group<0>();
     __syncthreads();
     for (int c = 0; c < nchunk; ++c) step(c);
     float a3[8][4];
@@ -222,30 +220,35 @@ __global__ void __launch_bounds__(RT_THREADS, 2) router_logits_kernel(const uint
 #pragma unroll
         for (int j = 0; j < 4; ++j) a3[i][j] = a3s[(i * 4 + j) * RT_THREADS] + a2[i][j];
 
-    const int ebase = e0 + 4 * eg;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        const int64_t t = t0 + (i < 4 ? 4 * tg + i : 64 + 4 * tg + (i - 4));
+        const int64_t t = t0 + (i < 4 ? 0 : 64) + 4 * tg + (i & 3);
         if (t >= T) continue;
-        float* dst = part + ((int64_t)sp * T + t) * E + ebase;
-        if (ebase + 3 < E && (E & 3) == 0) {
-            *reinterpret_cast<float4*>(dst) = make_float4(a3[i][0], a3[i][1], a3[i][2], a3[i][3]);
-        } else {
+        float* dst = part + ((int64_t)sp * T + t) * E + e0 + eg;
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                if (ebase + j < E) dst[j] = a3[i][j];
-        }
+        for (int j = 0; j < 4; ++j)
+            if (e0 + eg + 16 * j < E) dst[16 * j] = a3[i][j];
     }
-    // squared norms: two threads hold parts of each token row, four of each Wg row
-    float* red = rt_smem;  // the buffers are no longer read
-    red[tid] = nx;
-    red[RT_THREADS + tid] = nw;
-    __syncthreads();
-    if (blockIdx.x == 0 && tid < RT_BT && t0 + tid < T)
-        xsq[(int64_t)sp * T + t0 + tid] = red[tid] + red[tid + RT_BT];
-    if (blockIdx.y == 0 && tid < RT_BE && e0 + tid < E)
-        wsq[(int64_t)sp * E + e0 + tid] = (red[RT_THREADS + tid] + red[RT_THREADS + tid + 64]) +
-                                          (red[RT_THREADS + tid + 128] + red[RT_THREADS + tid + 192]);
+    // squared norms: the 4 lanes of a token row (xq) and the 8 of a Wg row (wq) are
+    // adjacent lanes of one warp
+#pragma unroll
+    for (int off = 1; off < 4; off <<= 1) {
+        nx0 += __shfl_xor_sync(0xffffffffu, nx0, off);
+        nx1 += __shfl_xor_sync(0xffffffffu, nx1, off);
+    }
+#pragma unroll
+    for (int off = 1; off < 8; off <<= 1) {
+        nw0 += __shfl_xor_sync(0xffffffffu, nw0, off);
+        nw1 += __shfl_xor_sync(0xffffffffu, nw1, off);
+    }
+    if (blockIdx.x == 0 && xq == 0) {
+        if (xv0) xsq[(int64_t)sp * T + t0 + xt] = nx0;
+        if (xv1) xsq[(int64_t)sp * T + t0 + xt + 64] = nx1;
+    }
+    if (wnorm && wq == 0) {
+        if (wv0) wsq[(int64_t)sp * E + e0 + we] = nw0;
+        if (wv1) wsq[(int64_t)sp * E + e0 + we + 32] = nw1;
+    }
 }
 
 // Compensated (doubled-precision) dot product of one bf16 x row with one fp32
