@@ -612,7 +612,7 @@ def bench_ours(args):
                       "frac": wk["layer_bytes"] / (ms * 1e-3) / 1e9 / peaks["hbm"],
                       "what": "algorithmic bytes of the whole layer step / step time, of the measured HBM peak"},
         "grouped_gemm_tflops": (wk["fc1_flops"] + wk["fc2_flops"]) / ((kernel_ms["fc1"] + kernel_ms["fc2"]) * 1e-3) / 1e12,
-        "rows": rows, "active_slots": active, "router_fp64_rechecked_tokens": refined_per_step,
+        "rows": rows, "active_slots": active, "router_rechecked_tokens": refined_per_step,
     }
     if rank == 0 and ws_ == 1 and not args.no_cpu_baseline:
         base, _ = run_cpu_baseline(inp, cfg, target_s=args.cpu_seconds)

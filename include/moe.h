@@ -108,8 +108,10 @@ MOE_API moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, moe_stream_t 
  * call synchronises `stream` (it copies 4 bytes to the host). */
 MOE_API moe_status_t moe_get_device_status(void *ws, moe_stream_t stream, int32_t *device_status);
 
-/* Number of tokens whose top-k decision needed the fp64 recheck in the last
- * moe_route calls since moe_workspace_init (diagnostic; synchronises). */
+/* Number of tokens whose top-k decision needed a recheck of a near-tied
+ * cluster (compensated fp32, and fp64 where that still leaves a gap inside its
+ * bound) in the moe_route calls since moe_workspace_init (diagnostic;
+ * synchronises). */
 MOE_API moe_status_t moe_get_route_stats(void *ws, moe_stream_t stream, int64_t *refined_tokens);
 
 /* ------------------------------------------------------------------------ */
