@@ -220,28 +220,54 @@ __device__ __forceinline__ void scatter_pairs(int64_t pb, const uint16_t* __rest
         pair_row[p] = row;
     }
     const int nj = (int)min((int64_t)PS_PAIRS, P - pb);
+    if (!wsc) {
+        // the pairs of one token share its row: each 16-byte vector of the row is loaded
+        // once (eight per lane in flight) and stored to every one of its pairs' rows
+        int j0 = 0;
+        while (j0 < nj) {
+            const int64_t tok = (pb + j0) / k;
+            int j1 = j0 + 1;
+            while (j1 < nj && (pb + j1) / k == tok) ++j1;
+            const uint4* src = reinterpret_cast<const uint4*>(x + tok * H);
+            for (int v0 = lane; v0 < vec; v0 += 32 * 8) {
+                uint4 buf[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int v = v0 + 32 * u;
+                    if (v < vec) buf[u] = __ldg(src + v);
+                }
+                for (int j = j0; j < j1; ++j) {
+                    const int32_t r = __shfl_sync(0xffffffffu, row, j);
+                    if (r < 0) continue;
+                    uint4* dst = reinterpret_cast<uint4*>(x_perm + (int64_t)r * H);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int v = v0 + 32 * u;
+                        if (v < vec) dst[v] = buf[u];
+                    }
+                }
+            }
+            j0 = j1;
+        }
+        return;
+    }
     for (int j = 0; j < nj; ++j) {
         const int32_t r = __shfl_sync(0xffffffffu, row, j);
         const float wj = __shfl_sync(0xffffffffu, wp, j);
         if (r < 0) continue;
         const uint4* src = reinterpret_cast<const uint4*>(x + ((pb + j) / k) * H);
         uint4* dst = reinterpret_cast<uint4*>(x_perm + (int64_t)r * H);
-        if (!wsc) {
+        // routing on the input: each pair's row scaled by its own weight; unrolled so the
+        // loads of several vectors are in flight before the first one's products are rounded
 #pragma unroll 4
-            for (int v = lane; v < vec; v += 32) dst[v] = __ldg(src + v);
-        } else {
-            // unrolled so the loads of several vectors are in flight before the first
-            // one's products are rounded
-#pragma unroll 4
-            for (int v = lane; v < vec; v += 32) {
-                float f[8];
-                unpack8(__ldg(src + v), f);
-                uint32_t o[4];
+        for (int v = lane; v < vec; v += 32) {
+            float f[8];
+            unpack8(__ldg(src + v), f);
+            uint32_t o[4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    o[i] = bf16_of_product(wj, f[2 * i]) | (bf16_of_product(wj, f[2 * i + 1]) << 16);
-                dst[v] = make_uint4(o[0], o[1], o[2], o[3]);
-            }
+            for (int i = 0; i < 4; ++i)
+                o[i] = bf16_of_product(wj, f[2 * i]) | (bf16_of_product(wj, f[2 * i + 1]) << 16);
+            dst[v] = make_uint4(o[0], o[1], o[2], o[3]);
         }
     }
 }
