@@ -614,6 +614,19 @@ def bench_ours(args):
         "grouped_gemm_tflops": (wk["fc1_flops"] + wk["fc2_flops"]) / ((kernel_ms["fc1"] + kernel_ms["fc2"]) * 1e-3) / 1e12,
         "rows": rows, "active_slots": active, "router_rechecked_tokens": refined_per_step,
     }
+    if "router_logits" in [l["kernel"] for l in launches_ms]:
+        # the gate GEMM on CUDA cores (T E H FMAs) against the derived fp32 peak: 152 SMs x 128
+        # lanes x 2 flops x the clock (the maximum, and the median the timed region sampled)
+        rl_ms = sum(l["ms"] for l in launches_ms if l["kernel"] == "router_logits")
+        tf = 2.0 * T * cfg.E * H / (rl_ms * 1e-3) / 1e12
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        mhz_max = (clk or {}).get("sm_max_mhz") or 2070.0
+        mhz = (clk or {}).get("sm_mhz") or mhz_max
+        res["router_logits"] = {"achieved_tflops": tf, "ms": rl_ms,
+                                "peak_tflops_at_max_clock": sms * 128 * 2 * mhz_max * 1e-6,
+                                "frac_at_max_clock": tf / (sms * 128 * 2 * mhz_max * 1e-6),
+                                "peak_tflops_at_sampled_clock": sms * 128 * 2 * mhz * 1e-6,
+                                "frac_at_sampled_clock": tf / (sms * 128 * 2 * mhz * 1e-6)}
     if rank == 0 and ws_ == 1 and not args.no_cpu_baseline:
         base, _ = run_cpu_baseline(inp, cfg, target_s=args.cpu_seconds)
         res["cpu_baseline"] = base
