@@ -204,7 +204,10 @@ MOE_API moe_status_t moe_route_grouped(const moe_bf16_t *x, const float *gate_w,
  *                                  are left unspecified
  *   pair_row  [T*k] int32 out      row of pair p, or -1
  *   x_perm    [T*k, H] bf16 out    x_perm[r] = x[perm_src[r] / k]; rows past the
- *                                  row count are left unspecified
+ *                                  row count are left unspecified.  May be NULL (then
+ *                                  x may be NULL too): only the routing tables are
+ *                                  written, for a consumer that reads the token rows
+ *                                  through pair_row (moe_forward_nvfp4)
  * Rows of one slot hold its pairs in ascending pair index (a stable grouping). */
 MOE_API moe_status_t moe_permute(const int32_t *topk_ids, float *topk_w, int64_t T, int k, int E,
                          const int32_t *rep_offset, const int32_t *rep_slots, int S,
@@ -220,7 +223,8 @@ MOE_API moe_status_t moe_permute(const int32_t *topk_ids, float *topk_w, int64_t
  * routing weight after the mask, rounded once to bf16 (nearest, ties to even):
  *     x_perm[r] = bf16(topk_w[p] * x[p / k]),  p = perm_src[r].
  * The expert outputs are then summed unweighted: pass topk_w = NULL to
- * moe_forward / moe_finalize.  Arguments, outputs and errors as moe_permute. */
+ * moe_forward / moe_finalize.  Arguments, outputs and errors as moe_permute
+ * (x and x_perm are required here). */
 MOE_API moe_status_t moe_permute_on_input(const int32_t *topk_ids, float *topk_w, int64_t T, int k, int E,
                                   const int32_t *rep_offset, const int32_t *rep_slots, int S, int local_start,
                                   int local_count, int nonlocal_mode, const moe_bf16_t *x, int H,
@@ -347,9 +351,15 @@ MOE_API moe_status_t moe_quantize_act_rows(const moe_bf16_t *v, int64_t rows, in
  *   W1sq [2*I_shared_total, H/2], W1s_sf, W1s_scale; W2sq [H, I_shared_total/2],
  *       W2s_sf, W2s_scale (the shared experts as one concatenated MLP; NULL if none)
  * H, I and I_shared_total at most 16384 (MOE_ERR_UNSUPPORTED otherwise).
- * x_perm must be 16-byte aligned.  Launches two quantisation kernels besides
- * moe_forward's three; their scratch is part of moe_workspace_size.  Everything
- * else as moe_forward. */
+ * With topk_w and x given (weights applied at the output) the rows of x_perm
+ * must be the copies of token rows that moe_permute writes; the call then
+ * quantises each token row of x once and places its codes at the rows of its
+ * pairs (pair_row) and at the shared experts' row, without reading x_perm, which
+ * may be NULL (moe_permute with x_perm = NULL then skips the row copies).  With
+ * topk_w = NULL (moe_permute_on_input) or x = NULL it quantises the rows of
+ * x_perm, which must be given.  x_perm (when read) and x must be 16-byte
+ * aligned.  Launches two quantisation kernels besides moe_forward's three; their
+ * scratch is part of moe_workspace_size.  Everything else as moe_forward. */
 MOE_API moe_status_t moe_forward_nvfp4(const moe_bf16_t *x_perm, const int32_t *offsets, int S_local, int64_t P_cap,
                                const uint8_t *W1q, const uint8_t *W1_sf, const float *W1_scale,
                                const uint8_t *W2q, const uint8_t *W2_sf, const float *W2_scale, int H, int I,

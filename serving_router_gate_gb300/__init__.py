@@ -215,7 +215,8 @@ def moe_route_noalloc(x, gate_w, logit_bias, k, renorm, topk_ids, topk_w, stream
 
 def moe_permute(topk_ids, topk_w, E, rep_offset, rep_slots, S, local_start, local_count, nonlocal_mode, x,
                 slot_ids, counts, offsets, perm_src, pair_row, x_perm, ws, stream=None, on_input=False):
-    """moe_permute, or moe_permute_on_input when on_input (rows scaled by the routing weights)."""
+    """moe_permute, or moe_permute_on_input when on_input (rows scaled by the routing weights).
+    x_perm=None (not with on_input): only the routing tables are written, no rows copied."""
     T, k = topk_ids.shape
     H = x.shape[1]
     S_local = local_count if local_count >= 0 else S
@@ -226,7 +227,8 @@ def moe_permute(topk_ids, topk_w, E, rep_offset, rep_slots, S, local_start, loca
                           nonlocal_mode, _ptr(x, "x", _bf16, (T, H)), H,
                           _ptr(slot_ids, "slot_ids", _i32, (T, k)), _ptr(counts, "counts", _i32, (S_local,)),
                           _ptr(offsets, "offsets", _i32, (S_local + 1,)), _ptr(perm_src, "perm_src", _i32, (T * k,)),
-                          _ptr(pair_row, "pair_row", _i32, (T, k)), _ptr(x_perm, "x_perm", _bf16, (T * k, H)),
+                          _ptr(pair_row, "pair_row", _i32, (T, k)),
+                          _ptr(x_perm, "x_perm", _bf16, (T * k, H), allow_none=True),
                           _ptr(ws, "ws", torch.uint8), ws.numel(), _stream(stream))
     _check("moe_permute_on_input" if on_input else "moe_permute", st)
 
@@ -398,16 +400,18 @@ def moe_quantize_nvfp4_rows(v, q, sb, scale, pow2=False, stream=None):
 
 def moe_forward_nvfp4(x_perm, offsets, W1q, W1sf, s1, W2q, W2sf, s2, pair_row, topk_w, x, W1sq, W1ssf, s1s,
                       W2sq, W2ssf, s2s, shared_gate_w, out, ws, stream=None):
-    """moe_forward with NVFP4 weights (moe_quantize_nvfp4_rows, pow2=False) and NVFP4 activations."""
-    P_cap, H = x_perm.shape
+    """moe_forward with NVFP4 weights (moe_quantize_nvfp4_rows, pow2=False) and NVFP4 activations.
+    With topk_w and x given, each token row of x is quantised once for its pairs' rows and
+    x_perm is not read (it may be None)."""
     S_local = offsets.shape[0] - 1
     I = 2 * W2q.shape[2]
     T, k = pair_row.shape
+    P_cap, H = x_perm.shape if x_perm is not None else (T * k, x.shape[1])
     I_sh = 0 if W2sq is None else 2 * W2sq.shape[1]
     u8 = torch.uint8
     fh, fi, fs = nvfp4_sf_row_bytes(H), nvfp4_sf_row_bytes(I), nvfp4_sf_row_bytes(I_sh) if I_sh else 0
     st = _lib.moe_forward_nvfp4(
-        _ptr(x_perm, "x_perm", _bf16), _ptr(offsets, "offsets", _i32), S_local, P_cap,
+        _ptr(x_perm, "x_perm", _bf16, allow_none=True), _ptr(offsets, "offsets", _i32), S_local, P_cap,
         _ptr(W1q, "W1q", u8, (S_local, 2 * I, H // 2)), _ptr(W1sf, "W1_sf", u8, (S_local, 2 * I, fh)),
         _ptr(s1, "W1_scale", _f32, (S_local, 2 * I)),
         _ptr(W2q, "W2q", u8, (S_local, H, I // 2)), _ptr(W2sf, "W2_sf", u8, (S_local, H, fi)),

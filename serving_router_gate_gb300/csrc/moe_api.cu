@@ -326,7 +326,9 @@ static moe_status_t permute_impl(bool scale_rows, const int32_t* topk_ids, float
         if (e == cudaSuccess) e = cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (size_t)(S_local + 1), s);
         return cuda_status(e);
     }
-    if (!topk_ids || !topk_w || !x || !slot_ids || !perm_src || !pair_row || !x_perm) return MOE_ERR_INVALID_ARG;
+    if (!topk_ids || !topk_w || !slot_ids || !perm_src || !pair_row) return MOE_ERR_INVALID_ARG;
+    if (x_perm && !x) return MOE_ERR_INVALID_ARG;
+    if (scale_rows && !x_perm) return MOE_ERR_INVALID_ARG;
     const int64_t P = T * k;
     if (!ws || ws_bytes < permute_need(P, S_local)) return MOE_ERR_WORKSPACE;
     PermuteLaunch L;
@@ -767,12 +769,17 @@ moe_status_t moe_forward_nvfp4(const moe_bf16_t* x_perm, const int32_t* offsets,
         P_cap >= (int64_t(1) << 31) || H > kNvfp4MaxK || I > kNvfp4MaxK || I_shared_total > kNvfp4MaxK)
         return MOE_ERR_UNSUPPORTED;
     if (T == 0) return MOE_OK;
-    if (!x_perm || !offsets || !W1q || !W1_sf || !W1_scale || !W2q || !W2_sf || !W2_scale || !pair_row || !out)
+    if (!offsets || !W1q || !W1_sf || !W1_scale || !W2q || !W2_sf || !W2_scale || !pair_row || !out)
         return MOE_ERR_INVALID_ARG;
     if (I_shared_total > 0 && (!x || !W1sq || !W1s_sf || !W1s_scale || !W2sq || !W2s_sf || !W2s_scale))
         return MOE_ERR_INVALID_ARG;
     if (shared_gate_w && (I_shared_total == 0 || !x)) return MOE_ERR_INVALID_ARG;
-    if (!aligned(x_perm, 16) || (I_shared_total > 0 && !aligned(x, 16))) return MOE_ERR_INVALID_ARG;
+    // weights applied at the output and the token rows given: the expert input rows are
+    // copies of token rows, so each token row is quantised once and placed at its pairs'
+    // rows (x_perm is then not read and may be NULL)
+    const bool from_tokens = topk_w && x;
+    if (!x_perm && !from_tokens) return MOE_ERR_INVALID_ARG;
+    if ((!from_tokens && !aligned(x_perm, 16)) || (x && !aligned(x, 16))) return MOE_ERR_INVALID_ARG;
     const ForwardLayout FL = forward_layout(P_cap, T, H, I, I_shared_total);
     if (!ws || ws_bytes < FL.total) return MOE_ERR_WORKSPACE;
     char* base = static_cast<char*>(ws);
@@ -787,11 +794,24 @@ moe_status_t moe_forward_nvfp4(const moe_bf16_t* x_perm, const int32_t* offsets,
     float* y_sh_part = ks > 1 ? reinterpret_cast<float*>(base + FL.y_sh_part) : nullptr;
     const int sms = device_sms();
     const int64_t T_sh = I_shared_total > 0 ? T : 0;
-    // the expert input rows (as many as offsets[S_local] says, read on the device) and the
-    // shared experts' input, to NVFP4 with power-of-two row scales
-    const Nvfp4QuantSeg qx[2] = {{x_perm, P_cap, offsets + S_local, H, 1, u8(FL.xq), u8(FL.xsf), f32(FL.sxq)},
-                                 {x, T_sh, nullptr, H, 1, u8(FL.xsq), u8(FL.xssf), f32(FL.sxs)}};
-    moe_status_t st = cuda_status(launch_quantize_nvfp4_rows(qx, T_sh > 0 ? 2 : 1, sms, s));
+    // the expert input rows and the shared experts' input, to NVFP4 with power-of-two
+    // row scales: per token row (placed at the shared rows and at its pairs' rows), or
+    // per row of x_perm (as many as offsets[S_local] says, read on the device)
+    moe_status_t st;
+    if (from_tokens) {
+        Nvfp4QuantSeg q = {x, T, nullptr, H, 1, T_sh > 0 ? u8(FL.xsq) : nullptr, u8(FL.xssf), f32(FL.sxs)};
+        q.pair_row = pair_row;
+        q.k = k;
+        q.q2 = u8(FL.xq);
+        q.sb2 = u8(FL.xsf);
+        q.scale2 = f32(FL.sxq);
+        q.dst2_rows = P_cap;
+        st = cuda_status(launch_quantize_nvfp4_rows(&q, 1, sms, s));
+    } else {
+        const Nvfp4QuantSeg qx[2] = {{x_perm, P_cap, offsets + S_local, H, 1, u8(FL.xq), u8(FL.xsf), f32(FL.sxq)},
+                                     {x, T_sh, nullptr, H, 1, u8(FL.xsq), u8(FL.xssf), f32(FL.sxs)}};
+        st = cuda_status(launch_quantize_nvfp4_rows(qx, T_sh > 0 ? 2 : 1, sms, s));
+    }
     if (st != MOE_OK) return st;
     const Nvfp4Operands o1 = {u8(FL.xq), u8(FL.xsf), f32(FL.sxq), W1q, W1_sf, W1_scale,
                               u8(FL.xsq), u8(FL.xssf), f32(FL.sxs), W1sq, W1s_sf, W1s_scale};

@@ -533,14 +533,22 @@ cudaError_t launch_quantize_fp8_rows(const uint16_t* w, int64_t rows, int K, uin
 // (activations), else amax / 2688 (weights).  A segment with rows_dev takes
 // min(rows, *rows_dev) rows, read on the device.
 struct Nvfp4QuantSeg {
-    const uint16_t* src;
+    const uint16_t* src;       // [rows, K] bf16
     int64_t rows;
-    const int32_t* rows_dev;
+    const int32_t* rows_dev;   // or null
     int K;
     int pow2;
-    uint8_t* q;
-    uint8_t* sb;
-    float* scale;
+    uint8_t* q;                // [rows, K/2] codes, or null
+    uint8_t* sb;               // [rows, nvfp4_sf_row_bytes(K)] block scales
+    float* scale;              // [rows] row scales
+    // optional: row t's codes and scales also go to rows pair_row[t * k + j] (j < k;
+    // -1 and rows past dst2_rows skipped) of q2 / sb2 / scale2
+    const int32_t* pair_row = nullptr;
+    int k = 0;
+    uint8_t* q2 = nullptr;
+    uint8_t* sb2 = nullptr;
+    float* scale2 = nullptr;
+    int64_t dst2_rows = 0;
 };
 cudaError_t launch_quantize_nvfp4_rows(const Nvfp4QuantSeg* seg, int nseg, int num_sms, cudaStream_t s);
 // bytes of one row of NVFP4 block scales

@@ -24,7 +24,8 @@
 //            base[c][s] = offsets[s] + earlier chunks' counts of s.
 //  3 scatter 8 pairs per warp step: row = base[chunk][slot] + rank; writes
 //            pair_row and perm_src, and the warp copies x[t] into x_perm[row]
-//            with 16-byte loads/stores.
+//            with 16-byte loads/stores (skipped when the caller passes no
+//            x_perm: a consumer that reads the token rows through pair_row).
 // Large batches run the phases as three kernels over the whole GPU; batches of
 // at most 8192 pairs run phases 1-2 in one CTA (one launch) separated by
 // barriers, and phase 3 too when its row copy is at most 256 KB.
@@ -195,7 +196,8 @@ __device__ __forceinline__ uint32_t bf16_of_product(float w, float x) {
 }
 
 // Copy (or, with wsc, scale by the pair's routing weight) the rows of pairs
-// pb .. pb+7 into their x_perm rows; also writes pair_row and perm_src.
+// pb .. pb+7 into their x_perm rows (none when x_perm is null); also writes
+// pair_row and perm_src.
 __device__ __forceinline__ void scatter_pairs(int64_t pb, const uint16_t* __restrict__ x,
                                               const int32_t* __restrict__ slot_ids, const int32_t* __restrict__ rank,
                                               const int32_t* __restrict__ chunk_base, int S_local, int64_t P, int k,
@@ -219,6 +221,7 @@ __device__ __forceinline__ void scatter_pairs(int64_t pb, const uint16_t* __rest
         }
         pair_row[p] = row;
     }
+    if (!x_perm) return;  // routing tables only
     const int nj = (int)min((int64_t)PS_PAIRS, P - pb);
     if (!wsc) {
         // the pairs of one token share its row: each 16-byte vector of the row is loaded
@@ -364,8 +367,9 @@ __global__ void __launch_bounds__(PT_THREADS) permute_tiny_kernel(
     int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ perm_src,
     int32_t* __restrict__ pair_row, uint16_t* __restrict__ x_perm, int scale_rows, int32_t* status) {
     extern __shared__ __align__(16) unsigned char pt_smem[];
+    const size_t xb = x_perm ? (size_t)T * H * 2 : 0;                        // no rows staged without x_perm
     uint16_t* xs = reinterpret_cast<uint16_t*>(pt_smem);                      // [T][H]
-    int32_t* cnt = reinterpret_cast<int32_t*>(pt_smem + (size_t)T * H * 2);   // [S_local]
+    int32_t* cnt = reinterpret_cast<int32_t*>(pt_smem + xb);                  // [S_local]
     int32_t* off = cnt + S_local;                                             // [S_local]
     const int P = T * k;
     int32_t* s_slot = off + S_local;                                          // [P]
@@ -378,7 +382,8 @@ __global__ void __launch_bounds__(PT_THREADS) permute_tiny_kernel(
     pdl_trigger();
 
     const int vec = H / 8;
-    for (int i = tid; i < T * vec; i += PT_THREADS) cp_async16(xs + (size_t)i * 8, x + (size_t)i * 8);
+    if (x_perm)
+        for (int i = tid; i < T * vec; i += PT_THREADS) cp_async16(xs + (size_t)i * 8, x + (size_t)i * 8);
     cp_async_commit();
     for (int s = tid; s < S_local; s += PT_THREADS) cnt[s] = 0;
     __syncthreads();
@@ -468,6 +473,7 @@ __global__ void __launch_bounds__(PT_THREADS) permute_tiny_kernel(
 
     // rows of x_perm from the staged token rows (or, with the routing applied on
     // the input, bf16(w * x))
+    if (!x_perm) return;
     for (int f = tid; f < P * vec; f += PT_THREADS) {
         const int p = f / vec, v = f - p * vec;
         const int32_t row = s_row[p];
@@ -515,7 +521,7 @@ cudaError_t launch_permute(const PermuteLaunch& L, int num_sms, cudaStream_t s) 
     const int64_t nchunks = (P + PM_CHUNK - 1) / PM_CHUNK;
     int32_t* status = &L.hdr->status;
     if (P <= PM_CHUNK && L.S_local <= 2 * PT_THREADS && L.T * (int64_t)L.H * 2 <= PT_MAX_X_BYTES) {
-        const size_t smem = (size_t)L.T * L.H * 2 + (size_t)2 * L.S_local * sizeof(int32_t) +
+        const size_t smem = (L.x_perm ? (size_t)L.T * L.H * 2 : 0) + (size_t)2 * L.S_local * sizeof(int32_t) +
                             (size_t)4 * P * sizeof(int32_t);
         cudaError_t e = cudaFuncSetAttribute(permute_tiny_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem);
@@ -533,7 +539,7 @@ cudaError_t launch_permute(const PermuteLaunch& L, int num_sms, cudaStream_t s) 
             if (e != cudaSuccess) return e;
         }
         // one CTA copies at most PM_SMALL_COPY bytes of rows; more go to the scatter kernel
-        const bool copy_here = (int64_t)P * L.H * 2 <= PM_SMALL_COPY;
+        const bool copy_here = !L.x_perm || (int64_t)P * L.H * 2 <= PM_SMALL_COPY;
         cudaError_t e = launch_k("permute_small", permute_small_kernel, dim3(1), dim3(PM_SCAN_THREADS), smem_small,
                                  s, L.ids, L.w, P, L.k, L.E, L.rep_offset, L.rep_slots, L.S, L.local_start, L.local_count, L.mode,
                                  L.S_local, L.slot_ids, L.rank, L.chunk_cnt, nchunks, L.x, L.H, L.counts, L.offsets,

@@ -113,11 +113,17 @@ class MoELayer:
             moe_route(x, self.Wg, self.bias, self.k, self.renorm, v["topk_ids"], v["topk_w"], self.ws, stream)
         return v
 
+    def rows_from_tokens(self) -> bool:
+        """Whether the expert input rows are read from the token rows through pair_row (NVFP4
+        experts with the weights applied at the output): x_perm is then not written."""
+        return self.fp4 and not self.on_input
+
     def permute(self, x: torch.Tensor, stream=None) -> dict:
         v = self.views(x.shape[0])
+        xp = None if self.rows_from_tokens() else v["x_perm"]
         moe_permute(v["topk_ids"], v["topk_w"], self.E, self.rep_offset, self.rep_slots, self.S,
                     self.local_start, self.local_count, self.mode, x, v["slot_ids"], v["counts"], v["offsets"],
-                    v["perm_src"], v["pair_row"], v["x_perm"], self.ws, stream, on_input=self.on_input)
+                    v["perm_src"], v["pair_row"], xp, self.ws, stream, on_input=self.on_input)
         return v
 
     def expert_forward(self, x: torch.Tensor, stream=None) -> dict:
@@ -129,8 +135,12 @@ class MoELayer:
             q1s = f1s = s1s = q2s = f2s = s2s = None
             if self.W1sf is not None:
                 (q1s, f1s, s1s), (q2s, f2s, s2s) = self.W1sf, self.W2sf
-            moe_forward_nvfp4(v["x_perm"], v["offsets"], q1, f1, s1, q2, f2, s2, v["pair_row"], w, xs, q1s, f1s, s1s,
-                              q2s, f2s, s2s, self.gate, v["out"], self.ws, stream)
+            if self.rows_from_tokens():
+                moe_forward_nvfp4(None, v["offsets"], q1, f1, s1, q2, f2, s2, v["pair_row"], w, x, q1s, f1s, s1s,
+                                  q2s, f2s, s2s, self.gate, v["out"], self.ws, stream)
+            else:
+                moe_forward_nvfp4(v["x_perm"], v["offsets"], q1, f1, s1, q2, f2, s2, v["pair_row"], w, xs, q1s, f1s,
+                                  s1s, q2s, f2s, s2s, self.gate, v["out"], self.ws, stream)
         elif self.fp8:
             fwd = moe_forward_w8a8 if self.act8 else moe_forward_fp8
             # E4M3 activations: x also lets large batches quantise each token row once

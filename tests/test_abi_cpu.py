@@ -152,6 +152,28 @@ def test_route_grouped_rejects_bad_group_parameters_on_host():
     assert r(None, None, None, 0, 256, 32, 4, 1, 8, 2, None, None, None, 0, None) == moe.MOE_OK  # T = 0
 
 
+def test_permute_without_x_perm_and_nvfp4_token_rows_validation():
+    p = moe._lib.moe_permute
+    args = lambda x, xp: (FAKE, FAKE, 16, 2, 8, None, None, 8, 0, -1, 0, x, 256, FAKE, FAKE, FAKE, FAKE, FAKE, xp,
+                          None, 1 << 30, None)
+    assert p(*args(None, FAKE)) == moe.MOE_ERR_INVALID_ARG  # rows to copy but no token rows
+    assert p(*args(FAKE, FAKE)[:19], None, 300, None) == moe.MOE_ERR_WORKSPACE
+    assert p(*args(None, None)[:19], FAKE, 300, None) == moe.MOE_ERR_WORKSPACE  # tables only: x not needed
+    # routing on the input scales the copied rows: x_perm is required
+    assert moe._lib.moe_permute_on_input(*args(FAKE, None)) == moe.MOE_ERR_INVALID_ARG
+    f = moe._lib.moe_forward_nvfp4
+    odd = ctypes.c_void_p(FAKE.value + 2)
+
+    def fwd(x_perm, topk_w, x):
+        return f(x_perm, FAKE, 4, 32, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 256, 256, FAKE, topk_w, 16, 2, x, None,
+                 None, None, None, None, None, 0, None, FAKE, FAKE, 1 << 30, None)
+
+    assert fwd(None, FAKE, None) == moe.MOE_ERR_INVALID_ARG   # token rows need x
+    assert fwd(None, None, FAKE) == moe.MOE_ERR_INVALID_ARG   # and the weights at the output
+    assert fwd(None, FAKE, odd) == moe.MOE_ERR_INVALID_ARG    # x must be 16-byte aligned
+    assert fwd(odd, None, None) == moe.MOE_ERR_INVALID_ARG    # x_perm too, when it is read
+
+
 def test_permute_on_input_shares_the_host_validation():
     p = moe._lib.moe_permute_on_input
     # S != E without a slot table

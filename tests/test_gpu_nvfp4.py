@@ -16,8 +16,8 @@ import oracle
 import serving_router_gate_gb300 as moe
 from serving_router_gate_gb300.layer import layer_from_inputs
 
-from parity_util import (check_out, check_routing, check_x_perm, make, oracle_layer, oracle_threads, run_gpu,
-                         sample_tokens, to_cpu, unpack_e2m1)
+from parity_util import (check_out, check_routing, make, oracle_layer, oracle_threads, run_gpu, sample_tokens,
+                         to_cpu, unpack_e2m1)
 
 pytestmark = pytest.mark.gpu
 
@@ -33,8 +33,9 @@ def _check(inp, local_start=0, local_count=-1, mode=0):
     check_routing(g, dict(ids=ref["ids"], w=ref["w"], w_masked=ref["w_masked"], slots=ref["slots"],
                           counts=ref["counts"], offsets=ref["offsets"], perm_src=ref["perm_src"],
                           pair_row=ref["pair_row"]), to_cpu(inp), masked=local_count >= 0)
-    if not inp["cfg"].on_input:
-        check_x_perm(g, inp["x"].cuda(), inp["cfg"].k)
+    # weights at the output: the layer quantises token rows through pair_row and leaves
+    # x_perm unwritten; routing on the input: x_perm holds the scaled rows (checked by
+    # the permute tests)
     check_out(g["out"], ref["out"])
     st = moe.moe_get_device_status(g["layer"].ws)
     assert st == 0, f"device status {st}"
@@ -77,6 +78,55 @@ def test_quantize_nvfp4_rows_bit_exact(K, pow2):
     assert np.array_equal(sc.view(np.uint32), rsc.view(np.uint32)), "row scales differ"
 
 
+def _threshold_rows(K):
+    """Rows whose quotients v / (sb s) land exactly on the E2M1 rounding thresholds
+    (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5; round-half-even decides them) under block
+    scales that are not powers of two, so a quotient formed as v * (1 / (sb s))
+    misses the tie by a few ulps: the row amax 2688 makes s = 1 in both modes, and
+    each block's maximum 6 c makes its scale exactly c."""
+    t = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
+    cs = [1.25, 1.5, 1.75, 1.875, 3.0, 3.5, 5.0, 7.0, 0.875, 0.625, 0.5625, 13.0, 0.1875, 26.0, 112.0]
+    rows = []
+    for r in range(2):
+        row = []
+        for b in range(K // 16):
+            if b == 0:
+                blk = [2688.0] + [0.0] * 15                 # sets s = 1
+            else:
+                c = cs[(b + 3 * r) % len(cs)]
+                blk = [6.0 * c] + [x * c for x in t] + [-x * c for x in t] + [0.5 * c]
+            row += blk
+        rows.append(row)
+    v = torch.tensor(rows, dtype=torch.float64)
+    assert torch.equal(v.to(torch.bfloat16).double(), v), "threshold values are not bf16 values"
+    return v.to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("pow2", [False, True])
+def test_quantize_nvfp4_rows_exact_ties_under_odd_block_scales(pow2):
+    v = _threshold_rows(256)
+    q, sb, sc = _quantize_gpu(v, pow2)
+    rq, rsb, rsc = oracle.quantize_nvfp4_rows(v, pow2=pow2)
+    assert np.array_equal(sc.view(np.uint32), rsc.view(np.uint32)) and (rsc == 1.0).all()
+    assert np.array_equal(sb[:, :16], rsb), "block scales differ"
+    assert np.array_equal(unpack_e2m1(q), rq), "E2M1 codes differ at the rounding ties"
+
+
+@pytest.mark.parametrize("pow2", [False, True])
+def test_quantize_nvfp4_rows_bit_exact_large_random(pow2):
+    g = torch.Generator().manual_seed(77 + pow2)
+    rows, K = 2048, 4096
+    scale = torch.exp(torch.empty(rows, 1).uniform_(-12.0, 12.0, generator=g))
+    v = torch.randn(rows, K, generator=g) * scale
+    v[::7] = torch.empty(rows // 7 + 1, K).uniform_(-1.0, 1.0, generator=g) * scale[::7]
+    v = v.to(torch.bfloat16)
+    q, sb, sc = _quantize_gpu(v, pow2)
+    rq, rsb, rsc = oracle.quantize_nvfp4_rows(v, pow2=pow2)
+    assert np.array_equal(sc.view(np.uint32), rsc.view(np.uint32)), "row scales differ"
+    assert np.array_equal(sb[:, : K // 16], rsb), "block scales differ"
+    assert np.array_equal(unpack_e2m1(q), rq), "E2M1 codes differ"
+
+
 def test_quantize_nvfp4_expert_stack_as_one_matrix():
     inp = mi.make_inputs(mi.MoEConfig("q4stack", T=4, H=256, I=128, E=3, k=1, renorm=True))
     q, sb, sc = _quantize_gpu(inp["W1"], False)
@@ -116,6 +166,38 @@ def test_nvfp4_local_ranges_routing_on_input_and_replicas():
     rep = mi.MoEConfig("rep_nvfp4", T=700, H=256, I=256, E=10, S=13, n_hot=3, zipf_s=1.1, k=4, renorm=True,
                        fp4=True)
     _check(mi.make_inputs(rep))
+
+
+def _forward_from_x_perm(layer, x):
+    """The layer's forward with the expert input rows copied into x_perm by moe_permute and
+    quantised row by row (x = None: no shared experts, so nothing reads the token rows)."""
+    v = layer.route(x)
+    moe.moe_permute(v["topk_ids"], v["topk_w"], layer.E, layer.rep_offset, layer.rep_slots, layer.S,
+                    layer.local_start, layer.local_count, layer.mode, x, v["slot_ids"], v["counts"], v["offsets"],
+                    v["perm_src"], v["pair_row"], v["x_perm"], layer.ws)
+    (q1, f1, s1), (q2, f2, s2) = layer.W1f, layer.W2f
+    moe.moe_forward_nvfp4(v["x_perm"], v["offsets"], q1, f1, s1, q2, f2, s2, v["pair_row"], v["topk_w"], None,
+                          None, None, None, None, None, None, None, v["out"], layer.ws)
+    torch.cuda.synchronize()
+    return v["out"].clone()
+
+
+@pytest.mark.parametrize("T,H,local", [(3, 512, None), (700, 512, (3, 9, 0)), (700, 512, (3, 9, 1)),
+                                       (4096, 2048, None)])
+def test_nvfp4_token_rows_equal_permuted_rows(T, H, local):
+    # each token row quantised once and placed at its pairs' rows (moe_permute copies no
+    # rows) must give the bits of quantising the permuted copies one by one; 4096 x 2048
+    # takes the warp-per-row quantiser, the smaller batches the spread one
+    cfg = mi.MoEConfig(f"tok_nvfp4_{T}", T=T, H=H, I=256, E=16, k=4, renorm=True, fp4=True)
+    inp = mi.make_inputs(cfg)
+    ls, lc, mode = local if local else (0, -1, moe.MOE_NONLOCAL_SKIP)
+    layer = layer_from_inputs(inp, "cuda", local_start=ls, local_count=lc, nonlocal_mode=mode)
+    assert layer.rows_from_tokens()
+    x = inp["x"].cuda()
+    a = layer.forward(x).clone()
+    b = _forward_from_x_perm(layer, x)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert moe.moe_get_device_status(layer.ws) == 0
 
 
 def test_nvfp4_zero_tokens_determinism_and_poisoned_workspace():
