@@ -324,8 +324,9 @@ def _work(cfg, rows: int, active_slots: int):
     fc2_bytes = (w2 + rows * (I * ab + ar) + T * (Ish * ab + (ar if Ish else 0))
                  + rows * H * 2 + (T * H * 2 if Ish else 0))
     # the whole layer: both GEMMs' bytes plus the router's x and fp32 gate weights, the
-    # permuted rows written, the expert outputs read back by the combine, and out
-    layer_bytes = (fc1_bytes + fc2_bytes + cfg.E * H * 4 + T * H * 2 + rows * H * 2 + rows * H * 2
+    # permuted expert input rows written (in FC1's input format), the expert outputs read
+    # back by the combine, and out
+    layer_bytes = (fc1_bytes + fc2_bytes + cfg.E * H * 4 + T * H * 2 + rows * (H * ab + ar) + rows * H * 2
                    + (T * H * 2 if Ish else 0) + T * H * 2)
     return dict(fc1_flops=fc1_flops, fc2_flops=fc2_flops, fc1_bytes=fc1_bytes, fc2_bytes=fc2_bytes,
                 gate_flops=2.0 * T * H * cfg.E, layer_bytes=layer_bytes)

@@ -207,7 +207,8 @@ MOE_API moe_status_t moe_route_grouped(const moe_bf16_t *x, const float *gate_w,
  *                                  row count are left unspecified.  May be NULL (then
  *                                  x may be NULL too): only the routing tables are
  *                                  written, for a consumer that reads the token rows
- *                                  through pair_row (moe_forward_nvfp4)
+ *                                  through pair_row (moe_forward_nvfp4,
+ *                                  moe_forward_w8a8)
  * Rows of one slot hold its pairs in ascending pair index (a stable grouping). */
 MOE_API moe_status_t moe_permute(const int32_t *topk_ids, float *topk_w, int64_t T, int k, int E,
                          const int32_t *rep_offset, const int32_t *rep_slots, int S,
@@ -309,10 +310,12 @@ MOE_API moe_status_t moe_quantize_fp8_rows(const moe_bf16_t *w, int64_t rows, in
  * (tcgen05.mma kind::f8f6f4, fp32 accumulation), and each accumulator is
  * multiplied by its A row's and its B row's scale.  With topk_w given (weights
  * applied at the output) the rows of x_perm must be the copies of token rows
- * that moe_permute writes: for batches of more than 64 tokens the call then
- * quantises each row of x once and places its codes at the token's pair rows
- * (pair_row) without reading x_perm; otherwise, and with topk_w = NULL
- * (moe_permute_on_input) or x = NULL, it quantises the rows of x_perm.  Launches two quantisation kernels besides moe_forward's three.  The workspace regions for the
+ * that moe_permute writes: for batches of more than 64 tokens, or when x_perm
+ * is NULL, the call then quantises each row of x once and places its codes at
+ * the token's pair rows (pair_row) without reading x_perm (moe_permute with
+ * x_perm = NULL then skips the row copies); otherwise, and with topk_w = NULL
+ * (moe_permute_on_input) or x = NULL, it quantises the rows of x_perm, which
+ * must then be given.  Launches two quantisation kernels besides moe_forward's three.  The workspace regions for the
  * quantised rows are part of moe_workspace_size.  Arguments, layouts,
  * ownership and errors as moe_forward_fp8. */
 MOE_API moe_status_t moe_forward_w8a8(const moe_bf16_t *x_perm, const int32_t *offsets, int S_local, int64_t P_cap,

@@ -268,13 +268,14 @@ def moe_forward_w8a8(x_perm, offsets, W1q, s1, W2q, s2, pair_row, topk_w, x, W1s
 
 def _forward_q(fn, x_perm, offsets, W1q, s1, W2q, s2, pair_row, topk_w, x, W1sq, s1s, W2sq, s2s, shared_gate_w,
                out, ws, stream):
-    P_cap, H = x_perm.shape
     S_local = offsets.shape[0] - 1
     I = W2q.shape[2]
     T, k = pair_row.shape
+    P_cap, H = x_perm.shape if x_perm is not None else (T * k, x.shape[1])
     I_sh = 0 if W2sq is None else W2sq.shape[1]
     u8 = torch.uint8
-    st = getattr(_lib, fn)(_ptr(x_perm, "x_perm", _bf16), _ptr(offsets, "offsets", _i32), S_local, P_cap,
+    st = getattr(_lib, fn)(_ptr(x_perm, "x_perm", _bf16, allow_none=True), _ptr(offsets, "offsets", _i32), S_local,
+                           P_cap,
                               _ptr(W1q, "W1q", u8, (S_local, 2 * I, H)), _ptr(s1, "W1_scale", _f32, (S_local, 2 * I)),
                               _ptr(W2q, "W2q", u8, (S_local, H, I)), _ptr(s2, "W2_scale", _f32, (S_local, H)), H, I,
                               _ptr(pair_row, "pair_row", _i32), _ptr(topk_w, "topk_w", _f32, (T, k), allow_none=True),

@@ -581,7 +581,10 @@ static moe_status_t forward_impl(const moe_bf16_t* x_perm, const int32_t* offset
         P_cap >= (int64_t(1) << 31))
         return MOE_ERR_UNSUPPORTED;
     if (T == 0) return MOE_OK;
-    if (!x_perm || !offsets || !W1 || !W2 || !pair_row || !out) return MOE_ERR_INVALID_ARG;
+    // E4M3 activations with the weights applied at the output: the token rows of x may
+    // stand in for x_perm (each quantised once and placed at its pairs' rows)
+    const bool from_tokens = act8 && topk_w && x;
+    if ((!x_perm && !from_tokens) || !offsets || !W1 || !W2 || !pair_row || !out) return MOE_ERR_INVALID_ARG;
     if (I_shared_total > 0 && (!x || !W1s || !W2s)) return MOE_ERR_INVALID_ARG;
     if (shared_gate_w && (I_shared_total == 0 || !x)) return MOE_ERR_INVALID_ARG;
     const bool fp8 = s1 != nullptr;
@@ -598,7 +601,7 @@ static moe_status_t forward_impl(const moe_bf16_t* x_perm, const int32_t* offset
     float* y_sh_part = ks > 1 ? reinterpret_cast<float*>(base + FL.y_sh_part) : nullptr;
     moe_status_t st;
     if (act8) {
-        if (!aligned(x_perm, 16) || (I_shared_total > 0 && !aligned(x, 16))) return MOE_ERR_INVALID_ARG;
+        if ((x_perm && !aligned(x_perm, 16)) || (x && !aligned(x, 16))) return MOE_ERR_INVALID_ARG;
         // E4M3 activations: quantise the expert input rows (as many as offsets[S_local]
         // says, read on the device) and the shared experts' input, run FC1 on them,
         // quantise the intermediate rows, run FC2
@@ -606,7 +609,7 @@ static moe_status_t forward_impl(const moe_bf16_t* x_perm, const int32_t* offset
         const int64_t T_sh = I_shared_total > 0 ? T : 0;
         auto u8 = [&](size_t off) { return reinterpret_cast<uint8_t*>(base + off); };
         auto f32 = [&](size_t off) { return reinterpret_cast<float*>(base + off); };
-        if (topk_w && x && T > 64) {
+        if (from_tokens && (T > 64 || !x_perm)) {
             // weights applied at the output: the expert input rows are copies of token
             // rows, so each token row is quantised once and its codes are placed at its
             // pairs' rows (and kept for the shared experts); small batches quantise the

@@ -113,14 +113,18 @@ class MoELayer:
             moe_route(x, self.Wg, self.bias, self.k, self.renorm, v["topk_ids"], v["topk_w"], self.ws, stream)
         return v
 
-    def rows_from_tokens(self) -> bool:
-        """Whether the expert input rows are read from the token rows through pair_row (NVFP4
-        experts with the weights applied at the output): x_perm is then not written."""
-        return self.fp4 and not self.on_input
+    def rows_from_tokens(self, T: int) -> bool:
+        """Whether the expert input rows are read from the token rows through pair_row, with
+        the weights applied at the output: NVFP4 experts, and E4M3 activations for batches of
+        more than 64 tokens (smaller ones quantise the copied rows, spread over more CTAs).
+        moe_permute then copies no rows into x_perm."""
+        if self.on_input:
+            return False
+        return self.fp4 or (self.act8 and T > 64)
 
     def permute(self, x: torch.Tensor, stream=None) -> dict:
         v = self.views(x.shape[0])
-        xp = None if self.rows_from_tokens() else v["x_perm"]
+        xp = None if self.rows_from_tokens(x.shape[0]) else v["x_perm"]
         moe_permute(v["topk_ids"], v["topk_w"], self.E, self.rep_offset, self.rep_slots, self.S,
                     self.local_start, self.local_count, self.mode, x, v["slot_ids"], v["counts"], v["offsets"],
                     v["perm_src"], v["pair_row"], xp, self.ws, stream, on_input=self.on_input)
@@ -135,7 +139,7 @@ class MoELayer:
             q1s = f1s = s1s = q2s = f2s = s2s = None
             if self.W1sf is not None:
                 (q1s, f1s, s1s), (q2s, f2s, s2s) = self.W1sf, self.W2sf
-            if self.rows_from_tokens():
+            if self.rows_from_tokens(x.shape[0]):
                 moe_forward_nvfp4(None, v["offsets"], q1, f1, s1, q2, f2, s2, v["pair_row"], w, x, q1s, f1s, s1s,
                                   q2s, f2s, s2s, self.gate, v["out"], self.ws, stream)
             else:
@@ -145,7 +149,8 @@ class MoELayer:
             fwd = moe_forward_w8a8 if self.act8 else moe_forward_fp8
             # E4M3 activations: x also lets large batches quantise each token row once
             xa = x if self.act8 else xs
-            fwd(v["x_perm"], v["offsets"], self.W1q, self.s1, self.W2q, self.s2, v["pair_row"], w, xa,
+            xp = None if self.rows_from_tokens(x.shape[0]) else v["x_perm"]
+            fwd(xp, v["offsets"], self.W1q, self.s1, self.W2q, self.s2, v["pair_row"], w, xa,
                 self.W1sq, self.s1s, self.W2sq, self.s2s, self.gate, v["out"], self.ws, stream)
         else:
             moe_forward(v["x_perm"], v["offsets"], self.W1, self.W2, v["pair_row"], w, xs, self.W1s, self.W2s,

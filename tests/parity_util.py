@@ -21,6 +21,7 @@ import torch
 
 import moe_inputs as mi
 import oracle
+import serving_router_gate_gb300 as moe
 from serving_router_gate_gb300.layer import layer_from_inputs
 
 U32 = 2.0 ** -24
@@ -80,9 +81,20 @@ def run_gpu(inp: dict, local_start=0, local_count=-1, mode=0, layer=None, on_inp
     res = {k: t.cpu().clone() for k, t in v.items() if k not in ("x_perm", "out")}
     res["rows"] = rows
     res["out"] = out.cpu().clone()
-    res["x_perm"] = v["x_perm"][:rows]
+    # None: the layer's experts read the token rows through pair_row and no rows were copied
+    res["x_perm"] = None if layer.rows_from_tokens(T) else v["x_perm"][:rows]
     res["layer"] = layer
     return res
+
+
+def permute_with_rows(layer, x):
+    """Route and permute x through the layer with the rows copied into layer.x_perm (as
+    moe_permute does for every layer whose experts read x_perm); returns the views."""
+    v = layer.route(x)
+    moe.moe_permute(v["topk_ids"], v["topk_w"], layer.E, layer.rep_offset, layer.rep_slots, layer.S,
+                    layer.local_start, layer.local_count, layer.mode, x, v["slot_ids"], v["counts"], v["offsets"],
+                    v["perm_src"], v["pair_row"], v["x_perm"], layer.ws)
+    return v
 
 
 def oracle_layer(inp_cpu: dict, local_start=0, local_count=-1, mode=0, tokens=None, on_input=None):
@@ -183,7 +195,7 @@ def check_routing(g: dict, ref: dict, inp_cpu: dict, masked: bool):
 
 def check_x_perm(g: dict, x_dev: torch.Tensor, k: int):
     rows = g["rows"]
-    if rows == 0:
+    if rows == 0 or g["x_perm"] is None:
         return
     src = g["perm_src"][:rows].to(torch.int64).cuda() // k
     want = x_dev.index_select(0, src)

@@ -16,8 +16,8 @@ import oracle
 import serving_router_gate_gb300 as moe
 from serving_router_gate_gb300.layer import layer_from_inputs
 
-from parity_util import (check_out, check_routing, make, oracle_layer, oracle_threads, run_gpu, sample_tokens,
-                         to_cpu, unpack_e2m1)
+from parity_util import (check_out, check_routing, make, oracle_layer, oracle_threads, permute_with_rows, run_gpu,
+                         sample_tokens, to_cpu, unpack_e2m1)
 
 pytestmark = pytest.mark.gpu
 
@@ -112,6 +112,40 @@ def test_quantize_nvfp4_rows_exact_ties_under_odd_block_scales(pow2):
     assert np.array_equal(unpack_e2m1(q), rq), "E2M1 codes differ at the rounding ties"
 
 
+def _every_value_under_every_block_scale():
+    """Rows of 16 blocks: the first block's 2688 makes s = 1; every other block is
+    [6 c, v1 .. v15] with c an E4M3 value (so the block scale is exactly c) and the v
+    running through every finite bf16 magnitude up to 6 c, for every positive E4M3 c,
+    with alternating signs."""
+    mags = (np.arange(0, 0x7F80, dtype=np.uint32) << 16).view(np.float32)
+    blocks = []
+    for code in range(1, 127):
+        e, m = code >> 3, code & 7
+        c = (m / 8.0) * 2.0 ** -6 if e == 0 else (1 + m / 8.0) * 2.0 ** (e - 7)
+        v = mags[mags <= 6 * c].copy()
+        v[1::2] *= -1.0
+        v = np.concatenate([v, np.zeros((-len(v)) % 15, np.float32)]).reshape(-1, 15)
+        blocks.append(np.concatenate([np.full((len(v), 1), 6 * c, np.float32), v], axis=1))
+    blocks = np.concatenate(blocks)
+    blocks = np.concatenate([blocks, np.zeros(((-len(blocks)) % 15, 16), np.float32)]).reshape(-1, 15 * 16)
+    first = np.zeros((len(blocks), 16), np.float32)
+    first[:, 0] = 2688.0
+    v = torch.from_numpy(np.concatenate([first, blocks], axis=1))
+    assert torch.equal(v.to(torch.bfloat16).float(), v)
+    return v.to(torch.bfloat16)
+
+
+def test_quantize_nvfp4_division_free_codes_exhaustive_over_block_scales():
+    # power-of-two row scales take the reciprocal-and-residual path: it must give the
+    # codes of the binary32 division for every (value, block scale) pair
+    v = _every_value_under_every_block_scale()
+    q, sb, sc = _quantize_gpu(v, True)
+    rq, rsb, rsc = oracle.quantize_nvfp4_rows(v, pow2=True)
+    assert (rsc == 1.0).all() and np.array_equal(sc.view(np.uint32), rsc.view(np.uint32))
+    assert np.array_equal(sb[:, :16], rsb), "block scales differ"
+    assert np.array_equal(unpack_e2m1(q), rq), "E2M1 codes differ from the division's"
+
+
 @pytest.mark.parametrize("pow2", [False, True])
 def test_quantize_nvfp4_rows_bit_exact_large_random(pow2):
     g = torch.Generator().manual_seed(77 + pow2)
@@ -171,10 +205,7 @@ def test_nvfp4_local_ranges_routing_on_input_and_replicas():
 def _forward_from_x_perm(layer, x):
     """The layer's forward with the expert input rows copied into x_perm by moe_permute and
     quantised row by row (x = None: no shared experts, so nothing reads the token rows)."""
-    v = layer.route(x)
-    moe.moe_permute(v["topk_ids"], v["topk_w"], layer.E, layer.rep_offset, layer.rep_slots, layer.S,
-                    layer.local_start, layer.local_count, layer.mode, x, v["slot_ids"], v["counts"], v["offsets"],
-                    v["perm_src"], v["pair_row"], v["x_perm"], layer.ws)
+    v = permute_with_rows(layer, x)
     (q1, f1, s1), (q2, f2, s2) = layer.W1f, layer.W2f
     moe.moe_forward_nvfp4(v["x_perm"], v["offsets"], q1, f1, s1, q2, f2, s2, v["pair_row"], v["topk_w"], None,
                           None, None, None, None, None, None, None, v["out"], layer.ws)
@@ -192,7 +223,7 @@ def test_nvfp4_token_rows_equal_permuted_rows(T, H, local):
     inp = mi.make_inputs(cfg)
     ls, lc, mode = local if local else (0, -1, moe.MOE_NONLOCAL_SKIP)
     layer = layer_from_inputs(inp, "cuda", local_start=ls, local_count=lc, nonlocal_mode=mode)
-    assert layer.rows_from_tokens()
+    assert layer.rows_from_tokens(T)
     x = inp["x"].cuda()
     a = layer.forward(x).clone()
     b = _forward_from_x_perm(layer, x)

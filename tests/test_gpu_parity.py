@@ -14,7 +14,7 @@ import oracle
 import serving_router_gate_gb300 as moe
 from serving_router_gate_gb300.layer import layer_from_inputs
 
-from parity_util import (check_out, check_routing, check_x_perm, make, oracle_layer, oracle_routing,
+from parity_util import (check_out, check_routing, check_x_perm, make, oracle_layer, oracle_routing, permute_with_rows,
                          oracle_threads, run_gpu, sample_tokens, to_cpu)
 
 pytestmark = pytest.mark.gpu
@@ -526,6 +526,7 @@ def test_w8a8_stage_gemms_against_oracle_rows():
     hq = torch.empty((P, cfg.I), dtype=torch.uint8, device=dev)
     sh = torch.empty(P, dtype=torch.float32, device=dev)
     y = torch.empty((P, cfg.H), dtype=torch.bfloat16, device=dev)
+    permute_with_rows(layer, inp["x"].cuda())  # the layer's own forward copies no rows at this size
     moe.moe_quantize_act_rows(layer.x_perm, xq, sx)
     moe.moe_grouped_fc1_w8a8(xq, sx, layer.offsets, layer.W1q, layer.s1, None, None, None, None, h, None, layer.ws)
     moe.moe_quantize_act_rows(h, hq, sh)

@@ -39,7 +39,8 @@ def _forward(layer, x, byte):
     got["offsets"] = layer.offsets.clone()
     rows = int(layer.offsets[-1])
     got["perm_src"] = layer.perm_src[:rows].clone()
-    got["x_perm"] = layer.x_perm[:rows].clone()
+    if not layer.rows_from_tokens(T):  # else the experts read the token rows and x_perm stays unwritten
+        got["x_perm"] = layer.x_perm[:rows].clone()
     return got
 
 
