@@ -115,12 +115,13 @@ class MoELayer:
 
     def rows_from_tokens(self, T: int) -> bool:
         """Whether the expert input rows are read from the token rows through pair_row, with
-        the weights applied at the output: NVFP4 experts, and E4M3 activations for batches of
-        more than 64 tokens (smaller ones quantise the copied rows, spread over more CTAs).
-        moe_permute then copies no rows into x_perm."""
+        the weights applied at the output: quantised activations (NVFP4, or E4M3 with E4M3
+        weights) are made once per token row and placed at its pairs' rows, so moe_permute
+        copies no rows into x_perm (at every batch size this saves more in the permute than
+        the token-row quantiser gives up in parallelism)."""
         if self.on_input:
             return False
-        return self.fp4 or (self.act8 and T > 64)
+        return self.fp4 or self.act8
 
     def permute(self, x: torch.Tensor, stream=None) -> dict:
         v = self.views(x.shape[0])
