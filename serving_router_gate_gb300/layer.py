@@ -131,8 +131,10 @@ class MoELayer:
                     v["perm_src"], v["pair_row"], xp, self.ws, stream, on_input=self.on_input)
         return v
 
-    def expert_forward(self, x: torch.Tensor, stream=None) -> dict:
+    def expert_forward(self, x: torch.Tensor, stream=None, out: Optional[torch.Tensor] = None) -> dict:
         v = self.views(x.shape[0])
+        if out is not None:
+            v["out"] = out
         w = None if self.on_input else v["topk_w"]
         xs = x if (self.I_sh > 0) else None
         if self.fp4:
@@ -158,7 +160,7 @@ class MoELayer:
                         self.gate, v["out"], self.ws, stream)
         return v
 
-    def capture(self, x: torch.Tensor, pre=None, post=None) -> "torch.cuda.CUDAGraph":
+    def capture(self, x: torch.Tensor, pre=None, post=None, out: Optional[torch.Tensor] = None) -> "torch.cuda.CUDAGraph":
         """Record one forward (optionally wrapped by pre()/post() stream work, e.g.
         host<->device copies) into a CUDA graph; replaying it re-runs the same
         kernels with the same pointers.  Every library call is capturable: none
@@ -170,7 +172,7 @@ class MoELayer:
         with torch.cuda.stream(side):
             if pre:
                 pre()
-            self.forward(x)
+            self.forward(x, out=out)
             if post:
                 post()
         torch.cuda.current_stream().wait_stream(side)
@@ -179,19 +181,77 @@ class MoELayer:
         with torch.cuda.graph(g):
             if pre:
                 pre()
-            self.forward(x)
+            self.forward(x, out=out)
             if post:
                 post()
         return g
 
-    def forward(self, x: torch.Tensor, stream=None) -> torch.Tensor:
-        """out [T, H] bf16 (a view of the layer's output buffer) for x [T, H] bf16, T <= max_T."""
+    def forward(self, x: torch.Tensor, stream=None, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+        """out [T, H] bf16 for x [T, H] bf16, T <= max_T: the given device tensor, or a view
+        of the layer's own output buffer."""
         assert x.shape[0] <= self.max_T and x.shape[1] == self.H
+        if out is not None:
+            assert out.shape == x.shape and out.dtype == torch.bfloat16 and out.device == x.device
         if x.shape[0] == 0:
-            return self.out[:0]
+            return self.out[:0] if out is None else out
         self.route(x, stream)
         self.permute(x, stream)
-        return self.expert_forward(x, stream)["out"]
+        return self.expert_forward(x, stream, out)["out"]
+
+
+class HostPipeline:
+    """Forward a sequence of host batches through one layer with the host<->device copies
+    overlapping the compute: while batch i runs on the compute stream, batch i+1's input is
+    copied to the device on one copy stream and batch i-1's output to the host on another.
+    Two device input buffers and two device output buffers alternate between batches;
+    events order every buffer's copies against the forwards that use it (an input buffer
+    is refilled only after the forward two batches back has read it, an output buffer is
+    rewritten only after its previous copy to the host).  Each forward is a replay of a
+    CUDA graph captured on its buffer pair.  Host tensors must be pinned for the copies to
+    run asynchronously.  Nothing is allocated per batch and the host never waits: read the
+    outputs after the device (or the output stream) is synchronised."""
+
+    def __init__(self, layer: MoELayer, example: torch.Tensor):
+        """example: one batch [T, H] bf16 (host or device); it fixes T and is the input of
+        the forwards run while the two graphs are captured."""
+        T = example.shape[0]
+        assert 0 < T <= layer.max_T and example.shape[1] == layer.H and example.dtype == torch.bfloat16
+        dev = layer.Wg.device
+        self.layer, self.T = layer, int(T)
+        shape = (self.T, layer.H)
+        self.x_dev = [example.to(dev).clone() for _ in range(2)]
+        self.out_dev = [torch.empty(shape, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+        self.s_in, self.s_cmp, self.s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+        self.ev_in = [torch.cuda.Event() for _ in range(2)]   # input buffer b filled
+        self.ev_fwd = [torch.cuda.Event() for _ in range(2)]  # forward on buffers b done
+        self.ev_out = [torch.cuda.Event() for _ in range(2)]  # output buffer b copied to the host
+        self.graphs = [layer.capture(self.x_dev[b], out=self.out_dev[b]) for b in range(2)]
+        self.n = 0  # batches issued so far (the buffer parity carries over between calls)
+
+    def run(self, xs_host, outs_host, before_forward=None):
+        """Issue the batches: xs_host[i] ([T, H] bf16, pinned) in, outs_host[i] out.
+        before_forward(i), if given, is called on the compute stream right before
+        forward i (e.g. to flush L2 for a measurement)."""
+        assert len(xs_host) == len(outs_host)
+        for i, (xh, oh) in enumerate(zip(xs_host, outs_host)):
+            assert xh.shape == (self.T, self.layer.H) and oh.shape == (self.T, self.layer.H)
+            b = self.n & 1
+            self.n += 1
+            self.s_in.wait_event(self.ev_fwd[b])
+            with torch.cuda.stream(self.s_in):
+                self.x_dev[b].copy_(xh, non_blocking=True)
+            self.ev_in[b].record(self.s_in)
+            self.s_cmp.wait_event(self.ev_in[b])
+            self.s_cmp.wait_event(self.ev_out[b])
+            with torch.cuda.stream(self.s_cmp):
+                if before_forward is not None:
+                    before_forward(i)
+                self.graphs[b].replay()
+            self.ev_fwd[b].record(self.s_cmp)
+            self.s_out.wait_event(self.ev_fwd[b])
+            with torch.cuda.stream(self.s_out):
+                oh.copy_(self.out_dev[b], non_blocking=True)
+            self.ev_out[b].record(self.s_out)
 
 
 def layer_from_inputs(inp: dict, device="cuda", max_T: Optional[int] = None, local_start: int = 0,
