@@ -17,8 +17,8 @@
 //   3. the block's TB x H/8 16-byte output vectors are spread over the 256
 //      threads, consecutive threads on consecutive vectors of a token; each
 //      thread issues the loads of up to 8 pairs' vectors and of the shared
-//      expert's vector before using them and accumulates in fp32 in fixed j
-//      order:
+//      expert's vector before using them (with k <= 4 and a bf16 shared row,
+//      those of two vectors) and accumulates in fp32 in fixed j order:
 //        acc = fma(w_j, y[row_j], acc) for j = 0..k-1 (rows of -1 skipped),
 //        acc = fma(g, y_shared, acc), out = bf16_rn(acc),
 //      where y_shared is the bf16 shared-expert row or, when the shared FC2 ran
@@ -88,59 +88,115 @@ __global__ void __launch_bounds__(FZ_THREADS, 4) finalize_kernel(
         __syncthreads();
 
         const int items = nt * vec;
-        for (int f = threadIdx.x; f < items; f += FZ_THREADS) {
-            const int tt = f / vec;
-            const int v = f - tt * vec;
-            float acc[8];
+        if (k <= 4 && !y_sh_part) {
+            // k <= 4 and a bf16 shared row (or none): two vectors per thread at a time, the
+            // loads of both (their pairs' vectors and shared-expert vectors) in flight
+            // before either is used; the shared vectors stay packed until they are added
+            for (int f0 = threadIdx.x; f0 < items; f0 += 2 * FZ_THREADS) {
+                uint4 ld[2][4], sv[2];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-            float shf[8];
-            if (y_sh_part) {
-                // split shared expert: fp32 partials of its K ranges, added in range order
-                const float4* pp = reinterpret_cast<const float4*>(y_sh_part + (t0 + tt) * H) + 2 * v;
-                const int64_t stride = T * (int64_t)H / 4;
-                float4 lo = __ldg(pp), hi = __ldg(pp + 1);
-                for (int q = 1; q < ksplit; ++q) {
-                    const float4 a = __ldg(pp + q * stride), b = __ldg(pp + q * stride + 1);
-                    lo.x += a.x; lo.y += a.y; lo.z += a.z; lo.w += a.w;
-                    hi.x += b.x; hi.y += b.y; hi.z += b.z; hi.w += b.w;
-                }
-                shf[0] = lo.x; shf[1] = lo.y; shf[2] = lo.z; shf[3] = lo.w;
-                shf[4] = hi.x; shf[5] = hi.y; shf[6] = hi.z; shf[7] = hi.w;
-            } else if (y_sh) {
-                unpack8(__ldg(reinterpret_cast<const uint4*>(y_sh + (t0 + tt) * H) + v), shf);
-            }
-            for (int j0 = 0; j0 < k; j0 += FZ_BATCH) {
-                uint4 ld[FZ_BATCH];
-                int32_t rr[FZ_BATCH];
+                for (int u = 0; u < 2; ++u) {
+                    const int f = f0 + u * FZ_THREADS;
+                    const bool ok = f < items;
+                    const int tt = ok ? f / vec : 0;
+                    const int v = ok ? f - tt * vec : 0;
 #pragma unroll
-                for (int b = 0; b < FZ_BATCH; ++b) {
-                    const int j = j0 + b;
-                    rr[b] = j < k ? s_row[tt][j] : -1;
-                    ld[b] = rr[b] >= 0 ? __ldg(reinterpret_cast<const uint4*>(y + (int64_t)rr[b] * H) + v)
-                                       : make_uint4(0, 0, 0, 0);
+                    for (int b = 0; b < 4; ++b) {
+                        const int32_t r = (ok && b < k) ? s_row[tt][b] : -1;
+                        ld[u][b] = r >= 0 ? __ldg(reinterpret_cast<const uint4*>(y + (int64_t)r * H) + v)
+                                          : make_uint4(0, 0, 0, 0);
+                    }
+                    sv[u] = (ok && y_sh) ? __ldg(reinterpret_cast<const uint4*>(y_sh + (t0 + tt) * H) + v)
+                                         : make_uint4(0, 0, 0, 0);
                 }
 #pragma unroll
-                for (int b = 0; b < FZ_BATCH; ++b) {
-                    if (rr[b] < 0) continue;
-                    const float wj = s_w[tt][j0 + b];
-                    float fv[8];
-                    unpack8(ld[b], fv);
+                for (int u = 0; u < 2; ++u) {
+                    const int f = f0 + u * FZ_THREADS;
+                    if (f >= items) continue;
+                    const int tt = f / vec;
+                    const int v = f - tt * vec;
+                    float acc[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, fv[i], acc[i]);
+                    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) {  // fixed j order
+                        if (b >= k || s_row[tt][b] < 0) continue;
+                        const float wj = s_w[tt][b];
+                        float fv[8];
+                        unpack8(ld[u][b], fv);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, fv[i], acc[i]);
+                    }
+                    if (has_sh) {
+                        const float g = gated ? s_g[tt] : 1.0f;
+                        float shf[8];
+                        unpack8(sv[u], shf);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) acc[i] = fmaf(g, shf[i], acc[i]);
+                    }
+                    uint4 o;
+                    o.x = pack_bf16x2(acc[0], acc[1]);
+                    o.y = pack_bf16x2(acc[2], acc[3]);
+                    o.z = pack_bf16x2(acc[4], acc[5]);
+                    o.w = pack_bf16x2(acc[6], acc[7]);
+                    reinterpret_cast<uint4*>(out + (t0 + tt) * H)[v] = o;
                 }
             }
-            if (has_sh) {
-                const float g = gated ? s_g[tt] : 1.0f;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) acc[i] = fmaf(g, shf[i], acc[i]);
+        } else {
+            for (int f = threadIdx.x; f < items; f += FZ_THREADS) {
+                const int tt = f / vec;
+                const int v = f - tt * vec;
+                float acc[8];
+    #pragma unroll
+                for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+                float shf[8];
+                if (y_sh_part) {
+                    // split shared expert: fp32 partials of its K ranges, added in range order
+                    const float4* pp = reinterpret_cast<const float4*>(y_sh_part + (t0 + tt) * H) + 2 * v;
+                    const int64_t stride = T * (int64_t)H / 4;
+                    float4 lo = __ldg(pp), hi = __ldg(pp + 1);
+                    for (int q = 1; q < ksplit; ++q) {
+                        const float4 a = __ldg(pp + q * stride), b = __ldg(pp + q * stride + 1);
+                        lo.x += a.x; lo.y += a.y; lo.z += a.z; lo.w += a.w;
+                        hi.x += b.x; hi.y += b.y; hi.z += b.z; hi.w += b.w;
+                    }
+                    shf[0] = lo.x; shf[1] = lo.y; shf[2] = lo.z; shf[3] = lo.w;
+                    shf[4] = hi.x; shf[5] = hi.y; shf[6] = hi.z; shf[7] = hi.w;
+                } else if (y_sh) {
+                    unpack8(__ldg(reinterpret_cast<const uint4*>(y_sh + (t0 + tt) * H) + v), shf);
+                }
+                for (int j0 = 0; j0 < k; j0 += FZ_BATCH) {
+                    uint4 ld[FZ_BATCH];
+                    int32_t rr[FZ_BATCH];
+    #pragma unroll
+                    for (int b = 0; b < FZ_BATCH; ++b) {
+                        const int j = j0 + b;
+                        rr[b] = j < k ? s_row[tt][j] : -1;
+                        ld[b] = rr[b] >= 0 ? __ldg(reinterpret_cast<const uint4*>(y + (int64_t)rr[b] * H) + v)
+                                           : make_uint4(0, 0, 0, 0);
+                    }
+    #pragma unroll
+                    for (int b = 0; b < FZ_BATCH; ++b) {
+                        if (rr[b] < 0) continue;
+                        const float wj = s_w[tt][j0 + b];
+                        float fv[8];
+                        unpack8(ld[b], fv);
+    #pragma unroll
+                        for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, fv[i], acc[i]);
+                    }
+                }
+                if (has_sh) {
+                    const float g = gated ? s_g[tt] : 1.0f;
+    #pragma unroll
+                    for (int i = 0; i < 8; ++i) acc[i] = fmaf(g, shf[i], acc[i]);
+                }
+                uint4 o;
+                o.x = pack_bf16x2(acc[0], acc[1]);
+                o.y = pack_bf16x2(acc[2], acc[3]);
+                o.z = pack_bf16x2(acc[4], acc[5]);
+                o.w = pack_bf16x2(acc[6], acc[7]);
+                reinterpret_cast<uint4*>(out + (t0 + tt) * H)[v] = o;
             }
-            uint4 o;
-            o.x = pack_bf16x2(acc[0], acc[1]);
-            o.y = pack_bf16x2(acc[2], acc[3]);
-            o.z = pack_bf16x2(acc[4], acc[5]);
-            o.w = pack_bf16x2(acc[6], acc[7]);
-            reinterpret_cast<uint4*>(out + (t0 + tt) * H)[v] = o;
         }
         __syncthreads();  // the next block rewrites the shared arrays
     }
