@@ -1,8 +1,7 @@
 """The bounds-checked library (compiled with MOE_CHECKED: kernels test every
 data-dependent global index -- permutation rows, GEMM output rows -- and report
 MOE_ERR_DEVICE_BOUNDS instead of accessing out of range) runs the mid-size
-parity tests clean: a stand-in for a memory checker, which this GPU pool does
-not offer.  The tests run in a child process with MOE_CHECKED=1, which makes
+parity tests clean: a stand-in for a run under a memory checker.  The tests run in a child process with MOE_CHECKED=1, which makes
 the binding load the checked build; each of them requires a clean device
 status word after its forward, so any failed check fails the run."""
 import os

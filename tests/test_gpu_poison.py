@@ -1,5 +1,5 @@
 """Reads of memory no kernel wrote, exposed by poisoning (a stand-in for a race
-and initialisation checker, which this GPU pool does not offer).
+and initialisation checker).
 
 Every buffer of a layer that a forward writes before it reads -- routing
 outputs, permutation outputs, x_perm, out, and the workspace body behind its
