@@ -11,9 +11,9 @@ passage of the source pages each step follows.
 
 Parity status of each function (see tests/test_oracle_pins.py for the pins):
   route, slot_map, local_mask, permute, expert_mlp, moe_tokens, bf16 rounding,
-  the E4M3 and NVFP4 quantisers and expert MLPs: pinned (closed forms, brute
-  force, invariants, independent numpy/torch routines).  No function here is
-  "parity unpinned".  The NVFP4 functions serve a GPU path not built yet.
+  the E4M3 and NVFP4 quantisers and expert MLPs, a2a_regroup: pinned (closed
+  forms, brute force, invariants, hand-worked examples, independent
+  numpy/torch routines).  No function here is "parity unpinned".
 """
 from __future__ import annotations
 
@@ -206,6 +206,26 @@ def permute(slots, S: int):
     lib.oracle_permute(_ptr(slots), P, S, _ptr(counts), _ptr(offsets), _ptr(perm_src), _ptr(pair_row))
     total = int(offsets[S])
     return counts, offsets, perm_src[:total].copy(), pair_row[:P].copy()
+
+
+def a2a_regroup(recv_counts):
+    """The GEMM order of the rows one rank receives in the all-to-all dispatch.
+
+    recv_counts [N, S_local]: rows source rank n sent for local slot c.  The rows
+    arrive source by source, each source's rows grouped by slot (the order of its
+    own permutation), so exchange row q belongs to local slot c of the block (n, c)
+    that holds it.  The experts take the rows grouped by slot, each slot's rows in
+    arrival order: a stable grouping by slot -- oracle_permute with one pair per
+    row.  Returns (offsets [S_local+1], gemm_row [R]: the GEMM-order row of each
+    exchange-order row, exch_row [R]: the inverse)."""
+    rc = np.asarray(recv_counts, dtype=np.int64)
+    N, S_l = rc.shape
+    if (rc < 0).any():
+        raise ValueError("negative count")
+    slot_of_row = [c for n in range(N) for c in range(S_l) for _ in range(int(rc[n, c]))]
+    slots = np.asarray(slot_of_row, dtype=np.int32).reshape(-1, 1)
+    counts, offsets, perm_src, pair_row = permute(slots, S_l)
+    return offsets, pair_row, perm_src
 
 
 def expert_mlp(x_row, W1, W2):

@@ -905,3 +905,60 @@ def test_nvfp4_layer_matches_numpy_mlp_of_dequantised_values():
             e = int(res["ids"][t, 0])
             ref = mlp(inp["x"][t], D1[e], D2[e]) + mlp(inp["x"][t], S1, S2)
             np.testing.assert_allclose(res["out"][t], ref, rtol=0, atol=1e-9 * np.abs(ref).max())
+
+
+# --------------------------------------------------------------------------- all-to-all receive order
+
+def _a2a_golden_cases():
+    cases, cur = [], None
+    for ln in _read_golden("a2a_regroup_example.txt"):
+        key, *vals = ln.split()
+        if key == "case":
+            cur = dict(N=int(vals[0]), S=int(vals[1]))
+            cases.append(cur)
+        else:
+            cur[key] = [int(v) for v in vals]
+    return cases
+
+
+def test_a2a_regroup_golden_examples():
+    cases = _a2a_golden_cases()
+    assert len(cases) == 3
+    for c in cases:
+        counts = np.array(c["counts"], np.int32).reshape(c["N"], c["S"])
+        offsets, gemm_row, exch_row = oracle.a2a_regroup(counts)
+        assert offsets.tolist() == c["offsets"]
+        assert gemm_row.tolist() == c["gemm_row"]
+        assert exch_row.tolist() == np.argsort(np.array(c["gemm_row"], np.int64)).tolist()
+
+
+@pytest.mark.parametrize("N,S_l,seed", [(2, 5, 0), (4, 3, 1), (8, 36, 2), (3, 1, 3), (1, 7, 4)])
+def test_a2a_regroup_invariants(N, S_l, seed):
+    g = torch.Generator().manual_seed(seed)
+    counts = torch.randint(0, 6, (N, S_l), generator=g).numpy().astype(np.int32)
+    counts[0, 0] = 0  # an empty block
+    offsets, gemm_row, exch_row = oracle.a2a_regroup(counts)
+    R = int(counts.sum())
+    # a bijection of the R received rows
+    assert sorted(gemm_row.tolist()) == list(range(R))
+    assert np.array_equal(exch_row[gemm_row], np.arange(R))
+    # slot c holds the column sum of its counts, contiguously from offsets[c]
+    assert np.array_equal(np.diff(offsets), counts.sum(0))
+    # walk the arrival order: block (n, c) lands inside slot c, after the blocks of
+    # sources n' < n for that slot, its rows in arrival order
+    q = 0
+    for n in range(N):
+        for c in range(S_l):
+            base = offsets[c] + counts[:n, c].sum()
+            for i in range(counts[n, c]):
+                assert gemm_row[q] == base + i
+                q += 1
+    assert q == R
+    # N = 1: arrival order is already grouped by slot (the identity)
+    if N == 1:
+        assert np.array_equal(gemm_row, np.arange(R))
+
+
+def test_a2a_regroup_rejects_negative_counts():
+    with pytest.raises(ValueError):
+        oracle.a2a_regroup(np.array([[1, -1]], np.int32))
