@@ -17,8 +17,10 @@ right before every kernel and one after the last.  With N > 1 (torchrun, or
 started by this script), the ranks split the layer by experts (--partition ep,
 the default: every rank routes the same batch, computes its contiguous slot
 range and its shard of the shared experts, and one all-reduce sums the
-partials; strong scaling) or run independent batches (--partition replicas;
-weak scaling, no collective).
+partials; strong scaling), exchange rows all-to-all (--partition a2a: every rank
+holds its own batch, sends each pair's row to the rank owning its slot and gets
+the expert outputs back; weak scaling) or run independent batches (--partition
+replicas; weak scaling, no collective).
 `--impl reference` times the fp64 CPU oracle on a bounded sample instead.
 """
 from __future__ import annotations
@@ -416,6 +418,21 @@ def _ep_layer(inp, cfg, world, rank, dev):
                       n_group=cfg.n_group, topk_group=cfg.topk_group, fp8=cfg.fp8, act8=cfg.act8, fp4=cfg.fp4)
 
 
+def _a2a_layer(inp, cfg, world, rank, dev):
+    """This rank's all-to-all expert-parallel layer over the workload's weights."""
+    from serving_router_gate_gb300.expert_parallel import EPAllToAllLayer
+    if cfg.fp8 or cfg.fp4:
+        raise SystemExit("bench.py: --partition a2a runs bf16 weights only")
+    W1s = W2s = None
+    if inp["W1s"] is not None:
+        W1s, W2s = mi.shared_concat(inp["W1s"], inp["W2s"])
+    d = lambda t: None if t is None else t.to(dev).contiguous()  # noqa: E731
+    return EPAllToAllLayer(d(inp["Wg"]), d(inp["W1"]), d(inp["W2"]), cfg.k, cfg.renorm, cfg.T, world, rank,
+                           logit_bias=d(inp["bias"]), rep_offset=d(inp["rep_offset"]),
+                           rep_slots=d(inp["rep_slots"]), W1s=d(W1s), W2s=d(W2s), shared_gate_w=d(inp["w_s"]),
+                           n_group=cfg.n_group, topk_group=cfg.topk_group, on_input=cfg.on_input)
+
+
 def bench_ours(args):
     import serving_router_gate_gb300 as moe
     from serving_router_gate_gb300.layer import HostPipeline, layer_from_inputs
@@ -428,8 +445,12 @@ def bench_ours(args):
     # its slot range and shared shard, and one all-reduce sums the partials; otherwise
     # (replicas) every rank runs its own batch through the whole layer
     ep = _ep_layer(inp, cfg, ws_, rank, dev) if (args.partition == "ep" and ws_ > 1) else None
+    # all-to-all expert parallelism: every rank holds its own batch of T tokens and the
+    # experts of its slot range; rows travel to their slots' ranks and back (NCCL).  The
+    # per-kernel pass and the roofline then describe the one-GPU layer on the rank's batch.
+    a2a = _a2a_layer(inp, cfg, ws_, rank, dev) if (args.partition == "a2a" and ws_ > 1) else None
     layer = ep.layer if ep is not None else layer_from_inputs(inp, dev)
-    x = inp["x"]
+    x = mi.rank_tokens(cfg, rank, cfg.T, dev) if a2a is not None else inp["x"]
     T, H = cfg.T, cfg.H
     stream = torch.cuda.current_stream()
     K, W = args.steps, args.warmup
@@ -443,10 +464,18 @@ def bench_ours(args):
     if status:
         raise RuntimeError(f"device status {status} after warm-up")
 
+    if a2a is not None:
+        for _ in range(W):
+            a2a.forward(x)
+        torch.cuda.synchronize()
     # launches one layer forward issues (the same kernels a graph replay re-issues)
     c0 = moe.moe_get_launch_count()
     layer.forward(x)
     kernels_per_step = moe.moe_get_launch_count() - c0
+    if a2a is not None:
+        c0 = moe.moe_get_launch_count()
+        a2a.forward(x)
+        a2a_launches = moe.moe_get_launch_count() - c0
     refined_per_step = moe.moe_get_route_stats(layer.ws) / (W + 1)
     flush = L2Flush(dev)
 
@@ -456,7 +485,9 @@ def bench_ours(args):
     # recorded on the stream around each replay also time the graph's own launch, a
     # cost a model-level graph pays once per model step rather than once per layer;
     # both are reported.
-    graph_ok = args.graph and ep is None  # the expert-parallel step runs eagerly (NCCL in the step)
+    # the expert-parallel steps run eagerly (NCCL in the step; the all-to-all one also waits
+    # for its split sizes on the host)
+    graph_ok = args.graph and ep is None and a2a is None
     inner = _external_events() if graph_ok else None
     if graph_ok:
         pre = (lambda: inner[0].record()) if inner else None
@@ -464,8 +495,14 @@ def bench_ours(args):
         graph = layer.capture(x, pre=pre, post=post)
     else:
         graph = None
-    step = graph.replay if graph is not None else ((lambda: ep.forward(x)) if ep is not None
-                                                   else (lambda: layer.forward(x)))
+    if graph is not None:
+        step = graph.replay
+    elif ep is not None:
+        step = lambda: ep.forward(x)  # noqa: E731
+    elif a2a is not None:
+        step = lambda: a2a.forward(x)  # noqa: E731
+    else:
+        step = lambda: layer.forward(x)  # noqa: E731
     for _ in range(W):
         step()
 
@@ -532,6 +569,8 @@ def bench_ours(args):
             h2d()
             if ep is not None:
                 layer.out[:T].copy_(ep.forward(x_dev))
+            elif a2a is not None:
+                layer.out[:T].copy_(a2a.forward(x_dev))
             else:
                 layer.forward(x_dev)
             d2h()
@@ -626,6 +665,10 @@ def bench_ours(args):
         "config": {"workload": cfg.name, "shape": mi.describe(cfg), "tokens_per_gpu": T,
                    "parallelism": (f"expert parallel x{ws_} (contiguous slot ranges, shared-expert shards, one "
                                    f"fp32 all-reduce of the partials)" if ep is not None else
+                                   f"all-to-all expert parallel x{ws_} (each rank its own batch, contiguous "
+                                   f"slot ranges, rows dispatched to their slots' ranks and returned; the "
+                                   f"per-kernel pass and roofline: the one-GPU layer on the rank's batch)"
+                                   if a2a is not None else
                                    f"replicas x{ws_} (independent token batches, no collective)"),
                    "cuda_graph": bool(graph_ok),
                    "l2": f"flushed before every timed step ({flush.describe()}); each step timed by "
@@ -634,7 +677,7 @@ def bench_ours(args):
         "e2e": {"value": total_tokens / (ms_e2e * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2,
                 "d2h_bytes_per_step": T * H * 2, "ms_per_step": ms_e2e, "method": e2e_how,
                 "serial": {"value": total_tokens / (ms_e2e_serial * 1e-3), "ms_per_step": ms_e2e_serial}},
-        "gpu_launches": kernels_per_step * K,
+        "gpu_launches": (a2a_launches if a2a is not None else kernels_per_step) * K,
         "clocks": clk,
         "kernels_ms": kernel_ms,
         "launches_ms": launches_ms,
@@ -728,9 +771,10 @@ def main():
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="launch every step from Python instead of replaying a CUDA graph of one step")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--partition", choices=["ep", "replicas"], default="ep",
-                    help="with more than one rank: expert parallelism over one batch (default) or independent "
-                         "replicas, each with its own batch")
+    ap.add_argument("--partition", choices=["ep", "a2a", "replicas"], default="ep",
+                    help="with more than one rank: expert parallelism over one batch with one reduction "
+                         "(default), all-to-all expert parallelism (each rank its own batch, rows dispatched "
+                         "to their experts' ranks and back) or independent replicas, each with its own batch")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

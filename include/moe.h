@@ -459,6 +459,38 @@ MOE_API moe_status_t moe_finalize(const moe_bf16_t *y, int64_t rows_cap, const i
                           const moe_bf16_t *shared_gate_w, moe_bf16_t *out,
                           void *ws, size_t ws_bytes, moe_stream_t stream);
 
+/* ---- all-to-all expert parallelism --------------------------------------- */
+
+/* moe_a2a_regroup -- the row reorder of one rank of the all-to-all
+ * expert-parallel layer ([TRT-10985] sequence diagram, all-to-all path: the
+ * tokens are dispatched to the ranks responsible for their experts, each rank
+ * computes the MoE on its local experts, the results go back to the tokens'
+ * ranks).  Each rank sends its moe_permute rows (grouped by slot; the slots of
+ * one destination rank are a contiguous range), so a rank receives them in
+ * EXCHANGE order: source rank 0's rows, then rank 1's, ...; inside a source's
+ * block, its rows of local slot 0, then slot 1, ...  The grouped GEMMs take
+ * GEMM order: slot 0's rows, then slot 1's, ...; inside a slot, the rows of
+ * source 0, then source 1, ... (each source's rows in the order it sent them).
+ * The call copies whole rows from one order to the other:
+ *
+ *   recv_counts [N, S_local] int32   rows source rank n sent for local slot c
+ *                                    (the counts exchanged before the rows)
+ *   N, S_local   ranks and local slots, N * S_local <= 4096 (MOE_ERR_UNSUPPORTED)
+ *   src, dst     [rows_cap, H] bf16, distinct buffers; rows past the total
+ *                sum(recv_counts) are neither read nor written
+ *   direction    MOE_A2A_TO_GEMM: src in exchange order, dst in GEMM order;
+ *                MOE_A2A_TO_EXCHANGE: src in GEMM order, dst in exchange order
+ *   offsets      [S_local + 1] int32 out, or NULL: the GEMM-order row offsets of
+ *                the local slots (offsets[S_local] = total), for moe_grouped_fc1/fc2
+ *   ws           workspace: only its status word is used
+ *
+ * A negative count, or a total above rows_cap, sets MOE_ERR_DEVICE_BOUNDS in the
+ * status word and moves no row (offsets are then not written). */
+enum { MOE_A2A_TO_GEMM = 0, MOE_A2A_TO_EXCHANGE = 1 };
+MOE_API moe_status_t moe_a2a_regroup(const int32_t *recv_counts, int N, int S_local, const moe_bf16_t *src,
+                                     moe_bf16_t *dst, int64_t rows_cap, int H, int direction, int32_t *offsets,
+                                     void *ws, size_t ws_bytes, moe_stream_t stream);
+
 /* ---- diagnostics ---------------------------------------------------------- */
 
 /* Launch one block whose single thread waits on an mbarrier that nothing ever

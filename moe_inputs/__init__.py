@@ -24,7 +24,8 @@ shared gate vector w_s ~ N(0, 0.02) in bf16.
 
 Seeding: tensor number i of a workload draws from its own torch.Generator
 seeded with seed * 1000 + i, in the order x (0), Wg (1), W1 (2), W2 (3), W1s
-(4), W2s (5), w_s (6), expert hotness order (7), slot shuffle (8).  Tensors
+(4), W2s (5), w_s (6), expert hotness order (7), slot shuffle (8); the own
+batch of expert-parallel rank r (all-to-all layer) is tensor 100 + r.  Tensors
 drawn on a CUDA device use a CUDA generator and so differ from CPU draws with
 the same seed; within one run both sides of every check read the same bytes.
 
@@ -206,6 +207,13 @@ def make_inputs(cfg: MoEConfig, device="cpu", weights_device=None) -> dict:
     return dict(cfg=cfg, x=x, Wg=Wg, bias=bias, W1=W1, W2=W2, W1s=W1s, W2s=W2s, w_s=w_s,
                 rep_offset=_dev(tab["rep_offset"]), rep_slots=_dev(tab["rep_slots"]),
                 expert_of_slot=tab["expert_of_slot"], rank=tab["rank"])
+
+
+def rank_tokens(cfg: MoEConfig, rank: int, T: int, device="cpu") -> torch.Tensor:
+    """Token rows [T, H] bf16 of one rank's own batch (expert parallelism with attention
+    data parallelism: every rank holds different tokens), N(0, 1) like x, drawn from the
+    generator seeded with seed * 1000 + 100 + rank."""
+    return _normal((T, cfg.H), 1.0, _gen(device, cfg.seed, 100 + rank), device, torch.bfloat16)
 
 
 def shared_concat(W1s: torch.Tensor, W2s: torch.Tensor):

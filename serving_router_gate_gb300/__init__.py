@@ -28,7 +28,8 @@ __all__ = [
     "moe_quantize_fp8_rows", "moe_forward_w8a8", "moe_quantize_act_rows", "moe_grouped_fc1_fp8",
     "moe_forward_nvfp4", "moe_quantize_nvfp4_rows", "nvfp4_sf_row_bytes", "MOE_WS_HEADER_BYTES",
     "moe_grouped_fc2_fp8", "moe_grouped_fc1_w8a8", "moe_grouped_fc2_w8a8", "moe_launch_events_arm",
-    "moe_launch_events_mark", "moe_launch_events_used", "EXPORTED_SYMBOLS",
+    "moe_launch_events_mark", "moe_launch_events_used", "EXPORTED_SYMBOLS", "moe_a2a_regroup",
+    "MOE_A2A_TO_GEMM", "MOE_A2A_TO_EXCHANGE",
 ]
 
 MOE_OK = 0
@@ -40,6 +41,8 @@ MOE_ERR_DEVICE_BOUNDS = 8
 MOE_ERR_TIMEOUT = 16
 MOE_NONLOCAL_SKIP = 0
 MOE_NONLOCAL_MOD = 1
+MOE_A2A_TO_GEMM = 0
+MOE_A2A_TO_EXCHANGE = 1
 MOE_LAUNCH_LABEL_BYTES = 48  # bytes per label written by moe_launch_events_used
 MOE_WS_HEADER_BYTES = 256    # the workspace header (status word, counters) a caller never writes
 
@@ -51,7 +54,7 @@ EXPORTED_SYMBOLS = (
     "moe_forward_fp8", "moe_quantize_fp8_rows", "moe_grouped_fc1_fp8", "moe_grouped_fc2_fp8",
     "moe_forward_nvfp4", "moe_quantize_nvfp4_rows",
     "moe_forward_w8a8", "moe_quantize_act_rows", "moe_grouped_fc1_w8a8", "moe_grouped_fc2_w8a8",
-    "moe_launch_events_arm", "moe_launch_events_mark", "moe_launch_events_used",
+    "moe_launch_events_arm", "moe_launch_events_mark", "moe_launch_events_used", "moe_a2a_regroup",
 )
 
 
@@ -101,6 +104,7 @@ def _load():
         "moe_grouped_fc1": ([P, i64, P, i32, P, i32, i32, P, i64, P, i32, P, P, P, sz, P], i32),
         "moe_grouped_fc2": ([P, i64, P, i32, P, i32, i32, P, i64, P, i32, P, P, P, sz, P], i32),
         "moe_finalize": ([P, i64, P, P, i64, i32, i32, P, P, P, P, P, sz, P], i32),
+        "moe_a2a_regroup": ([P, i32, i32, P, P, i64, i32, i32, P, P, sz, P], i32),
         "moe_debug_wait_timeout": ([P, sz, u64, P], i32),
         "moe_set_wait_timeout_ns": ([u64], None),
         "moe_route_noalloc": ([P, P, P, i64, i32, i32, i32, i32, P, P, P], i32),
@@ -480,6 +484,19 @@ def moe_finalize(y, pair_row, topk_w, y_shared, x, shared_gate_w, out, ws, strea
                            _ptr(shared_gate_w, "shared_gate_w", _bf16, (H,), allow_none=True),
                            _ptr(out, "out", _bf16, (T, H)), _ptr(ws, "ws", torch.uint8), ws.numel(), _stream(stream))
     _check("moe_finalize", st)
+
+
+def moe_a2a_regroup(recv_counts, src, dst, direction, offsets, ws, stream=None):
+    """Rows of an all-to-all expert-parallel rank from exchange order to GEMM order
+    (direction MOE_A2A_TO_GEMM, offsets [S_local+1] written unless None) or back
+    (MOE_A2A_TO_EXCHANGE).  recv_counts [N, S_local] int32; src, dst [rows_cap, H] bf16."""
+    N, S_l = recv_counts.shape
+    rows_cap, H = src.shape
+    st = _lib.moe_a2a_regroup(_ptr(recv_counts, "recv_counts", _i32, (N, S_l)), N, S_l, _ptr(src, "src", _bf16),
+                              _ptr(dst, "dst", _bf16, (rows_cap, H)), rows_cap, H, int(direction),
+                              _ptr(offsets, "offsets", _i32, (S_l + 1,), allow_none=True),
+                              _ptr(ws, "ws", torch.uint8), ws.numel(), _stream(stream))
+    _check("moe_a2a_regroup", st)
 
 
 def moe_debug_wait_timeout(ws, timeout_ns, stream=None):

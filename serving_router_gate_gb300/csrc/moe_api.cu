@@ -855,6 +855,31 @@ moe_status_t moe_quantize_fp8_rows(const moe_bf16_t* w, int64_t rows, int K, uin
     return cuda_status(launch_quantize_fp8_rows(w, rows, K, q, scale, device_sms(), (cudaStream_t)stream));
 }
 
+moe_status_t moe_a2a_regroup(const int32_t* recv_counts, int N, int S_local, const moe_bf16_t* src, moe_bf16_t* dst,
+                             int64_t rows_cap, int H, int direction, int32_t* offsets, void* ws, size_t ws_bytes,
+                             moe_stream_t stream) {
+    MOE_NVTX("moe_a2a_regroup");
+    if (N < 1 || S_local < 1 || rows_cap < 0 || H <= 0) return MOE_ERR_INVALID_ARG;
+    if (direction != MOE_A2A_TO_GEMM && direction != MOE_A2A_TO_EXCHANGE) return MOE_ERR_INVALID_ARG;
+    if ((int64_t)N * S_local > kA2aMaxBlocks || !dim_ok(H) || rows_cap > INT32_MAX) return MOE_ERR_UNSUPPORTED;
+    if (!recv_counts) return MOE_ERR_INVALID_ARG;
+    if (rows_cap > 0 && (!src || !dst || src == dst || !aligned(src, 16) || !aligned(dst, 16)))
+        return MOE_ERR_INVALID_ARG;
+    if (!ws || ws_bytes < kWsHeaderBytes) return MOE_ERR_WORKSPACE;
+    A2aRegroupLaunch L;
+    L.recv_counts = recv_counts;
+    L.N = N;
+    L.S_local = S_local;
+    L.rows_cap = rows_cap;
+    L.H = H;
+    L.src = src;
+    L.dst = dst;
+    L.to_exchange = direction == MOE_A2A_TO_EXCHANGE;
+    L.offsets = offsets;
+    L.hdr = static_cast<WsHeader*>(ws);
+    return cuda_status(launch_a2a_regroup(L, device_sms(), (cudaStream_t)stream));
+}
+
 moe_status_t moe_debug_wait_timeout(void* ws, size_t ws_bytes, uint64_t timeout_ns, moe_stream_t stream) {
     if (!ws || ws_bytes < kWsHeaderBytes) return MOE_ERR_WORKSPACE;
     if (timeout_ns == 0 || timeout_ns > 10000000000ull) return MOE_ERR_INVALID_ARG;

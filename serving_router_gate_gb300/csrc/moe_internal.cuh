@@ -503,6 +503,23 @@ struct FinalizeLaunch {
 };
 cudaError_t launch_finalize(const FinalizeLaunch& L, int num_sms, cudaStream_t s);
 
+// Rows of an all-to-all expert-parallel rank between exchange order and GEMM order
+// (moe_a2a_regroup).
+struct A2aRegroupLaunch {
+    const int32_t* recv_counts;  // [N, S_local]
+    int N, S_local;
+    int64_t rows_cap;
+    int H;
+    const uint16_t* src;
+    uint16_t* dst;
+    bool to_exchange;            // false: exchange -> GEMM order; true: GEMM -> exchange order
+    int32_t* offsets;            // [S_local + 1] GEMM-order slot offsets, or null
+    WsHeader* hdr;
+};
+constexpr int kA2aMaxBlocks = 4096;  // N * S_local the shared-memory tables hold
+size_t a2a_regroup_smem_bytes(int N, int S_local);
+cudaError_t launch_a2a_regroup(const A2aRegroupLaunch& L, int num_sms, cudaStream_t s);
+
 cudaError_t launch_wait_timeout_probe(WsHeader* hdr, uint64_t timeout_ns, cudaStream_t s);
 
 // Row-wise E4M3 quantisation of a bf16 matrix [rows, K] (moe_quantize_fp8_rows).

@@ -30,6 +30,7 @@ from typing import Optional, Tuple
 
 import torch
 
+from . import MOE_NONLOCAL_SKIP
 from .layer import MoELayer
 
 
@@ -112,3 +113,237 @@ class EPMoELayer:
 
     def forward(self, x: torch.Tensor, stream=None) -> torch.Tensor:
         return ep_reduce_output(self.partial(x, stream), self.group)
+
+
+# ----------------------------------------------------------------------------- all-to-all dispatch and combine
+
+def a2a_count_splits(S: int, world: int):
+    """Per-slot counts a rank sends to each rank: the counts of that rank's slot range,
+    so the splits are the ranges' sizes (every rank receives S_local counts per source)."""
+    return [ep_slot_range(S, world, d)[1] for d in range(world)]
+
+
+def a2a_send_splits(offsets, S: int, world: int):
+    """Rows a rank sends to each rank: its permuted rows of that rank's slot range, from
+    the offsets [S + 1] of its own permutation (host values)."""
+    res = []
+    for d in range(world):
+        lo, n = ep_slot_range(S, world, d)
+        res.append(int(offsets[lo + n]) - int(offsets[lo]))
+    return res
+
+
+def a2a_recv_splits(recv_counts):
+    """Rows a rank receives from each source rank: the row sums of recv_counts
+    [N, S_local] (host values)."""
+    return [int(sum(int(v) for v in row)) for row in recv_counts.tolist()]
+
+
+def _words(t: torch.Tensor) -> torch.Tensor:
+    """Rows of 2-byte elements travel as 32-bit words (element pairs; the rows' widths are
+    even): a bit copy that NCCL and gloo both move."""
+    return t.view(torch.int32) if t.element_size() == 2 else t
+
+
+class DistExchange:
+    """The all-to-all exchanges of EPAllToAllLayer over a torch.distributed process group
+    (NCCL between GPUs, gloo between CPU processes)."""
+
+    def __init__(self, group=None):
+        self.group = group
+
+    def all_to_all(self, out: torch.Tensor, inp: torch.Tensor, out_splits, in_splits) -> None:
+        """out = the rows every rank sent to this one, in rank order; inp = the rows this
+        rank sends, in_splits[d] of them (consecutive, in rank order) to rank d."""
+        import torch.distributed as dist
+        dist.all_to_all_single(_words(out), _words(inp), list(out_splits), list(in_splits), group=self.group)
+
+
+class EPAllToAllLayer:
+    """One rank of the all-to-all expert-parallel layer (TensorRT-LLM PR #10985, "MoE
+    all-to-all paradigm", sequence diagram, all-to-all path: the tokens are dispatched to
+    the ranks responsible for their experts, each rank computes the MoE on its local
+    experts, and the results are gathered back to the tokens' ranks).
+
+    Each rank holds its own batch of tokens (attention data parallelism), the whole router,
+    the whole shared experts (with attention data parallelism nothing is split by tensor
+    parallelism) and the experts of its contiguous slot range [r S / N, (r + 1) S / N).
+    One forward, all on the current stream:
+      1. dispatch: route the rank's tokens and group their pairs by slot over all S slots
+         (moe_route, moe_permute); the rows bound for one rank are one contiguous run;
+      2. the per-slot counts are exchanged (every rank receives, from every source, the
+         counts of its own slots), copied to the host with the row offsets (the one host
+         synchronisation: the row exchange needs its split sizes), then the rows;
+      3. experts: the received rows are put in slot order (moe_a2a_regroup), FC1+SwiGLU
+         and FC2 of the rank's slots run over them in the same launches as the shared
+         experts over the rank's own tokens (moe_grouped_fc1 / fc2), and the outputs go
+         back to arrival order;
+      4. combine: the reverse exchange returns every output row to its token's rank, into
+         the place its input row left from, and moe_finalize forms the weighted sum of each
+         token's k rows in fixed j order plus the shared output.
+    Every kept pair's output row is the one the one-GPU layer computes for it (the GEMMs
+    treat each row alone), so each rank's output equals the one-GPU layer's on its tokens.
+
+    recv_cap: rows a rank can receive (default world * max_T * k, every pair of every rank);
+    a forward that would receive more raises before the row exchange.  bf16 weights only."""
+
+    def __init__(self, Wg, W1, W2, k, renorm, max_T, world: int, rank: int, logit_bias=None, rep_offset=None,
+                 rep_slots=None, W1s=None, W2s=None, shared_gate_w=None, n_group: int = 1, topk_group: int = 1,
+                 on_input: bool = False, recv_cap: Optional[int] = None, exchange=None):
+        from . import moe_workspace_init, moe_workspace_size
+        self.world, self.rank = int(world), int(rank)
+        self.exchange = exchange if exchange is not None else DistExchange()
+        self.Wg, self.bias = Wg, logit_bias
+        self.E, self.H = Wg.shape
+        self.S = int(W1.shape[0])
+        self.I = int(W2.shape[2])
+        self.k, self.renorm = int(k), bool(renorm)
+        self.n_group, self.topk_group, self.on_input = int(n_group), int(topk_group), bool(on_input)
+        self.rep_offset, self.rep_slots = rep_offset, rep_slots
+        self.start, self.count = ep_slot_range(self.S, self.world, self.rank)
+        self.W1 = W1[self.start:self.start + self.count].contiguous()
+        self.W2 = W2[self.start:self.start + self.count].contiguous()
+        self.W1s, self.W2s, self.gate = W1s, W2s, shared_gate_w
+        self.I_sh = 0 if W2s is None else int(W2s.shape[1])
+        self.max_T = int(max_T)
+        self.recv_cap = int(recv_cap if recv_cap is not None else self.world * self.max_T * self.k)
+        dev = Wg.device
+        T, k, H, S, S_l = self.max_T, self.k, self.H, self.S, self.count
+        i32 = dict(dtype=torch.int32, device=dev)
+        bf = dict(dtype=torch.bfloat16, device=dev)
+        self.topk_ids = torch.empty((T, k), **i32)
+        self.topk_w = torch.empty((T, k), dtype=torch.float32, device=dev)
+        self.slot_ids = torch.empty((T, k), **i32)
+        self.counts = torch.empty((S,), **i32)
+        self.offsets = torch.empty((S + 1,), **i32)
+        self.perm_src = torch.empty((T * k,), **i32)
+        self.pair_row = torch.empty((T, k), **i32)
+        self.send = torch.empty((T * k, H), **bf)     # rows out; then the returned output rows
+        self.recv_counts = torch.empty((self.world, S_l), **i32)
+        self.local_offsets = torch.empty((S_l + 1,), **i32)
+        self.recv = torch.empty((self.recv_cap, H), **bf)   # arrival order: rows in, then outputs out
+        self.x_loc = torch.empty((self.recv_cap, H), **bf)  # slot order
+        self.h = torch.empty((self.recv_cap, self.I), **bf)
+        self.y_loc = torch.empty((self.recv_cap, H), **bf)
+        self.h_sh = torch.empty((T, self.I_sh), **bf) if self.I_sh else None
+        self.y_sh = torch.empty((T, H), **bf) if self.I_sh else None
+        self.out = torch.empty((T, H), **bf)
+        pin = dev.type == "cuda"
+        self.offsets_host = torch.empty((S + 1,), dtype=torch.int32, pin_memory=pin)
+        self.recv_counts_host = torch.empty((self.world, S_l), dtype=torch.int32, pin_memory=pin)
+        nbytes = moe_workspace_size(T, H, self.I, self.E, S, k, self.I_sh)
+        self.ws = torch.empty((nbytes,), dtype=torch.uint8, device=dev)
+        moe_workspace_init(self.ws)
+        self.T = 0
+        self.send_splits = self.recv_splits = None
+
+    # ---- the four steps (forward runs them in order; a2a_forward_local interleaves the
+    # ---- steps of several ranks held by one process)
+
+    def dispatch(self, x: torch.Tensor) -> None:
+        """Route x [T, H] and group its pairs by slot into self.send (rows) and self.counts."""
+        from . import moe_permute, moe_route, moe_route_grouped
+        T = x.shape[0]
+        assert T <= self.max_T and x.shape[1] == self.H and x.dtype == torch.bfloat16
+        self.T, self.x = T, x
+        if T == 0:  # nothing to route: the rank still takes part in every exchange
+            self.counts.zero_()
+            self.offsets.zero_()
+            return
+        ids, w = self.topk_ids[:T], self.topk_w[:T]
+        if self.n_group > 1:
+            moe_route_grouped(x, self.Wg, self.bias, self.k, self.renorm, self.n_group, self.topk_group, ids, w,
+                              self.ws)
+        else:
+            moe_route(x, self.Wg, self.bias, self.k, self.renorm, ids, w, self.ws)
+        moe_permute(ids, w, self.E, self.rep_offset, self.rep_slots, self.S, 0, -1, MOE_NONLOCAL_SKIP, x,
+                    self.slot_ids[:T], self.counts, self.offsets, self.perm_src[:T * self.k], self.pair_row[:T],
+                    self.send[:T * self.k], self.ws, on_input=self.on_input)
+
+    def plan(self) -> None:
+        """After the count exchange: the split sizes of the row exchanges, on the host."""
+        self.offsets_host.copy_(self.offsets, non_blocking=True)
+        self.recv_counts_host.copy_(self.recv_counts, non_blocking=True)
+        if self.offsets.is_cuda:
+            torch.cuda.current_stream().synchronize()
+        self.send_splits = a2a_send_splits(self.offsets_host, self.S, self.world)
+        self.recv_splits = a2a_recv_splits(self.recv_counts_host)
+        self.rows_out, self.rows_in = sum(self.send_splits), sum(self.recv_splits)
+        if self.rows_in > self.recv_cap:
+            raise RuntimeError(f"rank {self.rank} receives {self.rows_in} rows, more than recv_cap={self.recv_cap}")
+
+    def experts(self) -> None:
+        """The rank's slots over the received rows, and the shared experts over its own tokens."""
+        from . import MOE_A2A_TO_EXCHANGE, MOE_A2A_TO_GEMM, moe_a2a_regroup, moe_grouped_fc1, moe_grouped_fc2
+        T = self.T
+        moe_a2a_regroup(self.recv_counts, self.recv, self.x_loc, MOE_A2A_TO_GEMM, self.local_offsets, self.ws)
+        sh = self.I_sh > 0 and T > 0
+        moe_grouped_fc1(self.x_loc, self.local_offsets, self.W1, self.x if sh else None, self.W1s if sh else None,
+                        self.h, self.h_sh[:T] if sh else None, self.ws)
+        moe_grouped_fc2(self.h, self.local_offsets, self.W2, self.h_sh[:T] if sh else None,
+                        self.W2s if sh else None, self.y_loc, self.y_sh[:T] if sh else None, self.ws)
+        moe_a2a_regroup(self.recv_counts, self.y_loc, self.recv, MOE_A2A_TO_EXCHANGE, None, self.ws)
+
+    def combine(self) -> torch.Tensor:
+        """After the reverse exchange: each token's weighted sum (plus the shared output)."""
+        from . import moe_finalize
+        T = self.T
+        if T == 0:
+            return self.out[:0]
+        sh = self.I_sh > 0
+        moe_finalize(self.send, self.pair_row[:T], None if self.on_input else self.topk_w[:T],
+                     self.y_sh[:T] if sh else None, self.x if (sh and self.gate is not None) else None,
+                     self.gate if sh else None, self.out[:T], self.ws)
+        return self.out[:T]
+
+    def forward(self, x: torch.Tensor) -> torch.Tensor:
+        """out [T, H] bf16 for this rank's tokens x [T, H]; every rank calls it (T may differ
+        between ranks, and may be 0)."""
+        ex = self.exchange
+        self.dispatch(x)
+        ex.all_to_all(self.recv_counts.view(-1), self.counts, [self.count] * self.world,
+                      a2a_count_splits(self.S, self.world))
+        self.plan()
+        ex.all_to_all(self.recv[:self.rows_in], self.send[:self.rows_out], self.recv_splits, self.send_splits)
+        self.experts()
+        ex.all_to_all(self.send[:self.rows_out], self.recv[:self.rows_in], self.send_splits, self.recv_splits)
+        return self.combine()
+
+
+def a2a_forward_local(layers, xs):
+    """All ranks of an all-to-all layer held by one process on one device (a stand-in for N
+    GPUs): the ranks' steps run one after another, and each exchange is a set of device
+    copies between the ranks' buffers in the order an all-to-all delivers them.  Returns
+    each rank's output."""
+    N = len(layers)
+    assert all(L.world == N and L.rank == r for r, L in enumerate(layers)) and len(xs) == N
+    for L, x in zip(layers, xs):
+        L.dispatch(x)
+    for d, Ld in enumerate(layers):
+        for s, Ls in enumerate(layers):
+            Ld.recv_counts[s].copy_(Ls.counts[Ld.start:Ld.start + Ld.count])
+    for L in layers:
+        L.plan()
+
+    def blocks(splits):
+        at = [0]
+        for v in splits:
+            at.append(at[-1] + v)
+        return at
+
+    send_at = [blocks(L.send_splits) for L in layers]
+    recv_at = [blocks(L.recv_splits) for L in layers]
+    for d, Ld in enumerate(layers):
+        for s, Ls in enumerate(layers):
+            n = Ls.send_splits[d]
+            assert n == Ld.recv_splits[s]
+            if n:
+                Ld.recv[recv_at[d][s]:recv_at[d][s] + n].copy_(Ls.send[send_at[s][d]:send_at[s][d] + n])
+    for L in layers:
+        L.experts()
+    for d, Ld in enumerate(layers):
+        for s, Ls in enumerate(layers):
+            n = Ls.send_splits[d]
+            if n:
+                Ls.send[send_at[s][d]:send_at[s][d] + n].copy_(Ld.recv[recv_at[d][s]:recv_at[d][s] + n])
+    return [L.combine() for L in layers]

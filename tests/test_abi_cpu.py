@@ -181,6 +181,32 @@ def test_permute_on_input_shares_the_host_validation():
              FAKE, 1 << 30, None) == moe.MOE_ERR_INVALID_ARG
 
 
+def test_a2a_regroup_rejects_bad_arguments_on_host():
+    f = moe._lib.moe_a2a_regroup
+    other = ctypes.c_void_p(0x2000)
+    odd = ctypes.c_void_p(0x2002)
+    before = moe.moe_get_launch_count()
+
+    def call(N=4, S_l=8, src=FAKE, dst=other, rows=64, H=256, direction=moe.MOE_A2A_TO_GEMM, counts=FAKE,
+             ws=FAKE, ws_bytes=1 << 20):
+        return f(counts, N, S_l, src, dst, rows, H, direction, None, ws, ws_bytes, None)
+
+    assert call(N=0) == moe.MOE_ERR_INVALID_ARG
+    assert call(S_l=0) == moe.MOE_ERR_INVALID_ARG
+    assert call(rows=-1) == moe.MOE_ERR_INVALID_ARG
+    assert call(direction=2) == moe.MOE_ERR_INVALID_ARG
+    assert call(counts=None) == moe.MOE_ERR_INVALID_ARG
+    assert call(N=64, S_l=65) == moe.MOE_ERR_UNSUPPORTED       # more blocks than the tables hold
+    assert call(H=100) == moe.MOE_ERR_UNSUPPORTED              # H not a multiple of 64
+    assert call(rows=1 << 31) == moe.MOE_ERR_UNSUPPORTED       # rows beyond int32
+    assert call(dst=FAKE) == moe.MOE_ERR_INVALID_ARG           # in place
+    assert call(src=None) == moe.MOE_ERR_INVALID_ARG
+    assert call(dst=odd) == moe.MOE_ERR_INVALID_ARG            # not 16-byte aligned
+    assert call(ws=None) == moe.MOE_ERR_WORKSPACE
+    assert call(ws_bytes=64) == moe.MOE_ERR_WORKSPACE
+    assert moe.moe_get_launch_count() == before
+
+
 def test_launch_event_hook_host_side():
     lib = moe._lib
     assert lib.moe_launch_events_arm(None, -1) == moe.MOE_ERR_INVALID_ARG

@@ -1,10 +1,19 @@
-"""Expert parallelism (serving_router_gate_gb300.expert_parallel) on the CPU:
-the slot ranges and shared-expert shards partition the layer, and with gloo
-ranks (world sizes 2 and 4) the one SUM reduction of the ranks' partial
-outputs -- each computed by the fp64 oracle on that rank's slot range (SKIP)
-and shared shard -- equals the oracle's full layer.  The GPU side of each rank
-runs the same library calls as a one-GPU layer with a local range; its partials
-are checked on a GPU in tests/test_gpu_expert_parallel.py."""
+"""Expert parallelism (serving_router_gate_gb300.expert_parallel) on the CPU.
+
+Reduction mode: the slot ranges and shared-expert shards partition the layer,
+and with gloo ranks (world sizes 2 and 4) the one SUM reduction of the ranks'
+partial outputs -- each computed by the fp64 oracle on that rank's slot range
+(SKIP) and shared shard -- equals the oracle's full layer.
+
+All-to-all mode: with gloo ranks that each hold their own tokens, the
+package's split sizes and exchanges (DistExchange over gloo) carry every
+pair's row to the rank owning its slot and the expert outputs back; with the
+oracle standing in for the kernels on each rank (routing and permutation,
+the receive-side order, the expert MLPs, the combine), every rank's output
+equals the oracle's layer on its own tokens.
+
+The GPU side of both modes runs the library's calls; it is checked on a GPU
+in tests/test_gpu_expert_parallel.py."""
 import os
 import socket
 
@@ -16,8 +25,9 @@ import torch.multiprocessing as mp
 
 import moe_inputs as mi
 import oracle
-from serving_router_gate_gb300.expert_parallel import (ep_reduce_output, ep_shared_range, ep_shared_shard,
-                                                       ep_slot_range)
+from serving_router_gate_gb300.expert_parallel import (DistExchange, a2a_count_splits, a2a_recv_splits,
+                                                       a2a_send_splits, ep_reduce_output, ep_shared_range,
+                                                       ep_shared_shard, ep_slot_range)
 
 
 @pytest.mark.parametrize("S,world", [(60, 2), (64, 4), (288, 8), (13, 4), (8, 8), (5, 3)])
@@ -121,3 +131,100 @@ def test_partials_reduced_over_gloo_ranks_equal_the_full_layer(world):
         # every rank holds the same sum; the fp32 reduction rounds each partial once
         np.testing.assert_allclose(res[r], full, rtol=0, atol=1e-6 * np.abs(full).max())
         assert np.array_equal(res[r], res[0])
+
+
+# --------------------------------------------------------------------------- all-to-all mode
+
+def test_a2a_split_sizes():
+    S, world = 13, 4
+    assert a2a_count_splits(S, world) == [ep_slot_range(S, world, d)[1] for d in range(world)]
+    assert sum(a2a_count_splits(S, world)) == S
+    offsets = np.array([0, 2, 2, 5, 6, 6, 6, 9, 10, 10, 12, 15, 15, 20])  # S + 1 = 14 entries
+    sp = a2a_send_splits(offsets, S, world)
+    # ranges (0, 3), (3, 3), (6, 3), (9, 4): rows offsets[hi] - offsets[lo]
+    assert sp == [5, 1, 4, 10] and sum(sp) == offsets[-1]
+    rc = torch.tensor([[1, 0, 2], [0, 0, 0], [4, 1, 1]], dtype=torch.int32)
+    assert a2a_recv_splits(rc) == [3, 0, 6]
+
+
+A2A_CFG = mi.MoEConfig("a2a_cpu", T=24, H=128, I=128, E=8, k=3, renorm=True, n_shared=1, I_shared=128,
+                       shared_gate=True)
+A2A_TOKENS = {2: [24, 9], 4: [24, 0, 17, 5]}  # each rank's own batch (one rank without tokens)
+
+
+def _a2a_rank_output(inp, x, world, rank, ex):
+    """One rank of the all-to-all layer with the oracle in place of the kernels."""
+    cfg = inp["cfg"]
+    S, k, H = cfg.E, cfg.k, cfg.H
+    lo, S_l = ep_slot_range(S, world, rank)
+    T = x.shape[0]
+    # dispatch: route, slot map, group the pairs by slot (all S slots)
+    if T:
+        ids, w, _ = oracle.route(x, inp["Wg"], None, k, cfg.renorm)
+        counts, offsets, perm_src, pair_row = oracle.permute(oracle.slot_map(ids), S)
+        send = x[torch.from_numpy(perm_src.astype(np.int64) // k)]
+    else:
+        w = np.zeros((0, k))
+        counts, offsets, pair_row = np.zeros(S, np.int32), np.zeros(S + 1, np.int32), np.zeros(0, np.int32)
+        send = torch.empty((0, H), dtype=torch.bfloat16)
+    recv_counts = torch.empty((world, S_l), dtype=torch.int32)
+    ex.all_to_all(recv_counts.view(-1), torch.from_numpy(counts), [S_l] * world, a2a_count_splits(S, world))
+    send_splits = a2a_send_splits(offsets, S, world)
+    recv_splits = a2a_recv_splits(recv_counts)
+    recv = torch.empty((sum(recv_splits), H), dtype=torch.bfloat16)
+    ex.all_to_all(recv, send.contiguous(), recv_splits, send_splits)
+    # experts: the received rows in slot order, each through its slot's expert
+    off_l, gemm_row, exch_row = oracle.a2a_regroup(recv_counts.numpy())
+    y_loc = np.zeros((recv.shape[0], H))
+    for c in range(S_l):
+        for r in range(off_l[c], off_l[c + 1]):
+            y_loc[r] = oracle.expert_mlp(recv[int(exch_row[r])], inp["W1"][lo + c], inp["W2"][lo + c])[0]
+    y_ret = torch.empty((send.shape[0], H), dtype=torch.float64)
+    ex.all_to_all(y_ret, torch.from_numpy(y_loc[gemm_row]).contiguous(), send_splits, recv_splits)
+    # combine: fixed j order, then the gated shared expert on the rank's own tokens
+    out = np.zeros((T, H))
+    W1c, W2c = mi.shared_concat(inp["W1s"], inp["W2s"])
+    ws = inp["w_s"].to(torch.float64).numpy()
+    y_ret = y_ret.numpy()
+    for t in range(T):
+        for j in range(k):
+            out[t] += w[t, j] * y_ret[pair_row[t * k + j]]
+        g = 1.0 / (1.0 + np.exp(-float(x[t].to(torch.float64).numpy() @ ws)))
+        out[t] += g * oracle.expert_mlp(x[t], W1c, W2c)[0]
+    return out
+
+
+def _a2a_worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        inp = mi.make_inputs(A2A_CFG)
+        x = mi.rank_tokens(A2A_CFG, rank, A2A_TOKENS[world][rank])
+        q.put((rank, _a2a_rank_output(inp, x, world, rank, DistExchange())))
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world", [2, 4])
+def test_a2a_exchange_over_gloo_ranks_gives_each_rank_its_layer(world):
+    oracle.build()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_a2a_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    res = dict(q.get(timeout=300) for _ in procs)
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    inp = mi.make_inputs(A2A_CFG)
+    c1, c2 = mi.shared_concat(inp["W1s"], inp["W2s"])
+    for r in range(world):
+        x = mi.rank_tokens(A2A_CFG, r, A2A_TOKENS[world][r])
+        assert res[r].shape == (x.shape[0], A2A_CFG.H)
+        if x.shape[0] == 0:
+            continue
+        ref = oracle.moe_layer(x, inp["Wg"], None, A2A_CFG.k, A2A_CFG.renorm, inp["W1"], inp["W2"], W1s=c1[None],
+                               W2s=c2[None], shared_gate_w=inp["w_s"])["out"]
+        np.testing.assert_allclose(res[r], ref, rtol=0, atol=1e-12 * np.abs(ref).max())

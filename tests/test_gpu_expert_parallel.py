@@ -1,19 +1,32 @@
-"""The GPU side of expert parallelism on one GPU: each rank's partial output
-(its slot range under SKIP and its shard of the shared experts, through the
-same library calls a rank runs) is computed in turn, and the partials summed
-on the host equal the full layer -- against the fp64 oracle and against the
-one-GPU layer, within the output tolerance.  Ranks run one after another on
-one GPU: nothing waits on another rank."""
+"""The GPU side of expert parallelism on one GPU.
+
+Reduction mode: each rank's partial output (its slot range under SKIP and its
+shard of the shared experts, through the same library calls a rank runs) is
+computed in turn, and the partials summed on the host equal the full layer --
+against the fp64 oracle and against the one-GPU layer, within the output
+tolerance.
+
+All-to-all mode: moe_a2a_regroup moves rows into the oracle's receive-side
+order and back, bit for bit; and N ranks held by one process
+(a2a_forward_local: the ranks' steps one after another, the exchanges as
+device copies) give every rank the one-GPU layer's output on its own tokens,
+bit for bit, and the oracle's within the output tolerance -- on mid-size
+cases with ragged and empty batches, replica slots, group-limited top-k and
+routing on the input, and with the Qwen2-like and redundant-slot workloads'
+batches split over 4 and 8 ranks.
+
+Ranks run one after another on one GPU: nothing waits on another rank."""
 import numpy as np
 import pytest
 import torch
 
 import moe_inputs as mi
+import oracle
 import serving_router_gate_gb300 as moe
-from serving_router_gate_gb300.expert_parallel import EPMoELayer
+from serving_router_gate_gb300.expert_parallel import EPAllToAllLayer, EPMoELayer, a2a_forward_local
 from serving_router_gate_gb300.layer import layer_from_inputs
 
-from parity_util import check_out, oracle_layer, oracle_threads, to_cpu
+from parity_util import check_out, oracle_layer, oracle_threads, sample_tokens, to_cpu
 
 pytestmark = pytest.mark.gpu
 
@@ -60,3 +73,139 @@ def test_ep_with_replica_slots_and_uneven_ranges():
     inp = mi.make_inputs(cfg)
     out = _ep_partials(inp, 4)
     check_out(out, oracle_layer(to_cpu(inp))["out"], "sum of partials with replica slots")
+
+
+# --------------------------------------------------------------------------- all-to-all mode
+
+def _bits(t):
+    return t.view(torch.int16).cpu()
+
+
+@pytest.mark.parametrize("N,S_l,H,seed", [(2, 5, 64, 0), (4, 3, 192, 1), (8, 36, 2048, 2), (1, 7, 256, 3),
+                                          (64, 64, 64, 4), (3, 1, 7168, 5)])
+def test_a2a_regroup_matches_the_oracle_order(N, S_l, H, seed):
+    g = torch.Generator().manual_seed(seed)
+    counts = torch.randint(0, 5, (N, S_l), generator=g, dtype=torch.int32)
+    counts[0, 0] = 0       # an empty block
+    if N > 2:
+        counts[N - 2] = 0  # a source that sent nothing
+    R = int(counts.sum())
+    cap = R + 3            # rows past the total are neither read nor written
+    src = torch.randn(cap, H, generator=g).to(torch.bfloat16).cuda()
+    nan = torch.full((cap, H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ws = torch.zeros(moe.MOE_WS_HEADER_BYTES, dtype=torch.uint8, device="cuda")
+    rc = counts.cuda()
+    off = torch.full((S_l + 1,), -7, dtype=torch.int32, device="cuda")
+    dst = nan.clone()
+    before = moe.moe_get_launch_count()
+    moe.moe_a2a_regroup(rc, src, dst, moe.MOE_A2A_TO_GEMM, off, ws)
+    assert moe.moe_get_launch_count() == before + 1
+    ref_off, gemm_row, exch_row = oracle.a2a_regroup(counts.numpy())
+    assert off.cpu().tolist() == ref_off.tolist()
+    exch = torch.from_numpy(exch_row.astype(np.int64))
+    assert torch.equal(_bits(dst[:R]), _bits(src[:R])[exch])
+    assert torch.equal(_bits(dst[R:]), _bits(nan[R:]))
+    back = nan.clone()
+    moe.moe_a2a_regroup(rc, dst, back, moe.MOE_A2A_TO_EXCHANGE, None, ws)
+    assert torch.equal(_bits(back[:R]), _bits(src[:R]))
+    assert torch.equal(_bits(back[R:]), _bits(nan[R:]))
+    assert moe.moe_get_device_status(ws) == 0
+
+
+@pytest.mark.parametrize("bad", ["total", "negative"])
+def test_a2a_regroup_flags_bad_counts_and_moves_nothing(bad):
+    counts = torch.tensor([[3, 2], [1, 4]], dtype=torch.int32)
+    cap = 10
+    if bad == "total":
+        cap = 9            # 10 rows announced, room for 9
+    else:
+        counts[1, 0] = -1
+    src = torch.randn(cap, 64).to(torch.bfloat16).cuda()
+    dst = torch.zeros(cap, 64, dtype=torch.bfloat16, device="cuda")
+    off = torch.full((3,), -7, dtype=torch.int32, device="cuda")
+    ws = torch.zeros(moe.MOE_WS_HEADER_BYTES, dtype=torch.uint8, device="cuda")
+    moe.moe_a2a_regroup(counts.cuda(), src, dst, moe.MOE_A2A_TO_GEMM, off, ws)
+    assert moe.moe_get_device_status(ws) == moe.MOE_ERR_DEVICE_BOUNDS
+    assert int(dst.view(torch.int16).abs().sum()) == 0
+    assert off.cpu().tolist() == [-7, -7, -7]
+
+
+def _a2a_layers(inp, world, max_T, recv_cap=None):
+    cfg = inp["cfg"]
+    d = lambda t: None if t is None else t.cuda().contiguous()  # noqa: E731
+    W1s = W2s = None
+    if inp["W1s"] is not None:
+        W1s, W2s = mi.shared_concat(inp["W1s"], inp["W2s"])
+    Wg, W1, W2, bias, ro, rs, W1s, W2s, ws_ = (d(inp["Wg"]), d(inp["W1"]), d(inp["W2"]), d(inp["bias"]),
+                                               d(inp["rep_offset"]), d(inp["rep_slots"]), d(W1s), d(W2s),
+                                               d(inp["w_s"]))
+    return [EPAllToAllLayer(Wg, W1, W2, cfg.k, cfg.renorm, max_T, world, r, logit_bias=bias, rep_offset=ro,
+                            rep_slots=rs, W1s=W1s, W2s=W2s, shared_gate_w=ws_, n_group=cfg.n_group,
+                            topk_group=cfg.topk_group, on_input=cfg.on_input, recv_cap=recv_cap)
+            for r in range(world)]
+
+
+def _check_a2a(inp, xs, recv_cap=None, n_oracle=None):
+    """Every rank's output: bitwise the one-GPU layer's on its tokens, and the oracle's
+    within the output tolerance (on n_oracle sampled tokens, or all)."""
+    cfg = inp["cfg"]
+    world = len(xs)
+    max_T = max(1, max(x.shape[0] for x in xs))
+    layers = _a2a_layers(inp, world, max_T, recv_cap)
+    outs = a2a_forward_local(layers, [x.cuda() for x in xs])
+    torch.cuda.synchronize()
+    for L in layers:
+        assert moe.moe_get_device_status(L.ws) == 0
+    one = layer_from_inputs(inp, "cuda", max_T=max_T)
+    inp_cpu = to_cpu(inp)
+    for r, (x, out) in enumerate(zip(xs, outs)):
+        T = x.shape[0]
+        assert out.shape == (T, cfg.H)
+        if T == 0:
+            continue
+        ref = one.forward(x.cuda())
+        assert torch.equal(_bits(out), _bits(ref)), f"rank {r}: differs from the one-GPU layer"
+        tok = None if n_oracle is None else sample_tokens(T, n_oracle, seed=r)
+        part = oracle_layer(dict(inp_cpu, x=x.cpu()), tokens=tok)
+        check_out(out if tok is None else out[torch.from_numpy(tok).cuda()], part["out"], f"rank {r}")
+    # every pair went to exactly one rank: the rows received sum to the pairs sent
+    assert sum(L.rows_in for L in layers) == sum(L.rows_out for L in layers) == cfg.k * sum(x.shape[0] for x in xs)
+    return layers
+
+
+@pytest.mark.parametrize("tokens", [[129, 64], [300, 0, 77, 513]])
+def test_a2a_layer_gives_each_rank_its_layer(tokens):
+    cfg = mi.MoEConfig("a2a_gpu", T=16, H=256, I=256, E=16, k=4, renorm=True, n_shared=2, I_shared=128,
+                       shared_gate=True)
+    inp = mi.make_inputs(cfg)
+    xs = [mi.rank_tokens(cfg, r, T) for r, T in enumerate(tokens)]
+    _check_a2a(inp, xs)
+
+
+@pytest.mark.parametrize("variant", ["replicas", "grouped", "on_input"])
+def test_a2a_layer_routing_variants(variant):
+    if variant == "replicas":  # 13 slots over 4 ranks (3, 3, 3, 4), Zipf bias, no shared experts
+        cfg = mi.MoEConfig("a2a_rep", T=8, H=256, I=128, E=10, S=13, n_hot=3, zipf_s=1.1, k=3, renorm=True)
+    elif variant == "grouped":
+        cfg = mi.MoEConfig("a2a_grp", T=8, H=256, I=128, E=16, k=4, renorm=True, n_group=4, topk_group=2,
+                           n_shared=1, I_shared=128)
+    else:
+        cfg = mi.MoEConfig("a2a_oni", T=8, H=256, I=128, E=12, k=2, renorm=False, on_input=True)
+    inp = mi.make_inputs(cfg)
+    xs = [mi.rank_tokens(cfg, r, T) for r, T in enumerate([200, 33, 0, 150])]
+    _check_a2a(inp, xs)
+
+
+def test_a2a_qwen2_moe_like_batch_over_4_ranks():
+    # the workload's 4096 tokens as four ranks' batches of 1024
+    inp = mi.make_inputs(mi.CONFIGS["qwen2_moe_like_prefill"], device="cpu", weights_device="cuda")
+    xs = list(inp["x"].split(1024))
+    _check_a2a(inp, xs, n_oracle=12)
+
+
+def test_a2a_redundant_slots_batch_over_8_ranks():
+    # the workload's 16384 tokens as eight ranks' batches of 2048; 288 slots, 36 per rank
+    inp = mi.make_inputs(mi.CONFIGS["redundant_slots_prefill"], device="cpu", weights_device="cuda")
+    xs = list(inp["x"].split(2048))
+    layers = _check_a2a(inp, xs, recv_cap=3 * 2048 * 8, n_oracle=6)
+    assert max(L.rows_in for L in layers) <= 3 * 2048 * 8
