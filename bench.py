@@ -50,12 +50,12 @@ DEFAULT_WORKLOAD = "redundant_slots_prefill"
 # the recorded value.
 NCU_TRAFFIC = {
     # FC1 of the first forward, ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum:
-    # 822.31 MB read + 87.85 MB written (algorithmic 914.36 MB)
-    ("qwen2_moe_like_prefill", "158e60acb8eccf05"): 910.16e6,
-    # 115.52 MB read + 2.81 MB written (algorithmic 115.40 MB)
-    ("dsv2_lite_like_decode_t1", "158e60acb8eccf05"): 118.33e6,
-    # 1105.56 MB read + 32.93 MB written (algorithmic 1090.52 MB)
-    ("redundant_slots_cut16", "158e60acb8eccf05"): 1138.49e6,
+    # 822.25 MB read + 87.41 MB written (algorithmic 914.36 MB)
+    ("qwen2_moe_like_prefill", "f3a8bb44c1835ecc"): 909.66e6,
+    # 115.62 MB read + 2.99 MB written (algorithmic 115.40 MB)
+    ("dsv2_lite_like_decode_t1", "f3a8bb44c1835ecc"): 118.61e6,
+    # 1105.62 MB read + 33.02 MB written (algorithmic 1090.52 MB)
+    ("redundant_slots_cut16", "f3a8bb44c1835ecc"): 1138.64e6,
 }
 
 
@@ -65,8 +65,8 @@ NCU_TRAFFIC = {
 # Traffic grows in proportion: every slot's weight tile is streamed once and its A rows
 # stay in L2 across the slot's n-tiles, at either size.
 NCU_TRAFFIC_SCALED = {
-    ("redundant_slots_prefill", "158e60acb8eccf05"): (
-        1138.49e6, 1090.52e6,
+    ("redundant_slots_prefill", "f3a8bb44c1835ecc"): (
+        1138.64e6, 1090.52e6,
         "one capture of FC1 on the 16-slot cut (T=1024, H=7168, I=2048, E=16, k=8: 512 rows per slot)"),
 }
 
@@ -418,7 +418,7 @@ def _ep_layer(inp, cfg, world, rank, dev):
                       n_group=cfg.n_group, topk_group=cfg.topk_group, fp8=cfg.fp8, act8=cfg.act8, fp4=cfg.fp4)
 
 
-def _a2a_layer(inp, cfg, world, rank, dev):
+def _a2a_layer(inp, cfg, world, rank, dev, max_T=None):
     """This rank's all-to-all expert-parallel layer over the workload's weights."""
     from serving_router_gate_gb300.expert_parallel import EPAllToAllLayer
     if cfg.fp8 or cfg.fp4:
@@ -427,7 +427,7 @@ def _a2a_layer(inp, cfg, world, rank, dev):
     if inp["W1s"] is not None:
         W1s, W2s = mi.shared_concat(inp["W1s"], inp["W2s"])
     d = lambda t: None if t is None else t.to(dev).contiguous()  # noqa: E731
-    return EPAllToAllLayer(d(inp["Wg"]), d(inp["W1"]), d(inp["W2"]), cfg.k, cfg.renorm, cfg.T, world, rank,
+    return EPAllToAllLayer(d(inp["Wg"]), d(inp["W1"]), d(inp["W2"]), cfg.k, cfg.renorm, max_T or cfg.T, world, rank,
                            logit_bias=d(inp["bias"]), rep_offset=d(inp["rep_offset"]),
                            rep_slots=d(inp["rep_slots"]), W1s=d(W1s), W2s=d(W2s), shared_gate_w=d(inp["w_s"]),
                            n_group=cfg.n_group, topk_group=cfg.topk_group, on_input=cfg.on_input)
@@ -711,6 +711,103 @@ def bench_ours(args):
         dist.destroy_process_group()
 
 
+def bench_a2a_local(args):
+    """All-to-all expert parallelism over R ranks held by this process on one GPU
+    (a2a_forward_local: the ranks' steps one after another, the exchanges as device
+    copies), the workload's batch split into R ranks' batches.  Times the whole step and,
+    in a second pass, every library kernel between its own events (launch-event hook,
+    eager, a mark after each phase so the exchanges' copies fall in marked intervals);
+    reports the row reorder kernel against the HBM peak."""
+    import serving_router_gate_gb300 as moe
+    from serving_router_gate_gb300.expert_parallel import a2a_forward_local
+    R = args.a2a_ranks
+    cfg = mi.CONFIGS[args.workload]
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    inp = mi.make_inputs(cfg, device=dev)
+    per = -(-cfg.T // R)
+    xs = list(inp["x"].split(per))
+    if len(xs) != R:
+        raise SystemExit(f"bench.py: {cfg.T} tokens do not make {R} ranks' batches")
+    layers = [_a2a_layer(inp, cfg, R, r, dev, max_T=per) for r in range(R)]
+    stream = torch.cuda.current_stream()
+    flush = L2Flush(dev)
+    K, W = args.steps, args.warmup
+
+    def step():
+        return a2a_forward_local(layers, xs)
+
+    for _ in range(W):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(0)
+    clocks.start()
+    t = time_steps([step], K, flush, stream)[0]
+    clk = clocks.stop()
+    ms = statistics.mean(t)
+    for L in layers:
+        if moe.moe_get_device_status(L.ws):
+            raise RuntimeError("device status set after the timed steps")
+
+    # per-kernel pass
+    c0 = moe.moe_get_launch_count()
+    step()
+    n_launch = moe.moe_get_launch_count() - c0
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_launch + 8)]
+    for e in evs:
+        e.record(stream)
+    torch.cuda.synchronize()
+    per_pos, labels = None, None
+    for _ in range(K):
+        flush()
+        moe.moe_launch_events_arm(evs)
+        try:
+            step_out = a2a_forward_local(layers, xs, after_phase=lambda name: moe.moe_launch_events_mark())
+            labels = moe.moe_launch_events_used()
+        finally:
+            moe.moe_launch_events_arm(None)
+        torch.cuda.synchronize()
+        del step_out
+        if per_pos is None:
+            per_pos = [[] for _ in range(len(labels) - 1)]
+        for i in range(len(labels) - 1):
+            per_pos[i].append(evs[i].elapsed_time(evs[i + 1]))
+    med = [statistics.median(v) for v in per_pos]
+    kernels = {}
+    for lab, m in zip(labels, med):
+        if lab != "mark":
+            kernels[lab] = kernels.get(lab, 0.0) + m
+    # row reorders: one launch per rank, moving its received rows into slot order
+    rows_in = [L.rows_in for L in layers]
+    H = cfg.H
+    reg = [(i, m) for i, (lab, m) in enumerate(zip(labels, med)) if lab.startswith("a2a_regroup")]
+    reg_bytes = sum(2 * r * H * 2 for r in rows_in)
+    reg_ms = sum(m for _, m in reg)
+    peaks = _peaks()
+    gbs = reg_bytes / (reg_ms * 1e-3) / 1e9
+    res = {
+        "metric": METRIC, "value": cfg.T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": K,
+        "warmup": W, "ms_per_step": ms, "higher_is_better": True, "scaling": "strong", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic: seeded N(0,1) activations, N(0,sigma) random-init weights",
+        "config": {"workload": cfg.name, "shape": mi.describe(cfg),
+                   "parallelism": f"all-to-all expert parallel over {R} ranks held by one process on one GPU "
+                                  f"({per} tokens each; the exchanges are device copies; each rank's split "
+                                  f"sizes are read on the host, one synchronisation per rank per step)",
+                   "l2": f"flushed before every timed step ({flush.describe()})"},
+        "rows_received": rows_in,
+        "kernels_ms": kernels,
+        "a2a_regroup": {"bound": "hbm", "launches": len(reg), "algorithmic_bytes": reg_bytes,
+                        "ms": reg_ms, "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
+                        "frac": gbs / peaks["hbm"],
+                        "work": "2 x rows received x H x 2 bytes per launch (each row read and written once), "
+                                "one launch per rank (FC2 stores its rows back in arrival order itself)",
+                        "timing": "launch-event hook: a CUDA event before every library launch and a mark "
+                                  "after each phase, median per launch over the steps, each after an L2 flush"},
+        "clocks": clk,
+    }
+    print(json.dumps(res), flush=True)
+
+
 def bench_reference(args):
     """The fp64 oracle, as it stands, on the host cores: each step a bounded
     sample of the workload (its first n tokens through the whole layer)."""
@@ -771,6 +868,9 @@ def main():
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="launch every step from Python instead of replaying a CUDA graph of one step")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--a2a-ranks", type=int, default=0,
+                    help="one GPU: run the all-to-all expert-parallel layer over this many ranks held by one "
+                         "process (exchanges as device copies) and time its kernels")
     ap.add_argument("--partition", choices=["ep", "a2a", "replicas"], default="ep",
                     help="with more than one rank: expert parallelism over one batch with one reduction "
                          "(default), all-to-all expert parallelism (each rank its own batch, rows dispatched "
@@ -789,6 +889,10 @@ def main():
         sys.exit(f"bench.py: --gpus {args.gpus} but the launcher started {ws} ranks")
     if args.impl == "reference":
         bench_reference(args)
+    elif args.a2a_ranks > 0:
+        if ws is not None and int(ws) > 1:
+            sys.exit("bench.py: --a2a-ranks holds every rank in one process on one GPU")
+        bench_a2a_local(args)
     else:
         bench_ours(args)
 

@@ -417,6 +417,17 @@ MOE_API moe_status_t moe_grouped_fc2(const moe_bf16_t *h, int64_t rows_cap, cons
                              int I_shared_total, moe_bf16_t *y, moe_bf16_t *y_shared,
                              void *ws, size_t ws_bytes, moe_stream_t stream);
 
+/* moe_grouped_fc2 whose routed output row r is stored at y row y_row[r]
+ * (y_row [rows_cap] int32, device; its first offsets[G] entries must be
+ * distinct rows of y, e.g. the row map moe_a2a_regroup writes); the shared
+ * problem's rows are stored as they are.  An entry outside [0, rows_cap) is
+ * undefined behaviour (the bounds-checked build flags it and skips the row). */
+MOE_API moe_status_t moe_grouped_fc2_scatter(const moe_bf16_t *h, int64_t rows_cap, const int32_t *offsets, int G,
+                                     const moe_bf16_t *W2, int H, int I, const moe_bf16_t *h_shared, int64_t T,
+                                     const moe_bf16_t *W2s, int I_shared_total, const int32_t *y_row,
+                                     moe_bf16_t *y, moe_bf16_t *y_shared, void *ws, size_t ws_bytes,
+                                     moe_stream_t stream);
+
 /* moe_grouped_fc1 / moe_grouped_fc2 with E4M3 weights and fp32 row scales
  * (the stages of moe_forward_fp8; layouts as there). */
 MOE_API moe_status_t moe_grouped_fc1_fp8(const moe_bf16_t *a, int64_t rows_cap, const int32_t *offsets, int G,
@@ -482,14 +493,18 @@ MOE_API moe_status_t moe_finalize(const moe_bf16_t *y, int64_t rows_cap, const i
  *                MOE_A2A_TO_EXCHANGE: src in GEMM order, dst in exchange order
  *   offsets      [S_local + 1] int32 out, or NULL: the GEMM-order row offsets of
  *                the local slots (offsets[S_local] = total), for moe_grouped_fc1/fc2
+ *   row_map      [rows_cap] int32 out, or NULL: for each of the first `total` rows
+ *                of dst, the src row it was copied from (after MOE_A2A_TO_GEMM: the
+ *                exchange-order row of each GEMM row, the y_row that lets
+ *                moe_grouped_fc2_scatter store FC2's rows straight in exchange order)
  *   ws           workspace: only its status word is used
  *
  * A negative count, or a total above rows_cap, sets MOE_ERR_DEVICE_BOUNDS in the
- * status word and moves no row (offsets are then not written). */
+ * status word and moves no row (offsets and row_map are then not written). */
 enum { MOE_A2A_TO_GEMM = 0, MOE_A2A_TO_EXCHANGE = 1 };
 MOE_API moe_status_t moe_a2a_regroup(const int32_t *recv_counts, int N, int S_local, const moe_bf16_t *src,
                                      moe_bf16_t *dst, int64_t rows_cap, int H, int direction, int32_t *offsets,
-                                     void *ws, size_t ws_bytes, moe_stream_t stream);
+                                     int32_t *row_map, void *ws, size_t ws_bytes, moe_stream_t stream);
 
 /* ---- diagnostics ---------------------------------------------------------- */
 

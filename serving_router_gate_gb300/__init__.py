@@ -29,6 +29,7 @@ __all__ = [
     "moe_forward_nvfp4", "moe_quantize_nvfp4_rows", "nvfp4_sf_row_bytes", "MOE_WS_HEADER_BYTES",
     "moe_grouped_fc2_fp8", "moe_grouped_fc1_w8a8", "moe_grouped_fc2_w8a8", "moe_launch_events_arm",
     "moe_launch_events_mark", "moe_launch_events_used", "EXPORTED_SYMBOLS", "moe_a2a_regroup",
+    "moe_grouped_fc2_scatter",
     "MOE_A2A_TO_GEMM", "MOE_A2A_TO_EXCHANGE",
 ]
 
@@ -55,6 +56,7 @@ EXPORTED_SYMBOLS = (
     "moe_forward_nvfp4", "moe_quantize_nvfp4_rows",
     "moe_forward_w8a8", "moe_quantize_act_rows", "moe_grouped_fc1_w8a8", "moe_grouped_fc2_w8a8",
     "moe_launch_events_arm", "moe_launch_events_mark", "moe_launch_events_used", "moe_a2a_regroup",
+    "moe_grouped_fc2_scatter",
 )
 
 
@@ -104,7 +106,8 @@ def _load():
         "moe_grouped_fc1": ([P, i64, P, i32, P, i32, i32, P, i64, P, i32, P, P, P, sz, P], i32),
         "moe_grouped_fc2": ([P, i64, P, i32, P, i32, i32, P, i64, P, i32, P, P, P, sz, P], i32),
         "moe_finalize": ([P, i64, P, P, i64, i32, i32, P, P, P, P, P, sz, P], i32),
-        "moe_a2a_regroup": ([P, i32, i32, P, P, i64, i32, i32, P, P, sz, P], i32),
+        "moe_a2a_regroup": ([P, i32, i32, P, P, i64, i32, i32, P, P, P, sz, P], i32),
+        "moe_grouped_fc2_scatter": ([P, i64, P, i32, P, i32, i32, P, i64, P, i32, P, P, P, P, sz, P], i32),
         "moe_debug_wait_timeout": ([P, sz, u64, P], i32),
         "moe_set_wait_timeout_ns": ([u64], None),
         "moe_route_noalloc": ([P, P, P, i64, i32, i32, i32, i32, P, P, P], i32),
@@ -486,17 +489,36 @@ def moe_finalize(y, pair_row, topk_w, y_shared, x, shared_gate_w, out, ws, strea
     _check("moe_finalize", st)
 
 
-def moe_a2a_regroup(recv_counts, src, dst, direction, offsets, ws, stream=None):
+def moe_a2a_regroup(recv_counts, src, dst, direction, offsets, ws, stream=None, row_map=None):
     """Rows of an all-to-all expert-parallel rank from exchange order to GEMM order
     (direction MOE_A2A_TO_GEMM, offsets [S_local+1] written unless None) or back
-    (MOE_A2A_TO_EXCHANGE).  recv_counts [N, S_local] int32; src, dst [rows_cap, H] bf16."""
+    (MOE_A2A_TO_EXCHANGE).  recv_counts [N, S_local] int32; src, dst [rows_cap, H] bf16;
+    row_map [rows_cap] int32 (or None): the src row of each dst row."""
     N, S_l = recv_counts.shape
     rows_cap, H = src.shape
     st = _lib.moe_a2a_regroup(_ptr(recv_counts, "recv_counts", _i32, (N, S_l)), N, S_l, _ptr(src, "src", _bf16),
                               _ptr(dst, "dst", _bf16, (rows_cap, H)), rows_cap, H, int(direction),
                               _ptr(offsets, "offsets", _i32, (S_l + 1,), allow_none=True),
+                              _ptr(row_map, "row_map", _i32, (rows_cap,), allow_none=True),
                               _ptr(ws, "ws", torch.uint8), ws.numel(), _stream(stream))
     _check("moe_a2a_regroup", st)
+
+
+def moe_grouped_fc2_scatter(h, offsets, W2, h_shared, W2s, y_row, y, y_shared, ws, stream=None):
+    """moe_grouped_fc2 with routed output row r stored at y row y_row[r]."""
+    rows_cap, I = h.shape
+    G = offsets.shape[0] - 1
+    H = W2.shape[1]
+    T = 0 if h_shared is None else h_shared.shape[0]
+    I_sh = 0 if W2s is None else W2s.shape[1]
+    st = _lib.moe_grouped_fc2_scatter(_ptr(h, "h", _bf16), rows_cap, _ptr(offsets, "offsets", _i32), G,
+                                      _ptr(W2, "W2", _bf16, (G, H, I)), H, I,
+                                      _ptr(h_shared, "h_shared", _bf16, (T, I_sh), allow_none=True), T,
+                                      _ptr(W2s, "W2s", _bf16, (H, I_sh), allow_none=True), I_sh,
+                                      _ptr(y_row, "y_row", _i32, (rows_cap,)), _ptr(y, "y", _bf16, (rows_cap, H)),
+                                      _ptr(y_shared, "y_shared", _bf16, (T, H), allow_none=True),
+                                      _ptr(ws, "ws", torch.uint8), ws.numel(), _stream(stream))
+    _check("moe_grouped_fc2_scatter", st)
 
 
 def moe_debug_wait_timeout(ws, timeout_ns, stream=None):

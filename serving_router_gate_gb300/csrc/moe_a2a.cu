@@ -19,11 +19,13 @@
 // order (0 <= i < cnt[n][c]).  The GEMM-order slot offsets are G(0, c).
 //
 // One kernel moves rows either way (a pure copy; HBM-bound: 2 x rows x H x 2
-// bytes).  Each CTA loads the N x S_local counts into shared memory, forms X and
-// G with two block-wide scans, and its warps then take rows of the exchange
-// order grid-stride: a binary search over X finds the row's block, and the
-// warp's lanes copy the row as 16-byte vectors, several loads in flight per lane
-// before the stores.
+// bytes) and can record, for each destination row, its source row (with the
+// GEMM order as destination, that map lets FC2 store its output rows straight
+// back in exchange order).  Each CTA loads the N x S_local counts into shared
+// memory, forms X and G with two block-wide scans, and its warps then take rows
+// of the exchange order grid-stride: a binary search over X finds the row's
+// block, and the warp's lanes copy the row as 16-byte vectors, several loads in
+// flight per lane before the stores.
 #include <algorithm>
 
 #include "moe_internal.cuh"
@@ -74,7 +76,7 @@ __device__ int64_t block_exclusive_scan(const int32_t* val, int32_t* out, int nb
 __global__ void __launch_bounds__(A2A_THREADS, 4)
 a2a_regroup_kernel(const int32_t* __restrict__ cnt_g, int N, int S_l, int64_t rows_cap,
                    const uint4* __restrict__ src, uint4* __restrict__ dst, int row_vecs, int to_exchange,
-                   int32_t* __restrict__ offsets, int32_t* status) {
+                   int32_t* __restrict__ offsets, int32_t* __restrict__ row_map, int32_t* status) {
     extern __shared__ int32_t a2a_sm[];
     int32_t* X = a2a_sm;                // [N * S_l] exchange-order starts, then (first) the counts
     int32_t* G = a2a_sm + N * S_l;      // [N * S_l] GEMM-order starts
@@ -119,6 +121,7 @@ a2a_regroup_kernel(const int32_t* __restrict__ cnt_g, int N, int S_l, int64_t ro
         const int64_t r = (int64_t)G[b] + (q - X[b]);
         const int64_t from = to_exchange ? r : q, to = to_exchange ? q : r;
         if (!in_bounds(from, rows_cap, status) || !in_bounds(to, rows_cap, status)) continue;
+        if (row_map && lane == 0) row_map[to] = (int32_t)from;
         const uint4* s = src + from * row_vecs;
         uint4* d = dst + to * row_vecs;
         for (int v0 = lane; v0 < row_vecs; v0 += 32 * A2A_UNROLL) {
@@ -144,7 +147,7 @@ cudaError_t launch_a2a_regroup(const A2aRegroupLaunch& L, int num_sms, cudaStrea
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms * 4));
     return launch_k("a2a_regroup_kernel", a2a_regroup_kernel, dim3(grid), dim3(A2A_THREADS), smem, s, L.recv_counts,
                     L.N, L.S_local, L.rows_cap, reinterpret_cast<const uint4*>(L.src), reinterpret_cast<uint4*>(L.dst),
-                    L.H / 8, L.to_exchange ? 1 : 0, L.offsets, &L.hdr->status);
+                    L.H / 8, L.to_exchange ? 1 : 0, L.offsets, L.row_map, &L.hdr->status);
 }
 
 }  // namespace moe

@@ -386,7 +386,7 @@ static moe_status_t gemm_call(bool fc1, const moe_bf16_t* a, int64_t rows_cap, c
                               cudaStream_t s, float* out_sh_part = nullptr, int ksplit_sh = 1,
                               int64_t max_group_rows = -1, const float* b_scale = nullptr,
                               const float* b_scale_sh = nullptr, const float* a_scale = nullptr,
-                              const float* a_scale_sh = nullptr) {
+                              const float* a_scale_sh = nullptr, const int32_t* out_row = nullptr) {
     GemmLaunch L;
     L.swiglu = fc1;
     L.a = a;
@@ -398,6 +398,7 @@ static moe_status_t gemm_call(bool fc1, const moe_bf16_t* a, int64_t rows_cap, c
     L.Nb = fc1 ? 2 * I : H;
     L.N_out = fc1 ? I : H;
     L.out = out;
+    L.out_row = out_row;
     L.a_sh = a_sh;
     L.T_sh = I_sh > 0 ? T : 0;
     L.b_sh = Ws;
@@ -459,6 +460,19 @@ moe_status_t moe_grouped_fc2(const moe_bf16_t* h, int64_t rows_cap, const int32_
     if (st != MOE_OK) return st;
     return gemm_call(false, h, rows_cap, offsets, G, W2, H, I, h_shared, T, W2s, I_shared_total, y, y_shared, ws,
                      (cudaStream_t)stream);
+}
+
+moe_status_t moe_grouped_fc2_scatter(const moe_bf16_t* h, int64_t rows_cap, const int32_t* offsets, int G,
+                                     const moe_bf16_t* W2, int H, int I, const moe_bf16_t* h_shared, int64_t T,
+                                     const moe_bf16_t* W2s, int I_shared_total, const int32_t* y_row, moe_bf16_t* y,
+                                     moe_bf16_t* y_shared, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    MOE_NVTX("moe_grouped_fc2_scatter");
+    moe_status_t st = check_gemm_args(h, rows_cap, offsets, G, W2, H, I, h_shared, T, W2s, I_shared_total, y,
+                                      y_shared, ws, ws_bytes);
+    if (st != MOE_OK) return st;
+    if (rows_cap > 0 && !y_row) return MOE_ERR_INVALID_ARG;
+    return gemm_call(false, h, rows_cap, offsets, G, W2, H, I, h_shared, T, W2s, I_shared_total, y, y_shared, ws,
+                     (cudaStream_t)stream, nullptr, 1, -1, nullptr, nullptr, nullptr, nullptr, y_row);
 }
 
 static moe_status_t finalize_call(const moe_bf16_t* y, int64_t rows_cap, const int32_t* pair_row,
@@ -856,8 +870,8 @@ moe_status_t moe_quantize_fp8_rows(const moe_bf16_t* w, int64_t rows, int K, uin
 }
 
 moe_status_t moe_a2a_regroup(const int32_t* recv_counts, int N, int S_local, const moe_bf16_t* src, moe_bf16_t* dst,
-                             int64_t rows_cap, int H, int direction, int32_t* offsets, void* ws, size_t ws_bytes,
-                             moe_stream_t stream) {
+                             int64_t rows_cap, int H, int direction, int32_t* offsets, int32_t* row_map, void* ws,
+                             size_t ws_bytes, moe_stream_t stream) {
     MOE_NVTX("moe_a2a_regroup");
     if (N < 1 || S_local < 1 || rows_cap < 0 || H <= 0) return MOE_ERR_INVALID_ARG;
     if (direction != MOE_A2A_TO_GEMM && direction != MOE_A2A_TO_EXCHANGE) return MOE_ERR_INVALID_ARG;
@@ -876,6 +890,7 @@ moe_status_t moe_a2a_regroup(const int32_t* recv_counts, int N, int S_local, con
     L.dst = dst;
     L.to_exchange = direction == MOE_A2A_TO_EXCHANGE;
     L.offsets = offsets;
+    L.row_map = row_map;
     L.hdr = static_cast<WsHeader*>(ws);
     return cuda_status(launch_a2a_regroup(L, device_sms(), (cudaStream_t)stream));
 }

@@ -20,7 +20,8 @@
 //               K step, completion signalled through tcgen05.commit.
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes
 //               32*(w%4)..+31 = tile rows), FC1: h = bf16(silu(gate) * up);
-//               FC2: y = bf16(acc); 16-byte stores; rows past the slot's count
+//               FC2: y = bf16(acc); 16-byte stores (a routed row through the
+//               caller's row map when one is given); rows past the slot's count
 //               are not stored.  Two accumulators let the epilogue of one tile
 //               overlap the main loop of the next.
 // Pair mode (kPair, clusters of 2 CTAs): one tcgen05.mma.cta_group::2 of
@@ -108,6 +109,7 @@ struct GemmParams {
     int64_t T_sh;            // rows of the shared problem (0: none)
     uint16_t* out;
     uint16_t* out_sh;
+    const int32_t* out_row;  // or [rows_cap]: routed row r is stored at out row out_row[r]
     const float* scale;      // E4M3 weights: fp32 scale per B row, [G][Nb] (null: bf16 weights)
     const float* scale_sh;   // [Nb_sh]
     const float* a_scale;    // E4M3 activations: fp32 scale per A row, [rows_cap]
@@ -689,11 +691,16 @@ __global__ void __launch_bounds__(threads_of<kQ>(), 1)
             // short-tile launches hold 32 A rows: a taller tile (a caller's bound was
             // wrong) is reported and only its first 32 rows are stored
             if (kShort && tl.rows_valid > BM_SHORT && row_in == 0) report(p.status, MOE_ERR_DEVICE_BOUNDS);
-            const bool valid = row_in < (kShort ? min(tl.rows_valid, BM_SHORT) : tl.rows_valid) &&
-                               in_bounds(tl.row0 + row_in, tl.prob ? p.T_sh : p.rows_cap, p.status);
+            bool valid = row_in < (kShort ? min(tl.rows_valid, BM_SHORT) : tl.rows_valid) &&
+                         in_bounds(tl.row0 + row_in, tl.prob ? p.T_sh : p.rows_cap, p.status);
+            int64_t orow_i = (int64_t)tl.row0 + row_in;
+            if (p.out_row && !tl.prob && valid) {  // routed rows stored through the caller's row map
+                orow_i = __ldg(p.out_row + orow_i);
+                valid = in_bounds(orow_i, p.rows_cap, p.status);
+            }
             const int N_out = tl.prob ? p.N_out_sh : p.N_out;
             uint16_t* out = tl.prob ? p.out_sh : p.out;
-            uint16_t* orow = out + (int64_t)(tl.row0 + row_in) * N_out;
+            uint16_t* orow = out + orow_i * N_out;
             // E4M3 weights: the accumulator of output column n carries B row n's scale;
             // E4M3 activations: and its A row's scale (a power of two)
             constexpr bool kRowScaleB = kFp8 || kA8 || kF4, kRowScaleA = kA8 || kF4;
@@ -1194,6 +1201,7 @@ cudaError_t launch_bn(const GemmLaunch& L, int num_sms, int64_t bound, cudaStrea
     p.prefetch_sh = (kFC1 && has_shared && L.T_sh <= 64) ? 1 : 0;
     p.out = L.out;
     p.out_sh = L.out_sh;
+    p.out_row = L.out_row;
     p.status = &L.hdr->status;
     p.timeout_ns = L.timeout_ns;
 

@@ -459,6 +459,7 @@ struct GemmLaunch {
     const uint16_t* b;         // routed B [G, Nb, K]
     int K, Nb, N_out;          // Nb rows of B per group; N_out output columns
     uint16_t* out;             // [rows_cap, N_out]
+    const int32_t* out_row = nullptr;  // or [rows_cap]: routed row r is stored at out row out_row[r]
     const uint16_t* a_sh;      // shared A [T_sh, K_sh] (or null)
     int64_t T_sh;
     const uint16_t* b_sh;      // shared B [Nb_sh, K_sh]
@@ -514,6 +515,7 @@ struct A2aRegroupLaunch {
     uint16_t* dst;
     bool to_exchange;            // false: exchange -> GEMM order; true: GEMM -> exchange order
     int32_t* offsets;            // [S_local + 1] GEMM-order slot offsets, or null
+    int32_t* row_map;            // [rows_cap]: for each destination row, its source row; or null
     WsHeader* hdr;
 };
 constexpr int kA2aMaxBlocks = 4096;  // N * S_local the shared-memory tables hold

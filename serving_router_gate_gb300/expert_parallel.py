@@ -174,10 +174,11 @@ class EPAllToAllLayer:
       2. the per-slot counts are exchanged (every rank receives, from every source, the
          counts of its own slots), copied to the host with the row offsets (the one host
          synchronisation: the row exchange needs its split sizes), then the rows;
-      3. experts: the received rows are put in slot order (moe_a2a_regroup), FC1+SwiGLU
-         and FC2 of the rank's slots run over them in the same launches as the shared
-         experts over the rank's own tokens (moe_grouped_fc1 / fc2), and the outputs go
-         back to arrival order;
+      3. experts: the received rows are put in slot order (moe_a2a_regroup, which also
+         records each row's arrival position), FC1+SwiGLU and FC2 of the rank's slots run
+         over them in the same launches as the shared experts over the rank's own tokens
+         (moe_grouped_fc1 / moe_grouped_fc2_scatter), FC2 storing each output row at its
+         input's arrival position;
       4. combine: the reverse exchange returns every output row to its token's rank, into
          the place its input row left from, and moe_finalize forms the weighted sum of each
          token's k rows in fixed j order plus the shared output.
@@ -223,8 +224,8 @@ class EPAllToAllLayer:
         self.local_offsets = torch.empty((S_l + 1,), **i32)
         self.recv = torch.empty((self.recv_cap, H), **bf)   # arrival order: rows in, then outputs out
         self.x_loc = torch.empty((self.recv_cap, H), **bf)  # slot order
+        self.row_map = torch.empty((self.recv_cap,), **i32)  # arrival row of each slot-order row
         self.h = torch.empty((self.recv_cap, self.I), **bf)
-        self.y_loc = torch.empty((self.recv_cap, H), **bf)
         self.h_sh = torch.empty((T, self.I_sh), **bf) if self.I_sh else None
         self.y_sh = torch.empty((T, H), **bf) if self.I_sh else None
         self.out = torch.empty((T, H), **bf)
@@ -274,15 +275,18 @@ class EPAllToAllLayer:
 
     def experts(self) -> None:
         """The rank's slots over the received rows, and the shared experts over its own tokens."""
-        from . import MOE_A2A_TO_EXCHANGE, MOE_A2A_TO_GEMM, moe_a2a_regroup, moe_grouped_fc1, moe_grouped_fc2
+        from . import MOE_A2A_TO_GEMM, moe_a2a_regroup, moe_grouped_fc1, moe_grouped_fc2_scatter
         T = self.T
-        moe_a2a_regroup(self.recv_counts, self.recv, self.x_loc, MOE_A2A_TO_GEMM, self.local_offsets, self.ws)
+        moe_a2a_regroup(self.recv_counts, self.recv, self.x_loc, MOE_A2A_TO_GEMM, self.local_offsets, self.ws,
+                        row_map=self.row_map)
         sh = self.I_sh > 0 and T > 0
         moe_grouped_fc1(self.x_loc, self.local_offsets, self.W1, self.x if sh else None, self.W1s if sh else None,
                         self.h, self.h_sh[:T] if sh else None, self.ws)
-        moe_grouped_fc2(self.h, self.local_offsets, self.W2, self.h_sh[:T] if sh else None,
-                        self.W2s if sh else None, self.y_loc, self.y_sh[:T] if sh else None, self.ws)
-        moe_a2a_regroup(self.recv_counts, self.y_loc, self.recv, MOE_A2A_TO_EXCHANGE, None, self.ws)
+        # FC2 stores each output row at its input's arrival row (the received rows are
+        # no longer needed): the outputs are in exchange order for the return trip
+        moe_grouped_fc2_scatter(self.h, self.local_offsets, self.W2, self.h_sh[:T] if sh else None,
+                                self.W2s if sh else None, self.row_map, self.recv, self.y_sh[:T] if sh else None,
+                                self.ws)
 
     def combine(self) -> torch.Tensor:
         """After the reverse exchange: each token's weighted sum (plus the shared output)."""
@@ -310,20 +314,26 @@ class EPAllToAllLayer:
         return self.combine()
 
 
-def a2a_forward_local(layers, xs):
+def a2a_forward_local(layers, xs, after_phase=None):
     """All ranks of an all-to-all layer held by one process on one device (a stand-in for N
     GPUs): the ranks' steps run one after another, and each exchange is a set of device
     copies between the ranks' buffers in the order an all-to-all delivers them.  Returns
-    each rank's output."""
+    each rank's output.  after_phase(name), if given, is called after each phase (the
+    ranks' dispatches, the count exchange, the plans, the row exchange, the experts, the
+    reverse exchange, the combines), e.g. to separate their kernels in a timeline."""
     N = len(layers)
     assert all(L.world == N and L.rank == r for r, L in enumerate(layers)) and len(xs) == N
+    note = after_phase or (lambda name: None)
     for L, x in zip(layers, xs):
         L.dispatch(x)
+    note("dispatch")
     for d, Ld in enumerate(layers):
         for s, Ls in enumerate(layers):
             Ld.recv_counts[s].copy_(Ls.counts[Ld.start:Ld.start + Ld.count])
+    note("count exchange")
     for L in layers:
         L.plan()
+    note("plan")
 
     def blocks(splits):
         at = [0]
@@ -339,11 +349,16 @@ def a2a_forward_local(layers, xs):
             assert n == Ld.recv_splits[s]
             if n:
                 Ld.recv[recv_at[d][s]:recv_at[d][s] + n].copy_(Ls.send[send_at[s][d]:send_at[s][d] + n])
+    note("row exchange")
     for L in layers:
         L.experts()
+    note("experts")
     for d, Ld in enumerate(layers):
         for s, Ls in enumerate(layers):
             n = Ls.send_splits[d]
             if n:
                 Ls.send[send_at[s][d]:send_at[s][d] + n].copy_(Ld.recv[recv_at[d][s]:recv_at[d][s] + n])
-    return [L.combine() for L in layers]
+    note("reverse exchange")
+    outs = [L.combine() for L in layers]
+    note("combine")
+    return outs

@@ -189,7 +189,7 @@ def test_a2a_regroup_rejects_bad_arguments_on_host():
 
     def call(N=4, S_l=8, src=FAKE, dst=other, rows=64, H=256, direction=moe.MOE_A2A_TO_GEMM, counts=FAKE,
              ws=FAKE, ws_bytes=1 << 20):
-        return f(counts, N, S_l, src, dst, rows, H, direction, None, ws, ws_bytes, None)
+        return f(counts, N, S_l, src, dst, rows, H, direction, None, None, ws, ws_bytes, None)
 
     assert call(N=0) == moe.MOE_ERR_INVALID_ARG
     assert call(S_l=0) == moe.MOE_ERR_INVALID_ARG
@@ -204,6 +204,12 @@ def test_a2a_regroup_rejects_bad_arguments_on_host():
     assert call(dst=odd) == moe.MOE_ERR_INVALID_ARG            # not 16-byte aligned
     assert call(ws=None) == moe.MOE_ERR_WORKSPACE
     assert call(ws_bytes=64) == moe.MOE_ERR_WORKSPACE
+    # FC2 with a row map: the map is required when there are rows
+    fs = moe._lib.moe_grouped_fc2_scatter
+    assert fs(FAKE, 64, FAKE, 4, FAKE, 256, 256, None, 0, None, 0, None, other, None, FAKE, 1 << 20,
+              None) == moe.MOE_ERR_INVALID_ARG
+    assert fs(FAKE, 64, FAKE, 4, FAKE, 256, 250, None, 0, None, 0, FAKE, other, None, FAKE, 1 << 20,
+              None) == moe.MOE_ERR_UNSUPPORTED  # I not a multiple of 64
     assert moe.moe_get_launch_count() == before
 
 

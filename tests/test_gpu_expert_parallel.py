@@ -97,11 +97,14 @@ def test_a2a_regroup_matches_the_oracle_order(N, S_l, H, seed):
     rc = counts.cuda()
     off = torch.full((S_l + 1,), -7, dtype=torch.int32, device="cuda")
     dst = nan.clone()
+    row_map = torch.full((cap,), -5, dtype=torch.int32, device="cuda")
     before = moe.moe_get_launch_count()
-    moe.moe_a2a_regroup(rc, src, dst, moe.MOE_A2A_TO_GEMM, off, ws)
+    moe.moe_a2a_regroup(rc, src, dst, moe.MOE_A2A_TO_GEMM, off, ws, row_map=row_map)
     assert moe.moe_get_launch_count() == before + 1
     ref_off, gemm_row, exch_row = oracle.a2a_regroup(counts.numpy())
     assert off.cpu().tolist() == ref_off.tolist()
+    assert row_map[:R].cpu().tolist() == exch_row.tolist()
+    assert row_map[R:].cpu().tolist() == [-5] * (cap - R)
     exch = torch.from_numpy(exch_row.astype(np.int64))
     assert torch.equal(_bits(dst[:R]), _bits(src[:R])[exch])
     assert torch.equal(_bits(dst[R:]), _bits(nan[R:]))
@@ -128,6 +131,39 @@ def test_a2a_regroup_flags_bad_counts_and_moves_nothing(bad):
     assert moe.moe_get_device_status(ws) == moe.MOE_ERR_DEVICE_BOUNDS
     assert int(dst.view(torch.int16).abs().sum()) == 0
     assert off.cpu().tolist() == [-7, -7, -7]
+
+
+@pytest.mark.parametrize("shared", [False, True])
+def test_grouped_fc2_scatter_equals_fc2_with_rows_moved(shared):
+    # 7 groups with ragged counts (an empty one, a partial last tile), a shared problem
+    g = torch.Generator().manual_seed(11)
+    H, I, G, T = 256, 192, 7, 40
+    counts = [130, 0, 5, 64, 257, 1, 33]
+    rows = sum(counts)
+    cap = rows + 9
+    offsets = torch.tensor([0] + list(np.cumsum(counts)), dtype=torch.int32, device="cuda")
+    h = (torch.randn(cap, I, generator=g) * 0.5).to(torch.bfloat16).cuda()
+    W2 = (torch.randn(G, H, I, generator=g) * 0.05).to(torch.bfloat16).cuda()
+    h_sh = W2s = None
+    if shared:
+        h_sh = (torch.randn(T, 128, generator=g) * 0.5).to(torch.bfloat16).cuda()
+        W2s = (torch.randn(H, 128, generator=g) * 0.05).to(torch.bfloat16).cuda()
+    ws = torch.zeros(moe.MOE_WS_HEADER_BYTES, dtype=torch.uint8, device="cuda")
+    y = torch.empty(cap, H, dtype=torch.bfloat16, device="cuda")
+    ysh = torch.empty(T, H, dtype=torch.bfloat16, device="cuda") if shared else None
+    moe.moe_grouped_fc2(h, offsets, W2, h_sh, W2s, y, ysh, ws)
+    perm = torch.randperm(rows, generator=g)
+    y_row = torch.full((cap,), -1, dtype=torch.int32)
+    y_row[:rows] = perm.to(torch.int32)
+    y2 = torch.full((cap, H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ysh2 = torch.empty(T, H, dtype=torch.bfloat16, device="cuda") if shared else None
+    moe.moe_grouped_fc2_scatter(h, offsets, W2, h_sh, W2s, y_row.cuda(), y2, ysh2, ws)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status(ws) == 0
+    assert torch.equal(_bits(y2)[perm], _bits(y[:rows]))
+    assert torch.equal(_bits(y2[rows:]), _bits(torch.full((cap - rows, H), float("nan"), dtype=torch.bfloat16)))
+    if shared:
+        assert torch.equal(_bits(ysh2), _bits(ysh))
 
 
 def _a2a_layers(inp, world, max_T, recv_cap=None):
