@@ -405,8 +405,9 @@ def run_cpu_baseline(inp_dev, cfg, target_s=10.0, T_cap=None):
                 single_thread_sample=f"first {n1} tokens, {t1:.1f} s on one thread"), t
 
 
-def _ep_layer(inp, cfg, world, rank, dev):
-    """This rank's expert-parallel layer over the workload's inputs."""
+def _ep_layer(inp, cfg, world, rank, dev, peer=None):
+    """This rank's expert-parallel layer over the workload's inputs (peer: a PeerReduction
+    in place of the collective all-reduce)."""
     from serving_router_gate_gb300.expert_parallel import EPMoELayer
     W1s = W2s = None
     if inp["W1s"] is not None:
@@ -415,7 +416,8 @@ def _ep_layer(inp, cfg, world, rank, dev):
     return EPMoELayer(d(inp["Wg"]), d(inp["W1"]), d(inp["W2"]), cfg.k, cfg.renorm, cfg.T, world, rank,
                       logit_bias=d(inp["bias"]), rep_offset=d(inp["rep_offset"]), rep_slots=d(inp["rep_slots"]),
                       W1s=d(W1s), W2s=d(W2s), shared_gate_w=d(inp["w_s"]), on_input=cfg.on_input,
-                      n_group=cfg.n_group, topk_group=cfg.topk_group, fp8=cfg.fp8, act8=cfg.act8, fp4=cfg.fp4)
+                      n_group=cfg.n_group, topk_group=cfg.topk_group, fp8=cfg.fp8, act8=cfg.act8, fp4=cfg.fp4,
+                      peer=peer)
 
 
 def _a2a_layer(inp, cfg, world, rank, dev, max_T=None):
@@ -444,7 +446,11 @@ def bench_ours(args):
     # expert parallelism (more than one rank): every rank routes the whole batch, computes
     # its slot range and shared shard, and one all-reduce sums the partials; otherwise
     # (replicas) every rank runs its own batch through the whole layer
-    ep = _ep_layer(inp, cfg, ws_, rank, dev) if (args.partition == "ep" and ws_ > 1) else None
+    peer = None
+    if args.partition == "ep" and ws_ > 1 and args.reduce == "peer":
+        from serving_router_gate_gb300.expert_parallel import PeerReduction
+        peer = PeerReduction(cfg.T, cfg.H, ws_, rank, dev)
+    ep = _ep_layer(inp, cfg, ws_, rank, dev, peer) if (args.partition == "ep" and ws_ > 1) else None
     # all-to-all expert parallelism: every rank holds its own batch of T tokens and the
     # experts of its slot range; rows travel to their slots' ranks and back (NCCL).  The
     # per-kernel pass and the roofline then describe the one-GPU layer on the rank's batch.
@@ -664,7 +670,9 @@ def bench_ours(args):
                                  "workload's shapes (no checkpoint)",
         "config": {"workload": cfg.name, "shape": mi.describe(cfg), "tokens_per_gpu": T,
                    "parallelism": (f"expert parallel x{ws_} (contiguous slot ranges, shared-expert shards, one "
-                                   f"fp32 all-reduce of the partials)" if ep is not None else
+                                   + ("reduction by peer loads of the partials in rank order (moe_ep_reduce))"
+                                      if peer is not None else "fp32 all-reduce of the partials)")
+                                   if ep is not None else
                                    f"all-to-all expert parallel x{ws_} (each rank its own batch, contiguous "
                                    f"slot ranges, rows dispatched to their slots' ranks and returned; the "
                                    f"per-kernel pass and roofline: the one-GPU layer on the rank's batch)"
@@ -808,6 +816,92 @@ def bench_a2a_local(args):
     print(json.dumps(res), flush=True)
 
 
+def bench_ep_local(args):
+    """Expert parallelism with the peer reduction over R ranks held by this process on one
+    GPU (every rank routes the whole batch, computes its slot range and shared shard into
+    its partial slot, raises its flag; then every rank forms the rank-order sum of all
+    partials): times the whole step and reports the reduction kernel against the HBM peak
+    (all ranks' buffers are local here; on R GPUs R - 1 of the R reads go to peers)."""
+    import serving_router_gate_gb300 as moe
+    from serving_router_gate_gb300.expert_parallel import PeerReduction
+    R = args.ep_ranks
+    cfg = mi.CONFIGS[args.workload]
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    inp = mi.make_inputs(cfg, device=dev)
+    reds = PeerReduction.local_set(cfg.T, cfg.H, R, dev)
+    eps = [_ep_layer(inp, cfg, R, r, dev, reds[r]) for r in range(R)]
+    x = inp["x"]
+    stream = torch.cuda.current_stream()
+    flush = L2Flush(dev)
+    K, W = args.steps, args.warmup
+
+    def step():
+        for e in eps:
+            e.write_partial(x)
+        for r in reds:
+            r.reduce()
+
+    for _ in range(W):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(0)
+    clocks.start()
+    t = time_steps([step], K, flush, stream)[0]
+    clk = clocks.stop()
+    ms = statistics.mean(t)
+    c0 = moe.moe_get_launch_count()
+    step()
+    n_launch = moe.moe_get_launch_count() - c0
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_launch + 2)]
+    for e in evs:
+        e.record(stream)
+    torch.cuda.synchronize()
+    per_pos, labels = None, None
+    for _ in range(K):
+        flush()
+        moe.moe_launch_events_arm(evs)
+        try:
+            step()
+            moe.moe_launch_events_mark()
+            labels = moe.moe_launch_events_used()
+        finally:
+            moe.moe_launch_events_arm(None)
+        torch.cuda.synchronize()
+        if per_pos is None:
+            per_pos = [[] for _ in range(len(labels) - 1)]
+        for i in range(len(labels) - 1):
+            per_pos[i].append(evs[i].elapsed_time(evs[i + 1]))
+    for r in reds:
+        if moe.moe_get_device_status(r.ws):
+            raise RuntimeError("device status set by the reduction")
+    med = [statistics.median(v) for v in per_pos]
+    kernels = {}
+    for lab, m in zip(labels, med):
+        if lab != "mark":
+            kernels[lab] = kernels.get(lab, 0.0) + m
+    red_ms = kernels.get("ep_reduce_kernel", 0.0)
+    red_bytes = R * (R + 1) * cfg.T * cfg.H * 2  # per rank: R partials read, its output written
+    peaks = _peaks()
+    gbs = red_bytes / (red_ms * 1e-3) / 1e9
+    res = {
+        "metric": METRIC, "value": cfg.T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": K,
+        "warmup": W, "ms_per_step": ms, "higher_is_better": True, "scaling": "strong", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic: seeded N(0,1) activations, N(0,sigma) random-init weights",
+        "config": {"workload": cfg.name, "shape": mi.describe(cfg),
+                   "parallelism": f"expert parallel over {R} ranks held by one process on one GPU (slot ranges "
+                                  f"and shared shards; the reduction by loads of every rank's partial)",
+                   "l2": f"flushed before every timed step ({flush.describe()})"},
+        "kernels_ms": kernels,
+        "ep_reduce": {"bound": "hbm", "launches": R, "algorithmic_bytes": red_bytes, "ms": red_ms,
+                      "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s", "frac": gbs / peaks["hbm"],
+                      "work": "per rank: the R partials [T, H] bf16 read, its output written",
+                      "timing": "launch-event hook, median per launch over the steps, each after an L2 flush"},
+        "clocks": clk,
+    }
+    print(json.dumps(res), flush=True)
+
+
 def bench_reference(args):
     """The fp64 oracle, as it stands, on the host cores: each step a bounded
     sample of the workload (its first n tokens through the whole layer)."""
@@ -871,6 +965,12 @@ def main():
     ap.add_argument("--a2a-ranks", type=int, default=0,
                     help="one GPU: run the all-to-all expert-parallel layer over this many ranks held by one "
                          "process (exchanges as device copies) and time its kernels")
+    ap.add_argument("--ep-ranks", type=int, default=0,
+                    help="one GPU: run expert parallelism with the peer reduction over this many ranks held by "
+                         "one process and time its kernels")
+    ap.add_argument("--reduce", choices=["collective", "peer"], default="collective",
+                    help="--partition ep on several GPUs: the all-reduce of torch.distributed, or the library's "
+                         "reduction by loads of every rank's partial (CUDA IPC)")
     ap.add_argument("--partition", choices=["ep", "a2a", "replicas"], default="ep",
                     help="with more than one rank: expert parallelism over one batch with one reduction "
                          "(default), all-to-all expert parallelism (each rank its own batch, rows dispatched "
@@ -889,10 +989,13 @@ def main():
         sys.exit(f"bench.py: --gpus {args.gpus} but the launcher started {ws} ranks")
     if args.impl == "reference":
         bench_reference(args)
-    elif args.a2a_ranks > 0:
+    elif args.a2a_ranks > 0 or args.ep_ranks > 0:
         if ws is not None and int(ws) > 1:
-            sys.exit("bench.py: --a2a-ranks holds every rank in one process on one GPU")
-        bench_a2a_local(args)
+            sys.exit("bench.py: --a2a-ranks / --ep-ranks hold every rank in one process on one GPU")
+        if args.a2a_ranks > 0:
+            bench_a2a_local(args)
+        else:
+            bench_ep_local(args)
     else:
         bench_ours(args)
 

@@ -506,6 +506,56 @@ MOE_API moe_status_t moe_a2a_regroup(const int32_t *recv_counts, int N, int S_lo
                                      moe_bf16_t *dst, int64_t rows_cap, int H, int direction, int32_t *offsets,
                                      int32_t *row_map, void *ws, size_t ws_bytes, moe_stream_t stream);
 
+/* ---- the expert-parallel reduction by peer loads -------------------------- */
+
+/* The one SUM over the ranks of expert parallelism ([VLLM-EP] ep_reduce_output:
+ * each rank's routed plus shared partial output, summed over the ranks;
+ * ep_reduce_scatter_output: the same sum, each rank keeping a slice of the rows;
+ * [DS-6964]: one reduction per layer), done by plain loads of the ranks'
+ * partials instead of a collective library.  Each rank's bf16 partial [T, H]
+ * lives in memory every rank can read (its own GPU's, mapped into the others'
+ * address spaces with moe_ipc_export / moe_ipc_import); each rank holds an int32
+ * flag per rank.  Per step with epoch e (e grows by one per step; flags start
+ * at 0, so e starts at 1):
+ *   1. a rank writes its partial into slot e % 2 of its two partial buffers,
+ *   2. moe_ep_signal raises its flag to e in every rank's flag array,
+ *   3. moe_ep_reduce waits until every flag of its own array has reached e and
+ *      forms its rows of the sum from slot e % 2 of every rank.
+ * Two slots suffice: a rank writes slot e % 2 again at step e + 2 only after its
+ * step e + 1 reduce saw every rank's flag e + 1, which each rank raises after
+ * its own step e reduce (the last read of that slot) on its stream. */
+
+/* Raise this rank's flag to `epoch` in every rank's flag array: peer_flags is a
+ * HOST array of N device pointers, peer_flags[n] = rank n's int32 flags[N] (as
+ * mapped on this GPU); flag `rank` of each is written.  Enqueued on `stream`
+ * after the work that writes this rank's partial: the kernel waits for it,
+ * fences at system scope and stores with release semantics.  N <= 16. */
+MOE_API moe_status_t moe_ep_signal(int32_t *const *peer_flags, int N, int rank, int32_t epoch, moe_stream_t stream);
+
+/* out rows [row0, row1) of [T, H] = bf16( sum over n = 0 .. N-1, in that order,
+ * of the fp32 values of partials[n] rows ) (row1 = T on every rank: the
+ * all-reduce; a slice per rank: the reduce-scatter).  partials is a HOST array
+ * of N device pointers to the [T, H] bf16 partials (16-byte aligned; as mapped
+ * on this GPU).  The kernel first waits until flags[n] - epoch >= 0 (int32
+ * wrap-around) for every n, at most the library's wait limit
+ * (moe_set_wait_timeout_ns); on timeout it sets MOE_ERR_TIMEOUT in the status
+ * word and writes nothing.  ws: only its status word is used.  N <= 16. */
+MOE_API moe_status_t moe_ep_reduce(const moe_bf16_t *const *partials, int N, const int32_t *flags, int32_t epoch,
+                                   int64_t row0, int64_t row1, int H, moe_bf16_t *out, void *ws, size_t ws_bytes,
+                                   moe_stream_t stream);
+
+/* Host-side mapping of device buffers between processes (CUDA IPC), for the
+ * partial buffers and flags above.  moe_ipc_export writes the
+ * MOE_IPC_HANDLE_BYTES-byte handle of the allocation holding `ptr` and ptr's
+ * offset inside it; moe_ipc_import, in another process, maps that allocation
+ * (with peer access enabled) and returns the address of the same byte;
+ * moe_ipc_close unmaps it (pass the imported pointer and its offset).  The
+ * exporting process must keep the allocation alive while it is mapped. */
+#define MOE_IPC_HANDLE_BYTES 64
+MOE_API moe_status_t moe_ipc_export(const void *ptr, uint8_t *handle, int64_t *offset);
+MOE_API moe_status_t moe_ipc_import(const uint8_t *handle, int64_t offset, void **ptr);
+MOE_API moe_status_t moe_ipc_close(void *ptr, int64_t offset);
+
 /* ---- diagnostics ---------------------------------------------------------- */
 
 /* Launch one block whose single thread waits on an mbarrier that nothing ever

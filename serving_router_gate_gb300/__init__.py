@@ -29,7 +29,8 @@ __all__ = [
     "moe_forward_nvfp4", "moe_quantize_nvfp4_rows", "nvfp4_sf_row_bytes", "MOE_WS_HEADER_BYTES",
     "moe_grouped_fc2_fp8", "moe_grouped_fc1_w8a8", "moe_grouped_fc2_w8a8", "moe_launch_events_arm",
     "moe_launch_events_mark", "moe_launch_events_used", "EXPORTED_SYMBOLS", "moe_a2a_regroup",
-    "moe_grouped_fc2_scatter",
+    "moe_grouped_fc2_scatter", "moe_ep_signal", "moe_ep_reduce", "moe_ipc_export", "moe_ipc_import",
+    "moe_ipc_close", "MOE_IPC_HANDLE_BYTES",
     "MOE_A2A_TO_GEMM", "MOE_A2A_TO_EXCHANGE",
 ]
 
@@ -46,6 +47,7 @@ MOE_A2A_TO_GEMM = 0
 MOE_A2A_TO_EXCHANGE = 1
 MOE_LAUNCH_LABEL_BYTES = 48  # bytes per label written by moe_launch_events_used
 MOE_WS_HEADER_BYTES = 256    # the workspace header (status word, counters) a caller never writes
+MOE_IPC_HANDLE_BYTES = 64    # bytes of a handle moe_ipc_export writes
 
 EXPORTED_SYMBOLS = (
     "moe_status_string", "moe_workspace_size", "moe_workspace_init", "moe_get_device_status",
@@ -56,7 +58,8 @@ EXPORTED_SYMBOLS = (
     "moe_forward_nvfp4", "moe_quantize_nvfp4_rows",
     "moe_forward_w8a8", "moe_quantize_act_rows", "moe_grouped_fc1_w8a8", "moe_grouped_fc2_w8a8",
     "moe_launch_events_arm", "moe_launch_events_mark", "moe_launch_events_used", "moe_a2a_regroup",
-    "moe_grouped_fc2_scatter",
+    "moe_grouped_fc2_scatter", "moe_ep_signal", "moe_ep_reduce", "moe_ipc_export", "moe_ipc_import",
+    "moe_ipc_close",
 )
 
 
@@ -108,6 +111,11 @@ def _load():
         "moe_finalize": ([P, i64, P, P, i64, i32, i32, P, P, P, P, P, sz, P], i32),
         "moe_a2a_regroup": ([P, i32, i32, P, P, i64, i32, i32, P, P, P, sz, P], i32),
         "moe_grouped_fc2_scatter": ([P, i64, P, i32, P, i32, i32, P, i64, P, i32, P, P, P, P, sz, P], i32),
+        "moe_ep_signal": ([P, i32, i32, i32, P], i32),
+        "moe_ep_reduce": ([P, i32, P, i32, i64, i64, i32, P, P, sz, P], i32),
+        "moe_ipc_export": ([P, P, P], i32),
+        "moe_ipc_import": ([P, i64, P], i32),
+        "moe_ipc_close": ([P, i64], i32),
         "moe_debug_wait_timeout": ([P, sz, u64, P], i32),
         "moe_set_wait_timeout_ns": ([u64], None),
         "moe_route_noalloc": ([P, P, P, i64, i32, i32, i32, i32, P, P, P], i32),
@@ -519,6 +527,59 @@ def moe_grouped_fc2_scatter(h, offsets, W2, h_shared, W2s, y_row, y, y_shared, w
                                       _ptr(y_shared, "y_shared", _bf16, (T, H), allow_none=True),
                                       _ptr(ws, "ws", torch.uint8), ws.numel(), _stream(stream))
     _check("moe_grouped_fc2_scatter", st)
+
+
+def _ptr_array(ptrs, name):
+    """A host array of device addresses: ints (e.g. peer-mapped addresses) or CUDA tensors."""
+    vals = []
+    for i, p in enumerate(ptrs):
+        if isinstance(p, torch.Tensor):
+            if not p.is_cuda or not p.is_contiguous():
+                raise ValueError(f"{name}[{i}] must be a contiguous CUDA tensor")
+            p = p.data_ptr()
+        vals.append(int(p))
+    return (ctypes.c_void_p * len(vals))(*vals)
+
+
+def moe_ep_signal(peer_flags, rank, epoch, stream=None):
+    """Raise this rank's flag to `epoch` in every rank's flag array (peer_flags[n]: the
+    address on this GPU of rank n's int32 flags)."""
+    arr = _ptr_array(peer_flags, "peer_flags")
+    _check("moe_ep_signal", _lib.moe_ep_signal(arr, len(peer_flags), int(rank), int(epoch), _stream(stream)))
+
+
+def moe_ep_reduce(partials, flags, epoch, row0, row1, out, ws, stream=None):
+    """out rows [row0, row1) = bf16 of the rank-order fp32 sum of the ranks' bf16 partials
+    [T, H] (addresses or tensors), once flags (this rank's [N] int32) all reach epoch."""
+    N = len(partials)
+    T, H = out.shape
+    if not 0 <= row0 <= row1 <= T:
+        raise ValueError(f"rows [{row0}, {row1}) outside [0, {T})")
+    arr = _ptr_array(partials, "partials")
+    st = _lib.moe_ep_reduce(arr, N, _ptr(flags, "flags", _i32, (N,)), int(epoch), int(row0), int(row1), H,
+                            _ptr(out, "out", _bf16), _ptr(ws, "ws", torch.uint8), ws.numel(), _stream(stream))
+    _check("moe_ep_reduce", st)
+
+
+def moe_ipc_export(t: torch.Tensor):
+    """(handle bytes, offset) that let another process map the CUDA tensor t's memory."""
+    buf = ctypes.create_string_buffer(MOE_IPC_HANDLE_BYTES)
+    off = ctypes.c_int64(0)
+    _check("moe_ipc_export", _lib.moe_ipc_export(_ptr(t, "t"), buf, ctypes.byref(off)))
+    return bytes(buf.raw), int(off.value)
+
+
+def moe_ipc_import(handle: bytes, offset: int) -> int:
+    """Map another process's exported memory here; returns the address of its tensor."""
+    if len(handle) != MOE_IPC_HANDLE_BYTES:
+        raise ValueError("bad IPC handle")
+    p = ctypes.c_void_p(0)
+    _check("moe_ipc_import", _lib.moe_ipc_import(handle, int(offset), ctypes.byref(p)))
+    return int(p.value)
+
+
+def moe_ipc_close(addr: int, offset: int) -> None:
+    _check("moe_ipc_close", _lib.moe_ipc_close(ctypes.c_void_p(int(addr)), int(offset)))
 
 
 def moe_debug_wait_timeout(ws, timeout_ns, stream=None):

@@ -895,6 +895,82 @@ moe_status_t moe_a2a_regroup(const int32_t* recv_counts, int N, int S_local, con
     return cuda_status(launch_a2a_regroup(L, device_sms(), (cudaStream_t)stream));
 }
 
+moe_status_t moe_ep_signal(int32_t* const* peer_flags, int N, int rank, int32_t epoch, moe_stream_t stream) {
+    MOE_NVTX("moe_ep_signal");
+    if (!peer_flags || N < 1 || N > kEpMaxRanks || rank < 0 || rank >= N) return MOE_ERR_INVALID_ARG;
+    for (int n = 0; n < N; ++n)
+        if (!peer_flags[n] || !aligned(peer_flags[n], 4)) return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_ep_signal(peer_flags, N, rank, epoch, (cudaStream_t)stream));
+}
+
+moe_status_t moe_ep_reduce(const moe_bf16_t* const* partials, int N, const int32_t* flags, int32_t epoch, int64_t row0,
+                           int64_t row1, int H, moe_bf16_t* out, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    MOE_NVTX("moe_ep_reduce");
+    if (!partials || N < 1 || N > kEpMaxRanks || !flags || row0 < 0 || row1 < row0 || H <= 0)
+        return MOE_ERR_INVALID_ARG;
+    if (!dim_ok(H)) return MOE_ERR_UNSUPPORTED;
+    if (!ws || ws_bytes < kWsHeaderBytes) return MOE_ERR_WORKSPACE;
+    if (row1 == row0) return MOE_OK;
+    if (!out || !aligned(out, 16)) return MOE_ERR_INVALID_ARG;
+    EpReduceLaunch L = {};
+    for (int n = 0; n < N; ++n) {
+        if (!partials[n] || !aligned(partials[n], 16)) return MOE_ERR_INVALID_ARG;
+        L.partials[n] = partials[n];
+    }
+    L.N = N;
+    L.flags = flags;
+    L.epoch = epoch;
+    L.row0 = row0;
+    L.row1 = row1;
+    L.H = H;
+    L.out = out;
+    L.timeout_ns = g_timeout_ns.load();
+    L.hdr = static_cast<WsHeader*>(ws);
+    return cuda_status(launch_ep_reduce(L, device_sms(), (cudaStream_t)stream));
+}
+
+moe_status_t moe_ipc_export(const void* ptr, uint8_t* handle, int64_t* offset) {
+    MOE_NVTX("moe_ipc_export");
+    if (!ptr || !handle || !offset) return MOE_ERR_INVALID_ARG;
+    // cuMemGetAddressRange (driver API, version 3020): base and size of the allocation
+    using RangeFn = CUresult (*)(CUdeviceptr*, size_t*, CUdeviceptr);
+    static RangeFn range_fn = nullptr;
+    if (!range_fn) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &fn, 3020, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+            return MOE_ERR_CUDA;
+        range_fn = reinterpret_cast<RangeFn>(fn);
+    }
+    CUdeviceptr base = 0;
+    size_t size = 0;
+    if (range_fn(&base, &size, reinterpret_cast<CUdeviceptr>(ptr)) != CUDA_SUCCESS) return MOE_ERR_CUDA;
+    cudaIpcMemHandle_t h;
+    if (cudaIpcGetMemHandle(&h, reinterpret_cast<void*>(base)) != cudaSuccess) return MOE_ERR_CUDA;
+    std::memcpy(handle, &h, sizeof(h));
+    *offset = (int64_t)(reinterpret_cast<uintptr_t>(ptr) - (uintptr_t)base);
+    return MOE_OK;
+}
+
+moe_status_t moe_ipc_import(const uint8_t* handle, int64_t offset, void** ptr) {
+    MOE_NVTX("moe_ipc_import");
+    if (!handle || !ptr || offset < 0) return MOE_ERR_INVALID_ARG;
+    cudaIpcMemHandle_t h;
+    std::memcpy(&h, handle, sizeof(h));
+    void* base = nullptr;
+    if (cudaIpcOpenMemHandle(&base, h, cudaIpcMemLazyEnablePeerAccess) != cudaSuccess) return MOE_ERR_CUDA;
+    *ptr = static_cast<char*>(base) + offset;
+    return MOE_OK;
+}
+
+moe_status_t moe_ipc_close(void* ptr, int64_t offset) {
+    MOE_NVTX("moe_ipc_close");
+    if (!ptr || offset < 0) return MOE_ERR_INVALID_ARG;
+    return cuda_status(cudaIpcCloseMemHandle(static_cast<char*>(ptr) - offset));
+}
+
 moe_status_t moe_debug_wait_timeout(void* ws, size_t ws_bytes, uint64_t timeout_ns, moe_stream_t stream) {
     if (!ws || ws_bytes < kWsHeaderBytes) return MOE_ERR_WORKSPACE;
     if (timeout_ns == 0 || timeout_ns > 10000000000ull) return MOE_ERR_INVALID_ARG;

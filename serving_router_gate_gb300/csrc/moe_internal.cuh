@@ -522,6 +522,23 @@ constexpr int kA2aMaxBlocks = 4096;  // N * S_local the shared-memory tables hol
 size_t a2a_regroup_smem_bytes(int N, int S_local);
 cudaError_t launch_a2a_regroup(const A2aRegroupLaunch& L, int num_sms, cudaStream_t s);
 
+// The one reduction of expert parallelism by plain loads of the ranks' partials
+// (moe_ep_signal, moe_ep_reduce).
+constexpr int kEpMaxRanks = 16;
+struct EpReduceLaunch {
+    const uint16_t* partials[kEpMaxRanks];  // [T, H] bf16 partial of each rank (peer-mapped pointers)
+    int N;
+    const int32_t* flags;                    // [N] this rank's flags
+    int32_t epoch;
+    int64_t row0, row1;
+    int H;
+    uint16_t* out;
+    uint64_t timeout_ns;
+    WsHeader* hdr;
+};
+cudaError_t launch_ep_signal(int32_t* const* peer_flags, int N, int rank, int32_t epoch, cudaStream_t s);
+cudaError_t launch_ep_reduce(const EpReduceLaunch& L, int num_sms, cudaStream_t s);
+
 cudaError_t launch_wait_timeout_probe(WsHeader* hdr, uint64_t timeout_ns, cudaStream_t s);
 
 // Row-wise E4M3 quantisation of a bf16 matrix [rows, K] (moe_quantize_fp8_rows).

@@ -22,7 +22,13 @@ its precision) and the result is rounded to bf16 once.
 
 Every rank calls the same three library calls as a one-GPU layer (moe_route,
 moe_permute with its range, moe_forward with its shard); only the reduction is
-a collective.
+a collective -- torch.distributed's all-reduce, or (PeerReduction) the
+library's own kernels reading every rank's partial in rank order through
+mapped memory, with bounded flag waits.
+
+The all-to-all mode (EPAllToAllLayer, below) follows TensorRT-LLM PR #10985's
+other path: every rank holds its own tokens, dispatches each pair's row to
+the rank owning its slot and gets the expert outputs back.
 """
 from __future__ import annotations
 
@@ -82,6 +88,106 @@ def ep_reduce_output(partial: torch.Tensor, group=None, out: Optional[torch.Tens
     return res
 
 
+def ep_row_range(T: int, world: int, rank: int) -> Tuple[int, int]:
+    """Rows [lo, hi) of a [T, H] output that rank `rank` keeps in the reduce-scatter (the
+    vLLM EP patch's ep_reduce_scatter_output): contiguous, as even as T allows."""
+    if world < 1 or not 0 <= rank < world:
+        raise ValueError(f"rank {rank} outside a world of {world}")
+    return rank * T // world, (rank + 1) * T // world
+
+
+class PeerReduction:
+    """The one SUM of expert parallelism by plain loads of every rank's partial
+    (moe_ep_signal / moe_ep_reduce) instead of a collective library.
+
+    Each rank holds two bf16 partial slots [max_T, H] and an int32 flag per rank, all in
+    its own GPU's memory; the other ranks' slots and flags are mapped into this process
+    (CUDA IPC, handles exchanged over the process group), or -- for ranks held by one
+    process on one device (local_set) -- are plain device addresses.  Per step:
+    begin(T) advances the epoch e and returns slot e % 2 to write the partial into;
+    signal() raises this rank's flag to e in every rank's array once the partial is
+    written; reduce(T) waits for every rank's flag e and forms this rank's rows of the
+    sum (all rows, or its slice with scatter=True) in rank order."""
+
+    def __init__(self, max_T: int, H: int, world: int, rank: int, device, group=None, scatter: bool = False,
+                 _exchange: bool = True):
+        from . import MOE_WS_HEADER_BYTES, moe_workspace_init
+        if not 1 <= world <= 16:
+            raise ValueError("1 to 16 ranks")
+        self.max_T, self.H, self.world, self.rank = int(max_T), int(H), int(world), int(rank)
+        self.group, self.scatter = group, bool(scatter)
+        self.slots = torch.empty((2, self.max_T, self.H), dtype=torch.bfloat16, device=device)
+        self.flags = torch.zeros((self.world,), dtype=torch.int32, device=device)
+        self.ws = torch.empty((MOE_WS_HEADER_BYTES,), dtype=torch.uint8, device=device)
+        moe_workspace_init(self.ws)
+        self.out = torch.empty((self.max_T, self.H), dtype=torch.bfloat16, device=device)
+        self.epoch = 0
+        self._imported = []
+        self.peer_slots = self.peer_flags = None
+        if _exchange:
+            self._map_peers()
+
+    def _map_peers(self):
+        """Exchange IPC handles of the slots and flags over the process group and map the
+        other ranks' buffers."""
+        import torch.distributed as dist
+        from . import moe_ipc_export, moe_ipc_import
+        mine = (moe_ipc_export(self.slots), moe_ipc_export(self.flags))
+        allh = [None] * self.world
+        dist.all_gather_object(allh, mine, group=self.group)
+        self.peer_slots, self.peer_flags = [], []
+        for n, ((hs, os_), (hf, of)) in enumerate(allh):
+            if n == self.rank:
+                self.peer_slots.append(self.slots.data_ptr())
+                self.peer_flags.append(self.flags.data_ptr())
+                continue
+            a, b = moe_ipc_import(hs, os_), moe_ipc_import(hf, of)
+            self._imported += [(a, os_), (b, of)]
+            self.peer_slots.append(a)
+            self.peer_flags.append(b)
+
+    @classmethod
+    def local_set(cls, max_T: int, H: int, world: int, device, scatter: bool = False):
+        """The reductions of `world` ranks held by one process on one device, wired to
+        each other's buffers directly."""
+        reds = [cls(max_T, H, world, r, device, scatter=scatter, _exchange=False) for r in range(world)]
+        for r in reds:
+            r.peer_slots = [o.slots.data_ptr() for o in reds]
+            r.peer_flags = [o.flags.data_ptr() for o in reds]
+        return reds
+
+    def begin(self, T: int) -> torch.Tensor:
+        """The slot [T, H] this step's partial goes into (the epoch advances)."""
+        assert 0 < T <= self.max_T
+        self.epoch += 1
+        self.T = int(T)
+        return self.slots[self.epoch % 2, :T]
+
+    def signal(self, stream=None) -> None:
+        from . import moe_ep_signal
+        moe_ep_signal(self.peer_flags, self.rank, self.epoch, stream)
+
+    def rows(self):
+        return ep_row_range(self.T, self.world, self.rank) if self.scatter else (0, self.T)
+
+    def reduce(self, stream=None) -> torch.Tensor:
+        """This rank's rows of the sum over the ranks, bf16 [T, H] (rows outside its slice
+        unwritten with scatter=True)."""
+        from . import moe_ep_reduce
+        slot_bytes = self.max_T * self.H * 2 * (self.epoch % 2)
+        lo, hi = self.rows()
+        out = self.out[:self.T]
+        moe_ep_reduce([p + slot_bytes for p in self.peer_slots], self.flags, self.epoch, lo, hi, out, self.ws,
+                      stream)
+        return out
+
+    def close(self) -> None:
+        from . import moe_ipc_close
+        for a, off in self._imported:
+            moe_ipc_close(a, off)
+        self._imported = []
+
+
 class EPMoELayer:
     """One rank's share of an expert-parallel MoE layer.
 
@@ -92,9 +198,13 @@ class EPMoELayer:
     forward(x) returns the full layer output [T, H] after the reduction."""
 
     def __init__(self, Wg, W1, W2, k, renorm, max_T, world: int, rank: int, logit_bias=None, rep_offset=None,
-                 rep_slots=None, W1s=None, W2s=None, shared_gate_w=None, group=None, **layer_options):
+                 rep_slots=None, W1s=None, W2s=None, shared_gate_w=None, group=None,
+                 peer: Optional[PeerReduction] = None, **layer_options):
         S = W1.shape[0]
         self.world, self.rank, self.group = world, rank, group
+        # peer: the reduction by plain loads of the ranks' partials (moe_ep_reduce) instead of
+        # the all-reduce of a collective library
+        self.peer = peer
         self.start, self.count = ep_slot_range(S, world, rank)
         W1l = W1[self.start:self.start + self.count].contiguous()
         W2l = W2[self.start:self.start + self.count].contiguous()
@@ -112,7 +222,17 @@ class EPMoELayer:
         return self.layer.forward(x, stream)
 
     def forward(self, x: torch.Tensor, stream=None) -> torch.Tensor:
+        if self.peer is not None:
+            if x.shape[0] == 0:
+                return self.layer.out[:0]
+            self.write_partial(x, stream)
+            return self.peer.reduce(stream)
         return ep_reduce_output(self.partial(x, stream), self.group)
+
+    def write_partial(self, x: torch.Tensor, stream=None) -> None:
+        """Peer reduction, first half: this rank's partial into its slot, then its flag."""
+        self.layer.forward(x, stream, out=self.peer.begin(x.shape[0]))
+        self.peer.signal(stream)
 
 
 # ----------------------------------------------------------------------------- all-to-all dispatch and combine

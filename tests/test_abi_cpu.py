@@ -213,6 +213,36 @@ def test_a2a_regroup_rejects_bad_arguments_on_host():
     assert moe.moe_get_launch_count() == before
 
 
+def test_ep_signal_reduce_and_ipc_reject_bad_arguments_on_host():
+    lib = moe._lib
+    before = moe.moe_get_launch_count()
+    two = (ctypes.c_void_p * 2)(0x1000, 0x2000)
+    odd = (ctypes.c_void_p * 2)(0x1000, 0x2002)
+    nul = (ctypes.c_void_p * 2)(0x1000, 0)
+    assert lib.moe_ep_signal(None, 2, 0, 1, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_ep_signal(two, 0, 0, 1, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_ep_signal(two, 17, 0, 1, None) == moe.MOE_ERR_INVALID_ARG   # more than 16 ranks
+    assert lib.moe_ep_signal(two, 2, 2, 1, None) == moe.MOE_ERR_INVALID_ARG    # rank outside the world
+    assert lib.moe_ep_signal(nul, 2, 0, 1, None) == moe.MOE_ERR_INVALID_ARG
+    r = lib.moe_ep_reduce
+
+    def red(parts=two, N=2, flags=FAKE, r0=0, r1=8, H=256, out=FAKE, ws=FAKE, ws_bytes=1 << 20):
+        return r(parts, N, flags, 1, r0, r1, H, out, ws, ws_bytes, None)
+
+    assert red(parts=None) == moe.MOE_ERR_INVALID_ARG
+    assert red(flags=None) == moe.MOE_ERR_INVALID_ARG
+    assert red(r0=9) == moe.MOE_ERR_INVALID_ARG                # row1 < row0
+    assert red(H=100) == moe.MOE_ERR_UNSUPPORTED
+    assert red(ws=None) == moe.MOE_ERR_WORKSPACE
+    assert red(parts=odd) == moe.MOE_ERR_INVALID_ARG           # partials 16-byte aligned
+    assert red(out=None) == moe.MOE_ERR_INVALID_ARG
+    assert red(r0=4, r1=4) == moe.MOE_OK                        # no rows: nothing to do
+    assert moe.moe_get_launch_count() == before
+    assert lib.moe_ipc_export(None, None, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_ipc_import(None, 0, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_ipc_close(None, 0) == moe.MOE_ERR_INVALID_ARG
+
+
 def test_launch_event_hook_host_side():
     lib = moe._lib
     assert lib.moe_launch_events_arm(None, -1) == moe.MOE_ERR_INVALID_ARG

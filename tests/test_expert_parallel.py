@@ -26,8 +26,8 @@ import torch.multiprocessing as mp
 import moe_inputs as mi
 import oracle
 from serving_router_gate_gb300.expert_parallel import (DistExchange, a2a_count_splits, a2a_recv_splits,
-                                                       a2a_send_splits, ep_reduce_output, ep_shared_range,
-                                                       ep_shared_shard, ep_slot_range)
+                                                       a2a_send_splits, ep_reduce_output, ep_row_range,
+                                                       ep_shared_range, ep_shared_shard, ep_slot_range)
 
 
 @pytest.mark.parametrize("S,world", [(60, 2), (64, 4), (288, 8), (13, 4), (8, 8), (5, 3)])
@@ -44,6 +44,18 @@ def test_slot_ranges_are_contiguous_and_cover_every_slot(S, world):
     assert max(sizes) - min(sizes) <= 1
     if S % world == 0:
         assert set(sizes) == {S // world}  # E / ep_size slots per rank
+
+
+@pytest.mark.parametrize("T,world", [(300, 2), (300, 4), (7, 8), (1, 3), (4096, 8), (0, 2)])
+def test_reduce_scatter_row_ranges_cover_every_row_once(T, world):
+    seen = []
+    for r in range(world):
+        lo, hi = ep_row_range(T, world, r)
+        assert lo == (seen[-1] + 1 if seen else 0) or lo == hi
+        seen.extend(range(lo, hi))
+    assert seen == list(range(T))
+    sizes = [ep_row_range(T, world, r)[1] - ep_row_range(T, world, r)[0] for r in range(world)]
+    assert max(sizes) - min(sizes) <= 1
 
 
 def test_slot_range_rejects_more_ranks_than_slots():

@@ -15,6 +15,14 @@ cases with ragged and empty batches, replica slots, group-limited top-k and
 routing on the input, and with the Qwen2-like and redundant-slot workloads'
 batches split over 4 and 8 ranks.
 
+Peer reduction (moe_ep_signal / moe_ep_reduce): ranks held by one process
+write their partials and flags, then each forms its rows of the sum --
+bitwise the rank-order fp32 sum of the partials, two steps in a row (both
+slots), as an all-reduce and as a reduce-scatter; a flag nothing raises makes
+the bounded wait give up with MOE_ERR_TIMEOUT; and two processes on the GPU
+map each other's buffers by CUDA IPC (flags raised and the host synchronised
+before any reduce starts, so no kernel waits on the other process).
+
 Ranks run one after another on one GPU: nothing waits on another rank."""
 import numpy as np
 import pytest
@@ -23,7 +31,8 @@ import torch
 import moe_inputs as mi
 import oracle
 import serving_router_gate_gb300 as moe
-from serving_router_gate_gb300.expert_parallel import EPAllToAllLayer, EPMoELayer, a2a_forward_local
+from serving_router_gate_gb300.expert_parallel import (EPAllToAllLayer, EPMoELayer, PeerReduction, a2a_forward_local,
+                                                       ep_row_range)
 from serving_router_gate_gb300.layer import layer_from_inputs
 
 from parity_util import check_out, oracle_layer, oracle_threads, sample_tokens, to_cpu
@@ -245,3 +254,121 @@ def test_a2a_redundant_slots_batch_over_8_ranks():
     xs = list(inp["x"].split(2048))
     layers = _check_a2a(inp, xs, recv_cap=3 * 2048 * 8, n_oracle=6)
     assert max(L.rows_in for L in layers) <= 3 * 2048 * 8
+
+
+# --------------------------------------------------------------------------- peer reduction
+
+def _rank_order_sum(parts):
+    acc = parts[0].float()
+    for p in parts[1:]:
+        acc = acc + p.float()
+    return acc.to(torch.bfloat16)
+
+
+def _peer_case(world, scatter, steps=((300, 0), (177, 1))):
+    cfg = mi.MoEConfig("ep_peer", T=300, H=256, I=256, E=16, k=4, renorm=True, n_shared=2, I_shared=256,
+                       shared_gate=True)
+    inp = mi.make_inputs(cfg)
+    d = lambda t: None if t is None else t.cuda().contiguous()  # noqa: E731
+    W1s, W2s = mi.shared_concat(inp["W1s"], inp["W2s"])
+    reds = PeerReduction.local_set(cfg.T, cfg.H, world, "cuda", scatter=scatter)
+    eps = [EPMoELayer(d(inp["Wg"]), d(inp["W1"]), d(inp["W2"]), cfg.k, cfg.renorm, cfg.T, world, r,
+                      W1s=d(W1s), W2s=d(W2s), shared_gate_w=d(inp["w_s"]), peer=reds[r]) for r in range(world)]
+    inp_cpu = to_cpu(inp)
+    for T, seed in steps:  # two steps: slots 1 and 0
+        x = inp["x"][:T] if seed == 0 else mi.rank_tokens(cfg, seed, T)
+        xd = x.cuda()
+        for e in eps:
+            e.write_partial(xd)
+        outs = [e.peer.reduce().clone() for e in eps]
+        torch.cuda.synchronize()
+        for e in eps:
+            assert moe.moe_get_device_status(e.peer.ws) == 0
+            assert moe.moe_get_device_status(e.layer.ws) == 0
+        ep0 = eps[0].peer.epoch
+        parts = [r.slots[ep0 % 2, :T] for r in reds]
+        ref = _rank_order_sum(parts)
+        for r, out in enumerate(outs):
+            lo, hi = ep_row_range(T, world, r) if scatter else (0, T)
+            assert torch.equal(_bits(out[lo:hi]), _bits(ref[lo:hi])), f"rank {r}, T={T}"
+        full = torch.cat([outs[r][slice(*ep_row_range(T, world, r))] for r in range(world)]) if scatter else outs[0]
+        check_out(full, oracle_layer(dict(inp_cpu, x=x.cpu()))["out"], f"peer reduction of {world} ranks, T={T}")
+
+
+@pytest.mark.parametrize("world,scatter", [(2, False), (4, False), (3, True), (4, True)])
+def test_peer_reduction_of_local_ranks(world, scatter):
+    _peer_case(world, scatter)
+
+
+def test_peer_reduction_wait_times_out_on_a_missing_flag():
+    H, T = 256, 64
+    reds = PeerReduction.local_set(T, H, 2, "cuda")
+    for r in reds:
+        r.begin(T).fill_(1.0)
+    reds[0].signal()  # rank 1 never raises its flag
+    out = reds[0].out
+    out.fill_(3.0)
+    moe.moe_set_wait_timeout_ns(2_000_000)
+    try:
+        reds[0].reduce()
+        torch.cuda.synchronize()
+    finally:
+        moe.moe_set_wait_timeout_ns(4_000_000_000)
+    assert moe.moe_get_device_status(reds[0].ws) == moe.MOE_ERR_TIMEOUT
+    assert bool((out == 3.0).all())  # nothing written
+    reds[1].signal()  # now both flags are up: the same epoch reduces
+    res = reds[0].reduce()
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status(reds[0].ws) == 0
+    assert bool((res == 2.0).all())
+
+
+def _ipc_worker(rank, port, q):
+    import os
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=2)
+    try:
+        moe.moe_set_wait_timeout_ns(1_000_000_000)  # any wait ends within a second
+        cfg = mi.MoEConfig("ep_ipc", T=200, H=256, I=128, E=8, k=2, renorm=True)
+        inp = mi.make_inputs(cfg)
+        d = lambda t: None if t is None else t.cuda().contiguous()  # noqa: E731
+        red = PeerReduction(cfg.T, cfg.H, 2, rank, "cuda")
+        ep = EPMoELayer(d(inp["Wg"]), d(inp["W1"]), d(inp["W2"]), cfg.k, cfg.renorm, cfg.T, 2, rank, peer=red)
+        res = []
+        for T in (200, 131):
+            x = inp["x"][:T].cuda()
+            ep.write_partial(x)          # partial, then this rank's flag in both ranks' arrays
+            torch.cuda.synchronize()
+            dist.barrier()               # both flags are up before either reduce starts
+            out = red.reduce().clone()
+            torch.cuda.synchronize()
+            res.append((out.cpu(), red.slots[red.epoch % 2, :T].cpu(), moe.moe_get_device_status(red.ws)))
+            dist.barrier()               # both reduces done before the next step's partials
+        red.close()
+        dist.barrier()                   # no mapping left before either process frees its buffers
+        q.put((rank, res))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_peer_reduction_across_two_processes_by_ipc():
+    import socket
+    import torch.multiprocessing as mp
+    with socket.socket() as so:
+        so.bind(("127.0.0.1", 0))
+        port = so.getsockname()[1]
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_ipc_worker, args=(r, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = dict(q.get(timeout=600) for _ in procs)
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    for step in range(2):
+        (o0, p0, s0), (o1, p1, s1) = res[0][step], res[1][step]
+        assert s0 == 0 and s1 == 0
+        ref = _rank_order_sum([p0, p1])
+        assert torch.equal(_bits(o0), _bits(ref)) and torch.equal(_bits(o1), _bits(ref))
