@@ -88,6 +88,11 @@ def ep_reduce_output(partial: torch.Tensor, group=None, out: Optional[torch.Tens
     return res
 
 
+def wrap_int32(v: int) -> int:
+    """v as the signed 32-bit integer it wraps to (the flags' representation of an epoch)."""
+    return ((int(v) + 2 ** 31) % 2 ** 32) - 2 ** 31
+
+
 def ep_row_range(T: int, world: int, rank: int) -> Tuple[int, int]:
     """Rows [lo, hi) of a [T, H] output that rank `rank` keeps in the reduce-scatter (the
     vLLM EP patch's ep_reduce_scatter_output): contiguous, as even as T allows."""
@@ -106,8 +111,9 @@ class PeerReduction:
     process on one device (local_set) -- are plain device addresses.  Per step:
     begin(T) advances the epoch e and returns slot e % 2 to write the partial into;
     signal() raises this rank's flag to e in every rank's array once the partial is
-    written; reduce(T) waits for every rank's flag e and forms this rank's rows of the
-    sum (all rows, or its slice with scatter=True) in rank order."""
+    written; reduce() waits for every rank's flag e and forms this rank's rows of the
+    sum (all rows, or its slice with scatter=True) in rank order.  The flags hold e as a
+    32-bit integer that wraps around (the kernels compare differences)."""
 
     def __init__(self, max_T: int, H: int, world: int, rank: int, device, group=None, scatter: bool = False,
                  _exchange: bool = True):
@@ -163,9 +169,12 @@ class PeerReduction:
         self.T = int(T)
         return self.slots[self.epoch % 2, :T]
 
+    def _epoch32(self) -> int:
+        return wrap_int32(self.epoch)
+
     def signal(self, stream=None) -> None:
         from . import moe_ep_signal
-        moe_ep_signal(self.peer_flags, self.rank, self.epoch, stream)
+        moe_ep_signal(self.peer_flags, self.rank, self._epoch32(), stream)
 
     def rows(self):
         return ep_row_range(self.T, self.world, self.rank) if self.scatter else (0, self.T)
@@ -177,8 +186,8 @@ class PeerReduction:
         slot_bytes = self.max_T * self.H * 2 * (self.epoch % 2)
         lo, hi = self.rows()
         out = self.out[:self.T]
-        moe_ep_reduce([p + slot_bytes for p in self.peer_slots], self.flags, self.epoch, lo, hi, out, self.ws,
-                      stream)
+        moe_ep_reduce([p + slot_bytes for p in self.peer_slots], self.flags, self._epoch32(), lo, hi, out,
+                      self.ws, stream)
         return out
 
     def close(self) -> None:

@@ -27,7 +27,7 @@ import moe_inputs as mi
 import oracle
 from serving_router_gate_gb300.expert_parallel import (DistExchange, a2a_count_splits, a2a_recv_splits,
                                                        a2a_send_splits, ep_reduce_output, ep_row_range,
-                                                       ep_shared_range, ep_shared_shard, ep_slot_range)
+                                                       ep_shared_range, ep_shared_shard, ep_slot_range, wrap_int32)
 
 
 @pytest.mark.parametrize("S,world", [(60, 2), (64, 4), (288, 8), (13, 4), (8, 8), (5, 3)])
@@ -56,6 +56,17 @@ def test_reduce_scatter_row_ranges_cover_every_row_once(T, world):
     assert seen == list(range(T))
     sizes = [ep_row_range(T, world, r)[1] - ep_row_range(T, world, r)[0] for r in range(world)]
     assert max(sizes) - min(sizes) <= 1
+
+
+def test_epochs_wrap_to_int32_keeping_order_and_parity():
+    assert wrap_int32(1) == 1 and wrap_int32(2 ** 31 - 1) == 2 ** 31 - 1
+    assert wrap_int32(2 ** 31) == -2 ** 31 and wrap_int32(2 ** 32 + 5) == 5
+    for e in (1, 2 ** 31 - 2, 2 ** 31 - 1, 2 ** 31, 2 ** 32 - 1, 2 ** 32 + 7):
+        # the kernels compare int32 differences: the next epoch is ahead, the last one behind
+        nxt = wrap_int32(wrap_int32(e + 1) - wrap_int32(e))
+        prv = wrap_int32(wrap_int32(e - 1) - wrap_int32(e))
+        assert nxt == 1 and prv == -1
+        assert wrap_int32(e) % 2 == e % 2  # the slot parity survives the wrap
 
 
 def test_slot_range_rejects_more_ranks_than_slots():
