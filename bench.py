@@ -719,6 +719,42 @@ def bench_ours(args):
         dist.destroy_process_group()
 
 
+def eager_kernel_medians(step, marked_step, K, flush, stream, spare_events=8):
+    """Each library kernel of an eagerly launched step timed on its own: the launch-event
+    hook records a CUDA event before every launch (and marked_step may add marks, e.g.
+    after phases whose work is not the library's); K steps, each after an L2 flush.
+    Returns the labels and the median interval of each launch position, and the per-label
+    sums of those medians (marks left out)."""
+    import serving_router_gate_gb300 as moe
+    c0 = moe.moe_get_launch_count()
+    step()
+    n_launch = moe.moe_get_launch_count() - c0
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_launch + spare_events)]
+    for e in evs:
+        e.record(stream)
+    torch.cuda.synchronize()
+    per_pos, labels = None, None
+    for _ in range(K):
+        flush()
+        moe.moe_launch_events_arm(evs)
+        try:
+            marked_step()
+            labels = moe.moe_launch_events_used()
+        finally:
+            moe.moe_launch_events_arm(None)
+        torch.cuda.synchronize()
+        if per_pos is None:
+            per_pos = [[] for _ in range(len(labels) - 1)]
+        for i in range(len(labels) - 1):
+            per_pos[i].append(evs[i].elapsed_time(evs[i + 1]))
+    med = [statistics.median(v) for v in per_pos]
+    kernels = {}
+    for lab, m in zip(labels, med):
+        if lab != "mark":
+            kernels[lab] = kernels.get(lab, 0.0) + m
+    return labels[:-1], med, kernels
+
+
 def bench_a2a_local(args):
     """All-to-all expert parallelism over R ranks held by this process on one GPU
     (a2a_forward_local: the ranks' steps one after another, the exchanges as device
@@ -757,34 +793,10 @@ def bench_a2a_local(args):
         if moe.moe_get_device_status(L.ws):
             raise RuntimeError("device status set after the timed steps")
 
-    # per-kernel pass
-    c0 = moe.moe_get_launch_count()
-    step()
-    n_launch = moe.moe_get_launch_count() - c0
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_launch + 8)]
-    for e in evs:
-        e.record(stream)
-    torch.cuda.synchronize()
-    per_pos, labels = None, None
-    for _ in range(K):
-        flush()
-        moe.moe_launch_events_arm(evs)
-        try:
-            step_out = a2a_forward_local(layers, xs, after_phase=lambda name: moe.moe_launch_events_mark())
-            labels = moe.moe_launch_events_used()
-        finally:
-            moe.moe_launch_events_arm(None)
-        torch.cuda.synchronize()
-        del step_out
-        if per_pos is None:
-            per_pos = [[] for _ in range(len(labels) - 1)]
-        for i in range(len(labels) - 1):
-            per_pos[i].append(evs[i].elapsed_time(evs[i + 1]))
-    med = [statistics.median(v) for v in per_pos]
-    kernels = {}
-    for lab, m in zip(labels, med):
-        if lab != "mark":
-            kernels[lab] = kernels.get(lab, 0.0) + m
+    # per-kernel pass: a mark after each phase, so the exchanges' copies fall in marked intervals
+    labels, med, kernels = eager_kernel_medians(
+        step, lambda: a2a_forward_local(layers, xs, after_phase=lambda name: moe.moe_launch_events_mark()),
+        K, flush, stream)
     # row reorders: one launch per rank, moving its received rows into slot order
     rows_in = [L.rows_in for L in layers]
     H = cfg.H
@@ -850,36 +862,14 @@ def bench_ep_local(args):
     t = time_steps([step], K, flush, stream)[0]
     clk = clocks.stop()
     ms = statistics.mean(t)
-    c0 = moe.moe_get_launch_count()
-    step()
-    n_launch = moe.moe_get_launch_count() - c0
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_launch + 2)]
-    for e in evs:
-        e.record(stream)
-    torch.cuda.synchronize()
-    per_pos, labels = None, None
-    for _ in range(K):
-        flush()
-        moe.moe_launch_events_arm(evs)
-        try:
-            step()
-            moe.moe_launch_events_mark()
-            labels = moe.moe_launch_events_used()
-        finally:
-            moe.moe_launch_events_arm(None)
-        torch.cuda.synchronize()
-        if per_pos is None:
-            per_pos = [[] for _ in range(len(labels) - 1)]
-        for i in range(len(labels) - 1):
-            per_pos[i].append(evs[i].elapsed_time(evs[i + 1]))
+    def marked():
+        step()
+        moe.moe_launch_events_mark()
+
+    _, _, kernels = eager_kernel_medians(step, marked, K, flush, stream)
     for r in reds:
         if moe.moe_get_device_status(r.ws):
             raise RuntimeError("device status set by the reduction")
-    med = [statistics.median(v) for v in per_pos]
-    kernels = {}
-    for lab, m in zip(labels, med):
-        if lab != "mark":
-            kernels[lab] = kernels.get(lab, 0.0) + m
     red_ms = kernels.get("ep_reduce_kernel", 0.0)
     red_bytes = R * (R + 1) * cfg.T * cfg.H * 2  # per rank: R partials read, its output written
     peaks = _peaks()

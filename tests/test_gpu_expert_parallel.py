@@ -372,3 +372,63 @@ def test_peer_reduction_across_two_processes_by_ipc():
         assert s0 == 0 and s1 == 0
         ref = _rank_order_sum([p0, p1])
         assert torch.equal(_bits(o0), _bits(ref)) and torch.equal(_bits(o1), _bits(ref))
+
+
+# --------------------------------------------------------------------------- poisoned buffers
+
+_A2A_BUFS = ("topk_ids", "topk_w", "slot_ids", "counts", "offsets", "perm_src", "pair_row", "send", "recv_counts",
+             "local_offsets", "recv", "x_loc", "row_map", "h", "h_sh", "y_sh", "out")
+
+
+def _a2a_poisoned_run(layers, xs, byte):
+    for L in layers:
+        for name in _A2A_BUFS:
+            t = getattr(L, name)
+            if t is not None:
+                t.view(torch.uint8).fill_(byte)
+        L.ws[moe.MOE_WS_HEADER_BYTES:].fill_(byte)  # the header (status word, counters) stays
+    torch.cuda.synchronize()
+    outs = [o.clone() for o in a2a_forward_local(layers, [x.cuda() for x in xs])]
+    torch.cuda.synchronize()
+    return outs
+
+
+def test_a2a_layer_reads_no_unwritten_memory():
+    # every buffer of every rank filled with all-ones bytes (NaN in bf16 / fp32, -1 in int32)
+    # before a forward: the outputs must equal those of a forward on zero-filled buffers
+    cfg = mi.MoEConfig("a2a_poison", T=16, H=256, I=256, E=16, k=4, renorm=True, n_shared=1, I_shared=256,
+                       shared_gate=True)
+    inp = mi.make_inputs(cfg)
+    xs = [mi.rank_tokens(cfg, r, T) for r, T in enumerate([300, 0, 77, 513])]
+    layers = _a2a_layers(inp, 4, 513)
+    clean = _a2a_poisoned_run(layers, xs, 0x00)
+    poisoned = _a2a_poisoned_run(layers, xs, 0xFF)
+    for r, (a, b) in enumerate(zip(clean, poisoned)):
+        assert torch.equal(_bits(a), _bits(b)), f"rank {r} depends on unwritten memory"
+        assert torch.isfinite(b.float()).all()
+    for L in layers:
+        assert moe.moe_get_device_status(L.ws) == 0
+
+
+def test_peer_reduction_reads_no_unwritten_memory():
+    # the partial slots and outputs poisoned before a step (the flags are state and stay)
+    H, T, world = 256, 100, 3
+    g = torch.Generator().manual_seed(5)
+    parts = [(torch.randn(T, H, generator=g)).to(torch.bfloat16).cuda() for _ in range(world)]
+    results = []
+    for byte in (0x00, 0xFF):
+        reds = PeerReduction.local_set(128, H, world, "cuda", scatter=True)
+        for r in reds:
+            r.slots.view(torch.uint8).fill_(byte)
+            r.out.view(torch.uint8).fill_(byte)
+        for r, p in zip(reds, parts):
+            r.begin(T).copy_(p)
+            r.signal()
+        outs = [r.reduce().clone() for r in reds]
+        torch.cuda.synchronize()
+        full = torch.cat([outs[r][slice(*ep_row_range(T, world, r))] for r in range(world)])
+        results.append(full)
+        for r in reds:
+            assert moe.moe_get_device_status(r.ws) == 0
+    assert torch.equal(_bits(results[0]), _bits(results[1]))
+    assert torch.equal(_bits(results[0]), _bits(_rank_order_sum(parts)))
