@@ -106,3 +106,29 @@ def test_clock_sampler_keeps_region_samples_and_reasons(tmp_path):
     assert rec["samples"] == 3            # the last sample before it plus the two inside
     assert rec["sm_mhz"] == 2055.0 and rec["sm_max_mhz"] == 2070.0
     assert rec["reasons"] == ["sw_power_cap", "sw_thermal_slowdown"]
+
+
+def _bench_cli(args, env_extra):
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, **env_extra)
+    return subprocess.run([sys.executable, os.path.join(root, "bench.py")] + args, cwd=root, env=env,
+                          capture_output=True, text=True, timeout=300)
+
+
+def test_bench_refuses_inconsistent_rank_options_before_touching_a_gpu():
+    # a launcher's world size must match --gpus
+    r = _bench_cli(["--gpus", "1"], {"WORLD_SIZE": "2", "RANK": "0"})
+    assert r.returncode != 0 and "--gpus 1 but the launcher started 2 ranks" in r.stderr
+    # the one-GPU rank modes hold every rank in one process: not under a multi-rank launcher
+    for mode in ("--a2a-ranks", "--ep-ranks"):
+        r = _bench_cli(["--gpus", "2", mode, "4"], {"WORLD_SIZE": "2", "RANK": "0"})
+        assert r.returncode != 0 and "hold every rank in one process" in r.stderr, (mode, r.stderr[-500:])
+
+
+def test_bench_help_lists_the_partitions_and_reductions():
+    r = _bench_cli(["--help"], {})
+    assert r.returncode == 0
+    for word in ("--partition", "a2a", "--reduce", "peer", "--a2a-ranks", "--ep-ranks"):
+        assert word in r.stdout
